@@ -1,0 +1,436 @@
+/*
+ * oracle.c -- the CPU oracle. TEST INFRASTRUCTURE ONLY (see oracle.h).
+ *
+ * Plain single-threaded C, written from definitions:
+ *  - the IEEE-754 binary16 / bfloat16 and OCP FP8 E4M3 / FP4 E2M1 number formats;
+ *  - BlockToFloat dequantization, i.e. the CPU reference the on-core decode was
+ *    held bit-exact against ("vllm.cpp #3030, BACKEND-TENSTORRENT-KEEPQUANT: the 27B
+ *    arm", first comment: word-shadow decode "bit-exact vs BlockToFloat");
+ *  - the matmul seam Y = X . W^T with W packed, one matrix (E = 1) or a stacked
+ *    expert tower weight[E*N, K] (same issue, scope item 2 and the "Re-anchor"
+ *    comment);
+ *  - dequantize-then-matvec as the reference a fused kernel is compared with
+ *    ("A 320B MoE on a free Kaggle TPU", section "What I actually ran");
+ *  - NVFP4 E2M1 codes with E4M3 block scales and row-scaled FP8 weights, and the
+ *    activation quantizer for W4A4 prefill ("I Built a Custom Blackwell Kernel for
+ *    Qwen3.8-27B", section "What the custom path actually does").
+ * Byte sizes: Q8_0 34 B / 32 values, Q6_K 210 B / 256 ("#3030", "Budget on the
+ * 32 GB P150"); Q4_K 144 B / 256 (fp16 d, fp16 dmin, 12 B of 6-bit scales and
+ * mins, 128 B of nibbles), NVFP4 16-value blocks with an E4M3 scale and one fp32
+ * tensor scale, FP8 E4M3 with one fp32 scale per row.
+ *
+ * Where the pages give no bit-level layout, the reading taken is the one written
+ * in oracle.h (the plainest one consistent with the printed sizes).
+ */
+#include "oracle.h"
+#include <math.h>
+#include <string.h>
+#include <stdlib.h>
+
+/* ----------------------------------------------------------------------------
+ * Rounding to a small binary floating-point format, round-to-nearest-even.
+ * p = significand bits including the implicit one, emin = exponent of the
+ * smallest normal binade. Works on a non-negative magnitude; the result is the
+ * nearest representable magnitude (possibly one binade up after a carry).
+ * Every fp32 input divided by a power of two is exact in double, and rint()
+ * under the default rounding mode rounds ties to the even integer, i.e. to the
+ * even significand.
+ * -------------------------------------------------------------------------- */
+static double rne_to_format(double a, int p, int emin) {
+    if (a == 0.0) return 0.0;
+    int ex;
+    frexp(a, &ex);            /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1;           /* floor(log2 a) */
+    if (e < emin) e = emin;   /* subnormal range keeps the quantum of emin */
+    double q = ldexp(1.0, e - (p - 1));
+    return rint(a / q) * q;
+}
+
+/* ---- IEEE binary16 ------------------------------------------------------- */
+float or_fp16_to_f32(uint16_t h) {
+    int s = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0) v = ldexp((double)m, -24);
+    else if (e == 31) v = (m == 0) ? INFINITY : NAN;
+    else v = ldexp(1.0 + m / 1024.0, e - 15);
+    return (float)(s ? -v : v);
+}
+
+uint16_t or_f32_to_fp16(float f) {
+    uint16_t s = signbit(f) ? 0x8000 : 0;
+    if (isnan(f)) return 0x7E00;
+    double a = fabs((double)f);
+    if (isinf(f)) return s | 0x7C00;
+    double r = rne_to_format(a, 11, -14);
+    if (r > 65504.0) return s | 0x7C00;            /* overflow to infinity */
+    if (r == 0.0) return s;
+    if (r < ldexp(1.0, -14)) return s | (uint16_t)(r / ldexp(1.0, -24));
+    int ex; frexp(r, &ex); int e = ex - 1;
+    uint16_t m = (uint16_t)((r / ldexp(1.0, e) - 1.0) * 1024.0);
+    return s | (uint16_t)((e + 15) << 10) | m;
+}
+
+/* ---- bfloat16: the top half of an fp32 ----------------------------------- */
+float or_bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* ---- OCP FP8 E4M3: bias 7, 3 mantissa bits, S.1111.111 = NaN, max 448 ---- */
+float or_e4m3_to_f32(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);            /* 2^-6 * m/8 */
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return (float)(s ? -v : v);
+}
+
+uint8_t or_f32_to_e4m3(float f) {                    /* RNE, saturate to +-448 */
+    uint8_t s = signbit(f) ? 0x80 : 0;
+    if (isnan(f)) return 0x7F;
+    double r = rne_to_format(fabs((double)f), 4, -6);
+    if (r > 448.0) r = 448.0;
+    if (r == 0.0) return s;
+    if (r < ldexp(1.0, -6)) return s | (uint8_t)(r / ldexp(1.0, -9));
+    int ex; frexp(r, &ex); int e = ex - 1;
+    uint8_t m = (uint8_t)((r / ldexp(1.0, e) - 1.0) * 8.0);
+    return s | (uint8_t)((e + 7) << 3) | m;
+}
+
+/* ---- OCP FP4 E2M1: bias 1, 1 mantissa bit, max 6, no inf/NaN ------------- */
+float or_e2m1_to_f32(uint8_t c) {
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + m / 2.0, e - 1);
+    return (float)(s ? -v : v);
+}
+
+uint8_t or_f32_to_e2m1(float f) {                    /* RNE, saturate to +-6 */
+    uint8_t s = signbit(f) ? 0x8 : 0;
+    double r = rne_to_format(fabs((double)f), 2, 0);
+    if (r > 6.0) r = 6.0;
+    if (r == 0.0) return s;
+    if (r < 1.0) return s | 1;                       /* the subnormal 0.5 */
+    int ex; frexp(r, &ex); int e = ex - 1;
+    uint8_t m = (uint8_t)((r / ldexp(1.0, e) - 1.0) * 2.0);
+    return s | (uint8_t)((e + 1) << 1) | m;
+}
+
+/* ---- sizes ---------------------------------------------------------------- */
+int64_t or_block_values(int fmt) {
+    switch (fmt) {
+    case OR_Q8_0: return 32;
+    case OR_Q4_K: return 256;
+    case OR_Q6_K: return 256;
+    case OR_NVFP4: return 16;
+    case OR_FP8_ROW: return 1;
+    default: return 0;
+    }
+}
+
+int64_t or_canon_bytes(int fmt, int64_t rows, int64_t K) {
+    switch (fmt) {
+    case OR_Q8_0: return rows * (K / 32) * 34;
+    case OR_Q4_K: return rows * (K / 256) * 144;
+    case OR_Q6_K: return rows * (K / 256) * 210;
+    case OR_NVFP4: return rows * (K / 2) + rows * (K / 16) + 4;
+    case OR_FP8_ROW: return rows * K + rows * 4;
+    default: return -1;
+    }
+}
+
+static uint16_t rd16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+static void wr16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); }
+static float rdf32(const uint8_t* p) { float f; memcpy(&f, p, 4); return f; }
+static void wrf32(uint8_t* p, float f) { memcpy(p, &f, 4); }
+
+static float clampf(float v, float lo, float hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+/* 6-bit field f (0..15) of the 96-bit little-endian scale bitstream of Q4_K */
+static int q4k_field(const uint8_t* sc12, int f) {
+    int v = 0;
+    for (int b = 0; b < 6; b++) {
+        int bit = 6 * f + b;
+        v |= ((sc12[bit >> 3] >> (bit & 7)) & 1) << b;
+    }
+    return v;
+}
+static void q4k_set_field(uint8_t* sc12, int f, int v) {
+    for (int b = 0; b < 6; b++) {
+        int bit = 6 * f + b;
+        if ((v >> b) & 1) sc12[bit >> 3] |= (uint8_t)(1 << (bit & 7));
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Encoders (synthetic-data generation). Non-iterative round-to-nearest
+ * quantizers, fp32 arithmetic in the order written.
+ * ------------------------------------------------------------------------- */
+static void enc_q8_0_block(const float* x, uint8_t* blk) {
+    float amax = 0.0f;
+    for (int i = 0; i < 32; i++) { float a = fabsf(x[i]); if (a > amax) amax = a; }
+    uint16_t d = or_f32_to_fp16(amax / 127.0f);
+    float dd = or_fp16_to_f32(d);
+    wr16(blk, d);
+    for (int i = 0; i < 32; i++) {
+        float q = (dd == 0.0f) ? 0.0f : clampf(nearbyintf(x[i] / dd), -127.0f, 127.0f);
+        blk[2 + i] = (uint8_t)(int8_t)q;
+    }
+}
+
+static void enc_q4_k_block(const float* x, uint8_t* blk) {
+    float s[8], mn[8], smax = 0.0f, mmax = 0.0f;
+    for (int j = 0; j < 8; j++) {
+        float lo = 0.0f, hi = x[32 * j];
+        for (int i = 0; i < 32; i++) {
+            float v = x[32 * j + i];
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+        s[j] = (hi - lo) / 15.0f;
+        mn[j] = -lo;
+        if (s[j] > smax) smax = s[j];
+        if (mn[j] > mmax) mmax = mn[j];
+    }
+    uint16_t d = or_f32_to_fp16(smax / 63.0f), dmin = or_f32_to_fp16(mmax / 63.0f);
+    float dd = or_fp16_to_f32(d), dm = or_fp16_to_f32(dmin);
+    memset(blk, 0, 144);
+    wr16(blk, d);
+    wr16(blk + 2, dmin);
+    for (int j = 0; j < 8; j++) {
+        int sc = (dd == 0.0f) ? 0 : (int)clampf(nearbyintf(s[j] / dd), 0.0f, 63.0f);
+        int mq = (dm == 0.0f) ? 0 : (int)clampf(nearbyintf(mn[j] / dm), 0.0f, 63.0f);
+        q4k_set_field(blk + 4, j, sc);
+        q4k_set_field(blk + 4, 8 + j, mq);
+        float den = dd * (float)sc;
+        float off = dm * (float)mq;
+        for (int i = 0; i < 32; i++) {
+            int e = 32 * j + i;
+            float num = x[e] + off;
+            int q = (den == 0.0f) ? 0 : (int)clampf(nearbyintf(num / den), 0.0f, 15.0f);
+            blk[16 + e / 2] |= (uint8_t)(q << (4 * (e & 1)));
+        }
+    }
+}
+
+static void enc_q6_k_block(const float* x, uint8_t* blk) {
+    float s[16], smax = 0.0f;
+    for (int j = 0; j < 16; j++) {
+        float amax = 0.0f;
+        for (int i = 0; i < 16; i++) { float a = fabsf(x[16 * j + i]); if (a > amax) amax = a; }
+        s[j] = amax / 32.0f;
+        if (s[j] > smax) smax = s[j];
+    }
+    uint16_t d = or_f32_to_fp16(smax / 127.0f);
+    float dd = or_fp16_to_f32(d);
+    memset(blk, 0, 210);
+    for (int j = 0; j < 16; j++) {
+        int sc = (dd == 0.0f) ? 0 : (int)clampf(nearbyintf(s[j] / dd), -128.0f, 127.0f);
+        blk[192 + j] = (uint8_t)(int8_t)sc;
+        float den = dd * (float)sc;
+        for (int i = 0; i < 16; i++) {
+            int e = 16 * j + i;
+            int q = (den == 0.0f) ? 0 : (int)clampf(nearbyintf(x[e] / den), -32.0f, 31.0f);
+            int u = q + 32;                               /* 0..63 */
+            blk[e / 2] |= (uint8_t)((u & 15) << (4 * (e & 1)));
+            blk[128 + e / 4] |= (uint8_t)(((u >> 4) & 3) << (2 * (e & 3)));
+        }
+    }
+    wr16(blk + 208, d);
+}
+
+int or_encode(int fmt, const float* W, int64_t rows, int64_t K, float tensor_scale,
+              uint8_t* canon) {
+    int64_t bv = or_block_values(fmt);
+    if (bv == 0 || K % bv != 0) return 1;
+    if (fmt == OR_Q8_0 || fmt == OR_Q4_K || fmt == OR_Q6_K) {
+        int64_t bb = (fmt == OR_Q8_0) ? 34 : (fmt == OR_Q4_K ? 144 : 210);
+        for (int64_t r = 0; r < rows; r++)
+            for (int64_t b = 0; b < K / bv; b++) {
+                const float* x = W + r * K + b * bv;
+                uint8_t* blk = canon + (r * (K / bv) + b) * bb;
+                if (fmt == OR_Q8_0) enc_q8_0_block(x, blk);
+                else if (fmt == OR_Q4_K) enc_q4_k_block(x, blk);
+                else enc_q6_k_block(x, blk);
+            }
+        return 0;
+    }
+    if (fmt == OR_NVFP4) {
+        uint8_t* codes = canon;
+        uint8_t* scales = canon + rows * (K / 2);
+        memset(codes, 0, (size_t)(rows * (K / 2)));
+        float t = 6.0f * tensor_scale;
+        for (int64_t r = 0; r < rows; r++)
+            for (int64_t b = 0; b < K / 16; b++) {
+                const float* x = W + r * K + b * 16;
+                float amax = 0.0f;
+                for (int i = 0; i < 16; i++) { float a = fabsf(x[i]); if (a > amax) amax = a; }
+                uint8_t sb = (t > 0.0f) ? or_f32_to_e4m3(amax / t) : 0;
+                scales[r * (K / 16) + b] = sb;
+                float den = or_e4m3_to_f32(sb) * tensor_scale;
+                for (int i = 0; i < 16; i++) {
+                    uint8_t c = (den == 0.0f) ? 0 : or_f32_to_e2m1(x[i] / den);
+                    int64_t e = b * 16 + i;
+                    codes[r * (K / 2) + e / 2] |= (uint8_t)(c << (4 * (e & 1)));
+                }
+            }
+        wrf32(canon + rows * (K / 2) + rows * (K / 16), tensor_scale);
+        return 0;
+    }
+    if (fmt == OR_FP8_ROW) {
+        uint8_t* codes = canon;
+        uint8_t* rs = canon + rows * K;
+        for (int64_t r = 0; r < rows; r++) {
+            float amax = 0.0f;
+            for (int64_t k = 0; k < K; k++) { float a = fabsf(W[r * K + k]); if (a > amax) amax = a; }
+            float s = amax / 448.0f;
+            wrf32(rs + 4 * r, s);
+            for (int64_t k = 0; k < K; k++)
+                codes[r * K + k] = (s == 0.0f) ? 0 : or_f32_to_e4m3(W[r * K + k] / s);
+        }
+        return 0;
+    }
+    return 1;
+}
+
+/* ---------------------------------------------------------------------------
+ * BlockToFloat. fp32, the op order written here is the canonical one:
+ *   Q8_0 : w = d * q                                   (exact)
+ *   Q4_K : w = (d * sc_j) * q - (dmin * m_j)           (one rounding)
+ *   Q6_K : w = (d * sc_j) * (q - 32)                   (exact)
+ *   NVFP4: w = (e2m1(c) * e4m3(s_b)) * s_T             (one rounding)
+ *   FP8  : w = e4m3(c) * s_row                         (one rounding)
+ * ------------------------------------------------------------------------- */
+static int nvfp4_to_float(const uint8_t* canon, int64_t rows, int64_t K, float* W) {
+    const uint8_t* codes = canon;
+    const uint8_t* scales = canon + rows * (K / 2);
+    float sT = rdf32(canon + rows * (K / 2) + rows * (K / 16));
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t k = 0; k < K; k++) {
+            uint8_t c = (codes[r * (K / 2) + k / 2] >> (4 * (k & 1))) & 15;
+            float sb = or_e4m3_to_f32(scales[r * (K / 16) + k / 16]);
+            float p = or_e2m1_to_f32(c) * sb;
+            W[r * K + k] = p * sT;
+        }
+    return 0;
+}
+
+static int fp8_row_to_float(const uint8_t* canon, int64_t rows, int64_t K, float* W) {
+    for (int64_t r = 0; r < rows; r++) {
+        float s = rdf32(canon + rows * K + 4 * r);
+        for (int64_t k = 0; k < K; k++) W[r * K + k] = or_e4m3_to_f32(canon[r * K + k]) * s;
+    }
+    return 0;
+}
+
+/* For NVFP4 and FP8_ROW `canon` is the whole matrix stream of `rows` rows
+ * (codes, scales, then the tensor scale / row scales). */
+int or_block_to_float(int fmt, const uint8_t* canon, int64_t rows, int64_t K, float* W) {
+    int64_t bv = or_block_values(fmt);
+    if (bv == 0 || K % bv != 0) return 1;
+    if (fmt == OR_NVFP4) return nvfp4_to_float(canon, rows, K, W);
+    if (fmt == OR_FP8_ROW) return fp8_row_to_float(canon, rows, K, W);
+    for (int64_t r = 0; r < rows; r++) {
+        float* w = W + r * K;
+        if (fmt == OR_Q8_0) {
+            for (int64_t b = 0; b < K / 32; b++) {
+                const uint8_t* blk = canon + (r * (K / 32) + b) * 34;
+                float d = or_fp16_to_f32(rd16(blk));
+                for (int i = 0; i < 32; i++) w[b * 32 + i] = d * (float)(int8_t)blk[2 + i];
+            }
+        } else if (fmt == OR_Q4_K) {
+            for (int64_t b = 0; b < K / 256; b++) {
+                const uint8_t* blk = canon + (r * (K / 256) + b) * 144;
+                float d = or_fp16_to_f32(rd16(blk)), dmin = or_fp16_to_f32(rd16(blk + 2));
+                for (int e = 0; e < 256; e++) {
+                    int j = e / 32;
+                    int sc = q4k_field(blk + 4, j), m = q4k_field(blk + 4, 8 + j);
+                    int q = (blk[16 + e / 2] >> (4 * (e & 1))) & 15;
+                    float a = d * (float)sc;
+                    float c = dmin * (float)m;
+                    w[b * 256 + e] = a * (float)q - c;
+                }
+            }
+        } else { /* OR_Q6_K */
+            for (int64_t b = 0; b < K / 256; b++) {
+                const uint8_t* blk = canon + (r * (K / 256) + b) * 210;
+                float d = or_fp16_to_f32(rd16(blk + 208));
+                for (int e = 0; e < 256; e++) {
+                    int lo = (blk[e / 2] >> (4 * (e & 1))) & 15;
+                    int hi = (blk[128 + e / 4] >> (2 * (e & 3))) & 3;
+                    int q = lo | (hi << 4);
+                    int sc = (int8_t)blk[192 + e / 16];
+                    float a = d * (float)sc;
+                    w[b * 256 + e] = a * (float)(q - 32);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * y = x . W^T in fp64, plain k-order sums; den = sum |w x| (the error scale).
+ * ------------------------------------------------------------------------- */
+void or_gemv_f64(const float* W, int64_t N, int64_t K, const uint16_t* x_bf16, int64_t M,
+                 double* y, double* den) {
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0, ab = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double p = (double)W[n * K + k] * (double)or_bf16_to_f32(x_bf16[m * K + k]);
+                acc += p;
+                ab += fabs(p);
+            }
+            y[m * N + n] = acc;
+            if (den) den[m * N + n] = ab;
+        }
+}
+
+/* Distinct routed experts, ascending: each expert's rows are read once per step
+ * ("A 320B MoE on a free Kaggle TPU", "The decode kernel's cost is not 'distinct
+ * experts'": unique routed experts first, ascending). */
+int64_t or_unique_experts(const int32_t* ids, int64_t n, int32_t* out) {
+    int64_t u = 0;
+    for (int64_t i = 0; i < n; i++) {
+        int seen = 0;
+        for (int64_t j = 0; j < u; j++) if (out[j] == ids[i]) { seen = 1; break; }
+        if (!seen) out[u++] = ids[i];
+    }
+    for (int64_t i = 1; i < u; i++) {               /* insertion sort */
+        int32_t v = out[i];
+        int64_t j = i - 1;
+        while (j >= 0 && out[j] > v) { out[j + 1] = out[j]; j--; }
+        out[j + 1] = v;
+    }
+    return u;
+}
+
+/* NVFP4 activation quantizer for the W4A4 route: 16-value blocks, E4M3 block
+ * scale s_b = e4m3(amax_b / (6 x_scale)); codes c = e2m1(x / (s_b x_scale)),
+ * all zero when s_b is zero. x_scale is a given per-site constant. */
+void or_quant_act_nvfp4(const uint16_t* x_bf16, int64_t M, int64_t K, float x_scale,
+                        uint8_t* codes, uint8_t* scales) {
+    memset(codes, 0, (size_t)(M * (K / 2)));
+    float t = 6.0f * x_scale;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t b = 0; b < K / 16; b++) {
+            float xv[16], amax = 0.0f;
+            for (int i = 0; i < 16; i++) {
+                xv[i] = or_bf16_to_f32(x_bf16[m * K + b * 16 + i]);
+                float a = fabsf(xv[i]);
+                if (a > amax) amax = a;
+            }
+            uint8_t sb = (t > 0.0f) ? or_f32_to_e4m3(amax / t) : 0;
+            scales[m * (K / 16) + b] = sb;
+            if (sb == 0) continue;
+            float den = or_e4m3_to_f32(sb) * x_scale;
+            for (int i = 0; i < 16; i++) {
+                uint8_t c = or_f32_to_e2m1(xv[i] / den);
+                int64_t e = b * 16 + i;
+                codes[m * (K / 2) + e / 2] |= (uint8_t)(c << (4 * (e & 1)));
+            }
+        }
+}

@@ -1,0 +1,471 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+- page-printed byte counts (tests/golden/page_sizes.txt);
+- library conversions (numpy float16, torch float8_e4m3fn) and exhaustive code tables
+  against the closed-form format definitions;
+- hand-built blocks whose decoded values are worked out by hand and written literally;
+- encode -> decode round-trip error bounds derived from each quantizer;
+- exact rational arithmetic (fractions.Fraction) and numpy fp64 matmul for the dot products;
+- the closed-form expected number of distinct routed experts.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_sizes.txt")
+
+
+def _golden():
+    vals = {}
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, value, _unit, _where = [p.strip() for p in line.split("|")]
+        vals[name] = float(value)
+    return vals
+
+
+# ---------------------------------------------------------------------------
+# byte sizes printed on the pages
+# ---------------------------------------------------------------------------
+def test_block_sizes_match_pages():
+    g = _golden()
+    assert oracle.canon_bytes("q6_k", 1, 256) == g["q6_k_block_bytes"] == 210
+    assert oracle.canon_bytes("q8_0", 1, 32) == g["q8_0_block_bytes"] == 34
+    assert math.ceil(oracle.canon_bytes("q6_k", 1, 256) / 4) == g["q6_k_block_words"]
+    assert math.ceil(oracle.canon_bytes("q8_0", 1, 32) / 4) == g["q8_0_block_words"]
+    # fixtures: 32 Q6_K blocks and 512 Q8_0 blocks
+    assert oracle.canon_bytes("q6_k", 1, 32 * 256) == g["fixture_q6_k_bytes"]
+    assert oracle.canon_bytes("q8_0", 1, 512 * 32) == g["fixture_q8_0_bytes"]
+    # the untied head [248320 rows, 5120] at Q6_K, and its bf16 twin, in GiB
+    head = oracle.canon_bytes("q6_k", 248320, 5120)
+    assert head == 1_042_944_000
+    assert round(head / 2**30, 2) == g["output_head_q6_k_5120x248320_packed"]
+    assert round(248320 * 5120 * 2 / 2**30, 2) == g["output_head_bf16_twin"]
+    # token_embd at 144 B / 256 is the K-quant size closest to the printed 0.68
+    emb = oracle.canon_bytes("q4_k", 5120, 248320) / 2**30
+    candidates = {110: "q3_k", 144: "q4_k", 176: "q5_k", 210: "q6_k"}
+    best = min(candidates, key=lambda b: abs(5120 * 248320 / 256 * b / 2**30 - g["token_embd_q4_k_5120x248320_packed"]))
+    assert candidates[best] == "q4_k" and abs(emb - 0.68) < 0.02
+
+
+def test_nvfp4_fp8_sizes():
+    # NVFP4: 4-bit codes + one E4M3 byte per 16 values + one fp32 tensor scale
+    assert oracle.canon_bytes("nvfp4", 17408, 5120) == 44_564_480 + 5_570_560 + 4
+    # FP8 row: one byte per value + one fp32 per row
+    assert oracle.canon_bytes("fp8_row", 6144, 5120) == 31_457_280 + 24_576
+    assert oracle.canon_bytes("q4_k", 2048, 4096) == 4_718_592
+
+
+# ---------------------------------------------------------------------------
+# scalar formats
+# ---------------------------------------------------------------------------
+def test_fp16_decode_exhaustive_vs_numpy():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = codes.view(np.float16).astype(np.float32)
+    got = np.array([oracle.fp16_to_f32(int(c)) for c in codes], dtype=np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_fp16_encode_vs_numpy_rne():
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32) * np.float32(0.02),
+        (rng.standard_normal(2000) * 1e-5).astype(np.float32),       # subnormal range
+        (rng.standard_normal(1000) * 2e4).astype(np.float32),        # near overflow
+        np.array([0.0, -0.0, 65504.0, 65519.0, 65520.0, 1e9, 2.0**-25, 2.0**-24 * 1.5,
+                  1.0 + 2.0**-11, 1.0 + 3 * 2.0**-11], dtype=np.float32),   # ties
+    ])
+    ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f32_to_fp16(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def _e4m3_closed_form(c):
+    s, e, m = c >> 7, (c >> 3) & 15, c & 7
+    if e == 15 and m == 7:
+        return float("nan")
+    v = 2.0**-6 * m / 8 if e == 0 else 2.0 ** (e - 7) * (1 + m / 8)
+    return -v if s else v
+
+
+def test_e4m3_table_exhaustive():
+    lib = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    for c in range(256):
+        got = oracle.e4m3_to_f32(c)
+        want = _e4m3_closed_form(c)
+        if math.isnan(want):
+            assert math.isnan(got) and math.isnan(lib[c])
+        else:
+            assert got == want == lib[c], c
+    assert oracle.e4m3_to_f32(0x38) == 1.0 and oracle.e4m3_to_f32(0x7E) == 448.0
+    assert oracle.e4m3_to_f32(0x01) == 2.0**-9 and oracle.e4m3_to_f32(0x08) == 2.0**-6
+
+
+def test_e4m3_encode_rne_sat():
+    # every finite code round-trips
+    for c in range(256):
+        v = _e4m3_closed_form(c)
+        if not math.isnan(v) and c != 0x80:
+            assert oracle.f32_to_e4m3(v) == c
+    # against torch's RNE cast where it does not overflow, incl. midpoints
+    finite = sorted({abs(_e4m3_closed_form(c)) for c in range(128) if c != 0x7F})
+    mids = [(a + b) / 2 for a, b in zip(finite, finite[1:])]
+    rng = np.random.default_rng(2)
+    vals = np.concatenate([np.array(mids + finite, dtype=np.float32),
+                           (rng.standard_normal(3000) * 50).astype(np.float32)])
+    vals = np.concatenate([vals, -vals])
+    vals = vals[np.abs(vals) < 464]
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.f32_to_e4m3(float(v)) for v in vals], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+    # saturation beyond the largest finite value (448 = 0x7E)
+    for v in (464.0, 470.0, 1e6, float("inf")):
+        assert oracle.f32_to_e4m3(v) == 0x7E and oracle.f32_to_e4m3(-v) == 0xFE
+
+
+def test_e2m1_table_and_ties():
+    table = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    for c in range(16):
+        want = table[c & 7] * (-1 if c & 8 else 1)
+        assert oracle.e2m1_to_f32(c) == want
+        if c != 8:
+            assert oracle.f32_to_e2m1(want) == c
+    ties = {0.25: 0.0, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0, 5.0: 4.0,
+            6.5: 6.0, 7.0: 6.0, 100.0: 6.0, 0.3: 0.5, 0.2: 0.0}
+    for v, want in ties.items():
+        assert oracle.e2m1_to_f32(oracle.f32_to_e2m1(v)) == want, v
+        assert oracle.e2m1_to_f32(oracle.f32_to_e2m1(-v)) == -want, v
+    # brute force nearest, ties to the even code
+    rng = np.random.default_rng(3)
+    for v in rng.uniform(-8, 8, 2000).astype(np.float32):
+        mags = np.array(table)
+        d = np.abs(np.abs(float(v)) - mags)
+        best = np.flatnonzero(d == d.min())
+        code = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        if abs(float(v)) > 6:
+            code = 7
+        got = oracle.f32_to_e2m1(float(v))
+        assert got & 7 == code and (got >> 3) == (1 if np.signbit(v) else 0), v
+
+
+# ---------------------------------------------------------------------------
+# hand-built blocks (layouts as read: see oracle.h); values worked out by hand
+# ---------------------------------------------------------------------------
+def test_q8_0_handbuilt():
+    blk = bytearray(34)
+    blk[0:2] = (0x3C00).to_bytes(2, "little")          # d = 1.0
+    for i in range(32):
+        blk[2 + i] = (i - 16) & 0xFF
+    w = oracle.block_to_float("q8_0", np.frombuffer(bytes(blk), np.uint8), 1, 32)[0]
+    assert list(w) == [float(i - 16) for i in range(32)]
+    blk[0:2] = (0x3800).to_bytes(2, "little")          # d = 0.5
+    blk[2] = 0x81                                        # -127
+    w = oracle.block_to_float("q8_0", np.frombuffer(bytes(blk), np.uint8), 1, 32)[0]
+    assert w[0] == -63.5 and w[1] == -7.5 and w[31] == 7.5
+
+
+def _q4k_block(d16, dmin16, sc, mn, q):
+    bits = 0
+    for f in range(8):
+        bits |= sc[f] << (6 * f)
+        bits |= mn[f] << (6 * (8 + f))
+    blk = bytearray(144)
+    blk[0:2] = d16.to_bytes(2, "little")
+    blk[2:4] = dmin16.to_bytes(2, "little")
+    blk[4:16] = bits.to_bytes(12, "little")
+    for b in range(128):
+        blk[16 + b] = q[2 * b] | (q[2 * b + 1] << 4)
+    return bytes(blk)
+
+
+def test_q4_k_handbuilt_values():
+    blk = _q4k_block(0x3C00, 0x3C00, [j + 1 for j in range(8)], list(range(8)),
+                     [e % 16 for e in range(256)])
+    w = oracle.block_to_float("q4_k", np.frombuffer(blk, np.uint8), 1, 256)[0]
+    # e=0: j=0, q=0 -> 0      e=15: j=0 (sc 1, m 0), q=15 -> 15     e=33: j=1 (sc 2, m 1), q=1 -> 1
+    # e=100: j=3 (sc 4, m 3), q=4 -> 13     e=160: j=5 (sc 6, m 5), q=0 -> -5
+    # e=255: j=7 (sc 8, m 7), q=15 -> 113
+    hand = {0: 0.0, 15: 15.0, 33: 1.0, 100: 13.0, 160: -5.0, 255: 113.0}
+    for e, v in hand.items():
+        assert w[e] == v, (e, w[e], v)
+    # d = 0.5, dmin = 0.25 (0x3400), sc_j = 63, m_j = 63, q = 15 everywhere:
+    # w = 0.5*63*15 - 0.25*63 = 472.5 - 15.75 = 456.75
+    blk = _q4k_block(0x3800, 0x3400, [63] * 8, [63] * 8, [15] * 256)
+    w = oracle.block_to_float("q4_k", np.frombuffer(blk, np.uint8), 1, 256)[0]
+    assert np.all(w == 456.75)
+
+
+def test_q6_k_handbuilt():
+    # d = 0.5, sc_j = +1 (even j) / -1 (odd j), q_e = e mod 64  ->  w = 0.5 (q-32) sc_j
+    blk = bytearray(210)
+    for e in range(256):
+        q = e % 64
+        blk[e // 2] |= (q & 15) << (4 * (e & 1))
+        blk[128 + e // 4] |= ((q >> 4) & 3) << (2 * (e & 3))
+    for j in range(16):
+        blk[192 + j] = 1 if j % 2 == 0 else 0xFF
+    blk[208:210] = (0x3800).to_bytes(2, "little")
+    w = oracle.block_to_float("q6_k", np.frombuffer(bytes(blk), np.uint8), 1, 256)[0]
+    # e=0: q=0, j=0 (sc +1): 0.5*(-32) = -16      e=16: q=16, j=1 (sc -1): 0.5*(-16)*(-1) = 8
+    # e=31: q=31, j=1 (sc -1): 0.5*(-1)*(-1) = 0.5  e=63: q=63, j=3 (sc -1): 0.5*31*(-1) = -15.5
+    # e=64: q=0, j=4 (sc +1): -16                    e=255: q=63, j=15 (sc -1): -15.5
+    hand = {0: -16.0, 16: 8.0, 31: 0.5, 63: -15.5, 64: -16.0, 255: -15.5}
+    for e, v in hand.items():
+        assert w[e] == v, (e, w[e], v)
+
+
+def test_nvfp4_handbuilt():
+    K = 32
+    codes = bytearray(K // 2)
+    for e in range(K):
+        codes[e // 2] |= (e % 16) << (4 * (e & 1))
+    scales = bytes([0x38, 0x40])                       # 1.0, 2.0
+    canon = bytes(codes) + scales + np.float32(0.5).tobytes()
+    w = oracle.block_to_float("nvfp4", np.frombuffer(canon, np.uint8), 1, K)[0]
+    table = [0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.0, -0.5, -1, -1.5, -2, -3, -4, -6]
+    assert list(w[:16]) == [v * 0.5 for v in table]   # s_b = 1, s_T = 0.5
+    assert list(w[16:]) == table                        # s_b = 2, s_T = 0.5
+
+
+def test_fp8_row_handbuilt():
+    K = 256
+    codes = bytes(range(256))
+    canon = codes + np.float32(2.0).tobytes()
+    w = oracle.block_to_float("fp8_row", np.frombuffer(canon, np.uint8), 1, K)[0]
+    for c in range(256):
+        v = _e4m3_closed_form(c)
+        if math.isnan(v):
+            assert math.isnan(w[c])
+        else:
+            assert w[c] == 2.0 * v
+
+
+# ---------------------------------------------------------------------------
+# encode -> decode round trips on N(0, 0.02) data and edge blocks
+# ---------------------------------------------------------------------------
+def _data(rows, K, seed=0):
+    W = synth.weights(seed, rows, K).numpy()
+    W[0, :] = 0.0                                       # all-zero row
+    W[1, :] = -np.abs(W[1, :])                          # all-negative row
+    W[2, :256] = 0.0123                                 # constant block
+    return W
+
+
+def _f16(a):
+    return np.asarray(a, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def test_roundtrip_q8_0():
+    W = _data(8, 1024)
+    c = oracle.encode("q8_0", W)
+    D = oracle.block_to_float("q8_0", c, 8, 1024)
+    blocks = c.reshape(8, 32, 34)
+    d = _f16(blocks[:, :, 0].astype(np.uint16) | (blocks[:, :, 1].astype(np.uint16) << 8))
+    amax = np.abs(W.reshape(8, 32, 32)).max(-1)
+    bound = 0.5 * d + 127 * np.abs(d - amax / 127) + 1e-7
+    err = np.abs(W - D).reshape(8, 32, 32).max(-1)
+    assert np.all(err <= bound)
+    assert np.all(D[0] == 0)
+
+
+def test_roundtrip_q4_k():
+    W = _data(8, 1024)
+    c = oracle.encode("q4_k", W)
+    D = oracle.block_to_float("q4_k", c, 8, 1024)
+    Wb = W.reshape(8, 4, 8, 32)
+    lo = np.minimum(0, Wb.min(-1))
+    hi = Wb.max(-1)
+    s = (hi - lo) / 15
+    # the block's step and offset after 6-bit/fp16 rounding: within 1/2 of a
+    # 6-bit step of the ideal ones (plus fp16 rounding of d, dmin)
+    dd = _f16(c.reshape(8, 4, 144)[:, :, 0].astype(np.uint16) | (c.reshape(8, 4, 144)[:, :, 1].astype(np.uint16) << 8))
+    dm = _f16(c.reshape(8, 4, 144)[:, :, 2].astype(np.uint16) | (c.reshape(8, 4, 144)[:, :, 3].astype(np.uint16) << 8))
+    bound = (0.5 * s + 15 * 0.5 * dd[..., None] + 0.5 * dm[..., None]) * (1 + 2**-9) + 1e-7
+    err = np.abs(W - D).reshape(8, 4, 8, 32).max(-1)
+    assert np.all(err <= bound)
+    assert np.all(D[0] == 0)
+    rel = np.linalg.norm(W[3:] - D[3:]) / np.linalg.norm(W[3:])
+    assert rel < 0.12          # 4-bit asymmetric rounding on Gaussian data
+
+
+def test_roundtrip_q6_k():
+    W = _data(8, 1024)
+    c = oracle.encode("q6_k", W)
+    D = oracle.block_to_float("q6_k", c, 8, 1024)
+    blk = c.reshape(8, 4, 210)
+    d = _f16(blk[:, :, 208].astype(np.uint16) | (blk[:, :, 209].astype(np.uint16) << 8))
+    sc = blk[:, :, 192:208].view(np.int8).astype(np.float32)
+    step = d[..., None] * np.abs(sc)                                 # [8,4,16]
+    amax = np.abs(W.reshape(8, 4, 16, 16)).max(-1)
+    # rounding to the nearest step, or the clamp of +amax to code 31 (q - 32 <= 31)
+    bound = np.maximum(0.5 * step, amax - 31 * step) * (1 + 2**-20) + 1e-7
+    err = np.abs(W - D).reshape(8, 4, 16, 16).max(-1)
+    assert np.all(err <= bound)
+    rel = np.linalg.norm(W[3:] - D[3:]) / np.linalg.norm(W[3:])
+    assert rel < 0.03
+
+
+def test_roundtrip_nvfp4():
+    W = _data(8, 1024)
+    sT = np.float32(np.abs(W).max()) / np.float32(2688.0)
+    c = oracle.encode("nvfp4", W, float(sT))
+    D = oracle.block_to_float("nvfp4", c, 8, 1024)
+    sb = np.array([oracle.e4m3_to_f32(int(v)) for v in c[8 * 512: 8 * 512 + 8 * 64]],
+                  dtype=np.float32).reshape(8, 64)
+    unit = sb * sT                                                   # block quantum scale
+    amax = np.abs(W.reshape(8, 64, 16)).max(-1)
+    # half the widest E2M1 gap (1.0 between 4 and 6) plus saturation plus the final rounding
+    bound = unit * 1.0 + np.maximum(0, amax - 6 * unit) + np.abs(W).max() * 2**-23 * 4
+    err = np.abs(W - D).reshape(8, 64, 16).max(-1)
+    assert np.all(err <= bound + 1e-12)
+    rel = np.linalg.norm(W[3:] - D[3:]) / np.linalg.norm(W[3:])
+    assert rel < 0.15
+
+
+def test_roundtrip_fp8_row():
+    W = _data(8, 1024)
+    c = oracle.encode("fp8_row", W)
+    D = oracle.block_to_float("fp8_row", c, 8, 1024)
+    s = np.frombuffer(c[8 * 1024:].tobytes(), dtype=np.float32)
+    # relative half-ulp of a 3-bit mantissa for normals, 2^-10 s below 2^-6 s
+    bound = np.maximum(np.abs(W) * 2**-4, s[:, None] * 2**-10) * (1 + 2**-20)
+    assert np.all(np.abs(W - D) <= bound + 1e-12)
+    assert np.all(D[0] == 0)
+
+
+# ---------------------------------------------------------------------------
+# the dot products
+# ---------------------------------------------------------------------------
+def test_gemv_exact_rationals_tiny():
+    W = synth.weights(5, 3, 64).numpy()
+    x = synth.bf16_bits(synth.activations(5, 2, 64))
+    y, den = oracle.gemv_f64(W, x)
+    xf = np.array([[oracle.bf16_to_f32(int(v)) for v in row] for row in x], dtype=np.float32)
+    for m in range(2):
+        for n in range(3):
+            exact = sum(Fraction(float(W[n, k])) * Fraction(float(xf[m, k])) for k in range(64))
+            ab = sum(abs(Fraction(float(W[n, k])) * Fraction(float(xf[m, k]))) for k in range(64))
+            assert abs(Fraction(y[m, n]) - exact) <= ab * Fraction(64, 2**53)
+            assert abs(Fraction(den[m, n]) - ab) <= ab * Fraction(64, 2**53)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (8, 64, 256), (3, 17, 96)])
+def test_gemv_vs_numpy_f64(M, N, K):
+    W = synth.weights(7, N, K).numpy()
+    xb = synth.activations(7, M, K)
+    y, den = oracle.gemv_f64(W, synth.bf16_bits(xb))
+    ref = xb.float().numpy().astype(np.float64) @ W.astype(np.float64).T
+    assert np.allclose(y, ref, rtol=0, atol=1e-13 * np.abs(ref).max())
+    assert np.allclose(den, np.abs(xb.float().numpy().astype(np.float64))
+                       @ np.abs(W.astype(np.float64)).T, rtol=1e-12)
+
+
+def test_q4_k_factored_identity_exact():
+    """sum_k w_k x_k == sum_j (d sc_j) sum q x - (dmin m_j) sum x, exactly (rationals)."""
+    W = synth.weights(9, 1, 256).numpy()
+    c = oracle.encode("q4_k", W)
+    D = oracle.block_to_float("q4_k", c, 1, 256)[0]
+    x = synth.activations(9, 1, 256).float().numpy()[0]
+    blk = c.tobytes()
+    d = float(_f16(int.from_bytes(blk[0:2], "little")))
+    dmin = float(_f16(int.from_bytes(blk[2:4], "little")))
+    bits = int.from_bytes(blk[4:16], "little")
+    lhs = sum(Fraction(float(D[k])) * Fraction(float(x[k])) for k in range(256))
+    rhs = Fraction(0)
+    for j in range(8):
+        sc = (bits >> (6 * j)) & 63
+        m = (bits >> (6 * (8 + j))) & 63
+        sq = sum(Fraction(((blk[16 + e // 2] >> (4 * (e & 1))) & 15)) * Fraction(float(x[e]))
+                 for e in range(32 * j, 32 * j + 32))
+        sx = sum(Fraction(float(x[e])) for e in range(32 * j, 32 * j + 32))
+        rhs += Fraction(d) * sc * sq - Fraction(dmin) * m * sx
+    # the decoded w differs from (d sc) q - dmin m only by its one fp32 rounding
+    tol = sum(abs(Fraction(float(x[k]))) for k in range(256)) * Fraction(float(np.abs(D).max())) * Fraction(1, 2**23)
+    assert abs(lhs - rhs) <= tol
+
+
+# ---------------------------------------------------------------------------
+# routing
+# ---------------------------------------------------------------------------
+def test_unique_experts_vs_numpy():
+    ids = synth.expert_ids(0, 8, 8, 288)
+    assert np.array_equal(oracle.unique_experts(ids), np.unique(ids))
+    for t in range(8):
+        assert len(set(ids[t].tolist())) == 8          # distinct within a token
+
+
+def test_distinct_expert_formula():
+    g = _golden()
+    E, k = 288, 8
+    expect = lambda M: E * (1 - (1 - k / E) ** M)
+    assert round(expect(3), 1) == g["distinct_experts_3tok_top8_of_288"]
+    assert 3 * k == g["distinct_experts_3tok_pairs"]
+    assert expect(1) == pytest.approx(8.0)
+    for M, tol in ((3, 0.15), (4, 0.2), (8, 0.35)):
+        counts = [len(oracle.unique_experts(synth.expert_ids(s, M, k, E))) for s in range(400)]
+        assert abs(np.mean(counts) - expect(M)) < tol, (M, np.mean(counts), expect(M))
+
+
+def test_grouped_reference_vs_numpy():
+    E, N, K, M, topk = 6, 16, 256, 3, 2
+    W = synth.weights(11, E * N, K).numpy()
+    canon = oracle.encode("q4_k", W)
+    D = oracle.block_to_float("q4_k", canon, E * N, K)
+    ids = synth.expert_ids(11, M, topk, E)
+    x = synth.activations(11, M * topk, K)
+    xb = synth.bf16_bits(x)
+    Y, _ = oracle.grouped_f64(lambda e: D[e * N:(e + 1) * N], ids, xb, x_per_pair=True)
+    xf = x.float().numpy().astype(np.float64)
+    for t in range(M):
+        for j in range(topk):
+            e = ids[t, j]
+            ref = D[e * N:(e + 1) * N].astype(np.float64) @ xf[t * topk + j]
+            assert np.allclose(Y[t, j], ref, rtol=0, atol=1e-13 * np.abs(ref).max())
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 activation quantizer
+# ---------------------------------------------------------------------------
+def test_quant_act_nvfp4_brute_force():
+    M, K = 4, 256
+    x = synth.activations(13, M, K)
+    xb = synth.bf16_bits(x)
+    xf = x.float().numpy()
+    xf[1, 16:32] = 0.0                                  # a zero block
+    xb[1, 16:32] = 0
+    xs = np.float32(np.abs(xf).max()) / np.float32(2688.0)
+    codes, scales = oracle.quant_act_nvfp4(xb, float(xs))
+    table = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    t = np.float32(6.0) * xs
+    for m in range(M):
+        for b in range(K // 16):
+            blk = xf[m, 16 * b:16 * b + 16]
+            amax = np.float32(np.abs(blk).max())
+            sb_ref = torch.tensor([amax / t], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).item()
+            assert scales[m, b] == sb_ref
+            sbf = np.float32(oracle.e4m3_to_f32(int(sb_ref)))
+            for i in range(16):
+                e = 16 * b + i
+                c = (codes[m, e // 2] >> (4 * (e & 1))) & 15
+                if sb_ref == 0:
+                    assert c == 0
+                    continue
+                v = np.float32(blk[i]) / np.float32(sbf * xs)
+                d = np.abs(abs(float(v)) - table)
+                best = np.flatnonzero(d == d.min())
+                mag = best[0] if len(best) == 1 else [q for q in best if q % 2 == 0][0]
+                if abs(float(v)) > 6:
+                    mag = 7
+                assert (c & 7) == mag and (c >> 3) == (1 if np.signbit(v) else 0)
+    assert np.all(codes[1, 8:16] == 0) and scales[1, 1] == 0
