@@ -1,0 +1,229 @@
+"""Python binding of libqmv: block-quantized weight GEMV on GB300 (sm_103a).
+
+Argument marshalling only. Every function has the name of the C entry point it
+calls (include/qmv.h), takes torch tensors for device buffers, passes their raw
+pointers and the current CUDA stream, and raises QmvError on a non-zero status.
+All arithmetic runs in the CUDA kernels of libqmv.so; there is no fallback: if
+the library has not been built, importing this package raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqmv.so")
+
+QMV_Q8_0, QMV_Q4_K, QMV_Q6_K, QMV_NVFP4, QMV_FP8_ROW = 1, 2, 3, 4, 5
+FORMATS = {"q8_0": QMV_Q8_0, "q4_k": QMV_Q4_K, "q6_k": QMV_Q6_K, "nvfp4": QMV_NVFP4,
+           "fp8_row": QMV_FP8_ROW}
+QMV_ENTRY_GEMV, QMV_ENTRY_GROUPED, QMV_ENTRY_W4A4 = 1, 2, 3
+QMV_MAX_M = 8
+
+STATUS = {0: "QMV_OK", 1: "QMV_EINVAL", 2: "QMV_EALIGN", 3: "QMV_EUNSUPPORTED", 4: "QMV_ECUDA",
+          5: "QMV_EHEADER", 6: "QMV_ETIMEOUT", 7: "QMV_ERANGE", 8: "QMV_EWORKSPACE"}
+
+
+class QmvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({qmv_status_str(status)})")
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      f"`python block_quantized_weight_fly_gb300/build.py` (no CPU fallback exists)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+
+
+def _sig(name, res, args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = args
+    return f
+
+
+_canon_size = _sig("qmv_canon_size", _SZ, [_I, _I64, _I64, _I64])
+_pack_size = _sig("qmv_pack_size", _SZ, [_I, _I64, _I64, _I64])
+_pack = _sig("qmv_pack", _I, [_I, _P, _I64, _I64, _I64, _P, _P])
+_quantize = _sig("qmv_quantize", _I, [_I, _P, _I64, _I64, _F, _P, _P])
+_dequant = _sig("qmv_dequant", _I, [_I, _P, _I64, _I64, _I64, _I64, _I64, _P, _P])
+_ws_size = _sig("qmv_workspace_size", _SZ, [_I, _I, _I, _I64, _I64, _I64, _I])
+_gemv = _sig("qmv_gemv", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
+_grouped = _sig("qmv_grouped", _I, [_I, _P, _P, _P, _I, _P, _I, _I, _I64, _I64, _I64, _P, _SZ, _P])
+_quant_act = _sig("qmv_quant_act_nvfp4", _I, [_P, _F, _P, _P, _I, _I64, _P])
+_w4a4 = _sig("qmv_gemm_nvfp4_w4a4", _I, [_P, _P, _F, _P, _I, _I64, _I64, _P, _SZ, _P])
+_status_str = _sig("qmv_status_str", ctypes.c_char_p, [_I])
+_last_route = _sig("qmv_last_route", _I, [])
+_dev_status = _sig("qmv_device_status", _I, [_I])
+
+EXPORTED = ["qmv_canon_size", "qmv_pack_size", "qmv_pack", "qmv_quantize", "qmv_dequant",
+            "qmv_workspace_size", "qmv_gemv", "qmv_grouped", "qmv_quant_act_nvfp4",
+            "qmv_gemm_nvfp4_w4a4", "qmv_status_str", "qmv_last_route", "qmv_device_status"]
+
+
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise QmvError(st, what)
+
+
+def _bits16(x: torch.Tensor) -> torch.Tensor:
+    if x.dtype == torch.bfloat16:
+        return x
+    if x.dtype in (torch.int16, torch.uint16):
+        return x
+    raise ValueError("x must be bf16 (or its raw 16-bit patterns)")
+
+
+# ---- entry points -------------------------------------------------------------
+def qmv_status_str(status: int) -> str:
+    return _status_str(int(status)).decode()
+
+
+def qmv_last_route() -> int:
+    return int(_last_route())
+
+
+def qmv_device_status(reset: bool = True) -> int:
+    return int(_dev_status(1 if reset else 0))
+
+
+def qmv_canon_size(fmt, N: int, K: int, E: int = 1) -> int:
+    return int(_canon_size(_fmt(fmt), N, K, E))
+
+
+def qmv_pack_size(fmt, N: int, K: int, E: int = 1) -> int:
+    return int(_pack_size(_fmt(fmt), N, K, E))
+
+
+def qmv_workspace_size(entry: int, fmt, M: int, N: int, K: int, E: int = 1, topk: int = 1) -> int:
+    return int(_ws_size(int(entry), _fmt(fmt), M, N, K, E, topk))
+
+
+def qmv_pack(fmt, canon: torch.Tensor, N: int, K: int, E: int = 1, dst: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    _dev(canon, "canon")
+    size = qmv_pack_size(fmt, N, K, E)
+    if size == 0:
+        raise QmvError(3, "qmv_pack_size")
+    if dst is None:
+        dst = torch.empty(size, dtype=torch.uint8, device=canon.device)
+    _check(_pack(_fmt(fmt), _ptr(canon), N, K, E, _ptr(dst), _stream(stream)), "qmv_pack")
+    return dst
+
+
+def qmv_quantize(fmt, W: torch.Tensor, tensor_scale: float = 0.0, canon: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    _dev(W, "W")
+    if W.dtype != torch.float32 or W.dim() != 2:
+        raise ValueError("W must be a 2-D float32 tensor")
+    rows, K = W.shape
+    size = qmv_canon_size(fmt, rows, K, 1)
+    if canon is None:
+        canon = torch.empty(size, dtype=torch.uint8, device=W.device)
+    _check(_quantize(_fmt(fmt), _ptr(W), rows, K, float(tensor_scale), _ptr(canon), _stream(stream)),
+           "qmv_quantize")
+    return canon
+
+
+def qmv_dequant(fmt, packed: torch.Tensor, N: int, K: int, E: int = 1, row0: int = 0,
+                rows: int | None = None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _dev(packed, "packed")
+    rows = N * E - row0 if rows is None else rows
+    if out is None:
+        out = torch.empty((rows, K), dtype=torch.float32, device=packed.device)
+    _check(_dequant(_fmt(fmt), _ptr(packed), N, K, E, row0, rows, _ptr(out), _stream(stream)),
+           "qmv_dequant")
+    return out
+
+
+def workspace(entry: int, fmt, M: int, N: int, K: int, E: int = 1, topk: int = 1,
+              device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of the size the entry point needs."""
+    size = qmv_workspace_size(entry, fmt, M, N, K, E, topk)
+    if size == 0:
+        raise QmvError(1, "qmv_workspace_size")
+    return torch.zeros(size, dtype=torch.uint8, device=device)
+
+
+def qmv_gemv(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int,
+             ws: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _dev(packed_W, "packed_W"); _dev(x, "x"); _dev(ws, "ws")
+    x = _bits16(x)
+    M = x.shape[0] if x.dim() == 2 else 1
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(_gemv(_fmt(fmt), _ptr(packed_W), _ptr(x), _ptr(y), M, N, K, _ptr(ws), ws.numel(),
+                 _stream(stream)), "qmv_gemv")
+    return y
+
+
+def qmv_grouped(fmt, tower: torch.Tensor, expert_ids: torch.Tensor, x: torch.Tensor, N: int, K: int,
+                E: int, ws: torch.Tensor, x_per_pair: bool = False, y: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    _dev(tower, "tower"); _dev(expert_ids, "expert_ids"); _dev(x, "x"); _dev(ws, "ws")
+    if expert_ids.dtype != torch.int32 or expert_ids.dim() != 2:
+        raise ValueError("expert_ids must be int32 [M, topk]")
+    M, topk = expert_ids.shape
+    x = _bits16(x)
+    if y is None:
+        y = torch.empty((M, topk, N), dtype=torch.float32, device=x.device)
+    _check(_grouped(_fmt(fmt), _ptr(tower), _ptr(expert_ids), _ptr(x), 1 if x_per_pair else 0, _ptr(y),
+                    M, topk, N, K, E, _ptr(ws), ws.numel(), _stream(stream)), "qmv_grouped")
+    return y
+
+
+def qmv_quant_act_nvfp4(x: torch.Tensor, x_scale: float, codes: torch.Tensor | None = None,
+                        scales: torch.Tensor | None = None, stream=None):
+    _dev(x, "x")
+    x = _bits16(x)
+    M, K = x.shape
+    if codes is None:
+        codes = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((M, K // 16), dtype=torch.uint8, device=x.device)
+    _check(_quant_act(_ptr(x), float(x_scale), _ptr(codes), _ptr(scales), M, K, _stream(stream)),
+           "qmv_quant_act_nvfp4")
+    return codes, scales
+
+
+def qmv_gemm_nvfp4_w4a4(packed_W: torch.Tensor, x: torch.Tensor, x_scale: float, N: int, K: int,
+                        ws: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _dev(packed_W, "packed_W"); _dev(x, "x"); _dev(ws, "ws")
+    x = _bits16(x)
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(_w4a4(_ptr(packed_W), _ptr(x), float(x_scale), _ptr(y), M, N, K, _ptr(ws), ws.numel(),
+                 _stream(stream)), "qmv_gemm_nvfp4_w4a4")
+    return y

@@ -1,0 +1,213 @@
+// qmv_api.cu -- the extern "C" entry points of libqmv (declared in include/qmv.h):
+// host-side argument validation, the per-device status word, and dispatch to the
+// kernels. Nothing here allocates memory, synchronizes a stream or reads device
+// data, except qmv_device_status(), which is a diagnostics hook and says so.
+#include <cstdint>
+#include <cuda_runtime.h>
+#include "qmv.h"
+#include "qmv_internal.h"
+
+namespace {
+
+using namespace qmv;
+
+__device__ unsigned g_status;               // per-device latched status bits
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices] = {nullptr};
+thread_local int g_last_route = 0;
+
+unsigned* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ECUDA; }
+
+bool valid_fmt(int f) { return f >= QMV_Q8_0 && f <= QMV_FP8_ROW; }
+
+}  // namespace
+
+extern "C" {
+
+size_t qmv_canon_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E) {
+  if (!valid_fmt(fmt) || N <= 0 || K <= 0 || E <= 0) return 0;
+  const int64_t bv = (fmt == QMV_Q8_0) ? 32 : (fmt == QMV_NVFP4) ? 16 : (fmt == QMV_FP8_ROW) ? 1 : 256;
+  if (K % bv) return 0;
+  return (size_t)(E * canon_matrix_bytes((int)fmt, N, K));
+}
+
+size_t qmv_pack_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E) {
+  Layout L;
+  if (!make_layout((int)fmt, N, K, E, &L)) return 0;
+  return (size_t)L.total;
+}
+
+qmv_status qmv_pack(qmv_fmt fmt, const void* canon, int64_t N, int64_t K, int64_t E, void* dst,
+                    cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !canon || !dst || N <= 0 || K <= 0 || E <= 0) return QMV_EINVAL;
+  Layout L;
+  if (!make_layout((int)fmt, N, K, E, &L)) return QMV_EUNSUPPORTED;
+  if (!aligned(dst, 256)) return QMV_EALIGN;
+  qmv_status st = from_cuda(launch_pack(L, static_cast<const uint8_t*>(canon), static_cast<uint8_t*>(dst), stream));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + 6;
+  return st;
+}
+
+qmv_status qmv_quantize(qmv_fmt fmt, const float* W, int64_t rows, int64_t K, float tensor_scale,
+                        void* canon, cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !W || !canon || rows <= 0 || K <= 0) return QMV_EINVAL;
+  if (qmv_canon_size(fmt, rows, K, 1) == 0) return QMV_EUNSUPPORTED;
+  if (fmt == QMV_NVFP4 && !(tensor_scale >= 0.0f)) return QMV_EINVAL;
+  if (!aligned(W, 4)) return QMV_EALIGN;
+  qmv_status st = from_cuda(launch_quantize((int)fmt, W, rows, K, tensor_scale, static_cast<uint8_t*>(canon), stream));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + 7;
+  return st;
+}
+
+qmv_status qmv_dequant(qmv_fmt fmt, const void* packed, int64_t N, int64_t K, int64_t E, int64_t row0,
+                       int64_t rows, float* W_out, cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !packed || !W_out || N <= 0 || K <= 0 || E <= 0) return QMV_EINVAL;
+  if (row0 < 0 || rows < 0 || row0 + rows > N * E) return QMV_EINVAL;
+  Layout L;
+  if (!make_layout((int)fmt, N, K, E, &L)) return QMV_EUNSUPPORTED;
+  if (!aligned(packed, 256) || !aligned(W_out, 4)) return QMV_EALIGN;
+  unsigned* status = status_ptr();
+  if (!status) return QMV_ECUDA;
+  qmv_status st = from_cuda(launch_dequant(L, static_cast<const uint8_t*>(packed), row0, rows, W_out, status, stream));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + 5;
+  return st;
+}
+
+size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, int64_t E, int topk) {
+  (void)E; (void)topk;
+  if (!valid_fmt(fmt) || M <= 0 || N <= 0 || K <= 0) return 0;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return 0;
+  if (entry == QMV_ENTRY_GEMV || entry == QMV_ENTRY_GROUPED) {
+    if (M > QMV_MAX_M) return 0;
+    return (size_t)ws_plan_stream(M, 0, sms).total;
+  }
+  if (entry == QMV_ENTRY_W4A4) {
+    return (size_t)(align_up((int64_t)M * K / 2, 256) + align_up((int64_t)M * K / 16, 256) + 256);
+  }
+  return 0;
+}
+
+qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y, int M, int64_t N,
+                    int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !packed_W || !x || !y || !ws) return QMV_EINVAL;
+  if (M < 1 || M > QMV_MAX_M || N <= 0 || K <= 0) return QMV_EINVAL;
+  Layout L;
+  if (!make_layout((int)fmt, N, K, 1, &L)) return QMV_EUNSUPPORTED;
+  if (!aligned(packed_W, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return QMV_ECUDA;
+  if (ws_bytes < (size_t)ws_plan_stream(M, 0, sms).total) return QMV_EWORKSPACE;
+  unsigned* status = status_ptr();
+  if (!status) return QMV_ECUDA;
+  StreamArgs a;
+  a.L = L;
+  a.packed = static_cast<const uint8_t*>(packed_W);
+  a.x = x; a.y = y; a.ids = nullptr;
+  a.M = M; a.topk = 1; a.x_per_pair = 0;
+  a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
+  a.status = status;
+  const int64_t slabs = L.row_tiles * L.k_groups;
+  a.num_ctas = (int)(slabs < sms ? slabs : sms);
+  int variant = 0;
+  qmv_status st = from_cuda(launch_stream(a, stream, &variant));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
+  return st;
+}
+
+qmv_status qmv_grouped(qmv_fmt fmt, const void* tower, const int32_t* expert_ids, const uint16_t* x,
+                       int x_per_pair, float* y, int M, int topk, int64_t N, int64_t K, int64_t E,
+                       void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !tower || !expert_ids || !x || !y || !ws) return QMV_EINVAL;
+  if (M < 1 || M > QMV_MAX_M || topk < 1 || topk > 8 || N <= 0 || K <= 0 || E <= 0) return QMV_EINVAL;
+  if (x_per_pair != 0 && x_per_pair != 1) return QMV_EINVAL;
+  if (E > (int64_t)1 << 24) return QMV_EUNSUPPORTED;   // ids are packed with a 6-bit pair index
+  Layout L;
+  if (!make_layout((int)fmt, N, K, E, &L)) return QMV_EUNSUPPORTED;
+  if (!aligned(tower, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4) ||
+      !aligned(expert_ids, 4))
+    return QMV_EALIGN;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return QMV_ECUDA;
+  if (ws_bytes < (size_t)ws_plan_stream(M, 0, sms).total) return QMV_EWORKSPACE;
+  unsigned* status = status_ptr();
+  if (!status) return QMV_ECUDA;
+  StreamArgs a;
+  a.L = L;
+  a.packed = static_cast<const uint8_t*>(tower);
+  a.x = x; a.y = y; a.ids = expert_ids;
+  a.M = M; a.topk = topk; a.x_per_pair = x_per_pair;
+  a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
+  a.status = status;
+  a.num_ctas = sms;
+  int variant = 0;
+  qmv_status st = from_cuda(launch_stream(a, stream, &variant));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
+  return st;
+}
+
+qmv_status qmv_quant_act_nvfp4(const uint16_t* x, float x_scale, uint8_t* codes, uint8_t* scales, int M,
+                               int64_t K, cudaStream_t stream) {
+  if (!x || !codes || !scales || M < 1 || K <= 0 || !(x_scale >= 0.0f)) return QMV_EINVAL;
+  if (K % 16) return QMV_EUNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(codes, 8)) return QMV_EALIGN;
+  qmv_status st = from_cuda(launch_quant_act(x, x_scale, codes, scales, M, K, stream));
+  if (st == QMV_OK) g_last_route = QMV_NVFP4 * 100 + 8;
+  return st;
+}
+
+qmv_status qmv_gemm_nvfp4_w4a4(const void* packed_W, const uint16_t* x, float x_scale, float* y, int M,
+                               int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)packed_W; (void)x; (void)x_scale; (void)y; (void)M; (void)N; (void)K; (void)ws; (void)ws_bytes;
+  (void)stream;
+  return QMV_EUNSUPPORTED;
+}
+
+const char* qmv_status_str(qmv_status s) {
+  switch (s) {
+    case QMV_OK: return "ok";
+    case QMV_EINVAL: return "invalid argument";
+    case QMV_EALIGN: return "misaligned pointer";
+    case QMV_EUNSUPPORTED: return "unsupported shape or format";
+    case QMV_ECUDA: return "CUDA error";
+    case QMV_EHEADER: return "packed header does not match the arguments";
+    case QMV_ETIMEOUT: return "a bounded device wait timed out";
+    case QMV_ERANGE: return "expert id out of range";
+    case QMV_EWORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+int qmv_last_route(void) { return g_last_route; }
+
+qmv_status qmv_device_status(int reset) {
+  unsigned* p = status_ptr();
+  if (!p) return QMV_ECUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return QMV_ECUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return QMV_ECUDA;
+  if (reset) {
+    unsigned z = 0;
+    if (cudaMemcpyToSymbol(g_status, &z, sizeof(z)) != cudaSuccess) return QMV_ECUDA;
+  }
+  if (v & kStatHeader) return QMV_EHEADER;
+  if (v & kStatTimeout) return QMV_ETIMEOUT;
+  if (v & kStatRange) return QMV_ERANGE;
+  return QMV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// qmv_internal.h -- host-side launchers shared between the library's translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include "qmv_layout.cuh"
+
+namespace qmv {
+
+// device status bits (latched with atomicOr into the per-device status word)
+constexpr unsigned kStatHeader = 1u;
+constexpr unsigned kStatTimeout = 2u;
+constexpr unsigned kStatRange = 4u;
+
+// Arguments of the streaming GEMV kernel (dense and grouped forms).
+struct StreamArgs {
+  Layout L;
+  const uint8_t* packed;     // packed buffer (header at offset 0)
+  const uint16_t* x;         // bf16 activations
+  float* y;                  // fp32 outputs
+  const int32_t* ids;        // grouped: expert ids [M][topk]; dense: nullptr
+  int M;                     // tokens (rows of x for dense)
+  int topk;                  // grouped: slots per token; dense: 1
+  int x_per_pair;            // grouped: 1 if x has one row per (token, slot)
+  uint8_t* ws;               // workspace (zero-filled; status area in the first 256 B)
+  int64_t ws_bytes;
+  unsigned* status;          // per-device status word
+  int num_ctas;              // persistent grid size
+};
+
+// workspace carve-up (bytes), shared by the host size query and the kernels
+struct WsPlan {
+  int64_t counters_off, counters_bytes;
+  int64_t partials_off, partials_bytes;
+  int64_t total;
+};
+WsPlan ws_plan_stream(int M, int64_t tiles_max, int num_ctas);
+
+int num_sms_current_device();
+
+cudaError_t launch_pack(const Layout& L, const uint8_t* canon, uint8_t* dst, cudaStream_t s);
+cudaError_t launch_dequant(const Layout& L, const uint8_t* packed, int64_t row0, int64_t rows,
+                           float* out, unsigned* status, cudaStream_t s);
+cudaError_t launch_quantize(int fmt, const float* W, int64_t rows, int64_t K, float ts,
+                            uint8_t* canon, cudaStream_t s);
+cudaError_t launch_quant_act(const uint16_t* x, float xs, uint8_t* codes, uint8_t* scales, int M,
+                             int64_t K, cudaStream_t s);
+// returns the route variant launched (1 = CUDA-core M=1, 2 = mma M>1, 3 = grouped)
+cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant);
+
+}  // namespace qmv

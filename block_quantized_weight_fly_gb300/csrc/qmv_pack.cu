@@ -1,0 +1,418 @@
+// qmv_pack.cu -- load-phase kernels: canonical -> packed repack, BlockToFloat on the
+// packed layout, the synthetic-data quantizers, and the NVFP4 activation quantizer.
+//
+// None of these is on the per-token GEMV path except the activation quantizer
+// of the W4A4 prefill route.
+#include <cuda_fp16.h>
+#include "qmv_internal.h"
+
+namespace qmv {
+
+// ---------------------------------------------------------------------------
+// canonical -> packed. One thread per (expert, row < N, 32-value chunk); the
+// buffer is zero-filled first, which also writes every padding row, padding
+// chunk and alignment gap.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void copy_bytes(uint8_t* dst, const uint8_t* src, int n) {
+  for (int i = 0; i < n; ++i) dst[i] = src[i];
+}
+
+__device__ __forceinline__ uint8_t* group_plane(const Layout& L, uint8_t* base, int64_t e, int64_t g) {
+  return base + kHeaderBytes + e * L.expert_bytes + g * L.group_bytes;
+}
+
+__global__ void pack_kernel(Layout L, const uint8_t* __restrict__ canon, uint8_t* __restrict__ dst) {
+  const int64_t chunks = L.K / kChunk;
+  const int64_t total = L.E * L.N * chunks;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx == 0) {
+    PackedHeader* h = reinterpret_cast<PackedHeader*>(dst);
+    h->magic = kMagic; h->version = kVersion; h->fmt = (uint32_t)L.fmt; h->reserved = 0;
+    h->N = L.N; h->K = L.K; h->E = L.E;
+    h->expert_bytes = L.expert_bytes; h->plane_bytes = L.group_bytes;
+  }
+  if (idx >= total) return;
+  const int64_t c = idx % chunks;
+  const int64_t rest = idx / chunks;
+  const int64_t n = rest % L.N;
+  const int64_t e = rest / L.N;
+  const int64_t g = c / kChunksPerSlab;
+  const int cl = (int)(c % kChunksPerSlab);
+  uint8_t* plane = group_plane(L, dst, e, g);
+  uint8_t* rec = plane + n * L.rec;
+  uint8_t* extras = dst + kHeaderBytes + e * L.expert_bytes + L.k_groups * L.group_bytes;
+  const int64_t row = e * L.N + n;          // row of the stacked tower
+  switch (L.fmt) {
+    case F_Q8_0: {
+      const uint8_t* src = canon + (row * chunks + c) * 34;
+      copy_bytes(rec + 2 * cl, src, 2);
+      copy_bytes(rec + q80_q_off(cl, 0), src + 2, 32);
+    } break;
+    case F_Q4_K: {
+      const uint8_t* blk = canon + (row * (L.K / 256) + g) * 144;
+      copy_bytes(rec + q4k_q_off(cl), blk + 16 + 16 * cl, 16);
+      if (cl == 0) copy_bytes(rec, blk, 16);
+    } break;
+    case F_Q6_K: {
+      const uint8_t* blk = canon + (row * (L.K / 256) + g) * 210;
+      copy_bytes(rec + q6k_ql_off(cl), blk + 16 * cl, 16);
+      copy_bytes(rec + q6k_qh_off(cl), blk + 128 + 8 * cl, 8);
+      if (cl == 0) {
+        copy_bytes(rec + 192, blk + 192, 16);
+        copy_bytes(plane + L.plane_a + 2 * n, blk + 208, 2);
+      }
+    } break;
+    case F_NVFP4: {
+      const uint8_t* ce = canon + e * canon_matrix_bytes(F_NVFP4, L.N, L.K);
+      copy_bytes(rec + nv_q_off(cl), ce + n * (L.K / 2) + c * 16, 16);
+      copy_bytes(rec + 2 * cl, ce + L.N * (L.K / 2) + n * (L.K / 16) + 2 * c, 2);
+      if (n == 0 && c == 0) copy_bytes(extras, ce + L.N * (L.K / 2) + L.N * (L.K / 16), 4);
+    } break;
+    case F_FP8: {
+      const uint8_t* ce = canon + e * canon_matrix_bytes(F_FP8, L.N, L.K);
+      const int r = (int)(n & 7);
+      copy_bytes(rec + fp8_v_off(2 * cl, r), ce + n * L.K + 32 * c, 16);
+      copy_bytes(rec + fp8_v_off(2 * cl + 1, r), ce + n * L.K + 32 * c + 16, 16);
+      if (c == 0) copy_bytes(extras + 4 * n, ce + L.N * L.K + 4 * n, 4);
+    } break;
+  }
+}
+
+cudaError_t launch_pack(const Layout& L, const uint8_t* canon, uint8_t* dst, cudaStream_t s) {
+  cudaError_t err = cudaMemsetAsync(dst, 0, (size_t)L.total, s);
+  if (err != cudaSuccess) return err;
+  const int64_t total = L.E * L.N * (L.K / kChunk);
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  pack_kernel<<<(unsigned)blocks, threads, 0, s>>>(L, canon, dst);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// BlockToFloat on the packed layout. One thread per (tower row, chunk); the
+// op order is the canonical one and every product is rounded on its own
+// (__fmul_rn / __fsub_rn keep the compiler from fusing them).
+// ---------------------------------------------------------------------------
+__device__ bool header_ok(const uint8_t* packed, const Layout& L) {
+  const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed);
+  return h->magic == kMagic && h->version == kVersion && h->fmt == (uint32_t)L.fmt &&
+         h->N == L.N && h->K == L.K && h->E == L.E && h->expert_bytes == L.expert_bytes;
+}
+
+__global__ void dequant_kernel(Layout L, const uint8_t* __restrict__ packed, int64_t row0,
+                               int64_t rows, float* __restrict__ out, unsigned* status) {
+  const int64_t chunks = L.K / kChunk;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (!header_ok(packed, L)) {
+    if (idx == 0) atomicOr(status, kStatHeader);
+    return;
+  }
+  if (idx >= rows * chunks) return;
+  const int64_t c = idx % chunks;
+  const int64_t row = row0 + idx / chunks;
+  const int64_t e = row / L.N, n = row % L.N;
+  const int64_t g = c / kChunksPerSlab;
+  const int cl = (int)(c % kChunksPerSlab);
+  const uint8_t* plane = packed + kHeaderBytes + e * L.expert_bytes + g * L.group_bytes;
+  const uint8_t* rec = plane + n * L.rec;
+  const uint8_t* extras = packed + kHeaderBytes + e * L.expert_bytes + L.k_groups * L.group_bytes;
+  float* o = out + (row - row0) * L.K + c * kChunk;
+  switch (L.fmt) {
+    case F_Q8_0: {
+      const int8_t* q = reinterpret_cast<const int8_t*>(rec + q80_q_off(cl, 0));
+      float d = h2f(*reinterpret_cast<const uint16_t*>(rec + 2 * cl));
+      for (int i = 0; i < 32; ++i) o[i] = __fmul_rn(d, (float)q[i]);
+    } break;
+    case F_Q4_K: {
+      const uint8_t* q = rec + q4k_q_off(cl);
+      const uint32_t* hd = reinterpret_cast<const uint32_t*>(rec);
+      float d = h2f(hd[0]), dmin = h2f(hd[0] >> 16);
+      uint32_t sc = q4k_field(hd[1], hd[2], hd[3], cl), m = q4k_field(hd[1], hd[2], hd[3], 8 + cl);
+      float a = __fmul_rn(d, (float)sc), b = __fmul_rn(dmin, (float)m);
+      for (int i = 0; i < 32; ++i) {
+        uint32_t qq = (q[i >> 1] >> (4 * (i & 1))) & 15u;
+        o[i] = __fsub_rn(__fmul_rn(a, (float)qq), b);
+      }
+    } break;
+    case F_Q6_K: {
+      const uint8_t* ql = rec + q6k_ql_off(cl);
+      const uint8_t* qh = rec + q6k_qh_off(cl);
+      const int8_t* sc = reinterpret_cast<const int8_t*>(rec + 192);
+      float d = h2f(*reinterpret_cast<const uint16_t*>(plane + L.plane_a + 2 * n));
+      for (int i = 0; i < 32; ++i) {
+        int lo = (ql[i >> 1] >> (4 * (i & 1))) & 15;
+        int hi = (qh[i >> 2] >> (2 * (i & 3))) & 3;
+        int qq = lo | (hi << 4);
+        float a = __fmul_rn(d, (float)sc[2 * cl + (i >> 4)]);
+        o[i] = __fmul_rn(a, (float)(qq - 32));
+      }
+    } break;
+    case F_NVFP4: {
+      const uint8_t* cc = rec + nv_q_off(cl);
+      const float sT = *reinterpret_cast<const float*>(extras);
+      for (int i = 0; i < 32; ++i) {
+        uint32_t code = (cc[i >> 1] >> (4 * (i & 1))) & 15u;
+        float p = __fmul_rn(e2m1f(code), e4m3f(rec[2 * cl + (i >> 4)]));
+        o[i] = __fmul_rn(p, sT);
+      }
+    } break;
+    case F_FP8: {
+      const int r = (int)(n & 7);
+      const uint8_t* c0 = rec + fp8_v_off(2 * cl, r);
+      const uint8_t* c1 = rec + fp8_v_off(2 * cl + 1, r);
+      const float s = reinterpret_cast<const float*>(extras)[n];
+      for (int i = 0; i < 16; ++i) o[i] = __fmul_rn(e4m3f(c0[i]), s);
+      for (int i = 0; i < 16; ++i) o[16 + i] = __fmul_rn(e4m3f(c1[i]), s);
+    } break;
+  }
+}
+
+cudaError_t launch_dequant(const Layout& L, const uint8_t* packed, int64_t row0, int64_t rows,
+                           float* out, unsigned* status, cudaStream_t s) {
+  const int64_t total = rows * (L.K / kChunk);
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  if (blocks == 0) return cudaSuccess;
+  dequant_kernel<<<(unsigned)blocks, threads, 0, s>>>(L, packed, row0, rows, out, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Quantizers for synthetic data. fp32 arithmetic with every operation rounded
+// on its own, in the order written; round-to-nearest-even everywhere.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t f2h_bits(float f) {
+  return (uint32_t)__half_as_ushort(__float2half_rn(f));
+}
+__device__ __forceinline__ uint32_t f2e4m3(float f) {   // RNE, saturate to +-448
+  unsigned short v;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(v) : "f"(0.0f), "f"(f));
+  return v & 0xFFu;
+}
+__device__ __forceinline__ uint32_t f2e2m1(float f) {   // RNE, saturate to +-6
+  uint32_t v;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+      : "=r"(v) : "f"(0.0f), "f"(f));
+  return v & 0xFu;
+}
+__device__ __forceinline__ float clampf(float v, float lo, float hi) { return fminf(fmaxf(v, lo), hi); }
+
+__global__ void quant_q8_0_kernel(const float* __restrict__ W, int64_t nblk, uint8_t* __restrict__ out) {
+  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  const float* x = W + b * 32;
+  float amax = 0.0f;
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const uint32_t d = f2h_bits(__fdiv_rn(amax, 127.0f));
+  const float dd = h2f(d);
+  // assemble the 34-byte block in registers, then store it byte by byte
+  uint32_t words[9];
+  words[0] = d;
+  for (int i = 1; i < 9; ++i) words[i] = 0u;
+  for (int i = 0; i < 32; ++i) {
+    const float q = (dd == 0.0f) ? 0.0f : clampf(rintf(__fdiv_rn(x[i], dd)), -127.0f, 127.0f);
+    const uint32_t byte = (uint32_t)((int)q) & 0xFFu;
+    const int pos = 2 + i;
+    words[pos >> 2] |= byte << (8 * (pos & 3));
+  }
+  uint8_t* o = out + b * 34;
+  for (int i = 0; i < 34; ++i) o[i] = (uint8_t)(words[i >> 2] >> (8 * (i & 3)));
+}
+
+__global__ void quant_q4_k_kernel(const float* __restrict__ W, int64_t nblk, uint8_t* __restrict__ out) {
+  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  const float* x = W + b * 256;
+  uint8_t* o = out + b * 144;
+  float s[8], mn[8], smax = 0.0f, mmax = 0.0f;
+  for (int j = 0; j < 8; ++j) {
+    float lo = 0.0f, hi = x[32 * j];
+    for (int i = 0; i < 32; ++i) {
+      float v = x[32 * j + i];
+      lo = fminf(lo, v);
+      hi = fmaxf(hi, v);
+    }
+    s[j] = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+    mn[j] = -lo;
+    smax = fmaxf(smax, s[j]);
+    mmax = fmaxf(mmax, mn[j]);
+  }
+  uint32_t d = f2h_bits(__fdiv_rn(smax, 63.0f)), dmin = f2h_bits(__fdiv_rn(mmax, 63.0f));
+  float dd = h2f(d), dm = h2f(dmin);
+  uint32_t sw[3] = {0u, 0u, 0u};
+  uint32_t sc[8], mq[8];
+  for (int j = 0; j < 8; ++j) {
+    sc[j] = (dd == 0.0f) ? 0u : (uint32_t)clampf(rintf(__fdiv_rn(s[j], dd)), 0.0f, 63.0f);
+    mq[j] = (dm == 0.0f) ? 0u : (uint32_t)clampf(rintf(__fdiv_rn(mn[j], dm)), 0.0f, 63.0f);
+  }
+  for (int f = 0; f < 16; ++f) {
+    uint32_t v = f < 8 ? sc[f] : mq[f - 8];
+    for (int bit = 0; bit < 6; ++bit) {
+      int pos = 6 * f + bit;
+      sw[pos >> 5] |= ((v >> bit) & 1u) << (pos & 31);
+    }
+  }
+  o[0] = (uint8_t)d; o[1] = (uint8_t)(d >> 8); o[2] = (uint8_t)dmin; o[3] = (uint8_t)(dmin >> 8);
+  for (int i = 0; i < 12; ++i) o[4 + i] = (uint8_t)(sw[i >> 2] >> (8 * (i & 3)));
+  for (int j = 0; j < 8; ++j) {
+    float den = __fmul_rn(dd, (float)sc[j]);
+    float off = __fmul_rn(dm, (float)mq[j]);
+    for (int i = 0; i < 32; i += 2) {
+      uint32_t q2[2];
+      for (int u = 0; u < 2; ++u) {
+        float num = __fadd_rn(x[32 * j + i + u], off);
+        q2[u] = (den == 0.0f) ? 0u : (uint32_t)clampf(rintf(__fdiv_rn(num, den)), 0.0f, 15.0f);
+      }
+      o[16 + (32 * j + i) / 2] = (uint8_t)(q2[0] | (q2[1] << 4));
+    }
+  }
+}
+
+__global__ void quant_q6_k_kernel(const float* __restrict__ W, int64_t nblk, uint8_t* __restrict__ out) {
+  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  const float* x = W + b * 256;
+  uint8_t* o = out + b * 210;
+  float s[16], smax = 0.0f;
+  for (int j = 0; j < 16; ++j) {
+    float amax = 0.0f;
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[16 * j + i]));
+    s[j] = __fdiv_rn(amax, 32.0f);
+    smax = fmaxf(smax, s[j]);
+  }
+  uint32_t d = f2h_bits(__fdiv_rn(smax, 127.0f));
+  float dd = h2f(d);
+  for (int i = 0; i < 192; ++i) o[i] = 0;
+  for (int j = 0; j < 16; ++j) {
+    int sc = (dd == 0.0f) ? 0 : (int)clampf(rintf(__fdiv_rn(s[j], dd)), -128.0f, 127.0f);
+    o[192 + j] = (uint8_t)(int8_t)sc;
+    float den = __fmul_rn(dd, (float)sc);
+    for (int i = 0; i < 16; ++i) {
+      int e = 16 * j + i;
+      int q = (den == 0.0f) ? 0 : (int)clampf(rintf(__fdiv_rn(x[e], den)), -32.0f, 31.0f);
+      int u = q + 32;
+      o[e >> 1] |= (uint8_t)((u & 15) << (4 * (e & 1)));
+      o[128 + (e >> 2)] |= (uint8_t)(((u >> 4) & 3) << (2 * (e & 3)));
+    }
+  }
+  o[208] = (uint8_t)d; o[209] = (uint8_t)(d >> 8);
+}
+
+// NVFP4: one thread per 16-value block of row-major W[rows][K]
+__global__ void quant_nvfp4_kernel(const float* __restrict__ W, int64_t rows, int64_t K, float sT,
+                                   uint8_t* __restrict__ out) {
+  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t bpr = K / 16;
+  if (b >= rows * bpr) return;
+  const int64_t r = b / bpr, kb = b % bpr;
+  const float* x = W + r * K + kb * 16;
+  float amax = 0.0f;
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  float t = __fmul_rn(6.0f, sT);
+  uint32_t sb = (t > 0.0f) ? f2e4m3(__fdiv_rn(amax, t)) : 0u;
+  out[rows * (K / 2) + r * bpr + kb] = (uint8_t)sb;
+  float den = __fmul_rn(e4m3f(sb), sT);
+  uint8_t* codes = out + r * (K / 2) + kb * 8;
+  for (int i = 0; i < 16; i += 2) {
+    uint32_t c0 = (den == 0.0f) ? 0u : f2e2m1(__fdiv_rn(x[i], den));
+    uint32_t c1 = (den == 0.0f) ? 0u : f2e2m1(__fdiv_rn(x[i + 1], den));
+    codes[i >> 1] = (uint8_t)(c0 | (c1 << 4));
+  }
+  if (b == 0) *reinterpret_cast<float*>(out + rows * (K / 2) + rows * bpr) = sT;
+}
+
+// FP8 row-scaled: one block per row
+__global__ void quant_fp8_kernel(const float* __restrict__ W, int64_t rows, int64_t K,
+                                 uint8_t* __restrict__ out) {
+  const int64_t r = blockIdx.x;
+  const float* x = W + r * K;
+  __shared__ float red[32];
+  float amax = 0.0f;
+  for (int64_t k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(x[k]));
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float s = __fdiv_rn(red[0], 448.0f);
+  for (int64_t k = threadIdx.x; k < K; k += blockDim.x)
+    out[r * K + k] = (uint8_t)((s == 0.0f) ? 0u : f2e4m3(__fdiv_rn(x[k], s)));
+  if (threadIdx.x == 0) *reinterpret_cast<float*>(out + rows * K + 4 * r) = s;
+}
+
+cudaError_t launch_quantize(int fmt, const float* W, int64_t rows, int64_t K, float ts,
+                            uint8_t* canon, cudaStream_t s) {
+  const int threads = 128;
+  switch (fmt) {
+    case F_Q8_0: {
+      int64_t n = rows * (K / 32);
+      quant_q8_0_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, n, canon);
+    } break;
+    case F_Q4_K: {
+      int64_t n = rows * (K / 256);
+      quant_q4_k_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, n, canon);
+    } break;
+    case F_Q6_K: {
+      int64_t n = rows * (K / 256);
+      quant_q6_k_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, n, canon);
+    } break;
+    case F_NVFP4: {
+      int64_t n = rows * (K / 16);
+      quant_nvfp4_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, rows, K, ts, canon);
+    } break;
+    case F_FP8:
+      quant_fp8_kernel<<<(unsigned)rows, 256, 0, s>>>(W, rows, K, canon);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 activation quantizer: one thread per 16-value block of x[M][K].
+// s_b = e4m3(amax_b / (6 x_scale)); zero block scale -> zero codes;
+// else codes = e2m1(x / (s_b x_scale)).
+// ---------------------------------------------------------------------------
+__global__ void quant_act_kernel(const uint16_t* __restrict__ x, float xs, uint8_t* __restrict__ codes,
+                                 uint8_t* __restrict__ scales, int64_t M, int64_t K) {
+  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t bpr = K / 16;
+  if (b >= M * bpr) return;
+  const int64_t m = b / bpr, kb = b % bpr;
+  const uint4* src = reinterpret_cast<const uint4*>(x + m * K + kb * 16);
+  uint4 v0 = src[0], v1 = src[1];
+  uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float xv[16];
+  float amax = 0.0f;
+  for (int i = 0; i < 8; ++i) {
+    xv[2 * i] = bf2f(w[i]);
+    xv[2 * i + 1] = bf2f(w[i] >> 16);
+    amax = fmaxf(amax, fmaxf(fabsf(xv[2 * i]), fabsf(xv[2 * i + 1])));
+  }
+  const float t = __fmul_rn(6.0f, xs);
+  const uint32_t sb = (t > 0.0f) ? f2e4m3(__fdiv_rn(amax, t)) : 0u;
+  scales[m * bpr + kb] = (uint8_t)sb;
+  uint32_t packed[2] = {0u, 0u};
+  if (sb != 0u) {
+    const float den = __fmul_rn(e4m3f(sb), xs);
+    for (int i = 0; i < 16; ++i) packed[i >> 3] |= f2e2m1(__fdiv_rn(xv[i], den)) << (4 * (i & 7));
+  }
+  uint2* dst = reinterpret_cast<uint2*>(codes + m * (K / 2) + kb * 8);
+  *dst = make_uint2(packed[0], packed[1]);
+}
+
+cudaError_t launch_quant_act(const uint16_t* x, float xs, uint8_t* codes, uint8_t* scales, int M,
+                             int64_t K, cudaStream_t s) {
+  const int64_t n = (int64_t)M * (K / 16);
+  const int threads = 128;
+  if (n == 0) return cudaSuccess;
+  quant_act_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(x, xs, codes, scales, M, K);
+  return cudaGetLastError();
+}
+
+}  // namespace qmv

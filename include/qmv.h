@@ -1,0 +1,183 @@
+/*
+ * qmv.h -- C ABI of libqmv: decode-time matmul y[M,N] = x[M,K] . W[N,K]^T with W
+ * kept in a packed block-quantized format and decoded on the fly inside the
+ * kernel, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the keep-quant matmul seam Y = X . W^T with a quantized W,
+ * over one matrix (E = 1) or a stacked expert tower weight[E*N, K]
+ * ("vllm.cpp #3030, BACKEND-TENSTORRENT-KEEPQUANT: the 27B arm", scope item 2
+ * and the "Re-anchor" comment). Formats: GGUF-style Q8_0 / Q4_K / Q6_K keep-quant
+ * blocks (same issue, artifact table and "Budget on the 32 GB P150"), and NVFP4
+ * E2M1 codes with E4M3 block scales plus row-scaled FP8 ("I Built a Custom
+ * Blackwell Kernel for Qwen3.8-27B", "What the custom path actually does").
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller allocates and owns every buffer. The library never
+ *    allocates or frees memory, never synchronizes a stream, and never reads
+ *    device data on the host. All work is enqueued on `stream`.
+ *  - Pointers marked "device" must be device memory of the current device.
+ *    packed buffers and workspaces must be 256-byte aligned; x and y 16-byte
+ *    aligned.
+ *  - Errors: arguments are validated on the host before anything is launched;
+ *    a failed check returns its status and launches nothing. A launch failure
+ *    returns QMV_ECUDA. Faults detected on the device (a packed header that does
+ *    not match the arguments, an expert id out of range, a pipeline wait that
+ *    timed out) are latched in a per-device status word that
+ *    qmv_device_status() reads; the kernel then skips its work.
+ *  - Numerics: weights are decoded exactly (see qmv_dequant); products with the
+ *    bf16 activations are exact in fp32 and accumulate in fp32.
+ *
+ * Canonical byte layouts (the input of qmv_pack and output of qmv_quantize):
+ *   Q8_0  34 B per 32 values : fp16 d | 32 x int8 q;           w = d * q
+ *   Q4_K 144 B per 256 values: fp16 d | fp16 dmin | 12 B scales | 128 B nibbles
+ *         scales: 96-bit little-endian bitstream of sixteen 6-bit fields, fields
+ *         0..7 = sc_j, 8..15 = m_j for the eight 32-value sub-blocks; nibble byte b
+ *         holds element 2b (low) and 2b+1 (high);   w = (d * sc_j) * q - dmin * m_j
+ *   Q6_K 210 B per 256 values: 128 B ql | 64 B qh | 16 x int8 sc | fp16 d
+ *         q = ql nibble | (qh 2 bits << 4); ql byte b holds elements 2b, 2b+1;
+ *         qh byte b holds elements 4b..4b+3 at bits 0,2,4,6; w = (d * sc_j) * (q - 32)
+ *   NVFP4 per matrix: E2M1 codes [N][K/2] (element 2i = low nibble of byte i) |
+ *         E4M3 scales [N][K/16] | fp32 tensor scale s_T; w = (e2m1 * e4m3) * s_T
+ *   FP8_ROW per matrix: E4M3 codes [N][K] | fp32 row scales [N];  w = e4m3 * s_n
+ *   A tower of E experts is E such matrices back to back.
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QMV_Q8_0 = 1,
+    QMV_Q4_K = 2,
+    QMV_Q6_K = 3,
+    QMV_NVFP4 = 4,
+    QMV_FP8_ROW = 5
+} qmv_fmt;
+
+typedef enum {
+    QMV_OK = 0,
+    QMV_EINVAL = 1,        /* bad argument (null pointer, size, M out of range, ...) */
+    QMV_EALIGN = 2,        /* a pointer is not aligned as required */
+    QMV_EUNSUPPORTED = 3,  /* valid request this build does not serve (K not a multiple of
+                              the lane granule, format not allowed on this entry point) */
+    QMV_ECUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    QMV_EHEADER = 5,       /* device status: packed header does not match the arguments */
+    QMV_ETIMEOUT = 6,      /* device status: a bounded pipeline wait ran out */
+    QMV_ERANGE = 7,        /* device status: an expert id was outside [0, E), or one expert
+                              got more than 8 rows of x (ids repeated within a token) */
+    QMV_EWORKSPACE = 8     /* workspace too small for this call */
+} qmv_status;
+
+/* Entry ids for qmv_workspace_size. */
+enum { QMV_ENTRY_GEMV = 1, QMV_ENTRY_GROUPED = 2, QMV_ENTRY_W4A4 = 3 };
+
+/* Largest decode batch served by qmv_gemv / qmv_grouped (M rows of x). */
+#define QMV_MAX_M 8
+
+/* Bytes of the canonical stream of an E-expert tower of [N, K] matrices.
+ * Returns 0 for an unknown format or a K that is not a multiple of the block. */
+size_t qmv_canon_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
+
+/* Bytes of the device ("packed") layout, header included. The packed layout
+ * regroups each matrix into slabs of 128 rows x 256 values whose fields sit in
+ * 16-byte planes, so one bulk copy moves a slab and every lane's 128-bit load
+ * is aligned; rows are padded to a multiple of 128 with zero blocks. The slab
+ * bytes are the canonical bytes, only reordered (the per-value cost is
+ * unchanged). K must be a multiple of 32 (Q8_0, NVFP4, FP8_ROW) or 256 (Q4_K,
+ * Q6_K). Returns 0 if unsupported. */
+size_t qmv_pack_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
+
+/* Repack canonical bytes into the device layout. canon: device, qmv_canon_size
+ * bytes. dst: device, qmv_pack_size bytes, 256-B aligned; fully overwritten
+ * (header, slabs, padding). One-time load-phase work (the stacked tower loader
+ * and planar repack of the pages), not part of the per-token path. */
+qmv_status qmv_pack(qmv_fmt fmt, const void* canon, int64_t N, int64_t K, int64_t E,
+                    void* dst, cudaStream_t stream);
+
+/* Encode fp32 W[rows, K] (device, row-major) into canonical bytes (device,
+ * qmv_canon_size(fmt, rows, K, 1) bytes) with the round-to-nearest quantizers
+ * used for synthetic data. tensor_scale is the NVFP4 per-tensor scale s_T (a
+ * given constant); ignored for other formats. Not on the per-token path. */
+qmv_status qmv_quantize(qmv_fmt fmt, const float* W, int64_t rows, int64_t K,
+                        float tensor_scale, void* canon, cudaStream_t stream);
+
+/* BlockToFloat on the device layout: W_out[r][k] (fp32, device) for rows
+ * row0 .. row0+rows-1 of the stacked tower (row = e*N + n). Bit-exact with the
+ * canonical decode formulas above, in that op order. Used to check the layout. */
+qmv_status qmv_dequant(qmv_fmt fmt, const void* packed, int64_t N, int64_t K, int64_t E,
+                       int64_t row0, int64_t rows, float* W_out, cudaStream_t stream);
+
+/* Workspace bytes needed by an entry point for these sizes (host-only query; it
+ * reads the SM count of the current device). The workspace must be zero-filled
+ * once before its first use. It holds one flag word per CTA (bytes 256 ..
+ * 256 + 4 * SM count) and the partial sums of row tiles split between CTAs; a
+ * call that returns without a device status error leaves every flag word zero
+ * again, so the same workspace serves the next call as is. After a device status
+ * error, zero-fill it again. Calls sharing one workspace must not overlap. */
+size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, int64_t E,
+                          int topk);
+
+/* Decode GEMV, M = 1..8: y[m][n] = sum_k W[n][k] * x[m][k].
+ * packed_W: device layout of one [N, K] matrix (E = 1). x: device bf16 [M][K]
+ * (raw bits, row-major). y: device fp32 [M][N], fully overwritten. ws: device,
+ * qmv_workspace_size(QMV_ENTRY_GEMV, ...) bytes. The weights are streamed from
+ * HBM once per call for all M rows. */
+qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y, int M,
+                    int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Grouped per-expert GEMV over a stacked tower of E experts.
+ * expert_ids: device int32 [M][topk] (ids within a token distinct; never read
+ * on the host). x: device bf16, [M][K] if x_per_pair == 0 (every slot of a
+ * token uses its row) or [M*topk][K] if x_per_pair == 1 (one row per (token,
+ * slot)). y: device fp32 [M][topk][N], fully overwritten:
+ *   y[t][j][:] = W_{expert_ids[t][j]} . x_row(t, j).
+ * Each distinct routed expert's rows are streamed once per call, for every row
+ * of x routed to it ("A 320B MoE on a free Kaggle TPU", "The decode kernel's
+ * cost is not 'distinct experts'"). M = 1..8, topk = 1..8. */
+qmv_status qmv_grouped(qmv_fmt fmt, const void* tower, const int32_t* expert_ids,
+                       const uint16_t* x, int x_per_pair, float* y, int M, int topk,
+                       int64_t N, int64_t K, int64_t E, void* ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/* NVFP4 activation quantizer (W4A4 prefill): per 16-value block of bf16 x[M][K],
+ * s_b = e4m3_rne_sat(amax_b / (6 x_scale)); codes = e2m1_rne_sat(x / (s_b x_scale)),
+ * zero when s_b is zero. x_scale: the static per-site activation scale.
+ * codes: device [M][K/2] (element 2i in the low nibble); scales: device [M][K/16]. */
+qmv_status qmv_quant_act_nvfp4(const uint16_t* x, float x_scale, uint8_t* codes,
+                               uint8_t* scales, int M, int64_t K, cudaStream_t stream);
+
+/* NVFP4 W4A4 prefill GEMM: the activation is quantized to NVFP4 (as
+ * qmv_quant_act_nvfp4) into ws, then a tcgen05 block-scaled MMA computes
+ * y[m][n] = x_scale * s_T * sum_b s_b(x) s_b(W) sum_i e2m1(x) e2m1(W)
+ * in fp32 ("I Built a Custom Blackwell Kernel", "What the custom path actually
+ * does": W4A4 tensor-core kernels after quantising the activation).
+ * packed_W: device layout of one NVFP4 [N, K] matrix. M: any size >= 1 (meant for
+ * prefill, M >= 128). y: device fp32 [M][N]. K must be a multiple of 256 and N of 128. */
+qmv_status qmv_gemm_nvfp4_w4a4(const void* packed_W, const uint16_t* x, float x_scale,
+                               float* y, int M, int64_t N, int64_t K, void* ws,
+                               size_t ws_bytes, cudaStream_t stream);
+
+/* Human-readable name of a status. */
+const char* qmv_status_str(qmv_status s);
+
+/* Route id of the kernel the last successful call on this host thread launched:
+ * format * 100 + variant (1 = M=1 streaming CUDA-core GEMV, 2 = M>1 streaming
+ * mma.sync GEMV, 3 = grouped, 4 = W4A4 tcgen05, 5 = dequant, 6 = pack,
+ * 7 = quantize, 8 = activation quantizer). Test hook. */
+int qmv_last_route(void);
+
+/* Read (and, if reset != 0, clear) the device status word of the current
+ * device. Synchronizes the device. Returns QMV_OK or the first latched device
+ * status (QMV_EHEADER, QMV_ETIMEOUT, QMV_ERANGE). Test and diagnostics hook. */
+qmv_status qmv_device_status(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

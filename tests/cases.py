@@ -1,0 +1,110 @@
+"""Shared helpers for the GPU parity tests: building inputs on the oracle side
+(host, oracle encoders) and on the device side (seeded generator + the library's
+quantizer), and the normalised error of BASELINE's tolerance.
+
+The error of one output element is |y - y_ref| / sum_k |w_k x_k| (fp64), the bound
+is 1e-5; an element whose denominator is zero must be exactly zero.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+TOL = 1e-5
+
+# NVFP4 tensor scale of synthetic N(0, 0.02) weights: the generator's support is
+# |z| <= 6, so |w| <= 0.12 and s_T = 0.12 / (448 * 6) is a static per-tensor constant
+NVFP4_WEIGHT_AMAX = np.float32(0.12)
+NVFP4_TS = float(NVFP4_WEIGHT_AMAX / np.float32(2688.0))
+
+
+def tensor_scale(fmt) -> float:
+    return NVFP4_TS if fmt == "nvfp4" else 0.0
+
+
+def norm_err(y, ref, den) -> float:
+    y = np.asarray(y, dtype=np.float64)
+    zero = den == 0
+    if np.any(zero):
+        assert np.all(y[zero] == 0.0)
+    d = np.where(zero, 1.0, den)
+    e = np.abs(y - ref) / d
+    e[zero] = 0.0
+    return float(e.max()) if e.size else 0.0
+
+
+def host_matrix(fmt, seed, N, K, E=1):
+    """fp32 W[E*N, K] (host, synth) and its canonical bytes (oracle encoder).
+
+    Formats whose canonical stream is per matrix (NVFP4, FP8_ROW) are encoded one
+    expert at a time and concatenated."""
+    W = synth.weights(seed, E * N, K).numpy()
+    if fmt in ("nvfp4", "fp8_row"):
+        canon = np.concatenate([oracle.encode(fmt, W[e * N:(e + 1) * N], tensor_scale(fmt))
+                                for e in range(E)])
+    else:
+        canon = oracle.encode(fmt, W, tensor_scale(fmt))
+    return W, canon
+
+
+def host_dequant(fmt, canon, N, K, E=1):
+    if fmt in ("nvfp4", "fp8_row"):
+        per = oracle.canon_bytes(fmt, N, K)
+        return np.concatenate([oracle.block_to_float(fmt, canon[e * per:(e + 1) * per], N, K)
+                               for e in range(E)])
+    return oracle.block_to_float(fmt, canon, E * N, K)
+
+
+def host_rows_dequant(fmt, seed, rows, N, K):
+    """Oracle-side BlockToFloat of selected tower rows, regenerated from the seed
+    (row = e*N + n). NVFP4 uses the static tensor scale; FP8 row scales are per row,
+    so each row is a one-row matrix."""
+    W = synth.weights_rows(seed, rows, K).numpy()
+    if fmt in ("nvfp4", "fp8_row"):
+        out = np.empty_like(W)
+        for i in range(W.shape[0]):
+            c = oracle.encode(fmt, W[i:i + 1], tensor_scale(fmt))
+            out[i] = oracle.block_to_float(fmt, c, 1, K)[0]
+        return out
+    c = oracle.encode(fmt, W, tensor_scale(fmt))
+    return oracle.block_to_float(fmt, c, W.shape[0], K)
+
+
+def device_matrix(q, fmt, seed, N, K, E=1, dev="cuda"):
+    """Packed device tower generated on the device: synth (torch CUDA) -> the library
+    quantizer -> qmv_pack. Returns the packed buffer."""
+    chunk_rows = max(1, (1 << 26) // K)
+    canon_parts = []
+    for e in range(E):
+        parts = []
+        for r0 in range(0, N, chunk_rows):
+            n = min(chunk_rows, N - r0)
+            W = synth.weights(seed, n, K, device=dev, row0=e * N + r0)
+            if fmt in ("nvfp4", "fp8_row"):
+                parts.append(W)
+            else:
+                parts.append(q.qmv_quantize(fmt, W))
+        if fmt in ("nvfp4", "fp8_row"):
+            # per-matrix stream: quantize the whole expert matrix at once
+            Wm = torch.cat(parts)
+            canon_parts.append(q.qmv_quantize(fmt, Wm, tensor_scale(fmt)))
+            del Wm
+        else:
+            canon_parts.append(torch.cat(parts))
+        del parts
+    canon = torch.cat(canon_parts)
+    del canon_parts
+    packed = q.qmv_pack(fmt, canon, N, K, E)
+    del canon
+    return packed
+
+
+def sample_rows(N, count, seed=0):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 2, N - 1]
+    extra = rng.choice(N, size=min(count, N), replace=False).tolist()
+    rows = sorted(set([r for r in fixed + extra if 0 <= r < N]))
+    return np.array(rows, dtype=np.int64)

@@ -1,0 +1,78 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry point the
+header declares, and its host-side validation answers without touching a device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmv.h")
+LIB = os.path.join(ROOT, "block_quantized_weight_fly_gb300", "libqmv.so")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmv_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        import importlib.util
+        spec = importlib.util.spec_from_file_location(
+            "qmv_build", os.path.join(ROOT, "block_quantized_weight_fly_gb300", "build.py"))
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        mod.build()
+    return ctypes.CDLL(LIB)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert "qmv_gemv" in names and "qmv_grouped" in names and "qmv_pack" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_exposes_every_declared_symbol(lib):
+    import block_quantized_weight_fly_gb300 as q
+    for n in _declared():
+        assert n in q.EXPORTED and callable(getattr(q, n)), n
+
+
+def test_sizes_match_oracle(lib):
+    import block_quantized_weight_fly_gb300 as q
+    for fmt in ("q8_0", "q4_k", "q6_k", "nvfp4", "fp8_row"):
+        for N, K in ((512, 1024), (17408, 5120), (248320, 5120), (300, 768)):
+            assert q.qmv_canon_size(fmt, N, K) == oracle.canon_bytes(fmt, N, K)
+    # the packed layout moves the canonical bytes; only row/K padding and alignment add
+    for fmt, per in (("q8_0", 34 / 32), ("q4_k", 144 / 256), ("q6_k", 210 / 256),
+                     ("nvfp4", 18 / 32), ("fp8_row", 1.0)):
+        N, K = 17408, 5120
+        body = q.qmv_pack_size(fmt, N, K) - 256
+        assert N * K * per <= body <= N * K * per + 4 * N + 512
+    assert q.qmv_pack_size("q4_k", 100, 100) == 0          # K not a multiple of 256
+    assert q.qmv_pack_size("q8_0", 100, 48) == 0           # K not a multiple of 32
+
+
+def test_host_validation_without_device(lib):
+    import block_quantized_weight_fly_gb300 as q
+    P = ctypes.c_void_p
+    gemv = q._gemv
+    one = P(256)
+    # null pointers, M out of range, bad format, misalignment: refused before any launch
+    assert gemv(2, None, one, one, 1, 128, 256, one, 1 << 20, None) == 1
+    assert gemv(2, one, one, one, 0, 128, 256, one, 1 << 20, None) == 1
+    assert gemv(2, one, one, one, 9, 128, 256, one, 1 << 20, None) == 1
+    assert gemv(9, one, one, one, 1, 128, 256, one, 1 << 20, None) == 1
+    assert gemv(2, one, one, one, 1, 128, 100, one, 1 << 20, None) == 3
+    assert gemv(2, P(257), one, one, 1, 128, 256, one, 1 << 20, None) == 2
+    assert gemv(2, one, P(258), one, 1, 128, 256, one, 1 << 20, None) == 2
+    assert q._grouped(2, one, one, one, 2, one, 1, 1, 128, 256, 4, one, 1 << 20, None) == 1
+    assert q._grouped(2, one, one, one, 0, one, 1, 9, 128, 256, 4, one, 1 << 20, None) == 1
+    assert q.qmv_status_str(0) == "ok" and "workspace" in q.qmv_status_str(8)
