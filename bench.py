@@ -1,0 +1,549 @@
+#!/usr/bin/env python
+"""Benchmark of the block-quantized decode GEMV on GB300.
+
+Metric: effective weight-stream GB/s (and the fraction of HBM peak) of the M = 1
+quantized GEMV. Effective GB/s = algorithmic bytes / time, where the algorithmic
+bytes of a call are the canonical packed bytes of the weight rows it needs plus
+the bytes of x and y (and the expert ids of a grouped call); GB = 1e9 B.
+
+Default workload (one "step"): the Q4_K decode MLP at Qwen3.8-27B geometry, M = 1:
+gate and up W[17408, 5120] and down W[5120, 17408], three GEMV calls. Other
+configurations are selectable with --workload and print their own line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Inputs are seeded and synthetic (weights N(0, 0.02) quantized by the library's
+quantizer, bf16 activations N(0, 1)). Every step reads its weights from HBM: the
+packed weights are rotated over enough copies that the bytes between two uses of
+one copy exceed 4x the L2 cache. Steps are captured in CUDA graphs (the library's
+kernels only; several steps per graph when a step is small) and exactly K steps
+are timed with CUDA events between a barrier and a synchronize on both sides. With N > 1 (torchrun) every rank runs the same
+workload on its own GPU (replicas: the GEMV has no data-path exchange) and the
+maximum time over ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+NVFP4_TS = float(np.float32(0.12) / np.float32(2688.0))   # static per-tensor scale (generator bound)
+L2_BYTES = 129 * 10**6
+
+QWEN_HIDDEN, QWEN_MLP, QWEN_VOCAB = 5120, 17408, 248320
+
+WORKLOADS = {
+    "q4k_mlp_m1": dict(fmt="q4_k", M=1, mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
+                                              ("down", QWEN_HIDDEN, QWEN_MLP)],
+                       desc="Q4_K decode MLP, Qwen3.8-27B geometry: gate+up [17408,5120], down [5120,17408], M=1"),
+    "q4k_mlp_m8": dict(fmt="q4_k", M=8, mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
+                                              ("down", QWEN_HIDDEN, QWEN_MLP)],
+                       desc="Q4_K decode MLP, Qwen3.8-27B geometry, M=8 (speculative verify block)"),
+    "q6k_head_m1": dict(fmt="q6_k", M=1, mats=[("head", QWEN_VOCAB, QWEN_HIDDEN)],
+                        desc="Q6_K untied output head [248320,5120], M=1"),
+    "q6k_head_m8": dict(fmt="q6_k", M=8, mats=[("head", QWEN_VOCAB, QWEN_HIDDEN)],
+                        desc="Q6_K untied output head [248320,5120], M=8"),
+    "q6k_qkv_m1": dict(fmt="q6_k", M=1, mats=[("attn_qkv", 10240, QWEN_HIDDEN)],
+                       desc="Q6_K fused attn_qkv [10240,5120], M=1"),
+    "q6k_qkv_m8": dict(fmt="q6_k", M=8, mats=[("attn_qkv", 10240, QWEN_HIDDEN)],
+                       desc="Q6_K fused attn_qkv [10240,5120], M=8"),
+    "nvfp4_mlp_m1": dict(fmt="nvfp4", M=1, mats=[("up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
+                         desc="NVFP4 MLP [17408,5120] + [5120,17408], M=1"),
+    "nvfp4_mlp_m8": dict(fmt="nvfp4", M=8, mats=[("up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
+                         desc="NVFP4 MLP [17408,5120] + [5120,17408], M=8"),
+    "fp8_m1": dict(fmt="fp8_row", M=1, mats=[("proj", 6144, QWEN_HIDDEN)],
+                   desc="row-scaled FP8 projection [6144,5120], M=1"),
+    "fp8_m8": dict(fmt="fp8_row", M=8, mats=[("proj", 6144, QWEN_HIDDEN)],
+                   desc="row-scaled FP8 projection [6144,5120], M=8"),
+    "q8_0_tiny": dict(fmt="q8_0", M=1, mats=[("tiny", 512, 1024)],
+                      desc="Q8_0 tiny [512,1024], M=1"),
+    "tower_m1": dict(fmt="q4_k", M=1, tower=True, E=288, topk=8,
+                     mats=[("gate", 2048, 4096), ("up", 2048, 4096), ("down", 4096, 2048)],
+                     desc="grouped Q4_K tower, 288 experts x (gate,up [2048,4096], down [4096,2048]), top-8, M=1"),
+    "tower_m4": dict(fmt="q4_k", M=4, tower=True, E=288, topk=8,
+                     mats=[("gate", 2048, 4096), ("up", 2048, 4096), ("down", 4096, 2048)],
+                     desc="grouped Q4_K tower, 288 experts, top-8, M=4"),
+    "tower_m8": dict(fmt="q4_k", M=8, tower=True, E=288, topk=8,
+                     mats=[("gate", 2048, 4096), ("up", 2048, 4096), ("down", 4096, 2048)],
+                     desc="grouped Q4_K tower, 288 experts, top-8, M=8"),
+}
+DEFAULT_WORKLOAD = "q4k_mlp_m1"
+DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, "q6k_head_m8": 2000,
+                 "q6k_qkv_m1": 40000, "q6k_qkv_m8": 40000, "nvfp4_mlp_m1": 20000, "nvfp4_mlp_m8": 20000,
+                 "fp8_m1": 40000, "fp8_m8": 40000, "q8_0_tiny": 20000, "tower_m1": 20000,
+                 "tower_m4": 10000, "tower_m8": 5000}
+
+METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"
+CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q6_k": 210 / 256, "nvfp4": 18 / 32, "fp8_row": 1.0}
+
+
+def canon_bytes(fmt, N, K):
+    if fmt == "nvfp4":
+        return N * K // 2 + N * K // 16 + 4
+    if fmt == "fp8_row":
+        return N * K + 4 * N
+    return int(round(N * K * CANON_PER_VALUE[fmt]))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("block_quantized_weight_fly_gb300/csrc/qmv_stream.cu",
+                "block_quantized_weight_fly_gb300/csrc/qmv_layout.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(workload)
+    if not rec or rec.get("kernel_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        for line in (self.out or "").strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax = float(p[2])
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                               p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# device workload
+# ----------------------------------------------------------------------------
+def build_packed(q, fmt, seed, N, K, E, dev):
+    """Seeded weights -> library quantizer -> packed device tower (load phase, untimed)."""
+    chunk_rows = max(1, (1 << 26) // K)
+    canon_parts = []
+    for e in range(E):
+        if fmt in ("nvfp4", "fp8_row"):
+            W = synth.weights(seed, N, K, device=dev, row0=e * N, chunk_rows=chunk_rows)
+            canon_parts.append(q.qmv_quantize(fmt, W, NVFP4_TS if fmt == "nvfp4" else 0.0))
+            del W
+        else:
+            for r0 in range(0, N, chunk_rows):
+                n = min(chunk_rows, N - r0)
+                W = synth.weights(seed, n, K, device=dev, row0=e * N + r0, chunk_rows=n)
+                canon_parts.append(q.qmv_quantize(fmt, W))
+                del W
+    canon = torch.cat(canon_parts)
+    del canon_parts
+    packed = q.qmv_pack(fmt, canon, N, K, E)
+    del canon
+    return packed
+
+
+class DeviceWorkload:
+    def __init__(self, q, name, dev):
+        self.q, self.name, self.dev = q, name, dev
+        w = WORKLOADS[name]
+        self.fmt, self.M = w["fmt"], w["M"]
+        self.tower = w.get("tower", False)
+        self.E = w.get("E", 1)
+        self.topk = w.get("topk", 1)
+        self.mats = w["mats"]
+        torch.cuda.synchronize()
+        base = [build_packed(q, self.fmt, 100 + i, N, K, self.E, dev) for i, (_, N, K) in enumerate(self.mats)]
+        torch.cuda.synchronize()
+        # bytes a step streams, to size the rotation
+        if self.tower:
+            per_expert = [canon_bytes(self.fmt, N, K) for _, N, K in self.mats]
+            step_w = sum(per_expert) * min(self.E, self.M * self.topk)
+        else:
+            step_w = sum(canon_bytes(self.fmt, N, K) for _, N, K in self.mats)
+        self.copies = max(2, math.ceil(4 * L2_BYTES / max(step_w, 1)) + 1)
+        self.packed = [base] + [[b.clone() for b in base] for _ in range(self.copies - 1)]
+        # activations, outputs, workspaces
+        self.x, self.y, self.ws = [], [], []
+        for i, (_, N, K) in enumerate(self.mats):
+            rows = self.M * self.topk if (self.tower and i == len(self.mats) - 1) else self.M
+            self.x.append(synth.activations(200 + i, rows, K, device=dev))
+            ysh = (self.M, self.topk, N) if self.tower else (self.M, N)
+            self.y.append(torch.empty(ysh, dtype=torch.float32, device=dev))
+            entry = q.QMV_ENTRY_GROUPED if self.tower else q.QMV_ENTRY_GEMV
+            self.ws.append(q.workspace(entry, self.fmt, self.M, N, K, self.E, self.topk, device=dev))
+        # routing: a different id set every step (cycled), like consecutive decode steps
+        self.ids = []
+        self.unique = []
+        if self.tower:
+            for s in range(64):
+                ids = synth.expert_ids(1000 + s, self.M, self.topk, self.E)
+                self.ids.append(torch.from_numpy(ids).to(dev))
+                self.unique.append(len(np.unique(ids)))
+        self.launches_per_step = len(self.mats)
+
+    def step_bytes(self, s=0):
+        """algorithmic bytes of step s (weights of the rows needed + x + y (+ ids))."""
+        tot = 0
+        for i, (_, N, K) in enumerate(self.mats):
+            xb = self.x[i].numel() * 2
+            yb = self.y[i].numel() * 4
+            if self.tower:
+                u = self.unique[s % len(self.unique)]
+                tot += u * canon_bytes(self.fmt, N, K) + xb + yb + self.M * self.topk * 4
+            else:
+                tot += canon_bytes(self.fmt, N, K) + xb + yb
+        return tot
+
+    def launch_step(self, s):
+        q = self.q
+        c = s % self.copies
+        for i, (_, N, K) in enumerate(self.mats):
+            if self.tower:
+                q.qmv_grouped(self.fmt, self.packed[c][i], self.ids[s % len(self.ids)], self.x[i], N, K, self.E,
+                              self.ws[i], x_per_pair=(i == len(self.mats) - 1), y=self.y[i])
+            else:
+                q.qmv_gemv(self.fmt, self.packed[c][i], self.x[i], N, K, self.ws[i], y=self.y[i])
+
+    def steps_per_graph(self):
+        """Steps captured per CUDA graph: one for big steps, more for small ones so
+        that replaying graphs is not host-bound (about 200 MB of weights per graph)."""
+        return max(1, min(256, int(200e6 // max(self.step_bytes(0), 1))))
+
+    def graphs(self, K):
+        """CUDA graphs of `u` consecutive steps each (copy index = step % copies,
+        routing index = step % 64), and one graph of the K % u remaining steps."""
+        u = self.steps_per_graph()
+        period = self.copies if not self.tower else math.lcm(self.copies, len(self.ids))
+        period = min(period, 256)
+        ngraphs = max(1, -(-period // u))
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(min(period, 64)):
+                self.launch_step(i)       # warm (kernel attributes, module load)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        gs = []
+        for k in range(ngraphs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for j in range(u):
+                    self.launch_step(k * u + j)
+            gs.append(g)
+        rem = None
+        if K % u:
+            rem = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(rem):
+                for j in range(K % u):
+                    self.launch_step(ngraphs * u + j)
+        torch.cuda.synchronize()
+        return gs, rem, u
+
+
+def run_device(args, rank, world, dev):
+    import block_quantized_weight_fly_gb300 as q
+    wl = DeviceWorkload(q, args.workload, dev)
+    K, W = args.steps, args.warmup
+    graphs, rem_graph, u = wl.graphs(K)
+    period = len(graphs)
+    for i in range(max(1, -(-W // u))):
+        graphs[i % period].replay()
+    torch.cuda.synchronize()
+    if q.qmv_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        start.record()
+        for i in range(K // u):
+            graphs[(W + i) % period].replay()
+        if rem_graph is not None:
+            rem_graph.replay()
+        end.record()
+        end.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = start.elapsed_time(end)
+    status = q.qmv_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    step_bytes = [wl.step_bytes(W + i) for i in range(min(K, period))]
+    bytes_per_step = sum(step_bytes) / len(step_bytes)
+    total_bytes = bytes_per_step * K * world
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+    launches = K * wl.launches_per_step
+    avg_launch_s = (ms * 1e-3) / launches
+    achieved = (bytes_per_step / wl.launches_per_step) / avg_launch_s / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = recorded_traffic(args.workload)
+
+    # ---- end to end through the public API, host buffers -------------------
+    e2e_steps = min(K, 2000)
+    hx = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in wl.x]
+    for h, x in zip(hx, wl.x):
+        h.copy_(x.cpu())
+    hy = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in wl.y]
+    h2d = sum(h.numel() * h.element_size() for h in hx)
+    d2h = sum(h.numel() * h.element_size() for h in hy)
+    stream = torch.cuda.current_stream()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e_start.record()
+    for i in range(e2e_steps):
+        for h, x in zip(hx, wl.x):
+            x.copy_(h, non_blocking=True)
+        wl.launch_step(W + i)
+        for h, y in zip(hy, wl.y):
+            h.copy_(y, non_blocking=True)
+        stream.synchronize()
+    e_end.record()
+    e_end.synchronize()
+    e2e_ms = e_start.elapsed_time(e_end)
+    e2e_bytes = sum(wl.step_bytes(W + i) for i in range(e2e_steps))
+    e2e_value = e2e_bytes * world / (e2e_ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_max / K, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,0.02) weights quantized by the library, bf16 N(0,1) activations)",
+        "config": {
+            "workload": WORKLOADS[args.workload]["desc"],
+            "workload_id": args.workload,
+            "weights": wl.fmt,
+            "M": wl.M,
+            "matrices": [f"{n}[{N},{K}]" + (f"x{wl.E}" if wl.tower else "") for n, N, K in wl.mats],
+            "bytes_per_step": int(bytes_per_step),
+            "l2": f"inputs larger than L2: weights rotated over {wl.copies} copies "
+                  f"({wl.copies} x {int(bytes_per_step / 1e6)} MB per cycle)",
+            "graph": f"CUDA graphs of {u} step(s) each",
+            "parallelism": "replicas" if world > 1 else "single-gpu",
+        },
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "pct_of_nominal_8000": round(100.0 * value / world / 8000.0, 2),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": f"qmv::stream_kernel<{wl.fmt}, M={wl.M}>" + (" (grouped)" if wl.tower else ""),
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "avg_launch_us": round(avg_launch_s * 1e6, 3),
+            "algorithmic_bytes_per_launch": int(bytes_per_step / wl.launches_per_step),
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+                "ms_per_step": round(e2e_ms / e2e_steps, 6)},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if wl.tower:
+        result["config"]["unique_experts_mean"] = round(float(np.mean(wl.unique)), 2)
+    return result
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle
+# ----------------------------------------------------------------------------
+def oracle_sample(workload, rows_per_mat):
+    """Canonical bytes of the first rows of each matrix of the workload (oracle
+    encoder), x rows, and the canonical bytes they hold. Untimed preparation."""
+    import oracle
+    w = WORKLOADS[workload]
+    fmt = w["fmt"]
+    items = []
+    for i, (_, N, K) in enumerate(w["mats"]):
+        r = min(rows_per_mat[i], N)
+        W = synth.weights_rows(100 + i, np.arange(r), K).numpy()
+        canon = oracle.encode(fmt, W, NVFP4_TS if fmt == "nvfp4" else 0.0)
+        x = synth.bf16_bits(synth.activations(200 + i, w["M"], K))
+        items.append((fmt, canon, r, K, x))
+    return items
+
+
+def time_oracle(items, min_seconds):
+    import oracle
+    done_bytes, reps = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        for fmt, canon, r, K, x in items:
+            D = oracle.block_to_float(fmt, canon, r, K)
+            oracle.gemv_f64(D, x)
+            done_bytes += canon.size + x.size * 2 + r * x.shape[0] * 4
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    return done_bytes, time.perf_counter() - t0, reps
+
+
+def cpu_baseline(workload, seconds=10.0):
+    w = WORKLOADS[workload]
+    # about the same canonical bytes from each matrix (~4.4 MB each for the MLP)
+    rows = [max(1, int(4.4e6 / canon_bytes(w["fmt"], 1, K))) for _, _, K in w["mats"]]
+    items = oracle_sample(workload, rows)
+    nbytes, secs, reps = time_oracle(items, seconds)
+    sample = ", ".join(f"{n}: first {r} rows" for (n, _, _), r in zip(w["mats"], rows))
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{sample} (BlockToFloat + fp64 dot, {reps} passes, {secs:.1f} s)"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle as it stands, one bounded sample per step."""
+    w = WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    budget = 150.0                                 # seconds for the whole run
+    probe = oracle_sample(args.workload, [16] * len(w["mats"]))
+    nb, secs, _ = time_oracle(probe, 0.0)
+    per_row_s = secs / (16 * len(w["mats"]))
+    rows = max(1, int(budget / max(K + W, 1) / max(per_row_s * len(w["mats"]), 1e-9)))
+    items = oracle_sample(args.workload, [rows] * len(w["mats"]))
+    import oracle
+    for _ in range(W):
+        for fmt, canon, r, K_, x in items:
+            oracle.gemv_f64(oracle.block_to_float(fmt, canon, r, K_), x)
+    nbytes = 0
+    t0 = time.perf_counter()
+    for _ in range(K):
+        for fmt, canon, r, K_, x in items:
+            oracle.gemv_f64(oracle.block_to_float(fmt, canon, r, K_), x)
+            nbytes += canon.size + x.size * 2 + r * x.shape[0] * 4
+    secs = time.perf_counter() - t0
+    value = nbytes / secs / 1e9
+    sample = f"first {rows} rows of each of {', '.join(n for n, _, _ in w['mats'])} per step"
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": K, "warmup": W,
+        "ms_per_step": round(secs * 1e3 / max(K, 1), 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w["desc"], "workload_id": args.workload, "weights": w["fmt"], "M": w["M"]},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload]
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and world > 1:
+        args.gpus = world
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    try:
+        result = run_device(args, rank, world, dev)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(args.workload)
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -15,10 +15,30 @@
 //
 // so the bytes of (any row range) x (one k-group) are one contiguous span per
 // plane: one bulk copy moves a 128-row x 256-value slab into shared memory. The
-// bytes are the canonical bytes, regrouped; the bytes streamed per value equal
-// the canonical block size. Records of 144, 208 and 272 bytes are odd multiples
-// of 16, so 8 consecutive rows read at the same offset hit 8 different 16-byte
-// bank groups; the 256-byte FP8 record gets the same property from its rotation.
+// bytes are the canonical bytes, regrouped (and, inside some 32-bit words, their
+// nibbles permuted -- see below); the bytes streamed per value equal the
+// canonical block size.
+//
+// Nibble order inside 32-bit quant words. The kernels turn two 4-bit fields into
+// two exact bf16 values with one AND-OR against the bf16 pattern of 128.0:
+// ((word >> 4p) & 0x000F000F) | 0x43004300 = {128 + field(p), 128 + field(p+4)}.
+// So each word stores the fields of consecutive element pairs at nibbles (p, p+4):
+//   Q4_K : word w of a 32-value chunk = elements 8w..8w+7; element 8w+2p -> nibble p,
+//          element 8w+2p+1 -> nibble p+4                              (p = 0..3)
+//   Q8_0 : byte u = q XOR 0x80 (0..255, the code plus 128); word w = elements 4w..4w+3:
+//          low nibbles of elements (4w, 4w+1) -> nibbles (0, 4), of (4w+2, 4w+3) ->
+//          (1, 5); high nibbles of (4w, 4w+1) -> (2, 6), of (4w+2, 4w+3) -> (3, 7)
+//   Q6_K : ql word w of a chunk = low nibbles of elements {4w..4w+3, 16+4w..16+4w+3}
+//          as pairs (4w,4w+1) -> (0,4), (4w+2,4w+3) -> (1,5), (16+4w,..) -> (2,6),
+//          (16+4w+2,..) -> (3,7); qh word h (h = 0, 1) of a chunk: for element pairs of
+//          quad w = 2h + s (s = 0, 1), pair k's 2-bit highs sit at bits
+//          8s + 2k, 8s + 2k + 16 (k indexes the same four pairs as the ql word)
+// NVFP4 and FP8 codes keep their canonical order (element 2i in the low nibble or
+// byte), which the hardware FP4/FP8 -> f16x2 conversions consume directly.
+//
+// Records of 144, 208 and 272 bytes are odd multiples of 16, so 8 consecutive rows
+// read at the same offset hit 8 different 16-byte bank groups; the 256-byte FP8
+// record gets the same property from its rotation.
 //
 // This regrouping is the planar-repack idea ("A 320B MoE on a free Kaggle TPU",
 // "The 110 GB claim, checked against the tensor index": blocks split into dense
@@ -42,7 +62,7 @@ constexpr int kChunk = 32;           // values per lane chunk
 constexpr int kChunksPerSlab = 8;
 constexpr int kHeaderBytes = 256;
 constexpr uint32_t kMagic = 0x31564D51u;  // "QMV1"
-constexpr uint32_t kVersion = 2;
+constexpr uint32_t kVersion = 4;
 
 enum Fmt { F_Q8_0 = 1, F_Q4_K = 2, F_Q6_K = 3, F_NVFP4 = 4, F_FP8 = 5 };
 
@@ -119,15 +139,17 @@ __host__ __device__ inline int64_t canon_matrix_bytes(int fmt, int64_t N, int64_
 }
 
 // ---- record-internal offsets --------------------------------------------------
-// Q8_0: d of chunk c at 2c; 16-byte vector h (0,1) of chunk c at 16 + 32c + 16h
-__host__ __device__ inline int q80_q_off(int c, int h) { return 16 + 32 * c + 16 * h; }
-// Q4_K: header at 0, 16 nibble bytes of chunk c at 16 + 16c
-__host__ __device__ inline int q4k_q_off(int c) { return 16 + 16 * c; }
-// NVFP4: scales at 0 (byte b = block b of 16 values), codes of chunk c at 16 + 16c
-__host__ __device__ inline int nv_q_off(int c) { return 16 + 16 * c; }
-// Q6_K: ql of chunk c at 16c, qh of chunk c at 128 + 8c, scales at 192
-__host__ __device__ inline int q6k_ql_off(int c) { return 16 * c; }
-__host__ __device__ inline int q6k_qh_off(int c) { return 128 + 8 * c; }
+// Quant words are stored thread-major: the consumer thread t (t = 0..3) of an mma
+// quad reads, for every 32-value chunk j of the k-group, the same 4 (or 8) bytes;
+// those bytes of all 8 chunks are contiguous, so one or two 128-bit loads fetch them.
+//   Q4_K / NVFP4: word t of chunk j (its elements 8t..8t+7) at 16 + 32t + 4j
+//   Q8_0        : words 2t, 2t+1 of chunk j (elements 8t..8t+7) at 16 + 64t + 8j
+//   Q6_K        : ql word t of chunk j at 32t + 4j; qh word h of chunk j at 128 + 32h + 4j
+__host__ __device__ inline int q4k_word_off(int t, int j) { return 16 + 32 * t + 4 * j; }
+__host__ __device__ inline int nv_word_off(int t, int j) { return 16 + 32 * t + 4 * j; }
+__host__ __device__ inline int q80_word_off(int t, int j) { return 16 + 64 * t + 8 * j; }
+__host__ __device__ inline int q6k_ql_word_off(int t, int j) { return 32 * t + 4 * j; }
+__host__ __device__ inline int q6k_qh_word_off(int h, int j) { return 128 + 32 * h + 4 * j; }
 // FP8: 16-byte vector v (0..15) of row r sits at 16 * (v ^ (r & 7))
 __host__ __device__ inline int fp8_v_off(int v, int r) { return 16 * (v ^ (r & 7)); }
 
@@ -160,6 +182,52 @@ __device__ __forceinline__ uint32_t q4k_field(uint32_t s1, uint32_t s2, uint32_t
   const uint64_t src = (bit < 32) ? lo : hi;
   const int sh = (bit < 32) ? bit : bit - 32;
   return (uint32_t)(src >> sh) & 63u;
+}
+
+// ---- nibble permutations of the packed words (see the comment at the top) ---
+// canonical nibble n (element 8w+n of a Q4_K word) -> packed nibble position
+__host__ __device__ inline int q4k_pos(int n) { return (n & 1) ? (n >> 1) + 4 : (n >> 1); }
+__host__ __device__ inline uint32_t q4k_permute(uint32_t w) {
+  uint32_t o = 0;
+  for (int n = 0; n < 8; ++n) o |= ((w >> (4 * n)) & 15u) << (4 * q4k_pos(n));
+  return o;
+}
+__host__ __device__ inline uint32_t q4k_unpermute(uint32_t w) {
+  uint32_t o = 0;
+  for (int n = 0; n < 8; ++n) o |= ((w >> (4 * q4k_pos(n))) & 15u) << (4 * n);
+  return o;
+}
+// Q8_0 word of 4 signed codes (byte i = element 4w+i) -> packed word
+__host__ __device__ inline uint32_t q80_permute(uint32_t w) {
+  uint32_t u = w ^ 0x80808080u, o = 0;
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = (u >> (8 * i)) & 15u, hi = (u >> (8 * i + 4)) & 15u;
+    const int pl = (i >> 1) + 4 * (i & 1);        // low nibbles: pairs (0,4), (1,5)
+    const int ph = 2 + (i >> 1) + 4 * (i & 1);    // high nibbles: pairs (2,6), (3,7)
+    o |= lo << (4 * pl);
+    o |= hi << (4 * ph);
+  }
+  return o;
+}
+__host__ __device__ inline uint32_t q80_unpermute(uint32_t w) {   // -> canonical signed bytes
+  uint32_t o = 0;
+  for (int i = 0; i < 4; ++i) {
+    const int pl = (i >> 1) + 4 * (i & 1);
+    const int ph = 2 + (i >> 1) + 4 * (i & 1);
+    const uint32_t u = ((w >> (4 * pl)) & 15u) | (((w >> (4 * ph)) & 15u) << 4);
+    o |= (u ^ 0x80u) << (8 * i);
+  }
+  return o;
+}
+// Q6_K: element e (0..31) of a chunk -> (ql word, nibble) and (qh word, bit)
+__host__ __device__ inline void q6k_pos(int e, int* lw, int* ln, int* hw, int* hb) {
+  const int half = e >> 4, r = e & 15;           // sub-block of 16 within the chunk
+  const int w = r >> 2, q = r & 3;               // quad w of the sub-block, element q
+  const int k = 2 * half + (q >> 1);             // pair index within the word (0..3)
+  *lw = w;
+  *ln = (q & 1) ? k + 4 : k;
+  *hw = w >> 1;
+  *hb = 8 * (w & 1) + 2 * k + ((q & 1) ? 16 : 0);
 }
 
 }  // namespace qmv

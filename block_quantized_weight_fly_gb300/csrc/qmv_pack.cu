@@ -16,6 +16,10 @@ namespace qmv {
 __device__ __forceinline__ void copy_bytes(uint8_t* dst, const uint8_t* src, int n) {
   for (int i = 0; i < n; ++i) dst[i] = src[i];
 }
+// little-endian 32-bit load from a byte address of any alignment
+__device__ __forceinline__ uint32_t load_u32(const uint8_t* p) {
+  return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
 
 __device__ __forceinline__ uint8_t* group_plane(const Layout& L, uint8_t* base, int64_t e, int64_t g) {
   return base + kHeaderBytes + e * L.expert_bytes + g * L.group_bytes;
@@ -46,17 +50,30 @@ __global__ void pack_kernel(Layout L, const uint8_t* __restrict__ canon, uint8_t
     case F_Q8_0: {
       const uint8_t* src = canon + (row * chunks + c) * 34;
       copy_bytes(rec + 2 * cl, src, 2);
-      copy_bytes(rec + q80_q_off(cl, 0), src + 2, 32);
+      for (int wd = 0; wd < 8; ++wd)
+        *reinterpret_cast<uint32_t*>(rec + q80_word_off(wd >> 1, cl) + 4 * (wd & 1)) =
+            q80_permute(load_u32(src + 2 + 4 * wd));
     } break;
     case F_Q4_K: {
       const uint8_t* blk = canon + (row * (L.K / 256) + g) * 144;
-      copy_bytes(rec + q4k_q_off(cl), blk + 16 + 16 * cl, 16);
+      for (int wd = 0; wd < 4; ++wd)
+        *reinterpret_cast<uint32_t*>(rec + q4k_word_off(wd, cl)) = q4k_permute(load_u32(blk + 16 + 16 * cl + 4 * wd));
       if (cl == 0) copy_bytes(rec, blk, 16);
     } break;
     case F_Q6_K: {
       const uint8_t* blk = canon + (row * (L.K / 256) + g) * 210;
-      copy_bytes(rec + q6k_ql_off(cl), blk + 16 * cl, 16);
-      copy_bytes(rec + q6k_qh_off(cl), blk + 128 + 8 * cl, 8);
+      uint32_t lw[4] = {0u, 0u, 0u, 0u}, hw[2] = {0u, 0u};
+      for (int e = 0; e < 32; ++e) {
+        const int ce = 32 * cl + e;                       // element within the superblock
+        const uint32_t lo = (blk[ce >> 1] >> (4 * (ce & 1))) & 15u;
+        const uint32_t hi = (blk[128 + (ce >> 2)] >> (2 * (ce & 3))) & 3u;
+        int a, b, c2, d2;
+        q6k_pos(e, &a, &b, &c2, &d2);
+        lw[a] |= lo << (4 * b);
+        hw[c2] |= hi << d2;
+      }
+      for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(rec + q6k_ql_word_off(i, cl)) = lw[i];
+      for (int h = 0; h < 2; ++h) *reinterpret_cast<uint32_t*>(rec + q6k_qh_word_off(h, cl)) = hw[h];
       if (cl == 0) {
         copy_bytes(rec + 192, blk + 192, 16);
         copy_bytes(plane + L.plane_a + 2 * n, blk + 208, 2);
@@ -64,7 +81,8 @@ __global__ void pack_kernel(Layout L, const uint8_t* __restrict__ canon, uint8_t
     } break;
     case F_NVFP4: {
       const uint8_t* ce = canon + e * canon_matrix_bytes(F_NVFP4, L.N, L.K);
-      copy_bytes(rec + nv_q_off(cl), ce + n * (L.K / 2) + c * 16, 16);
+      for (int wd = 0; wd < 4; ++wd)
+        *reinterpret_cast<uint32_t*>(rec + nv_word_off(wd, cl)) = load_u32(ce + n * (L.K / 2) + c * 16 + 4 * wd);
       copy_bytes(rec + 2 * cl, ce + L.N * (L.K / 2) + n * (L.K / 16) + 2 * c, 2);
       if (n == 0 && c == 0) copy_bytes(extras, ce + L.N * (L.K / 2) + L.N * (L.K / 16), 4);
     } break;
@@ -119,39 +137,44 @@ __global__ void dequant_kernel(Layout L, const uint8_t* __restrict__ packed, int
   float* o = out + (row - row0) * L.K + c * kChunk;
   switch (L.fmt) {
     case F_Q8_0: {
-      const int8_t* q = reinterpret_cast<const int8_t*>(rec + q80_q_off(cl, 0));
       float d = h2f(*reinterpret_cast<const uint16_t*>(rec + 2 * cl));
-      for (int i = 0; i < 32; ++i) o[i] = __fmul_rn(d, (float)q[i]);
+      for (int wd = 0; wd < 8; ++wd) {
+        const uint32_t cw = q80_unpermute(
+            *reinterpret_cast<const uint32_t*>(rec + q80_word_off(wd >> 1, cl) + 4 * (wd & 1)));
+        for (int i = 0; i < 4; ++i) o[4 * wd + i] = __fmul_rn(d, (float)(int8_t)((cw >> (8 * i)) & 0xFFu));
+      }
     } break;
     case F_Q4_K: {
-      const uint8_t* q = rec + q4k_q_off(cl);
       const uint32_t* hd = reinterpret_cast<const uint32_t*>(rec);
       float d = h2f(hd[0]), dmin = h2f(hd[0] >> 16);
       uint32_t sc = q4k_field(hd[1], hd[2], hd[3], cl), m = q4k_field(hd[1], hd[2], hd[3], 8 + cl);
       float a = __fmul_rn(d, (float)sc), b = __fmul_rn(dmin, (float)m);
-      for (int i = 0; i < 32; ++i) {
-        uint32_t qq = (q[i >> 1] >> (4 * (i & 1))) & 15u;
-        o[i] = __fsub_rn(__fmul_rn(a, (float)qq), b);
+      for (int wd = 0; wd < 4; ++wd) {
+        const uint32_t cw = q4k_unpermute(*reinterpret_cast<const uint32_t*>(rec + q4k_word_off(wd, cl)));
+        for (int i = 0; i < 8; ++i) o[8 * wd + i] = __fsub_rn(__fmul_rn(a, (float)((cw >> (4 * i)) & 15u)), b);
       }
     } break;
     case F_Q6_K: {
-      const uint8_t* ql = rec + q6k_ql_off(cl);
-      const uint8_t* qh = rec + q6k_qh_off(cl);
+      uint32_t lw[4], hw[2];
+      for (int i = 0; i < 4; ++i) lw[i] = *reinterpret_cast<const uint32_t*>(rec + q6k_ql_word_off(i, cl));
+      for (int h = 0; h < 2; ++h) hw[h] = *reinterpret_cast<const uint32_t*>(rec + q6k_qh_word_off(h, cl));
       const int8_t* sc = reinterpret_cast<const int8_t*>(rec + 192);
       float d = h2f(*reinterpret_cast<const uint16_t*>(plane + L.plane_a + 2 * n));
       for (int i = 0; i < 32; ++i) {
-        int lo = (ql[i >> 1] >> (4 * (i & 1))) & 15;
-        int hi = (qh[i >> 2] >> (2 * (i & 3))) & 3;
-        int qq = lo | (hi << 4);
-        float a = __fmul_rn(d, (float)sc[2 * cl + (i >> 4)]);
-        o[i] = __fmul_rn(a, (float)(qq - 32));
+        int a, b, c2, d2;
+        q6k_pos(i, &a, &b, &c2, &d2);
+        const int lo = (int)((lw[a] >> (4 * b)) & 15u);
+        const int hi = (int)((hw[c2] >> d2) & 3u);
+        const int qq = lo | (hi << 4);
+        const float as = __fmul_rn(d, (float)sc[2 * cl + (i >> 4)]);
+        o[i] = __fmul_rn(as, (float)(qq - 32));
       }
     } break;
     case F_NVFP4: {
-      const uint8_t* cc = rec + nv_q_off(cl);
       const float sT = *reinterpret_cast<const float*>(extras);
       for (int i = 0; i < 32; ++i) {
-        uint32_t code = (cc[i >> 1] >> (4 * (i & 1))) & 15u;
+        const uint32_t cw = *reinterpret_cast<const uint32_t*>(rec + nv_word_off(i >> 3, cl));
+        uint32_t code = (cw >> (4 * (i & 7))) & 15u;
         float p = __fmul_rn(e2m1f(code), e4m3f(rec[2 * cl + (i >> 4)]));
         o[i] = __fmul_rn(p, sT);
       }

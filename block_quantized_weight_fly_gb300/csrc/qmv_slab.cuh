@@ -1,0 +1,554 @@
+// qmv_slab.cuh -- per-format decode + tensor-core inner product of one slab
+// (128 rows x 256 values of packed weights, already in shared memory).
+//
+// A consumer warp w owns rows 16w .. 16w+15 of the slab. The inner product runs
+// on mma.sync m16n8k16 with the weight rows as the 16-row A operand; the weights
+// are decoded in registers straight into A fragments:
+//   K-quants -> bf16:  one AND-OR per two 4-bit fields gives {128 + q_lo, 128 + q_hi}
+//                      exactly (the packed layout stores element pairs at nibbles
+//                      (p, p+4) of each 32-bit word); the +128 offset is removed with
+//                      the per-block min term through X = sum x.
+//   NVFP4, FP8 -> f16: hardware cvt of FP4/FP8 pairs to f16x2 (exact); for NVFP4 the
+//                      E4M3 block scale is multiplied in with one exact f16x2 multiply.
+// Products of these small exact values with the activations are exact and the
+// tensor core accumulates in fp32.
+//
+// The 8 columns of the mma output are used in one of two ways:
+//   M = 1 ("unit columns"): column n holds the partial sum of sub-block (unit) n
+//     of the slab. A thread's B registers carry activations only for its own unit,
+//     zero elsewhere, so one accumulator collects all 8 units' partial sums at once
+//     and each block scale is applied once per slab. A thread (g, t) ends with the
+//     partial sums of rows g, g+8 over units 2t, 2t+1; the four threads of a quad
+//     are added at the end of the row tile.
+//   M = 2..8 ("token columns"): column n is token n; each 32-value sub-block gets
+//     its own accumulator and its scale is applied per sub-block. Thread (g, t)
+//     holds rows g, g+8 x tokens 2t, 2t+1.
+#pragma once
+#include <cstdint>
+#include "qmv_layout.cuh"
+
+namespace qmv {
+
+constexpr int kXStride = 576;          // bytes per token row of a stage's x slice (512 + 64 pad)
+constexpr int kTblStride = 17;         // float2 entries per row of a warp's scale table
+constexpr uint32_t kOnesBf16 = 0x3F803F80u;
+
+// ---------------------------------------------------------------------------
+// helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t lds32(const void* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint2 lds64(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ uint4 lds128v(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+__device__ __forceinline__ void load8(const uint8_t* p, uint32_t* w) {    // 32 bytes, 16-B aligned
+  const uint4 a = lds128v(p), b = lds128v(p + 16);
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+__device__ __forceinline__ void load16(const uint8_t* p, uint32_t* w) {   // 64 bytes, 16-B aligned
+  load8(p, w);
+  load8(p + 32, w + 8);
+}
+// two 4-bit fields at nibbles (p, p+4) -> bf16x2 {128 + lo, 128 + hi}
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int p) {
+  return ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+}
+// two 2-bit fields at bits (2k, 2k + 16) -> bf16x2 {128 + lo, 128 + hi}
+__device__ __forceinline__ uint32_t bit2_pair(uint32_t w, int k) {
+  return ((w >> (2 * k)) & 0x00030003u) | 0x43004300u;
+}
+// FP4 E2M1 pair (one byte) -> f16x2, exact
+__device__ __forceinline__ uint32_t e2m1x2_f16(uint32_t byte) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
+  return r;
+}
+// FP8 E4M3 pair (low 16 bits) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_f16(uint32_t two) {
+  uint32_t r;
+  const unsigned short v = (unsigned short)(two & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// bf16x2 activations -> f16x2 (round to nearest; exact for |x| in fp16's normal range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  uint32_t r;
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// a small non-negative integer (< 2^23) -> exact fp32, without I2F
+__device__ __forceinline__ float u2f_small(uint32_t v) {
+  return __uint_as_float(v | 0x4B000000u) - 8388608.0f;
+}
+__device__ __forceinline__ float i8f(uint32_t byte) {   // signed int8 -> fp32
+  return __uint_as_float(((byte & 0xFFu) ^ 0x80u) | 0x4B000000u) - 8388736.0f;
+}
+// keep v if this thread's unit is the current one, else zero (sparse unit-column B)
+__device__ __forceinline__ uint32_t sel(bool mine, uint32_t v) { return mine ? v : 0u; }
+
+template <int FMT, int MT>
+struct Slab;
+
+// ============================================================================
+// Q4_K. w = a_j q - b_j (a_j = d sc_j, b_j = dmin m_j, sub-block j = 32 values);
+// with A = 128 + q: sum w x = a_j D_j - c_j X_j, c_j = 128 a_j + b_j.
+// ============================================================================
+__device__ __forceinline__ void q4k_pair_scales(const uint4 hd, int t, float* a, float* c) {
+  // sc_j, m_j of sub-blocks j = 2t, 2t+1 (12 consecutive bits each)
+  const float d = h2f(hd.x), dm = h2f(hd.x >> 16);
+  const uint64_t lo = ((uint64_t)hd.z << 32) | hd.y, hi = ((uint64_t)hd.w << 32) | hd.z;
+  const uint32_t s = (uint32_t)(lo >> (12 * t)), m = (uint32_t)(hi >> (16 + 12 * t));
+  a[0] = d * u2f_small(s & 63u);
+  a[1] = d * u2f_small((s >> 6) & 63u);
+  c[0] = fmaf(128.0f, a[0], dm * u2f_small(m & 63u));
+  c[1] = fmaf(128.0f, a[1], dm * u2f_small((m >> 6) & 63u));
+}
+
+template <>
+struct Slab<F_Q4_K, 1> {
+  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int, int w, int lane,
+                             float2*, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* rA = st + (16 * w + g) * 144;
+    const uint8_t* rB = rA + 8 * 144;
+    const uint4 xv = lds128v(xs + 64 * g + 16 * t);          // unit g = chunk g of token 0
+    uint32_t WA[8], WB[8];
+    load8(rA + q4k_word_off(t, 0), WA);
+    load8(rB + q4k_word_off(t, 0), WB);
+    float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t wa = WA[j], wb = WB[j];
+      const bool mine = (g == j);
+      float* d = (j & 1) ? dO : dE;
+      mma_bf16(d, nib_pair(wa, 0), nib_pair(wb, 0), nib_pair(wa, 1), nib_pair(wb, 1), sel(mine, xv.x),
+               sel(mine, xv.y));
+      mma_bf16(d, nib_pair(wa, 2), nib_pair(wb, 2), nib_pair(wa, 3), nib_pair(wb, 3), sel(mine, xv.z),
+               sel(mine, xv.w));
+    }
+    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
+    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+    float aA[2], cA[2], aB[2], cB[2];
+    q4k_pair_scales(lds128v(rA), t, aA, cA);
+    q4k_pair_scales(lds128v(rB), t, aB, cB);
+    acc[0] += fmaf(aA[0], dE[0] + dO[0], fmaf(aA[1], dE[1] + dO[1], -fmaf(cA[0], xx[0], cA[1] * xx[1])));
+    acc[1] += fmaf(aB[0], dE[2] + dO[2], fmaf(aB[1], dE[3] + dO[3], -fmaf(cB[0], xx[2], cB[1] * xx[3])));
+  }
+};
+
+template <>
+struct Slab<F_Q4_K, 8> {
+  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int R, int w, int lane,
+                             float2* tbl, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    {   // scale table of the warp's 16 rows: lane -> (row lane/2, sub-blocks 4h..4h+3)
+      const int rl = lane >> 1, h = lane & 1;
+      const uint4 hd = lds128v(st + (16 * w + rl) * 144);
+      float a[2], c[2];
+      q4k_pair_scales(hd, 2 * h, a, c);
+      tbl[rl * kTblStride + 4 * h + 0] = make_float2(a[0], c[0]);
+      tbl[rl * kTblStride + 4 * h + 1] = make_float2(a[1], c[1]);
+      q4k_pair_scales(hd, 2 * h + 1, a, c);
+      tbl[rl * kTblStride + 4 * h + 2] = make_float2(a[0], c[0]);
+      tbl[rl * kTblStride + 4 * h + 3] = make_float2(a[1], c[1]);
+    }
+    __syncwarp();
+    uint32_t WA[8], WB[8];
+    load8(st + (16 * w + g) * 144 + q4k_word_off(t, 0), WA);
+    load8(st + (16 * w + g + 8) * 144 + q4k_word_off(t, 0), WB);
+    const bool has_x = g < R;
+#pragma unroll
+    for (int j0 = 0; j0 < 8; j0 += 4) {
+      float dd[4][4], xx[4][4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dd[q][e] = xx[q][e] = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = j0 + q;
+        const uint32_t wa = WA[j], wb = WB[j];
+        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
+        mma_bf16(dd[q], nib_pair(wa, 0), nib_pair(wb, 0), nib_pair(wa, 1), nib_pair(wb, 1), xv.x, xv.y);
+        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
+        mma_bf16(dd[q], nib_pair(wa, 2), nib_pair(wb, 2), nib_pair(wa, 3), nib_pair(wb, 3), xv.z, xv.w);
+        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 sA = tbl[g * kTblStride + j0 + q], sB = tbl[(g + 8) * kTblStride + j0 + q];
+        acc[0] = fmaf(sA.x, dd[q][0], fmaf(-sA.y, xx[q][0], acc[0]));
+        acc[1] = fmaf(sA.x, dd[q][1], fmaf(-sA.y, xx[q][1], acc[1]));
+        acc[2] = fmaf(sB.x, dd[q][2], fmaf(-sB.y, xx[q][2], acc[2]));
+        acc[3] = fmaf(sB.x, dd[q][3], fmaf(-sB.y, xx[q][3], acc[3]));
+      }
+    }
+    __syncwarp();
+  }
+};
+
+// ============================================================================
+// Q8_0. q = u - 128 with u = 16 uh + ul; D_lo / D_hi over (128 + ul) / (128 + uh):
+// sum q x = D_lo + 16 D_hi - 2304 X; w = d q (d per 32-value chunk).
+// ============================================================================
+template <>
+struct Slab<F_Q8_0, 1> {
+  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int, int w, int lane,
+                             float2*, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* rA = st + (16 * w + g) * 272;
+    const uint8_t* rB = rA + 8 * 272;
+    const uint4 xv = lds128v(xs + 64 * g + 16 * t);
+    uint32_t WA[16], WB[16];
+    load16(rA + q80_word_off(t, 0), WA);
+    load16(rB + q80_word_off(t, 0), WB);
+    float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint2 wa = make_uint2(WA[2 * j], WA[2 * j + 1]), wb = make_uint2(WB[2 * j], WB[2 * j + 1]);
+      const bool mine = (g == j);
+      const uint32_t b0 = sel(mine, xv.x), b1 = sel(mine, xv.y), b2 = sel(mine, xv.z), b3 = sel(mine, xv.w);
+      mma_bf16(lo, nib_pair(wa.x, 0), nib_pair(wb.x, 0), nib_pair(wa.x, 1), nib_pair(wb.x, 1), b0, b1);
+      mma_bf16(hi, nib_pair(wa.x, 2), nib_pair(wb.x, 2), nib_pair(wa.x, 3), nib_pair(wb.x, 3), b0, b1);
+      mma_bf16(lo, nib_pair(wa.y, 0), nib_pair(wb.y, 0), nib_pair(wa.y, 1), nib_pair(wb.y, 1), b2, b3);
+      mma_bf16(hi, nib_pair(wa.y, 2), nib_pair(wb.y, 2), nib_pair(wa.y, 3), nib_pair(wb.y, 3), b2, b3);
+    }
+    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
+    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+    const uint32_t dA = lds32(rA + 4 * t), dB = lds32(rB + 4 * t);     // d of chunks 2t, 2t+1
+    const float a0 = h2f(dA), a1 = h2f(dA >> 16), b0 = h2f(dB), b1 = h2f(dB >> 16);
+    acc[0] += fmaf(a0, fmaf(16.f, hi[0], lo[0]) - 2304.f * xx[0], a1 * (fmaf(16.f, hi[1], lo[1]) - 2304.f * xx[1]));
+    acc[1] += fmaf(b0, fmaf(16.f, hi[2], lo[2]) - 2304.f * xx[2], b1 * (fmaf(16.f, hi[3], lo[3]) - 2304.f * xx[3]));
+  }
+};
+
+template <>
+struct Slab<F_Q8_0, 8> {
+  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int R, int w, int lane,
+                             float2* tbl, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    {
+      const int rl = lane >> 1, h = lane & 1;
+      const uint2 dv = lds64(st + (16 * w + rl) * 272 + 8 * h);
+      const uint32_t dw[2] = {dv.x, dv.y};
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float d = h2f(dw[jj >> 1] >> (16 * (jj & 1)));
+        tbl[rl * kTblStride + 4 * h + jj] = make_float2(d, 2304.0f * d);
+      }
+    }
+    __syncwarp();
+    uint32_t WA[16], WB[16];
+    load16(st + (16 * w + g) * 272 + q80_word_off(t, 0), WA);
+    load16(st + (16 * w + g + 8) * 272 + q80_word_off(t, 0), WB);
+    const bool has_x = g < R;
+#pragma unroll
+    for (int j0 = 0; j0 < 8; j0 += 2) {
+      float lo[2][4], hi[2][4], xx[2][4];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) lo[q][e] = hi[q][e] = xx[q][e] = 0.f;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int j = j0 + q;
+        const uint2 wa = make_uint2(WA[2 * j], WA[2 * j + 1]), wb = make_uint2(WB[2 * j], WB[2 * j + 1]);
+        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
+        mma_bf16(lo[q], nib_pair(wa.x, 0), nib_pair(wb.x, 0), nib_pair(wa.x, 1), nib_pair(wb.x, 1), xv.x, xv.y);
+        mma_bf16(hi[q], nib_pair(wa.x, 2), nib_pair(wb.x, 2), nib_pair(wa.x, 3), nib_pair(wb.x, 3), xv.x, xv.y);
+        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
+        mma_bf16(lo[q], nib_pair(wa.y, 0), nib_pair(wb.y, 0), nib_pair(wa.y, 1), nib_pair(wb.y, 1), xv.z, xv.w);
+        mma_bf16(hi[q], nib_pair(wa.y, 2), nib_pair(wb.y, 2), nib_pair(wa.y, 3), nib_pair(wb.y, 3), xv.z, xv.w);
+        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float2 sA = tbl[g * kTblStride + j0 + q], sB = tbl[(g + 8) * kTblStride + j0 + q];
+        acc[0] = fmaf(sA.x, fmaf(16.f, hi[q][0], lo[q][0]), fmaf(-sA.y, xx[q][0], acc[0]));
+        acc[1] = fmaf(sA.x, fmaf(16.f, hi[q][1], lo[q][1]), fmaf(-sA.y, xx[q][1], acc[1]));
+        acc[2] = fmaf(sB.x, fmaf(16.f, hi[q][2], lo[q][2]), fmaf(-sB.y, xx[q][2], acc[2]));
+        acc[3] = fmaf(sB.x, fmaf(16.f, hi[q][3], lo[q][3]), fmaf(-sB.y, xx[q][3], acc[3]));
+      }
+    }
+    __syncwarp();
+  }
+};
+
+// ============================================================================
+// Q6_K. q = ql + 16 qh, w = a_u (q - 32), a_u = d sc_u per 16-value sub-block u;
+// sum w x = a_u (D_lo + 16 D_hi - 2208 X). k-step s of chunk j covers sub-block
+// u = 2j + s; the thread's slots hold elements 16s + 4t .. 16s + 4t + 3 of chunk j.
+// ============================================================================
+template <>
+struct Slab<F_Q6_K, 1> {
+  // 16 units (sub-blocks): units 0..7 -> accumulator group 0, 8..15 -> group 1,
+  // column n = u % 8. Thread (g', t) carries activations for units g' and g' + 8.
+  __device__ static void run(const uint8_t* st, const uint8_t* dplane, const uint8_t* xs, int, int w,
+                             int lane, float2*, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    const int rowA = 16 * w + g, rowB = rowA + 8;
+    const uint8_t* rA = st + rowA * 208;
+    const uint8_t* rB = st + rowB * 208;
+    const int hsh = 8 * (t & 1);
+    // unit g' = 2j' + s': chunk j' = g'/2, s' = g' & 1; unit g' + 8: chunk j' + 4
+    const uint2 x0 = lds64(xs + 64 * (g >> 1) + 32 * (g & 1) + 8 * t);
+    const uint2 x1 = lds64(xs + 64 * ((g >> 1) + 4) + 32 * (g & 1) + 8 * t);
+    uint32_t LA[8], LB[8], HA[8], HB[8];
+    load8(rA + q6k_ql_word_off(t, 0), LA);
+    load8(rB + q6k_ql_word_off(t, 0), LB);
+    load8(rA + q6k_qh_word_off(t >> 1, 0), HA);
+    load8(rB + q6k_qh_word_off(t >> 1, 0), HB);
+    float lo[2][4], hi[2][4], xx[2][4];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) lo[q][e] = hi[q][e] = xx[q][e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t la = LA[j], lb = LB[j];
+      const uint32_t ha = HA[j] >> hsh;
+      const uint32_t hb = HB[j] >> hsh;
+      const int grp = j >> 2;
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const int u = 2 * j + s2;
+        const bool mine = ((u & 7) == g);
+        const uint2 xv = grp ? x1 : x0;
+        const uint32_t b0 = sel(mine, xv.x), b1 = sel(mine, xv.y);
+        mma_bf16(lo[grp], nib_pair(la, 2 * s2), nib_pair(lb, 2 * s2), nib_pair(la, 2 * s2 + 1),
+                 nib_pair(lb, 2 * s2 + 1), b0, b1);
+        mma_bf16(hi[grp], bit2_pair(ha, 2 * s2), bit2_pair(hb, 2 * s2), bit2_pair(ha, 2 * s2 + 1),
+                 bit2_pair(hb, 2 * s2 + 1), b0, b1);
+      }
+    }
+    mma_bf16(xx[0], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, x0.x, x0.y);
+    mma_bf16(xx[1], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, x1.x, x1.y);
+    // this thread's columns 2t, 2t+1 -> units {2t, 2t+1} (group 0), {8+2t, 9+2t} (group 1)
+    const float dA = h2f(*reinterpret_cast<const unsigned short*>(dplane + 2 * rowA));
+    const float dB = h2f(*reinterpret_cast<const unsigned short*>(dplane + 2 * rowB));
+    const uint32_t sA0 = *reinterpret_cast<const unsigned short*>(rA + 192 + 2 * t);
+    const uint32_t sA1 = *reinterpret_cast<const unsigned short*>(rA + 200 + 2 * t);
+    const uint32_t sB0 = *reinterpret_cast<const unsigned short*>(rB + 192 + 2 * t);
+    const uint32_t sB1 = *reinterpret_cast<const unsigned short*>(rB + 200 + 2 * t);
+    float vA = 0.f, vB = 0.f;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t scA = q ? sA1 : sA0, scB = q ? sB1 : sB0;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float aa = dA * i8f(scA >> (8 * e)), ab = dB * i8f(scB >> (8 * e));
+        vA = fmaf(aa, fmaf(16.f, hi[q][e], lo[q][e]) - 2208.f * xx[q][e], vA);
+        vB = fmaf(ab, fmaf(16.f, hi[q][2 + e], lo[q][2 + e]) - 2208.f * xx[q][2 + e], vB);
+      }
+    }
+    acc[0] += vA;
+    acc[1] += vB;
+  }
+};
+
+template <>
+struct Slab<F_Q6_K, 8> {
+  __device__ static void run(const uint8_t* st, const uint8_t* dplane, const uint8_t* xs, int R, int w,
+                             int lane, float2* tbl, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    {
+      const int rl = lane >> 1, h = lane & 1;
+      const int row = 16 * w + rl;
+      const float d = h2f(*reinterpret_cast<const unsigned short*>(dplane + 2 * row));
+      const uint2 sv = lds64(st + row * 208 + 192 + 8 * h);
+      const uint32_t sw[2] = {sv.x, sv.y};
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const float a = d * i8f(sw[jj >> 2] >> (8 * (jj & 3)));
+        tbl[rl * kTblStride + 8 * h + jj] = make_float2(a, 2208.0f * a);
+      }
+    }
+    __syncwarp();
+    const uint8_t* rA = st + (16 * w + g) * 208;
+    const uint8_t* rB = rA + 8 * 208;
+    const int hsh = 8 * (t & 1);
+    const bool has_x = g < R;
+    uint32_t LA[8], LB[8], HA[8], HB[8];
+    load8(rA + q6k_ql_word_off(t, 0), LA);
+    load8(rB + q6k_ql_word_off(t, 0), LB);
+    load8(rA + q6k_qh_word_off(t >> 1, 0), HA);
+    load8(rB + q6k_qh_word_off(t >> 1, 0), HB);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t la = LA[j], lb = LB[j];
+      const uint32_t ha = HA[j] >> hsh;
+      const uint32_t hb = HB[j] >> hsh;
+      float lo[2][4], hi[2][4], xx[2][4];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) lo[q][e] = hi[q][e] = xx[q][e] = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const uint2 xv = has_x ? lds64(xs + 64 * j + 32 * s2 + 8 * t) : make_uint2(0u, 0u);
+        mma_bf16(lo[s2], nib_pair(la, 2 * s2), nib_pair(lb, 2 * s2), nib_pair(la, 2 * s2 + 1),
+                 nib_pair(lb, 2 * s2 + 1), xv.x, xv.y);
+        mma_bf16(hi[s2], bit2_pair(ha, 2 * s2), bit2_pair(hb, 2 * s2), bit2_pair(ha, 2 * s2 + 1),
+                 bit2_pair(hb, 2 * s2 + 1), xv.x, xv.y);
+        mma_bf16(xx[s2], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
+      }
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const float2 sA = tbl[g * kTblStride + 2 * j + s2], sB = tbl[(g + 8) * kTblStride + 2 * j + s2];
+        acc[0] = fmaf(sA.x, fmaf(16.f, hi[s2][0], lo[s2][0]), fmaf(-sA.y, xx[s2][0], acc[0]));
+        acc[1] = fmaf(sA.x, fmaf(16.f, hi[s2][1], lo[s2][1]), fmaf(-sA.y, xx[s2][1], acc[1]));
+        acc[2] = fmaf(sB.x, fmaf(16.f, hi[s2][2], lo[s2][2]), fmaf(-sB.y, xx[s2][2], acc[2]));
+        acc[3] = fmaf(sB.x, fmaf(16.f, hi[s2][3], lo[s2][3]), fmaf(-sB.y, xx[s2][3], acc[3]));
+      }
+    }
+    __syncwarp();
+  }
+};
+
+// ============================================================================
+// NVFP4. A = e2m1(c) * s_b in f16 (exact), B = x in f16; s_T in the epilogue.
+// ============================================================================
+__device__ __forceinline__ void nv_frag(uint32_t code_word, uint32_t sbyte, uint32_t* p) {
+  const uint32_t s = e4m3x2_f16(sbyte | (sbyte << 8));
+  p[0] = hmul2(e2m1x2_f16(code_word & 0xFFu), s);
+  p[1] = hmul2(e2m1x2_f16((code_word >> 8) & 0xFFu), s);
+  p[2] = hmul2(e2m1x2_f16((code_word >> 16) & 0xFFu), s);
+  p[3] = hmul2(e2m1x2_f16(code_word >> 24), s);
+}
+
+template <>
+struct Slab<F_NVFP4, 1> {
+  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int, int w, int lane,
+                             float2*, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* rA = st + (16 * w + g) * 144;
+    const uint8_t* rB = rA + 8 * 144;
+    const uint4 xr = lds128v(xs + 64 * g + 16 * t);
+    const uint32_t x0 = bf16x2_to_f16x2(xr.x), x1 = bf16x2_to_f16x2(xr.y);
+    const uint32_t x2 = bf16x2_to_f16x2(xr.z), x3 = bf16x2_to_f16x2(xr.w);
+    uint32_t CA[8], CB[8];
+    load8(rA + nv_word_off(t, 0), CA);
+    load8(rB + nv_word_off(t, 0), CB);
+    float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t pa[4], pb[4];
+      nv_frag(CA[j], rA[2 * j + (t >> 1)], pa);
+      nv_frag(CB[j], rB[2 * j + (t >> 1)], pb);
+      const bool mine = (g == j);
+      float* d = (j & 1) ? dO : dE;
+      mma_f16(d, pa[0], pb[0], pa[1], pb[1], sel(mine, x0), sel(mine, x1));
+      mma_f16(d, pa[2], pb[2], pa[3], pb[3], sel(mine, x2), sel(mine, x3));
+    }
+    acc[0] += (dE[0] + dO[0]) + (dE[1] + dO[1]);
+    acc[1] += (dE[2] + dO[2]) + (dE[3] + dO[3]);
+  }
+};
+
+template <>
+struct Slab<F_NVFP4, 8> {
+  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int R, int w, int lane,
+                             float2*, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* rA = st + (16 * w + g) * 144;
+    const uint8_t* rB = rA + 8 * 144;
+    const bool has_x = g < R;
+    uint32_t CA[8], CB[8];
+    load8(rA + nv_word_off(t, 0), CA);
+    load8(rB + nv_word_off(t, 0), CB);
+    float dO[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t pa[4], pb[4];
+      nv_frag(CA[j], rA[2 * j + (t >> 1)], pa);
+      nv_frag(CB[j], rB[2 * j + (t >> 1)], pb);
+      uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
+      float* d = (j & 1) ? dO : acc;
+      mma_f16(d, pa[0], pb[0], pa[1], pb[1], bf16x2_to_f16x2(xv.x), bf16x2_to_f16x2(xv.y));
+      mma_f16(d, pa[2], pb[2], pa[3], pb[3], bf16x2_to_f16x2(xv.z), bf16x2_to_f16x2(xv.w));
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] += dO[e];
+  }
+};
+
+// ============================================================================
+// FP8 row-scaled. A = e4m3 in f16 (exact), B = x in f16; s_row in the epilogue.
+// The thread's 8 values of chunk j are bytes 8(t&1).. of 16-byte vector 2j + t/2.
+// ============================================================================
+template <>
+struct Slab<F_FP8, 1> {
+  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int, int w, int lane,
+                             float2*, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    const int rowA = 16 * w + g, rowB = rowA + 8;
+    const uint8_t* rA = st + rowA * 256 + 8 * (t & 1);
+    const uint8_t* rB = st + rowB * 256 + 8 * (t & 1);
+    const uint4 xr = lds128v(xs + 64 * g + 16 * t);
+    const uint32_t x0 = bf16x2_to_f16x2(xr.x), x1 = bf16x2_to_f16x2(xr.y);
+    const uint32_t x2 = bf16x2_to_f16x2(xr.z), x3 = bf16x2_to_f16x2(xr.w);
+    float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int v = 2 * j + (t >> 1);
+      const uint2 ca = lds64(rA + fp8_v_off(v, rowA & 7)), cb = lds64(rB + fp8_v_off(v, rowB & 7));
+      const bool mine = (g == j);
+      float* d = (j & 1) ? dO : dE;
+      mma_f16(d, e4m3x2_f16(ca.x), e4m3x2_f16(cb.x), e4m3x2_f16(ca.x >> 16), e4m3x2_f16(cb.x >> 16),
+              sel(mine, x0), sel(mine, x1));
+      mma_f16(d, e4m3x2_f16(ca.y), e4m3x2_f16(cb.y), e4m3x2_f16(ca.y >> 16), e4m3x2_f16(cb.y >> 16),
+              sel(mine, x2), sel(mine, x3));
+    }
+    acc[0] += (dE[0] + dO[0]) + (dE[1] + dO[1]);
+    acc[1] += (dE[2] + dO[2]) + (dE[3] + dO[3]);
+  }
+};
+
+template <>
+struct Slab<F_FP8, 8> {
+  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int R, int w, int lane,
+                             float2*, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    const int rowA = 16 * w + g, rowB = rowA + 8;
+    const uint8_t* rA = st + rowA * 256 + 8 * (t & 1);
+    const uint8_t* rB = st + rowB * 256 + 8 * (t & 1);
+    const bool has_x = g < R;
+    float dO[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int v = 2 * j + (t >> 1);
+      const uint2 ca = lds64(rA + fp8_v_off(v, rowA & 7)), cb = lds64(rB + fp8_v_off(v, rowB & 7));
+      const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
+      float* d = (j & 1) ? dO : acc;
+      mma_f16(d, e4m3x2_f16(ca.x), e4m3x2_f16(cb.x), e4m3x2_f16(ca.x >> 16), e4m3x2_f16(cb.x >> 16),
+              bf16x2_to_f16x2(xv.x), bf16x2_to_f16x2(xv.y));
+      mma_f16(d, e4m3x2_f16(ca.y), e4m3x2_f16(cb.y), e4m3x2_f16(ca.y >> 16), e4m3x2_f16(cb.y >> 16),
+              bf16x2_to_f16x2(xv.z), bf16x2_to_f16x2(xv.w));
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] += dO[e];
+  }
+};
+
+}  // namespace qmv

@@ -30,6 +30,7 @@
 // QMV_ETIMEOUT in the device status word and stops.
 #include <cuda_fp16.h>
 #include "qmv_internal.h"
+#include "qmv_slab.cuh"
 
 namespace qmv {
 
@@ -38,6 +39,7 @@ constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kMaxStages = 16;
 constexpr int kMaxSeg = 64;
 constexpr unsigned long long kTimeoutNs = 1000000000ull;   // 1 s
+constexpr uint32_t kSuspendNs = 2000;    // a waiting thread sleeps up to this long per try (wakes on completion)
 
 struct Seg {
   int expert;
@@ -70,9 +72,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
-      : "r"(smem_u32(b)), "r"(parity)
+      : "r"(smem_u32(b)), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -108,112 +110,6 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
-// per-format chunk dot products: one row, one 32-value chunk, one x row.
-// xf: the 32 x values (fp32, exact bf16). Returns the chunk's contribution.
-// ---------------------------------------------------------------------------
-template <int FMT>
-struct ChunkDot;
-
-template <>
-struct ChunkDot<F_Q4_K> {
-  // w = (d sc) q - dmin m  =>  contribution = (d sc) sum(q x) - (dmin m) sum(x)
-  __device__ static float run(const uint8_t* rec, const uint8_t*, int row, int w, const float* xf,
-                              float xsum) {
-    (void)row;
-    const uint4 hd = lds128(rec);
-    const uint4 q = lds128(rec + q4k_q_off(w));
-    const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
-    const float a = d * (float)q4k_field(hd.y, hd.z, hd.w, w);
-    const float b = dmin * (float)q4k_field(hd.y, hd.z, hd.w, 8 + w);
-    const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-    float s = 0.0f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int v = 0; v < 8; ++v) s = fmaf((float)((qw[u] >> (4 * v)) & 15u), xf[8 * u + v], s);
-    return fmaf(a, s, -b * xsum);
-  }
-};
-
-template <>
-struct ChunkDot<F_Q8_0> {
-  __device__ static float run(const uint8_t* rec, const uint8_t*, int row, int w, const float* xf,
-                              float) {
-    (void)row;
-    const float d = h2f(*reinterpret_cast<const unsigned short*>(rec + 2 * w));
-    const uint4 q0 = lds128(rec + q80_q_off(w, 0));
-    const uint4 q1 = lds128(rec + q80_q_off(w, 1));
-    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    float s = 0.0f;
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-#pragma unroll
-      for (int v = 0; v < 4; ++v)
-        s = fmaf((float)(int)(int8_t)((qw[u] >> (8 * v)) & 0xFFu), xf[4 * u + v], s);
-    return d * s;
-  }
-};
-
-template <>
-struct ChunkDot<F_Q6_K> {
-  // w = (d sc_j) (q - 32), sc_j per 16 values
-  __device__ static float run(const uint8_t* rec, const uint8_t* dplane, int row, int w,
-                              const float* xf, float) {
-    const uint4 ql = lds128(rec + q6k_ql_off(w));
-    const uint2 qh = *reinterpret_cast<const uint2*>(rec + q6k_qh_off(w));
-    const int sc0 = (int)(int8_t)rec[192 + 2 * w], sc1 = (int)(int8_t)rec[192 + 2 * w + 1];
-    const float d = h2f(*reinterpret_cast<const unsigned short*>(dplane + 2 * row));
-    const uint32_t lw[4] = {ql.x, ql.y, ql.z, ql.w};
-    const uint32_t hw[2] = {qh.x, qh.y};
-    float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int lo = (int)((lw[e >> 3] >> (4 * (e & 7))) & 15u);
-      const int hi = (int)((hw[e >> 4] >> (2 * (e & 15))) & 3u);
-      const float qv = (float)((lo | (hi << 4)) - 32);
-      if (e < 16) s0 = fmaf(qv, xf[e], s0);
-      else s1 = fmaf(qv, xf[e], s1);
-    }
-    return fmaf(d * (float)sc0, s0, (d * (float)sc1) * s1);
-  }
-};
-
-template <>
-struct ChunkDot<F_NVFP4> {
-  // w = e2m1 * s_b (* s_T in the epilogue)
-  __device__ static float run(const uint8_t* rec, const uint8_t*, int row, int w, const float* xf,
-                              float) {
-    (void)row;
-    const uint4 c = lds128(rec + nv_q_off(w));
-    const float sb0 = e4m3f(rec[2 * w]), sb1 = e4m3f(rec[2 * w + 1]);
-    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-    float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float v = e2m1f((cw[e >> 3] >> (4 * (e & 7))) & 15u);
-      if (e < 16) s0 = fmaf(v, xf[e], s0);
-      else s1 = fmaf(v, xf[e], s1);
-    }
-    return fmaf(sb0, s0, sb1 * s1);
-  }
-};
-
-template <>
-struct ChunkDot<F_FP8> {
-  // w = e4m3 (* s_row in the epilogue)
-  __device__ static float run(const uint8_t* rec, const uint8_t*, int row, int w, const float* xf,
-                              float) {
-    const uint4 c0 = lds128(rec + fp8_v_off(2 * w, row & 7));
-    const uint4 c1 = lds128(rec + fp8_v_off(2 * w + 1, row & 7));
-    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    float s = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) s = fmaf(e4m3f((cw[e >> 2] >> (8 * (e & 3))) & 0xFFu), xf[e], s);
-    return s;
-  }
-};
-
-// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 struct KParams {
@@ -222,9 +118,9 @@ struct KParams {
   int stage_bytes;
   int x_off;         // offset of the x slices inside a stage
   int b_off;         // offset of plane B (Q6_K d) inside a stage
-  int red_off;       // offset of the reduction buffer
+  int tbl_off;       // offset of the per-warp scale tables
   int stage_base;    // offset of stage 0
-  int mt;            // partial stride (rows of x per partial record)
+  int mt;            // partial stride (token columns per partial record)
   unsigned* flags;   // [num_ctas]
   float* partials;   // [num_ctas][128][mt]
 };
@@ -236,14 +132,19 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
   const Layout& L = a.L;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  uint64_t* red_full = empty + kMaxStages;
-  uint64_t* red_free = red_full + 1;
+  uint64_t* fin = empty + kMaxStages;
   volatile int* misc = reinterpret_cast<volatile int*>(smem + 8 * (2 * kMaxStages + 2));
   Seg* segs = reinterpret_cast<Seg*>(smem + 512);
-  float* red = reinterpret_cast<float*>(smem + kp.red_off);
+  float2* tbls = reinterpret_cast<float2*>(smem + kp.tbl_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
+
+  // Programmatic dependent launch: the next kernel in the stream may start its own
+  // prologue and weight prefetch as SMs free up. Everything that could depend on
+  // the previous kernel (the activations, the workspace, the outputs) is touched
+  // only after griddepcontrol.wait (a no-op when launched without the attribute).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- set-up: header check, segment table, barriers -----------------------
   if (tid == 0) {
@@ -256,8 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
-    mbar_init(red_full, kConsumerWarps);
-    mbar_init(red_free, kConsumerWarps);
+    mbar_init(fin, kConsumerWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -274,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
       // ranked by counting smaller keys; runs of equal ids become segments whose
       // pairs keep their (token, slot) order.
       const int P = a.M * a.topk;            // <= 64
-      int* skeys = reinterpret_cast<int*>(smem + kp.red_off);      // scratch before first use
+      int* skeys = reinterpret_cast<int*>(smem + kp.tbl_off);      // scratch before first use
+      asm volatile("griddepcontrol.wait;" ::: "memory");          // ids come from earlier work
       int* sorted = skeys + 64;
       bool bad = false;
       for (int p = lane; p < P; p += 32) {
@@ -293,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
           sorted[rank] = key;
         }
         __syncwarp();
-        // first-of-run flags over the 64 sorted positions
         const int k0 = lane < P ? sorted[lane] : 0x7fffffff;
         const int k1 = lane + 32 < P ? sorted[lane + 32] : 0x7fffffff;
         const int pk0 = lane >= 1 && lane - 1 < P ? sorted[lane - 1] : -1;
@@ -349,30 +249,55 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
   if (warp == 0) {
     // ---------------------------- producer --------------------------------
     if (lane != 0) return;
+    // slab s -> (segment, row tile t, k-group g), advanced incrementally (no 64-bit
+    // division inside the loop)
+    int64_t g = s0 % G, t = (s0 / G) % L.row_tiles, seg = (s0 / G) / L.row_tiles;
+    int stage = 0;
+    uint32_t rphase = 0;          // parity of the current round over the stage ring
     int64_t it = 0;
+    // The first round of stages: weights first (independent of earlier kernels),
+    // then wait for the previous grid, then the activations of those stages.
+    const int64_t first = (s1 - s0) < kp.stages ? (s1 - s0) : kp.stages;
+    {
+      int64_t gg = g, t2 = t, sg2 = seg;
+      for (int64_t i = 0; i < first; ++i) {
+        const Seg& sg = segs[sg2];
+        uint8_t* st = smem + kp.stage_base + (int)i * kp.stage_bytes;
+        const uint8_t* plane = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + gg * L.group_bytes;
+        const uint32_t abytes = (uint32_t)(kSlabRows * L.rec);
+        const uint32_t bbytes = (FMT == F_Q6_K) ? (uint32_t)(kSlabRows * 2) : 0u;
+        const int64_t kv = (L.K - gg * kSlabK) < kSlabK ? (L.K - gg * kSlabK) : kSlabK;
+        const int R = sg.R < MT ? sg.R : MT;
+        mbar_expect_tx(&full[i], abytes + bbytes + (uint32_t)(kv * 2) * (uint32_t)R);
+        bulk_g2s(st, plane + t2 * kSlabRows * L.rec, abytes, &full[i]);
+        if (FMT == F_Q6_K) bulk_g2s(st + kp.b_off, plane + L.plane_a + t2 * kSlabRows * 2, bbytes, &full[i]);
+        if (++gg == G) { gg = 0; if (++t2 == L.row_tiles) { t2 = 0; ++sg2; } }
+      }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int64_t s = s0; s < s1; ++s, ++it) {
-      const int stage = (int)(it % kp.stages);
-      if (it >= kp.stages) {
-        const uint32_t par = (uint32_t)(((it / kp.stages) - 1) & 1);
-        if (!mbar_wait(&empty[stage], par, a.status)) { misc[0] = 1; break; }
+      if (it >= kp.stages) {      // round r >= 1 waits for the consumers' release of round r-1
+        if (!mbar_wait(&empty[stage], rphase ^ 1u, a.status)) { misc[0] = 1; break; }
       }
       if (misc[0]) break;
-      const int64_t T = s / G, g = s % G;
-      const Seg& sg = segs[T / L.row_tiles];
-      const int64_t t = T % L.row_tiles;
-      uint8_t* st = smem + kp.stage_base + (int64_t)stage * kp.stage_bytes;
+      const Seg& sg = segs[seg];
+      uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
       const uint8_t* plane = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + g * L.group_bytes;
       const uint32_t abytes = (uint32_t)(kSlabRows * L.rec);
       const uint32_t bbytes = (FMT == F_Q6_K) ? (uint32_t)(kSlabRows * 2) : 0u;
       const int64_t kv = (L.K - g * kSlabK) < kSlabK ? (L.K - g * kSlabK) : kSlabK;
       const uint32_t xbytes = (uint32_t)(kv * 2);
       const int R = sg.R < MT ? sg.R : MT;
-      mbar_expect_tx(&full[stage], abytes + bbytes + xbytes * (uint32_t)R);
-      bulk_g2s(st, plane + t * kSlabRows * L.rec, abytes, &full[stage]);
-      if (FMT == F_Q6_K) bulk_g2s(st + kp.b_off, plane + L.plane_a + t * kSlabRows * 2, bbytes, &full[stage]);
+      if (it >= first) {
+        mbar_expect_tx(&full[stage], abytes + bbytes + xbytes * (uint32_t)R);
+        bulk_g2s(st, plane + t * kSlabRows * L.rec, abytes, &full[stage]);
+        if (FMT == F_Q6_K) bulk_g2s(st + kp.b_off, plane + L.plane_a + t * kSlabRows * 2, bbytes, &full[stage]);
+      }
       for (int r = 0; r < R; ++r)
-        bulk_g2s(st + kp.x_off + r * (kSlabK * 2), a.x + (int64_t)sg.xrow[r] * L.K + g * kSlabK, xbytes,
+        bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + g * kSlabK, xbytes,
                  &full[stage]);
+      if (++stage == kp.stages) { stage = 0; rphase ^= 1u; }
+      if (++g == G) { g = 0; if (++t == L.row_tiles) { t = 0; ++seg; } }
     }
     // drain: copies issued into stages the consumers may not have waited for
     if (misc[0]) {
@@ -384,96 +309,77 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
   }
 
   // ------------------------------ consumers ---------------------------------
-  const int w = warp - 1;               // chunk index of this warp
+  const int w = warp - 1;               // this warp owns rows 16w .. 16w+15 of a slab
+  const int g = lane >> 2, tq = lane & 3;
   const int ctid = tid - 32;            // 0..255
-  float acc[4][MT];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int r = 0; r < MT; ++r) acc[i][r] = 0.0f;
-  int64_t it = 0;
-  int flushes = 0;
-  for (int64_t s = s0; s < s1; ++s, ++it) {
+  float2* tbl = tbls + w * (16 * kTblStride);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int nfin = 0;                          // phases of the `fin` rendezvous used so far
+  int64_t gk = s0 % G, T = s0 / G;
+  int64_t tt = T % L.row_tiles, seg = T / L.row_tiles;
+  int stage = 0;
+  uint32_t fphase = 0;                   // parity of the full barrier for this stage round
+  for (int64_t s = s0; s < s1; ++s) {
     if (misc[0]) break;
-    const int stage = (int)(it % kp.stages);
-    const int64_t T = s / G, g = s % G;
-    const Seg& sg = segs[T / L.row_tiles];
-    if (!mbar_wait(&full[stage], (uint32_t)((it / kp.stages) & 1), a.status)) { misc[0] = 1; break; }
-    const uint8_t* st = smem + kp.stage_base + (int64_t)stage * kp.stage_bytes;
-    const int64_t k0 = g * kSlabK + (int64_t)w * kChunk;
-    if (k0 < L.K) {
-      for (int r = 0; r < sg.R && r < MT; ++r) {
-        float xf[32];
-        const uint8_t* xs = st + kp.x_off + r * (kSlabK * 2) + w * 64;
-        float xsum = 0.0f;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const uint4 v = lds128(xs + 16 * h);
-          const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            xf[8 * h + 2 * u] = bf2f(vw[u]);
-            xf[8 * h + 2 * u + 1] = bf2f(vw[u] >> 16);
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) xsum += xf[e];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = lane + 32 * i;
-          const float v = ChunkDot<FMT>::run(st + row * L.rec, st + kp.b_off, row, w, xf, xsum);
-#pragma unroll
-          for (int rr = 0; rr < MT; ++rr)
-            if (rr == r) acc[i][rr] += v;
-        }
+    const Seg& sg = segs[seg];
+    const int R = sg.R < MT ? sg.R : MT;
+    if (!mbar_wait(&full[stage], fphase, a.status)) { misc[0] = 1; break; }
+    const uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
+    const bool has_x = g < R;
+    const uint8_t* xrow0 = st + kp.x_off;
+    // the last k-group may be narrower than 256: its padded blocks are zero and
+    // the x beyond K is never copied, so the stale tail of each x row is zeroed
+    // (by one thread of each warp, before that warp reads it)
+    const int64_t kv = (L.K - gk * kSlabK) < kSlabK ? (L.K - gk * kSlabK) : kSlabK;
+    if (kv < kSlabK) {
+      if (has_x && tq == 0) {
+        uint8_t* xw = const_cast<uint8_t*>(xrow0) + g * kXStride;
+        for (int64_t o = kv * 2; o < kSlabK * 2; o += 4) *reinterpret_cast<uint32_t*>(xw + o) = 0u;
       }
+      __syncwarp();
+    }
+    if (MT == 1) {
+      Slab<FMT, 1>::run(st, st + kp.b_off, xrow0, R, w, lane, tbl, acc);
+    } else {
+      Slab<FMT, MT>::run(st, st + kp.b_off, xrow0 + (has_x ? g : 0) * kXStride, R, w, lane, tbl, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == kp.stages) { stage = 0; fphase ^= 1u; }
 
-    const bool tile_end = (s + 1 == s1) || ((s + 1) / G != T);
+    // advance (k-group, tile, segment); the tile ends when the k-group wraps
+    const int64_t Tcur = T, tcur = tt;
+    const bool tile_end = (s + 1 == s1) || (gk + 1 == G);
+    if (++gk == G) { gk = 0; ++T; if (++tt == L.row_tiles) { tt = 0; ++seg; } }
     if (!tile_end) continue;
 
-    // ---- flush tile T ------------------------------------------------------
-    const int64_t head = T * G, tail = (T + 1) * G;
+    // ---- flush tile T: this thread owns rows rA, rB of it and tokens 2tq, 2tq+1 ----
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // workspace and y after earlier kernels
+    if (MT == 1) {
+      // unit columns: add the quad's partial sums of rows rA, rB (token 0)
+      float vA = acc[0], vB = acc[1];
+      vA += __shfl_xor_sync(0xffffffffu, vA, 1);
+      vB += __shfl_xor_sync(0xffffffffu, vB, 1);
+      vA += __shfl_xor_sync(0xffffffffu, vA, 2);
+      vB += __shfl_xor_sync(0xffffffffu, vB, 2);
+      acc[0] = vA; acc[1] = 0.f; acc[2] = vB; acc[3] = 0.f;
+    }
+    const int64_t head = Tcur * G, tail = (Tcur + 1) * G;
     const bool full_cover = (s0 <= head) && (s1 >= tail);
     const bool reducer = (s0 <= head);
-    const int R = sg.R < MT ? sg.R : MT;
-    if (flushes > 0) {
-      if (!mbar_wait(red_free, (uint32_t)((flushes - 1) & 1), a.status)) { misc[0] = 1; break; }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int r = 0; r < MT; ++r) red[(w * kSlabRows + lane + 32 * i) * MT + r] = acc[i][r];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(red_full);
-    if (!mbar_wait(red_full, (uint32_t)(flushes & 1), a.status)) { misc[0] = 1; break; }
-
-    const int64_t t = T % L.row_tiles;
+    const int64_t t = tcur;
+    const int rA = 16 * w + g, rB = rA + 8;
     const uint8_t* extras = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + L.k_groups * L.group_bytes;
-    // pairs handled by this thread: p = ctid + 256 j, p < 128 * R
-    float vals[(kSlabRows * MT + 255) / 256];
-    int np = 0;
-    for (int p = ctid; p < kSlabRows * R; p += 256, ++np) {
-      const int row = p / R, r = p % R;
-      float v = 0.0f;
-#pragma unroll
-      for (int ww = 0; ww < kConsumerWarps; ++ww) v += red[(ww * kSlabRows + row) * MT + r];
-      vals[np] = v;
-    }
     bool ok = true;
     if (!full_cover && !reducer) {
-      // publish this CTA's partial sums of its first tile
       float* part = kp.partials + c * (kSlabRows * kp.mt);
-      np = 0;
-      for (int p = ctid; p < kSlabRows * R; p += 256, ++np) {
-        const int row = p / R, r = p % R;
-        part[row * kp.mt + r] = vals[np];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+        if (tok < R) part[row * kp.mt + tok] = acc[e];
       }
       __threadfence();
     } else if (!full_cover && reducer) {
-      // add the peers' partial sums in CTA order
       for (int64_t cp = c + 1; cp < P; ++cp) {
         const int64_t ps0 = (cp * S) / P, ps1 = ((cp + 1) * S) / P;
         if (ps0 >= tail) break;
@@ -487,38 +393,37 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
         }
         if (!ok) break;
         const float* part = kp.partials + cp * (kSlabRows * kp.mt);
-        np = 0;
-        for (int p = ctid; p < kSlabRows * R; p += 256, ++np) {
-          const int row = p / R, r = p % R;
-          vals[np] += __ldcg(part + row * kp.mt + r);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+          if (tok < R) acc[e] += __ldcg(part + row * kp.mt + tok);
         }
       }
     }
     if (ok && (full_cover || reducer)) {
-      np = 0;
-      for (int p = ctid; p < kSlabRows * R; p += 256, ++np) {
-        const int row = p / R, r = p % R;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
         const int64_t n = t * kSlabRows + row;
-        if (n >= L.N) continue;
-        float v = vals[np];
+        if (tok >= R || n >= L.N) continue;
+        float v = acc[e];
         if (FMT == F_NVFP4) v *= *reinterpret_cast<const float*>(extras);
         if (FMT == F_FP8) v *= reinterpret_cast<const float*>(extras)[n];
-        a.y[(int64_t)sg.yrow[r] * L.N + n] = v;
+        a.y[(int64_t)sg.yrow[tok] * L.N + n] = v;
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(red_free);
     if (!ok) { misc[0] = 1; break; }
     if (!full_cover) {
-      if (!reducer) {
-        if (ctid == 0) {
-          if (!mbar_wait(red_free, (uint32_t)(flushes & 1), a.status)) misc[0] = 1;
-          else st_release(kp.flags + c, 1u);
-        }
-      } else if (ctid == 0) {
-        // every consumer thread has read the peers' flags and sums: reset the flags
-        if (!mbar_wait(red_free, (uint32_t)(flushes & 1), a.status)) misc[0] = 1;
-        else {
+      // rendezvous of the consumer warps: every partial is written (peer) or every
+      // peer partial has been read (reducer); then one thread publishes / resets
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fin);
+      if (ctid == 0) {
+        if (!mbar_wait(fin, (uint32_t)(nfin & 1), a.status)) {
+          misc[0] = 1;
+        } else if (!reducer) {
+          st_release(kp.flags + c, 1u);
+        } else {
           for (int64_t cp = c + 1; cp < P; ++cp) {
             const int64_t ps0 = (cp * S) / P, ps1 = ((cp + 1) * S) / P;
             if (ps0 >= tail) break;
@@ -526,12 +431,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
           }
         }
       }
+      ++nfin;
+      // the next rendezvous may only start after this one completed
+      if (ctid != 0 && lane == 0) {
+        if (!mbar_wait(fin, (uint32_t)((nfin - 1) & 1), a.status)) misc[0] = 1;
+      }
+      __syncwarp();
     }
-    ++flushes;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int r = 0; r < MT; ++r) acc[i][r] = 0.0f;
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
   }
 }
 
@@ -567,14 +474,14 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   KParams kp;
   kp.a = a;
   kp.mt = MT;
-  kp.red_off = 512 + kMaxSeg * (int)sizeof(Seg);
-  const int red_bytes = kConsumerWarps * kSlabRows * MT * 4;
-  kp.stage_base = (int)align_up(kp.red_off + red_bytes, 1024);
+  kp.tbl_off = 512 + kMaxSeg * (int)sizeof(Seg);
+  const int tbl_bytes = kConsumerWarps * 16 * kTblStride * (int)sizeof(float2);
+  kp.stage_base = (int)align_up(kp.tbl_off + tbl_bytes, 1024);
   const int abytes = kSlabRows * a.L.rec;
   kp.b_off = (int)align_up(abytes, 128);
   const int bbytes = (FMT == F_Q6_K) ? kSlabRows * 2 : 0;
   kp.x_off = (int)align_up(kp.b_off + bbytes, 128);
-  kp.stage_bytes = (int)align_up(kp.x_off + MT * kSlabK * 2, 1024);
+  kp.stage_bytes = (int)align_up(kp.x_off + MT * kXStride, 1024);
   kp.stages = (smem_max - kp.stage_base) / kp.stage_bytes;
   if (kp.stages > kMaxStages) kp.stages = kMaxStages;
   if (kp.stages < 2) return cudaErrorInvalidConfiguration;
@@ -582,16 +489,27 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   kp.flags = reinterpret_cast<unsigned*>(a.ws + plan.counters_off);
   kp.partials = reinterpret_cast<float*>(a.ws + plan.partials_off);
   const int smem = kp.stage_base + kp.stages * kp.stage_bytes;
-  err = cudaFuncSetAttribute(stream_kernel<FMT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
+  // opt in to the large dynamic shared memory once per device (not per launch, so
+  // that stream capture records launches only)
+  static int opted[64] = {0};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (opted[dev] < smem) {
+    err = cudaFuncSetAttribute(stream_kernel<FMT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    opted[dev] = smem;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.num_ctas);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
+  // One CTA per SM and at most one CTA per SM fits, so every CTA of the grid is
+  // resident once the previous kernel's CTAs have left: a reducer's bounded wait
+  // on its peers' flags ends. Programmatic stream serialization lets this grid's
+  // prologue overlap the previous kernel's tail (see griddepcontrol in the kernel).
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;   // peers wait on each other's flags
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   err = cudaLaunchKernelEx(&cfg, stream_kernel<FMT, MT>, kp);

@@ -5,8 +5,8 @@ bf16 activations and routed expert ids. Quantization (encoding) and everything
 after it live in the CUDA library and, independently, in the CPU oracle.
 
 One counter-based generator, evaluated with exact integer and IEEE-754 fp32 ops
-only, so the same element index gives the same bits on the host (torch CPU) and on
-the GPU (torch CUDA):
+only, so the same element index gives the same bits on the host (numpy uint32
+arithmetic) and on the GPU (torch int64 arithmetic on CUDA tensors):
 
   key_j      = lowbias32(seed * 0x9E3779B9 + stream * 0x85EBCA6B + j * 0xC2B2AE35)
   h_j(i)     = lowbias32(lowbias32(lo32(i) ^ key_j) ^ hi32(i))           j = 0..5
@@ -69,8 +69,33 @@ def _key(seed: int, stream: int, j: int) -> int:
     return _lowbias32_int(seed * 0x9E3779B9 + stream * 0x85EBCA6B + j * 0xC2B2AE35)
 
 
+def _lowbias32_np(x: np.ndarray) -> np.ndarray:
+    """lowbias32 on a uint32 numpy array (uint32 arithmetic wraps mod 2^32)."""
+    x = x ^ (x >> np.uint32(16))
+    x = x * np.uint32(0x7FEB352D)
+    x = x ^ (x >> np.uint32(15))
+    x = x * np.uint32(0x846CA68B)
+    x = x ^ (x >> np.uint32(16))
+    return x
+
+
+def normal_at_np(seed: int, stream: int, idx: np.ndarray) -> np.ndarray:
+    """z(i) on the host with numpy uint32 arithmetic (same bits as normal_at)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    lo = (idx & M32).astype(np.uint32)
+    hi = (idx >> 32).astype(np.uint32)
+    S = np.zeros(idx.shape, dtype=np.int64)
+    with np.errstate(over="ignore"):
+        for j in range(6):
+            h = _lowbias32_np(_lowbias32_np(lo ^ np.uint32(_key(seed, stream, j))) ^ hi)
+            S += (h & np.uint32(0xFFFF)).astype(np.int64) + (h >> np.uint32(16)).astype(np.int64)
+    return (S - 393210).astype(np.float32) / np.float32(65536.0)
+
+
 def normal_at(seed: int, stream: int, idx: torch.Tensor) -> torch.Tensor:
     """z(i) for an int64 tensor of element indices (any device) -> float32."""
+    if not idx.is_cuda:
+        return torch.from_numpy(normal_at_np(seed, stream, idx.numpy()))
     idx = idx.to(torch.int64)
     lo = idx & M32
     hi = idx >> 32
@@ -86,7 +111,7 @@ def weights_rows(seed: int, rows, K: int, device="cpu", stream: int = STREAM_W) 
     rows = torch.as_tensor(rows, dtype=torch.int64, device=device).reshape(-1, 1)
     k = torch.arange(K, dtype=torch.int64, device=device).reshape(1, -1)
     z = normal_at(seed, stream, rows * K + k)
-    return z * torch.tensor(0.02, dtype=torch.float32, device=device)
+    return z * torch.tensor(0.02, dtype=torch.float32, device=z.device)
 
 
 def weights(seed: int, N: int, K: int, device="cpu", row0: int = 0,
