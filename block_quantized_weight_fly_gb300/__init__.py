@@ -58,6 +58,7 @@ _quantize = _sig("qmv_quantize", _I, [_I, _P, _I64, _I64, _F, _P, _P])
 _dequant = _sig("qmv_dequant", _I, [_I, _P, _I64, _I64, _I64, _I64, _I64, _P, _P])
 _ws_size = _sig("qmv_workspace_size", _SZ, [_I, _I, _I, _I64, _I64, _I64, _I])
 _gemv = _sig("qmv_gemv", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
+_gemv_noalloc = _sig("qmv_gemv_noalloc", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P])
 _grouped = _sig("qmv_grouped", _I, [_I, _P, _P, _P, _I, _P, _I, _I, _I64, _I64, _I64, _P, _SZ, _P])
 _quant_act = _sig("qmv_quant_act_nvfp4", _I, [_P, _F, _P, _P, _I, _I64, _P])
 _w4a4 = _sig("qmv_gemm_nvfp4_w4a4", _I, [_P, _P, _F, _P, _I, _I64, _I64, _P, _SZ, _P])
@@ -67,7 +68,8 @@ _dev_status = _sig("qmv_device_status", _I, [_I])
 
 EXPORTED = ["qmv_canon_size", "qmv_pack_size", "qmv_pack", "qmv_quantize", "qmv_dequant",
             "qmv_workspace_size", "qmv_gemv", "qmv_grouped", "qmv_quant_act_nvfp4",
-            "qmv_gemm_nvfp4_w4a4", "qmv_status_str", "qmv_last_route", "qmv_device_status"]
+            "qmv_gemm_nvfp4_w4a4", "qmv_status_str", "qmv_last_route", "qmv_device_status",
+            "qmv_gemv_noalloc"]
 
 
 def _fmt(fmt) -> int:
@@ -185,6 +187,18 @@ def qmv_gemv(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int,
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
     _check(_gemv(_fmt(fmt), _ptr(packed_W), _ptr(x), _ptr(y), M, N, K, _ptr(ws), ws.numel(),
                  _stream(stream)), "qmv_gemv")
+    return y
+
+
+def qmv_gemv_noalloc(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int,
+                     y: torch.Tensor, stream=None) -> torch.Tensor:
+    """qmv_gemv with the library's built-in scratch instead of a workspace. y is
+    required (the caller owns every buffer); nothing is allocated."""
+    _dev(packed_W, "packed_W"); _dev(x, "x"); _dev(y, "y")
+    x = _bits16(x)
+    M = x.shape[0] if x.dim() == 2 else 1
+    _check(_gemv_noalloc(_fmt(fmt), _ptr(packed_W), _ptr(x), _ptr(y), M, N, K, _stream(stream)),
+           "qmv_gemv_noalloc")
     return y
 
 

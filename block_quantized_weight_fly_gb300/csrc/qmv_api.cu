@@ -211,3 +211,69 @@ qmv_status qmv_device_status(int reset) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// qmv_gemv_noalloc: qmv_gemv with its split-K scratch in the library's own
+// device image instead of a caller workspace.
+// ---------------------------------------------------------------------------
+
+// The one scratch array all qmv_gemv_noalloc calls on a device share (flag words
+// and partial sums of the split-K reduction). 1 MiB covers the need of qmv_gemv
+// up to 255 SMs at M = 2..8 (and more SMs at M = 1).
+static __device__ __align__(256) unsigned char g_gemv_scratch[QMV_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+uint8_t* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Set-up, once per device, with that device current: the device address of the
+// scratch array. The first qmv_gemv_noalloc call on each device runs it.
+qmv_status scratch_ptr(uint8_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMV_ECUDA;
+  if (g_scratch_ptr[dev] == nullptr) {
+    uint8_t* ptr = nullptr;
+    if (cudaGetSymbolAddress((void**)&ptr, g_gemv_scratch) != cudaSuccess) return QMV_ECUDA;
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return QMV_OK;
+}
+
+}  // namespace
+
+extern "C" qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y,
+                                       int M, int64_t N, int64_t K, cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !packed_W || !x || !y) return QMV_EINVAL;
+  if (M < 1 || M > QMV_MAX_M || N <= 0 || K <= 0) return QMV_EINVAL;
+  Layout L;
+  if (!make_layout((int)fmt, N, K, 1, &L)) return QMV_EUNSUPPORTED;
+  if (!aligned(packed_W, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return QMV_ECUDA;
+  const WsPlan plan = ws_plan_stream(M, 0, sms);
+  if ((size_t)plan.total > (size_t)QMV_STATIC_SCRATCH_BYTES) return QMV_EWORKSPACE;
+  uint8_t* scratch = nullptr;
+  qmv_status st = scratch_ptr(&scratch);
+  if (st != QMV_OK) return st;
+  unsigned* status = status_ptr();
+  if (!status) return QMV_ECUDA;
+  // The array keeps whatever the previous call left; the flag words must start at
+  // zero (a failed call can leave some set). Partial sums are written before they
+  // are read and need no clearing.
+  st = from_cuda(cudaMemsetAsync(scratch + plan.counters_off, 0, (size_t)plan.counters_bytes, stream));
+  if (st != QMV_OK) return st;
+  StreamArgs a;
+  a.L = L;
+  a.packed = static_cast<const uint8_t*>(packed_W);
+  a.x = x; a.y = y; a.ids = nullptr;
+  a.M = M; a.topk = 1; a.x_per_pair = 0;
+  a.ws = scratch; a.ws_bytes = (int64_t)QMV_STATIC_SCRATCH_BYTES;
+  a.status = status;
+  const int64_t slabs = L.row_tiles * L.k_groups;
+  a.num_ctas = (int)(slabs < sms ? slabs : sms);
+  int variant = 0;
+  st = from_cuda(launch_stream(a, stream, &variant));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
+  return st;
+}

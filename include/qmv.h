@@ -131,6 +131,30 @@ size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, i
 qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y, int M,
                     int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Bytes of the device scratch array built into the library for qmv_gemv_noalloc. */
+#define QMV_STATIC_SCRATCH_BYTES (1u << 20)
+
+/* qmv_gemv without a workspace argument; it allocates nothing. The pages have no
+ * counterpart: it is a library convenience. It serves callers that cannot hand
+ * over device memory per call -- an engine whose allocator has already reserved
+ * the device for its own pool, or a plugin interface that passes only input and
+ * output pointers -- and that must not call cudaMalloc/cudaFree on the decode
+ * path, since those can fail under a full pool or synchronize the device.
+ * The split-K flag words and partial sums live instead in one fixed array of
+ * QMV_STATIC_SCRATCH_BYTES in the library's device image.
+ * Set-up: the first call on each device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * Every call on a device shares the one array, which keeps what the last call
+ * left: each call first clears the flag words on `stream` (cudaMemsetAsync, no
+ * allocation). Calls that overlap in time (on other streams or host threads)
+ * race on the array; the caller must serialize them.
+ * Returns QMV_EWORKSPACE when the scratch this device needs,
+ * qmv_workspace_size(QMV_ENTRY_GEMV, fmt, M, N, K, 1, 1), exceeds
+ * QMV_STATIC_SCRATCH_BYTES (M = 2..8 on a device of more than 255 SMs).
+ * Otherwise arguments, results and errors as qmv_gemv. */
+qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y,
+                            int M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* Grouped per-expert GEMV over a stacked tower of E experts.
  * expert_ids: device int32 [M][topk] (ids within a token distinct; never read
  * on the host). x: device bf16, [M][K] if x_per_pair == 0 (every slot of a
