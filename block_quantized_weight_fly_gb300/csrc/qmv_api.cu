@@ -107,7 +107,7 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
   if (!valid_fmt(fmt) || !packed_W || !x || !y || !ws) return QMV_EINVAL;
   if (M < 1 || M > QMV_MAX_M || N <= 0 || K <= 0) return QMV_EINVAL;
   Layout L;
-  if (!make_layout((int)fmt, N, K, 1, &L)) return QMV_EUNSUPPORTED;
+  if (!make_layout((int)fmt, N, K, 1, &L) || !slab_count_ok(L, 1)) return QMV_EUNSUPPORTED;
   if (!aligned(packed_W, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
@@ -138,6 +138,7 @@ qmv_status qmv_grouped(qmv_fmt fmt, const void* tower, const int32_t* expert_ids
   if (E > (int64_t)1 << 24) return QMV_EUNSUPPORTED;   // ids are packed with a 6-bit pair index
   Layout L;
   if (!make_layout((int)fmt, N, K, E, &L)) return QMV_EUNSUPPORTED;
+  if (!slab_count_ok(L, (int64_t)M * topk < E ? (int64_t)M * topk : E)) return QMV_EUNSUPPORTED;
   if (!aligned(tower, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4) ||
       !aligned(expert_ids, 4))
     return QMV_EALIGN;
@@ -217,9 +218,9 @@ qmv_status qmv_device_status(int reset) {
 // device image instead of a caller workspace.
 // ---------------------------------------------------------------------------
 
-// The one scratch array all qmv_gemv_noalloc calls on a device share (flag words
-// and partial sums of the split-K reduction). 1 MiB covers the need of qmv_gemv
-// up to 255 SMs at M = 2..8 (and more SMs at M = 1).
+// The one scratch array all qmv_gemv_noalloc calls on a device share (the partial
+// sums of the split-K reduction). 1 MiB covers the need of qmv_gemv up to 256 SMs
+// at M = 2..8 (and more SMs at M = 1).
 static __device__ __align__(256) unsigned char g_gemv_scratch[QMV_STATIC_SCRATCH_BYTES];
 
 namespace {
@@ -247,7 +248,7 @@ extern "C" qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const 
   if (!valid_fmt(fmt) || !packed_W || !x || !y) return QMV_EINVAL;
   if (M < 1 || M > QMV_MAX_M || N <= 0 || K <= 0) return QMV_EINVAL;
   Layout L;
-  if (!make_layout((int)fmt, N, K, 1, &L)) return QMV_EUNSUPPORTED;
+  if (!make_layout((int)fmt, N, K, 1, &L) || !slab_count_ok(L, 1)) return QMV_EUNSUPPORTED;
   if (!aligned(packed_W, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
@@ -258,10 +259,9 @@ extern "C" qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const 
   if (st != QMV_OK) return st;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
-  // The array keeps whatever the previous call left; the flag words must start at
-  // zero (a failed call can leave some set). Partial sums are written before they
-  // are read and need no clearing.
-  st = from_cuda(cudaMemsetAsync(scratch + plan.counters_off, 0, (size_t)plan.counters_bytes, stream));
+  // The array keeps whatever the previous call left; the partial-sum words must
+  // start at zero (a successful call leaves them zero, a failed one may not).
+  st = from_cuda(cudaMemsetAsync(scratch + plan.partials_off, 0, (size_t)plan.partials_bytes, stream));
   if (st != QMV_OK) return st;
   StreamArgs a;
   a.L = L;

@@ -21,7 +21,7 @@ struct StreamArgs {
   int M;                     // tokens (rows of x for dense)
   int topk;                  // grouped: slots per token; dense: 1
   int x_per_pair;            // grouped: 1 if x has one row per (token, slot)
-  uint8_t* ws;               // workspace (zero-filled; status area in the first 256 B)
+  uint8_t* ws;               // workspace: per-CTA partial sums (zero between calls)
   int64_t ws_bytes;
   unsigned* status;          // per-device status word
   int num_ctas;              // persistent grid size
@@ -29,13 +29,18 @@ struct StreamArgs {
 
 // workspace carve-up (bytes), shared by the host size query and the kernels
 struct WsPlan {
-  int64_t counters_off, counters_bytes;
   int64_t partials_off, partials_bytes;
   int64_t total;
 };
 WsPlan ws_plan_stream(int M, int64_t tiles_max, int num_ctas);
 
 int num_sms_current_device();
+
+// The streaming kernel numbers its slabs (segment, row tile, k-group) with 32-bit
+// integers: segments x row tiles x k-groups must stay below 2^31.
+inline bool slab_count_ok(const Layout& L, int64_t segments) {
+  return segments * L.row_tiles * L.k_groups < ((int64_t)1 << 31);
+}
 
 cudaError_t launch_pack(const Layout& L, const uint8_t* canon, uint8_t* dst, cudaStream_t s);
 cudaError_t launch_dequant(const Layout& L, const uint8_t* packed, int64_t row0, int64_t rows,

@@ -30,6 +30,8 @@
 namespace qmv {
 
 constexpr int kXStride = 576;          // bytes per token row of a stage's x slice (512 + 64 pad)
+constexpr int kXZero = 512;            // M = 1: the pad after x row 0 holds zeros ...
+constexpr int kXZeroBytes = 64;        // ... (64 bytes, written once per kernel)
 constexpr int kTblStride = 17;         // float2 entries per row of a warp's scale table
 constexpr uint32_t kOnesBf16 = 0x3F803F80u;
 
@@ -64,13 +66,27 @@ __device__ __forceinline__ void load16(const uint8_t* p, uint32_t* w) {   // 64 
   load8(p, w);
   load8(p + 32, w + 8);
 }
+// (a & m) | o as one three-input logic op
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t m, uint32_t o) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(m), "r"(o));
+  return d;
+}
 // two 4-bit fields at nibbles (p, p+4) -> bf16x2 {128 + lo, 128 + hi}
 __device__ __forceinline__ uint32_t nib_pair(uint32_t w, int p) {
-  return ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+  return and_or(p ? (w >> (4 * p)) : w, 0x000F000Fu, 0x43004300u);
 }
 // two 2-bit fields at bits (2k, 2k + 16) -> bf16x2 {128 + lo, 128 + hi}
 __device__ __forceinline__ uint32_t bit2_pair(uint32_t w, int k) {
-  return ((w >> (2 * k)) & 0x00030003u) | 0x43004300u;
+  return and_or(k ? (w >> (2 * k)) : w, 0x00030003u, 0x43004300u);
+}
+// the low 6 bits of v as an exact fp32
+__device__ __forceinline__ float u6f(uint32_t v) {
+  return __uint_as_float(and_or(v, 63u, 0x4B000000u)) - 8388608.0f;
+}
+// the two fp16 values of a 32-bit word as fp32 (exact)
+__device__ __forceinline__ float2 h2x2f(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 // FP4 E2M1 pair (one byte) -> f16x2, exact
 __device__ __forceinline__ uint32_t e2m1x2_f16(uint32_t byte) {
@@ -106,6 +122,15 @@ __device__ __forceinline__ float i8f(uint32_t byte) {   // signed int8 -> fp32
 }
 // keep v if this thread's unit is the current one, else zero (sparse unit-column B)
 __device__ __forceinline__ uint32_t sel(bool mine, uint32_t v) { return mine ? v : 0u; }
+// Sparse unit-column B from shared memory: the thread's own activations for the
+// sub-block it owns, the zero pad for every other sub-block (one address select
+// per load instead of one select per register).
+__device__ __forceinline__ uint4 ldx128(const uint8_t* xs, bool mine, uint32_t off) {
+  return lds128v(xs + (mine ? off : (uint32_t)kXZero));
+}
+__device__ __forceinline__ uint2 ldx64(const uint8_t* xs, bool mine, uint32_t off) {
+  return lds64(xs + (mine ? off : (uint32_t)kXZero));
+}
 
 template <int FMT, int MT>
 struct Slab;
@@ -116,13 +141,27 @@ struct Slab;
 // ============================================================================
 __device__ __forceinline__ void q4k_pair_scales(const uint4 hd, int t, float* a, float* c) {
   // sc_j, m_j of sub-blocks j = 2t, 2t+1 (12 consecutive bits each)
-  const float d = h2f(hd.x), dm = h2f(hd.x >> 16);
+  const float2 dd = h2x2f(hd.x);
   const uint64_t lo = ((uint64_t)hd.z << 32) | hd.y, hi = ((uint64_t)hd.w << 32) | hd.z;
   const uint32_t s = (uint32_t)(lo >> (12 * t)), m = (uint32_t)(hi >> (16 + 12 * t));
-  a[0] = d * u2f_small(s & 63u);
-  a[1] = d * u2f_small((s >> 6) & 63u);
-  c[0] = fmaf(128.0f, a[0], dm * u2f_small(m & 63u));
-  c[1] = fmaf(128.0f, a[1], dm * u2f_small((m >> 6) & 63u));
+  a[0] = dd.x * u6f(s);
+  a[1] = dd.x * u6f(s >> 6);
+  c[0] = fmaf(128.0f, a[0], dd.y * u6f(m));
+  c[1] = fmaf(128.0f, a[1], dd.y * u6f(m >> 6));
+}
+// the same from a record in shared memory: the scale stream starts at byte 4 and
+// the fields of sub-blocks 2t, 2t+1 sit at stream bits 12t (sc) and 48 + 12t (m);
+// each pair is taken from two aligned 32-bit words with one funnel shift
+__device__ __forceinline__ void q4k_pair_scales_rec(const uint8_t* rec, int t, float* a, float* c) {
+  const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 4);
+  const int bs = 12 * t, bm = 48 + 12 * t;
+  const uint32_t s = __funnelshift_r(sw[bs >> 5], sw[(bs >> 5) + 1], bs & 31);
+  const uint32_t m = __funnelshift_r(sw[bm >> 5], sw[(bm >> 5) + 1], bm & 31);
+  const float2 dd = h2x2f(*reinterpret_cast<const uint32_t*>(rec));
+  a[0] = dd.x * u6f(s);
+  a[1] = dd.x * u6f(s >> 6);
+  c[0] = fmaf(128.0f, a[0], dd.y * u6f(m));
+  c[1] = fmaf(128.0f, a[1], dd.y * u6f(m >> 6));
 }
 
 template <>
@@ -132,7 +171,7 @@ struct Slab<F_Q4_K, 1> {
     const int g = lane >> 2, t = lane & 3;
     const uint8_t* rA = st + (16 * w + g) * 144;
     const uint8_t* rB = rA + 8 * 144;
-    const uint4 xv = lds128v(xs + 64 * g + 16 * t);          // unit g = chunk g of token 0
+    const uint32_t xo = 64 * g + 16 * t;                     // unit g = chunk g of token 0
     uint32_t WA[8], WB[8];
     load8(rA + q4k_word_off(t, 0), WA);
     load8(rB + q4k_word_off(t, 0), WB);
@@ -140,18 +179,17 @@ struct Slab<F_Q4_K, 1> {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t wa = WA[j], wb = WB[j];
-      const bool mine = (g == j);
+      const uint4 b = ldx128(xs, g == j, xo);
       float* d = (j & 1) ? dO : dE;
-      mma_bf16(d, nib_pair(wa, 0), nib_pair(wb, 0), nib_pair(wa, 1), nib_pair(wb, 1), sel(mine, xv.x),
-               sel(mine, xv.y));
-      mma_bf16(d, nib_pair(wa, 2), nib_pair(wb, 2), nib_pair(wa, 3), nib_pair(wb, 3), sel(mine, xv.z),
-               sel(mine, xv.w));
+      mma_bf16(d, nib_pair(wa, 0), nib_pair(wb, 0), nib_pair(wa, 1), nib_pair(wb, 1), b.x, b.y);
+      mma_bf16(d, nib_pair(wa, 2), nib_pair(wb, 2), nib_pair(wa, 3), nib_pair(wb, 3), b.z, b.w);
     }
+    const uint4 xv = lds128v(xs + xo);
     mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
     mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
     float aA[2], cA[2], aB[2], cB[2];
-    q4k_pair_scales(lds128v(rA), t, aA, cA);
-    q4k_pair_scales(lds128v(rB), t, aB, cB);
+    q4k_pair_scales_rec(rA, t, aA, cA);
+    q4k_pair_scales_rec(rB, t, aB, cB);
     acc[0] += fmaf(aA[0], dE[0] + dO[0], fmaf(aA[1], dE[1] + dO[1], -fmaf(cA[0], xx[0], cA[1] * xx[1])));
     acc[1] += fmaf(aB[0], dE[2] + dO[2], fmaf(aB[1], dE[3] + dO[3], -fmaf(cB[0], xx[2], cB[1] * xx[3])));
   }
@@ -219,7 +257,7 @@ struct Slab<F_Q8_0, 1> {
     const int g = lane >> 2, t = lane & 3;
     const uint8_t* rA = st + (16 * w + g) * 272;
     const uint8_t* rB = rA + 8 * 272;
-    const uint4 xv = lds128v(xs + 64 * g + 16 * t);
+    const uint32_t xo = 64 * g + 16 * t;
     uint32_t WA[16], WB[16];
     load16(rA + q80_word_off(t, 0), WA);
     load16(rB + q80_word_off(t, 0), WB);
@@ -227,17 +265,19 @@ struct Slab<F_Q8_0, 1> {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint2 wa = make_uint2(WA[2 * j], WA[2 * j + 1]), wb = make_uint2(WB[2 * j], WB[2 * j + 1]);
-      const bool mine = (g == j);
-      const uint32_t b0 = sel(mine, xv.x), b1 = sel(mine, xv.y), b2 = sel(mine, xv.z), b3 = sel(mine, xv.w);
+      const uint4 bv = ldx128(xs, g == j, xo);
+      const uint32_t b0 = bv.x, b1 = bv.y, b2 = bv.z, b3 = bv.w;
       mma_bf16(lo, nib_pair(wa.x, 0), nib_pair(wb.x, 0), nib_pair(wa.x, 1), nib_pair(wb.x, 1), b0, b1);
       mma_bf16(hi, nib_pair(wa.x, 2), nib_pair(wb.x, 2), nib_pair(wa.x, 3), nib_pair(wb.x, 3), b0, b1);
       mma_bf16(lo, nib_pair(wa.y, 0), nib_pair(wb.y, 0), nib_pair(wa.y, 1), nib_pair(wb.y, 1), b2, b3);
       mma_bf16(hi, nib_pair(wa.y, 2), nib_pair(wb.y, 2), nib_pair(wa.y, 3), nib_pair(wb.y, 3), b2, b3);
     }
+    const uint4 xv = lds128v(xs + xo);
     mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
     mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
     const uint32_t dA = lds32(rA + 4 * t), dB = lds32(rB + 4 * t);     // d of chunks 2t, 2t+1
-    const float a0 = h2f(dA), a1 = h2f(dA >> 16), b0 = h2f(dB), b1 = h2f(dB >> 16);
+    const float2 da = h2x2f(dA), db = h2x2f(dB);
+    const float a0 = da.x, a1 = da.y, b0 = db.x, b1 = db.y;
     acc[0] += fmaf(a0, fmaf(16.f, hi[0], lo[0]) - 2304.f * xx[0], a1 * (fmaf(16.f, hi[1], lo[1]) - 2304.f * xx[1]));
     acc[1] += fmaf(b0, fmaf(16.f, hi[2], lo[2]) - 2304.f * xx[2], b1 * (fmaf(16.f, hi[3], lo[3]) - 2304.f * xx[3]));
   }
@@ -333,9 +373,8 @@ struct Slab<F_Q6_K, 1> {
 #pragma unroll
       for (int s2 = 0; s2 < 2; ++s2) {
         const int u = 2 * j + s2;
-        const bool mine = ((u & 7) == g);
-        const uint2 xv = grp ? x1 : x0;
-        const uint32_t b0 = sel(mine, xv.x), b1 = sel(mine, xv.y);
+        const uint2 xv = ldx64(xs, (u & 7) == g, 32 * u + 8 * t);
+        const uint32_t b0 = xv.x, b1 = xv.y;
         mma_bf16(lo[grp], nib_pair(la, 2 * s2), nib_pair(lb, 2 * s2), nib_pair(la, 2 * s2 + 1),
                  nib_pair(lb, 2 * s2 + 1), b0, b1);
         mma_bf16(hi[grp], bit2_pair(ha, 2 * s2), bit2_pair(hb, 2 * s2), bit2_pair(ha, 2 * s2 + 1),

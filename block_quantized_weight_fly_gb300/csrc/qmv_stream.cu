@@ -13,20 +13,23 @@
 //  * warp 0 is a producer: one elected lane streams each slab (and the matching
 //    256-value slice of every x row routed to it) into a ring of shared-memory
 //    stages with cp.async.bulk, completion tracked by mbarriers; no multicast;
-//  * warps 1..8 are consumers: warp w decodes 32-value chunk w of the slab for
-//    its 128 rows (lane = row, four passes), the decode is in registers and the
-//    inner product is factored per block: y += scale * sum(q * x) (- min * sum x);
-//  * at the end of a row tile the warps' partial sums are added in shared
-//    memory in a fixed order. A tile split between CTAs is finished by the CTA
-//    that holds its first k-groups: the others publish their partial sums and a
-//    flag, and it adds them in CTA order -- deterministic, no float atomics.
+//  * the other warps are consumers, in groups of eight: warp w of a group decodes
+//    rows 16w .. 16w+15 of a slab on mma.sync (see qmv_slab.cuh), the decode in
+//    registers and the inner product factored per block: y += scale * sum(q * x)
+//    (- min * sum x). At M = 1 two groups take alternate slabs and add their sums
+//    in shared memory at the end of each row tile, in a fixed order;
+//  * a row tile split between CTAs is finished by the CTA that holds its first
+//    k-groups: the others publish their partial sums in the workspace, each word
+//    non-zero so that it is its own completion flag (no fence, no flag word), and
+//    the finishing CTA adds them in CTA order -- deterministic, no float atomics --
+//    and clears them for the next call.
 //
 // Grouped form: the distinct routed experts are found on the device (sorted,
 // each expert once, "A 320B MoE on a free Kaggle TPU", "The decode kernel's
 // cost is not 'distinct experts'"); each becomes a segment whose slabs are
 // streamed once and dotted with every x row routed to it.
 //
-// Every wait (mbarrier, peer flag) is bounded in time; on expiry the CTA latches
+// Every wait (mbarrier, peer partial sum) is bounded in time; on expiry the CTA latches
 // QMV_ETIMEOUT in the device status word and stops.
 #include <cuda_fp16.h>
 #include "qmv_internal.h"
@@ -34,8 +37,11 @@
 
 namespace qmv {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kConsumerWarps = 8;       // warps of one consumer group (16 rows each)
+// M = 1 runs two consumer groups that take alternate slabs (more warps to hide the
+// decode's latency); M > 1 runs one (its per-warp state is larger).
+template <int MT> struct Groups { static constexpr int value = (MT == 1) ? 2 : 1; };
+template <int MT> constexpr int threads_of() { return 32 * (1 + kConsumerWarps * Groups<MT>::value); }
 constexpr int kMaxStages = 16;
 constexpr int kMaxSeg = 64;
 constexpr unsigned long long kTimeoutNs = 1000000000ull;   // 1 s
@@ -97,13 +103,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
-__device__ __forceinline__ uint32_t ld_acquire(const unsigned* p) {
+__device__ __forceinline__ uint32_t ld_relaxed(const unsigned* p) {
   uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_release(unsigned* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_relaxed(unsigned* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// the bits of a partial sum as stored in the workspace: never zero
+__device__ __forceinline__ uint32_t nonzero_bits(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return u == 0u ? 0x80000000u : u;
 }
 __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
@@ -119,20 +130,19 @@ struct KParams {
   int x_off;         // offset of the x slices inside a stage
   int b_off;         // offset of plane B (Q6_K d) inside a stage
   int tbl_off;       // offset of the per-warp scale tables
+  int comb_off;      // offset of the consumer groups' exchange area (two tiles)
   int stage_base;    // offset of stage 0
   int mt;            // partial stride (token columns per partial record)
-  unsigned* flags;   // [num_ctas]
   float* partials;   // [num_ctas][128][mt]
 };
 
 template <int FMT, int MT>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
+__global__ void __launch_bounds__(threads_of<MT>(), 1) stream_kernel(const KParams kp) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const StreamArgs& a = kp.a;
   const Layout& L = a.L;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  uint64_t* fin = empty + kMaxStages;
   volatile int* misc = reinterpret_cast<volatile int*>(smem + 8 * (2 * kMaxStages + 2));
   Seg* segs = reinterpret_cast<Seg*>(smem + 512);
   float2* tbls = reinterpret_cast<float2*>(smem + kp.tbl_off);
@@ -157,9 +167,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
-    mbar_init(fin, kConsumerWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (MT == 1 && warp >= 1) {
+    // the zero pad after x row 0 of every stage (the unit-column B operand of the
+    // sub-blocks a thread does not own is read from it; copies never write it)
+    for (int i = tid - 32; i < kp.stages * (kXZeroBytes / 4); i += (int)blockDim.x - 32) {
+      uint8_t* st = smem + kp.stage_base + (i / (kXZeroBytes / 4)) * kp.stage_bytes;
+      *reinterpret_cast<uint32_t*>(st + kp.x_off + kXZero + 4 * (i % (kXZeroBytes / 4))) = 0u;
+    }
   }
   if (warp == 0) {
     if (a.ids == nullptr) {
@@ -237,45 +254,48 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
   __syncthreads();
   if (misc[0]) return;
 
-  const int64_t nseg = misc[1];
-  const int64_t G = L.k_groups;
-  const int64_t tiles = nseg * L.row_tiles;
-  const int64_t S = tiles * G;
-  const int64_t P = gridDim.x;
-  const int64_t c = blockIdx.x;
-  const int64_t s0 = (c * S) / P, s1 = ((c + 1) * S) / P;
+  const int nseg = misc[1];
+  // slab counts fit in 32 bits (the host refuses larger problems)
+  const int G = (int)L.k_groups;
+  const int RT = (int)L.row_tiles;
+  const int S = nseg * RT * G;
+  const int P = (int)gridDim.x;
+  const int c = (int)blockIdx.x;
+  const int s0 = (int)(((int64_t)c * S) / P), s1 = (int)(((int64_t)(c + 1) * S) / P);
   if (s0 >= s1) return;
+  // the last k-group is narrower than 256 only for formats with 16/32-value blocks
+  constexpr bool kMayBeRagged = (FMT == F_Q8_0 || FMT == F_NVFP4 || FMT == F_FP8);
+  const int kv_last = (int)(L.K - (int64_t)(G - 1) * kSlabK);
 
   if (warp == 0) {
     // ---------------------------- producer --------------------------------
     if (lane != 0) return;
-    // slab s -> (segment, row tile t, k-group g), advanced incrementally (no 64-bit
-    // division inside the loop)
-    int64_t g = s0 % G, t = (s0 / G) % L.row_tiles, seg = (s0 / G) / L.row_tiles;
+    // slab s -> (segment, row tile t, k-group g), advanced incrementally
+    int g = s0 % G, t = (s0 / G) % RT, seg = (s0 / G) / RT;
     int stage = 0;
     uint32_t rphase = 0;          // parity of the current round over the stage ring
-    int64_t it = 0;
+    int it = 0;
+    const uint32_t abytes = (uint32_t)(kSlabRows * L.rec);
+    const uint32_t bbytes = (FMT == F_Q6_K) ? (uint32_t)(kSlabRows * 2) : 0u;
     // The first round of stages: weights first (independent of earlier kernels),
     // then wait for the previous grid, then the activations of those stages.
-    const int64_t first = (s1 - s0) < kp.stages ? (s1 - s0) : kp.stages;
+    const int first = (s1 - s0) < kp.stages ? (s1 - s0) : kp.stages;
     {
-      int64_t gg = g, t2 = t, sg2 = seg;
-      for (int64_t i = 0; i < first; ++i) {
+      int gg = g, t2 = t, sg2 = seg;
+      for (int i = 0; i < first; ++i) {
         const Seg& sg = segs[sg2];
-        uint8_t* st = smem + kp.stage_base + (int)i * kp.stage_bytes;
+        uint8_t* st = smem + kp.stage_base + i * kp.stage_bytes;
         const uint8_t* plane = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + gg * L.group_bytes;
-        const uint32_t abytes = (uint32_t)(kSlabRows * L.rec);
-        const uint32_t bbytes = (FMT == F_Q6_K) ? (uint32_t)(kSlabRows * 2) : 0u;
-        const int64_t kv = (L.K - gg * kSlabK) < kSlabK ? (L.K - gg * kSlabK) : kSlabK;
+        const int kv = (kMayBeRagged && gg == G - 1) ? kv_last : kSlabK;
         const int R = sg.R < MT ? sg.R : MT;
         mbar_expect_tx(&full[i], abytes + bbytes + (uint32_t)(kv * 2) * (uint32_t)R);
-        bulk_g2s(st, plane + t2 * kSlabRows * L.rec, abytes, &full[i]);
-        if (FMT == F_Q6_K) bulk_g2s(st + kp.b_off, plane + L.plane_a + t2 * kSlabRows * 2, bbytes, &full[i]);
-        if (++gg == G) { gg = 0; if (++t2 == L.row_tiles) { t2 = 0; ++sg2; } }
+        bulk_g2s(st, plane + (int64_t)t2 * kSlabRows * L.rec, abytes, &full[i]);
+        if (FMT == F_Q6_K) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t2 * kSlabRows * 2, bbytes, &full[i]);
+        if (++gg == G) { gg = 0; if (++t2 == RT) { t2 = 0; ++sg2; } }
       }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int64_t s = s0; s < s1; ++s, ++it) {
+    for (int s = s0; s < s1; ++s, ++it) {
       if (it >= kp.stages) {      // round r >= 1 waits for the consumers' release of round r-1
         if (!mbar_wait(&empty[stage], rphase ^ 1u, a.status)) { misc[0] = 1; break; }
       }
@@ -283,162 +303,167 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const KParams kp) {
       const Seg& sg = segs[seg];
       uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
       const uint8_t* plane = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + g * L.group_bytes;
-      const uint32_t abytes = (uint32_t)(kSlabRows * L.rec);
-      const uint32_t bbytes = (FMT == F_Q6_K) ? (uint32_t)(kSlabRows * 2) : 0u;
-      const int64_t kv = (L.K - g * kSlabK) < kSlabK ? (L.K - g * kSlabK) : kSlabK;
+      const int kv = (kMayBeRagged && g == G - 1) ? kv_last : kSlabK;
       const uint32_t xbytes = (uint32_t)(kv * 2);
       const int R = sg.R < MT ? sg.R : MT;
       if (it >= first) {
         mbar_expect_tx(&full[stage], abytes + bbytes + xbytes * (uint32_t)R);
-        bulk_g2s(st, plane + t * kSlabRows * L.rec, abytes, &full[stage]);
-        if (FMT == F_Q6_K) bulk_g2s(st + kp.b_off, plane + L.plane_a + t * kSlabRows * 2, bbytes, &full[stage]);
+        bulk_g2s(st, plane + (int64_t)t * kSlabRows * L.rec, abytes, &full[stage]);
+        if (FMT == F_Q6_K) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t * kSlabRows * 2, bbytes, &full[stage]);
       }
       for (int r = 0; r < R; ++r)
-        bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + g * kSlabK, xbytes,
+        bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)g * kSlabK, xbytes,
                  &full[stage]);
       if (++stage == kp.stages) { stage = 0; rphase ^= 1u; }
-      if (++g == G) { g = 0; if (++t == L.row_tiles) { t = 0; ++seg; } }
+      if (++g == G) { g = 0; if (++t == RT) { t = 0; ++seg; } }
     }
     // drain: copies issued into stages the consumers may not have waited for
     if (misc[0]) {
-      const int64_t issued = it;
-      for (int64_t j = (issued > kp.stages ? issued - kp.stages : 0); j < issued; ++j)
+      const int issued = it;
+      for (int j = (issued > kp.stages ? issued - kp.stages : 0); j < issued; ++j)
         (void)mbar_wait(&full[j % kp.stages], (uint32_t)((j / kp.stages) & 1), a.status);
     }
     return;
   }
 
   // ------------------------------ consumers ---------------------------------
-  const int w = warp - 1;               // this warp owns rows 16w .. 16w+15 of a slab
+  // After an abort (a wait that timed out, here or in another warp) a warp still
+  // walks its slab sequence but skips the waits, the arithmetic and the stores, so
+  // that every consumer warp reaches every tile end (the groups meet at a named
+  // barrier there).
+  constexpr int NG = Groups<MT>::value;
+  const int cwarp = warp - 1;
+  const int grp = cwarp / kConsumerWarps;   // group grp takes the slabs s with (s - s0) % NG == grp
+  const int w = cwarp % kConsumerWarps;     // this warp owns rows 16w .. 16w+15 of a slab
   const int g = lane >> 2, tq = lane & 3;
-  const int ctid = tid - 32;            // 0..255
+  const int gtid = tid - 32 - grp * 32 * kConsumerWarps;   // 0..255 within the group
   float2* tbl = tbls + w * (16 * kTblStride);
+  const int rA = 16 * w + g, rB = rA + 8;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  int nfin = 0;                          // phases of the `fin` rendezvous used so far
-  int64_t gk = s0 % G, T = s0 / G;
-  int64_t tt = T % L.row_tiles, seg = T / L.row_tiles;
+  int T = s0 / G;                        // current tile (over segments x row tiles)
+  int tt = T % RT, seg = T / RT;
   int stage = 0;
   uint32_t fphase = 0;                   // parity of the full barrier for this stage round
-  for (int64_t s = s0; s < s1; ++s) {
-    if (misc[0]) break;
+  bool aborted = false;
+  bool my_turn = (grp == 0);             // NG = 2: this group takes slab s
+  for (int s = s0; s < s1;) {
+    aborted = aborted || misc[0];
     const Seg& sg = segs[seg];
     const int R = sg.R < MT ? sg.R : MT;
-    if (!mbar_wait(&full[stage], fphase, a.status)) { misc[0] = 1; break; }
-    const uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
     const bool has_x = g < R;
-    const uint8_t* xrow0 = st + kp.x_off;
-    // the last k-group may be narrower than 256: its padded blocks are zero and
-    // the x beyond K is never copied, so the stale tail of each x row is zeroed
-    // (by one thread of each warp, before that warp reads it)
-    const int64_t kv = (L.K - gk * kSlabK) < kSlabK ? (L.K - gk * kSlabK) : kSlabK;
-    if (kv < kSlabK) {
-      if (has_x && tq == 0) {
-        uint8_t* xw = const_cast<uint8_t*>(xrow0) + g * kXStride;
-        for (int64_t o = kv * 2; o < kSlabK * 2; o += 4) *reinterpret_cast<uint32_t*>(xw + o) = 0u;
+    const int head = T * G, tail = head + G;
+    const int send = tail < s1 ? tail : s1;
+    for (; s < send; ++s) {
+      if (my_turn && !aborted) {
+        if (!mbar_wait(&full[stage], fphase, a.status)) {
+          misc[0] = 1;
+          aborted = true;
+        } else {
+          const uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
+          const uint8_t* xrow0 = st + kp.x_off;
+          // a last k-group narrower than 256: its padded blocks are zero and the x
+          // beyond K is never copied, so the stale tail of each x row is zeroed (by
+          // one thread of each warp, before that warp reads it)
+          if (kMayBeRagged && s == tail - 1 && kv_last < kSlabK) {
+            if (has_x && tq == 0) {
+              uint8_t* xw = const_cast<uint8_t*>(xrow0) + g * kXStride;
+              for (int o = kv_last * 2; o < kSlabK * 2; o += 4) *reinterpret_cast<uint32_t*>(xw + o) = 0u;
+            }
+            __syncwarp();
+          }
+          if (MT == 1) {
+            Slab<FMT, 1>::run(st, st + kp.b_off, xrow0, R, w, lane, tbl, acc);
+          } else {
+            Slab<FMT, MT>::run(st, st + kp.b_off, xrow0 + (has_x ? g : 0) * kXStride, R, w, lane, tbl, acc);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[stage]);
+        }
       }
-      __syncwarp();
+      if (NG > 1) my_turn = !my_turn;
+      if (++stage == kp.stages) { stage = 0; fphase ^= 1u; }
     }
-    if (MT == 1) {
-      Slab<FMT, 1>::run(st, st + kp.b_off, xrow0, R, w, lane, tbl, acc);
-    } else {
-      Slab<FMT, MT>::run(st, st + kp.b_off, xrow0 + (has_x ? g : 0) * kXStride, R, w, lane, tbl, acc);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == kp.stages) { stage = 0; fphase ^= 1u; }
 
-    // advance (k-group, tile, segment); the tile ends when the k-group wraps
-    const int64_t Tcur = T, tcur = tt;
-    const bool tile_end = (s + 1 == s1) || (gk + 1 == G);
-    if (++gk == G) { gk = 0; ++T; if (++tt == L.row_tiles) { tt = 0; ++seg; } }
-    if (!tile_end) continue;
-
-    // ---- flush tile T: this thread owns rows rA, rB of it and tokens 2tq, 2tq+1 ----
-    asm volatile("griddepcontrol.wait;" ::: "memory");   // workspace and y after earlier kernels
-    if (MT == 1) {
-      // unit columns: add the quad's partial sums of rows rA, rB (token 0)
-      float vA = acc[0], vB = acc[1];
-      vA += __shfl_xor_sync(0xffffffffu, vA, 1);
-      vB += __shfl_xor_sync(0xffffffffu, vB, 1);
-      vA += __shfl_xor_sync(0xffffffffu, vA, 2);
-      vB += __shfl_xor_sync(0xffffffffu, vB, 2);
-      acc[0] = vA; acc[1] = 0.f; acc[2] = vB; acc[3] = 0.f;
+    // ---- end of tile T: this thread owns rows rA, rB of it and tokens 2tq, 2tq+1 ----
+    if (NG > 1) {
+      // the groups' sums of this tile meet in shared memory (one buffer per tile
+      // parity, so a group can never overwrite a buffer that is still being read)
+      float4* cmb = reinterpret_cast<float4*>(smem + kp.comb_off) + (T & 1) * (32 * kConsumerWarps) + gtid;
+      if (grp != 0) *cmb = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps * NG) : "memory");
+      if (grp == 0) {
+        const float4 o = *cmb;
+        acc[0] += o.x; acc[1] += o.y; acc[2] += o.z; acc[3] += o.w;
+      }
     }
-    const int64_t head = Tcur * G, tail = (Tcur + 1) * G;
-    const bool full_cover = (s0 <= head) && (s1 >= tail);
-    const bool reducer = (s0 <= head);
-    const int64_t t = tcur;
-    const int rA = 16 * w + g, rB = rA + 8;
-    const uint8_t* extras = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + L.k_groups * L.group_bytes;
-    bool ok = true;
-    if (!full_cover && !reducer) {
-      float* part = kp.partials + c * (kSlabRows * kp.mt);
+    if (grp == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");   // workspace and y after earlier kernels
+      if (MT == 1) {
+        // unit columns: add the quad's partial sums of rows rA, rB (token 0)
+        float vA = acc[0], vB = acc[1];
+        vA += __shfl_xor_sync(0xffffffffu, vA, 1);
+        vB += __shfl_xor_sync(0xffffffffu, vB, 1);
+        vA += __shfl_xor_sync(0xffffffffu, vA, 2);
+        vB += __shfl_xor_sync(0xffffffffu, vB, 2);
+        acc[0] = vA; acc[1] = 0.f; acc[2] = vB; acc[3] = 0.f;
+      }
+      const bool full_cover = (s0 <= head) && (s1 >= tail);
+      const bool reducer = (s0 <= head);
+      if (!full_cover && !reducer) {
+        // peer: publish the partial sums. Each word is its own completion flag: a
+        // stored word is never zero (+0.0 is stored as -0.0, which adds the same),
+        // and the reducer waits for each word to become non-zero -- no fence, no flag.
+        if (!aborted) {
+          unsigned* part = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)c * (kSlabRows * kp.mt);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
-        if (tok < R) part[row * kp.mt + tok] = acc[e];
-      }
-      __threadfence();
-    } else if (!full_cover && reducer) {
-      for (int64_t cp = c + 1; cp < P; ++cp) {
-        const int64_t ps0 = (cp * S) / P, ps1 = ((cp + 1) * S) / P;
-        if (ps0 >= tail) break;
-        if (ps0 >= ps1) continue;           // an empty range publishes nothing
-        const unsigned* flag = kp.flags + cp;
-        if (ld_acquire(flag) == 0u) {
-          const unsigned long long t0 = globaltimer();
-          while (ld_acquire(flag) == 0u) {
-            if (globaltimer() - t0 > kTimeoutNs) { atomicOr(a.status, kStatTimeout); ok = false; break; }
+          for (int e = 0; e < 4; ++e) {
+            const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+            if (tok < R) st_relaxed(part + row * kp.mt + tok, nonzero_bits(acc[e]));
           }
         }
-        if (!ok) break;
-        const float* part = kp.partials + cp * (kSlabRows * kp.mt);
+      } else if (!full_cover && !aborted) {
+        // reducer: add the peers' partial sums in CTA order, clearing each word after
+        // reading it (the workspace is all zero again when the call ends)
+        for (int cp = c + 1; cp < P && !aborted; ++cp) {
+          const int ps0 = (int)(((int64_t)cp * S) / P), ps1 = (int)(((int64_t)(cp + 1) * S) / P);
+          if (ps0 >= tail) break;
+          if (ps0 >= ps1) continue;           // an empty range publishes nothing
+          unsigned* part = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)cp * (kSlabRows * kp.mt);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+            if (tok >= R) continue;
+            unsigned* wp = part + row * kp.mt + tok;
+            uint32_t u = ld_relaxed(wp);
+            if (u == 0u) {
+              const unsigned long long t0 = globaltimer();
+              while ((u = ld_relaxed(wp)) == 0u) {
+                if (globaltimer() - t0 > kTimeoutNs) break;
+              }
+              if (u == 0u) { atomicOr(a.status, kStatTimeout); misc[0] = 1; aborted = true; break; }
+            }
+            st_relaxed(wp, 0u);
+            acc[e] += __uint_as_float(u);
+          }
+        }
+      }
+      if (!aborted && (full_cover || reducer)) {
+        const uint8_t* extras = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + L.k_groups * L.group_bytes;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
-          if (tok < R) acc[e] += __ldcg(part + row * kp.mt + tok);
+          const int64_t n = (int64_t)tt * kSlabRows + row;
+          if (tok >= R || n >= L.N) continue;
+          float v = acc[e];
+          if (FMT == F_NVFP4) v *= *reinterpret_cast<const float*>(extras);
+          if (FMT == F_FP8) v *= reinterpret_cast<const float*>(extras)[n];
+          a.y[(int64_t)sg.yrow[tok] * L.N + n] = v;
         }
       }
-    }
-    if (ok && (full_cover || reducer)) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
-        const int64_t n = t * kSlabRows + row;
-        if (tok >= R || n >= L.N) continue;
-        float v = acc[e];
-        if (FMT == F_NVFP4) v *= *reinterpret_cast<const float*>(extras);
-        if (FMT == F_FP8) v *= reinterpret_cast<const float*>(extras)[n];
-        a.y[(int64_t)sg.yrow[tok] * L.N + n] = v;
-      }
-    }
-    if (!ok) { misc[0] = 1; break; }
-    if (!full_cover) {
-      // rendezvous of the consumer warps: every partial is written (peer) or every
-      // peer partial has been read (reducer); then one thread publishes / resets
-      __syncwarp();
-      if (lane == 0) mbar_arrive(fin);
-      if (ctid == 0) {
-        if (!mbar_wait(fin, (uint32_t)(nfin & 1), a.status)) {
-          misc[0] = 1;
-        } else if (!reducer) {
-          st_release(kp.flags + c, 1u);
-        } else {
-          for (int64_t cp = c + 1; cp < P; ++cp) {
-            const int64_t ps0 = (cp * S) / P, ps1 = ((cp + 1) * S) / P;
-            if (ps0 >= tail) break;
-            if (ps0 < ps1) kp.flags[cp] = 0u;
-          }
-        }
-      }
-      ++nfin;
-      // the next rendezvous may only start after this one completed
-      if (ctid != 0 && lane == 0) {
-        if (!mbar_wait(fin, (uint32_t)((nfin - 1) & 1), a.status)) misc[0] = 1;
-      }
-      __syncwarp();
     }
     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    ++T;
+    if (++tt == RT) { tt = 0; ++seg; }
   }
 }
 
@@ -449,9 +474,7 @@ WsPlan ws_plan_stream(int M, int64_t tiles_max, int num_ctas) {
   (void)tiles_max;
   WsPlan p;
   const int mt = (M <= 1) ? 1 : 8;
-  p.counters_off = 256;
-  p.counters_bytes = align_up((int64_t)num_ctas * 4, 256);
-  p.partials_off = p.counters_off + p.counters_bytes;
+  p.partials_off = 0;
   p.partials_bytes = align_up((int64_t)num_ctas * kSlabRows * mt * 4, 256);
   p.total = p.partials_off + p.partials_bytes;
   return p;
@@ -476,7 +499,9 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   kp.mt = MT;
   kp.tbl_off = 512 + kMaxSeg * (int)sizeof(Seg);
   const int tbl_bytes = kConsumerWarps * 16 * kTblStride * (int)sizeof(float2);
-  kp.stage_base = (int)align_up(kp.tbl_off + tbl_bytes, 1024);
+  kp.comb_off = (int)align_up(kp.tbl_off + tbl_bytes, 16);
+  const int comb_bytes = (Groups<MT>::value > 1) ? 2 * 32 * kConsumerWarps * 4 * (int)sizeof(float) : 0;
+  kp.stage_base = (int)align_up(kp.comb_off + comb_bytes, 1024);
   const int abytes = kSlabRows * a.L.rec;
   kp.b_off = (int)align_up(abytes, 128);
   const int bbytes = (FMT == F_Q6_K) ? kSlabRows * 2 : 0;
@@ -485,8 +510,9 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   kp.stages = (smem_max - kp.stage_base) / kp.stage_bytes;
   if (kp.stages > kMaxStages) kp.stages = kMaxStages;
   if (kp.stages < 2) return cudaErrorInvalidConfiguration;
+  const int64_t pairs = (int64_t)a.M * a.topk;
+  if (!slab_count_ok(a.L, a.ids ? (pairs < a.L.E ? pairs : a.L.E) : 1)) return cudaErrorInvalidValue;
   const WsPlan plan = ws_plan_stream(MT, 0, a.num_ctas);
-  kp.flags = reinterpret_cast<unsigned*>(a.ws + plan.counters_off);
   kp.partials = reinterpret_cast<float*>(a.ws + plan.partials_off);
   const int smem = kp.stage_base + kp.stages * kp.stage_bytes;
   // opt in to the large dynamic shared memory once per device (not per launch, so
@@ -500,12 +526,12 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.num_ctas);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_of<MT>());
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
   // One CTA per SM and at most one CTA per SM fits, so every CTA of the grid is
   // resident once the previous kernel's CTAs have left: a reducer's bounded wait
-  // on its peers' flags ends. Programmatic stream serialization lets this grid's
+  // on its peers' partial sums ends. Programmatic stream serialization lets this grid's
   // prologue overlap the previous kernel's tail (see griddepcontrol in the kernel).
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -115,11 +115,11 @@ qmv_status qmv_dequant(qmv_fmt fmt, const void* packed, int64_t N, int64_t K, in
 
 /* Workspace bytes needed by an entry point for these sizes (host-only query; it
  * reads the SM count of the current device). The workspace must be zero-filled
- * once before its first use. It holds one flag word per CTA (bytes 256 ..
- * 256 + 4 * SM count) and the partial sums of row tiles split between CTAs; a
- * call that returns without a device status error leaves every flag word zero
- * again, so the same workspace serves the next call as is. After a device status
- * error, zero-fill it again. Calls sharing one workspace must not overlap. */
+ * once before its first use. It holds the partial sums of row tiles split
+ * between CTAs (a zero word means "not yet written"); a call that returns
+ * without a device status error leaves the whole workspace zero again, so the
+ * same workspace serves the next call as is. After a device status error,
+ * zero-fill it again. Calls sharing one workspace must not overlap. */
 size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, int64_t E,
                           int topk);
 
@@ -140,17 +140,17 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
  * the device for its own pool, or a plugin interface that passes only input and
  * output pointers -- and that must not call cudaMalloc/cudaFree on the decode
  * path, since those can fail under a full pool or synchronize the device.
- * The split-K flag words and partial sums live instead in one fixed array of
+ * The split-K partial sums live instead in one fixed array of
  * QMV_STATIC_SCRATCH_BYTES in the library's device image.
  * Set-up: the first call on each device (with that device current) looks up the
  * array's device address; make that first call before any stream capture.
  * Every call on a device shares the one array, which keeps what the last call
- * left: each call first clears the flag words on `stream` (cudaMemsetAsync, no
+ * left: each call first clears the words it uses on `stream` (cudaMemsetAsync, no
  * allocation). Calls that overlap in time (on other streams or host threads)
  * race on the array; the caller must serialize them.
  * Returns QMV_EWORKSPACE when the scratch this device needs,
  * qmv_workspace_size(QMV_ENTRY_GEMV, fmt, M, N, K, 1, 1), exceeds
- * QMV_STATIC_SCRATCH_BYTES (M = 2..8 on a device of more than 255 SMs).
+ * QMV_STATIC_SCRATCH_BYTES (M = 2..8 on a device of more than 256 SMs).
  * Otherwise arguments, results and errors as qmv_gemv. */
 qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y,
                             int M, int64_t N, int64_t K, cudaStream_t stream);

@@ -105,8 +105,8 @@ def test_gemv_parity(q, fmt, N, K, M):
     assert route == q.FORMATS[fmt] * 100 + (1 if M == 1 else 2)
     e = norm_err(y, ref, den)
     assert e <= TOL, e
-    # the per-CTA flag words are back at zero for the next call
-    assert int(ws[256:256 + 4 * _sms()].count_nonzero()) == 0
+    # the workspace is all zero again for the next call
+    assert int(ws.count_nonzero()) == 0
 
 
 def test_gemv_tiny_config_q8_0(q):
@@ -174,7 +174,7 @@ def test_grouped_parity(q, fmt, M, topk, E, x_per_pair):
     y = y.cpu().numpy()
     assert q.qmv_device_status() == 0
     assert norm_err(y, Y, Dn) <= TOL
-    assert int(ws[256:256 + 4 * _sms()].count_nonzero()) == 0
+    assert int(ws.count_nonzero()) == 0
 
 
 # ---------------------------------------------------------------------------
