@@ -7,17 +7,17 @@
 // reads halved latency). So the kernel is built around streaming the packed
 // weights from HBM exactly once per call for all M rows of x:
 //
-//  * persistent grid, one CTA per SM; the work is the list of slabs
+//  * persistent grid, one CTA per SM per call; the work is the list of slabs
 //    (segment, 128-row tile, 256-value k-group) in tile-major order, cut into
 //    equal contiguous ranges, one per CTA (split-K at slab granularity);
 //  * warp 0 is a producer: one elected lane streams each slab (and the matching
 //    256-value slice of every x row routed to it) into a ring of shared-memory
 //    stages with cp.async.bulk, completion tracked by mbarriers; no multicast;
-//  * the other warps are consumers, in groups of eight: warp w of a group decodes
-//    rows 16w .. 16w+15 of a slab on mma.sync (see qmv_slab.cuh), the decode in
-//    registers and the inner product factored per block: y += scale * sum(q * x)
-//    (- min * sum x). At M = 1 two groups take alternate slabs and add their sums
-//    in shared memory at the end of each row tile, in a fixed order;
+//  * the other eight warps are consumers: warp w decodes rows 16w .. 16w+15 of a
+//    slab on mma.sync (see qmv_slab.cuh), the decode in registers and the inner
+//    product factored per block: y += scale * sum(q * x) (- min * sum x);
+//  * at M = 1 a CTA takes half an SM, so that the next call's CTAs are resident
+//    beside the running ones and copy their first weight slabs meanwhile;
 //  * a row tile split between CTAs is finished by the CTA that holds its first
 //    k-groups: the others publish their partial sums in the workspace, each word
 //    non-zero so that it is its own completion flag (no fence, no flag word), and
@@ -37,11 +37,13 @@
 
 namespace qmv {
 
-constexpr int kConsumerWarps = 8;       // warps of one consumer group (16 rows each)
-// M = 1 runs two consumer groups that take alternate slabs (more warps to hide the
-// decode's latency); M > 1 runs one (its per-warp state is larger).
-template <int MT> struct Groups { static constexpr int value = (MT == 1) ? 2 : 1; };
-template <int MT> constexpr int threads_of() { return 32 * (1 + kConsumerWarps * Groups<MT>::value); }
+constexpr int kConsumerWarps = 8;       // consumer warps (16 rows of a slab each)
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+// CTAs resident per SM. At M = 1 a CTA takes half of the SM (shared memory and
+// registers), so that the next call's CTA is resident beside the running one and
+// runs its prologue and first weight copies during the running call's compute;
+// the M > 1 kernels need more registers per thread and take a whole SM.
+template <int MT> constexpr int ctas_per_sm() { return MT == 1 ? 2 : 1; }
 constexpr int kMaxStages = 16;
 constexpr int kMaxSeg = 64;
 constexpr unsigned long long kTimeoutNs = 1000000000ull;   // 1 s
@@ -130,14 +132,13 @@ struct KParams {
   int x_off;         // offset of the x slices inside a stage
   int b_off;         // offset of plane B (Q6_K d) inside a stage
   int tbl_off;       // offset of the per-warp scale tables
-  int comb_off;      // offset of the consumer groups' exchange area (two tiles)
   int stage_base;    // offset of stage 0
   int mt;            // partial stride (token columns per partial record)
   float* partials;   // [num_ctas][128][mt]
 };
 
 template <int FMT, int MT>
-__global__ void __launch_bounds__(threads_of<MT>(), 1) stream_kernel(const KParams kp) {
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(const KParams kp) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const StreamArgs& a = kp.a;
   const Layout& L = a.L;
@@ -328,15 +329,9 @@ __global__ void __launch_bounds__(threads_of<MT>(), 1) stream_kernel(const KPara
 
   // ------------------------------ consumers ---------------------------------
   // After an abort (a wait that timed out, here or in another warp) a warp still
-  // walks its slab sequence but skips the waits, the arithmetic and the stores, so
-  // that every consumer warp reaches every tile end (the groups meet at a named
-  // barrier there).
-  constexpr int NG = Groups<MT>::value;
-  const int cwarp = warp - 1;
-  const int grp = cwarp / kConsumerWarps;   // group grp takes the slabs s with (s - s0) % NG == grp
-  const int w = cwarp % kConsumerWarps;     // this warp owns rows 16w .. 16w+15 of a slab
+  // walks its slab sequence but skips the waits, the arithmetic and the stores.
+  const int w = warp - 1;               // this warp owns rows 16w .. 16w+15 of a slab
   const int g = lane >> 2, tq = lane & 3;
-  const int gtid = tid - 32 - grp * 32 * kConsumerWarps;   // 0..255 within the group
   float2* tbl = tbls + w * (16 * kTblStride);
   const int rA = 16 * w + g, rB = rA + 8;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -345,7 +340,6 @@ __global__ void __launch_bounds__(threads_of<MT>(), 1) stream_kernel(const KPara
   int stage = 0;
   uint32_t fphase = 0;                   // parity of the full barrier for this stage round
   bool aborted = false;
-  bool my_turn = (grp == 0);             // NG = 2: this group takes slab s
   for (int s = s0; s < s1;) {
     aborted = aborted || misc[0];
     const Seg& sg = segs[seg];
@@ -354,7 +348,7 @@ __global__ void __launch_bounds__(threads_of<MT>(), 1) stream_kernel(const KPara
     const int head = T * G, tail = head + G;
     const int send = tail < s1 ? tail : s1;
     for (; s < send; ++s) {
-      if (my_turn && !aborted) {
+      if (!aborted) {
         if (!mbar_wait(&full[stage], fphase, a.status)) {
           misc[0] = 1;
           aborted = true;
@@ -380,23 +374,11 @@ __global__ void __launch_bounds__(threads_of<MT>(), 1) stream_kernel(const KPara
           if (lane == 0) mbar_arrive(&empty[stage]);
         }
       }
-      if (NG > 1) my_turn = !my_turn;
       if (++stage == kp.stages) { stage = 0; fphase ^= 1u; }
     }
 
     // ---- end of tile T: this thread owns rows rA, rB of it and tokens 2tq, 2tq+1 ----
-    if (NG > 1) {
-      // the groups' sums of this tile meet in shared memory (one buffer per tile
-      // parity, so a group can never overwrite a buffer that is still being read)
-      float4* cmb = reinterpret_cast<float4*>(smem + kp.comb_off) + (T & 1) * (32 * kConsumerWarps) + gtid;
-      if (grp != 0) *cmb = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps * NG) : "memory");
-      if (grp == 0) {
-        const float4 o = *cmb;
-        acc[0] += o.x; acc[1] += o.y; acc[2] += o.z; acc[3] += o.w;
-      }
-    }
-    if (grp == 0) {
+    {
       asm volatile("griddepcontrol.wait;" ::: "memory");   // workspace and y after earlier kernels
       if (MT == 1) {
         // unit columns: add the quad's partial sums of rows rA, rB (token 0)
@@ -494,14 +476,18 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   if (err != cudaSuccess) return err;
   err = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (err != cudaSuccess) return err;
+  int smem_sm = 0;
+  err = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (err != cudaSuccess) return err;
+  // per CTA: its share of the SM less the 1 KB the hardware reserves per CTA
+  const int smem_cta = smem_sm / ctas_per_sm<MT>() - 1024;
+  if (smem_cta < smem_max) smem_max = smem_cta;
   KParams kp;
   kp.a = a;
   kp.mt = MT;
   kp.tbl_off = 512 + kMaxSeg * (int)sizeof(Seg);
   const int tbl_bytes = kConsumerWarps * 16 * kTblStride * (int)sizeof(float2);
-  kp.comb_off = (int)align_up(kp.tbl_off + tbl_bytes, 16);
-  const int comb_bytes = (Groups<MT>::value > 1) ? 2 * 32 * kConsumerWarps * 4 * (int)sizeof(float) : 0;
-  kp.stage_base = (int)align_up(kp.comb_off + comb_bytes, 1024);
+  kp.stage_base = (int)align_up(kp.tbl_off + tbl_bytes, 1024);
   const int abytes = kSlabRows * a.L.rec;
   kp.b_off = (int)align_up(abytes, 128);
   const int bbytes = (FMT == F_Q6_K) ? kSlabRows * 2 : 0;
@@ -526,13 +512,14 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.num_ctas);
-  cfg.blockDim = dim3(threads_of<MT>());
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
-  // One CTA per SM and at most one CTA per SM fits, so every CTA of the grid is
-  // resident once the previous kernel's CTAs have left: a reducer's bounded wait
-  // on its peers' partial sums ends. Programmatic stream serialization lets this grid's
-  // prologue overlap the previous kernel's tail (see griddepcontrol in the kernel).
+  // The grid has at most one CTA per SM and ctas_per_sm() CTAs fit on an SM, so
+  // every CTA of the grid is resident at once as soon as the previous kernel's
+  // CTAs have left (none of which waits on this grid): a reducer's bounded wait on
+  // its peers' partial sums ends. Programmatic stream serialization lets this
+  // grid's prologue overlap the previous kernel (see griddepcontrol in the kernel).
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
