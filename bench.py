@@ -112,7 +112,9 @@ def measured_peaks():
 def kernel_source_hash():
     h = hashlib.sha256()
     for rel in ("block_quantized_weight_fly_gb300/csrc/qmv_stream.cu",
-                "block_quantized_weight_fly_gb300/csrc/qmv_layout.cuh"):
+                "block_quantized_weight_fly_gb300/csrc/qmv_slab.cuh",
+                "block_quantized_weight_fly_gb300/csrc/qmv_layout.cuh",
+                "block_quantized_weight_fly_gb300/csrc/qmv_internal.h"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -271,16 +273,20 @@ class DeviceWorkload:
                 q.qmv_gemv(self.fmt, self.packed[c][i], self.x[i], N, K, self.ws[i], y=self.y[i])
 
     def steps_per_graph(self):
-        """Steps captured per CUDA graph: one for big steps, more for small ones so
-        that replaying graphs is not host-bound (about 200 MB of weights per graph)."""
-        return max(1, min(256, int(200e6 // max(self.step_bytes(0), 1))))
+        """Steps captured per CUDA graph: about 1 GB of weights per graph (at most
+        256 steps), so that consecutive calls stay inside one graph, where each
+        call's prologue overlaps the previous call (programmatic launch edges),
+        and replaying graphs is never host-bound."""
+        return max(1, min(256, math.ceil(1e9 / max(self.step_bytes(0), 1))))
 
     def graphs(self, K):
         """CUDA graphs of `u` consecutive steps each (copy index = step % copies,
         routing index = step % 64), and one graph of the K % u remaining steps."""
-        u = self.steps_per_graph()
         period = self.copies if not self.tower else math.lcm(self.copies, len(self.ids))
         period = min(period, 256)
+        # whole rotation periods per graph, so that graph boundaries keep the
+        # distance between two uses of one weight copy
+        u = min(256, period * -(-self.steps_per_graph() // period))
         ngraphs = max(1, -(-period // u))
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -386,7 +392,7 @@ def run_device(args, rank, world, dev):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "f16" if wl.fmt in ("nvfp4", "fp8_row") else "bf16",
         "data": "synthetic (seeded N(0,0.02) weights quantized by the library, bf16 N(0,1) activations)",
         "config": {
             "workload": WORKLOADS[args.workload]["desc"],
@@ -398,6 +404,8 @@ def run_device(args, rank, world, dev):
             "l2": f"inputs larger than L2: weights rotated over {wl.copies} copies "
                   f"({wl.copies} x {int(bytes_per_step / 1e6)} MB per cycle)",
             "graph": f"CUDA graphs of {u} step(s) each",
+            "arithmetic": "weights decoded exactly to " + ("f16" if wl.fmt in ("nvfp4", "fp8_row") else "bf16")
+                          + ", products on mma.sync, fp32 accumulation",
             "parallelism": "replicas" if world > 1 else "single-gpu",
         },
         "pct_of_peak": round(100.0 * value / world / peak, 2),
