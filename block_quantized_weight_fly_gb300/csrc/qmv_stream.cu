@@ -347,6 +347,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     const bool has_x = g < R;
     const int head = T * G, tail = head + G;
     const int send = tail < s1 ? tail : s1;
+    const bool full_cover = (s0 <= head) && (s1 >= tail);
+    const bool reducer = (s0 <= head);
     for (; s < send; ++s) {
       if (!aborted) {
         if (!mbar_wait(&full[stage], fphase, a.status)) {
@@ -389,8 +391,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         vB += __shfl_xor_sync(0xffffffffu, vB, 2);
         acc[0] = vA; acc[1] = 0.f; acc[2] = vB; acc[3] = 0.f;
       }
-      const bool full_cover = (s0 <= head) && (s1 >= tail);
-      const bool reducer = (s0 <= head);
       if (!full_cover && !reducer) {
         // peer: publish the partial sums. Each word is its own completion flag: a
         // stored word is never zero (+0.0 is stored as -0.0, which adds the same),
@@ -405,27 +405,49 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         }
       } else if (!full_cover && !aborted) {
         // reducer: add the peers' partial sums in CTA order, clearing each word after
-        // reading it (the workspace is all zero again when the call ends)
-        for (int cp = c + 1; cp < P && !aborted; ++cp) {
-          const int ps0 = (int)(((int64_t)cp * S) / P), ps1 = (int)(((int64_t)(cp + 1) * S) / P);
-          if (ps0 >= tail) break;
-          if (ps0 >= ps1) continue;           // an empty range publishes nothing
-          unsigned* part = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)cp * (kSlabRows * kp.mt);
+        // reading it (the workspace is all zero again when the call ends). The words
+        // of up to kPeerBatch peers are loaded at once, so their latencies overlap.
+        constexpr int kPeerBatch = 4;
+        int cp = c + 1;
+        while (cp < P && !aborted) {
+          int ids[kPeerBatch];
+          int nb = 0;
+          for (; cp < P && nb < kPeerBatch; ++cp) {
+            const int ps0 = (int)(((int64_t)cp * S) / P), ps1 = (int)(((int64_t)(cp + 1) * S) / P);
+            if (ps0 >= tail) { cp = P; break; }
+            if (ps0 < ps1) ids[nb++] = cp;      // an empty range publishes nothing
+          }
+          uint32_t u[kPeerBatch][4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
-            if (tok >= R) continue;
-            unsigned* wp = part + row * kp.mt + tok;
-            uint32_t u = ld_relaxed(wp);
-            if (u == 0u) {
-              const unsigned long long t0 = globaltimer();
-              while ((u = ld_relaxed(wp)) == 0u) {
-                if (globaltimer() - t0 > kTimeoutNs) break;
-              }
-              if (u == 0u) { atomicOr(a.status, kStatTimeout); misc[0] = 1; aborted = true; break; }
+          for (int k = 0; k < kPeerBatch; ++k) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+              u[k][e] = 0u;
+              if (k < nb && tok < R)
+                u[k][e] = ld_relaxed(reinterpret_cast<const unsigned*>(kp.partials) +
+                                     (int64_t)ids[k] * (kSlabRows * kp.mt) + row * kp.mt + tok);
             }
-            st_relaxed(wp, 0u);
-            acc[e] += __uint_as_float(u);
+          }
+#pragma unroll
+          for (int k = 0; k < kPeerBatch; ++k) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+              if (k >= nb || tok >= R || aborted) continue;
+              unsigned* wp = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)ids[k] * (kSlabRows * kp.mt) +
+                             row * kp.mt + tok;
+              uint32_t v = u[k][e];
+              if (v == 0u) {
+                const unsigned long long t0 = globaltimer();
+                while ((v = ld_relaxed(wp)) == 0u) {
+                  if (globaltimer() - t0 > kTimeoutNs) break;
+                }
+                if (v == 0u) { atomicOr(a.status, kStatTimeout); misc[0] = 1; aborted = true; continue; }
+              }
+              st_relaxed(wp, 0u);
+              acc[e] += __uint_as_float(v);
+            }
           }
         }
       }
@@ -486,7 +508,8 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   kp.a = a;
   kp.mt = MT;
   kp.tbl_off = 512 + kMaxSeg * (int)sizeof(Seg);
-  const int tbl_bytes = kConsumerWarps * 16 * kTblStride * (int)sizeof(float2);
+  // the per-warp scale tables serve the token-column (M > 1) decoders only
+  const int tbl_bytes = (MT > 1) ? kConsumerWarps * 16 * kTblStride * (int)sizeof(float2) : 0;
   kp.stage_base = (int)align_up(kp.tbl_off + tbl_bytes, 1024);
   const int abytes = kSlabRows * a.L.rec;
   kp.b_off = (int)align_up(abytes, 128);
