@@ -262,16 +262,18 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   const int S = nseg * RT * G;
   const int P = (int)gridDim.x;
   const int c = (int)blockIdx.x;
-  const int s0 = (int)(((int64_t)c * S) / P), s1 = (int)(((int64_t)(c + 1) * S) / P);
+  // range start of CTA i: floor(i * S / P), in 32-bit arithmetic (S = Sq * P + Sr;
+  // i * Sr < P * P), so that the peer loops below stay cheap
+  const int Sq = S / P, Sr = S % P;
+  auto range_start = [&](int i) { return i * Sq + (i * Sr) / P; };
+  const int s0 = range_start(c), s1 = range_start(c + 1);
   if (s0 >= s1) return;
   // the last k-group is narrower than 256 only for formats with 16/32-value blocks
   constexpr bool kMayBeRagged = (FMT == F_Q8_0 || FMT == F_NVFP4 || FMT == F_FP8);
   const int kv_last = (int)(L.K - (int64_t)(G - 1) * kSlabK);
 
-  if (warp == 0) {
-    // ---------------------------- producer --------------------------------
-    if (lane != 0) return;
-    // slab s -> (segment, row tile t, k-group g), advanced incrementally
+  // one lane of the producer warp streams the slabs of [s0, s1) into the stages
+  auto produce = [&]() {
     int g = s0 % G, t = (s0 / G) % RT, seg = (s0 / G) / RT;
     int stage = 0;
     uint32_t rphase = 0;          // parity of the current round over the stage ring
@@ -324,9 +326,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       for (int j = (issued > kp.stages ? issued - kp.stages : 0); j < issued; ++j)
         (void)mbar_wait(&full[j % kp.stages], (uint32_t)((j / kp.stages) & 1), a.status);
     }
+  };
+
+  if (warp == 0) {
+    // ---------------------------- producer --------------------------------
+    if (lane == 0) produce();
+    __syncwarp();
     return;
   }
-
   // ------------------------------ consumers ---------------------------------
   // After an abort (a wait that timed out, here or in another warp) a warp still
   // walks its slab sequence but skips the waits, the arithmetic and the stores.
@@ -406,36 +413,41 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       } else if (!full_cover && !aborted) {
         // reducer: add the peers' partial sums in CTA order, clearing each word after
         // reading it (the workspace is all zero again when the call ends). The words
-        // of up to kPeerBatch peers are loaded at once, so their latencies overlap.
-        constexpr int kPeerBatch = 4;
+        // of up to four peers are loaded at once, so that their latencies overlap.
         int cp = c + 1;
-        while (cp < P && !aborted) {
-          int ids[kPeerBatch];
-          int nb = 0;
-          for (; cp < P && nb < kPeerBatch; ++cp) {
-            const int ps0 = (int)(((int64_t)cp * S) / P), ps1 = (int)(((int64_t)(cp + 1) * S) / P);
-            if (ps0 >= tail) { cp = P; break; }
-            if (ps0 < ps1) ids[nb++] = cp;      // an empty range publishes nothing
-          }
-          uint32_t u[kPeerBatch][4];
+        bool more = true;
+        while (more && !aborted) {
+          int pid[4];
 #pragma unroll
-          for (int k = 0; k < kPeerBatch; ++k) {
+          for (int k = 0; k < 4; ++k) {          // the next four peers (-1: none)
+            pid[k] = -1;
+            while (cp < P) {
+              const int ps0 = range_start(cp), ps1 = range_start(cp + 1);
+              if (ps0 >= tail) { cp = P; break; }
+              ++cp;
+              if (ps0 < ps1) { pid[k] = cp - 1; break; }   // an empty range publishes nothing
+            }
+          }
+          more = (pid[3] >= 0);
+          uint32_t u[4][4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
               u[k][e] = 0u;
-              if (k < nb && tok < R)
+              if (pid[k] >= 0 && tok < R)
                 u[k][e] = ld_relaxed(reinterpret_cast<const unsigned*>(kp.partials) +
-                                     (int64_t)ids[k] * (kSlabRows * kp.mt) + row * kp.mt + tok);
+                                     (int64_t)pid[k] * (kSlabRows * kp.mt) + row * kp.mt + tok);
             }
           }
 #pragma unroll
-          for (int k = 0; k < kPeerBatch; ++k) {
+          for (int k = 0; k < 4; ++k) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
-              if (k >= nb || tok >= R || aborted) continue;
-              unsigned* wp = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)ids[k] * (kSlabRows * kp.mt) +
+              if (pid[k] < 0 || tok >= R || aborted) continue;
+              unsigned* wp = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)pid[k] * (kSlabRows * kp.mt) +
                              row * kp.mt + tok;
               uint32_t v = u[k][e];
               if (v == 0u) {
