@@ -212,3 +212,25 @@ def test_errors(q):
     y = q.qmv_gemv("q4_k", packed, x, N, K, ws2).cpu().numpy()
     assert q.qmv_device_status() == 0
     assert norm_err(y, ref, den) <= TOL
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 activation quantizer (W4A4 prefill input)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M,K", [(1, 256), (7, 5120), (512, 1024), (3, 48)])
+def test_quant_act_nvfp4_bit_exact(q, M, K):
+    x = synth.activations(31 + M, M, K)
+    xb = synth.bf16_bits(x)
+    xf = x.float().numpy()
+    xf[0, :16] = 0.0                                  # an all-zero block: scale 0, codes 0
+    if K >= 64:
+        xf[-1, 16:32] *= 1e-3                         # a small block next to normal ones
+        xf[-1, 40] = 300.0                            # an outlier that saturates its block
+    x = torch.from_numpy(xf).to(torch.bfloat16)
+    xb = synth.bf16_bits(x)
+    x_scale = float(np.float32(np.abs(xf).max()) / np.float32(2688.0))
+    codes_ref, scales_ref = oracle.quant_act_nvfp4(xb, x_scale)
+    codes, scales = q.qmv_quant_act_nvfp4(x.cuda(), x_scale)
+    assert q.qmv_last_route() == q.FORMATS["nvfp4"] * 100 + 8
+    assert np.array_equal(scales.cpu().numpy(), scales_ref)
+    assert np.array_equal(codes.cpu().numpy(), codes_ref)
