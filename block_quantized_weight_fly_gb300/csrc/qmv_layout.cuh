@@ -7,7 +7,9 @@
 // k-group g there is a plane of n_pad row records:
 //
 //   Q4_K : record = the canonical 144-byte superblock (d, dmin, 12 B scales, 128 B nibbles)
-//   NVFP4: record = 16 B of E4M3 block scales | 128 B of E2M1 codes          (144 B)
+//   NVFP4: plane A = E2M1 codes, 128 B per row, in tensor-core tiles (below)  (128 B)
+//          plus a plane B of E4M3 block scales, 16 B per row, in the tile layout
+//          the tensor memory copy of block scale factors takes                 (16 B)
 //   Q8_0 : record = 8 fp16 d | 8 x 32 int8 quants                             (272 B)
 //   Q6_K : record = 128 B ql | 64 B qh | 16 B int8 scales                     (208 B)
 //          plus a second plane of n_pad fp16 d                                (2 B)
@@ -36,6 +38,16 @@
 // NVFP4 and FP8 codes keep their canonical order (element 2i in the low nibble or
 // byte), which the hardware FP4/FP8 -> f16x2 conversions consume directly.
 //
+// NVFP4 tiles. The codes of a 128-row tile of a k-group (16 KB) are stored as the
+// K-major "core matrices" of the 5th-generation tensor core: 8 rows x 16 bytes (32
+// codes) each, 128 contiguous bytes; core (row group r/8, K chunk kc) at
+// (r/8)*1024 + kc*128, row r%8 at +16*(r%8). So the same 16 KB serve a tcgen05.mma
+// operand directly (leading byte offset 128, stride byte offset 1024) and the GEMV
+// decoder. The block scales of the tile (2 KB) are four 512-byte blocks, one per
+// 64-value K step: the scale of 16-value block kb (0..3) of row r at
+// 16*(r%32) + 4*(r/32) + kb -- the 32 x 16-byte layout that tcgen05.cp.32x128b.warpx4
+// replicates into the four lane quadrants of tensor memory.
+//
 // Records of 144, 208 and 272 bytes are odd multiples of 16, so 8 consecutive rows
 // read at the same offset hit 8 different 16-byte bank groups; the 256-byte FP8
 // record gets the same property from its rotation.
@@ -62,7 +74,7 @@ constexpr int kChunk = 32;           // values per lane chunk
 constexpr int kChunksPerSlab = 8;
 constexpr int kHeaderBytes = 256;
 constexpr uint32_t kMagic = 0x31564D51u;  // "QMV1"
-constexpr uint32_t kVersion = 4;
+constexpr uint32_t kVersion = 5;
 
 enum Fmt { F_Q8_0 = 1, F_Q4_K = 2, F_Q6_K = 3, F_NVFP4 = 4, F_FP8 = 5 };
 
@@ -85,7 +97,7 @@ __host__ __device__ inline int rec_bytes(int fmt) {
     case F_Q8_0: return 272;
     case F_Q4_K: return 144;
     case F_Q6_K: return 208;
-    case F_NVFP4: return 144;
+    case F_NVFP4: return 128;
     case F_FP8: return 256;
     default: return 0;
   }
@@ -99,7 +111,7 @@ struct Layout {
   int64_t n_pad;        // N rounded up to 128
   int64_t k_groups;     // ceil(K / 256)
   int64_t plane_a;      // bytes of one k-group's plane A (n_pad * rec)
-  int64_t plane_b;      // bytes of one k-group's plane B (Q6_K d: n_pad * 2), else 0
+  int64_t plane_b;      // bytes of one k-group's plane B (Q6_K d: n_pad * 2; NVFP4 scales: n_pad * 16), else 0
   int64_t group_bytes;  // plane_a + plane_b
   int64_t extras;       // per-expert extras bytes (aligned to 256)
   int64_t expert_bytes; // bytes per expert (aligned to 256)
@@ -116,7 +128,7 @@ __host__ __device__ inline bool make_layout(int fmt, int64_t N, int64_t K, int64
   L->n_pad = L->row_tiles * kSlabRows;
   L->k_groups = (K + kSlabK - 1) / kSlabK;
   L->plane_a = L->n_pad * L->rec;
-  L->plane_b = (fmt == F_Q6_K) ? L->n_pad * 2 : 0;
+  L->plane_b = (fmt == F_Q6_K) ? L->n_pad * 2 : (fmt == F_NVFP4) ? L->n_pad * 16 : 0;
   L->group_bytes = L->plane_a + L->plane_b;
   int64_t ex = 0;
   if (fmt == F_NVFP4) ex = 256;
@@ -142,11 +154,18 @@ __host__ __device__ inline int64_t canon_matrix_bytes(int fmt, int64_t N, int64_
 // Quant words are stored thread-major: the consumer thread t (t = 0..3) of an mma
 // quad reads, for every 32-value chunk j of the k-group, the same 4 (or 8) bytes;
 // those bytes of all 8 chunks are contiguous, so one or two 128-bit loads fetch them.
-//   Q4_K / NVFP4: word t of chunk j (its elements 8t..8t+7) at 16 + 32t + 4j
+//   Q4_K        : word t of chunk j (its elements 8t..8t+7) at 16 + 32t + 4j
 //   Q8_0        : words 2t, 2t+1 of chunk j (elements 8t..8t+7) at 16 + 64t + 8j
 //   Q6_K        : ql word t of chunk j at 32t + 4j; qh word h of chunk j at 128 + 32h + 4j
 __host__ __device__ inline int q4k_word_off(int t, int j) { return 16 + 32 * t + 4 * j; }
-__host__ __device__ inline int nv_word_off(int t, int j) { return 16 + 32 * t + 4 * j; }
+// NVFP4: byte offset (within plane A of a k-group) of code word wd (0..3) of K chunk kc
+// (0..7) of row n, and (within plane B) of the scale of 16-value block b (0..15)
+__host__ __device__ inline int64_t nv_code_off(int64_t n, int kc, int wd) {
+  return (n >> 7) * 16384 + ((n & 127) >> 3) * 1024 + kc * 128 + (n & 7) * 16 + 4 * wd;
+}
+__host__ __device__ inline int64_t nv_scale_off(int64_t n, int b) {
+  return (n >> 7) * 2048 + (b >> 2) * 512 + 16 * (n & 31) + 4 * ((n & 127) >> 5) + (b & 3);
+}
 __host__ __device__ inline int q80_word_off(int t, int j) { return 16 + 64 * t + 8 * j; }
 __host__ __device__ inline int q6k_ql_word_off(int t, int j) { return 32 * t + 4 * j; }
 __host__ __device__ inline int q6k_qh_word_off(int h, int j) { return 128 + 32 * h + 4 * j; }

@@ -82,8 +82,10 @@ __global__ void pack_kernel(Layout L, const uint8_t* __restrict__ canon, uint8_t
     case F_NVFP4: {
       const uint8_t* ce = canon + e * canon_matrix_bytes(F_NVFP4, L.N, L.K);
       for (int wd = 0; wd < 4; ++wd)
-        *reinterpret_cast<uint32_t*>(rec + nv_word_off(wd, cl)) = load_u32(ce + n * (L.K / 2) + c * 16 + 4 * wd);
-      copy_bytes(rec + 2 * cl, ce + L.N * (L.K / 2) + n * (L.K / 16) + 2 * c, 2);
+        *reinterpret_cast<uint32_t*>(plane + nv_code_off(n, cl, wd)) = load_u32(ce + n * (L.K / 2) + c * 16 + 4 * wd);
+      const uint8_t* sc = ce + L.N * (L.K / 2) + n * (L.K / 16) + 2 * c;
+      plane[L.plane_a + nv_scale_off(n, 2 * cl)] = sc[0];
+      plane[L.plane_a + nv_scale_off(n, 2 * cl + 1)] = sc[1];
       if (n == 0 && c == 0) copy_bytes(extras, ce + L.N * (L.K / 2) + L.N * (L.K / 16), 4);
     } break;
     case F_FP8: {
@@ -173,9 +175,9 @@ __global__ void dequant_kernel(Layout L, const uint8_t* __restrict__ packed, int
     case F_NVFP4: {
       const float sT = *reinterpret_cast<const float*>(extras);
       for (int i = 0; i < 32; ++i) {
-        const uint32_t cw = *reinterpret_cast<const uint32_t*>(rec + nv_word_off(i >> 3, cl));
+        const uint32_t cw = *reinterpret_cast<const uint32_t*>(plane + nv_code_off(n, cl, i >> 3));
         uint32_t code = (cw >> (4 * (i & 7))) & 15u;
-        float p = __fmul_rn(e2m1f(code), e4m3f(rec[2 * cl + (i >> 4)]));
+        float p = __fmul_rn(e2m1f(code), e4m3f(plane[L.plane_a + nv_scale_off(n, 2 * cl + (i >> 4))]));
         o[i] = __fmul_rn(p, sT);
       }
     } break;

@@ -467,7 +467,24 @@ struct Slab<F_Q6_K, 8> {
 
 // ============================================================================
 // NVFP4. A = e2m1(c) * s_b in f16 (exact), B = x in f16; s_T in the epilogue.
+// The codes of row r, K chunk j sit in the tensor-core tile at
+// (r/8)*1024 + j*128 + (r%8)*16 (thread t reads word t: elements 8t..8t+7); the
+// scales of the row's four blocks of K step ks are one 32-bit word of plane B at
+// ks*512 + 16*(r%32) + 4*(r/32); chunk j uses block 2(j%2) + t/2 of step j/2.
 // ============================================================================
+__device__ __forceinline__ void nv_load(const uint8_t* st, const uint8_t* sf, int r, int t, uint32_t* C,
+                                        uint32_t* S) {
+  const uint8_t* c = st + (r >> 3) * 1024 + (r & 7) * 16 + 4 * t;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) C[j] = lds32(c + 128 * j);
+  const uint8_t* s = sf + 16 * (r & 31) + 4 * (r >> 5);
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) S[ks] = lds32(s + 512 * ks);
+}
+// the E4M3 scale byte of chunk j for thread t
+__device__ __forceinline__ uint32_t nv_sbyte(const uint32_t* S, int j, int t) {
+  return (S[j >> 1] >> (8 * (2 * (j & 1) + (t >> 1)))) & 0xFFu;
+}
 __device__ __forceinline__ void nv_frag(uint32_t code_word, uint32_t sbyte, uint32_t* p) {
   const uint32_t s = e4m3x2_f16(sbyte | (sbyte << 8));
   p[0] = hmul2(e2m1x2_f16(code_word & 0xFFu), s);
@@ -478,23 +495,21 @@ __device__ __forceinline__ void nv_frag(uint32_t code_word, uint32_t sbyte, uint
 
 template <>
 struct Slab<F_NVFP4, 1> {
-  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int, int w, int lane,
+  __device__ static void run(const uint8_t* st, const uint8_t* sf, const uint8_t* xs, int, int w, int lane,
                              float2*, float* acc) {
     const int g = lane >> 2, t = lane & 3;
-    const uint8_t* rA = st + (16 * w + g) * 144;
-    const uint8_t* rB = rA + 8 * 144;
     const uint4 xr = lds128v(xs + 64 * g + 16 * t);
     const uint32_t x0 = bf16x2_to_f16x2(xr.x), x1 = bf16x2_to_f16x2(xr.y);
     const uint32_t x2 = bf16x2_to_f16x2(xr.z), x3 = bf16x2_to_f16x2(xr.w);
-    uint32_t CA[8], CB[8];
-    load8(rA + nv_word_off(t, 0), CA);
-    load8(rB + nv_word_off(t, 0), CB);
+    uint32_t CA[8], CB[8], SA[4], SB[4];
+    nv_load(st, sf, 16 * w + g, t, CA, SA);
+    nv_load(st, sf, 16 * w + g + 8, t, CB, SB);
     float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       uint32_t pa[4], pb[4];
-      nv_frag(CA[j], rA[2 * j + (t >> 1)], pa);
-      nv_frag(CB[j], rB[2 * j + (t >> 1)], pb);
+      nv_frag(CA[j], nv_sbyte(SA, j, t), pa);
+      nv_frag(CB[j], nv_sbyte(SB, j, t), pb);
       const bool mine = (g == j);
       float* d = (j & 1) ? dO : dE;
       mma_f16(d, pa[0], pb[0], pa[1], pb[1], sel(mine, x0), sel(mine, x1));
@@ -507,21 +522,19 @@ struct Slab<F_NVFP4, 1> {
 
 template <>
 struct Slab<F_NVFP4, 8> {
-  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int R, int w, int lane,
+  __device__ static void run(const uint8_t* st, const uint8_t* sf, const uint8_t* xs, int R, int w, int lane,
                              float2*, float* acc) {
     const int g = lane >> 2, t = lane & 3;
-    const uint8_t* rA = st + (16 * w + g) * 144;
-    const uint8_t* rB = rA + 8 * 144;
     const bool has_x = g < R;
-    uint32_t CA[8], CB[8];
-    load8(rA + nv_word_off(t, 0), CA);
-    load8(rB + nv_word_off(t, 0), CB);
+    uint32_t CA[8], CB[8], SA[4], SB[4];
+    nv_load(st, sf, 16 * w + g, t, CA, SA);
+    nv_load(st, sf, 16 * w + g + 8, t, CB, SB);
     float dO[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       uint32_t pa[4], pb[4];
-      nv_frag(CA[j], rA[2 * j + (t >> 1)], pa);
-      nv_frag(CB[j], rB[2 * j + (t >> 1)], pb);
+      nv_frag(CA[j], nv_sbyte(SA, j, t), pa);
+      nv_frag(CB[j], nv_sbyte(SB, j, t), pb);
       uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
       float* d = (j & 1) ? dO : acc;
       mma_f16(d, pa[0], pb[0], pa[1], pb[1], bf16x2_to_f16x2(xv.x), bf16x2_to_f16x2(xv.y));

@@ -45,6 +45,8 @@ constexpr int kThreads = 32 * (1 + kConsumerWarps);
 // the M > 1 kernels need more registers per thread and take a whole SM.
 template <int MT> constexpr int ctas_per_sm() { return MT == 1 ? 2 : 1; }
 constexpr int kMaxStages = 16;
+// bytes per row of plane B (Q6_K d, NVFP4 block scales)
+template <int FMT> constexpr int plane_b_row() { return FMT == F_Q6_K ? 2 : FMT == F_NVFP4 ? 16 : 0; }
 constexpr int kMaxSeg = 64;
 constexpr unsigned long long kTimeoutNs = 1000000000ull;   // 1 s
 constexpr uint32_t kSuspendNs = 2000;    // a waiting thread sleeps up to this long per try (wakes on completion)
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     uint32_t rphase = 0;          // parity of the current round over the stage ring
     int it = 0;
     const uint32_t abytes = (uint32_t)(kSlabRows * L.rec);
-    const uint32_t bbytes = (FMT == F_Q6_K) ? (uint32_t)(kSlabRows * 2) : 0u;
+    const uint32_t bbytes = (uint32_t)(kSlabRows * plane_b_row<FMT>());
     // The first round of stages: weights first (independent of earlier kernels),
     // then wait for the previous grid, then the activations of those stages.
     const int first = (s1 - s0) < kp.stages ? (s1 - s0) : kp.stages;
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         const int R = sg.R < MT ? sg.R : MT;
         mbar_expect_tx(&full[i], abytes + bbytes + (uint32_t)(kv * 2) * (uint32_t)R);
         bulk_g2s(st, plane + (int64_t)t2 * kSlabRows * L.rec, abytes, &full[i]);
-        if (FMT == F_Q6_K) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t2 * kSlabRows * 2, bbytes, &full[i]);
+        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t2 * bbytes, bbytes, &full[i]);
         if (++gg == G) { gg = 0; if (++t2 == RT) { t2 = 0; ++sg2; } }
       }
     }
@@ -312,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       if (it >= first) {
         mbar_expect_tx(&full[stage], abytes + bbytes + xbytes * (uint32_t)R);
         bulk_g2s(st, plane + (int64_t)t * kSlabRows * L.rec, abytes, &full[stage]);
-        if (FMT == F_Q6_K) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t * kSlabRows * 2, bbytes, &full[stage]);
+        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t * bbytes, bbytes, &full[stage]);
       }
       for (int r = 0; r < R; ++r)
         bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)g * kSlabK, xbytes,
@@ -525,7 +527,7 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   kp.stage_base = (int)align_up(kp.tbl_off + tbl_bytes, 1024);
   const int abytes = kSlabRows * a.L.rec;
   kp.b_off = (int)align_up(abytes, 128);
-  const int bbytes = (FMT == F_Q6_K) ? kSlabRows * 2 : 0;
+  const int bbytes = kSlabRows * plane_b_row<FMT>();
   kp.x_off = (int)align_up(kp.b_off + bbytes, 128);
   kp.stage_bytes = (int)align_up(kp.x_off + MT * kXStride, 1024);
   kp.stages = (smem_max - kp.stage_base) / kp.stage_bytes;
