@@ -97,7 +97,10 @@ size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, i
     return (size_t)ws_plan_stream(M, 0, sms).total;
   }
   if (entry == QMV_ENTRY_W4A4) {
-    return (size_t)(align_up((int64_t)M * K / 2, 256) + align_up((int64_t)M * K / 16, 256) + 256);
+    // the activation's NVFP4 tiles: per 256-value k-group, m_pad rows x (128 B codes + 16 B scales)
+    if (fmt != QMV_NVFP4 || K % 256) return 0;
+    const int64_t m_pad = align_up(M, 128);
+    return (size_t)((K / 256) * m_pad * 144);
   }
   return 0;
 }
@@ -173,9 +176,21 @@ qmv_status qmv_quant_act_nvfp4(const uint16_t* x, float x_scale, uint8_t* codes,
 
 qmv_status qmv_gemm_nvfp4_w4a4(const void* packed_W, const uint16_t* x, float x_scale, float* y, int M,
                                int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)packed_W; (void)x; (void)x_scale; (void)y; (void)M; (void)N; (void)K; (void)ws; (void)ws_bytes;
-  (void)stream;
-  return QMV_EUNSUPPORTED;
+  if (!packed_W || !x || !y || !ws || M < 1 || N <= 0 || K <= 0 || !(x_scale >= 0.0f)) return QMV_EINVAL;
+  if (K % 256) return QMV_EUNSUPPORTED;
+  Layout L;
+  if (!make_layout(QMV_NVFP4, N, K, 1, &L)) return QMV_EUNSUPPORTED;
+  if (!aligned(packed_W, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 16)) return QMV_EALIGN;
+  const int64_t m_pad = align_up(M, 128);
+  if (ws_bytes < (size_t)((K / 256) * m_pad * 144)) return QMV_EWORKSPACE;
+  unsigned* status = status_ptr();
+  if (!status) return QMV_ECUDA;
+  uint8_t* planes = static_cast<uint8_t*>(ws);
+  qmv_status st = from_cuda(launch_quant_act_tiled(x, x_scale, planes, M, m_pad, K, stream));
+  if (st != QMV_OK) return st;
+  st = from_cuda(launch_w4a4(L, static_cast<const uint8_t*>(packed_W), planes, x_scale, y, M, m_pad, status, stream));
+  if (st == QMV_OK) g_last_route = QMV_NVFP4 * 100 + 4;
+  return st;
 }
 
 const char* qmv_status_str(qmv_status s) {

@@ -49,6 +49,13 @@ cudaError_t launch_quantize(int fmt, const float* W, int64_t rows, int64_t K, fl
                             uint8_t* canon, cudaStream_t s);
 cudaError_t launch_quant_act(const uint16_t* x, float xs, uint8_t* codes, uint8_t* scales, int M,
                              int64_t K, cudaStream_t s);
+// NVFP4 activation quantizer into the W4A4 GEMM's tiled activation planes
+cudaError_t launch_quant_act_tiled(const uint16_t* x, float xs, uint8_t* planes, int M, int64_t m_pad, int64_t K,
+                                   cudaStream_t s);
+// W4A4 block-scaled GEMM (tcgen05): y[M][N] = x_scale * s_T * (x codes . W codes) with
+// the activation planes written by launch_quant_act_tiled
+cudaError_t launch_w4a4(const Layout& L, const uint8_t* packed, const uint8_t* act_planes, float x_scale,
+                        float* y, int M, int64_t m_pad, unsigned* status, cudaStream_t s);
 // returns the route variant launched (1 = CUDA-core M=1, 2 = mma M>1, 3 = grouped)
 cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant);
 

@@ -403,13 +403,9 @@ cudaError_t launch_quantize(int fmt, const float* W, int64_t rows, int64_t K, fl
 // s_b = e4m3(amax_b / (6 x_scale)); zero block scale -> zero codes;
 // else codes = e2m1(x / (s_b x_scale)).
 // ---------------------------------------------------------------------------
-__global__ void quant_act_kernel(const uint16_t* __restrict__ x, float xs, uint8_t* __restrict__ codes,
-                                 uint8_t* __restrict__ scales, int64_t M, int64_t K) {
-  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t bpr = K / 16;
-  if (b >= M * bpr) return;
-  const int64_t m = b / bpr, kb = b % bpr;
-  const uint4* src = reinterpret_cast<const uint4*>(x + m * K + kb * 16);
+// one 16-value block: the E4M3 scale and the 16 E2M1 codes (element i at nibble i)
+__device__ __forceinline__ uint32_t quant_block16(const uint16_t* src16, float xs, uint32_t* packed) {
+  const uint4* src = reinterpret_cast<const uint4*>(src16);
   uint4 v0 = src[0], v1 = src[1];
   uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
   float xv[16];
@@ -421,14 +417,51 @@ __global__ void quant_act_kernel(const uint16_t* __restrict__ x, float xs, uint8
   }
   const float t = __fmul_rn(6.0f, xs);
   const uint32_t sb = (t > 0.0f) ? f2e4m3(__fdiv_rn(amax, t)) : 0u;
-  scales[m * bpr + kb] = (uint8_t)sb;
-  uint32_t packed[2] = {0u, 0u};
+  packed[0] = packed[1] = 0u;
   if (sb != 0u) {
     const float den = __fmul_rn(e4m3f(sb), xs);
     for (int i = 0; i < 16; ++i) packed[i >> 3] |= f2e2m1(__fdiv_rn(xv[i], den)) << (4 * (i & 7));
   }
+  return sb;
+}
+
+__global__ void quant_act_kernel(const uint16_t* __restrict__ x, float xs, uint8_t* __restrict__ codes,
+                                 uint8_t* __restrict__ scales, int64_t M, int64_t K) {
+  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t bpr = K / 16;
+  if (b >= M * bpr) return;
+  const int64_t m = b / bpr, kb = b % bpr;
+  uint32_t packed[2];
+  scales[m * bpr + kb] = (uint8_t)quant_block16(x + m * K + kb * 16, xs, packed);
   uint2* dst = reinterpret_cast<uint2*>(codes + m * (K / 2) + kb * 8);
   *dst = make_uint2(packed[0], packed[1]);
+}
+
+// The same quantizer writing the tensor-core tiles of the W4A4 GEMM's activation
+// operand: per k-group a plane of m_pad rows x 128 B of codes (core-matrix tiles,
+// as the NVFP4 weight planes) followed by m_pad x 16 B of scales (tcgen05.cp tile
+// layout). Rows m >= M (padding up to a multiple of 128) get zero codes and scales.
+__global__ void quant_act_tiled_kernel(const uint16_t* __restrict__ x, float xs, uint8_t* __restrict__ planes,
+                                       int64_t M, int64_t m_pad, int64_t K) {
+  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t bpr = K / 16;
+  if (b >= m_pad * bpr) return;
+  const int64_t m = b / bpr, kb = b % bpr;
+  uint32_t packed[2] = {0u, 0u};
+  uint32_t sb = 0u;
+  if (m < M) sb = quant_block16(x + m * K + kb * 16, xs, packed);
+  uint8_t* plane = planes + (kb / 16) * (m_pad * 144);
+  const int blk = (int)(kb % 16);
+  *reinterpret_cast<uint2*>(plane + nv_code_off(m, blk >> 1, 2 * (blk & 1))) = make_uint2(packed[0], packed[1]);
+  plane[m_pad * 128 + nv_scale_off(m, blk)] = (uint8_t)sb;
+}
+
+cudaError_t launch_quant_act_tiled(const uint16_t* x, float xs, uint8_t* planes, int M, int64_t m_pad, int64_t K,
+                                   cudaStream_t s) {
+  const int64_t total = m_pad * (K / 16);
+  const int threads = 256;
+  quant_act_tiled_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, s>>>(x, xs, planes, M, m_pad, K);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quant_act(const uint16_t* x, float xs, uint8_t* codes, uint8_t* scales, int M,
