@@ -72,6 +72,10 @@ WORKLOADS = {
                    desc="row-scaled FP8 projection [6144,5120], M=8"),
     "q8_0_tiny": dict(fmt="q8_0", M=1, mats=[("tiny", 512, 1024)],
                       desc="Q8_0 tiny [512,1024], M=1"),
+    "nvfp4_w4a4_m512": dict(fmt="nvfp4", M=512, w4a4=True,
+                            mats=[("up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
+                            desc="NVFP4 W4A4 prefill, M=512: activation quantized to NVFP4, tcgen05 block-scaled "
+                                 "MMA, [17408,5120] + [5120,17408]"),
     "tower_m1": dict(fmt="q4_k", M=1, tower=True, E=288, topk=8,
                      mats=[("gate", 2048, 4096), ("up", 2048, 4096), ("down", 4096, 2048)],
                      desc="grouped Q4_K tower, 288 experts x (gate,up [2048,4096], down [4096,2048]), top-8, M=1"),
@@ -86,7 +90,7 @@ DEFAULT_WORKLOAD = "q4k_mlp_m1"
 DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, "q6k_head_m8": 2000,
                  "q6k_qkv_m1": 40000, "q6k_qkv_m8": 40000, "nvfp4_mlp_m1": 20000, "nvfp4_mlp_m8": 20000,
                  "fp8_m1": 40000, "fp8_m8": 40000, "q8_0_tiny": 20000, "tower_m1": 20000,
-                 "tower_m4": 10000, "tower_m8": 5000}
+                 "tower_m4": 10000, "tower_m8": 5000, "nvfp4_w4a4_m512": 2000}
 
 METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"
 CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q6_k": 210 / 256, "nvfp4": 18 / 32, "fp8_row": 1.0}
@@ -98,6 +102,17 @@ def canon_bytes(fmt, N, K):
     if fmt == "fp8_row":
         return N * K + 4 * N
     return int(round(N * K * CANON_PER_VALUE[fmt]))
+
+
+def measured_fp4_peak():
+    """Dense FP4 tensor peak: the measured bf16 GEMM rate times the nominal FP4/bf16
+    ratio of the part (13.5 / 2.25 PFLOP/s)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d.get("bf16_tflops", 1900.0)) * 6.0, "measured bf16 x 6 (nominal fp4/bf16 ratio)"
+    return 1900.0 * 6.0, "fallback bf16 x 6 (nominal fp4/bf16 ratio)"
 
 
 def measured_peaks():
@@ -216,6 +231,7 @@ class DeviceWorkload:
         w = WORKLOADS[name]
         self.fmt, self.M = w["fmt"], w["M"]
         self.tower = w.get("tower", False)
+        self.w4a4 = w.get("w4a4", False)
         self.E = w.get("E", 1)
         self.topk = w.get("topk", 1)
         self.mats = w["mats"]
@@ -237,8 +253,10 @@ class DeviceWorkload:
             self.x.append(synth.activations(200 + i, rows, K, device=dev))
             ysh = (self.M, self.topk, N) if self.tower else (self.M, N)
             self.y.append(torch.empty(ysh, dtype=torch.float32, device=dev))
-            entry = q.QMV_ENTRY_GROUPED if self.tower else q.QMV_ENTRY_GEMV
+            entry = q.QMV_ENTRY_GROUPED if self.tower else (q.QMV_ENTRY_W4A4 if self.w4a4 else q.QMV_ENTRY_GEMV)
             self.ws.append(q.workspace(entry, self.fmt, self.M, N, K, self.E, self.topk, device=dev))
+        # W4A4: the static activation scale of each x (amax / (448 * 6)), computed once
+        self.x_scale = [float(x.float().abs().max()) / 2688.0 for x in self.x] if self.w4a4 else []
         # routing: a different id set every step (cycled), like consecutive decode steps
         self.ids = []
         self.unique = []
@@ -247,7 +265,11 @@ class DeviceWorkload:
                 ids = synth.expert_ids(1000 + s, self.M, self.topk, self.E)
                 self.ids.append(torch.from_numpy(ids).to(dev))
                 self.unique.append(len(np.unique(ids)))
-        self.launches_per_step = len(self.mats)
+        # W4A4 runs the activation quantizer and the GEMM per matrix
+        self.launches_per_step = len(self.mats) * (2 if self.w4a4 else 1)
+
+    def step_flops(self):
+        return sum(2.0 * self.M * N * K for _, N, K in self.mats)
 
     def step_bytes(self, s=0):
         """algorithmic bytes of step s (weights of the rows needed + x + y (+ ids))."""
@@ -269,6 +291,8 @@ class DeviceWorkload:
             if self.tower:
                 q.qmv_grouped(self.fmt, self.packed[c][i], self.ids[s % len(self.ids)], self.x[i], N, K, self.E,
                               self.ws[i], x_per_pair=(i == len(self.mats) - 1), y=self.y[i])
+            elif self.w4a4:
+                q.qmv_gemm_nvfp4_w4a4(self.packed[c][i], self.x[i], self.x_scale[i], N, K, self.ws[i], y=self.y[i])
             else:
                 q.qmv_gemv(self.fmt, self.packed[c][i], self.x[i], N, K, self.ws[i], y=self.y[i])
 
@@ -355,6 +379,14 @@ def run_device(args, rank, world, dev):
     achieved = (bytes_per_step / wl.launches_per_step) / avg_launch_s / 1e9
     peak, peak_kind = measured_peaks()
     traffic = recorded_traffic(args.workload)
+    if wl.w4a4:
+        # a dense contraction: TFLOP/s against the tensor roofline; each matrix's
+        # time includes its activation quantizer (the GEMM's share is in profiles/)
+        flops = wl.step_flops()
+        value = flops * K * world / (ms_max * 1e-3) / 1e12
+        gemm_s = (ms * 1e-3) / (K * len(wl.mats))
+        achieved = (flops / len(wl.mats)) / gemm_s / 1e12
+        peak, peak_kind = measured_fp4_peak()
 
     # ---- end to end through the public API, host buffers -------------------
     e2e_steps = min(K, 2000)
@@ -428,6 +460,22 @@ def run_device(args, rank, world, dev):
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
+    if wl.w4a4:
+        result["metric"] = "NVFP4 W4A4 prefill throughput (M=512)"
+        result["unit"] = "TFLOP/s"
+        result["dtype"] = "fp4 (e2m1 x e2m1, ue4m3 block scales, fp32 accumulation)"
+        result["config"]["arithmetic"] = "tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X, TMEM fp32 accumulators"
+        result["config"]["flops_per_step"] = wl.step_flops()
+        del result["pct_of_nominal_8000"]
+        result["pct_of_peak"] = round(100.0 * value / world / peak, 2)
+        result["roofline"].update({
+            "bound": "tensor", "kernel": "qmv::w4a4_kernel (+ its activation quantizer)", "unit": "TFLOP/s",
+            "achieved": round(achieved, 2), "peak": round(peak, 1), "frac": round(achieved / peak, 4),
+            "avg_launch_us": round(gemm_s * 1e6, 3),
+            "algorithmic_flops_per_launch": wl.step_flops() / len(wl.mats)})
+        del result["roofline"]["algorithmic_bytes_per_launch"]
+        result["e2e"]["unit"] = "TFLOP/s"
+        result["e2e"]["value"] = round(wl.step_flops() * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, 2)
     if wl.tower:
         result["config"]["unique_experts_mean"] = round(float(np.mean(wl.unique)), 2)
     return result
