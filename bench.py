@@ -149,6 +149,24 @@ def recorded_traffic(workload):
 
 
 # ----------------------------------------------------------------------------
+# N > 1: replicas, one per rank; the job's rate is the units of all ranks over the
+# slowest rank's time
+# ----------------------------------------------------------------------------
+def slowest_rank_ms(ms, dev):
+    """The maximum over ranks of a rank's timed-region milliseconds (every rank calls it)."""
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=dev)
+    if torch.distributed.is_available() and torch.distributed.is_initialized() and \
+            torch.distributed.get_world_size() > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step, steps, world, ms_max):
+    """Units (bytes or FLOPs) of all ranks' steps per second, over the slowest rank's time."""
+    return units_per_step * steps * world / (ms_max * 1e-3)
+
+
+# ----------------------------------------------------------------------------
 # clocks during the timed region
 # ----------------------------------------------------------------------------
 class ClockSampler:
@@ -366,14 +384,10 @@ def run_device(args, rank, world, dev):
     status = q.qmv_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = slowest_rank_ms(ms, dev)
     step_bytes = [wl.step_bytes(W + i) for i in range(min(K, period))]
     bytes_per_step = sum(step_bytes) / len(step_bytes)
-    total_bytes = bytes_per_step * K * world
-    value = total_bytes / (ms_max * 1e-3) / 1e9
+    value = whole_job_rate(bytes_per_step, K, world, ms_max) / 1e9
     launches = K * wl.launches_per_step
     avg_launch_s = (ms * 1e-3) / launches
     achieved = (bytes_per_step / wl.launches_per_step) / avg_launch_s / 1e9
@@ -383,7 +397,7 @@ def run_device(args, rank, world, dev):
         # a dense contraction: TFLOP/s against the tensor roofline; each matrix's
         # time includes its activation quantizer (the GEMM's share is in profiles/)
         flops = wl.step_flops()
-        value = flops * K * world / (ms_max * 1e-3) / 1e12
+        value = whole_job_rate(flops, K, world, ms_max) / 1e12
         gemm_s = (ms * 1e-3) / (K * len(wl.mats))
         achieved = (flops / len(wl.mats)) / gemm_s / 1e12
         peak, peak_kind = measured_fp4_peak()
