@@ -16,7 +16,7 @@
 //  * the other eight warps are consumers: warp w decodes rows 16w .. 16w+15 of a
 //    slab on mma.sync (see qmv_slab.cuh), the decode in registers and the inner
 //    product factored per block: y += scale * sum(q * x) (- min * sum x);
-//  * at M = 1 a CTA takes half an SM, so that the next call's CTAs are resident
+//  * a CTA takes half an SM, so that the next call's CTAs are resident
 //    beside the running ones and copy their first weight slabs meanwhile;
 //  * a row tile split between CTAs is finished by the CTA that holds its first
 //    k-groups: the others publish their partial sums in the workspace, each word
@@ -39,11 +39,10 @@ namespace qmv {
 
 constexpr int kConsumerWarps = 8;       // consumer warps (16 rows of a slab each)
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
-// CTAs resident per SM. At M = 1 a CTA takes half of the SM (shared memory and
-// registers), so that the next call's CTA is resident beside the running one and
-// runs its prologue and first weight copies during the running call's compute;
-// the M > 1 kernels need more registers per thread and take a whole SM.
-template <int MT> constexpr int ctas_per_sm() { return MT == 1 ? 2 : 1; }
+// CTAs resident per SM: a CTA takes half of the SM (shared memory and registers),
+// so that the next call's CTA is resident beside the running one and runs its
+// prologue and first weight copies during the running call's compute.
+template <int MT> constexpr int ctas_per_sm() { return 2; }
 constexpr int kMaxStages = 16;
 // bytes per row of plane B (Q6_K d, NVFP4 block scales)
 template <int FMT> constexpr int plane_b_row() { return FMT == F_Q6_K ? 2 : FMT == F_NVFP4 ? 16 : 0; }
@@ -107,6 +106,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// 16-byte global -> shared copy; completion is tracked per thread (cp_async_arrive_noinc)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// the barrier counts one arrival of this thread once all its earlier cp.async have landed
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* b) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(b)) : "memory");
+}
 __device__ __forceinline__ uint32_t ld_relaxed(const unsigned* p) {
   uint32_t v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     if (bad) atomicOr(a.status, kStatHeader);
     misc[0] = bad;   // abort flag
     for (int i = 0; i < kp.stages; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], MT == 1 ? 1 : 1 + 32);   // M > 1: + one cp.async arrival per producer lane
       mbar_init(&empty[i], kConsumerWarps);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -274,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   constexpr bool kMayBeRagged = (FMT == F_Q8_0 || FMT == F_NVFP4 || FMT == F_FP8);
   const int kv_last = (int)(L.K - (int64_t)(G - 1) * kSlabK);
 
-  // one lane of the producer warp streams the slabs of [s0, s1) into the stages
-  auto produce = [&]() {
+  // M = 1: one lane of the producer warp streams the slabs of [s0, s1) into the stages
+  auto produce1 = [&]() {
     int g = s0 % G, t = (s0 / G) % RT, seg = (s0 / G) / RT;
     int stage = 0;
     uint32_t rphase = 0;          // parity of the current round over the stage ring
@@ -330,9 +337,97 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     }
   };
 
+  // M > 1: the producer warp streams the slabs of [s0, s1) into the stages. One lane
+  // moves the weights with bulk copies; the 32 lanes copy the slices of the x rows
+  // with 16-byte cp.async, each lane's copies tracked by the stage's full barrier
+  // (cp.async.mbarrier.arrive.noinc: 32 more arrivals), so R x rows cost no more
+  // than one bulk copy.
+  // lanes taking part: M = 1 -> lane 0 only (the others leave), M > 1 -> all 32
+  constexpr unsigned kPMask = (MT == 1) ? 1u : 0xffffffffu;
+  auto produce8 = [&]() {
+    int g = s0 % G, t = (s0 / G) % RT, seg = (s0 / G) / RT;
+    int stage = 0;
+    uint32_t rphase = 0;          // parity of the current round over the stage ring
+    int it = 0;
+    const uint32_t abytes = (uint32_t)(kSlabRows * L.rec);
+    const uint32_t bbytes = (uint32_t)(kSlabRows * plane_b_row<FMT>());
+    // The first round of stages: weights first (independent of earlier kernels),
+    // then wait for the previous grid, then the activations of those stages.
+    const int first = (s1 - s0) < kp.stages ? (s1 - s0) : kp.stages;
+    if (lane == 0) {
+      int gg = g, t2 = t, sg2 = seg;
+      for (int i = 0; i < first; ++i) {
+        const Seg& sg = segs[sg2];
+        uint8_t* st = smem + kp.stage_base + i * kp.stage_bytes;
+        const uint8_t* plane = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + gg * L.group_bytes;
+        const int kv = (kMayBeRagged && gg == G - 1) ? kv_last : kSlabK;
+        const int R = sg.R < MT ? sg.R : MT;
+        const uint32_t xtx = (MT == 1) ? (uint32_t)(kv * 2) * (uint32_t)R : 0u;
+        mbar_expect_tx(&full[i], abytes + bbytes + xtx);
+        bulk_g2s(st, plane + (int64_t)t2 * kSlabRows * L.rec, abytes, &full[i]);
+        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t2 * bbytes, bbytes, &full[i]);
+        if (++gg == G) { gg = 0; if (++t2 == RT) { t2 = 0; ++sg2; } }
+      }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int s = s0; s < s1; ++s, ++it) {
+      if (it >= kp.stages) {      // round r >= 1 waits for the consumers' release of round r-1
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[stage], rphase ^ 1u, a.status);
+        ok = __shfl_sync(kPMask, ok, 0);
+        if (!ok) { if (lane == 0) misc[0] = 1; break; }
+      }
+      if (__shfl_sync(kPMask, misc[0], 0)) break;
+      const Seg& sg = segs[seg];
+      uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
+      const uint8_t* plane = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + g * L.group_bytes;
+      const int kv = (kMayBeRagged && g == G - 1) ? kv_last : kSlabK;
+      const uint32_t xbytes = (uint32_t)(kv * 2);
+      const int R = sg.R < MT ? sg.R : MT;
+      if (lane == 0 && it >= first) {
+        mbar_expect_tx(&full[stage], abytes + bbytes + (MT == 1 ? xbytes * (uint32_t)R : 0u));
+        bulk_g2s(st, plane + (int64_t)t * kSlabRows * L.rec, abytes, &full[stage]);
+        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t * bbytes, bbytes, &full[stage]);
+      }
+      if (MT == 1) {
+        if (lane == 0)
+          for (int r = 0; r < R; ++r)
+            bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)g * kSlabK, xbytes,
+                     &full[stage]);
+      } else {
+        const int chunks = (int)(xbytes / 16);       // 16-byte pieces of one row's slice
+        for (int r = 0; r < R; ++r) {
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)g * kSlabK);
+          uint8_t* dst = st + kp.x_off + r * kXStride;
+          for (int c16 = lane; c16 < chunks; c16 += 32) cp_async16(dst + 16 * c16, src + 16 * c16);
+        }
+        cp_async_arrive_noinc(&full[stage]);
+      }
+      if (++stage == kp.stages) { stage = 0; rphase ^= 1u; }
+      if (++g == G) { g = 0; if (++t == RT) { t = 0; ++seg; } }
+    }
+    // drain: copies issued into stages the consumers may not have waited for. At
+    // M > 1 the first-round stages not reached above still expect the lanes'
+    // arrivals: the lanes arrive on them without copies, so they complete.
+    if (__shfl_sync(kPMask, misc[0], 0)) {
+      const int issued = it > first ? it : first;
+      if (MT > 1)
+        for (int j = it; j < first; ++j) mbar_arrive(&full[j]);
+      __syncwarp(kPMask);
+      if (lane == 0)
+        for (int j = (issued > kp.stages ? issued - kp.stages : 0); j < issued; ++j)
+          (void)mbar_wait(&full[j % kp.stages], (uint32_t)((j / kp.stages) & 1), a.status);
+    }
+    if (MT > 1) asm volatile("cp.async.wait_all;" ::: "memory");
+  };
+
   if (warp == 0) {
     // ---------------------------- producer --------------------------------
-    if (lane == 0) produce();
+    if constexpr (MT == 1) {
+      if (lane == 0) produce1();
+    } else {
+      produce8();
+    }
     __syncwarp();
     return;
   }
