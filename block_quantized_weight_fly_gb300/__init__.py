@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libqmv.so")
 QMV_Q8_0, QMV_Q4_K, QMV_Q6_K, QMV_NVFP4, QMV_FP8_ROW = 1, 2, 3, 4, 5
 FORMATS = {"q8_0": QMV_Q8_0, "q4_k": QMV_Q4_K, "q6_k": QMV_Q6_K, "nvfp4": QMV_NVFP4,
            "fp8_row": QMV_FP8_ROW}
-QMV_ENTRY_GEMV, QMV_ENTRY_GROUPED, QMV_ENTRY_W4A4 = 1, 2, 3
+QMV_ENTRY_GEMV, QMV_ENTRY_GROUPED, QMV_ENTRY_W4A4, QMV_ENTRY_SWIGLU = 1, 2, 3, 4
 QMV_MAX_M = 8
 
 STATUS = {0: "QMV_OK", 1: "QMV_EINVAL", 2: "QMV_EALIGN", 3: "QMV_EUNSUPPORTED", 4: "QMV_ECUDA",
@@ -58,6 +58,7 @@ _quantize = _sig("qmv_quantize", _I, [_I, _P, _I64, _I64, _F, _P, _P])
 _dequant = _sig("qmv_dequant", _I, [_I, _P, _I64, _I64, _I64, _I64, _I64, _P, _P])
 _ws_size = _sig("qmv_workspace_size", _SZ, [_I, _I, _I, _I64, _I64, _I64, _I])
 _gemv = _sig("qmv_gemv", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
+_gemv_swiglu = _sig("qmv_gemv_swiglu", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
 _gemv_noalloc = _sig("qmv_gemv_noalloc", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P])
 _grouped = _sig("qmv_grouped", _I, [_I, _P, _P, _P, _I, _P, _I, _I, _I64, _I64, _I64, _P, _SZ, _P])
 _quant_act = _sig("qmv_quant_act_nvfp4", _I, [_P, _F, _P, _P, _I, _I64, _P])
@@ -69,7 +70,7 @@ _dev_status = _sig("qmv_device_status", _I, [_I])
 EXPORTED = ["qmv_canon_size", "qmv_pack_size", "qmv_pack", "qmv_quantize", "qmv_dequant",
             "qmv_workspace_size", "qmv_gemv", "qmv_grouped", "qmv_quant_act_nvfp4",
             "qmv_gemm_nvfp4_w4a4", "qmv_status_str", "qmv_last_route", "qmv_device_status",
-            "qmv_gemv_noalloc"]
+            "qmv_gemv_noalloc", "qmv_gemv_swiglu"]
 
 
 def _fmt(fmt) -> int:
@@ -188,6 +189,19 @@ def qmv_gemv(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int,
     _check(_gemv(_fmt(fmt), _ptr(packed_W), _ptr(x), _ptr(y), M, N, K, _ptr(ws), ws.numel(),
                  _stream(stream)), "qmv_gemv")
     return y
+
+
+def qmv_gemv_swiglu(fmt, tower: torch.Tensor, x: torch.Tensor, N: int, K: int, ws: torch.Tensor,
+                    h: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """h = silu(gate . x) * (up . x) over a 2-expert tower (gate = expert 0, up = expert 1)."""
+    _dev(tower, "tower"); _dev(x, "x"); _dev(ws, "ws")
+    x = _bits16(x)
+    M = x.shape[0] if x.dim() == 2 else 1
+    if h is None:
+        h = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(_gemv_swiglu(_fmt(fmt), _ptr(tower), _ptr(x), _ptr(h), M, N, K, _ptr(ws), ws.numel(),
+                        _stream(stream)), "qmv_gemv_swiglu")
+    return h
 
 
 def qmv_gemv_noalloc(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int,

@@ -96,6 +96,10 @@ size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, i
     if (M > QMV_MAX_M) return 0;
     return (size_t)ws_plan_stream(M, 0, sms).total;
   }
+  if (entry == QMV_ENTRY_SWIGLU) {
+    if (M > QMV_MAX_M) return 0;
+    return (size_t)ws_plan_stream(M, 0, sms, 2).total;
+  }
   if (entry == QMV_ENTRY_W4A4) {
     // the activation's NVFP4 tiles: per 256-value k-group, m_pad rows x (128 B codes + 16 B scales)
     if (fmt != QMV_NVFP4 || K % 256) return 0;
@@ -121,7 +125,7 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
   a.L = L;
   a.packed = static_cast<const uint8_t*>(packed_W);
   a.x = x; a.y = y; a.ids = nullptr;
-  a.M = M; a.topk = 1; a.x_per_pair = 0;
+  a.M = M; a.topk = 1; a.x_per_pair = 0; a.swiglu = 0;
   a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
   a.status = status;
   const int64_t slabs = L.row_tiles * L.k_groups;
@@ -154,10 +158,37 @@ qmv_status qmv_grouped(qmv_fmt fmt, const void* tower, const int32_t* expert_ids
   a.L = L;
   a.packed = static_cast<const uint8_t*>(tower);
   a.x = x; a.y = y; a.ids = expert_ids;
-  a.M = M; a.topk = topk; a.x_per_pair = x_per_pair;
+  a.M = M; a.topk = topk; a.x_per_pair = x_per_pair; a.swiglu = 0;
   a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
   a.status = status;
   a.num_ctas = sms;
+  int variant = 0;
+  qmv_status st = from_cuda(launch_stream(a, stream, &variant));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
+  return st;
+}
+
+qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, float* h, int M, int64_t N,
+                           int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !tower || !x || !h || !ws) return QMV_EINVAL;
+  if (M < 1 || M > QMV_MAX_M || N <= 0 || K <= 0) return QMV_EINVAL;
+  Layout L;
+  if (!make_layout((int)fmt, N, K, 2, &L) || !slab_count_ok(L, 2)) return QMV_EUNSUPPORTED;
+  if (!aligned(tower, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(h, 4)) return QMV_EALIGN;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return QMV_ECUDA;
+  if (ws_bytes < (size_t)ws_plan_stream(M, 0, sms, 2).total) return QMV_EWORKSPACE;
+  unsigned* status = status_ptr();
+  if (!status) return QMV_ECUDA;
+  StreamArgs a;
+  a.L = L;
+  a.packed = static_cast<const uint8_t*>(tower);
+  a.x = x; a.y = h; a.ids = nullptr;
+  a.M = M; a.topk = 1; a.x_per_pair = 0; a.swiglu = 1;
+  a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
+  a.status = status;
+  const int64_t slabs = 2 * L.row_tiles * L.k_groups;
+  a.num_ctas = (int)(slabs < sms ? slabs : sms);
   int variant = 0;
   qmv_status st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
@@ -282,7 +313,7 @@ extern "C" qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const 
   a.L = L;
   a.packed = static_cast<const uint8_t*>(packed_W);
   a.x = x; a.y = y; a.ids = nullptr;
-  a.M = M; a.topk = 1; a.x_per_pair = 0;
+  a.M = M; a.topk = 1; a.x_per_pair = 0; a.swiglu = 0;
   a.ws = scratch; a.ws_bytes = (int64_t)QMV_STATIC_SCRATCH_BYTES;
   a.status = status;
   const int64_t slabs = L.row_tiles * L.k_groups;

@@ -21,6 +21,7 @@ struct StreamArgs {
   int M;                     // tokens (rows of x for dense)
   int topk;                  // grouped: slots per token; dense: 1
   int x_per_pair;            // grouped: 1 if x has one row per (token, slot)
+  int swiglu;                // 1: fused gate|up over a 2-expert tower, y = silu(gate.x) * (up.x)
   uint8_t* ws;               // workspace: per-CTA partial sums (zero between calls)
   int64_t ws_bytes;
   unsigned* status;          // per-device status word
@@ -32,7 +33,8 @@ struct WsPlan {
   int64_t partials_off, partials_bytes;
   int64_t total;
 };
-WsPlan ws_plan_stream(int M, int64_t tiles_max, int num_ctas);
+// passes: 1, or 2 for the fused gate|up (gate and up partial sums)
+WsPlan ws_plan_stream(int M, int64_t tiles_max, int num_ctas, int passes = 1);
 
 int num_sms_current_device();
 
@@ -56,7 +58,7 @@ cudaError_t launch_quant_act_tiled(const uint16_t* x, float xs, uint8_t* planes,
 // the activation planes written by launch_quant_act_tiled
 cudaError_t launch_w4a4(const Layout& L, const uint8_t* packed, const uint8_t* act_planes, float x_scale,
                         float* y, int M, int64_t m_pad, unsigned* status, cudaStream_t s);
-// returns the route variant launched (1 = CUDA-core M=1, 2 = mma M>1, 3 = grouped)
+// returns the route variant launched (1 = M=1, 2 = M>1, 3 = grouped, 9 = fused gate|up SwiGLU)
 cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant);
 
 }  // namespace qmv

@@ -146,7 +146,11 @@ struct KParams {
   float* partials;   // [num_ctas][128][mt]
 };
 
-template <int FMT, int MT>
+// SW: fused gate|up with the SwiGLU epilogue. The tower holds two experts (gate,
+// up) over the same x; each row tile's gate k-groups and then the same rows' up
+// k-groups form one unit, so a thread ends a unit holding g and u of its outputs
+// and writes silu(g) * u.
+template <int FMT, int MT, bool SW>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(const KParams kp) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const StreamArgs& a = kp.a;
@@ -191,10 +195,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   if (warp == 0) {
     if (a.ids == nullptr) {
       if (lane == 0) {
-        misc[1] = 1;
-        segs[0].expert = 0;
-        segs[0].R = a.M;
-        for (int r = 0; r < 8; ++r) { segs[0].xrow[r] = r; segs[0].yrow[r] = r; }
+        misc[1] = SW ? 2 : 1;
+        for (int sgi = 0; sgi < (SW ? 2 : 1); ++sgi) {
+          segs[sgi].expert = sgi;
+          segs[sgi].R = a.M;
+          for (int r = 0; r < 8; ++r) { segs[sgi].xrow[r] = r; segs[sgi].yrow[r] = r; }
+        }
       }
     } else {
       // Distinct routed experts, ascending. Key = id * 64 + pair index (unique),
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
 
   // M = 1: one lane of the producer warp streams the slabs of [s0, s1) into the stages
   auto produce1 = [&]() {
-    int g = s0 % G, t = (s0 / G) % RT, seg = (s0 / G) / RT;
+    int g = s0 % G, t = SW ? (s0 / G) / 2 : (s0 / G) % RT, seg = SW ? (s0 / G) % 2 : (s0 / G) / RT;
     int stage = 0;
     uint32_t rphase = 0;          // parity of the current round over the stage ring
     int it = 0;
@@ -303,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         mbar_expect_tx(&full[i], abytes + bbytes + (uint32_t)(kv * 2) * (uint32_t)R);
         bulk_g2s(st, plane + (int64_t)t2 * kSlabRows * L.rec, abytes, &full[i]);
         if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t2 * bbytes, bbytes, &full[i]);
-        if (++gg == G) { gg = 0; if (++t2 == RT) { t2 = 0; ++sg2; } }
+        if (++gg == G) { gg = 0; if (SW) { if (++sg2 == 2) { sg2 = 0; ++t2; } } else if (++t2 == RT) { t2 = 0; ++sg2; } }
       }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)g * kSlabK, xbytes,
                  &full[stage]);
       if (++stage == kp.stages) { stage = 0; rphase ^= 1u; }
-      if (++g == G) { g = 0; if (++t == RT) { t = 0; ++seg; } }
+      if (++g == G) { g = 0; if (SW) { if (++seg == 2) { seg = 0; ++t; } } else if (++t == RT) { t = 0; ++seg; } }
     }
     // drain: copies issued into stages the consumers may not have waited for
     if (misc[0]) {
@@ -345,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   // lanes taking part: M = 1 -> lane 0 only (the others leave), M > 1 -> all 32
   constexpr unsigned kPMask = (MT == 1) ? 1u : 0xffffffffu;
   auto produce8 = [&]() {
-    int g = s0 % G, t = (s0 / G) % RT, seg = (s0 / G) / RT;
+    int g = s0 % G, t = SW ? (s0 / G) / 2 : (s0 / G) % RT, seg = SW ? (s0 / G) % 2 : (s0 / G) / RT;
     int stage = 0;
     uint32_t rphase = 0;          // parity of the current round over the stage ring
     int it = 0;
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         mbar_expect_tx(&full[i], abytes + bbytes + xtx);
         bulk_g2s(st, plane + (int64_t)t2 * kSlabRows * L.rec, abytes, &full[i]);
         if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t2 * bbytes, bbytes, &full[i]);
-        if (++gg == G) { gg = 0; if (++t2 == RT) { t2 = 0; ++sg2; } }
+        if (++gg == G) { gg = 0; if (SW) { if (++sg2 == 2) { sg2 = 0; ++t2; } } else if (++t2 == RT) { t2 = 0; ++sg2; } }
       }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -404,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         cp_async_arrive_noinc(&full[stage]);
       }
       if (++stage == kp.stages) { stage = 0; rphase ^= 1u; }
-      if (++g == G) { g = 0; if (++t == RT) { t = 0; ++seg; } }
+      if (++g == G) { g = 0; if (SW) { if (++seg == 2) { seg = 0; ++t; } } else if (++t == RT) { t = 0; ++seg; } }
     }
     // drain: copies issued into stages the consumers may not have waited for. At
     // M > 1 the first-round stages not reached above still expect the lanes'
@@ -438,9 +444,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   const int g = lane >> 2, tq = lane & 3;
   float2* tbl = tbls + w * (16 * kTblStride);
   const int rA = 16 * w + g, rB = rA + 8;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  int T = s0 / G;                        // current tile (over segments x row tiles)
-  int tt = T % RT, seg = T / RT;
+  // accumulator words per thread: rows rA, rB x tokens 2tq, 2tq+1 (x gate, up for SW)
+  constexpr int NV = SW ? 8 : 4;
+  constexpr int UG = SW ? 2 : 1;          // k-group passes per unit (gate, up)
+  const int UL = UG * G;                  // slabs per unit
+  const int pstride = kSlabRows * kp.mt;  // partial words per pass
+  float acc[NV];
+#pragma unroll
+  for (int e = 0; e < NV; ++e) acc[e] = 0.f;
+  int T = s0 / UL;                        // current unit: a row tile of one segment (SW: of both)
+  int tt = SW ? T : T % RT, seg = SW ? 0 : T / RT;
   int stage = 0;
   uint32_t fphase = 0;                   // parity of the full barrier for this stage round
   bool aborted = false;
@@ -449,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     const Seg& sg = segs[seg];
     const int R = sg.R < MT ? sg.R : MT;
     const bool has_x = g < R;
-    const int head = T * G, tail = head + G;
+    const int head = T * UL, tail = head + UL;
     const int send = tail < s1 ? tail : s1;
     const bool full_cover = (s0 <= head) && (s1 >= tail);
     const bool reducer = (s0 <= head);
@@ -461,10 +474,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         } else {
           const uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
           const uint8_t* xrow0 = st + kp.x_off;
+          const int gk = (s - head) % G;
+          float* ap = acc + ((SW && s - head >= G) ? 4 : 0);
           // a last k-group narrower than 256: its padded blocks are zero and the x
           // beyond K is never copied, so the stale tail of each x row is zeroed (by
           // one thread of each warp, before that warp reads it)
-          if (kMayBeRagged && s == tail - 1 && kv_last < kSlabK) {
+          if (kMayBeRagged && gk == G - 1 && kv_last < kSlabK) {
             if (has_x && tq == 0) {
               uint8_t* xw = const_cast<uint8_t*>(xrow0) + g * kXStride;
               for (int o = kv_last * 2; o < kSlabK * 2; o += 4) *reinterpret_cast<uint32_t*>(xw + o) = 0u;
@@ -472,9 +487,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
             __syncwarp();
           }
           if (MT == 1) {
-            Slab<FMT, 1>::run(st, st + kp.b_off, xrow0, R, w, lane, tbl, acc);
+            Slab<FMT, 1>::run(st, st + kp.b_off, xrow0, R, w, lane, tbl, ap);
           } else {
-            Slab<FMT, MT>::run(st, st + kp.b_off, xrow0 + (has_x ? g : 0) * kXStride, R, w, lane, tbl, acc);
+            Slab<FMT, MT>::run(st, st + kp.b_off, xrow0 + (has_x ? g : 0) * kXStride, R, w, lane, tbl, ap);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[stage]);
@@ -483,40 +498,44 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       if (++stage == kp.stages) { stage = 0; fphase ^= 1u; }
     }
 
-    // ---- end of tile T: this thread owns rows rA, rB of it and tokens 2tq, 2tq+1 ----
+    // ---- end of unit T: this thread owns rows rA, rB of it and tokens 2tq, 2tq+1 ----
     {
       asm volatile("griddepcontrol.wait;" ::: "memory");   // workspace and y after earlier kernels
       if (MT == 1) {
         // unit columns: add the quad's partial sums of rows rA, rB (token 0)
-        float vA = acc[0], vB = acc[1];
-        vA += __shfl_xor_sync(0xffffffffu, vA, 1);
-        vB += __shfl_xor_sync(0xffffffffu, vB, 1);
-        vA += __shfl_xor_sync(0xffffffffu, vA, 2);
-        vB += __shfl_xor_sync(0xffffffffu, vB, 2);
-        acc[0] = vA; acc[1] = 0.f; acc[2] = vB; acc[3] = 0.f;
+#pragma unroll
+        for (int pp = 0; pp < UG; ++pp) {
+          float vA = acc[4 * pp], vB = acc[4 * pp + 1];
+          vA += __shfl_xor_sync(0xffffffffu, vA, 1);
+          vB += __shfl_xor_sync(0xffffffffu, vB, 1);
+          vA += __shfl_xor_sync(0xffffffffu, vA, 2);
+          vB += __shfl_xor_sync(0xffffffffu, vB, 2);
+          acc[4 * pp] = vA; acc[4 * pp + 1] = 0.f; acc[4 * pp + 2] = vB; acc[4 * pp + 3] = 0.f;
+        }
       }
       if (!full_cover && !reducer) {
         // peer: publish the partial sums. Each word is its own completion flag: a
         // stored word is never zero (+0.0 is stored as -0.0, which adds the same),
         // and the reducer waits for each word to become non-zero -- no fence, no flag.
         if (!aborted) {
-          unsigned* part = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)c * (kSlabRows * kp.mt);
+          unsigned* part = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)c * (UG * pstride);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
-            if (tok < R) st_relaxed(part + row * kp.mt + tok, nonzero_bits(acc[e]));
+          for (int e = 0; e < NV; ++e) {
+            const int tok = 2 * tq + (e & 1), row = ((e & 3) < 2) ? rA : rB;
+            if (tok < R) st_relaxed(part + (e >> 2) * pstride + row * kp.mt + tok, nonzero_bits(acc[e]));
           }
         }
       } else if (!full_cover && !aborted) {
         // reducer: add the peers' partial sums in CTA order, clearing each word after
         // reading it (the workspace is all zero again when the call ends). The words
-        // of up to four peers are loaded at once, so that their latencies overlap.
+        // of up to KB peers are loaded at once, so that their latencies overlap.
+        constexpr int KB = SW ? 2 : 4;
         int cp = c + 1;
         bool more = true;
         while (more && !aborted) {
-          int pid[4];
+          int pid[KB];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {          // the next four peers (-1: none)
+          for (int k = 0; k < KB; ++k) {          // the next KB peers (-1: none)
             pid[k] = -1;
             while (cp < P) {
               const int ps0 = range_start(cp), ps1 = range_start(cp + 1);
@@ -525,27 +544,27 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
               if (ps0 < ps1) { pid[k] = cp - 1; break; }   // an empty range publishes nothing
             }
           }
-          more = (pid[3] >= 0);
-          uint32_t u[4][4];
+          more = (pid[KB - 1] >= 0);
+          uint32_t u[KB][NV];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < KB; ++k) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+            for (int e = 0; e < NV; ++e) {
+              const int tok = 2 * tq + (e & 1), row = ((e & 3) < 2) ? rA : rB;
               u[k][e] = 0u;
               if (pid[k] >= 0 && tok < R)
                 u[k][e] = ld_relaxed(reinterpret_cast<const unsigned*>(kp.partials) +
-                                     (int64_t)pid[k] * (kSlabRows * kp.mt) + row * kp.mt + tok);
+                                     (int64_t)pid[k] * (UG * pstride) + (e >> 2) * pstride + row * kp.mt + tok);
             }
           }
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < KB; ++k) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+            for (int e = 0; e < NV; ++e) {
+              const int tok = 2 * tq + (e & 1), row = ((e & 3) < 2) ? rA : rB;
               if (pid[k] < 0 || tok >= R || aborted) continue;
-              unsigned* wp = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)pid[k] * (kSlabRows * kp.mt) +
-                             row * kp.mt + tok;
+              unsigned* wp = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)pid[k] * (UG * pstride) +
+                             (e >> 2) * pstride + row * kp.mt + tok;
               uint32_t v = u[k][e];
               if (v == 0u) {
                 const unsigned long long t0 = globaltimer();
@@ -562,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       }
       if (!aborted && (full_cover || reducer)) {
         const uint8_t* extras = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + L.k_groups * L.group_bytes;
+        const uint8_t* extras_u = extras + L.expert_bytes;     // SW: the up expert's
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
@@ -570,25 +590,32 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
           float v = acc[e];
           if (FMT == F_NVFP4) v *= *reinterpret_cast<const float*>(extras);
           if (FMT == F_FP8) v *= reinterpret_cast<const float*>(extras)[n];
+          if (SW) {
+            float u = acc[4 + e];
+            if (FMT == F_NVFP4) u *= *reinterpret_cast<const float*>(extras_u);
+            if (FMT == F_FP8) u *= reinterpret_cast<const float*>(extras_u)[n];
+            v = (v / (1.0f + expf(-v))) * u;               // silu(g) * u
+          }
           a.y[(int64_t)sg.yrow[tok] * L.N + n] = v;
         }
       }
+#pragma unroll
+      for (int e = 0; e < NV; ++e) acc[e] = 0.f;
     }
-    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     ++T;
-    if (++tt == RT) { tt = 0; ++seg; }
+    if (SW) { ++tt; } else if (++tt == RT) { tt = 0; ++seg; }
   }
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-WsPlan ws_plan_stream(int M, int64_t tiles_max, int num_ctas) {
+WsPlan ws_plan_stream(int M, int64_t tiles_max, int num_ctas, int passes) {
   (void)tiles_max;
   WsPlan p;
   const int mt = (M <= 1) ? 1 : 8;
   p.partials_off = 0;
-  p.partials_bytes = align_up((int64_t)num_ctas * kSlabRows * mt * 4, 256);
+  p.partials_bytes = align_up((int64_t)num_ctas * passes * kSlabRows * mt * 4, 256);
   p.total = p.partials_off + p.partials_bytes;
   return p;
 }
@@ -600,7 +627,7 @@ int num_sms_current_device() {
   return n;
 }
 
-template <int FMT, int MT>
+template <int FMT, int MT, bool SW>
 static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   int dev = 0, smem_max = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -630,7 +657,7 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   if (kp.stages < 2) return cudaErrorInvalidConfiguration;
   const int64_t pairs = (int64_t)a.M * a.topk;
   if (!slab_count_ok(a.L, a.ids ? (pairs < a.L.E ? pairs : a.L.E) : 1)) return cudaErrorInvalidValue;
-  const WsPlan plan = ws_plan_stream(MT, 0, a.num_ctas);
+  const WsPlan plan = ws_plan_stream(MT, 0, a.num_ctas, SW ? 2 : 1);
   kp.partials = reinterpret_cast<float*>(a.ws + plan.partials_off);
   const int smem = kp.stage_base + kp.stages * kp.stage_bytes;
   // opt in to the large dynamic shared memory once per device (not per launch, so
@@ -638,7 +665,7 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   static int opted[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (opted[dev] < smem) {
-    err = cudaFuncSetAttribute(stream_kernel<FMT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    err = cudaFuncSetAttribute(stream_kernel<FMT, MT, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     opted[dev] = smem;
   }
@@ -657,7 +684,7 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, stream_kernel<FMT, MT>, kp);
+  err = cudaLaunchKernelEx(&cfg, stream_kernel<FMT, MT, SW>, kp);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -666,8 +693,13 @@ template <int FMT>
 static cudaError_t launch_fmt(const StreamArgs& a, cudaStream_t s, int* variant) {
   const bool grouped = a.ids != nullptr;
   *variant = grouped ? 3 : (a.M <= 1 ? 1 : 2);
-  if (a.M <= 1) return launch_t<FMT, 1>(a, s);   // grouped at M = 1: one x row per expert
-  return launch_t<FMT, 8>(a, s);
+  if (a.swiglu) {
+    *variant = 9;
+    if (a.M <= 1) return launch_t<FMT, 1, true>(a, s);
+    return launch_t<FMT, 8, true>(a, s);
+  }
+  if (a.M <= 1) return launch_t<FMT, 1, false>(a, s);   // grouped at M = 1: one x row per expert
+  return launch_t<FMT, 8, false>(a, s);
 }
 
 cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant) {

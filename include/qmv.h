@@ -75,7 +75,7 @@ typedef enum {
 } qmv_status;
 
 /* Entry ids for qmv_workspace_size. */
-enum { QMV_ENTRY_GEMV = 1, QMV_ENTRY_GROUPED = 2, QMV_ENTRY_W4A4 = 3 };
+enum { QMV_ENTRY_GEMV = 1, QMV_ENTRY_GROUPED = 2, QMV_ENTRY_W4A4 = 3, QMV_ENTRY_SWIGLU = 4 };
 
 /* Largest decode batch served by qmv_gemv / qmv_grouped (M rows of x). */
 #define QMV_MAX_M 8
@@ -169,6 +169,19 @@ qmv_status qmv_grouped(qmv_fmt fmt, const void* tower, const int32_t* expert_ids
                        int64_t N, int64_t K, int64_t E, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
 
+/* Fused gate|up decode GEMV with the SwiGLU epilogue, M = 1..8:
+ *   h[m][n] = silu(g) * u,  g = sum_k Wg[n][k] x[m][k],  u = sum_k Wu[n][k] x[m][k],
+ *   silu(g) = g / (1 + exp(-g)),
+ * one pass over the two matrices that share x: the MLP's gate/up projection read as
+ * one, with the SwiGLU fused behind it ("Qwen3.8-27B on one Tenstorrent P150",
+ * "4. Measuring the ceiling, and lots of dead ends"). tower: the device layout of a 2-expert tower,
+ * gate = expert 0, up = expert 1 (qmv_pack with E = 2). x: device bf16 [M][K].
+ * h: device fp32 [M][N], fully overwritten. ws: device,
+ * qmv_workspace_size(QMV_ENTRY_SWIGLU, ...) bytes, zero-filled once (as for
+ * qmv_gemv). Each gate and up row is streamed from HBM once per call. */
+qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, float* h, int M,
+                           int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* NVFP4 activation quantizer (W4A4 prefill): per 16-value block of bf16 x[M][K],
  * s_b = e4m3_rne_sat(amax_b / (6 x_scale)); codes = e2m1_rne_sat(x / (s_b x_scale)),
  * zero when s_b is zero. x_scale: the static per-site activation scale.
@@ -198,7 +211,7 @@ const char* qmv_status_str(qmv_status s);
 /* Route id of the kernel the last successful call on this host thread launched:
  * format * 100 + variant (1 = M=1 streaming CUDA-core GEMV, 2 = M>1 streaming
  * mma.sync GEMV, 3 = grouped, 4 = W4A4 tcgen05, 5 = dequant, 6 = pack,
- * 7 = quantize, 8 = activation quantizer). Test hook. */
+ * 7 = quantize, 8 = activation quantizer, 9 = fused gate|up SwiGLU). Test hook. */
 int qmv_last_route(void);
 
 /* Read (and, if reset != 0, clear) the device status word of the current

@@ -74,6 +74,8 @@ def _load():
     lib.or_unique_experts.argtypes = [P, I64, P]
     lib.or_quant_act_nvfp4.restype = None
     lib.or_quant_act_nvfp4.argtypes = [P, I64, I64, ctypes.c_float, P, P]
+    lib.or_swiglu_f64.restype = None
+    lib.or_swiglu_f64.argtypes = [P, P, I64, P]
     _lib = lib
     return lib
 
@@ -179,6 +181,16 @@ def quant_act_nvfp4(x_bf16: np.ndarray, x_scale: float):
     scales = np.zeros((M, K // 16), dtype=np.uint8)
     _load().or_quant_act_nvfp4(_ptr(x), M, K, float(x_scale), _ptr(codes), _ptr(scales))
     return codes, scales
+
+
+def swiglu_f64(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """h = silu(g) * u elementwise, fp64 (the SwiGLU behind the gate/up projection)."""
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    assert g.shape == u.shape
+    h = np.empty_like(g)
+    _load().or_swiglu_f64(_ptr(g), _ptr(u), g.size, _ptr(h))
+    return h
 
 
 def grouped_f64(tower_canon_rows, ids: np.ndarray, x_bf16: np.ndarray, x_per_pair: bool):

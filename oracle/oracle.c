@@ -434,3 +434,12 @@ void or_quant_act_nvfp4(const uint16_t* x_bf16, int64_t M, int64_t K, float x_sc
             }
         }
 }
+
+/* SwiGLU of the gate/up projection read as one ("Qwen3.8-27B on one Tenstorrent
+ * P150", "4. Measuring the ceiling, and lots of dead ends": the MLP gate/up
+ * projection and its fused SwiGLU; "A 320B MoE on a free Kaggle TPU": the gate
+ * matrix inside a SwiGLU): h = silu(g) * u with silu(g) = g / (1 + exp(-g)), in
+ * fp64, elementwise over n values. */
+void or_swiglu_f64(const double* g, const double* u, int64_t n, double* h) {
+    for (int64_t i = 0; i < n; i++) h[i] = (g[i] / (1.0 + exp(-g[i]))) * u[i];
+}

@@ -70,6 +70,9 @@ int64_t or_unique_experts(const int32_t* ids, int64_t n, int32_t* out);
 void or_quant_act_nvfp4(const uint16_t* x_bf16, int64_t M, int64_t K, float x_scale,
                         uint8_t* codes, uint8_t* scales);
 
+/* SwiGLU: h = silu(g) * u, silu(g) = g / (1 + exp(-g)), fp64 elementwise */
+void or_swiglu_f64(const double* g, const double* u, int64_t n, double* h);
+
 #ifdef __cplusplus
 }
 #endif

@@ -469,3 +469,28 @@ def test_quant_act_nvfp4_brute_force():
                     mag = 7
                 assert (c & 7) == mag and (c >> 3) == (1 if np.signbit(v) else 0)
     assert np.all(codes[1, 8:16] == 0) and scales[1, 1] == 0
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU: closed forms and the identity silu(x) - silu(-x) = x
+# ---------------------------------------------------------------------------
+def test_swiglu_closed_forms():
+    import math
+    ln3 = math.log(3.0)
+    # sigmoid(ln 3) = 3/4, sigmoid(-ln 3) = 1/4, sigmoid(0) = 1/2
+    g = np.array([0.0, ln3, -ln3, 2 * math.log(2.0), 40.0, -40.0])
+    u = np.array([5.0, 2.0, 2.0, 1.0, 0.5, 3.0])
+    h = oracle.swiglu_f64(g, u)
+    want = np.array([0.0, ln3 * 0.75 * 2.0, -ln3 * 0.25 * 2.0, 2 * math.log(2.0) * 0.8, 20.0, 0.0])
+    assert np.allclose(h, want, rtol=1e-15, atol=1e-15)
+
+
+def test_swiglu_odd_part_is_identity():
+    rng = np.random.default_rng(3)
+    x = rng.normal(size=1000) * 4.0
+    ones = np.ones_like(x)
+    d = oracle.swiglu_f64(x, ones) - oracle.swiglu_f64(-x, ones)
+    assert np.allclose(d, x, rtol=1e-14, atol=1e-14)
+    # linear in u
+    u = rng.normal(size=1000)
+    assert np.allclose(oracle.swiglu_f64(x, 3.0 * u), 3.0 * oracle.swiglu_f64(x, u), rtol=1e-15, atol=1e-15)
