@@ -51,6 +51,10 @@ WORKLOADS = {
     "q4k_mlp_m1": dict(fmt="q4_k", M=1, mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
                                               ("down", QWEN_HIDDEN, QWEN_MLP)],
                        desc="Q4_K decode MLP, Qwen3.8-27B geometry: gate+up [17408,5120], down [5120,17408], M=1"),
+    "q4k_mlp_fused_m1": dict(fmt="q4_k", M=1, fused=True,
+                             mats=[("gate|up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
+                             desc="Q4_K decode MLP, Qwen3.8-27B geometry, M=1: fused gate|up [2 x 17408, 5120] "
+                                  "with the SwiGLU epilogue, then down [5120,17408]"),
     "q4k_mlp_m8": dict(fmt="q4_k", M=8, mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
                                               ("down", QWEN_HIDDEN, QWEN_MLP)],
                        desc="Q4_K decode MLP, Qwen3.8-27B geometry, M=8 (speculative verify block)"),
@@ -90,7 +94,8 @@ DEFAULT_WORKLOAD = "q4k_mlp_m1"
 DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, "q6k_head_m8": 2000,
                  "q6k_qkv_m1": 40000, "q6k_qkv_m8": 40000, "nvfp4_mlp_m1": 20000, "nvfp4_mlp_m8": 20000,
                  "fp8_m1": 40000, "fp8_m8": 40000, "q8_0_tiny": 20000, "tower_m1": 20000,
-                 "tower_m4": 10000, "tower_m8": 5000, "nvfp4_w4a4_m512": 2000}
+                 "tower_m4": 10000, "tower_m8": 5000, "nvfp4_w4a4_m512": 2000,
+                 "q4k_mlp_fused_m1": 20000}
 
 METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"
 CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q6_k": 210 / 256, "nvfp4": 18 / 32, "fp8_row": 1.0}
@@ -250,18 +255,21 @@ class DeviceWorkload:
         self.fmt, self.M = w["fmt"], w["M"]
         self.tower = w.get("tower", False)
         self.w4a4 = w.get("w4a4", False)
+        self.fused = w.get("fused", False)
         self.E = w.get("E", 1)
         self.topk = w.get("topk", 1)
         self.mats = w["mats"]
         torch.cuda.synchronize()
-        base = [build_packed(q, self.fmt, 100 + i, N, K, self.E, dev) for i, (_, N, K) in enumerate(self.mats)]
+        base = [build_packed(q, self.fmt, 100 + i, N, K, 2 if (self.fused and i == 0) else self.E, dev)
+                for i, (_, N, K) in enumerate(self.mats)]
         torch.cuda.synchronize()
         # bytes a step streams, to size the rotation
         if self.tower:
             per_expert = [canon_bytes(self.fmt, N, K) for _, N, K in self.mats]
             step_w = sum(per_expert) * min(self.E, self.M * self.topk)
         else:
-            step_w = sum(canon_bytes(self.fmt, N, K) for _, N, K in self.mats)
+            step_w = sum(canon_bytes(self.fmt, N, K) * (2 if (self.fused and i == 0) else 1)
+                         for i, (_, N, K) in enumerate(self.mats))
         self.copies = max(2, math.ceil(4 * L2_BYTES / max(step_w, 1)) + 1)
         self.packed = [base] + [[b.clone() for b in base] for _ in range(self.copies - 1)]
         # activations, outputs, workspaces
@@ -272,6 +280,8 @@ class DeviceWorkload:
             ysh = (self.M, self.topk, N) if self.tower else (self.M, N)
             self.y.append(torch.empty(ysh, dtype=torch.float32, device=dev))
             entry = q.QMV_ENTRY_GROUPED if self.tower else (q.QMV_ENTRY_W4A4 if self.w4a4 else q.QMV_ENTRY_GEMV)
+            if self.fused and i == 0:
+                entry = q.QMV_ENTRY_SWIGLU
             self.ws.append(q.workspace(entry, self.fmt, self.M, N, K, self.E, self.topk, device=dev))
         # W4A4: the static activation scale of each x (amax / (448 * 6)), computed once
         self.x_scale = [float(x.float().abs().max()) / 2688.0 for x in self.x] if self.w4a4 else []
@@ -299,7 +309,7 @@ class DeviceWorkload:
                 u = self.unique[s % len(self.unique)]
                 tot += u * canon_bytes(self.fmt, N, K) + xb + yb + self.M * self.topk * 4
             else:
-                tot += canon_bytes(self.fmt, N, K) + xb + yb
+                tot += canon_bytes(self.fmt, N, K) * (2 if (self.fused and i == 0) else 1) + xb + yb
         return tot
 
     def launch_step(self, s):
@@ -309,6 +319,8 @@ class DeviceWorkload:
             if self.tower:
                 q.qmv_grouped(self.fmt, self.packed[c][i], self.ids[s % len(self.ids)], self.x[i], N, K, self.E,
                               self.ws[i], x_per_pair=(i == len(self.mats) - 1), y=self.y[i])
+            elif self.fused and i == 0:
+                q.qmv_gemv_swiglu(self.fmt, self.packed[c][i], self.x[i], N, K, self.ws[i], h=self.y[i])
             elif self.w4a4:
                 q.qmv_gemm_nvfp4_w4a4(self.packed[c][i], self.x[i], self.x_scale[i], N, K, self.ws[i], y=self.y[i])
             else:
