@@ -20,8 +20,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
-Q8_0, Q4_K, Q6_K, NVFP4, FP8_ROW = 1, 2, 3, 4, 5
-FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "q6_k": Q6_K, "nvfp4": NVFP4, "fp8_row": FP8_ROW}
+Q8_0, Q4_K, Q6_K, NVFP4, FP8_ROW, Q5_K = 1, 2, 3, 4, 5, 6
+FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "q6_k": Q6_K, "nvfp4": NVFP4, "fp8_row": FP8_ROW,
+           "q5_k": Q5_K}
 
 _lib = None
 

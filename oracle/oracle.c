@@ -16,7 +16,10 @@
  *    Qwen3.8-27B", section "What the custom path actually does").
  * Byte sizes: Q8_0 34 B / 32 values, Q6_K 210 B / 256 ("#3030", "Budget on the
  * 32 GB P150"); Q4_K 144 B / 256 (fp16 d, fp16 dmin, 12 B of 6-bit scales and
- * mins, 128 B of nibbles), NVFP4 16-value blocks with an E4M3 scale and one fp32
+ * mins, 128 B of nibbles), Q5_K 176 B / 256 (the 5-bit member of the same K-quant
+ * family, named with Q4_K/Q6_K/Q8_0 in "#3030" scope item 1 and owed by the
+ * grouped kernel in its "Re-anchor" comment; the pages print no layout for it, so
+ * it is Q4_K's header and nibbles plus one 32-byte plane of fifth bits), NVFP4 16-value blocks with an E4M3 scale and one fp32
  * tensor scale, FP8 E4M3 with one fp32 scale per row.
  *
  * Where the pages give no bit-level layout, the reading taken is the one written
@@ -123,6 +126,7 @@ int64_t or_block_values(int fmt) {
     switch (fmt) {
     case OR_Q8_0: return 32;
     case OR_Q4_K: return 256;
+    case OR_Q5_K: return 256;
     case OR_Q6_K: return 256;
     case OR_NVFP4: return 16;
     case OR_FP8_ROW: return 1;
@@ -134,6 +138,7 @@ int64_t or_canon_bytes(int fmt, int64_t rows, int64_t K) {
     switch (fmt) {
     case OR_Q8_0: return rows * (K / 32) * 34;
     case OR_Q4_K: return rows * (K / 256) * 144;
+    case OR_Q5_K: return rows * (K / 256) * 176;
     case OR_Q6_K: return rows * (K / 256) * 210;
     case OR_NVFP4: return rows * (K / 2) + rows * (K / 16) + 4;
     case OR_FP8_ROW: return rows * K + rows * 4;
@@ -215,6 +220,43 @@ static void enc_q4_k_block(const float* x, uint8_t* blk) {
     }
 }
 
+/* Q5_K: Q4_K's quantizer with 32 levels per sub-block instead of 16 */
+static void enc_q5_k_block(const float* x, uint8_t* blk) {
+    float s[8], mn[8], smax = 0.0f, mmax = 0.0f;
+    for (int j = 0; j < 8; j++) {
+        float lo = 0.0f, hi = x[32 * j];
+        for (int i = 0; i < 32; i++) {
+            float v = x[32 * j + i];
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+        s[j] = (hi - lo) / 31.0f;
+        mn[j] = -lo;
+        if (s[j] > smax) smax = s[j];
+        if (mn[j] > mmax) mmax = mn[j];
+    }
+    uint16_t d = or_f32_to_fp16(smax / 63.0f), dmin = or_f32_to_fp16(mmax / 63.0f);
+    float dd = or_fp16_to_f32(d), dm = or_fp16_to_f32(dmin);
+    memset(blk, 0, 176);
+    wr16(blk, d);
+    wr16(blk + 2, dmin);
+    for (int j = 0; j < 8; j++) {
+        int sc = (dd == 0.0f) ? 0 : (int)clampf(nearbyintf(s[j] / dd), 0.0f, 63.0f);
+        int mq = (dm == 0.0f) ? 0 : (int)clampf(nearbyintf(mn[j] / dm), 0.0f, 63.0f);
+        q4k_set_field(blk + 4, j, sc);
+        q4k_set_field(blk + 4, 8 + j, mq);
+        float den = dd * (float)sc;
+        float off = dm * (float)mq;
+        for (int i = 0; i < 32; i++) {
+            int e = 32 * j + i;
+            float num = x[e] + off;
+            int q = (den == 0.0f) ? 0 : (int)clampf(nearbyintf(num / den), 0.0f, 31.0f);
+            blk[16 + e / 8] |= (uint8_t)(((q >> 4) & 1) << (e & 7));
+            blk[48 + e / 2] |= (uint8_t)((q & 15) << (4 * (e & 1)));
+        }
+    }
+}
+
 static void enc_q6_k_block(const float* x, uint8_t* blk) {
     float s[16], smax = 0.0f;
     for (int j = 0; j < 16; j++) {
@@ -245,14 +287,15 @@ int or_encode(int fmt, const float* W, int64_t rows, int64_t K, float tensor_sca
               uint8_t* canon) {
     int64_t bv = or_block_values(fmt);
     if (bv == 0 || K % bv != 0) return 1;
-    if (fmt == OR_Q8_0 || fmt == OR_Q4_K || fmt == OR_Q6_K) {
-        int64_t bb = (fmt == OR_Q8_0) ? 34 : (fmt == OR_Q4_K ? 144 : 210);
+    if (fmt == OR_Q8_0 || fmt == OR_Q4_K || fmt == OR_Q5_K || fmt == OR_Q6_K) {
+        int64_t bb = (fmt == OR_Q8_0) ? 34 : (fmt == OR_Q4_K ? 144 : (fmt == OR_Q5_K ? 176 : 210));
         for (int64_t r = 0; r < rows; r++)
             for (int64_t b = 0; b < K / bv; b++) {
                 const float* x = W + r * K + b * bv;
                 uint8_t* blk = canon + (r * (K / bv) + b) * bb;
                 if (fmt == OR_Q8_0) enc_q8_0_block(x, blk);
                 else if (fmt == OR_Q4_K) enc_q4_k_block(x, blk);
+                else if (fmt == OR_Q5_K) enc_q5_k_block(x, blk);
                 else enc_q6_k_block(x, blk);
             }
         return 0;
@@ -299,6 +342,7 @@ int or_encode(int fmt, const float* W, int64_t rows, int64_t K, float tensor_sca
  * BlockToFloat. fp32, the op order written here is the canonical one:
  *   Q8_0 : w = d * q                                   (exact)
  *   Q4_K : w = (d * sc_j) * q - (dmin * m_j)           (one rounding)
+ *   Q5_K : the same expression, q = lo | hi << 4 in 0..31 (one rounding)
  *   Q6_K : w = (d * sc_j) * (q - 32)                   (exact)
  *   NVFP4: w = (e2m1(c) * e4m3(s_b)) * s_T             (one rounding)
  *   FP8  : w = e4m3(c) * s_row                         (one rounding)
@@ -348,6 +392,21 @@ int or_block_to_float(int fmt, const uint8_t* canon, int64_t rows, int64_t K, fl
                     int j = e / 32;
                     int sc = q4k_field(blk + 4, j), m = q4k_field(blk + 4, 8 + j);
                     int q = (blk[16 + e / 2] >> (4 * (e & 1))) & 15;
+                    float a = d * (float)sc;
+                    float c = dmin * (float)m;
+                    w[b * 256 + e] = a * (float)q - c;
+                }
+            }
+        } else if (fmt == OR_Q5_K) {
+            for (int64_t b = 0; b < K / 256; b++) {
+                const uint8_t* blk = canon + (r * (K / 256) + b) * 176;
+                float d = or_fp16_to_f32(rd16(blk)), dmin = or_fp16_to_f32(rd16(blk + 2));
+                for (int e = 0; e < 256; e++) {
+                    int j = e / 32;
+                    int sc = q4k_field(blk + 4, j), m = q4k_field(blk + 4, 8 + j);
+                    int lo = (blk[48 + e / 2] >> (4 * (e & 1))) & 15;
+                    int hi = (blk[16 + e / 8] >> (e & 7)) & 1;
+                    int q = lo | (hi << 4);
                     float a = d * (float)sc;
                     float c = dmin * (float)m;
                     w[b * 256 + e] = a * (float)q - c;

@@ -19,6 +19,10 @@
  *         scales = 96-bit LSB-first bitstream of sixteen 6-bit fields,
  *         fields 0..7 = sub-block scales sc_j, fields 8..15 = sub-block mins m_j;
  *         quant byte b: low nibble = element 2b, high nibble = element 2b+1
+ *   Q5_K 176 B per 256 values: fp16 d | fp16 dmin | 12 B scales | 32 B qh | 128 B qs
+ *         scales exactly as Q4_K; qs exactly as Q4_K's quants (low 4 bits);
+ *         qh = 256-bit LSB-first bitstream, bit e = 5th bit (value 16) of element e;
+ *         q = lo | hi << 4 in 0..31
  *   Q6_K 210 B per 256 values: 128 B ql | 64 B qh | 16 x int8 scales | fp16 d
  *         ql byte b: low nibble = low 4 bits of element 2b, high = of 2b+1;
  *         qh byte b: bits 2i..2i+1 = high 2 bits of element 4b+i (i = 0..3)
@@ -37,7 +41,7 @@
 extern "C" {
 #endif
 
-enum { OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q6_K = 3, OR_NVFP4 = 4, OR_FP8_ROW = 5 };
+enum { OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q6_K = 3, OR_NVFP4 = 4, OR_FP8_ROW = 5, OR_Q5_K = 6 };
 
 /* scalar number formats */
 float or_fp16_to_f32(uint16_t h);

@@ -206,6 +206,57 @@ def test_q4_k_handbuilt_values():
     assert np.all(w == 456.75)
 
 
+def _q5k_block(d16, dmin16, sc, mn, q):
+    """Q5_K as read: Q4_K's header, a 32-byte plane of fifth bits, then the nibbles."""
+    q4 = _q4k_block(d16, dmin16, sc, mn, [v & 15 for v in q])
+    qh = 0
+    for e in range(256):
+        qh |= ((q[e] >> 4) & 1) << e
+    return q4[:16] + qh.to_bytes(32, "little") + q4[16:]
+
+
+def test_q5_k_handbuilt_values():
+    blk = _q5k_block(0x3C00, 0x3C00, [j + 1 for j in range(8)], list(range(8)),
+                     [e % 32 for e in range(256)])
+    assert len(blk) == 176
+    w = oracle.block_to_float("q5_k", np.frombuffer(blk, np.uint8), 1, 256)[0]
+    # w = sc_j * q - m_j with d = dmin = 1, q = e mod 32, sc_j = j + 1, m_j = j
+    # e=0: 0      e=16: j=0, q=16 -> 16      e=31: q=31 -> 31      e=33: j=1, q=1 -> 2-1 = 1
+    # e=50: j=1, q=18 -> 36-1 = 35     e=100: j=3, q=4 -> 16-3 = 13     e=255: j=7, q=31 -> 248-7 = 241
+    hand = {0: 0.0, 16: 16.0, 31: 31.0, 33: 1.0, 50: 35.0, 100: 13.0, 255: 241.0}
+    for e, v in hand.items():
+        assert w[e] == v, (e, w[e], v)
+    # d = 0.5, dmin = 0.25, sc = m = 63:  q = 16 -> 504 - 15.75;  q = 31 -> 976.5 - 15.75
+    blk = _q5k_block(0x3800, 0x3400, [63] * 8, [63] * 8, [16] * 128 + [31] * 128)
+    w = oracle.block_to_float("q5_k", np.frombuffer(blk, np.uint8), 1, 256)[0]
+    assert np.all(w[:128] == 488.25) and np.all(w[128:] == 960.75)
+
+
+@pytest.mark.parametrize("e_hot", [0, 7, 8, 77, 200, 255])
+def test_q5_k_fifth_bit_position(e_hot):
+    """One set bit in the qh plane at byte e/8, bit e%8 moves exactly element e by 16."""
+    blk = bytearray(176)
+    blk[0:2] = (0x3C00).to_bytes(2, "little")
+    bits = sum(1 << (6 * f) for f in range(8))          # sc_j = 1, m_j = 0
+    blk[4:16] = bits.to_bytes(12, "little")
+    blk[16 + e_hot // 8] = 1 << (e_hot % 8)
+    w = oracle.block_to_float("q5_k", np.frombuffer(bytes(blk), np.uint8), 1, 256)[0]
+    expect = np.zeros(256, np.float32)
+    expect[e_hot] = 16.0
+    assert np.array_equal(w, expect)
+
+
+def test_q5_k_without_fifth_bits_is_q4_k():
+    """A Q5_K block whose qh plane is zero decodes exactly like the Q4_K block with
+    the same header and nibbles (the 5-bit format extends the 4-bit one)."""
+    W = synth.weights(21, 2, 512).numpy()
+    c4 = oracle.encode("q4_k", W).reshape(2, 2, 144)
+    c5 = np.concatenate([c4[..., :16], np.zeros((2, 2, 32), np.uint8), c4[..., 16:]], -1)
+    D4 = oracle.block_to_float("q4_k", c4.reshape(-1), 2, 512)
+    D5 = oracle.block_to_float("q5_k", c5.reshape(-1), 2, 512)
+    assert np.array_equal(D4, D5)
+
+
 def test_q6_k_handbuilt():
     # d = 0.5, sc_j = +1 (even j) / -1 (odd j), q_e = e mod 64  ->  w = 0.5 (q-32) sc_j
     blk = bytearray(210)
@@ -297,6 +348,29 @@ def test_roundtrip_q4_k():
     assert np.all(D[0] == 0)
     rel = np.linalg.norm(W[3:] - D[3:]) / np.linalg.norm(W[3:])
     assert rel < 0.12          # 4-bit asymmetric rounding on Gaussian data
+
+
+def test_roundtrip_q5_k():
+    W = _data(8, 1024)
+    c = oracle.encode("q5_k", W)
+    D = oracle.block_to_float("q5_k", c, 8, 1024)
+    Wb = W.reshape(8, 4, 8, 32)
+    lo = np.minimum(0, Wb.min(-1))
+    hi = Wb.max(-1)
+    s = (hi - lo) / 31
+    cb = c.reshape(8, 4, 176).astype(np.uint16)
+    dd = _f16(cb[:, :, 0] | (cb[:, :, 1] << 8))
+    dm = _f16(cb[:, :, 2] | (cb[:, :, 3] << 8))
+    # half a step of the ideal 31-level grid, plus the 6-bit rounding of sc_j
+    # (up to 31 levels of it) and of m_j, plus fp16 rounding of d, dmin
+    bound = (0.5 * s + 31 * 0.5 * dd[..., None] + 0.5 * dm[..., None]) * (1 + 2**-9) + 1e-7
+    err = np.abs(W - D).reshape(8, 4, 8, 32).max(-1)
+    assert np.all(err <= bound)
+    assert np.all(D[0] == 0)
+    rel5 = np.linalg.norm(W[3:] - D[3:]) / np.linalg.norm(W[3:])
+    D4 = oracle.block_to_float("q4_k", oracle.encode("q4_k", W), 8, 1024)
+    rel4 = np.linalg.norm(W[3:] - D4[3:]) / np.linalg.norm(W[3:])
+    assert rel5 < 0.07 and rel5 < 0.65 * rel4   # one more bit: about half the error
 
 
 def test_roundtrip_q6_k():
@@ -391,6 +465,31 @@ def test_q4_k_factored_identity_exact():
         sx = sum(Fraction(float(x[e])) for e in range(32 * j, 32 * j + 32))
         rhs += Fraction(d) * sc * sq - Fraction(dmin) * m * sx
     # the decoded w differs from (d sc) q - dmin m only by its one fp32 rounding
+    tol = sum(abs(Fraction(float(x[k]))) for k in range(256)) * Fraction(float(np.abs(D).max())) * Fraction(1, 2**23)
+    assert abs(lhs - rhs) <= tol
+
+
+def test_q5_k_factored_identity_exact():
+    """The Q5_K sum factors like Q4_K's with q = lo | hi << 4 (rationals)."""
+    W = synth.weights(10, 1, 256).numpy()
+    c = oracle.encode("q5_k", W)
+    D = oracle.block_to_float("q5_k", c, 1, 256)[0]
+    x = synth.activations(10, 1, 256).float().numpy()[0]
+    blk = c.tobytes()
+    d = float(_f16(int.from_bytes(blk[0:2], "little")))
+    dmin = float(_f16(int.from_bytes(blk[2:4], "little")))
+    bits = int.from_bytes(blk[4:16], "little")
+    qh = int.from_bytes(blk[16:48], "little")
+    assert qh != 0                                      # the fifth bits are in use
+    lhs = sum(Fraction(float(D[k])) * Fraction(float(x[k])) for k in range(256))
+    rhs = Fraction(0)
+    for j in range(8):
+        sc = (bits >> (6 * j)) & 63
+        m = (bits >> (6 * (8 + j))) & 63
+        sq = sum(Fraction(((blk[48 + e // 2] >> (4 * (e & 1))) & 15) | (((qh >> e) & 1) << 4))
+                 * Fraction(float(x[e])) for e in range(32 * j, 32 * j + 32))
+        sx = sum(Fraction(float(x[e])) for e in range(32 * j, 32 * j + 32))
+        rhs += Fraction(d) * sc * sq - Fraction(dmin) * m * sx
     tol = sum(abs(Fraction(float(x[k]))) for k in range(256)) * Fraction(float(np.abs(D).max())) * Fraction(1, 2**23)
     assert abs(lhs - rhs) <= tol
 
