@@ -58,6 +58,12 @@ WORKLOADS = {
     "q4k_mlp_m8": dict(fmt="q4_k", M=8, mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
                                               ("down", QWEN_HIDDEN, QWEN_MLP)],
                        desc="Q4_K decode MLP, Qwen3.8-27B geometry, M=8 (speculative verify block)"),
+    "q5k_mlp_m1": dict(fmt="q5_k", M=1, mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
+                                              ("down", QWEN_HIDDEN, QWEN_MLP)],
+                       desc="Q5_K decode MLP, Qwen3.8-27B geometry: gate+up [17408,5120], down [5120,17408], M=1"),
+    "q5k_mlp_m8": dict(fmt="q5_k", M=8, mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
+                                              ("down", QWEN_HIDDEN, QWEN_MLP)],
+                       desc="Q5_K decode MLP, Qwen3.8-27B geometry, M=8"),
     "q6k_head_m1": dict(fmt="q6_k", M=1, mats=[("head", QWEN_VOCAB, QWEN_HIDDEN)],
                         desc="Q6_K untied output head [248320,5120], M=1"),
     "q6k_head_m8": dict(fmt="q6_k", M=8, mats=[("head", QWEN_VOCAB, QWEN_HIDDEN)],
@@ -95,10 +101,11 @@ DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, 
                  "q6k_qkv_m1": 40000, "q6k_qkv_m8": 40000, "nvfp4_mlp_m1": 20000, "nvfp4_mlp_m8": 20000,
                  "fp8_m1": 40000, "fp8_m8": 40000, "q8_0_tiny": 20000, "tower_m1": 20000,
                  "tower_m4": 10000, "tower_m8": 5000, "nvfp4_w4a4_m512": 2000,
-                 "q4k_mlp_fused_m1": 20000}
+                 "q4k_mlp_fused_m1": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000}
 
 METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"
-CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q6_k": 210 / 256, "nvfp4": 18 / 32, "fp8_row": 1.0}
+CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q5_k": 176 / 256, "q6_k": 210 / 256,
+                   "nvfp4": 18 / 32, "fp8_row": 1.0}
 
 
 def canon_bytes(fmt, N, K):

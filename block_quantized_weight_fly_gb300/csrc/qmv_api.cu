@@ -32,7 +32,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 qmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ECUDA; }
 
-bool valid_fmt(int f) { return f >= QMV_Q8_0 && f <= QMV_FP8_ROW; }
+bool valid_fmt(int f) { return f >= QMV_Q8_0 && f <= QMV_Q5_K; }
 
 }  // namespace
 

@@ -7,6 +7,8 @@
 // k-group g there is a plane of n_pad row records:
 //
 //   Q4_K : record = the canonical 144-byte superblock (d, dmin, 12 B scales, 128 B nibbles)
+//   Q5_K : record = the 16-byte header (d, dmin, 12 B scales) | 128 B of 5-bit words |
+//          32 B of nibble words (below)                                      (176 B)
 //   NVFP4: plane A = E2M1 codes, 128 B per row, in tensor-core tiles (below)  (128 B)
 //          plus a plane B of E4M3 block scales, 16 B per row, in the tile layout
 //          the tensor memory copy of block scale factors takes                 (16 B)
@@ -27,6 +29,13 @@
 // So each word stores the fields of consecutive element pairs at nibbles (p, p+4):
 //   Q4_K : word w of a 32-value chunk = elements 8w..8w+7; element 8w+2p -> nibble p,
 //          element 8w+2p+1 -> nibble p+4                              (p = 0..3)
+//   Q5_K : 5-bit fields, decoded by the same AND-OR with mask 0x001F001F. Word w of a
+//          chunk (its elements 8w..8w+7): the pairs (8w+2p, 8w+2p+1), p = 0..2, as
+//          5-bit fields at bits (5p, 16+5p); bits 15 and 31 = the fifth bits of
+//          elements 8w+6 and 8w+7. The low nibbles of those two elements sit in the
+//          chunk's shared nibble word, at nibbles w and w+4. So a pair costs one
+//          shift and one AND-OR, the last pair two of each; the record holds the
+//          canonical 176 bytes' information in 176 bytes.
 //   Q8_0 : byte u = q XOR 0x80 (0..255, the code plus 128); word w = elements 4w..4w+3:
 //          low nibbles of elements (4w, 4w+1) -> nibbles (0, 4), of (4w+2, 4w+3) ->
 //          (1, 5); high nibbles of (4w, 4w+1) -> (2, 6), of (4w+2, 4w+3) -> (3, 7)
@@ -48,7 +57,7 @@
 // 16*(r%32) + 4*(r/32) + kb -- the 32 x 16-byte layout that tcgen05.cp.32x128b.warpx4
 // replicates into the four lane quadrants of tensor memory.
 //
-// Records of 144, 208 and 272 bytes are odd multiples of 16, so 8 consecutive rows
+// Records of 144, 176, 208 and 272 bytes are odd multiples of 16, so 8 consecutive rows
 // read at the same offset hit 8 different 16-byte bank groups; the 256-byte FP8
 // record gets the same property from its rotation.
 //
@@ -76,7 +85,7 @@ constexpr int kHeaderBytes = 256;
 constexpr uint32_t kMagic = 0x31564D51u;  // "QMV1"
 constexpr uint32_t kVersion = 5;
 
-enum Fmt { F_Q8_0 = 1, F_Q4_K = 2, F_Q6_K = 3, F_NVFP4 = 4, F_FP8 = 5 };
+enum Fmt { F_Q8_0 = 1, F_Q4_K = 2, F_Q6_K = 3, F_NVFP4 = 4, F_FP8 = 5, F_Q5_K = 6 };
 
 struct PackedHeader {                 // first 256 bytes of a packed buffer
   uint32_t magic, version, fmt, reserved;
@@ -88,7 +97,7 @@ __host__ __device__ inline int64_t align_up(int64_t v, int64_t a) { return (v + 
 
 // Granule of K the packed layout serves.
 __host__ __device__ inline int64_t k_granule(int fmt) {
-  return (fmt == F_Q4_K || fmt == F_Q6_K) ? 256 : (fmt == F_NVFP4 ? 16 : 32);
+  return (fmt == F_Q4_K || fmt == F_Q5_K || fmt == F_Q6_K) ? 256 : (fmt == F_NVFP4 ? 16 : 32);
 }
 
 // bytes of one row record of plane A (per 256 values)
@@ -96,6 +105,7 @@ __host__ __device__ inline int rec_bytes(int fmt) {
   switch (fmt) {
     case F_Q8_0: return 272;
     case F_Q4_K: return 144;
+    case F_Q5_K: return 176;
     case F_Q6_K: return 208;
     case F_NVFP4: return 128;
     case F_FP8: return 256;
@@ -119,7 +129,7 @@ struct Layout {
 };
 
 __host__ __device__ inline bool make_layout(int fmt, int64_t N, int64_t K, int64_t E, Layout* L) {
-  if (fmt < F_Q8_0 || fmt > F_FP8 || N <= 0 || K <= 0 || E <= 0) return false;
+  if (fmt < F_Q8_0 || fmt > F_Q5_K || N <= 0 || K <= 0 || E <= 0) return false;
   if (K % k_granule(fmt) != 0 || K % 32 != 0) return false;
   L->fmt = fmt;
   L->rec = rec_bytes(fmt);
@@ -143,6 +153,7 @@ __host__ __device__ inline int64_t canon_matrix_bytes(int fmt, int64_t N, int64_
   switch (fmt) {
     case F_Q8_0: return N * (K / 32) * 34;
     case F_Q4_K: return N * (K / 256) * 144;
+    case F_Q5_K: return N * (K / 256) * 176;
     case F_Q6_K: return N * (K / 256) * 210;
     case F_NVFP4: return N * (K / 2) + N * (K / 16) + 4;
     case F_FP8: return N * K + N * 4;
@@ -155,9 +166,12 @@ __host__ __device__ inline int64_t canon_matrix_bytes(int fmt, int64_t N, int64_
 // quad reads, for every 32-value chunk j of the k-group, the same 4 (or 8) bytes;
 // those bytes of all 8 chunks are contiguous, so one or two 128-bit loads fetch them.
 //   Q4_K        : word t of chunk j (its elements 8t..8t+7) at 16 + 32t + 4j
+//   Q5_K        : 5-bit word t of chunk j at 16 + 32t + 4j; nibble word of chunk j at 144 + 4j
 //   Q8_0        : words 2t, 2t+1 of chunk j (elements 8t..8t+7) at 16 + 64t + 8j
 //   Q6_K        : ql word t of chunk j at 32t + 4j; qh word h of chunk j at 128 + 32h + 4j
 __host__ __device__ inline int q4k_word_off(int t, int j) { return 16 + 32 * t + 4 * j; }
+__host__ __device__ inline int q5k_word_off(int t, int j) { return 16 + 32 * t + 4 * j; }
+__host__ __device__ inline int q5k_nib_off(int j) { return 144 + 4 * j; }
 // NVFP4: byte offset (within plane A of a k-group) of code word wd (0..3) of K chunk kc
 // (0..7) of row n, and (within plane B) of the scale of 16-value block b (0..15)
 __host__ __device__ inline int64_t nv_code_off(int64_t n, int kc, int wd) {
@@ -237,6 +251,22 @@ __host__ __device__ inline uint32_t q80_unpermute(uint32_t w) {   // -> canonica
     o |= (u ^ 0x80u) << (8 * i);
   }
   return o;
+}
+// Q5_K: the 5-bit word of elements 8w..8w+7 (q[i] = element 8w+i, 0..31) and its
+// part of the chunk's nibble word (nibbles w, w+4)
+__host__ __device__ inline uint32_t q5k_word(const uint32_t* q) {
+  uint32_t v = 0;
+  for (int p = 0; p < 3; ++p) v |= (q[2 * p] << (5 * p)) | (q[2 * p + 1] << (16 + 5 * p));
+  return v | ((q[6] >> 4) << 15) | ((q[7] >> 4) << 31);
+}
+__host__ __device__ inline uint32_t q5k_nibs(const uint32_t* q, int w) {
+  return ((q[6] & 15u) << (4 * w)) | ((q[7] & 15u) << (16 + 4 * w));
+}
+// ... and back: element 8w+i of a word and its nibble word
+__host__ __device__ inline uint32_t q5k_elem(uint32_t v, uint32_t u, int w, int i) {
+  if (i < 6) return (v >> ((i & 1) * 16 + 5 * (i >> 1))) & 31u;
+  const int h = (i & 1) * 16;
+  return ((u >> (h + 4 * w)) & 15u) | (((v >> (15 + h)) & 1u) << 4);
 }
 // Q6_K: element e (0..31) of a chunk -> (ql word, nibble) and (qh word, bit)
 __host__ __device__ inline void q6k_pos(int e, int* lw, int* ln, int* hw, int* hb) {

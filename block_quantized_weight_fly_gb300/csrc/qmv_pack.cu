@@ -60,6 +60,21 @@ __global__ void pack_kernel(Layout L, const uint8_t* __restrict__ canon, uint8_t
         *reinterpret_cast<uint32_t*>(rec + q4k_word_off(wd, cl)) = q4k_permute(load_u32(blk + 16 + 16 * cl + 4 * wd));
       if (cl == 0) copy_bytes(rec, blk, 16);
     } break;
+    case F_Q5_K: {
+      const uint8_t* blk = canon + (row * (L.K / 256) + g) * 176;
+      uint32_t nibs = 0u;
+      for (int wd = 0; wd < 4; ++wd) {
+        uint32_t q[8];
+        for (int i = 0; i < 8; ++i) {
+          const int ce = 32 * cl + 8 * wd + i;            // element within the superblock
+          q[i] = ((blk[48 + (ce >> 1)] >> (4 * (ce & 1))) & 15u) | (((blk[16 + (ce >> 3)] >> (ce & 7)) & 1u) << 4);
+        }
+        *reinterpret_cast<uint32_t*>(rec + q5k_word_off(wd, cl)) = q5k_word(q);
+        nibs |= q5k_nibs(q, wd);
+      }
+      *reinterpret_cast<uint32_t*>(rec + q5k_nib_off(cl)) = nibs;
+      if (cl == 0) copy_bytes(rec, blk, 16);
+    } break;
     case F_Q6_K: {
       const uint8_t* blk = canon + (row * (L.K / 256) + g) * 210;
       uint32_t lw[4] = {0u, 0u, 0u, 0u}, hw[2] = {0u, 0u};
@@ -154,6 +169,17 @@ __global__ void dequant_kernel(Layout L, const uint8_t* __restrict__ packed, int
       for (int wd = 0; wd < 4; ++wd) {
         const uint32_t cw = q4k_unpermute(*reinterpret_cast<const uint32_t*>(rec + q4k_word_off(wd, cl)));
         for (int i = 0; i < 8; ++i) o[8 * wd + i] = __fsub_rn(__fmul_rn(a, (float)((cw >> (4 * i)) & 15u)), b);
+      }
+    } break;
+    case F_Q5_K: {
+      const uint32_t* hd = reinterpret_cast<const uint32_t*>(rec);
+      float d = h2f(hd[0]), dmin = h2f(hd[0] >> 16);
+      uint32_t sc = q4k_field(hd[1], hd[2], hd[3], cl), m = q4k_field(hd[1], hd[2], hd[3], 8 + cl);
+      float a = __fmul_rn(d, (float)sc), b = __fmul_rn(dmin, (float)m);
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(rec + q5k_nib_off(cl));
+      for (int wd = 0; wd < 4; ++wd) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(rec + q5k_word_off(wd, cl));
+        for (int i = 0; i < 8; ++i) o[8 * wd + i] = __fsub_rn(__fmul_rn(a, (float)q5k_elem(v, u, wd, i)), b);
       }
     } break;
     case F_Q6_K: {
@@ -293,6 +319,59 @@ __global__ void quant_q4_k_kernel(const float* __restrict__ W, int64_t nblk, uin
   }
 }
 
+// Q5_K: the Q4_K quantizer with 32 levels; fifth bits at 16 + e/8, nibbles at 48 + e/2
+__global__ void quant_q5_k_kernel(const float* __restrict__ W, int64_t nblk, uint8_t* __restrict__ out) {
+  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  const float* x = W + b * 256;
+  uint8_t* o = out + b * 176;
+  float s[8], mn[8], smax = 0.0f, mmax = 0.0f;
+  for (int j = 0; j < 8; ++j) {
+    float lo = 0.0f, hi = x[32 * j];
+    for (int i = 0; i < 32; ++i) {
+      float v = x[32 * j + i];
+      lo = fminf(lo, v);
+      hi = fmaxf(hi, v);
+    }
+    s[j] = __fdiv_rn(__fsub_rn(hi, lo), 31.0f);
+    mn[j] = -lo;
+    smax = fmaxf(smax, s[j]);
+    mmax = fmaxf(mmax, mn[j]);
+  }
+  uint32_t d = f2h_bits(__fdiv_rn(smax, 63.0f)), dmin = f2h_bits(__fdiv_rn(mmax, 63.0f));
+  float dd = h2f(d), dm = h2f(dmin);
+  uint32_t sw[3] = {0u, 0u, 0u};
+  uint32_t sc[8], mq[8];
+  for (int j = 0; j < 8; ++j) {
+    sc[j] = (dd == 0.0f) ? 0u : (uint32_t)clampf(rintf(__fdiv_rn(s[j], dd)), 0.0f, 63.0f);
+    mq[j] = (dm == 0.0f) ? 0u : (uint32_t)clampf(rintf(__fdiv_rn(mn[j], dm)), 0.0f, 63.0f);
+  }
+  for (int f = 0; f < 16; ++f) {
+    uint32_t v = f < 8 ? sc[f] : mq[f - 8];
+    for (int bit = 0; bit < 6; ++bit) {
+      int pos = 6 * f + bit;
+      sw[pos >> 5] |= ((v >> bit) & 1u) << (pos & 31);
+    }
+  }
+  o[0] = (uint8_t)d; o[1] = (uint8_t)(d >> 8); o[2] = (uint8_t)dmin; o[3] = (uint8_t)(dmin >> 8);
+  for (int i = 0; i < 12; ++i) o[4 + i] = (uint8_t)(sw[i >> 2] >> (8 * (i & 3)));
+  for (int j = 0; j < 8; ++j) {
+    float den = __fmul_rn(dd, (float)sc[j]);
+    float off = __fmul_rn(dm, (float)mq[j]);
+    uint32_t hb = 0u;                                   // fifth bits of the sub-block
+    for (int i = 0; i < 32; i += 2) {
+      uint32_t q2[2];
+      for (int u = 0; u < 2; ++u) {
+        float num = __fadd_rn(x[32 * j + i + u], off);
+        q2[u] = (den == 0.0f) ? 0u : (uint32_t)clampf(rintf(__fdiv_rn(num, den)), 0.0f, 31.0f);
+        hb |= (q2[u] >> 4) << (i + u);
+      }
+      o[48 + (32 * j + i) / 2] = (uint8_t)((q2[0] & 15u) | ((q2[1] & 15u) << 4));
+    }
+    for (int i = 0; i < 4; ++i) o[16 + 4 * j + i] = (uint8_t)(hb >> (8 * i));
+  }
+}
+
 __global__ void quant_q6_k_kernel(const float* __restrict__ W, int64_t nblk, uint8_t* __restrict__ out) {
   int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= nblk) return;
@@ -380,6 +459,10 @@ cudaError_t launch_quantize(int fmt, const float* W, int64_t rows, int64_t K, fl
     case F_Q4_K: {
       int64_t n = rows * (K / 256);
       quant_q4_k_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, n, canon);
+    } break;
+    case F_Q5_K: {
+      int64_t n = rows * (K / 256);
+      quant_q5_k_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, n, canon);
     } break;
     case F_Q6_K: {
       int64_t n = rows * (K / 256);

@@ -247,6 +247,115 @@ struct Slab<F_Q4_K, 8> {
 };
 
 // ============================================================================
+// Q5_K. The Q4_K scheme with q = 0..31: A = 128 + q is still exact in bf16, the
+// header (d, dmin, scale stream) is Q4_K's, and the pairs come from the 5-bit
+// words plus the chunk's nibble word (packed layout: qmv_layout.cuh).
+// ============================================================================
+// the four pairs {128 + q(8t+2p), 128 + q(8t+2p+1)} of a thread's 5-bit word v;
+// u = the chunk's nibble word already shifted right by 4t
+__device__ __forceinline__ void q5k_quad(uint32_t v, uint32_t u, uint32_t* a) {
+  a[0] = and_or(v, 0x001F001Fu, 0x43004300u);
+  a[1] = and_or(v >> 5, 0x001F001Fu, 0x43004300u);
+  a[2] = and_or(v >> 10, 0x001F001Fu, 0x43004300u);
+  a[3] = and_or(v >> 11, 0x00100010u, and_or(u, 0x000F000Fu, 0x43004300u));
+}
+
+template <>
+struct Slab<F_Q5_K, 1> {
+  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int, int w, int lane,
+                             float2*, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* rA = st + (16 * w + g) * 176;
+    const uint8_t* rB = rA + 8 * 176;
+    const uint32_t xo = 64 * g + 16 * t;                     // unit g = chunk g of token 0
+    uint32_t WA[8], WB[8], UA[8], UB[8];
+    load8(rA + q5k_word_off(t, 0), WA);
+    load8(rB + q5k_word_off(t, 0), WB);
+    load8(rA + q5k_nib_off(0), UA);
+    load8(rB + q5k_nib_off(0), UB);
+    const int us = 4 * t;
+    float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t pa[4], pb[4];
+      q5k_quad(WA[j], UA[j] >> us, pa);
+      q5k_quad(WB[j], UB[j] >> us, pb);
+      const uint4 b = ldx128(xs, g == j, xo);
+      float* d = (j & 1) ? dO : dE;
+      mma_bf16(d, pa[0], pb[0], pa[1], pb[1], b.x, b.y);
+      mma_bf16(d, pa[2], pb[2], pa[3], pb[3], b.z, b.w);
+    }
+    const uint4 xv = lds128v(xs + xo);
+    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
+    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+    float aA[2], cA[2], aB[2], cB[2];
+    q4k_pair_scales_rec(rA, t, aA, cA);
+    q4k_pair_scales_rec(rB, t, aB, cB);
+    acc[0] += fmaf(aA[0], dE[0] + dO[0], fmaf(aA[1], dE[1] + dO[1], -fmaf(cA[0], xx[0], cA[1] * xx[1])));
+    acc[1] += fmaf(aB[0], dE[2] + dO[2], fmaf(aB[1], dE[3] + dO[3], -fmaf(cB[0], xx[2], cB[1] * xx[3])));
+  }
+};
+
+template <>
+struct Slab<F_Q5_K, 8> {
+  __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int R, int w, int lane,
+                             float2* tbl, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    {   // scale table of the warp's 16 rows: lane -> (row lane/2, sub-blocks 4h..4h+3)
+      const int rl = lane >> 1, h = lane & 1;
+      const uint4 hd = lds128v(st + (16 * w + rl) * 176);
+      float a[2], c[2];
+      q4k_pair_scales(hd, 2 * h, a, c);
+      tbl[rl * kTblStride + 4 * h + 0] = make_float2(a[0], c[0]);
+      tbl[rl * kTblStride + 4 * h + 1] = make_float2(a[1], c[1]);
+      q4k_pair_scales(hd, 2 * h + 1, a, c);
+      tbl[rl * kTblStride + 4 * h + 2] = make_float2(a[0], c[0]);
+      tbl[rl * kTblStride + 4 * h + 3] = make_float2(a[1], c[1]);
+    }
+    __syncwarp();
+    const uint8_t* rA = st + (16 * w + g) * 176;
+    const uint8_t* rB = rA + 8 * 176;
+    uint32_t WA[8], WB[8];
+    load8(rA + q5k_word_off(t, 0), WA);
+    load8(rB + q5k_word_off(t, 0), WB);
+    const int us = 4 * t;
+    const bool has_x = g < R;
+#pragma unroll
+    for (int j0 = 0; j0 < 8; j0 += 4) {
+      // the nibble words of these four chunks only (fewer live registers)
+      const uint4 ua = lds128v(rA + q5k_nib_off(j0)), ub = lds128v(rB + q5k_nib_off(j0));
+      const uint32_t UA[4] = {ua.x, ua.y, ua.z, ua.w}, UB[4] = {ub.x, ub.y, ub.z, ub.w};
+      float dd[4][4], xx[4][4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dd[q][e] = xx[q][e] = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = j0 + q;
+        uint32_t pa[4], pb[4];
+        q5k_quad(WA[j], UA[q] >> us, pa);
+        q5k_quad(WB[j], UB[q] >> us, pb);
+        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
+        mma_bf16(dd[q], pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
+        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
+        mma_bf16(dd[q], pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
+        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 sA = tbl[g * kTblStride + j0 + q], sB = tbl[(g + 8) * kTblStride + j0 + q];
+        acc[0] = fmaf(sA.x, dd[q][0], fmaf(-sA.y, xx[q][0], acc[0]));
+        acc[1] = fmaf(sA.x, dd[q][1], fmaf(-sA.y, xx[q][1], acc[1]));
+        acc[2] = fmaf(sB.x, dd[q][2], fmaf(-sB.y, xx[q][2], acc[2]));
+        acc[3] = fmaf(sB.x, dd[q][3], fmaf(-sB.y, xx[q][3], acc[3]));
+      }
+    }
+    __syncwarp();
+  }
+};
+
+// ============================================================================
 // Q8_0. q = u - 128 with u = 16 uh + ul; D_lo / D_hi over (128 + ul) / (128 + uh):
 // sum q x = D_lo + 16 D_hi - 2304 X; w = d q (d per 32-value chunk).
 // ============================================================================

@@ -706,6 +706,7 @@ cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant) {
   switch (a.L.fmt) {
     case F_Q8_0: return launch_fmt<F_Q8_0>(a, s, variant);
     case F_Q4_K: return launch_fmt<F_Q4_K>(a, s, variant);
+    case F_Q5_K: return launch_fmt<F_Q5_K>(a, s, variant);
     case F_Q6_K: return launch_fmt<F_Q6_K>(a, s, variant);
     case F_NVFP4: return launch_fmt<F_NVFP4>(a, s, variant);
     case F_FP8: return launch_fmt<F_FP8>(a, s, variant);

@@ -7,7 +7,9 @@
  * over one matrix (E = 1) or a stacked expert tower weight[E*N, K]
  * ("vllm.cpp #3030, BACKEND-TENSTORRENT-KEEPQUANT: the 27B arm", scope item 2
  * and the "Re-anchor" comment). Formats: GGUF-style Q8_0 / Q4_K / Q6_K keep-quant
- * blocks (same issue, artifact table and "Budget on the 32 GB P150"), and NVFP4
+ * blocks (same issue, artifact table and "Budget on the 32 GB P150"), Q5_K (the
+ * 5-bit member named with them in scope item 1 and owed by the grouped kernel in
+ * the "Re-anchor" comment), and NVFP4
  * E2M1 codes with E4M3 block scales plus row-scaled FP8 ("I Built a Custom
  * Blackwell Kernel for Qwen3.8-27B", "What the custom path actually does").
  *
@@ -33,6 +35,11 @@
  *         scales: 96-bit little-endian bitstream of sixteen 6-bit fields, fields
  *         0..7 = sc_j, 8..15 = m_j for the eight 32-value sub-blocks; nibble byte b
  *         holds element 2b (low) and 2b+1 (high);   w = (d * sc_j) * q - dmin * m_j
+ *   Q5_K 176 B per 256 values: fp16 d | fp16 dmin | 12 B scales | 32 B qh | 128 B nibbles
+ *         header and nibbles exactly as Q4_K (low 4 bits of q); qh bit e (byte e/8,
+ *         bit e%8) = bit 4 of element e; q = 0..31; w = (d * sc_j) * q - dmin * m_j
+ *         (the pages print no byte layout for Q5_K: this is the Q4_K reading plus
+ *         one bit plane)
  *   Q6_K 210 B per 256 values: 128 B ql | 64 B qh | 16 x int8 sc | fp16 d
  *         q = ql nibble | (qh 2 bits << 4); ql byte b holds elements 2b, 2b+1;
  *         qh byte b holds elements 4b..4b+3 at bits 0,2,4,6; w = (d * sc_j) * (q - 32)
@@ -57,7 +64,8 @@ typedef enum {
     QMV_Q4_K = 2,
     QMV_Q6_K = 3,
     QMV_NVFP4 = 4,
-    QMV_FP8_ROW = 5
+    QMV_FP8_ROW = 5,
+    QMV_Q5_K = 6
 } qmv_fmt;
 
 typedef enum {
@@ -90,7 +98,7 @@ size_t qmv_canon_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
  * is aligned; rows are padded to a multiple of 128 with zero blocks. The slab
  * bytes are the canonical bytes, only reordered (the per-value cost is
  * unchanged). K must be a multiple of 32 (Q8_0, NVFP4, FP8_ROW) or 256 (Q4_K,
- * Q6_K). Returns 0 if unsupported. */
+ * Q5_K, Q6_K). Returns 0 if unsupported. */
 size_t qmv_pack_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
 
 /* Repack canonical bytes into the device layout. canon: device, qmv_canon_size

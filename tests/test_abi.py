@@ -47,16 +47,17 @@ def test_binding_exposes_every_declared_symbol(lib):
 
 def test_sizes_match_oracle(lib):
     import block_quantized_weight_fly_gb300 as q
-    for fmt in ("q8_0", "q4_k", "q6_k", "nvfp4", "fp8_row"):
+    for fmt in ("q8_0", "q4_k", "q5_k", "q6_k", "nvfp4", "fp8_row"):
         for N, K in ((512, 1024), (17408, 5120), (248320, 5120), (300, 768)):
             assert q.qmv_canon_size(fmt, N, K) == oracle.canon_bytes(fmt, N, K)
     # the packed layout moves the canonical bytes; only row/K padding and alignment add
-    for fmt, per in (("q8_0", 34 / 32), ("q4_k", 144 / 256), ("q6_k", 210 / 256),
+    for fmt, per in (("q8_0", 34 / 32), ("q4_k", 144 / 256), ("q5_k", 176 / 256), ("q6_k", 210 / 256),
                      ("nvfp4", 18 / 32), ("fp8_row", 1.0)):
         N, K = 17408, 5120
         body = q.qmv_pack_size(fmt, N, K) - 256
         assert N * K * per <= body <= N * K * per + 4 * N + 512
     assert q.qmv_pack_size("q4_k", 100, 100) == 0          # K not a multiple of 256
+    assert q.qmv_pack_size("q5_k", 100, 1000) == 0
     assert q.qmv_pack_size("q8_0", 100, 48) == 0           # K not a multiple of 32
 
 
@@ -70,6 +71,8 @@ def test_host_validation_without_device(lib):
     assert gemv(2, one, one, one, 0, 128, 256, one, 1 << 20, None) == 1
     assert gemv(2, one, one, one, 9, 128, 256, one, 1 << 20, None) == 1
     assert gemv(9, one, one, one, 1, 128, 256, one, 1 << 20, None) == 1
+    assert gemv(7, one, one, one, 1, 128, 256, one, 1 << 20, None) == 1
+    assert gemv(6, one, one, one, 1, 128, 100, one, 1 << 20, None) == 3
     assert gemv(2, one, one, one, 1, 128, 100, one, 1 << 20, None) == 3
     assert gemv(2, P(257), one, one, 1, 128, 256, one, 1 << 20, None) == 2
     assert gemv(2, one, P(258), one, 1, 128, 256, one, 1 << 20, None) == 2

@@ -24,6 +24,8 @@ QWEN_HIDDEN, QWEN_MLP, QWEN_VOCAB = 5120, 17408, 248320
 DENSE = [
     ("q4_k", QWEN_MLP, QWEN_HIDDEN),     # gate / up
     ("q4_k", QWEN_HIDDEN, QWEN_MLP),     # down
+    ("q5_k", QWEN_MLP, QWEN_HIDDEN),
+    ("q5_k", QWEN_HIDDEN, QWEN_MLP),
     ("q6_k", QWEN_VOCAB, QWEN_HIDDEN),   # untied output head
     ("q6_k", 10240, QWEN_HIDDEN),        # fused attn_qkv
     ("nvfp4", QWEN_MLP, QWEN_HIDDEN),

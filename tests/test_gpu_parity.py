@@ -18,7 +18,7 @@ from cases import (TOL, host_dequant, host_matrix, norm_err, tensor_scale)
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["q8_0", "q4_k", "q6_k", "nvfp4", "fp8_row"]
+FMTS = ["q8_0", "q4_k", "q5_k", "q6_k", "nvfp4", "fp8_row"]
 
 
 @pytest.fixture(scope="module")
@@ -34,7 +34,7 @@ def _sms():
 
 
 def _kq(fmt):
-    return fmt in ("q4_k", "q6_k")
+    return fmt in ("q4_k", "q5_k", "q6_k")
 
 
 # ---------------------------------------------------------------------------
