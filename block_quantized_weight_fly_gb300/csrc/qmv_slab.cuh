@@ -164,6 +164,35 @@ __device__ __forceinline__ void q4k_pair_scales_rec(const uint8_t* rec, int t, f
   c[1] = fmaf(128.0f, a[1], dd.y * u6f(m >> 6));
 }
 
+// M = 1 decodes through bf16's linear range instead: the bit patterns 0..255 of a
+// bf16 are exactly the values 0..255 x 2^-133 (subnormals and the first normal
+// binade), so a word masked with 0x000F000F gives {q, q'} x 2^-133 and masked with
+// 0x00F000F0 gives {q, q'} x 2^-129 -- no shift for two of the four pairs and no
+// +128 offset. The activations are scaled by 2^67 (low-nibble pairs) or 2^63
+// (high-nibble pairs) with one exact bf16x2 multiply each, so every product is
+// q x 2^-66: a normal fp32 value for 2^-60 <= |x| < 2^61 (the tensor core keeps
+// subnormal bf16 operands exactly). The sum is rescaled by 2^66 through a_j.
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+constexpr uint32_t kX67 = 0x61006100u;   // bf16x2 {2^67, 2^67}
+constexpr uint32_t kX63 = 0x5F005F00u;   // bf16x2 {2^63, 2^63}
+// a_j x 2^66 and b_j for sub-blocks 2t, 2t+1 of a record in shared memory
+__device__ __forceinline__ void q4k_pair_scales_lin_rec(const uint8_t* rec, int t, float* a, float* b) {
+  const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 4);
+  const int bs = 12 * t, bm = 48 + 12 * t;
+  const uint32_t s = __funnelshift_r(sw[bs >> 5], sw[(bs >> 5) + 1], bs & 31);
+  const uint32_t m = __funnelshift_r(sw[bm >> 5], sw[(bm >> 5) + 1], bm & 31);
+  const float2 dd = h2x2f(*reinterpret_cast<const uint32_t*>(rec));
+  const float d66 = dd.x * 7.3786976294838206e19f;      // d x 2^66 (exact)
+  a[0] = d66 * u6f(s);
+  a[1] = d66 * u6f(s >> 6);
+  b[0] = dd.y * u6f(m);
+  b[1] = dd.y * u6f(m >> 6);
+}
+
 template <>
 struct Slab<F_Q4_K, 1> {
   __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int, int w, int lane,
@@ -178,22 +207,36 @@ struct Slab<F_Q4_K, 1> {
     float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint32_t wa = WA[j], wb = WB[j];
+      const uint32_t wa = WA[j], wb = WB[j], ha = wa >> 8, hb = wb >> 8;
       const uint4 b = ldx128(xs, g == j, xo);
       float* d = (j & 1) ? dO : dE;
-      mma_bf16(d, nib_pair(wa, 0), nib_pair(wb, 0), nib_pair(wa, 1), nib_pair(wb, 1), b.x, b.y);
-      mma_bf16(d, nib_pair(wa, 2), nib_pair(wb, 2), nib_pair(wa, 3), nib_pair(wb, 3), b.z, b.w);
+      mma_bf16(d, wa & 0x000F000Fu, wb & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x00F000F0u, bmul2(b.x, kX67),
+               bmul2(b.y, kX63));
+      mma_bf16(d, ha & 0x000F000Fu, hb & 0x000F000Fu, ha & 0x00F000F0u, hb & 0x00F000F0u, bmul2(b.z, kX67),
+               bmul2(b.w, kX63));
     }
     const uint4 xv = lds128v(xs + xo);
     mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
     mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
-    float aA[2], cA[2], aB[2], cB[2];
-    q4k_pair_scales_rec(rA, t, aA, cA);
-    q4k_pair_scales_rec(rB, t, aB, cB);
-    acc[0] += fmaf(aA[0], dE[0] + dO[0], fmaf(aA[1], dE[1] + dO[1], -fmaf(cA[0], xx[0], cA[1] * xx[1])));
-    acc[1] += fmaf(aB[0], dE[2] + dO[2], fmaf(aB[1], dE[3] + dO[3], -fmaf(cB[0], xx[2], cB[1] * xx[3])));
+    float aA[2], bA[2], aB[2], bB[2];
+    q4k_pair_scales_lin_rec(rA, t, aA, bA);
+    q4k_pair_scales_lin_rec(rB, t, aB, bB);
+    acc[0] += fmaf(aA[0], dE[0] + dO[0], fmaf(aA[1], dE[1] + dO[1], -fmaf(bA[0], xx[0], bA[1] * xx[1])));
+    acc[1] += fmaf(aB[0], dE[2] + dO[2], fmaf(aB[1], dE[3] + dO[3], -fmaf(bB[0], xx[2], bB[1] * xx[3])));
   }
 };
+
+// the same from the header words in registers (the M > 1 scale tables)
+__device__ __forceinline__ void q4k_pair_scales_lin(const uint4 hd, int t, float* a, float* b) {
+  const float2 dd = h2x2f(hd.x);
+  const uint64_t lo = ((uint64_t)hd.z << 32) | hd.y, hi = ((uint64_t)hd.w << 32) | hd.z;
+  const uint32_t s = (uint32_t)(lo >> (12 * t)), m = (uint32_t)(hi >> (16 + 12 * t));
+  const float d66 = dd.x * 7.3786976294838206e19f;      // d x 2^66 (exact)
+  a[0] = d66 * u6f(s);
+  a[1] = d66 * u6f(s >> 6);
+  b[0] = dd.y * u6f(m);
+  b[1] = dd.y * u6f(m >> 6);
+}
 
 template <>
 struct Slab<F_Q4_K, 8> {
@@ -203,13 +246,13 @@ struct Slab<F_Q4_K, 8> {
     {   // scale table of the warp's 16 rows: lane -> (row lane/2, sub-blocks 4h..4h+3)
       const int rl = lane >> 1, h = lane & 1;
       const uint4 hd = lds128v(st + (16 * w + rl) * 144);
-      float a[2], c[2];
-      q4k_pair_scales(hd, 2 * h, a, c);
-      tbl[rl * kTblStride + 4 * h + 0] = make_float2(a[0], c[0]);
-      tbl[rl * kTblStride + 4 * h + 1] = make_float2(a[1], c[1]);
-      q4k_pair_scales(hd, 2 * h + 1, a, c);
-      tbl[rl * kTblStride + 4 * h + 2] = make_float2(a[0], c[0]);
-      tbl[rl * kTblStride + 4 * h + 3] = make_float2(a[1], c[1]);
+      float a[2], b[2];
+      q4k_pair_scales_lin(hd, 2 * h, a, b);
+      tbl[rl * kTblStride + 4 * h + 0] = make_float2(a[0], b[0]);
+      tbl[rl * kTblStride + 4 * h + 1] = make_float2(a[1], b[1]);
+      q4k_pair_scales_lin(hd, 2 * h + 1, a, b);
+      tbl[rl * kTblStride + 4 * h + 2] = make_float2(a[0], b[0]);
+      tbl[rl * kTblStride + 4 * h + 3] = make_float2(a[1], b[1]);
     }
     __syncwarp();
     uint32_t WA[8], WB[8];
@@ -226,11 +269,13 @@ struct Slab<F_Q4_K, 8> {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int j = j0 + q;
-        const uint32_t wa = WA[j], wb = WB[j];
+        const uint32_t wa = WA[j], wb = WB[j], ha = wa >> 8, hb = wb >> 8;
         const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
-        mma_bf16(dd[q], nib_pair(wa, 0), nib_pair(wb, 0), nib_pair(wa, 1), nib_pair(wb, 1), xv.x, xv.y);
+        mma_bf16(dd[q], wa & 0x000F000Fu, wb & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x00F000F0u,
+                 bmul2(xv.x, kX67), bmul2(xv.y, kX63));
         mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
-        mma_bf16(dd[q], nib_pair(wa, 2), nib_pair(wb, 2), nib_pair(wa, 3), nib_pair(wb, 3), xv.z, xv.w);
+        mma_bf16(dd[q], ha & 0x000F000Fu, hb & 0x000F000Fu, ha & 0x00F000F0u, hb & 0x00F000F0u,
+                 bmul2(xv.z, kX67), bmul2(xv.w, kX63));
         mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
       }
 #pragma unroll

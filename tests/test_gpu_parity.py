@@ -138,6 +138,27 @@ def test_gemv_deterministic_and_guarded(q, fmt):
     assert bool((buf[:32] == canary).all()) and bool((buf[32 + M * N:] == canary).all())
 
 
+@pytest.mark.parametrize("lo,hi", [(-50, 40), (-60, 0), (0, 57)])
+@pytest.mark.parametrize("M", [1, 3])
+def test_q4k_activation_range(q, lo, hi, M):
+    """The Q4_K decoders scale x by 2^63 / 2^67: exact products for
+    2^-60 <= |x| < 2^61. Activations with magnitudes spread over that range (per
+    element 2^e, e uniform in [lo, hi]) still meet the tolerance."""
+    fmt, N, K = "q4_k", 1000, 2048
+    W, canon = host_matrix(fmt, 19, N, K)
+    z = synth.activations(19, M, K).float()
+    rng = np.random.default_rng((lo + 100) * 1000 + hi + 100 + M)
+    e = torch.from_numpy(rng.integers(lo, hi + 1, size=(M, K)).astype(np.float32))
+    x = (z * torch.pow(2.0, e)).to(torch.bfloat16)
+    ref, den = oracle.gemv_f64(host_dequant(fmt, canon, N, K), synth.bf16_bits(x))
+    packed = q.qmv_pack(fmt, torch.from_numpy(canon).cuda(), N, K)
+    ws = q.workspace(q.QMV_ENTRY_GEMV, fmt, M, N, K)
+    y = q.qmv_gemv(fmt, packed, x.cuda(), N, K, ws).cpu().numpy()
+    assert q.qmv_device_status() == 0
+    assert np.isfinite(y).all()
+    assert norm_err(y, ref, den) <= TOL
+
+
 def test_gemv_rows_of_m8_match_m1_within_tolerance(q):
     fmt, N, K = "q6_k", 640, 1024
     W, canon = host_matrix(fmt, 17, N, K)
