@@ -34,6 +34,15 @@ qmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ECU
 
 bool valid_fmt(int f) { return f >= QMV_Q8_0 && f <= QMV_Q5_K; }
 
+// CTAs of a stream-kernel grid for `slabs` slabs. Two CTAs per SM hide the
+// consumers' latency better than one and win at M > 1 and for the grouped call.
+// A dense M = 1 call keeps one per SM: the free slots let the next call's CTAs
+// start and prefetch their first slabs early, which wins in back-to-back layers.
+int stream_grid(int64_t slabs, int M, bool grouped, int sms) {
+  const int64_t n = (M > 1 || grouped) ? 2 * (int64_t)sms : (int64_t)sms;
+  return (int)(slabs < n ? slabs : n);
+}
+
 }  // namespace
 
 extern "C" {
@@ -92,13 +101,14 @@ size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, i
   if (!valid_fmt(fmt) || M <= 0 || N <= 0 || K <= 0) return 0;
   const int sms = num_sms_current_device();
   if (sms <= 0) return 0;
+  // room for the largest grid the entry point launches (two CTAs per SM)
   if (entry == QMV_ENTRY_GEMV || entry == QMV_ENTRY_GROUPED) {
     if (M > QMV_MAX_M) return 0;
-    return (size_t)ws_plan_stream(M, 0, sms).total;
+    return (size_t)ws_plan_stream(M, 0, 2 * sms).total;
   }
   if (entry == QMV_ENTRY_SWIGLU) {
     if (M > QMV_MAX_M) return 0;
-    return (size_t)ws_plan_stream(M, 0, sms, 2).total;
+    return (size_t)ws_plan_stream(M, 0, 2 * sms, 2).total;
   }
   if (entry == QMV_ENTRY_W4A4) {
     // the activation's NVFP4 tiles: per 256-value k-group, m_pad rows x (128 B codes + 16 B scales)
@@ -118,7 +128,9 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
   if (!aligned(packed_W, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
-  if (ws_bytes < (size_t)ws_plan_stream(M, 0, sms).total) return QMV_EWORKSPACE;
+  const int64_t slabs = L.row_tiles * L.k_groups;
+  const int ctas = stream_grid(slabs, M, false, sms);
+  if (ws_bytes < (size_t)ws_plan_stream(M, 0, ctas).total) return QMV_EWORKSPACE;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
   StreamArgs a;
@@ -128,8 +140,7 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
   a.M = M; a.topk = 1; a.x_per_pair = 0; a.swiglu = 0;
   a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
   a.status = status;
-  const int64_t slabs = L.row_tiles * L.k_groups;
-  a.num_ctas = (int)(slabs < sms ? slabs : sms);
+  a.num_ctas = ctas;
   int variant = 0;
   qmv_status st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
@@ -151,7 +162,11 @@ qmv_status qmv_grouped(qmv_fmt fmt, const void* tower, const int32_t* expert_ids
     return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
-  if (ws_bytes < (size_t)ws_plan_stream(M, 0, sms).total) return QMV_EWORKSPACE;
+  // the distinct experts are found on the device: size the grid for the most
+  // there can be (CTAs beyond the slab count get empty ranges)
+  const int64_t experts = (int64_t)M * topk < E ? (int64_t)M * topk : E;
+  const int ctas = stream_grid(experts * L.row_tiles * L.k_groups, M, true, sms);
+  if (ws_bytes < (size_t)ws_plan_stream(M, 0, ctas).total) return QMV_EWORKSPACE;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
   StreamArgs a;
@@ -161,7 +176,7 @@ qmv_status qmv_grouped(qmv_fmt fmt, const void* tower, const int32_t* expert_ids
   a.M = M; a.topk = topk; a.x_per_pair = x_per_pair; a.swiglu = 0;
   a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
   a.status = status;
-  a.num_ctas = sms;
+  a.num_ctas = ctas;
   int variant = 0;
   qmv_status st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
@@ -177,7 +192,9 @@ qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, fl
   if (!aligned(tower, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(h, 4)) return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
-  if (ws_bytes < (size_t)ws_plan_stream(M, 0, sms, 2).total) return QMV_EWORKSPACE;
+  const int64_t slabs = 2 * L.row_tiles * L.k_groups;
+  const int ctas = stream_grid(slabs, M, false, sms);
+  if (ws_bytes < (size_t)ws_plan_stream(M, 0, ctas, 2).total) return QMV_EWORKSPACE;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
   StreamArgs a;
@@ -187,8 +204,7 @@ qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, fl
   a.M = M; a.topk = 1; a.x_per_pair = 0; a.swiglu = 1;
   a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
   a.status = status;
-  const int64_t slabs = 2 * L.row_tiles * L.k_groups;
-  a.num_ctas = (int)(slabs < sms ? slabs : sms);
+  a.num_ctas = ctas;
   int variant = 0;
   qmv_status st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;

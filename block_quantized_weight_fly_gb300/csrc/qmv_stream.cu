@@ -7,17 +7,19 @@
 // reads halved latency). So the kernel is built around streaming the packed
 // weights from HBM exactly once per call for all M rows of x:
 //
-//  * persistent grid, one CTA per SM per call; the work is the list of slabs
-//    (segment, 128-row tile, 256-value k-group) in tile-major order, cut into
-//    equal contiguous ranges, one per CTA (split-K at slab granularity);
+//  * persistent grid of one or two CTAs per SM (chosen per call by the entry
+//    point); the work is the list of slabs (segment, 128-row tile, 256-value
+//    k-group) in tile-major order, cut into equal contiguous ranges, one per CTA
+//    (split-K at slab granularity);
 //  * warp 0 is a producer: one elected lane streams each slab (and the matching
 //    256-value slice of every x row routed to it) into a ring of shared-memory
 //    stages with cp.async.bulk, completion tracked by mbarriers; no multicast;
 //  * the other eight warps are consumers: warp w decodes rows 16w .. 16w+15 of a
 //    slab on mma.sync (see qmv_slab.cuh), the decode in registers and the inner
 //    product factored per block: y += scale * sum(q * x) (- min * sum x);
-//  * a CTA takes half an SM, so that the next call's CTAs are resident
-//    beside the running ones and copy their first weight slabs meanwhile;
+//  * a CTA takes half an SM: with a grid of one CTA per SM the next call's CTAs
+//    are resident beside the running ones and copy their first weight slabs
+//    meanwhile; with two per SM the call's own warps hide each other's latency;
 //  * a row tile split between CTAs is finished by the CTA that holds its first
 //    k-groups: the others publish their partial sums in the workspace, each word
 //    non-zero so that it is its own completion flag (no fence, no flag word), and
@@ -637,6 +639,10 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   int smem_sm = 0;
   err = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (err != cudaSuccess) return err;
+  int sm_count = 0;
+  err = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  if (a.num_ctas < 1 || a.num_ctas > ctas_per_sm<MT>() * sm_count) return cudaErrorInvalidConfiguration;
   // per CTA: its share of the SM less the 1 KB the hardware reserves per CTA
   const int smem_cta = smem_sm / ctas_per_sm<MT>() - 1024;
   if (smem_cta < smem_max) smem_max = smem_cta;
@@ -674,11 +680,12 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
-  // The grid has at most one CTA per SM and ctas_per_sm() CTAs fit on an SM, so
-  // every CTA of the grid is resident at once as soon as the previous kernel's
-  // CTAs have left (none of which waits on this grid): a reducer's bounded wait on
-  // its peers' partial sums ends. Programmatic stream serialization lets this
-  // grid's prologue overlap the previous kernel (see griddepcontrol in the kernel).
+  // The grid has at most ctas_per_sm() CTAs per SM (checked above) and that many
+  // fit on an SM, so every CTA of the grid is resident at once as soon as the
+  // previous kernel's CTAs have left (none of which waits on this grid): a
+  // reducer's bounded wait on its peers' partial sums ends. With one CTA per SM the
+  // next call's CTAs take the free slots early; programmatic stream serialization
+  // lets their prologue overlap this grid (see griddepcontrol in the kernel).
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -159,10 +159,10 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
  * left: each call first clears the words it uses on `stream` (cudaMemsetAsync, no
  * allocation). Calls that overlap in time (on other streams or host threads)
  * race on the array; the caller must serialize them.
- * Returns QMV_EWORKSPACE when the scratch this device needs,
- * qmv_workspace_size(QMV_ENTRY_GEMV, fmt, M, N, K, 1, 1), exceeds
- * QMV_STATIC_SCRATCH_BYTES (M = 2..8 on a device of more than 256 SMs).
- * Otherwise arguments, results and errors as qmv_gemv. */
+ * Its grid is always one CTA per SM, whose partial sums take SMs x 128 x c x 4
+ * bytes (c = 1 at M = 1, else 8; rounded up to 256). Returns QMV_EWORKSPACE when
+ * that exceeds QMV_STATIC_SCRATCH_BYTES (M = 2..8 on a device of more than 256
+ * SMs). Otherwise arguments, results and errors as qmv_gemv. */
 qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y,
                             int M, int64_t N, int64_t K, cudaStream_t stream);
 
