@@ -111,10 +111,11 @@ size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, i
     return (size_t)ws_plan_stream(M, 0, 2 * sms, 2).total;
   }
   if (entry == QMV_ENTRY_W4A4) {
-    // the activation's NVFP4 tiles: per 256-value k-group, m_pad rows x (128 B codes + 16 B scales)
+    // the activation's NVFP4 tiles (per 256-value k-group, m_pad rows x (128 B codes +
+    // 16 B scales)), then the split-K partial sums
     if (fmt != QMV_NVFP4 || K % 256) return 0;
     const int64_t m_pad = align_up(M, 128);
-    return (size_t)((K / 256) * m_pad * 144);
+    return (size_t)(align_up((K / 256) * m_pad * 144, 256) + w4a4_partials_bytes(sms));
   }
   return 0;
 }
@@ -229,13 +230,19 @@ qmv_status qmv_gemm_nvfp4_w4a4(const void* packed_W, const uint16_t* x, float x_
   if (!make_layout(QMV_NVFP4, N, K, 1, &L)) return QMV_EUNSUPPORTED;
   if (!aligned(packed_W, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 16)) return QMV_EALIGN;
   const int64_t m_pad = align_up(M, 128);
-  if (ws_bytes < (size_t)((K / 256) * m_pad * 144)) return QMV_EWORKSPACE;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return QMV_ECUDA;
+  if (m_pad / 128 > sms) return QMV_EUNSUPPORTED;       // one CTA group per 128 tokens
+  const int64_t planes_bytes = align_up((K / 256) * m_pad * 144, 256);
+  if (ws_bytes < (size_t)(planes_bytes + w4a4_partials_bytes(sms))) return QMV_EWORKSPACE;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
   uint8_t* planes = static_cast<uint8_t*>(ws);
+  uint8_t* partials = planes + planes_bytes;
   qmv_status st = from_cuda(launch_quant_act_tiled(x, x_scale, planes, M, m_pad, K, stream));
   if (st != QMV_OK) return st;
-  st = from_cuda(launch_w4a4(L, static_cast<const uint8_t*>(packed_W), planes, x_scale, y, M, m_pad, status, stream));
+  st = from_cuda(launch_w4a4(L, static_cast<const uint8_t*>(packed_W), planes, partials, x_scale, y, M, m_pad,
+                             status, stream));
   if (st == QMV_OK) g_last_route = QMV_NVFP4 * 100 + 4;
   return st;
 }

@@ -56,8 +56,10 @@ cudaError_t launch_quant_act_tiled(const uint16_t* x, float xs, uint8_t* planes,
                                    cudaStream_t s);
 // W4A4 block-scaled GEMM (tcgen05): y[M][N] = x_scale * s_T * (x codes . W codes) with
 // the activation planes written by launch_quant_act_tiled
-cudaError_t launch_w4a4(const Layout& L, const uint8_t* packed, const uint8_t* act_planes, float x_scale,
-                        float* y, int M, int64_t m_pad, unsigned* status, cudaStream_t s);
+cudaError_t launch_w4a4(const Layout& L, const uint8_t* packed, const uint8_t* act_planes, uint8_t* partials,
+                        float x_scale, float* y, int M, int64_t m_pad, unsigned* status, cudaStream_t s);
+// bytes of the W4A4 split-K region (partial-sum slots, then flags) for a device of `sms` SMs
+int64_t w4a4_partials_bytes(int sms);
 // returns the route variant launched (1 = M=1, 2 = M>1, 3 = grouped, 9 = fused gate|up SwiGLU)
 cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant);
 

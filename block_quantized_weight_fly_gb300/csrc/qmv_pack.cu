@@ -526,6 +526,9 @@ __global__ void quant_act_kernel(const uint16_t* __restrict__ x, float xs, uint8
 // layout). Rows m >= M (padding up to a multiple of 128) get zero codes and scales.
 __global__ void quant_act_tiled_kernel(const uint16_t* __restrict__ x, float xs, uint8_t* __restrict__ planes,
                                        int64_t M, int64_t m_pad, int64_t K) {
+  // the GEMM launched next may start its prologue and weight copies now; it reads
+  // these planes only after its grid-dependency wait
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t bpr = K / 16;
   if (b >= m_pad * bpr) return;

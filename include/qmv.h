@@ -208,10 +208,14 @@ qmv_status qmv_quant_act_nvfp4(const uint16_t* x, float x_scale, uint8_t* codes,
  * The MMA is tcgen05.mma kind::mxf4nvf4.block_scale (E2M1 x E2M1, UE4M3 scale per
  * 16 values, fp32 accumulator in tensor memory), reading the packed weight tiles
  * as they are. packed_W: device layout of one NVFP4 [N, K] matrix; K a multiple
- * of 256. M: any size >= 1 (meant for prefill, M >= 128). ws: device,
- * qmv_workspace_size(QMV_ENTRY_W4A4, QMV_NVFP4, M, N, K, 1, 1) bytes (the
- * activation's NVFP4 tiles; no zero-fill needed). y: device fp32 [M][N],
- * 16-byte aligned, fully overwritten. */
+ * of 256. M: 1 .. 128 x (number of SMs), meant for prefill (M >= 128); larger M
+ * returns QMV_EUNSUPPORTED (split the tokens into calls). ws: device,
+ * qmv_workspace_size(QMV_ENTRY_W4A4, QMV_NVFP4, M, N, K, 1, 1) bytes: the
+ * activation's NVFP4 tiles (rewritten by every call), then one slot of split-K
+ * partial sums and one publication flag per SM. As for qmv_gemv, zero-fill the
+ * workspace once; a call that returns without a device status error leaves every
+ * flag zero again. Calls sharing a workspace must not overlap.
+ * y: device fp32 [M][N], 16-byte aligned, fully overwritten. */
 qmv_status qmv_gemm_nvfp4_w4a4(const void* packed_W, const uint16_t* x, float x_scale,
                                float* y, int M, int64_t N, int64_t K, void* ws,
                                size_t ws_bytes, cudaStream_t stream);

@@ -66,6 +66,31 @@ def test_w4a4_small(q, M, N, K):
     assert norm_err(y, ref, den) <= TOL
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 512, 4096), (384, 768, 2048), (300, 1280, 3072)])
+def test_w4a4_split_k_deterministic_and_clean(q, M, N, K):
+    """Shapes whose output tiles are split between many CTAs: the finishing CTAs add
+    the published partial sums, every publication flag is zero again after the call,
+    and a second call with the same workspace gives the same bits."""
+    W, canon = host_matrix("nvfp4", 47, N, K)
+    Wd = host_dequant("nvfp4", canon, N, K)
+    x = synth.activations(53 + M, M, K)
+    xs = x_scale_of(x)
+    ref, den = ref_w4a4(Wd, act_dequant(x, xs))
+    packed = q.qmv_pack("nvfp4", torch.from_numpy(canon).cuda(), N, K)
+    ws = q.workspace(q.QMV_ENTRY_W4A4, "nvfp4", M, N, K)
+    y1 = q.qmv_gemm_nvfp4_w4a4(packed, x.cuda(), xs, N, K, ws).clone()
+    # workspace: activation planes, then one 128 KB partial-sum slot and one flag per SM
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    planes = -(-((K // 256) * (-(-M // 128) * 128) * 144) // 256) * 256
+    flags = ws[planes + sms * 131072:planes + sms * 131072 + 4 * sms]
+    assert int(flags.count_nonzero()) == 0
+    y2 = q.qmv_gemm_nvfp4_w4a4(packed, x.cuda(), xs, N, K, ws)
+    assert q.qmv_device_status() == 0
+    assert torch.equal(y1, y2)
+    assert int(flags.count_nonzero()) == 0
+    assert norm_err(y1.cpu().numpy(), ref, den) <= TOL
+
+
 @pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
 def test_w4a4_full_size_sampled(q, N, K):
     """The prefill configuration, M = 512: weights generated on the device, sampled
