@@ -137,13 +137,14 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of every kernel source: a recorded traffic figure is used only while it matches."""
     h = hashlib.sha256()
-    for rel in ("block_quantized_weight_fly_gb300/csrc/qmv_stream.cu",
-                "block_quantized_weight_fly_gb300/csrc/qmv_slab.cuh",
-                "block_quantized_weight_fly_gb300/csrc/qmv_layout.cuh",
-                "block_quantized_weight_fly_gb300/csrc/qmv_internal.h"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+    csrc = os.path.join(ROOT, "block_quantized_weight_fly_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 
