@@ -524,27 +524,32 @@ __global__ void quant_act_kernel(const uint16_t* __restrict__ x, float xs, uint8
 // operand: per k-group a plane of m_pad rows x 128 B of codes (core-matrix tiles,
 // as the NVFP4 weight planes) followed by m_pad x 16 B of scales (tcgen05.cp tile
 // layout). Rows m >= M (padding up to a multiple of 128) get zero codes and scales.
+// One thread per row and 32-value chunk (two blocks), rows fastest across the
+// threads: a warp's code stores cover whole 128-byte lines of the core-matrix tiles.
 __global__ void quant_act_tiled_kernel(const uint16_t* __restrict__ x, float xs, uint8_t* __restrict__ planes,
                                        int64_t M, int64_t m_pad, int64_t K) {
   // the GEMM launched next may start its prologue and weight copies now; it reads
   // these planes only after its grid-dependency wait
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t bpr = K / 16;
-  if (b >= m_pad * bpr) return;
-  const int64_t m = b / bpr, kb = b % bpr;
-  uint32_t packed[2] = {0u, 0u};
-  uint32_t sb = 0u;
-  if (m < M) sb = quant_block16(x + m * K + kb * 16, xs, packed);
-  uint8_t* plane = planes + (kb / 16) * (m_pad * 144);
-  const int blk = (int)(kb % 16);
-  *reinterpret_cast<uint2*>(plane + nv_code_off(m, blk >> 1, 2 * (blk & 1))) = make_uint2(packed[0], packed[1]);
-  plane[m_pad * 128 + nv_scale_off(m, blk)] = (uint8_t)sb;
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t cpr = K / 32;                      // 32-value chunks per row
+  if (b >= m_pad * cpr) return;
+  const int64_t m = b % m_pad, kc = b / m_pad;
+  uint32_t packed[4] = {0u, 0u, 0u, 0u};
+  uint32_t s0 = 0u, s1 = 0u;
+  if (m < M) {
+    s0 = quant_block16(x + m * K + kc * 32, xs, packed);
+    s1 = quant_block16(x + m * K + kc * 32 + 16, xs, packed + 2);
+  }
+  uint8_t* plane = planes + (kc / 8) * (m_pad * 144);
+  const int c = (int)(kc % 8);                    // chunk within the k-group: blocks 2c, 2c+1
+  *reinterpret_cast<uint4*>(plane + nv_code_off(m, c, 0)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  *reinterpret_cast<uint16_t*>(plane + m_pad * 128 + nv_scale_off(m, 2 * c)) = (uint16_t)(s0 | (s1 << 8));
 }
 
 cudaError_t launch_quant_act_tiled(const uint16_t* x, float xs, uint8_t* planes, int M, int64_t m_pad, int64_t K,
                                    cudaStream_t s) {
-  const int64_t total = m_pad * (K / 16);
+  const int64_t total = m_pad * (K / 32);
   const int threads = 256;
   quant_act_tiled_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, s>>>(x, xs, planes, M, m_pad, K);
   return cudaGetLastError();
