@@ -95,13 +95,22 @@ WORKLOADS = {
     "tower_m8": dict(fmt="q4_k", M=8, tower=True, E=288, topk=8,
                      mats=[("gate", 2048, 4096), ("up", 2048, 4096), ("down", 4096, 2048)],
                      desc="grouped Q4_K tower, 288 experts, top-8, M=8"),
+    "tower_fused_m1": dict(fmt="q4_k", M=1, tower=True, fused=True, E=288, topk=8,
+                           mats=[("gate|up", 2048, 4096), ("down", 4096, 2048)],
+                           desc="grouped Q4_K tower, 288 experts, top-8, M=1: fused gate|up [2 x 2048, 4096] "
+                                "with the SwiGLU epilogue, then down [4096,2048]"),
+    "tower_fused_m8": dict(fmt="q4_k", M=8, tower=True, fused=True, E=288, topk=8,
+                           mats=[("gate|up", 2048, 4096), ("down", 4096, 2048)],
+                           desc="grouped Q4_K tower, 288 experts, top-8, M=8: fused gate|up with the SwiGLU "
+                                "epilogue, then down"),
 }
 DEFAULT_WORKLOAD = "q4k_mlp_m1"
 DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, "q6k_head_m8": 2000,
                  "q6k_qkv_m1": 40000, "q6k_qkv_m8": 40000, "nvfp4_mlp_m1": 20000, "nvfp4_mlp_m8": 20000,
                  "fp8_m1": 40000, "fp8_m8": 40000, "q8_0_tiny": 20000, "tower_m1": 20000,
                  "tower_m4": 10000, "tower_m8": 5000, "nvfp4_w4a4_m512": 2000,
-                 "q4k_mlp_fused_m1": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000}
+                 "q4k_mlp_fused_m1": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000,
+                 "tower_fused_m1": 20000, "tower_fused_m8": 5000}
 
 METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"
 CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q5_k": 176 / 256, "q6_k": 210 / 256,
@@ -268,12 +277,14 @@ class DeviceWorkload:
         self.topk = w.get("topk", 1)
         self.mats = w["mats"]
         torch.cuda.synchronize()
-        base = [build_packed(q, self.fmt, 100 + i, N, K, 2 if (self.fused and i == 0) else self.E, dev)
+        # fused gate|up: a tower of both matrices (gate experts first, then up)
+        base = [build_packed(q, self.fmt, 100 + i, N, K, self.E * (2 if (self.fused and i == 0) else 1), dev)
                 for i, (_, N, K) in enumerate(self.mats)]
         torch.cuda.synchronize()
         # bytes a step streams, to size the rotation
         if self.tower:
-            per_expert = [canon_bytes(self.fmt, N, K) for _, N, K in self.mats]
+            per_expert = [canon_bytes(self.fmt, N, K) * (2 if (self.fused and i == 0) else 1)
+                          for i, (_, N, K) in enumerate(self.mats)]
             step_w = sum(per_expert) * min(self.E, self.M * self.topk)
         else:
             step_w = sum(canon_bytes(self.fmt, N, K) * (2 if (self.fused and i == 0) else 1)
@@ -289,7 +300,7 @@ class DeviceWorkload:
             self.y.append(torch.empty(ysh, dtype=torch.float32, device=dev))
             entry = q.QMV_ENTRY_GROUPED if self.tower else (q.QMV_ENTRY_W4A4 if self.w4a4 else q.QMV_ENTRY_GEMV)
             if self.fused and i == 0:
-                entry = q.QMV_ENTRY_SWIGLU
+                entry = q.QMV_ENTRY_GROUPED_SWIGLU if self.tower else q.QMV_ENTRY_SWIGLU
             self.ws.append(q.workspace(entry, self.fmt, self.M, N, K, self.E, self.topk, device=dev))
         # W4A4: the static activation scale of each x (amax / (448 * 6)), computed once
         self.x_scale = [float(x.float().abs().max()) / 2688.0 for x in self.x] if self.w4a4 else []
@@ -315,7 +326,8 @@ class DeviceWorkload:
             yb = self.y[i].numel() * 4
             if self.tower:
                 u = self.unique[s % len(self.unique)]
-                tot += u * canon_bytes(self.fmt, N, K) + xb + yb + self.M * self.topk * 4
+                wb = canon_bytes(self.fmt, N, K) * (2 if (self.fused and i == 0) else 1)
+                tot += u * wb + xb + yb + self.M * self.topk * 4
             else:
                 tot += canon_bytes(self.fmt, N, K) * (2 if (self.fused and i == 0) else 1) + xb + yb
         return tot
@@ -324,7 +336,10 @@ class DeviceWorkload:
         q = self.q
         c = s % self.copies
         for i, (_, N, K) in enumerate(self.mats):
-            if self.tower:
+            if self.tower and self.fused and i == 0:
+                q.qmv_grouped_swiglu(self.fmt, self.packed[c][i], self.ids[s % len(self.ids)], self.x[i], N, K,
+                                     self.E, self.ws[i], h=self.y[i])
+            elif self.tower:
                 q.qmv_grouped(self.fmt, self.packed[c][i], self.ids[s % len(self.ids)], self.x[i], N, K, self.E,
                               self.ws[i], x_per_pair=(i == len(self.mats) - 1), y=self.y[i])
             elif self.fused and i == 0:

@@ -20,6 +20,7 @@ QMV_Q8_0, QMV_Q4_K, QMV_Q6_K, QMV_NVFP4, QMV_FP8_ROW, QMV_Q5_K = 1, 2, 3, 4, 5, 
 FORMATS = {"q8_0": QMV_Q8_0, "q4_k": QMV_Q4_K, "q6_k": QMV_Q6_K, "nvfp4": QMV_NVFP4,
            "fp8_row": QMV_FP8_ROW, "q5_k": QMV_Q5_K}
 QMV_ENTRY_GEMV, QMV_ENTRY_GROUPED, QMV_ENTRY_W4A4, QMV_ENTRY_SWIGLU = 1, 2, 3, 4
+QMV_ENTRY_GROUPED_SWIGLU = 5
 QMV_MAX_M = 8
 
 STATUS = {0: "QMV_OK", 1: "QMV_EINVAL", 2: "QMV_EALIGN", 3: "QMV_EUNSUPPORTED", 4: "QMV_ECUDA",
@@ -61,6 +62,7 @@ _gemv = _sig("qmv_gemv", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
 _gemv_swiglu = _sig("qmv_gemv_swiglu", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
 _gemv_noalloc = _sig("qmv_gemv_noalloc", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P])
 _grouped = _sig("qmv_grouped", _I, [_I, _P, _P, _P, _I, _P, _I, _I, _I64, _I64, _I64, _P, _SZ, _P])
+_grouped_swiglu = _sig("qmv_grouped_swiglu", _I, [_I, _P, _P, _P, _P, _I, _I, _I64, _I64, _I64, _P, _SZ, _P])
 _quant_act = _sig("qmv_quant_act_nvfp4", _I, [_P, _F, _P, _P, _I, _I64, _P])
 _w4a4 = _sig("qmv_gemm_nvfp4_w4a4", _I, [_P, _P, _F, _P, _I, _I64, _I64, _P, _SZ, _P])
 _status_str = _sig("qmv_status_str", ctypes.c_char_p, [_I])
@@ -70,7 +72,7 @@ _dev_status = _sig("qmv_device_status", _I, [_I])
 EXPORTED = ["qmv_canon_size", "qmv_pack_size", "qmv_pack", "qmv_quantize", "qmv_dequant",
             "qmv_workspace_size", "qmv_gemv", "qmv_grouped", "qmv_quant_act_nvfp4",
             "qmv_gemm_nvfp4_w4a4", "qmv_status_str", "qmv_last_route", "qmv_device_status",
-            "qmv_gemv_noalloc", "qmv_gemv_swiglu"]
+            "qmv_gemv_noalloc", "qmv_gemv_swiglu", "qmv_grouped_swiglu"]
 
 
 def _fmt(fmt) -> int:
@@ -229,6 +231,23 @@ def qmv_grouped(fmt, tower: torch.Tensor, expert_ids: torch.Tensor, x: torch.Ten
     _check(_grouped(_fmt(fmt), _ptr(tower), _ptr(expert_ids), _ptr(x), 1 if x_per_pair else 0, _ptr(y),
                     M, topk, N, K, E, _ptr(ws), ws.numel(), _stream(stream)), "qmv_grouped")
     return y
+
+
+def qmv_grouped_swiglu(fmt, tower: torch.Tensor, expert_ids: torch.Tensor, x: torch.Tensor, N: int,
+                       K: int, E: int, ws: torch.Tensor, h: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """h[t, j] = silu(gate_e . x[t]) * (up_e . x[t]), e = expert_ids[t, j], over a
+    2E-expert tower (gate matrices 0..E-1, then up matrices E..2E-1)."""
+    _dev(tower, "tower"); _dev(expert_ids, "expert_ids"); _dev(x, "x"); _dev(ws, "ws")
+    if expert_ids.dtype != torch.int32 or expert_ids.dim() != 2:
+        raise ValueError("expert_ids must be int32 [M, topk]")
+    M, topk = expert_ids.shape
+    x = _bits16(x)
+    if h is None:
+        h = torch.empty((M, topk, N), dtype=torch.float32, device=x.device)
+    _check(_grouped_swiglu(_fmt(fmt), _ptr(tower), _ptr(expert_ids), _ptr(x), _ptr(h), M, topk, N, K, E,
+                           _ptr(ws), ws.numel(), _stream(stream)), "qmv_grouped_swiglu")
+    return h
 
 
 def qmv_quant_act_nvfp4(x: torch.Tensor, x_scale: float, codes: torch.Tensor | None = None,

@@ -106,7 +106,7 @@ size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, i
     if (M > QMV_MAX_M) return 0;
     return (size_t)ws_plan_stream(M, 0, 2 * sms).total;
   }
-  if (entry == QMV_ENTRY_SWIGLU) {
+  if (entry == QMV_ENTRY_SWIGLU || entry == QMV_ENTRY_GROUPED_SWIGLU) {
     if (M > QMV_MAX_M) return 0;
     return (size_t)ws_plan_stream(M, 0, 2 * sms, 2).total;
   }
@@ -203,6 +203,39 @@ qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, fl
   a.packed = static_cast<const uint8_t*>(tower);
   a.x = x; a.y = h; a.ids = nullptr;
   a.M = M; a.topk = 1; a.x_per_pair = 0; a.swiglu = 1;
+  a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
+  a.status = status;
+  a.num_ctas = ctas;
+  int variant = 0;
+  qmv_status st = from_cuda(launch_stream(a, stream, &variant));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
+  return st;
+}
+
+qmv_status qmv_grouped_swiglu(qmv_fmt fmt, const void* tower, const int32_t* expert_ids, const uint16_t* x,
+                              float* h, int M, int topk, int64_t N, int64_t K, int64_t E, void* ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !tower || !expert_ids || !x || !h || !ws) return QMV_EINVAL;
+  if (M < 1 || M > QMV_MAX_M || topk < 1 || topk > 8 || N <= 0 || K <= 0 || E <= 0) return QMV_EINVAL;
+  if (E > (int64_t)1 << 23) return QMV_EUNSUPPORTED;   // ids are packed with a 6-bit pair index
+  Layout L;
+  if (!make_layout((int)fmt, N, K, 2 * E, &L)) return QMV_EUNSUPPORTED;
+  const int64_t experts = (int64_t)M * topk < E ? (int64_t)M * topk : E;
+  if (!slab_count_ok(L, 2 * experts)) return QMV_EUNSUPPORTED;
+  if (!aligned(tower, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(h, 4) ||
+      !aligned(expert_ids, 4))
+    return QMV_EALIGN;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return QMV_ECUDA;
+  const int ctas = stream_grid(2 * experts * L.row_tiles * L.k_groups, M, true, sms);
+  if (ws_bytes < (size_t)ws_plan_stream(M, 0, ctas, 2).total) return QMV_EWORKSPACE;
+  unsigned* status = status_ptr();
+  if (!status) return QMV_ECUDA;
+  StreamArgs a;
+  a.L = L;
+  a.packed = static_cast<const uint8_t*>(tower);
+  a.x = x; a.y = h; a.ids = expert_ids;
+  a.M = M; a.topk = topk; a.x_per_pair = 0; a.swiglu = 1;
   a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
   a.status = status;
   a.num_ctas = ctas;

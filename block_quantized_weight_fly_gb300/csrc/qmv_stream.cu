@@ -148,10 +148,37 @@ struct KParams {
   float* partials;   // [num_ctas][128][mt]
 };
 
-// SW: fused gate|up with the SwiGLU epilogue. The tower holds two experts (gate,
-// up) over the same x; each row tile's gate k-groups and then the same rows' up
-// k-groups form one unit, so a thread ends a unit holding g and u of its outputs
-// and writes silu(g) * u.
+// SW: fused gate|up with the SwiGLU epilogue. The tower holds 2E experts: the E
+// gate matrices, then the E up matrices (E = 1 for the dense call). Each segment is
+// one (routed) expert e; a row tile's gate k-groups (expert e) and then the same
+// rows' up k-groups (expert E + e) form one unit over the same x rows, so a thread
+// ends a unit holding g and u of its outputs and writes silu(g) * u.
+//
+// The slab sequence: segment-major, then row tile, then (SW) pass gate/up, then
+// k-group. A cursor walks it.
+// position in the slab sequence (segment, row tile, SW pass, k-group)
+template <bool SW>
+struct Cursor {
+  int g, pass, t, seg;
+  __device__ __forceinline__ void init(int s, int G, int RT) {
+    g = s % G;
+    int u = s / G;
+    pass = 0;
+    if constexpr (SW) { pass = u & 1; u >>= 1; }
+    t = u % RT;
+    seg = u / RT;
+  }
+  __device__ __forceinline__ void next(int G, int RT) {
+    if (++g < G) return;
+    g = 0;
+    if constexpr (SW) {
+      if (++pass < 2) return;
+      pass = 0;
+    }
+    if (++t == RT) { t = 0; ++seg; }
+  }
+};
+
 template <int FMT, int MT, bool SW>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(const KParams kp) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -197,12 +224,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   if (warp == 0) {
     if (a.ids == nullptr) {
       if (lane == 0) {
-        misc[1] = SW ? 2 : 1;
-        for (int sgi = 0; sgi < (SW ? 2 : 1); ++sgi) {
-          segs[sgi].expert = sgi;
-          segs[sgi].R = a.M;
-          for (int r = 0; r < 8; ++r) { segs[sgi].xrow[r] = r; segs[sgi].yrow[r] = r; }
-        }
+        misc[1] = 1;
+        segs[0].expert = 0;
+        segs[0].R = a.M;
+        for (int r = 0; r < 8; ++r) { segs[0].xrow[r] = r; segs[0].yrow[r] = r; }
       }
     } else {
       // Distinct routed experts, ascending. Key = id * 64 + pair index (unique),
@@ -215,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       bool bad = false;
       for (int p = lane; p < P; p += 32) {
         const int id = a.ids[p];
-        bad |= (id < 0 || (int64_t)id >= L.E);
+        bad |= (id < 0 || (int64_t)id >= (SW ? L.E / 2 : L.E));   // SW: ids index the gate half
         skeys[p] = (id << 6) | p;
       }
       if (__any_sync(0xffffffffu, bad)) {
@@ -276,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   // slab counts fit in 32 bits (the host refuses larger problems)
   const int G = (int)L.k_groups;
   const int RT = (int)L.row_tiles;
-  const int S = nseg * RT * G;
+  const int S = nseg * RT * G * (SW ? 2 : 1);
+  const int Eh = SW ? (int)(L.E / 2) : 0;        // SW: the up matrix of expert e is expert Eh + e
   const int P = (int)gridDim.x;
   const int c = (int)blockIdx.x;
   // range start of CTA i: floor(i * S / P), in 32-bit arithmetic (S = Sq * P + Sr;
@@ -291,7 +317,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
 
   // M = 1: one lane of the producer warp streams the slabs of [s0, s1) into the stages
   auto produce1 = [&]() {
-    int g = s0 % G, t = SW ? (s0 / G) / 2 : (s0 / G) % RT, seg = SW ? (s0 / G) % 2 : (s0 / G) / RT;
+    Cursor<SW> cur;
+    cur.init(s0, G, RT);
     int stage = 0;
     uint32_t rphase = 0;          // parity of the current round over the stage ring
     int it = 0;
@@ -301,17 +328,18 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     // then wait for the previous grid, then the activations of those stages.
     const int first = (s1 - s0) < kp.stages ? (s1 - s0) : kp.stages;
     {
-      int gg = g, t2 = t, sg2 = seg;
+      Cursor<SW> c2 = cur;
       for (int i = 0; i < first; ++i) {
-        const Seg& sg = segs[sg2];
+        const Seg& sg = segs[c2.seg];
         uint8_t* st = smem + kp.stage_base + i * kp.stage_bytes;
-        const uint8_t* plane = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + gg * L.group_bytes;
-        const int kv = (kMayBeRagged && gg == G - 1) ? kv_last : kSlabK;
+        const uint8_t* plane =
+            a.packed + kHeaderBytes + (sg.expert + c2.pass * Eh) * L.expert_bytes + c2.g * L.group_bytes;
+        const int kv = (kMayBeRagged && c2.g == G - 1) ? kv_last : kSlabK;
         const int R = sg.R < MT ? sg.R : MT;
         mbar_expect_tx(&full[i], abytes + bbytes + (uint32_t)(kv * 2) * (uint32_t)R);
-        bulk_g2s(st, plane + (int64_t)t2 * kSlabRows * L.rec, abytes, &full[i]);
-        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t2 * bbytes, bbytes, &full[i]);
-        if (++gg == G) { gg = 0; if (SW) { if (++sg2 == 2) { sg2 = 0; ++t2; } } else if (++t2 == RT) { t2 = 0; ++sg2; } }
+        bulk_g2s(st, plane + (int64_t)c2.t * kSlabRows * L.rec, abytes, &full[i]);
+        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)c2.t * bbytes, bbytes, &full[i]);
+        c2.next(G, RT);
       }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -320,22 +348,23 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         if (!mbar_wait(&empty[stage], rphase ^ 1u, a.status)) { misc[0] = 1; break; }
       }
       if (misc[0]) break;
-      const Seg& sg = segs[seg];
+      const Seg& sg = segs[cur.seg];
       uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
-      const uint8_t* plane = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + g * L.group_bytes;
-      const int kv = (kMayBeRagged && g == G - 1) ? kv_last : kSlabK;
+      const uint8_t* plane =
+          a.packed + kHeaderBytes + (sg.expert + cur.pass * Eh) * L.expert_bytes + cur.g * L.group_bytes;
+      const int kv = (kMayBeRagged && cur.g == G - 1) ? kv_last : kSlabK;
       const uint32_t xbytes = (uint32_t)(kv * 2);
       const int R = sg.R < MT ? sg.R : MT;
       if (it >= first) {
         mbar_expect_tx(&full[stage], abytes + bbytes + xbytes * (uint32_t)R);
-        bulk_g2s(st, plane + (int64_t)t * kSlabRows * L.rec, abytes, &full[stage]);
-        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t * bbytes, bbytes, &full[stage]);
+        bulk_g2s(st, plane + (int64_t)cur.t * kSlabRows * L.rec, abytes, &full[stage]);
+        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)cur.t * bbytes, bbytes, &full[stage]);
       }
       for (int r = 0; r < R; ++r)
-        bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)g * kSlabK, xbytes,
+        bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)cur.g * kSlabK, xbytes,
                  &full[stage]);
       if (++stage == kp.stages) { stage = 0; rphase ^= 1u; }
-      if (++g == G) { g = 0; if (SW) { if (++seg == 2) { seg = 0; ++t; } } else if (++t == RT) { t = 0; ++seg; } }
+      cur.next(G, RT);
     }
     // drain: copies issued into stages the consumers may not have waited for
     if (misc[0]) {
@@ -353,7 +382,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   // lanes taking part: M = 1 -> lane 0 only (the others leave), M > 1 -> all 32
   constexpr unsigned kPMask = (MT == 1) ? 1u : 0xffffffffu;
   auto produce8 = [&]() {
-    int g = s0 % G, t = SW ? (s0 / G) / 2 : (s0 / G) % RT, seg = SW ? (s0 / G) % 2 : (s0 / G) / RT;
+    Cursor<SW> cur;
+    cur.init(s0, G, RT);
     int stage = 0;
     uint32_t rphase = 0;          // parity of the current round over the stage ring
     int it = 0;
@@ -363,18 +393,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     // then wait for the previous grid, then the activations of those stages.
     const int first = (s1 - s0) < kp.stages ? (s1 - s0) : kp.stages;
     if (lane == 0) {
-      int gg = g, t2 = t, sg2 = seg;
+      Cursor<SW> c2 = cur;
       for (int i = 0; i < first; ++i) {
-        const Seg& sg = segs[sg2];
+        const Seg& sg = segs[c2.seg];
         uint8_t* st = smem + kp.stage_base + i * kp.stage_bytes;
-        const uint8_t* plane = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + gg * L.group_bytes;
-        const int kv = (kMayBeRagged && gg == G - 1) ? kv_last : kSlabK;
+        const uint8_t* plane =
+            a.packed + kHeaderBytes + (sg.expert + c2.pass * Eh) * L.expert_bytes + c2.g * L.group_bytes;
+        const int kv = (kMayBeRagged && c2.g == G - 1) ? kv_last : kSlabK;
         const int R = sg.R < MT ? sg.R : MT;
         const uint32_t xtx = (MT == 1) ? (uint32_t)(kv * 2) * (uint32_t)R : 0u;
         mbar_expect_tx(&full[i], abytes + bbytes + xtx);
-        bulk_g2s(st, plane + (int64_t)t2 * kSlabRows * L.rec, abytes, &full[i]);
-        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t2 * bbytes, bbytes, &full[i]);
-        if (++gg == G) { gg = 0; if (SW) { if (++sg2 == 2) { sg2 = 0; ++t2; } } else if (++t2 == RT) { t2 = 0; ++sg2; } }
+        bulk_g2s(st, plane + (int64_t)c2.t * kSlabRows * L.rec, abytes, &full[i]);
+        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)c2.t * bbytes, bbytes, &full[i]);
+        c2.next(G, RT);
       }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -386,33 +417,35 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         if (!ok) { if (lane == 0) misc[0] = 1; break; }
       }
       if (__shfl_sync(kPMask, misc[0], 0)) break;
-      const Seg& sg = segs[seg];
+      const Seg& sg = segs[cur.seg];
       uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
-      const uint8_t* plane = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + g * L.group_bytes;
-      const int kv = (kMayBeRagged && g == G - 1) ? kv_last : kSlabK;
+      const uint8_t* plane =
+          a.packed + kHeaderBytes + (sg.expert + cur.pass * Eh) * L.expert_bytes + cur.g * L.group_bytes;
+      const int kv = (kMayBeRagged && cur.g == G - 1) ? kv_last : kSlabK;
       const uint32_t xbytes = (uint32_t)(kv * 2);
       const int R = sg.R < MT ? sg.R : MT;
       if (lane == 0 && it >= first) {
         mbar_expect_tx(&full[stage], abytes + bbytes + (MT == 1 ? xbytes * (uint32_t)R : 0u));
-        bulk_g2s(st, plane + (int64_t)t * kSlabRows * L.rec, abytes, &full[stage]);
-        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)t * bbytes, bbytes, &full[stage]);
+        bulk_g2s(st, plane + (int64_t)cur.t * kSlabRows * L.rec, abytes, &full[stage]);
+        if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)cur.t * bbytes, bbytes, &full[stage]);
       }
       if (MT == 1) {
         if (lane == 0)
           for (int r = 0; r < R; ++r)
-            bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)g * kSlabK, xbytes,
-                     &full[stage]);
+            bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)cur.g * kSlabK,
+                     xbytes, &full[stage]);
       } else {
         const int chunks = (int)(xbytes / 16);       // 16-byte pieces of one row's slice
         for (int r = 0; r < R; ++r) {
-          const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)g * kSlabK);
+          const uint8_t* src =
+              reinterpret_cast<const uint8_t*>(a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)cur.g * kSlabK);
           uint8_t* dst = st + kp.x_off + r * kXStride;
           for (int c16 = lane; c16 < chunks; c16 += 32) cp_async16(dst + 16 * c16, src + 16 * c16);
         }
         cp_async_arrive_noinc(&full[stage]);
       }
       if (++stage == kp.stages) { stage = 0; rphase ^= 1u; }
-      if (++g == G) { g = 0; if (SW) { if (++seg == 2) { seg = 0; ++t; } } else if (++t == RT) { t = 0; ++seg; } }
+      cur.next(G, RT);
     }
     // drain: copies issued into stages the consumers may not have waited for. At
     // M > 1 the first-round stages not reached above still expect the lanes'
@@ -455,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
 #pragma unroll
   for (int e = 0; e < NV; ++e) acc[e] = 0.f;
   int T = s0 / UL;                        // current unit: a row tile of one segment (SW: of both)
-  int tt = SW ? T : T % RT, seg = SW ? 0 : T / RT;
+  int tt = T % RT, seg = T / RT;
   int stage = 0;
   uint32_t fphase = 0;                   // parity of the full barrier for this stage round
   bool aborted = false;
@@ -583,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       }
       if (!aborted && (full_cover || reducer)) {
         const uint8_t* extras = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + L.k_groups * L.group_bytes;
-        const uint8_t* extras_u = extras + L.expert_bytes;     // SW: the up expert's
+        const uint8_t* extras_u = extras + (int64_t)Eh * L.expert_bytes;     // SW: the up expert's
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
@@ -605,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       for (int e = 0; e < NV; ++e) acc[e] = 0.f;
     }
     ++T;
-    if (SW) { ++tt; } else if (++tt == RT) { tt = 0; ++seg; }
+    if (++tt == RT) { tt = 0; ++seg; }
   }
 }
 
@@ -662,7 +695,9 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   if (kp.stages > kMaxStages) kp.stages = kMaxStages;
   if (kp.stages < 2) return cudaErrorInvalidConfiguration;
   const int64_t pairs = (int64_t)a.M * a.topk;
-  if (!slab_count_ok(a.L, a.ids ? (pairs < a.L.E ? pairs : a.L.E) : 1)) return cudaErrorInvalidValue;
+  const int64_t e_ids = SW ? a.L.E / 2 : a.L.E;      // experts the ids may name
+  const int64_t segs_max = a.ids ? (pairs < e_ids ? pairs : e_ids) : 1;
+  if (!slab_count_ok(a.L, segs_max * (SW ? 2 : 1))) return cudaErrorInvalidValue;
   const WsPlan plan = ws_plan_stream(MT, 0, a.num_ctas, SW ? 2 : 1);
   kp.partials = reinterpret_cast<float*>(a.ws + plan.partials_off);
   const int smem = kp.stage_base + kp.stages * kp.stage_bytes;
@@ -701,7 +736,7 @@ static cudaError_t launch_fmt(const StreamArgs& a, cudaStream_t s, int* variant)
   const bool grouped = a.ids != nullptr;
   *variant = grouped ? 3 : (a.M <= 1 ? 1 : 2);
   if (a.swiglu) {
-    *variant = 9;
+    *variant = grouped ? 10 : 9;
     if (a.M <= 1) return launch_t<FMT, 1, true>(a, s);
     return launch_t<FMT, 8, true>(a, s);
   }

@@ -86,7 +86,13 @@ typedef enum {
 } qmv_status;
 
 /* Entry ids for qmv_workspace_size. */
-enum { QMV_ENTRY_GEMV = 1, QMV_ENTRY_GROUPED = 2, QMV_ENTRY_W4A4 = 3, QMV_ENTRY_SWIGLU = 4 };
+enum {
+  QMV_ENTRY_GEMV = 1,
+  QMV_ENTRY_GROUPED = 2,
+  QMV_ENTRY_W4A4 = 3,
+  QMV_ENTRY_SWIGLU = 4,
+  QMV_ENTRY_GROUPED_SWIGLU = 5
+};
 
 /* Largest decode batch served by qmv_gemv / qmv_grouped (M rows of x). */
 #define QMV_MAX_M 8
@@ -192,6 +198,22 @@ qmv_status qmv_grouped(qmv_fmt fmt, const void* tower, const int32_t* expert_ids
  * qmv_gemv). Each gate and up row is streamed from HBM once per call. */
 qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, float* h, int M,
                            int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Grouped fused gate|up with the SwiGLU epilogue: the routed experts' first MLP
+ * projection in one call, M = 1..8, topk = 1..8:
+ *   h[t][j][n] = silu(g) * u,  g = W_{e} . x[t],  u = W_{E+e} . x[t],  e = expert_ids[t][j],
+ * the union of qmv_grouped (each distinct routed expert streamed once per call)
+ * and qmv_gemv_swiglu (gate and up read in one pass, SwiGLU in the epilogue).
+ * tower: the device layout of a 2E-expert tower (qmv_pack with 2E experts): the E
+ * gate matrices first (expert e), then the E up matrices (expert E + e).
+ * expert_ids: device int32 [M][topk] in 0..E-1, distinct within a token (an id
+ * outside that range latches QMV_ERANGE in the device status and writes nothing). x: device bf16
+ * [M][K]. h: device fp32 [M][topk][N], fully overwritten. ws: device,
+ * qmv_workspace_size(QMV_ENTRY_GROUPED_SWIGLU, ...) bytes, zero-filled once (as
+ * for qmv_gemv). E <= 2^23. */
+qmv_status qmv_grouped_swiglu(qmv_fmt fmt, const void* tower, const int32_t* expert_ids,
+                              const uint16_t* x, float* h, int M, int topk, int64_t N, int64_t K,
+                              int64_t E, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* NVFP4 activation quantizer (W4A4 prefill): per 16-value block of bf16 x[M][K],
  * s_b = e4m3_rne_sat(amax_b / (6 x_scale)); codes = e2m1_rne_sat(x / (s_b x_scale)),

@@ -76,3 +76,68 @@ def test_swiglu_full_size_q4k(q):
         assert q.qmv_device_status() == 0
         err = np.abs(got - href) / swiglu_bound(g, dg, u, du, href)
         assert float(err.max()) <= 1.0, (M, float(err.max()))
+
+
+# ---------------------------------------------------------------------------
+# grouped: the routed experts' gate|up over a 2E-expert tower
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,topk,E", [(1, 8, 16), (1, 1, 3), (4, 2, 5), (8, 4, 6), (8, 8, 8)])
+def test_grouped_swiglu_parity(q, fmt, M, topk, E):
+    N, K = 200, 512
+    W, canon = host_matrix(fmt, 83, N, K, 2 * E)          # gate experts 0..E-1, up experts E..2E-1
+    D = host_dequant(fmt, canon, N, K, 2 * E)
+    ids = synth.expert_ids(83 + M + E, M, topk, E)
+    x = synth.activations(89 + M, M, K)
+    xb = synth.bf16_bits(x)
+    g, dg = oracle.grouped_f64(lambda e: D[e * N:(e + 1) * N], ids, xb, False)
+    u, du = oracle.grouped_f64(lambda e: D[(E + e) * N:(E + e + 1) * N], ids, xb, False)
+    href = oracle.swiglu_f64(g, u)
+    tower = q.qmv_pack(fmt, torch.from_numpy(canon).cuda(), N, K, 2 * E)
+    ws = q.workspace(q.QMV_ENTRY_GROUPED_SWIGLU, fmt, M, N, K, E, topk)
+    h = q.qmv_grouped_swiglu(fmt, tower, torch.from_numpy(ids).cuda(), x.cuda(), N, K, E, ws)
+    assert q.qmv_last_route() == q.FORMATS[fmt] * 100 + 10
+    h = h.cpu().numpy().astype(np.float64)
+    assert q.qmv_device_status() == 0
+    err = np.abs(h - href) / swiglu_bound(g, dg, u, du, href)
+    assert float(err.max()) <= 1.0, float(err.max())
+    assert int(ws.count_nonzero()) == 0
+
+
+def test_grouped_swiglu_ragged_and_shared(q):
+    """K with a ragged last k-group (Q8_0, K = 800), N not a multiple of 128, and
+    experts shared by several tokens (8 tokens over 3 experts)."""
+    fmt, N, K, E, M, topk = "q8_0", 333, 800, 3, 8, 2
+    W, canon = host_matrix(fmt, 97, N, K, 2 * E)
+    D = host_dequant(fmt, canon, N, K, 2 * E)
+    ids = synth.expert_ids(97, M, topk, E)
+    x = synth.activations(97, M, K)
+    xb = synth.bf16_bits(x)
+    g, dg = oracle.grouped_f64(lambda e: D[e * N:(e + 1) * N], ids, xb, False)
+    u, du = oracle.grouped_f64(lambda e: D[(E + e) * N:(E + e + 1) * N], ids, xb, False)
+    href = oracle.swiglu_f64(g, u)
+    tower = q.qmv_pack(fmt, torch.from_numpy(canon).cuda(), N, K, 2 * E)
+    ws = q.workspace(q.QMV_ENTRY_GROUPED_SWIGLU, fmt, M, N, K, E, topk)
+    h = q.qmv_grouped_swiglu(fmt, tower, torch.from_numpy(ids).cuda(), x.cuda(), N, K, E, ws)
+    h = h.cpu().numpy().astype(np.float64)
+    assert q.qmv_device_status() == 0
+    err = np.abs(h - href) / swiglu_bound(g, dg, u, du, href)
+    assert float(err.max()) <= 1.0, float(err.max())
+    assert int(ws.count_nonzero()) == 0
+
+
+def test_grouped_swiglu_id_range(q):
+    """An id naming an up matrix (E <= id < 2E) is outside the gate half: the call
+    latches the range status and leaves h as it was."""
+    fmt, N, K, E = "q4_k", 128, 256, 3
+    W, canon = host_matrix(fmt, 5, N, K, 2 * E)
+    tower = q.qmv_pack(fmt, torch.from_numpy(canon).cuda(), N, K, 2 * E)
+    ws = q.workspace(q.QMV_ENTRY_GROUPED_SWIGLU, fmt, 1, N, K, E, 2)
+    x = synth.activations(5, 1, K).cuda()
+    h = torch.full((1, 2, N), 7.0, device="cuda")
+    q.qmv_device_status(reset=True)
+    q.qmv_grouped_swiglu(fmt, tower, torch.tensor([[0, E]], dtype=torch.int32, device="cuda"), x, N, K, E,
+                         ws, h=h)
+    assert q.qmv_device_status(reset=True) == 7
+    assert bool((h == 7.0).all())
+    assert int(ws.count_nonzero()) == 0
