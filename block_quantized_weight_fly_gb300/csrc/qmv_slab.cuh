@@ -88,18 +88,40 @@ __device__ __forceinline__ float u6f(uint32_t v) {
 __device__ __forceinline__ float2 h2x2f(uint32_t v) {
   return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
-// FP4 E2M1 pair (one byte) -> f16x2, exact
-__device__ __forceinline__ uint32_t e2m1x2_f16(uint32_t byte) {
-  uint32_t r;
-  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
-  return r;
-}
 // FP8 E4M3 pair (low 16 bits) -> f16x2, exact
 __device__ __forceinline__ uint32_t e4m3x2_f16(uint32_t two) {
   uint32_t r;
   const unsigned short v = (unsigned short)(two & 0xFFFFu);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
+}
+// the four E2M1 pairs of a word (bytes 0..3) -> four f16x2, exact. The bytes are
+// taken as the low bytes of the word's 16-bit halves and of those of word >> 8, so
+// one shift serves all four conversions.
+__device__ __forceinline__ void e2m1x4_f16(uint32_t w, uint32_t* p) {
+  asm("{ .reg .b16 l, h, l8, h8; .reg .b8 b0, b1, b2, b3; .reg .b32 s;\n\t"
+      "shr.b32 s, %4, 8;\n\t"
+      "mov.b32 {l, h}, %4;\n\t"
+      "mov.b32 {l8, h8}, s;\n\t"
+      "cvt.u8.u16 b0, l;\n\t"
+      "cvt.u8.u16 b1, l8;\n\t"
+      "cvt.u8.u16 b2, h;\n\t"
+      "cvt.u8.u16 b3, h8;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3])
+      : "r"(w));
+}
+// the two E4M3 pairs of a word (halves 0, 1) -> two f16x2, exact
+__device__ __forceinline__ void e4m3x4_f16(uint32_t w, uint32_t* p) {
+  asm("{ .reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(p[0]), "=r"(p[1])
+      : "r"(w));
 }
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -641,36 +663,71 @@ __device__ __forceinline__ uint32_t nv_sbyte(const uint32_t* S, int j, int t) {
 }
 __device__ __forceinline__ void nv_frag(uint32_t code_word, uint32_t sbyte, uint32_t* p) {
   const uint32_t s = e4m3x2_f16(sbyte | (sbyte << 8));
-  p[0] = hmul2(e2m1x2_f16(code_word & 0xFFu), s);
-  p[1] = hmul2(e2m1x2_f16((code_word >> 8) & 0xFFu), s);
-  p[2] = hmul2(e2m1x2_f16((code_word >> 16) & 0xFFu), s);
-  p[3] = hmul2(e2m1x2_f16(code_word >> 24), s);
+  e2m1x4_f16(code_word, p);
+  p[0] = hmul2(p[0], s);
+  p[1] = hmul2(p[1], s);
+  p[2] = hmul2(p[2], s);
+  p[3] = hmul2(p[3], s);
 }
 
+// M = 1: block-separated unit columns. Chunk j's two 16-value blocks land in
+// columns 2(j/2) and 2(j/2) + 1 of accumulator set j%2, so each of a row's 16
+// blocks in the slab keeps its own output slot; the codes go to the MMA as plain
+// e2m1 values and each block's E4M3 scale multiplies its sum once, after the MMAs.
+// Column c is fed by lanes (c, t): x of chunk pair c/2, and only from the lanes
+// whose k positions hold block c%2 of the chunk (t/2 == c%2); other lanes feed 0.
+// Lane (g, t) ends with blocks 4t..4t+3 of rows g and g + 8 -- K step t of the
+// scale plane, one 32-bit word per row.
 template <>
 struct Slab<F_NVFP4, 1> {
   __device__ static void run(const uint8_t* st, const uint8_t* sf, const uint8_t* xs, int, int w, int lane,
                              float2*, float* acc) {
     const int g = lane >> 2, t = lane & 3;
-    const uint4 xr = lds128v(xs + 64 * g + 16 * t);
-    const uint32_t x0 = bf16x2_to_f16x2(xr.x), x1 = bf16x2_to_f16x2(xr.y);
-    const uint32_t x2 = bf16x2_to_f16x2(xr.z), x3 = bf16x2_to_f16x2(xr.w);
-    uint32_t CA[8], CB[8], SA[4], SB[4];
-    nv_load(st, sf, 16 * w + g, t, CA, SA);
-    nv_load(st, sf, 16 * w + g + 8, t, CB, SB);
+    const int rA = 16 * w + g, rB = rA + 8;
+    const int jp = g >> 1;                           // the chunk pair this lane's column serves
+    const bool feeds = ((t >> 1) == (g & 1));
+    uint32_t xe[4], xo[4];
+    {
+      const uint4 a = lds128v(xs + 128 * jp + 16 * t);
+      const uint4 b = lds128v(xs + 128 * jp + 64 + 16 * t);
+      xe[0] = feeds ? bf16x2_to_f16x2(a.x) : 0u;
+      xe[1] = feeds ? bf16x2_to_f16x2(a.y) : 0u;
+      xe[2] = feeds ? bf16x2_to_f16x2(a.z) : 0u;
+      xe[3] = feeds ? bf16x2_to_f16x2(a.w) : 0u;
+      xo[0] = feeds ? bf16x2_to_f16x2(b.x) : 0u;
+      xo[1] = feeds ? bf16x2_to_f16x2(b.y) : 0u;
+      xo[2] = feeds ? bf16x2_to_f16x2(b.z) : 0u;
+      xo[3] = feeds ? bf16x2_to_f16x2(b.w) : 0u;
+    }
+    uint32_t CA[8], CB[8];
+    {
+      const uint8_t* ca = st + (rA >> 3) * 1024 + (rA & 7) * 16 + 4 * t;
+      const uint8_t* cb = st + (rB >> 3) * 1024 + (rB & 7) * 16 + 4 * t;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { CA[j] = lds32(ca + 128 * j); CB[j] = lds32(cb + 128 * j); }
+    }
     float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      uint32_t pa[4], pb[4];
-      nv_frag(CA[j], nv_sbyte(SA, j, t), pa);
-      nv_frag(CB[j], nv_sbyte(SB, j, t), pb);
-      const bool mine = (g == j);
+      const uint32_t wa = CA[j], wb = CB[j];
+      const bool mine = (j >> 1) == jp;
+      const uint32_t* xv = (j & 1) ? xo : xe;
       float* d = (j & 1) ? dO : dE;
-      mma_f16(d, pa[0], pb[0], pa[1], pb[1], sel(mine, x0), sel(mine, x1));
-      mma_f16(d, pa[2], pb[2], pa[3], pb[3], sel(mine, x2), sel(mine, x3));
+      uint32_t pa[4], pb[4];
+      e2m1x4_f16(wa, pa);
+      e2m1x4_f16(wb, pb);
+      mma_f16(d, pa[0], pb[0], pa[1], pb[1], sel(mine, xv[0]), sel(mine, xv[1]));
+      mma_f16(d, pa[2], pb[2], pa[3], pb[3], sel(mine, xv[2]), sel(mine, xv[3]));
     }
-    acc[0] += (dE[0] + dO[0]) + (dE[1] + dO[1]);
-    acc[1] += (dE[2] + dO[2]) + (dE[3] + dO[3]);
+    const uint32_t sA = lds32(sf + 512 * t + 16 * (rA & 31) + 4 * (rA >> 5));
+    const uint32_t sB = lds32(sf + 512 * t + 16 * (rB & 31) + 4 * (rB >> 5));
+    uint32_t hA[2], hB[2];
+    e4m3x4_f16(sA, hA);
+    e4m3x4_f16(sB, hB);
+    const float2 a01 = h2x2f(hA[0]), a23 = h2x2f(hA[1]);
+    const float2 b01 = h2x2f(hB[0]), b23 = h2x2f(hB[1]);
+    acc[0] += fmaf(a01.x, dE[0], fmaf(a01.y, dE[1], fmaf(a23.x, dO[0], a23.y * dO[1])));
+    acc[1] += fmaf(b01.x, dE[2], fmaf(b01.y, dE[3], fmaf(b23.x, dO[2], b23.y * dO[3])));
   }
 };
 
@@ -721,10 +778,13 @@ struct Slab<F_FP8, 1> {
       const uint2 ca = lds64(rA + fp8_v_off(v, rowA & 7)), cb = lds64(rB + fp8_v_off(v, rowB & 7));
       const bool mine = (g == j);
       float* d = (j & 1) ? dO : dE;
-      mma_f16(d, e4m3x2_f16(ca.x), e4m3x2_f16(cb.x), e4m3x2_f16(ca.x >> 16), e4m3x2_f16(cb.x >> 16),
-              sel(mine, x0), sel(mine, x1));
-      mma_f16(d, e4m3x2_f16(ca.y), e4m3x2_f16(cb.y), e4m3x2_f16(ca.y >> 16), e4m3x2_f16(cb.y >> 16),
-              sel(mine, x2), sel(mine, x3));
+      uint32_t a0[2], b0[2], a1[2], b1[2];
+      e4m3x4_f16(ca.x, a0);
+      e4m3x4_f16(cb.x, b0);
+      e4m3x4_f16(ca.y, a1);
+      e4m3x4_f16(cb.y, b1);
+      mma_f16(d, a0[0], b0[0], a0[1], b0[1], sel(mine, x0), sel(mine, x1));
+      mma_f16(d, a1[0], b1[0], a1[1], b1[1], sel(mine, x2), sel(mine, x3));
     }
     acc[0] += (dE[0] + dO[0]) + (dE[1] + dO[1]);
     acc[1] += (dE[2] + dO[2]) + (dE[3] + dO[3]);
@@ -747,10 +807,13 @@ struct Slab<F_FP8, 8> {
       const uint2 ca = lds64(rA + fp8_v_off(v, rowA & 7)), cb = lds64(rB + fp8_v_off(v, rowB & 7));
       const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
       float* d = (j & 1) ? dO : acc;
-      mma_f16(d, e4m3x2_f16(ca.x), e4m3x2_f16(cb.x), e4m3x2_f16(ca.x >> 16), e4m3x2_f16(cb.x >> 16),
-              bf16x2_to_f16x2(xv.x), bf16x2_to_f16x2(xv.y));
-      mma_f16(d, e4m3x2_f16(ca.y), e4m3x2_f16(cb.y), e4m3x2_f16(ca.y >> 16), e4m3x2_f16(cb.y >> 16),
-              bf16x2_to_f16x2(xv.z), bf16x2_to_f16x2(xv.w));
+      uint32_t a0[2], b0[2], a1[2], b1[2];
+      e4m3x4_f16(ca.x, a0);
+      e4m3x4_f16(cb.x, b0);
+      e4m3x4_f16(ca.y, a1);
+      e4m3x4_f16(cb.y, b1);
+      mma_f16(d, a0[0], b0[0], a0[1], b0[1], bf16x2_to_f16x2(xv.x), bf16x2_to_f16x2(xv.y));
+      mma_f16(d, a1[0], b1[0], a1[1], b1[1], bf16x2_to_f16x2(xv.z), bf16x2_to_f16x2(xv.w));
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] += dO[e];
