@@ -20,7 +20,7 @@ QMV_Q8_0, QMV_Q4_K, QMV_Q6_K, QMV_NVFP4, QMV_FP8_ROW, QMV_Q5_K = 1, 2, 3, 4, 5, 
 FORMATS = {"q8_0": QMV_Q8_0, "q4_k": QMV_Q4_K, "q6_k": QMV_Q6_K, "nvfp4": QMV_NVFP4,
            "fp8_row": QMV_FP8_ROW, "q5_k": QMV_Q5_K}
 QMV_ENTRY_GEMV, QMV_ENTRY_GROUPED, QMV_ENTRY_W4A4, QMV_ENTRY_SWIGLU = 1, 2, 3, 4
-QMV_ENTRY_GROUPED_SWIGLU = 5
+QMV_ENTRY_GROUPED_SWIGLU, QMV_ENTRY_KQUANT = 5, 6
 QMV_MAX_M = 8
 
 STATUS = {0: "QMV_OK", 1: "QMV_EINVAL", 2: "QMV_EALIGN", 3: "QMV_EUNSUPPORTED", 4: "QMV_ECUDA",
@@ -65,6 +65,7 @@ _grouped = _sig("qmv_grouped", _I, [_I, _P, _P, _P, _I, _P, _I, _I, _I64, _I64, 
 _grouped_swiglu = _sig("qmv_grouped_swiglu", _I, [_I, _P, _P, _P, _P, _I, _I, _I64, _I64, _I64, _P, _SZ, _P])
 _quant_act = _sig("qmv_quant_act_nvfp4", _I, [_P, _F, _P, _P, _I, _I64, _P])
 _w4a4 = _sig("qmv_gemm_nvfp4_w4a4", _I, [_P, _P, _F, _P, _I, _I64, _I64, _P, _SZ, _P])
+_kquant = _sig("qmv_gemm_kquant", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
 _status_str = _sig("qmv_status_str", ctypes.c_char_p, [_I])
 _last_route = _sig("qmv_last_route", _I, [])
 _dev_status = _sig("qmv_device_status", _I, [_I])
@@ -72,7 +73,7 @@ _dev_status = _sig("qmv_device_status", _I, [_I])
 EXPORTED = ["qmv_canon_size", "qmv_pack_size", "qmv_pack", "qmv_quantize", "qmv_dequant",
             "qmv_workspace_size", "qmv_gemv", "qmv_grouped", "qmv_quant_act_nvfp4",
             "qmv_gemm_nvfp4_w4a4", "qmv_status_str", "qmv_last_route", "qmv_device_status",
-            "qmv_gemv_noalloc", "qmv_gemv_swiglu", "qmv_grouped_swiglu"]
+            "qmv_gemv_noalloc", "qmv_gemv_swiglu", "qmv_grouped_swiglu", "qmv_gemm_kquant"]
 
 
 def _fmt(fmt) -> int:
@@ -273,4 +274,17 @@ def qmv_gemm_nvfp4_w4a4(packed_W: torch.Tensor, x: torch.Tensor, x_scale: float,
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
     _check(_w4a4(_ptr(packed_W), _ptr(x), float(x_scale), _ptr(y), M, N, K, _ptr(ws), ws.numel(),
                  _stream(stream)), "qmv_gemm_nvfp4_w4a4")
+    return y
+
+
+def qmv_gemm_kquant(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int, ws: torch.Tensor,
+                    y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = x . W^T for a K-quant W at prefill sizes (tensor cores, each weight read once)."""
+    _dev(packed_W, "packed_W"); _dev(x, "x"); _dev(ws, "ws")
+    x = _bits16(x)
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(_kquant(_fmt(fmt), _ptr(packed_W), _ptr(x), _ptr(y), M, N, K, _ptr(ws), ws.numel(), _stream(stream)),
+           "qmv_gemm_kquant")
     return y

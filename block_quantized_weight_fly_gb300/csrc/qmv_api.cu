@@ -110,6 +110,10 @@ size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, i
     if (M > QMV_MAX_M) return 0;
     return (size_t)ws_plan_stream(M, 0, 2 * sms, 2).total;
   }
+  if (entry == QMV_ENTRY_KQUANT) {
+    if (fmt != QMV_Q4_K || K % 256) return 0;
+    return (size_t)kq_workspace_bytes(align_up(M, 128), K, sms);
+  }
   if (entry == QMV_ENTRY_W4A4) {
     // the activation's NVFP4 tiles (per 256-value k-group, m_pad rows x (128 B codes +
     // 16 B scales)), then the split-K partial sums
@@ -242,6 +246,26 @@ qmv_status qmv_grouped_swiglu(qmv_fmt fmt, const void* tower, const int32_t* exp
   int variant = 0;
   qmv_status st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
+  return st;
+}
+
+qmv_status qmv_gemm_kquant(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y, int M, int64_t N,
+                           int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !packed_W || !x || !y || !ws || M < 1 || N <= 0 || K <= 0) return QMV_EINVAL;
+  if (fmt != QMV_Q4_K) return QMV_EUNSUPPORTED;
+  Layout L;
+  if (!make_layout(QMV_Q4_K, N, K, 1, &L)) return QMV_EUNSUPPORTED;
+  if (!aligned(packed_W, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return QMV_ECUDA;
+  const int64_t m_pad = align_up(M, 128);
+  if (L.row_tiles * (m_pad / 128) * L.k_groups * (int64_t)sms >= ((int64_t)1 << 31)) return QMV_EUNSUPPORTED;
+  if (ws_bytes < (size_t)kq_workspace_bytes(m_pad, K, sms)) return QMV_EWORKSPACE;
+  unsigned* status = status_ptr();
+  if (!status) return QMV_ECUDA;
+  qmv_status st = from_cuda(launch_kq(L, static_cast<const uint8_t*>(packed_W), x, y, M,
+                                      static_cast<uint8_t*>(ws), status, stream));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + 11;
   return st;
 }
 

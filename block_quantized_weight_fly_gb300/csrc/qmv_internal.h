@@ -60,6 +60,11 @@ cudaError_t launch_w4a4(const Layout& L, const uint8_t* packed, const uint8_t* a
                         float x_scale, float* y, int M, int64_t m_pad, unsigned* status, cudaStream_t s);
 // bytes of the W4A4 split-K region (partial-sum slots, then flags) for a device of `sms` SMs
 int64_t w4a4_partials_bytes(int sms);
+// K-quant (Q4_K) prefill GEMM (tcgen05, f16 operands): the x pre-pass, then the GEMM.
+// ws: [x tiles: m_pad*K*2][sum tiles: m_tiles*(K/256)*4096][partial tiles: sms*64 KB][flags]
+cudaError_t launch_kq(const Layout& L, const uint8_t* packed, const uint16_t* x, float* y, int M, uint8_t* ws,
+                      unsigned* status, cudaStream_t s);
+int64_t kq_workspace_bytes(int64_t m_pad, int64_t K, int sms);
 // returns the route variant launched (1 = M=1, 2 = M>1, 3 = grouped, 9 = fused gate|up SwiGLU)
 cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant);
 

@@ -1,0 +1,107 @@
+"""GPU parity of the K-quant (Q4_K) prefill GEMM on the tensor cores (tcgen05 kind::f16).
+
+Expected values come from the CPU oracle only: BlockToFloat of the Q4_K weights and
+fp64 dots with the bf16 activations -- the same definition the GEMV meets. The bound
+is the GEMV's: |y - y_ref| <= 1e-5 sum_k |w x| per output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from cases import TOL, device_matrix, host_dequant, host_matrix, host_rows_dequant, norm_err, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q():
+    import block_quantized_weight_fly_gb300 as q
+    torch.cuda.set_device(0)
+    q.qmv_device_status(reset=True)
+    return q
+
+
+def flags_view(q, ws, M, K):
+    """The per-SM publication flags at the end of the workspace."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    m_pad = -(-M // 128) * 128
+    off = m_pad * K * 2 + (m_pad // 128) * (K // 256) * 4096 + sms * 128 * 128 * 4
+    return ws[off:off + 4 * sms]
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (1, 128, 256), (129, 200, 512), (300, 384, 1024),
+                                   (257, 1000, 2048), (512, 640, 4096)])
+def test_kquant_parity(q, M, N, K):
+    W, canon = host_matrix("q4_k", 51, N, K)
+    D = host_dequant("q4_k", canon, N, K)
+    x = synth.activations(53 + M, M, K)
+    ref, den = oracle.gemv_f64(D, synth.bf16_bits(x))
+    packed = q.qmv_pack("q4_k", torch.from_numpy(canon).cuda(), N, K)
+    ws = q.workspace(q.QMV_ENTRY_KQUANT, "q4_k", M, N, K)
+    y = q.qmv_gemm_kquant("q4_k", packed, x.cuda(), N, K, ws)
+    assert q.qmv_last_route() == q.FORMATS["q4_k"] * 100 + 11
+    y = y.cpu().numpy()
+    assert q.qmv_device_status() == 0
+    assert norm_err(y, ref, den) <= TOL
+    assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 2048), (384, 130, 4096)])
+def test_kquant_split_k_deterministic(q, M, N, K):
+    """Few tiles over many CTAs: every tile is split across CTAs and finished from
+    its peers' partial tiles. Two calls give identical bits, the flags end at zero."""
+    W, canon = host_matrix("q4_k", 57, N, K)
+    D = host_dequant("q4_k", canon, N, K)
+    x = synth.activations(59, M, K)
+    ref, den = oracle.gemv_f64(D, synth.bf16_bits(x))
+    packed = q.qmv_pack("q4_k", torch.from_numpy(canon).cuda(), N, K)
+    ws = q.workspace(q.QMV_ENTRY_KQUANT, "q4_k", M, N, K)
+    xd = x.cuda()
+    y1 = q.qmv_gemm_kquant("q4_k", packed, xd, N, K, ws).cpu()
+    y2 = q.qmv_gemm_kquant("q4_k", packed, xd, N, K, ws).cpu()
+    assert q.qmv_device_status() == 0
+    assert torch.equal(y1, y2)
+    assert norm_err(y1.numpy(), ref, den) <= TOL
+    assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
+def test_kquant_full_size_sampled(q, N, K):
+    """The 27B MLP matrices at M = 512 (the prefill configuration), sampled rows."""
+    M, seed = 512, 61
+    packed = device_matrix(q, "q4_k", seed, N, K)
+    rows = sample_rows(N, 24, seed)
+    Dr = host_rows_dequant("q4_k", seed, rows, N, K)
+    x = synth.activations(seed + 1, M, K)
+    ref, den = oracle.gemv_f64(Dr, synth.bf16_bits(x))
+    ws = q.workspace(q.QMV_ENTRY_KQUANT, "q4_k", M, N, K)
+    y = q.qmv_gemm_kquant("q4_k", packed, x.cuda(), N, K, ws)
+    got = y[:, torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert q.qmv_device_status() == 0
+    assert norm_err(got, ref, den) <= TOL
+    assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
+
+
+def test_kquant_errors(q):
+    N, K, M = 256, 512, 130
+    W, canon = host_matrix("q4_k", 63, N, K)
+    packed = q.qmv_pack("q4_k", torch.from_numpy(canon).cuda(), N, K)
+    x = synth.activations(63, M, K).cuda()
+    ws = q.workspace(q.QMV_ENTRY_KQUANT, "q4_k", M, N, K)
+    for fmt in ("q6_k", "q8_0", "nvfp4"):
+        with pytest.raises(q.QmvError) as ei:
+            q.qmv_gemm_kquant(fmt, packed, x, N, K, ws)
+        assert ei.value.status == 3
+    with pytest.raises(q.QmvError) as ei:
+        q.qmv_gemm_kquant("q4_k", packed, x, N, K, ws[:4096])
+    assert ei.value.status == 8
+    assert q.qmv_workspace_size(q.QMV_ENTRY_KQUANT, "q4_k", M, N, 300) == 0
+    # arguments that disagree with the packed header: detected on the device, y untouched
+    y = torch.full((M, N - 128), 3.0, device="cuda")
+    q.qmv_device_status(reset=True)
+    q.qmv_gemm_kquant("q4_k", packed, x, N - 128, K, ws, y=y)
+    assert q.qmv_device_status(reset=True) == 5
+    assert bool((y == 3.0).all())
+    assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
