@@ -86,6 +86,10 @@ WORKLOADS = {
                             mats=[("up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
                             desc="NVFP4 W4A4 prefill, M=512: activation quantized to NVFP4, tcgen05 block-scaled "
                                  "MMA, [17408,5120] + [5120,17408]"),
+    "q4k_prefill_m512": dict(fmt="q4_k", M=512, kquant=True,
+                             mats=[("up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
+                             desc="Q4_K prefill, M=512: tcgen05 kind::f16 GEMM over exactly decoded Q4_K weights, "
+                                  "[17408,5120] + [5120,17408]"),
     "tower_m1": dict(fmt="q4_k", M=1, tower=True, E=288, topk=8,
                      mats=[("gate", 2048, 4096), ("up", 2048, 4096), ("down", 4096, 2048)],
                      desc="grouped Q4_K tower, 288 experts x (gate,up [2048,4096], down [4096,2048]), top-8, M=1"),
@@ -110,7 +114,7 @@ DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, 
                  "fp8_m1": 40000, "fp8_m8": 40000, "q8_0_tiny": 20000, "tower_m1": 20000,
                  "tower_m4": 10000, "tower_m8": 5000, "nvfp4_w4a4_m512": 2000,
                  "q4k_mlp_fused_m1": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000,
-                 "tower_fused_m1": 20000, "tower_fused_m8": 5000}
+                 "tower_fused_m1": 20000, "tower_fused_m8": 5000, "q4k_prefill_m512": 2000}
 
 METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"
 CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q5_k": 176 / 256, "q6_k": 210 / 256,
@@ -134,6 +138,17 @@ def measured_fp4_peak():
             d = json.load(f)
         return float(d.get("bf16_tflops", 1900.0)) * 6.0, "measured bf16 x 6 (nominal fp4/bf16 ratio)"
     return 1900.0 * 6.0, "fallback bf16 x 6 (nominal fp4/bf16 ratio)"
+
+
+def measured_f16_peak():
+    """Dense f16 tensor peak: the measured bf16 GEMM rate (the part's f16 and bf16
+    rates are the same)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d.get("bf16_tflops", 1900.0)), "measured bf16 (= dense f16 rate)"
+    return 1900.0, "fallback bf16 (= dense f16 rate)"
 
 
 def measured_peaks():
@@ -272,6 +287,7 @@ class DeviceWorkload:
         self.fmt, self.M = w["fmt"], w["M"]
         self.tower = w.get("tower", False)
         self.w4a4 = w.get("w4a4", False)
+        self.kquant = w.get("kquant", False)
         self.fused = w.get("fused", False)
         self.E = w.get("E", 1)
         self.topk = w.get("topk", 1)
@@ -299,6 +315,8 @@ class DeviceWorkload:
             ysh = (self.M, self.topk, N) if self.tower else (self.M, N)
             self.y.append(torch.empty(ysh, dtype=torch.float32, device=dev))
             entry = q.QMV_ENTRY_GROUPED if self.tower else (q.QMV_ENTRY_W4A4 if self.w4a4 else q.QMV_ENTRY_GEMV)
+            if self.kquant:
+                entry = q.QMV_ENTRY_KQUANT
             if self.fused and i == 0:
                 entry = q.QMV_ENTRY_GROUPED_SWIGLU if self.tower else q.QMV_ENTRY_SWIGLU
             self.ws.append(q.workspace(entry, self.fmt, self.M, N, K, self.E, self.topk, device=dev))
@@ -313,7 +331,7 @@ class DeviceWorkload:
                 self.ids.append(torch.from_numpy(ids).to(dev))
                 self.unique.append(len(np.unique(ids)))
         # W4A4 runs the activation quantizer and the GEMM per matrix
-        self.launches_per_step = len(self.mats) * (2 if self.w4a4 else 1)
+        self.launches_per_step = len(self.mats) * (2 if (self.w4a4 or self.kquant) else 1)
 
     def step_flops(self):
         return sum(2.0 * self.M * N * K for _, N, K in self.mats)
@@ -344,6 +362,8 @@ class DeviceWorkload:
                               self.ws[i], x_per_pair=(i == len(self.mats) - 1), y=self.y[i])
             elif self.fused and i == 0:
                 q.qmv_gemv_swiglu(self.fmt, self.packed[c][i], self.x[i], N, K, self.ws[i], h=self.y[i])
+            elif self.kquant:
+                q.qmv_gemm_kquant(self.fmt, self.packed[c][i], self.x[i], N, K, self.ws[i], y=self.y[i])
             elif self.w4a4:
                 q.qmv_gemm_nvfp4_w4a4(self.packed[c][i], self.x[i], self.x_scale[i], N, K, self.ws[i], y=self.y[i])
             else:
@@ -428,14 +448,14 @@ def run_device(args, rank, world, dev):
     achieved = (bytes_per_step / wl.launches_per_step) / avg_launch_s / 1e9
     peak, peak_kind = measured_peaks()
     traffic = recorded_traffic(args.workload)
-    if wl.w4a4:
+    if wl.w4a4 or wl.kquant:
         # a dense contraction: TFLOP/s against the tensor roofline; each matrix's
         # time includes its activation quantizer (the GEMM's share is in profiles/)
         flops = wl.step_flops()
         value = whole_job_rate(flops, K, world, ms_max) / 1e12
         gemm_s = (ms * 1e-3) / (K * len(wl.mats))
         achieved = (flops / len(wl.mats)) / gemm_s / 1e12
-        peak, peak_kind = measured_fp4_peak()
+        peak, peak_kind = measured_fp4_peak() if wl.w4a4 else measured_f16_peak()
 
     # ---- end to end through the public API, host buffers -------------------
     e2e_steps = min(K, 2000)
@@ -525,6 +545,23 @@ def run_device(args, rank, world, dev):
         del result["roofline"]["algorithmic_bytes_per_launch"]
         result["e2e"]["unit"] = "TFLOP/s"
         result["e2e"]["value"] = round(wl.step_flops() * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, 2)
+    if wl.kquant:
+        result["metric"] = "Q4_K prefill GEMM throughput (M=512)"
+        result["unit"] = "TFLOP/s"
+        result["dtype"] = "f16 (exactly decoded Q4_K sc*q x f16 x, fp32 accumulation)"
+        result["config"]["arithmetic"] = ("tcgen05.mma kind::f16, per-superblock TMEM accumulators folded with "
+                                          "d and dmin in fp32")
+        result["config"]["flops_per_step"] = wl.step_flops()
+        del result["pct_of_nominal_8000"]
+        result["pct_of_peak"] = round(100.0 * value / world / peak, 2)
+        result["roofline"].update({
+            "bound": "tensor", "kernel": "qmv::kq_kernel (+ its x pre-pass)", "unit": "TFLOP/s",
+            "achieved": round(achieved, 2), "peak": round(peak, 1), "frac": round(achieved / peak, 4),
+            "avg_launch_us": round(gemm_s * 1e6, 3),
+            "algorithmic_flops_per_launch": wl.step_flops() / len(wl.mats)})
+        del result["roofline"]["algorithmic_bytes_per_launch"]
+        result["e2e"]["unit"] = "TFLOP/s"
+        result["e2e"]["value"] = round(wl.step_flops() * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, 2)
     if wl.tower:
         result["config"]["unique_experts_mean"] = round(float(np.mean(wl.unique)), 2)
     return result
@@ -549,29 +586,52 @@ def oracle_sample(workload, rows_per_mat):
     return items
 
 
+def tensor_workload(workload):
+    w = WORKLOADS[workload]
+    return bool(w.get("w4a4") or w.get("kquant"))
+
+
+def metric_of(workload):
+    """(metric, unit) of the workload's JSON line (both arms)."""
+    w = WORKLOADS[workload]
+    if w.get("w4a4"):
+        return "NVFP4 W4A4 prefill throughput (M=512)", "TFLOP/s"
+    if w.get("kquant"):
+        return "Q4_K prefill GEMM throughput (M=512)", "TFLOP/s"
+    return METRIC, "GB/s"
+
+
 def time_oracle(items, min_seconds):
+    """Runs the oracle over the sample until min_seconds have passed: (bytes, flops,
+    seconds, passes)."""
     import oracle
-    done_bytes, reps = 0, 0
+    done_bytes, done_flops, reps = 0, 0, 0
     t0 = time.perf_counter()
     while True:
         for fmt, canon, r, K, x in items:
             D = oracle.block_to_float(fmt, canon, r, K)
             oracle.gemv_f64(D, x)
             done_bytes += canon.size + x.size * 2 + r * x.shape[0] * 4
+            done_flops += 2 * r * K * x.shape[0]
         reps += 1
         if time.perf_counter() - t0 >= min_seconds:
             break
-    return done_bytes, time.perf_counter() - t0, reps
+    return done_bytes, done_flops, time.perf_counter() - t0, reps
 
 
 def cpu_baseline(workload, seconds=10.0):
     w = WORKLOADS[workload]
     # about the same canonical bytes from each matrix (~4.4 MB each for the MLP)
     rows = [max(1, int(4.4e6 / canon_bytes(w["fmt"], 1, K))) for _, _, K in w["mats"]]
+    if tensor_workload(workload):
+        # M = 512 rows of x: fewer weight rows for the same CPU time
+        rows = [max(1, r // 64) for r in rows]
     items = oracle_sample(workload, rows)
-    nbytes, secs, reps = time_oracle(items, seconds)
+    nbytes, nflops, secs, reps = time_oracle(items, seconds)
     sample = ", ".join(f"{n}: first {r} rows" for (n, _, _), r in zip(w["mats"], rows))
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    _, unit = metric_of(workload)
+    value = nflops / secs / 1e12 if unit == "TFLOP/s" else nbytes / secs / 1e9
+    return {"value": round(value, 6), "unit": unit, "cores": 1, "kind": "oracle",
             "sample": f"{sample} (BlockToFloat + fp64 dot, {reps} passes, {secs:.1f} s)"}
 
 
@@ -581,7 +641,7 @@ def run_reference(args):
     K, W = args.steps, args.warmup
     budget = 150.0                                 # seconds for the whole run
     probe = oracle_sample(args.workload, [16] * len(w["mats"]))
-    nb, secs, _ = time_oracle(probe, 0.0)
+    nb, nf, secs, _ = time_oracle(probe, 0.0)
     per_row_s = secs / (16 * len(w["mats"]))
     rows = max(1, int(budget / max(K + W, 1) / max(per_row_s * len(w["mats"]), 1e-9)))
     items = oracle_sample(args.workload, [rows] * len(w["mats"]))
@@ -589,23 +649,25 @@ def run_reference(args):
     for _ in range(W):
         for fmt, canon, r, K_, x in items:
             oracle.gemv_f64(oracle.block_to_float(fmt, canon, r, K_), x)
-    nbytes = 0
+    nbytes, nflops = 0, 0
     t0 = time.perf_counter()
     for _ in range(K):
         for fmt, canon, r, K_, x in items:
             oracle.gemv_f64(oracle.block_to_float(fmt, canon, r, K_), x)
             nbytes += canon.size + x.size * 2 + r * x.shape[0] * 4
+            nflops += 2 * r * K_ * x.shape[0]
     secs = time.perf_counter() - t0
-    value = nbytes / secs / 1e9
+    metric, unit = metric_of(args.workload)
+    value = nflops / secs / 1e12 if unit == "TFLOP/s" else nbytes / secs / 1e9
     sample = f"first {rows} rows of each of {', '.join(n for n, _, _ in w['mats'])} per step"
     return {
-        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": K, "warmup": W,
+        "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": args.gpus, "steps": K, "warmup": W,
         "ms_per_step": round(secs * 1e3 / max(K, 1), 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w["desc"], "workload_id": args.workload, "weights": w["fmt"], "M": w["M"]},
         "impl": "reference",
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
