@@ -90,6 +90,10 @@ WORKLOADS = {
                              mats=[("up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
                              desc="Q4_K prefill, M=512: tcgen05 kind::f16 GEMM over exactly decoded Q4_K weights, "
                                   "[17408,5120] + [5120,17408]"),
+    "q5k_prefill_m512": dict(fmt="q5_k", M=512, kquant=True,
+                             mats=[("up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
+                             desc="Q5_K prefill, M=512: tcgen05 kind::f16 GEMM over exactly decoded Q5_K weights, "
+                                  "[17408,5120] + [5120,17408]"),
     "tower_m1": dict(fmt="q4_k", M=1, tower=True, E=288, topk=8,
                      mats=[("gate", 2048, 4096), ("up", 2048, 4096), ("down", 4096, 2048)],
                      desc="grouped Q4_K tower, 288 experts x (gate,up [2048,4096], down [4096,2048]), top-8, M=1"),
@@ -114,7 +118,8 @@ DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, 
                  "fp8_m1": 40000, "fp8_m8": 40000, "q8_0_tiny": 20000, "tower_m1": 20000,
                  "tower_m4": 10000, "tower_m8": 5000, "nvfp4_w4a4_m512": 2000,
                  "q4k_mlp_fused_m1": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000,
-                 "tower_fused_m1": 20000, "tower_fused_m8": 5000, "q4k_prefill_m512": 2000}
+                 "tower_fused_m1": 20000, "tower_fused_m8": 5000, "q4k_prefill_m512": 2000,
+                 "q5k_prefill_m512": 2000}
 
 METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"
 CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q5_k": 176 / 256, "q6_k": 210 / 256,
@@ -546,9 +551,9 @@ def run_device(args, rank, world, dev):
         result["e2e"]["unit"] = "TFLOP/s"
         result["e2e"]["value"] = round(wl.step_flops() * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, 2)
     if wl.kquant:
-        result["metric"] = "Q4_K prefill GEMM throughput (M=512)"
+        result["metric"] = f"{wl.fmt.upper()} prefill GEMM throughput (M=512)"
         result["unit"] = "TFLOP/s"
-        result["dtype"] = "f16 (exactly decoded Q4_K sc*q x f16 x, fp32 accumulation)"
+        result["dtype"] = f"f16 (exactly decoded {wl.fmt.upper()} sc*q x f16 x, fp32 accumulation)"
         result["config"]["arithmetic"] = ("tcgen05.mma kind::f16, per-superblock TMEM accumulators folded with "
                                           "d and dmin in fp32")
         result["config"]["flops_per_step"] = wl.step_flops()
@@ -597,7 +602,7 @@ def metric_of(workload):
     if w.get("w4a4"):
         return "NVFP4 W4A4 prefill throughput (M=512)", "TFLOP/s"
     if w.get("kquant"):
-        return "Q4_K prefill GEMM throughput (M=512)", "TFLOP/s"
+        return f"{w['fmt'].upper()} prefill GEMM throughput (M=512)", "TFLOP/s"
     return METRIC, "GB/s"
 
 

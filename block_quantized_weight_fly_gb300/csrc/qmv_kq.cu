@@ -154,6 +154,40 @@ __device__ __forceinline__ void tld16(uint32_t* r, uint32_t taddr) {
 __device__ __forceinline__ void tld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// 32-bit word w of a packed record (byte offset o, a compile-time constant after unrolling)
+template <int NV>
+__device__ __forceinline__ uint32_t rec_word(const uint4 (&cur)[NV], int o) {
+  const uint4 cv = cur[o >> 4];
+  const int e = (o & 15) >> 2;
+  return e == 0 ? cv.x : e == 1 ? cv.y : e == 2 ? cv.z : cv.w;
+}
+
+// The eight values (elements 8t..8t+7 of sub-block j) of one packed word as sc_j q 2^-14
+// in f16 pairs: each pair masked into f16's subnormal range (q 2^-24, or q 2^-20 for a
+// Q4_K high nibble) and multiplied by sc_j 2^10 (2^6), exact.
+template <int FMT, int NV>
+__device__ __forceinline__ uint4 kq_decode_word(const uint4 (&cur)[NV], int t, int j, uint32_t S, uint32_t S16) {
+  uint4 out;
+  if constexpr (FMT == F_Q4_K) {
+    // nibbles (p, p+4) = elements (8t+2p, 8t+2p+1)
+    const uint32_t w = rec_word(cur, 16 + 32 * t + 4 * j), w8 = w >> 8;
+    out.x = hmul2(w & 0x000F000Fu, S);
+    out.y = hmul2(w & 0x00F000F0u, S16);
+    out.z = hmul2(w8 & 0x000F000Fu, S);
+    out.w = hmul2(w8 & 0x00F000F0u, S16);
+  } else {
+    // Q5_K: pairs p = 0..2 as 5-bit fields at bits (5p, 16+5p); the last pair's low
+    // nibbles in the sub-block's nibble word (nibbles t, t+4), fifth bits at 15, 31
+    (void)S16;
+    const uint32_t v = rec_word(cur, 16 + 32 * t + 4 * j), u = rec_word(cur, 144 + 4 * j);
+    out.x = hmul2(v & 0x001F001Fu, S);
+    out.y = hmul2((v >> 5) & 0x001F001Fu, S);
+    out.z = hmul2((v >> 10) & 0x001F001Fu, S);
+    out.w = hmul2(((u >> (4 * t)) & 0x000F000Fu) | ((v >> 11) & 0x00100010u), S);
+  }
+  return out;
+}
+
 struct KqParams {
   Layout L;
   const uint8_t* packed;
@@ -173,7 +207,10 @@ __device__ __forceinline__ int range_start(int i, int units, int P) {
   return i * q + (i * r) / P;
 }
 
+template <int FMT>
 __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
+  constexpr int kRec = (FMT == F_Q5_K) ? 176 : 144;     // record bytes per row and superblock
+  constexpr int kRecV = kRec / 16;
   extern __shared__ __align__(1024) uint8_t smem[];
   const Layout& L = p.L;
   uint64_t* x_full = reinterpret_cast<uint64_t*>(smem);
@@ -199,7 +236,7 @@ __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
 
   if (threadIdx.x == 0) {
     const PackedHeader* h = reinterpret_cast<const PackedHeader*>(p.packed);
-    const bool bad = !(h->magic == kMagic && h->version == kVersion && h->fmt == (uint32_t)F_Q4_K &&
+    const bool bad = !(h->magic == kMagic && h->version == kVersion && h->fmt == (uint32_t)FMT &&
                        h->N == L.N && h->K == L.K && h->E == 1 && h->expert_bytes == L.expert_bytes);
     if (bad) atomicOr(p.status, kStatHeader);
     *abort_flag = bad ? 1 : 0;
@@ -318,20 +355,20 @@ __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
   } else if (warp < 6) {
     // ------------------------------ decoders --------------------------------
     const int r = threadIdx.x - 64;                         // weight row of the tile
-    uint4 nxt[9];
+    uint4 nxt[kRecV];
     auto load_rec = [&](int u) {
       const int kb = u % KB, nt = (u / KB) / p.m_tiles;
-      const uint8_t* rec = p.packed + kHeaderBytes + (int64_t)kb * L.group_bytes + ((int64_t)nt * 128 + r) * 144;
+      const uint8_t* rec = p.packed + kHeaderBytes + (int64_t)kb * L.group_bytes + ((int64_t)nt * 128 + r) * kRec;
 #pragma unroll
-      for (int v = 0; v < 9; ++v) nxt[v] = ldg_nc(rec + 16 * v);
+      for (int v = 0; v < kRecV; ++v) nxt[v] = ldg_nc(rec + 16 * v);
     };
     if (n > 0 && !bad_header) load_rec(u0);
     int as = 0, ss = 0, ai = 0;
     uint32_t aph = 0, sph = 0;
     for (int i = 0; i < n && !bad_header; ++i) {
-      uint4 cur[9];
+      uint4 cur[kRecV];
 #pragma unroll
-      for (int v = 0; v < 9; ++v) cur[v] = nxt[v];
+      for (int v = 0; v < kRecV; ++v) cur[v] = nxt[v];
       if (i + 1 < n) load_rec(u0 + i + 1);
       const uint32_t hw[4] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w};
       const float d = h2f(hw[0]), dmin = h2f(hw[0] >> 16);
@@ -376,19 +413,8 @@ __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
           const float sc = (float)q4k_field(hw[1], hw[2], hw[3], j);
           const uint32_t S = f16x2_dup(sc * 1024.0f), S16 = f16x2_dup(sc * 64.0f);
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int o = 16 + 32 * t + 4 * j;                    // word t of sub-block j: elements 8t..8t+7
-            const uint4 cv = cur[o >> 4];
-            const int e = (o & 15) >> 2;
-            const uint32_t w = e == 0 ? cv.x : e == 1 ? cv.y : e == 2 ? cv.z : cv.w;
-            const uint32_t w8 = w >> 8;
-            uint4 out;
-            out.x = hmul2(w & 0x000F000Fu, S);                    // elements 8t, 8t+1
-            out.y = hmul2(w & 0x00F000F0u, S16);                  // 8t+2, 8t+3
-            out.z = hmul2(w8 & 0x000F000Fu, S);                   // 8t+4, 8t+5
-            out.w = hmul2(w8 & 0x00F000F0u, S16);                 // 8t+6, 8t+7
-            *reinterpret_cast<uint4*>(at + (4 * jj + t) * 128) = out;
-          }
+          for (int t = 0; t < 4; ++t)                             // word t: elements 8t..8t+7
+            *reinterpret_cast<uint4*>(at + (4 * jj + t) * 128) = kq_decode_word<FMT>(cur, t, j, S, S16);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -593,7 +619,9 @@ cudaError_t launch_kq(const Layout& L, const uint8_t* packed, const uint16_t* x,
   static int opted[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!opted[dev]) {
-    err = cudaFuncSetAttribute(kq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKqSmem);
+    err = cudaFuncSetAttribute(kq_kernel<F_Q4_K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKqSmem);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kq_kernel<F_Q5_K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKqSmem);
     if (err != cudaSuccess) return err;
     opted[dev] = 1;
   }
@@ -611,7 +639,7 @@ cudaError_t launch_kq(const Layout& L, const uint8_t* packed, const uint16_t* x,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, kq_kernel, p);
+  err = (L.fmt == F_Q5_K) ? cudaLaunchKernelEx(&cfg, kq_kernel<F_Q5_K>, p) : cudaLaunchKernelEx(&cfg, kq_kernel<F_Q4_K>, p);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

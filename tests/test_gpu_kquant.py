@@ -31,53 +31,54 @@ def flags_view(q, ws, M, K):
     return ws[off:off + 4 * sms]
 
 
+@pytest.mark.parametrize("fmt", ["q4_k", "q5_k"])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (1, 128, 256), (129, 200, 512), (300, 384, 1024),
                                    (257, 1000, 2048), (512, 640, 4096)])
-def test_kquant_parity(q, M, N, K):
-    W, canon = host_matrix("q4_k", 51, N, K)
-    D = host_dequant("q4_k", canon, N, K)
+def test_kquant_parity(q, fmt, M, N, K):
+    W, canon = host_matrix(fmt, 51, N, K)
+    D = host_dequant(fmt, canon, N, K)
     x = synth.activations(53 + M, M, K)
     ref, den = oracle.gemv_f64(D, synth.bf16_bits(x))
-    packed = q.qmv_pack("q4_k", torch.from_numpy(canon).cuda(), N, K)
-    ws = q.workspace(q.QMV_ENTRY_KQUANT, "q4_k", M, N, K)
-    y = q.qmv_gemm_kquant("q4_k", packed, x.cuda(), N, K, ws)
-    assert q.qmv_last_route() == q.FORMATS["q4_k"] * 100 + 11
+    packed = q.qmv_pack(fmt, torch.from_numpy(canon).cuda(), N, K)
+    ws = q.workspace(q.QMV_ENTRY_KQUANT, fmt, M, N, K)
+    y = q.qmv_gemm_kquant(fmt, packed, x.cuda(), N, K, ws)
+    assert q.qmv_last_route() == q.FORMATS[fmt] * 100 + 11
     y = y.cpu().numpy()
     assert q.qmv_device_status() == 0
     assert norm_err(y, ref, den) <= TOL
     assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 2048), (384, 130, 4096)])
-def test_kquant_split_k_deterministic(q, M, N, K):
+@pytest.mark.parametrize("fmt,M,N,K", [("q4_k", 256, 256, 2048), ("q4_k", 384, 130, 4096), ("q5_k", 256, 300, 2048)])
+def test_kquant_split_k_deterministic(q, fmt, M, N, K):
     """Few tiles over many CTAs: every tile is split across CTAs and finished from
     its peers' partial tiles. Two calls give identical bits, the flags end at zero."""
-    W, canon = host_matrix("q4_k", 57, N, K)
-    D = host_dequant("q4_k", canon, N, K)
+    W, canon = host_matrix(fmt, 57, N, K)
+    D = host_dequant(fmt, canon, N, K)
     x = synth.activations(59, M, K)
     ref, den = oracle.gemv_f64(D, synth.bf16_bits(x))
-    packed = q.qmv_pack("q4_k", torch.from_numpy(canon).cuda(), N, K)
-    ws = q.workspace(q.QMV_ENTRY_KQUANT, "q4_k", M, N, K)
+    packed = q.qmv_pack(fmt, torch.from_numpy(canon).cuda(), N, K)
+    ws = q.workspace(q.QMV_ENTRY_KQUANT, fmt, M, N, K)
     xd = x.cuda()
-    y1 = q.qmv_gemm_kquant("q4_k", packed, xd, N, K, ws).cpu()
-    y2 = q.qmv_gemm_kquant("q4_k", packed, xd, N, K, ws).cpu()
+    y1 = q.qmv_gemm_kquant(fmt, packed, xd, N, K, ws).cpu()
+    y2 = q.qmv_gemm_kquant(fmt, packed, xd, N, K, ws).cpu()
     assert q.qmv_device_status() == 0
     assert torch.equal(y1, y2)
     assert norm_err(y1.numpy(), ref, den) <= TOL
     assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
 
 
-@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
-def test_kquant_full_size_sampled(q, N, K):
+@pytest.mark.parametrize("fmt,N,K", [("q4_k", 17408, 5120), ("q4_k", 5120, 17408), ("q5_k", 17408, 5120)])
+def test_kquant_full_size_sampled(q, fmt, N, K):
     """The 27B MLP matrices at M = 512 (the prefill configuration), sampled rows."""
     M, seed = 512, 61
-    packed = device_matrix(q, "q4_k", seed, N, K)
+    packed = device_matrix(q, fmt, seed, N, K)
     rows = sample_rows(N, 24, seed)
-    Dr = host_rows_dequant("q4_k", seed, rows, N, K)
+    Dr = host_rows_dequant(fmt, seed, rows, N, K)
     x = synth.activations(seed + 1, M, K)
     ref, den = oracle.gemv_f64(Dr, synth.bf16_bits(x))
-    ws = q.workspace(q.QMV_ENTRY_KQUANT, "q4_k", M, N, K)
-    y = q.qmv_gemm_kquant("q4_k", packed, x.cuda(), N, K, ws)
+    ws = q.workspace(q.QMV_ENTRY_KQUANT, fmt, M, N, K)
+    y = q.qmv_gemm_kquant(fmt, packed, x.cuda(), N, K, ws)
     got = y[:, torch.from_numpy(rows).cuda()].cpu().numpy()
     assert q.qmv_device_status() == 0
     assert norm_err(got, ref, den) <= TOL
@@ -90,7 +91,7 @@ def test_kquant_errors(q):
     packed = q.qmv_pack("q4_k", torch.from_numpy(canon).cuda(), N, K)
     x = synth.activations(63, M, K).cuda()
     ws = q.workspace(q.QMV_ENTRY_KQUANT, "q4_k", M, N, K)
-    for fmt in ("q6_k", "q8_0", "nvfp4"):
+    for fmt in ("q6_k", "q8_0", "nvfp4", "fp8_row"):
         with pytest.raises(q.QmvError) as ei:
             q.qmv_gemm_kquant(fmt, packed, x, N, K, ws)
         assert ei.value.status == 3
