@@ -1,4 +1,4 @@
-// qmv_kq.cu -- K-quant (Q4_K) prefill GEMM on the 5th-generation tensor cores:
+// qmv_kq.cu -- K-quant (Q4_K, Q5_K) prefill GEMM on the 5th-generation tensor cores:
 //   y[m][n] = sum_k x[m][k] w[n][k],  w = d sc_j q - dmin m_j  (per 256-value superblock kb
 // of row n and 32-value sub-block j), for M in the hundreds to thousands of tokens, with
 // each weight slab streamed from HBM once per call instead of once per 8 tokens (the
@@ -12,10 +12,10 @@
 //   D2[n][m] = sum_j m_j[n] (xs_hi[m][j] + xs_lo[m][j])      (f16 x f16, fp32 accumulator)
 //   y[m][n] += (d[n] 2^14) D1[n][m] - dmin[n] D2[n][m]       (fp32, per superblock)
 // where xs = the fp32 sum of x over the sub-block, split into two f16 (hi + lo, 2^-22
-// relative). sc_j q <= 63 * 15 = 945 and m_j <= 63 are exact in f16; the decoder makes
-// sc_j q 2^-14 with one mask (the nibble lands in f16's subnormal range: q 2^-24, or
-// q 2^-20 for a high nibble) and one f16 multiply by sc_j 2^10 (2^6), so every product
-// is exact and only the fp32 accumulations round. x is taken in f16 (exact for bf16
+// relative). sc_j q <= 63 * 15 = 945 (Q5_K: 63 * 31 = 1953) and m_j <= 63 are exact in
+// f16; the decoder makes sc_j q 2^-14 with one mask (the field lands in f16's subnormal
+// range: q 2^-24, or q 2^-20 for a Q4_K high nibble) and one f16 multiply by sc_j 2^10
+// (2^6), so every product is exact and only the fp32 accumulations round. x is taken in f16 (exact for bf16
 // values of magnitude 2^-14 .. 65504; smaller ones keep an absolute error below 2^-25).
 //
 // Work: output tiles of 128 weight rows x 128 tokens, each a sum over K's superblocks;
@@ -30,7 +30,7 @@
 //  * warp 0, one lane: after the grid-dependency wait (the activation tiles come from
 //    the pre-pass launched just before), bulk-copies per superblock the x sub-block-sum
 //    tile (4 KB) and the four 64-value K steps of the x tile (16 KB each) into rings;
-//  * warps 2..5, one thread per weight row: load the row's 144-byte Q4_K record of the
+//  * warps 2..5, one thread per weight row: load the row's 144-byte Q4_K (176-byte Q5_K) record of the
 //    superblock from global memory (the next unit's is loaded while the current one is
 //    decoded), write the mins tile row (m_j as f16, twice) and (d 2^14, dmin), then
 //    decode each K step into the decoded-weight ring (K-major core matrices);
