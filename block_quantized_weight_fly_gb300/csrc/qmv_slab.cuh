@@ -201,6 +201,9 @@ __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
 }
 constexpr uint32_t kX67 = 0x61006100u;   // bf16x2 {2^67, 2^67}
 constexpr uint32_t kX63 = 0x5F005F00u;   // bf16x2 {2^63, 2^63}
+constexpr uint32_t kX71 = 0x63006300u;   // bf16x2 {2^71, 2^71}
+constexpr uint32_t kX69 = 0x62006200u;   // bf16x2 {2^69, 2^69}
+constexpr uint32_t kX65 = 0x60006000u;   // bf16x2 {2^65, 2^65}
 // a_j x 2^66 and b_j for sub-blocks 2t, 2t+1 of a record in shared memory
 __device__ __forceinline__ void q4k_pair_scales_lin_rec(const uint8_t* rec, int t, float* a, float* b) {
   const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 4);
@@ -516,6 +519,29 @@ struct Slab<F_Q8_0, 8> {
 // sum w x = a_u (D_lo + 16 D_hi - 2208 X). k-step s of chunk j covers sub-block
 // u = 2j + s; the thread's slots hold elements 16s + 4t .. 16s + 4t + 3 of chunk j.
 // ============================================================================
+// Q6_K through bf16's linear range: the low nibbles of pair p of an ql word sit at
+// nibbles (p, p+4), their 2-bit highs at bits (2k, 2k+16) of the thread's qh word (k = p),
+// so masks alone give exact bf16 values {v, v'} x 2^(s - 133): s = 0, 4 for nibble pairs
+// 0, 1 (pairs 2, 3 after one shift by 8) and s = 0, 2, 4, 6 for the 2-bit pairs. x is
+// scaled per k position to bring every product to (lo + 16 hi) x 2^-66, so the lo and hi
+// MMAs add into sums of one scale: lo gets x 2^67 | 2^63, hi x 2^71 | 2^69 (pairs 0, 1)
+// and x 2^67 | 2^65 (pairs 2, 3). Exact for |x| < 2^56.
+__device__ __forceinline__ void q6k_linear_mma(float* lo, float* hi, uint32_t la, uint32_t lb, uint32_t ha,
+                                               uint32_t hb, int s2, uint2 xv) {
+  if (s2 == 0) {
+    mma_bf16(lo, la & 0x000F000Fu, lb & 0x000F000Fu, la & 0x00F000F0u, lb & 0x00F000F0u, bmul2(xv.x, kX67),
+             bmul2(xv.y, kX63));
+    mma_bf16(hi, ha & 0x00030003u, hb & 0x00030003u, ha & 0x000C000Cu, hb & 0x000C000Cu, bmul2(xv.x, kX71),
+             bmul2(xv.y, kX69));
+  } else {
+    const uint32_t la8 = la >> 8, lb8 = lb >> 8;
+    mma_bf16(lo, la8 & 0x000F000Fu, lb8 & 0x000F000Fu, la8 & 0x00F000F0u, lb8 & 0x00F000F0u, bmul2(xv.x, kX67),
+             bmul2(xv.y, kX63));
+    mma_bf16(hi, ha & 0x00300030u, hb & 0x00300030u, ha & 0x00C000C0u, hb & 0x00C000C0u, bmul2(xv.x, kX67),
+             bmul2(xv.y, kX65));
+  }
+}
+
 template <>
 struct Slab<F_Q6_K, 1> {
   // 16 units (sub-blocks): units 0..7 -> accumulator group 0, 8..15 -> group 1,
@@ -550,11 +576,7 @@ struct Slab<F_Q6_K, 1> {
       for (int s2 = 0; s2 < 2; ++s2) {
         const int u = 2 * j + s2;
         const uint2 xv = ldx64(xs, (u & 7) == g, 32 * u + 8 * t);
-        const uint32_t b0 = xv.x, b1 = xv.y;
-        mma_bf16(lo[grp], nib_pair(la, 2 * s2), nib_pair(lb, 2 * s2), nib_pair(la, 2 * s2 + 1),
-                 nib_pair(lb, 2 * s2 + 1), b0, b1);
-        mma_bf16(hi[grp], bit2_pair(ha, 2 * s2), bit2_pair(hb, 2 * s2), bit2_pair(ha, 2 * s2 + 1),
-                 bit2_pair(hb, 2 * s2 + 1), b0, b1);
+        q6k_linear_mma(lo[grp], hi[grp], la, lb, ha, hb, s2, xv);
       }
     }
     mma_bf16(xx[0], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, x0.x, x0.y);
@@ -573,8 +595,9 @@ struct Slab<F_Q6_K, 1> {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float aa = dA * i8f(scA >> (8 * e)), ab = dB * i8f(scB >> (8 * e));
-        vA = fmaf(aa, fmaf(16.f, hi[q][e], lo[q][e]) - 2208.f * xx[q][e], vA);
-        vB = fmaf(ab, fmaf(16.f, hi[q][2 + e], lo[q][2 + e]) - 2208.f * xx[q][2 + e], vB);
+        // sum (q - 32) x = 2^66 (lo + hi) - 32 sum x
+        vA = fmaf(aa * 7.3786976294838206e19f, lo[q][e] + hi[q][e], fmaf(-32.f * aa, xx[q][e], vA));
+        vB = fmaf(ab * 7.3786976294838206e19f, lo[q][2 + e] + hi[q][2 + e], fmaf(-32.f * ab, xx[q][2 + e], vB));
       }
     }
     acc[0] += vA;
@@ -596,7 +619,7 @@ struct Slab<F_Q6_K, 8> {
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const float a = d * i8f(sw[jj >> 2] >> (8 * (jj & 3)));
-        tbl[rl * kTblStride + 8 * h + jj] = make_float2(a, 2208.0f * a);
+        tbl[rl * kTblStride + 8 * h + jj] = make_float2(a * 7.3786976294838206e19f, 32.0f * a);
       }
     }
     __syncwarp();
@@ -622,19 +645,16 @@ struct Slab<F_Q6_K, 8> {
 #pragma unroll
       for (int s2 = 0; s2 < 2; ++s2) {
         const uint2 xv = has_x ? lds64(xs + 64 * j + 32 * s2 + 8 * t) : make_uint2(0u, 0u);
-        mma_bf16(lo[s2], nib_pair(la, 2 * s2), nib_pair(lb, 2 * s2), nib_pair(la, 2 * s2 + 1),
-                 nib_pair(lb, 2 * s2 + 1), xv.x, xv.y);
-        mma_bf16(hi[s2], bit2_pair(ha, 2 * s2), bit2_pair(hb, 2 * s2), bit2_pair(ha, 2 * s2 + 1),
-                 bit2_pair(hb, 2 * s2 + 1), xv.x, xv.y);
+        q6k_linear_mma(lo[s2], hi[s2], la, lb, ha, hb, s2, xv);
         mma_bf16(xx[s2], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
       }
 #pragma unroll
       for (int s2 = 0; s2 < 2; ++s2) {
         const float2 sA = tbl[g * kTblStride + 2 * j + s2], sB = tbl[(g + 8) * kTblStride + 2 * j + s2];
-        acc[0] = fmaf(sA.x, fmaf(16.f, hi[s2][0], lo[s2][0]), fmaf(-sA.y, xx[s2][0], acc[0]));
-        acc[1] = fmaf(sA.x, fmaf(16.f, hi[s2][1], lo[s2][1]), fmaf(-sA.y, xx[s2][1], acc[1]));
-        acc[2] = fmaf(sB.x, fmaf(16.f, hi[s2][2], lo[s2][2]), fmaf(-sB.y, xx[s2][2], acc[2]));
-        acc[3] = fmaf(sB.x, fmaf(16.f, hi[s2][3], lo[s2][3]), fmaf(-sB.y, xx[s2][3], acc[3]));
+        acc[0] = fmaf(sA.x, lo[s2][0] + hi[s2][0], fmaf(-sA.y, xx[s2][0], acc[0]));
+        acc[1] = fmaf(sA.x, lo[s2][1] + hi[s2][1], fmaf(-sA.y, xx[s2][1], acc[1]));
+        acc[2] = fmaf(sB.x, lo[s2][2] + hi[s2][2], fmaf(-sB.y, xx[s2][2], acc[2]));
+        acc[3] = fmaf(sB.x, lo[s2][3] + hi[s2][3], fmaf(-sB.y, xx[s2][3], acc[3]));
       }
     }
     __syncwarp();
