@@ -30,7 +30,8 @@
  *    bf16 activations are exact in fp32 and accumulate in fp32. NVFP4 and FP8_ROW
  *    take x as f16 (exact for 2^-14 <= |x| <= 65504); the Q4_K decoders scale
  *    x by 2^63 or 2^67 (exact for |x| < 2^61, products normal for
- *    |x| >= 2^-60); the other K-quant paths take bf16 x as it is.
+ *    |x| >= 2^-60), the Q6_K decoders by 2^63 .. 2^71 (exact for |x| < 2^56);
+ *    the other K-quant paths take bf16 x as it is.
  *
  * Canonical byte layouts (the input of qmv_pack and output of qmv_quantize):
  *   Q8_0  34 B per 32 values : fp16 d | 32 x int8 q;           w = d * q
