@@ -159,6 +159,26 @@ def test_q4k_activation_range(q, lo, hi, M):
     assert norm_err(y, ref, den) <= TOL
 
 
+@pytest.mark.parametrize("lo,hi", [(-50, 40), (-60, 0), (0, 52)])
+@pytest.mark.parametrize("M", [1, 3])
+def test_q6k_activation_range(q, lo, hi, M):
+    """The Q6_K decoders scale x by 2^63 .. 2^71: exact products for
+    2^-60 <= |x| < 2^56 (|z| < 8 here, so e <= 52)."""
+    fmt, N, K = "q6_k", 1000, 2048
+    W, canon = host_matrix(fmt, 23, N, K)
+    z = synth.activations(23, M, K).float()
+    rng = np.random.default_rng((lo + 100) * 1000 + hi + 100 + M)
+    e = torch.from_numpy(rng.integers(lo, hi + 1, size=(M, K)).astype(np.float32))
+    x = (z * torch.pow(2.0, e)).to(torch.bfloat16)
+    ref, den = oracle.gemv_f64(host_dequant(fmt, canon, N, K), synth.bf16_bits(x))
+    packed = q.qmv_pack(fmt, torch.from_numpy(canon).cuda(), N, K)
+    ws = q.workspace(q.QMV_ENTRY_GEMV, fmt, M, N, K)
+    y = q.qmv_gemv(fmt, packed, x.cuda(), N, K, ws).cpu().numpy()
+    assert q.qmv_device_status() == 0
+    assert np.isfinite(y).all()
+    assert norm_err(y, ref, den) <= TOL
+
+
 def test_gemv_rows_of_m8_match_m1_within_tolerance(q):
     fmt, N, K = "q6_k", 640, 1024
     W, canon = host_matrix(fmt, 17, N, K)
