@@ -768,8 +768,8 @@ struct Slab<F_NVFP4, 8> {
       nv_frag(CB[j], nv_sbyte(SB, j, t), pb);
       uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
       float* d = (j & 1) ? dO : acc;
-      mma_f16(d, pa[0], pb[0], pa[1], pb[1], bf16x2_to_f16x2(xv.x), bf16x2_to_f16x2(xv.y));
-      mma_f16(d, pa[2], pb[2], pa[3], pb[3], bf16x2_to_f16x2(xv.z), bf16x2_to_f16x2(xv.w));
+      mma_f16(d, pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);     // x already f16 (converted per stage)
+      mma_f16(d, pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] += dO[e];
@@ -832,8 +832,8 @@ struct Slab<F_FP8, 8> {
       e4m3x4_f16(cb.x, b0);
       e4m3x4_f16(ca.y, a1);
       e4m3x4_f16(cb.y, b1);
-      mma_f16(d, a0[0], b0[0], a0[1], b0[1], bf16x2_to_f16x2(xv.x), bf16x2_to_f16x2(xv.y));
-      mma_f16(d, a1[0], b1[0], a1[1], b1[1], bf16x2_to_f16x2(xv.z), bf16x2_to_f16x2(xv.w));
+      mma_f16(d, a0[0], b0[0], a0[1], b0[1], xv.x, xv.y);     // x already f16 (converted per stage)
+      mma_f16(d, a1[0], b1[0], a1[1], b1[1], xv.z, xv.w);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] += dO[e];

@@ -476,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   // After an abort (a wait that timed out, here or in another warp) a warp still
   // walks its slab sequence but skips the waits, the arithmetic and the stores.
   const int w = warp - 1;               // this warp owns rows 16w .. 16w+15 of a slab
+  constexpr bool kConvX = (MT > 1) && (FMT == F_NVFP4 || FMT == F_FP8);
   const int g = lane >> 2, tq = lane & 3;
   float2* tbl = tbls + w * (16 * kTblStride);
   const int rA = 16 * w + g, rB = rA + 8;
@@ -502,19 +503,48 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     const bool full_cover = (s0 <= head) && (s1 >= tail);
     const bool reducer = (s0 <= head);
     for (; s < send; ++s) {
+      bool have = false;
       if (!aborted) {
         if (!mbar_wait(&full[stage], fphase, a.status)) {
           misc[0] = 1;
           aborted = true;
         } else {
+          have = true;
+        }
+      }
+      if constexpr (kConvX) {
+        // the f16-operand formats at M > 1: the eight consumer warps turn the stage's x
+        // rows from bf16 into f16 in place, warp w row w, 16 bytes per lane (zeros past
+        // a ragged K), once for all warps; every warp meets the barrier once per slab,
+        // whether it waited for the slab or not
+        if (have && w < (segs[seg].R < MT ? segs[seg].R : MT)) {
+          uint4* xv = reinterpret_cast<uint4*>(smem + kp.stage_base + stage * kp.stage_bytes + kp.x_off +
+                                               w * kXStride + 16 * lane);
+          const int gk = (s - head) % G;
+          uint4 v = *xv;
+          if (kMayBeRagged && gk == G - 1 && 8 * lane >= kv_last) {
+            v = make_uint4(0u, 0u, 0u, 0u);
+          } else {
+            v.x = bf16x2_to_f16x2(v.x);
+            v.y = bf16x2_to_f16x2(v.y);
+            v.z = bf16x2_to_f16x2(v.z);
+            v.w = bf16x2_to_f16x2(v.w);
+          }
+          *xv = v;
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+      }
+      if (have) {
+        {
           const uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
           const uint8_t* xrow0 = st + kp.x_off;
           const int gk = (s - head) % G;
           float* ap = acc + ((SW && s - head >= G) ? 4 : 0);
           // a last k-group narrower than 256: its padded blocks are zero and the x
           // beyond K is never copied, so the stale tail of each x row is zeroed (by
-          // one thread of each warp, before that warp reads it)
-          if (kMayBeRagged && gk == G - 1 && kv_last < kSlabK) {
+          // one thread of each warp, before that warp reads it; the converted formats
+          // zeroed it above)
+          if (!kConvX && kMayBeRagged && gk == G - 1 && kv_last < kSlabK) {
             if (has_x && tq == 0) {
               uint8_t* xw = const_cast<uint8_t*>(xrow0) + g * kXStride;
               for (int o = kv_last * 2; o < kSlabK * 2; o += 4) *reinterpret_cast<uint32_t*>(xw + o) = 0u;
