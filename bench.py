@@ -664,7 +664,7 @@ def run_reference(args):
     secs = time.perf_counter() - t0
     metric, unit = metric_of(args.workload)
     value = nflops / secs / 1e12 if unit == "TFLOP/s" else nbytes / secs / 1e9
-    sample = f"first {rows} rows of each of {', '.join(n for n, _, _ in w['mats'])} per step"
+    sample = "per step: " + ", ".join(f"{n}: first {min(rows, N)} rows" for n, N, _ in w["mats"])
     return {
         "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": args.gpus, "steps": K, "warmup": W,
         "ms_per_step": round(secs * 1e3 / max(K, 1), 6), "higher_is_better": True, "scaling": "weak",
