@@ -3,7 +3,8 @@
 // of row n and 32-value sub-block j), for M in the hundreds to thousands of tokens, with
 // each weight slab streamed from HBM once per call instead of once per 8 tokens (the
 // re-streaming that made prefill slow on the Tenstorrent card: "Qwen3.8-27B on one
-// Tenstorrent P150", "3. Prefill was the real bug"; the per-sub-block factored form of
+// Tenstorrent P150", "3. Porting the 9B stack to 27B geometry", its prefill fixes; the
+// per-sub-block factored form of
 // the decode kernels: "I Built a Custom Blackwell Kernel for Qwen3.8-27B", "What the
 // custom path actually does").
 //

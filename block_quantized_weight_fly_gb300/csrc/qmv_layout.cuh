@@ -64,8 +64,9 @@
 // This regrouping is the planar-repack idea ("A 320B MoE on a free Kaggle TPU",
 // "The 110 GB claim, checked against the tensor index": blocks split into dense
 // planes with the matrix row on the lane axis) and the word-shadow idea of padding
-// blocks to aligned words ("vllm.cpp #3030", "Budget on the 32 GB P150"), laid out
-// for 128-bit loads and TMA bulk copies.
+// blocks to aligned words ("feat(BACKEND-TENSTORRENT-KEEPQUANT): the 27B arm — on-core
+// decode residency, TT grouped keep-quant GEMM, e2e gate", "Budget on the 32 GB
+// P150"), laid out for 128-bit loads and TMA bulk copies.
 //
 // Per expert, after its planes, an "extras" area holds the NVFP4 tensor scale
 // (fp32) or the FP8 row scales (fp32 [n_pad]). A 256-byte header precedes the first

@@ -5,11 +5,11 @@
  *
  * The operation is the keep-quant matmul seam Y = X . W^T with a quantized W,
  * over one matrix (E = 1) or a stacked expert tower weight[E*N, K]
- * ("vllm.cpp #3030, BACKEND-TENSTORRENT-KEEPQUANT: the 27B arm", scope item 2
- * and the "Re-anchor" comment). Formats: GGUF-style Q8_0 / Q4_K / Q6_K keep-quant
- * blocks (same issue, artifact table and "Budget on the 32 GB P150"), Q5_K (the
- * 5-bit member named with them in scope item 1 and owed by the grouped kernel in
- * the "Re-anchor" comment), and NVFP4
+ * ("feat(BACKEND-TENSTORRENT-KEEPQUANT): the 27B arm — on-core decode residency,
+ * TT grouped keep-quant GEMM, e2e gate", scope item 2 and the "Re-anchor" comment).
+ * Formats: GGUF-style Q8_0 / Q4_K / Q6_K keep-quant blocks (same issue, artifact
+ * table and "Budget on the 32 GB P150"), Q5_K (the 5-bit member named with them in
+ * scope item 1 and owed by the grouped kernel in the "Re-anchor" comment), and NVFP4
  * E2M1 codes with E4M3 block scales plus row-scaled FP8 ("I Built a Custom
  * Blackwell Kernel for Qwen3.8-27B", "What the custom path actually does").
  *
@@ -247,8 +247,9 @@ qmv_status qmv_gemm_nvfp4_w4a4(const void* packed_W, const uint16_t* x, float x_
 /* K-quant prefill GEMM on the 5th-generation tensor cores, for M in the hundreds to
  * thousands of tokens: y[m][n] = sum_k x[m][k] BlockToFloat(W)[n][k], each weight
  * superblock streamed from HBM once per call rather than once per 8 tokens (the
- * re-streaming prefill bug: "Qwen3.8-27B on one Tenstorrent P150", "3. Prefill was the
- * real bug"). fmt: QMV_Q4_K or QMV_Q5_K (others return QMV_EUNSUPPORTED). Per superblock,
+ * re-streaming prefill bug: "Qwen3.8-27B on one Tenstorrent P150", "3. Porting the 9B
+ * stack to 27B geometry", its prefill fixes). fmt: QMV_Q4_K or QMV_Q5_K (others return
+ * QMV_EUNSUPPORTED). Per superblock,
  * tcgen05.mma kind::f16 forms sum_k (sc_j q) x and sum_j m_j xsum_j in fp32 tensor memory
  * (sc_j q <= 1953 and m_j exact in f16; x in f16, exact for |x| in [2^-14, 65504]; xsum_j = the
  * fp32 sum of x over the 32-value sub-block, as two f16 terms, so |xsum_j| < 65504),

@@ -4,8 +4,10 @@
  * Plain single-threaded C, written from definitions:
  *  - the IEEE-754 binary16 / bfloat16 and OCP FP8 E4M3 / FP4 E2M1 number formats;
  *  - BlockToFloat dequantization, i.e. the CPU reference the on-core decode was
- *    held bit-exact against ("vllm.cpp #3030, BACKEND-TENSTORRENT-KEEPQUANT: the 27B
- *    arm", first comment: word-shadow decode "bit-exact vs BlockToFloat");
+ *    held bit-exact against ("feat(BACKEND-TENSTORRENT-KEEPQUANT): the 27B arm —
+ *    on-core decode residency, TT grouped keep-quant GEMM, e2e gate", the W4
+ *    residency paragraph: the word-shadow decode matched the CPU BlockToFloat bit
+ *    for bit);
  *  - the matmul seam Y = X . W^T with W packed, one matrix (E = 1) or a stacked
  *    expert tower weight[E*N, K] (same issue, scope item 2 and the "Re-anchor"
  *    comment);
