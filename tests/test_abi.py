@@ -79,3 +79,27 @@ def test_host_validation_without_device(lib):
     assert q._grouped(2, one, one, one, 2, one, 1, 1, 128, 256, 4, one, 1 << 20, None) == 1
     assert q._grouped(2, one, one, one, 0, one, 1, 9, 128, 256, 4, one, 1 << 20, None) == 1
     assert q.qmv_status_str(0) == "ok" and "workspace" in q.qmv_status_str(8)
+
+
+def test_host_validation_new_entries(lib):
+    """The grouped SwiGLU and prefill entries refuse bad arguments before any launch."""
+    import block_quantized_weight_fly_gb300 as q
+    P = ctypes.c_void_p
+    one = P(256)
+    gs = q._grouped_swiglu       # fmt, tower, ids, x, h, M, topk, N, K, E, ws, ws_bytes, stream
+    assert gs(2, None, one, one, one, 1, 1, 128, 256, 4, one, 1 << 20, None) == 1   # null tower
+    assert gs(2, one, one, one, one, 0, 1, 128, 256, 4, one, 1 << 20, None) == 1    # M = 0
+    assert gs(2, one, one, one, one, 9, 1, 128, 256, 4, one, 1 << 20, None) == 1    # M > 8
+    assert gs(2, one, one, one, one, 1, 9, 128, 256, 4, one, 1 << 20, None) == 1    # topk > 8
+    assert gs(2, one, one, one, one, 1, 1, 128, 256, 0, one, 1 << 20, None) == 1    # E = 0
+    assert gs(2, one, one, one, one, 1, 1, 128, 100, 4, one, 1 << 20, None) == 3    # K % 256
+    assert gs(2, P(257), one, one, one, 1, 1, 128, 256, 4, one, 1 << 20, None) == 2  # tower alignment
+    kq = q._kquant               # fmt, W, x, y, M, N, K, ws, ws_bytes, stream
+    assert kq(2, None, one, one, 512, 128, 256, one, 1 << 20, None) == 1
+    assert kq(2, one, one, one, 0, 128, 256, one, 1 << 20, None) == 1
+    assert kq(7, one, one, one, 512, 128, 256, one, 1 << 20, None) == 1              # not a format
+    for fmt in (1, 3, 4, 5):                                                         # Q8_0, Q6_K, NVFP4, FP8
+        assert kq(fmt, one, one, one, 512, 128, 256, one, 1 << 20, None) == 3
+    assert kq(2, one, one, one, 512, 128, 300, one, 1 << 20, None) == 3              # K % 256
+    assert kq(6, one, one, one, 512, 128, 300, one, 1 << 20, None) == 3
+    assert kq(2, one, P(264), one, 512, 128, 256, one, 1 << 20, None) == 2           # x alignment
