@@ -97,3 +97,35 @@ def test_tower_full_size_sampled(q, mat, M):
             assert err <= TOL, (t, j, e, err)
     del tower
     torch.cuda.empty_cache()
+
+
+def test_tower_swiglu_full_size_sampled(q):
+    """Fused gate|up SwiGLU over the 288-expert tower at its full gate/up shape
+    [2048, 4096] (a 576-expert tower: gates, then ups), top-8, M = 1 and 8; sampled
+    rows of every routed expert of the first tokens against the oracle's fp64
+    gate and up dots and its SwiGLU, within the bound carried through silu."""
+    E, topk, N, K, seed = 288, 8, 2048, 4096, 720
+    tower = device_matrix(q, "q4_k", seed, N, K, 2 * E)
+    rows = sample_rows(N, 12, seed)
+    for M in (1, 8):
+        ids = synth.expert_ids(seed + M, M, topk, E)
+        x = synth.activations(seed + 10 * M, M, K)
+        ws = q.workspace(q.QMV_ENTRY_GROUPED_SWIGLU, "q4_k", M, N, K, E, topk)
+        h = q.qmv_grouped_swiglu("q4_k", tower, torch.from_numpy(ids).cuda(), x.cuda(), N, K, E, ws)
+        assert q.qmv_last_route() == q.FORMATS["q4_k"] * 100 + 10
+        h = h.cpu().numpy().astype(np.float64)
+        assert q.qmv_device_status() == 0
+        assert int(ws.count_nonzero()) == 0
+        xb = synth.bf16_bits(x)
+        for t in range(min(M, 2)):
+            for j in range(topk):
+                e = int(ids[t, j])
+                g, dg = oracle.gemv_f64(host_rows_dequant("q4_k", seed, e * N + rows, N, K), xb[t][None, :])
+                u, du = oracle.gemv_f64(host_rows_dequant("q4_k", seed, (E + e) * N + rows, N, K), xb[t][None, :])
+                href = oracle.swiglu_f64(g, u)
+                s = np.abs(oracle.swiglu_f64(g, np.ones_like(g)))
+                bound = 1.1 * TOL * dg * (np.abs(u) + TOL * du) + s * TOL * du + 1e-6 * np.abs(href) + 1e-30
+                err = np.abs(h[t, j, rows][None, :] - href) / bound
+                assert float(err.max()) <= 1.0, (M, t, j, e, float(err.max()))
+    del tower
+    torch.cuda.empty_cache()

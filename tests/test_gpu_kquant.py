@@ -49,6 +49,21 @@ def test_kquant_parity(q, fmt, M, N, K):
     assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
 
 
+@pytest.mark.parametrize("fmt,M,N,K", [("q4_k", 2048, 384, 1024), ("q5_k", 1000, 260, 512)])
+def test_kquant_large_and_ragged_m(q, fmt, M, N, K):
+    """Many token tiles (M = 2048: 16 tiles) and a ragged last token tile (M = 1000)."""
+    W, canon = host_matrix(fmt, 65, N, K)
+    D = host_dequant(fmt, canon, N, K)
+    x = synth.activations(67, M, K)
+    ref, den = oracle.gemv_f64(D, synth.bf16_bits(x))
+    packed = q.qmv_pack(fmt, torch.from_numpy(canon).cuda(), N, K)
+    ws = q.workspace(q.QMV_ENTRY_KQUANT, fmt, M, N, K)
+    y = q.qmv_gemm_kquant(fmt, packed, x.cuda(), N, K, ws).cpu().numpy()
+    assert q.qmv_device_status() == 0
+    assert norm_err(y, ref, den) <= TOL
+    assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
+
+
 @pytest.mark.parametrize("fmt,M,N,K", [("q4_k", 256, 256, 2048), ("q4_k", 384, 130, 4096), ("q5_k", 256, 300, 2048)])
 def test_kquant_split_k_deterministic(q, fmt, M, N, K):
     """Few tiles over many CTAs: every tile is split across CTAs and finished from
