@@ -730,14 +730,17 @@ struct Slab<F_NVFP4, 1> {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t wa = CA[j], wb = CB[j];
-      const bool mine = (j >> 1) == jp;
+      // the B operand is x only in the chunk pair this lane's column serves: zeroed by a
+      // multiply with an f16x2 {1, 1} / {0, 0} mask on the FMA pipe (x is finite),
+      // which keeps the ALU pipe for the decode
+      const uint32_t mk = ((j >> 1) == jp) ? 0x3C003C00u : 0u;
       const uint32_t* xv = (j & 1) ? xo : xe;
       float* d = (j & 1) ? dO : dE;
       uint32_t pa[4], pb[4];
       e2m1x4_f16(wa, pa);
       e2m1x4_f16(wb, pb);
-      mma_f16(d, pa[0], pb[0], pa[1], pb[1], sel(mine, xv[0]), sel(mine, xv[1]));
-      mma_f16(d, pa[2], pb[2], pa[3], pb[3], sel(mine, xv[2]), sel(mine, xv[3]));
+      mma_f16(d, pa[0], pb[0], pa[1], pb[1], hmul2(xv[0], mk), hmul2(xv[1], mk));
+      mma_f16(d, pa[2], pb[2], pa[3], pb[3], hmul2(xv[2], mk), hmul2(xv[3], mk));
     }
     const uint32_t sA = lds32(sf + 512 * t + 16 * (rA & 31) + 4 * (rA >> 5));
     const uint32_t sB = lds32(sf + 512 * t + 16 * (rB & 31) + 4 * (rB >> 5));
