@@ -165,15 +165,26 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash():
-    """Hash of every kernel source: a recorded traffic figure is used only while it matches."""
+def kernel_unit(workload):
+    """The translation unit that holds the workload's dominant kernel."""
+    w = WORKLOADS[workload]
+    if w.get("w4a4"):
+        return "qmv_w4a4.cu"
+    return "qmv_kq.cu" if w.get("kquant") else "qmv_stream.cu"
+
+
+def kernel_source_hash(unit):
+    """Hash of what one kernel is built from: its translation unit, the host launch code
+    and every header. A recorded traffic figure is used only while it matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_weight_fly_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    files = [os.path.join(csrc, n) for n in sorted(os.listdir(csrc))
+             if n in (unit, "qmv_api.cu") or n.endswith((".cuh", ".h"))]
+    files.append(os.path.join(ROOT, "include", "qmv.h"))
+    for path in files:
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -185,7 +196,7 @@ def recorded_traffic(workload):
     with open(path) as f:
         d = json.load(f)
     rec = d.get(workload)
-    if not rec or rec.get("kernel_hash") != kernel_source_hash():
+    if not rec or rec.get("kernel_hash") != kernel_source_hash(kernel_unit(workload)):
         return None
     return rec.get("dram_bytes_per_launch")
 
