@@ -179,7 +179,7 @@ struct Cursor {
   }
 };
 
-template <int FMT, int MT, bool SW>
+template <int FMT, int MT, bool SW, bool GR>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(const KParams kp) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const StreamArgs& a = kp.a;
@@ -327,9 +327,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     // The first round of stages: weights first (independent of earlier kernels),
     // then wait for the previous grid, then the activations of those stages.
     const int first = (s1 - s0) < kp.stages ? (s1 - s0) : kp.stages;
+    // grouped: the weights of every stage are fetched only now (they follow from the
+    // ids), and all CTAs start at once; the first stage goes alone, so that it lands
+    // first and the consumers start while the others are in flight
+    const int first_w = (GR && first > 1) ? 1 : first;
     {
       Cursor<SW> c2 = cur;
-      for (int i = 0; i < first; ++i) {
+      for (int i = 0; i < first_w; ++i) {
         const Seg& sg = segs[c2.seg];
         uint8_t* st = smem + kp.stage_base + i * kp.stage_bytes;
         const uint8_t* plane =
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       const int kv = (kMayBeRagged && cur.g == G - 1) ? kv_last : kSlabK;
       const uint32_t xbytes = (uint32_t)(kv * 2);
       const int R = sg.R < MT ? sg.R : MT;
-      if (it >= first) {
+      if (it >= first_w) {
         mbar_expect_tx(&full[stage], abytes + bbytes + xbytes * (uint32_t)R);
         bulk_g2s(st, plane + (int64_t)cur.t * kSlabRows * L.rec, abytes, &full[stage]);
         if (bbytes) bulk_g2s(st + kp.b_off, plane + L.plane_a + (int64_t)cur.t * bbytes, bbytes, &full[stage]);
@@ -363,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       for (int r = 0; r < R; ++r)
         bulk_g2s(st + kp.x_off + r * kXStride, a.x + (int64_t)sg.xrow[r] * L.K + (int64_t)cur.g * kSlabK, xbytes,
                  &full[stage]);
+      if (GR && it == 0 && first > 1 && !mbar_wait(&full[0], 0u, a.status)) misc[0] = 1;
       if (++stage == kp.stages) { stage = 0; rphase ^= 1u; }
       cur.next(G, RT);
     }
@@ -731,14 +736,17 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   const WsPlan plan = ws_plan_stream(MT, 0, a.num_ctas, SW ? 2 : 1);
   kp.partials = reinterpret_cast<float*>(a.ws + plan.partials_off);
   const int smem = kp.stage_base + kp.stages * kp.stage_bytes;
-  // opt in to the large dynamic shared memory once per device (not per launch, so
-  // that stream capture records launches only)
-  static int opted[64] = {0};
+  // M = 1 grouped calls have an instance of their own (the producer's first-stage start)
+  const bool gr = MT == 1 && a.ids != nullptr;
+  void (*kern)(const KParams) = gr ? stream_kernel<FMT, MT, SW, MT == 1> : stream_kernel<FMT, MT, SW, false>;
+  // opt in to the large dynamic shared memory once per device and instance (not per
+  // launch, so that stream capture records launches only)
+  static int opted[2][64] = {{0}};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (opted[dev] < smem) {
-    err = cudaFuncSetAttribute(stream_kernel<FMT, MT, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (opted[gr][dev] < smem) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    opted[dev] = smem;
+    opted[gr][dev] = smem;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.num_ctas);
@@ -756,7 +764,7 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, stream_kernel<FMT, MT, SW>, kp);
+  err = cudaLaunchKernelEx(&cfg, kern, kp);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
