@@ -77,6 +77,21 @@ def test_fp16_decode_exhaustive_vs_numpy():
     assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
 
 
+def test_bf16_decode_exhaustive():
+    # bf16 is the upper half of an IEEE binary32: decode = the code shifted into the top bits
+    codes = np.arange(65536, dtype=np.uint32)
+    ref = (codes << 16).view(np.float32)
+    got = np.array([oracle.bf16_to_f32(int(c)) for c in codes], dtype=np.float32)
+    nan = np.isnan(ref)          # a signalling NaN comes back quieted through a Python float
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2 * 127
+    assert np.array_equal(got.view(np.uint32)[~nan], ref.view(np.uint32)[~nan])
+
+
+def test_block_lengths():
+    # values per quantization block: Q8_0 32, K-quant superblocks 256, NVFP4 16
+    assert [oracle.block_values(f) for f in ("q8_0", "q4_k", "q5_k", "q6_k", "nvfp4")] == [32, 256, 256, 256, 16]
+
+
 def test_fp16_encode_vs_numpy_rne():
     rng = np.random.default_rng(1)
     vals = np.concatenate([
