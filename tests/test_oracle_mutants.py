@@ -1,0 +1,94 @@
+"""The oracle's pins catch plausible mistakes: each case plants one mistake in a copy of
+the oracle's C source (a dropped term, a wrong sign, index or bit position, swapped or
+transposed operands), rebuilds the copy and runs the pins of test_oracle.py against it;
+at least one pin must fail. Nothing here touches the real oracle or the CUDA path."""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# (name, statement in oracle.c, the same statement with the mistake planted)
+MUTANTS = [
+    ("q4_k min term dropped",
+     "w[b * 256 + e] = a * (float)q - c;\n                }\n            }\n        } else if (fmt == OR_Q5_K)",
+     "w[b * 256 + e] = a * (float)q;\n                }\n            }\n        } else if (fmt == OR_Q5_K)"),
+    ("q4_k scale and min fields swapped",
+     "int sc = q4k_field(blk + 4, j), m = q4k_field(blk + 4, 8 + j);\n                    int q = (blk[16",
+     "int sc = q4k_field(blk + 4, 8 + j), m = q4k_field(blk + 4, j);\n                    int q = (blk[16"),
+    ("q4_k nibble order",
+     "int q = (blk[16 + e / 2] >> (4 * (e & 1))) & 15;",
+     "int q = (blk[16 + e / 2] >> (4 * (1 - (e & 1)))) & 15;"),
+    ("q4_k sub-blocks of 16",
+     "                    int j = e / 32;\n                    int sc = q4k_field(blk + 4, j), m = q4k_field(blk + 4, 8 + j);\n"
+     "                    int q = (blk[16",
+     "                    int j = (e / 16) & 7;\n                    int sc = q4k_field(blk + 4, j), m = q4k_field(blk + 4, 8 + j);\n"
+     "                    int q = (blk[16"),
+    ("q5_k fifth bit taken column-wise",
+     "int hi = (blk[16 + e / 8] >> (e & 7)) & 1;",
+     "int hi = (blk[16 + (e & 31)] >> (e / 32)) & 1;"),
+    ("q5_k fifth bit weighted 8",
+     "int q = lo | (hi << 4);\n                    float a = d * (float)sc;\n                    float c",
+     "int q = lo | (hi << 3);\n                    float a = d * (float)sc;\n                    float c"),
+    ("q6_k offset sign", "w[b * 256 + e] = a * (float)(q - 32);", "w[b * 256 + e] = a * (float)(q + 32);"),
+    ("q6_k scales unsigned", "int sc = (int8_t)blk[192 + e / 16];", "int sc = (uint8_t)blk[192 + e / 16];"),
+    ("q6_k one scale per 32", "int sc = (int8_t)blk[192 + e / 16];", "int sc = (int8_t)blk[192 + e / 32];"),
+    ("q8_0 quants unsigned", "w[b * 32 + i] = d * (float)(int8_t)blk[2 + i];", "w[b * 32 + i] = d * (float)blk[2 + i];"),
+    ("nvfp4 tensor scale dropped", "W[r * K + k] = p * sT;", "W[r * K + k] = p;"),
+    ("nvfp4 one block scale per 32", "float sb = or_e4m3_to_f32(scales[r * (K / 16) + k / 16]);",
+     "float sb = or_e4m3_to_f32(scales[r * (K / 16) + k / 32]);"),
+    ("fp8 row scale indexed by column", "W[r * K + k] = or_e4m3_to_f32(canon[r * K + k]) * s;",
+     "W[r * K + k] = or_e4m3_to_f32(canon[r * K + k]) * rdf32(canon + rows * K + 4 * (k % rows));"),
+    ("gemv with W transposed",
+     "double p = (double)W[n * K + k] * (double)or_bf16_to_f32(x_bf16[m * K + k]);",
+     "double p = (double)W[k * N % (N * K) + n] * (double)or_bf16_to_f32(x_bf16[m * K + k]);"),
+    ("gemv drops the last k", "for (int64_t k = 0; k < K; k++) {\n                double p",
+     "for (int64_t k = 0; k < K - 1; k++) {\n                double p"),
+    ("error scale signed", "ab += fabs(p);", "ab += p;"),
+    ("silu sign", "h[i] = (g[i] / (1.0 + exp(-g[i]))) * u[i];", "h[i] = (g[i] / (1.0 + exp(g[i]))) * u[i];"),
+    ("gate and up swapped", "h[i] = (g[i] / (1.0 + exp(-g[i]))) * u[i];", "h[i] = (u[i] / (1.0 + exp(-u[i]))) * g[i];"),
+    ("activation block scale 1.5x too small", "or_f32_to_e4m3(amax / t) : 0;\n            scales[m",
+     "or_f32_to_e4m3(amax / (t / 1.5f)) : 0;\n            scales[m"),
+    ("activation nibble order", "codes[m * (K / 2) + e / 2] |= (uint8_t)(c << (4 * (e & 1)));",
+     "codes[m * (K / 2) + e / 2] |= (uint8_t)(c << (4 * (1 - (e & 1))));"),
+    ("distinct experts sorted descending", "while (j >= 0 && out[j] > v)", "while (j >= 0 && out[j] < v)"),
+]
+
+
+def _copy(dst):
+    os.makedirs(dst / "tests")
+    shutil.copytree(os.path.join(ROOT, "oracle"), dst / "oracle",
+                    ignore=shutil.ignore_patterns("*.so", "*.tmp*", "__pycache__"))
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), dst / "tests" / "golden")
+    for f in ("tests/test_oracle.py", "tests/conftest.py", "synth.py"):
+        shutil.copy(os.path.join(ROOT, f), dst / f)
+
+
+@pytest.mark.parametrize("name,good,bad", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(name, good, bad, tmp_path):
+    _copy(tmp_path)
+    src = tmp_path / "oracle" / "oracle.c"
+    text = src.read_text()
+    assert text.count(good) == 1, f"the statement for '{name}' is no longer in oracle.c"
+    src.write_text(text.replace(good, bad))
+    r = subprocess.run([sys.executable, "-c", "import oracle; oracle.build()"], cwd=tmp_path,
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "tests/test_oracle.py"], cwd=tmp_path, capture_output=True, text=True)
+    assert r.returncode == 1, f"no pin caught '{name}':\n{r.stdout[-2000:]}"
+
+
+def test_unmodified_copy_passes(tmp_path):
+    # the control: the copied pins pass on the copied oracle as it stands, so a failure
+    # above is the planted mistake's doing and not the copy's
+    _copy(tmp_path)
+    r = subprocess.run([sys.executable, "-c", "import oracle; oracle.build()"], cwd=tmp_path,
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "tests/test_oracle.py"],
+                       cwd=tmp_path, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout[-2000:]
