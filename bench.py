@@ -687,6 +687,28 @@ def run_reference(args):
     }
 
 
+def read_ceiling(dev, gib=4, reps=10):
+    """Read-side HBM ceiling: a PyTorch sum over a bf16 buffer of `gib` GiB (larger than
+    L2), timed with CUDA events after warm-up. A library reduction, not this library's
+    kernel: context for the roofline, whose peak stays the measured copy bandwidth."""
+    n = gib * (1 << 30) // 2
+    buf = torch.ones(n, dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        buf.sum(dtype=torch.float32)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        buf.sum(dtype=torch.float32)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = n * 2
+    del buf
+    return {"read_probe": "torch bf16 sum", "bytes": nbytes, "ms": round(ms, 4),
+            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -695,6 +717,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--read-probe", action="store_true",
+                    help="print the read-only HBM ceiling (a PyTorch sum over 4 GiB) and exit")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = DEFAULT_STEPS[args.workload]
@@ -714,6 +738,9 @@ def main():
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.read_probe:
+        print(json.dumps(read_ceiling(dev)), flush=True)
+        return
     if world > 1:
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         torch.distributed.init_process_group("nccl", device_id=dev)
