@@ -103,3 +103,55 @@ def test_host_validation_new_entries(lib):
     assert kq(2, one, one, one, 512, 128, 300, one, 1 << 20, None) == 3              # K % 256
     assert kq(6, one, one, one, 512, 128, 300, one, 1 << 20, None) == 3
     assert kq(2, one, P(264), one, 512, 128, 256, one, 1 << 20, None) == 2           # x alignment
+
+
+def test_host_validation_remaining_entries(lib):
+    """The dense SwiGLU, no-workspace GEMV, activation quantizer, W4A4 GEMM, pack,
+    dequant and quantize entries refuse bad arguments before any launch (every case
+    below fails a host check, so nothing is launched on any machine)."""
+    import block_quantized_weight_fly_gb300 as q
+    P = ctypes.c_void_p
+    one = P(256)
+    nan = float("nan")
+    sw = q._gemv_swiglu          # fmt, tower, x, h, M, N, K, ws, ws_bytes, stream
+    assert sw(2, None, one, one, 1, 128, 256, one, 1 << 20, None) == 1
+    assert sw(2, one, one, one, 0, 128, 256, one, 1 << 20, None) == 1
+    assert sw(2, one, one, one, 9, 128, 256, one, 1 << 20, None) == 1
+    assert sw(2, one, one, one, 1, 128, 100, one, 1 << 20, None) == 3
+    assert sw(2, P(257), one, one, 1, 128, 256, one, 1 << 20, None) == 2
+    assert q._gemv(2, one, one, one, 1, 0, 256, one, 1 << 20, None) == 1          # N = 0
+    assert q._gemv(2, one, one, one, 1, 128, 256, P(260), 1 << 20, None) == 2     # ws alignment
+    na = q._gemv_noalloc         # fmt, W, x, y, M, N, K, stream
+    assert na(2, None, one, one, 1, 128, 256, None) == 1
+    assert na(2, one, one, one, 9, 128, 256, None) == 1
+    assert na(2, one, one, one, 1, 128, 100, None) == 3
+    qa = q._quant_act            # x, x_scale, codes, scales, M, K, stream
+    assert qa(None, 1.0, one, one, 4, 256, None) == 1
+    assert qa(one, 1.0, one, one, 0, 256, None) == 1
+    assert qa(one, -1.0, one, one, 4, 256, None) == 1                            # negative scale
+    assert qa(one, nan, one, one, 4, 256, None) == 1
+    assert qa(one, 1.0, one, one, 4, 40, None) == 3                              # K % 16
+    w4 = q._w4a4                 # W, x, x_scale, y, M, N, K, ws, ws_bytes, stream
+    assert w4(None, one, 1.0, one, 512, 128, 256, one, 1 << 24, None) == 1
+    assert w4(one, one, 1.0, one, 0, 128, 256, one, 1 << 24, None) == 1
+    assert w4(one, one, nan, one, 512, 128, 256, one, 1 << 24, None) == 1
+    assert w4(one, one, 1.0, one, 512, 128, 40, one, 1 << 24, None) == 3         # K % 256
+    assert w4(P(257), one, 1.0, one, 512, 128, 256, one, 1 << 24, None) == 2
+    pk = q._pack                 # fmt, canon, N, K, E, dst, stream
+    assert pk(2, None, 128, 256, 1, one, None) == 1
+    assert pk(2, one, 128, 256, 0, one, None) == 1                               # E = 0
+    assert pk(9, one, 128, 256, 1, one, None) == 1
+    assert pk(2, one, 128, 100, 1, one, None) == 3
+    assert pk(2, one, 128, 256, 1, P(257), None) == 2
+    dq = q._dequant              # fmt, packed, N, K, E, row0, rows, out, stream
+    assert dq(2, None, 128, 256, 1, 0, 128, one, None) == 1
+    assert dq(2, one, 128, 256, 1, 100, 100, one, None) == 1                     # rows past N
+    assert dq(2, one, 128, 256, 1, -1, 10, one, None) == 1
+    qz = q._quantize             # fmt, W, rows, K, tensor_scale, canon, stream
+    assert qz(2, None, 128, 256, 0.0, one, None) == 1
+    assert qz(9, one, 128, 256, 0.0, one, None) == 1
+    assert qz(2, one, 128, 100, 0.0, one, None) == 3
+    # workspace sizes of impossible requests are 0
+    assert q._ws_size(1, 2, 0, 128, 256, 1, 1) == 0                              # M = 0
+    assert q._ws_size(9, 2, 1, 128, 256, 1, 1) == 0                              # no such entry
+    assert q._ws_size(1, 2, 9, 128, 256, 1, 1) == 0                              # M > 8
