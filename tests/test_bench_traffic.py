@@ -1,5 +1,7 @@
-"""The benchmark's recorded DRAM traffic: each record is keyed by the sources of its own
-kernel, so editing one kernel invalidates that kernel's record and no other."""
+"""Host-side parts of the benchmark's roofline and clock records: each recorded DRAM
+traffic figure is keyed by the sources of its own kernel, so editing one kernel
+invalidates that kernel's record and no other; the SM clock summary is parsed from
+nvidia-smi's CSV lines."""
 import importlib.util
 import json
 import os
@@ -86,3 +88,21 @@ def test_committed_records_name_known_workloads(bench):
         assert rec["dram_bytes_per_launch"] > 0
         assert len(rec["kernel_hash"]) == 16
         assert rec["source"].startswith("ncu ") and "--clock-control none" in rec["source"]
+
+
+def test_clock_summary_parses_nvidia_smi_lines(bench):
+    s = bench.ClockSampler(0)
+    s.out = "\n".join([
+        "0, 2070, 2070, 812.40, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1390.10, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1401.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "garbage line",
+        "0, [N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ])
+    d = s.summary()
+    assert d["sm_mhz"] == 2070.0 and d["sm_max_mhz"] == 2070.0 and d["samples"] == 3
+    assert d["reasons"] == ["sw_power_cap"]
+    s.out = "0, 1500, 2070, 900, 0x8, Active, Not Active, Active, Not Active"
+    assert bench.ClockSampler.summary(s)["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    s.out = ""
+    assert s.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
