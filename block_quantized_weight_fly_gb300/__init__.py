@@ -69,11 +69,13 @@ _kquant = _sig("qmv_gemm_kquant", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, 
 _status_str = _sig("qmv_status_str", ctypes.c_char_p, [_I])
 _last_route = _sig("qmv_last_route", _I, [])
 _dev_status = _sig("qmv_device_status", _I, [_I])
+_split_fault = _sig("qmv_debug_split_k_fault", None, [_I, ctypes.c_uint64])
 
 EXPORTED = ["qmv_canon_size", "qmv_pack_size", "qmv_pack", "qmv_quantize", "qmv_dequant",
             "qmv_workspace_size", "qmv_gemv", "qmv_grouped", "qmv_quant_act_nvfp4",
             "qmv_gemm_nvfp4_w4a4", "qmv_status_str", "qmv_last_route", "qmv_device_status",
-            "qmv_gemv_noalloc", "qmv_gemv_swiglu", "qmv_grouped_swiglu", "qmv_gemm_kquant"]
+            "qmv_gemv_noalloc", "qmv_gemv_swiglu", "qmv_grouped_swiglu", "qmv_gemm_kquant",
+            "qmv_debug_split_k_fault"]
 
 
 def _fmt(fmt) -> int:
@@ -111,6 +113,47 @@ def _bits16(x: torch.Tensor) -> torch.Tensor:
     raise ValueError("x must be bf16 (or its raw 16-bit patterns)")
 
 
+def _act(x: torch.Tensor, K: int, rows: int | None = None) -> tuple[torch.Tensor, int]:
+    """Check an activation tensor [M, K] (or [K]) and return it with its row count.
+    The library reads M * K values through a raw pointer, so a short or strided x
+    is refused here rather than read out of bounds on the device."""
+    x = _bits16(x)
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if x.dim() == 1:
+        M = 1
+        if x.shape[0] != K:
+            raise ValueError(f"x has {x.shape[0]} values, K = {K}")
+    elif x.dim() == 2:
+        M = x.shape[0]
+        if x.shape[1] != K:
+            raise ValueError(f"x has rows of {x.shape[1]} values, K = {K}")
+    else:
+        raise ValueError("x must be [M, K] or [K]")
+    if rows is not None and M != rows:
+        raise ValueError(f"x has {M} rows, {rows} expected")
+    return x, M
+
+
+def _out(y: torch.Tensor | None, shape, dev, name: str) -> torch.Tensor:
+    """An fp32 output of `shape`: allocated if None, else checked (float32, contiguous,
+    on x's device, at least as many values as the library writes)."""
+    if y is None:
+        return torch.empty(shape, dtype=torch.float32, device=dev)
+    if not y.is_cuda or y.device != torch.device(dev):
+        raise ValueError(f"{name} must be a CUDA tensor on {dev}")
+    if y.dtype != torch.float32:
+        raise ValueError(f"{name} must be float32")
+    if not y.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    need = 1
+    for d in shape:
+        need *= int(d)
+    if y.numel() < need:
+        raise ValueError(f"{name} holds {y.numel()} values, {need} needed")
+    return y
+
+
 # ---- entry points -------------------------------------------------------------
 def qmv_status_str(status: int) -> str:
     return _status_str(int(status)).decode()
@@ -122,6 +165,13 @@ def qmv_last_route() -> int:
 
 def qmv_device_status(reset: bool = True) -> int:
     return int(_dev_status(1 if reset else 0))
+
+
+def qmv_debug_split_k_fault(mode: int, wait_limit_ns: int = 0) -> None:
+    """Test hook of the split-K reduction (include/qmv.h): mode 1, peers publish
+    nothing and reducers time out after wait_limit_ns; mode 2, reducers give up at
+    once and leave their peers' partial sums behind; mode 0, normal operation."""
+    _split_fault(int(mode), int(wait_limit_ns))
 
 
 def qmv_canon_size(fmt, N: int, K: int, E: int = 1) -> int:
@@ -142,8 +192,12 @@ def qmv_pack(fmt, canon: torch.Tensor, N: int, K: int, E: int = 1, dst: torch.Te
     size = qmv_pack_size(fmt, N, K, E)
     if size == 0:
         raise QmvError(3, "qmv_pack_size")
+    if canon.numel() * canon.element_size() < qmv_canon_size(fmt, N, K, E):
+        raise ValueError("canon is shorter than qmv_canon_size")
     if dst is None:
         dst = torch.empty(size, dtype=torch.uint8, device=canon.device)
+    elif not dst.is_cuda or not dst.is_contiguous() or dst.numel() * dst.element_size() < size:
+        raise ValueError(f"dst must be a contiguous CUDA tensor of at least {size} bytes")
     _check(_pack(_fmt(fmt), _ptr(canon), N, K, E, _ptr(dst), _stream(stream)), "qmv_pack")
     return dst
 
@@ -155,8 +209,12 @@ def qmv_quantize(fmt, W: torch.Tensor, tensor_scale: float = 0.0, canon: torch.T
         raise ValueError("W must be a 2-D float32 tensor")
     rows, K = W.shape
     size = qmv_canon_size(fmt, rows, K, 1)
+    if not W.is_contiguous():
+        raise ValueError("W must be contiguous")
     if canon is None:
         canon = torch.empty(size, dtype=torch.uint8, device=W.device)
+    elif not canon.is_cuda or not canon.is_contiguous() or canon.numel() * canon.element_size() < size:
+        raise ValueError(f"canon must be a contiguous CUDA tensor of at least {size} bytes")
     _check(_quantize(_fmt(fmt), _ptr(W), rows, K, float(tensor_scale), _ptr(canon), _stream(stream)),
            "qmv_quantize")
     return canon
@@ -166,8 +224,7 @@ def qmv_dequant(fmt, packed: torch.Tensor, N: int, K: int, E: int = 1, row0: int
                 rows: int | None = None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     _dev(packed, "packed")
     rows = N * E - row0 if rows is None else rows
-    if out is None:
-        out = torch.empty((rows, K), dtype=torch.float32, device=packed.device)
+    out = _out(out, (rows, K), packed.device, "out")
     _check(_dequant(_fmt(fmt), _ptr(packed), N, K, E, row0, rows, _ptr(out), _stream(stream)),
            "qmv_dequant")
     return out
@@ -185,10 +242,8 @@ def workspace(entry: int, fmt, M: int, N: int, K: int, E: int = 1, topk: int = 1
 def qmv_gemv(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int,
              ws: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     _dev(packed_W, "packed_W"); _dev(x, "x"); _dev(ws, "ws")
-    x = _bits16(x)
-    M = x.shape[0] if x.dim() == 2 else 1
-    if y is None:
-        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    x, M = _act(x, K)
+    y = _out(y, (M, N), x.device, "y")
     _check(_gemv(_fmt(fmt), _ptr(packed_W), _ptr(x), _ptr(y), M, N, K, _ptr(ws), ws.numel(),
                  _stream(stream)), "qmv_gemv")
     return y
@@ -198,10 +253,8 @@ def qmv_gemv_swiglu(fmt, tower: torch.Tensor, x: torch.Tensor, N: int, K: int, w
                     h: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """h = silu(gate . x) * (up . x) over a 2-expert tower (gate = expert 0, up = expert 1)."""
     _dev(tower, "tower"); _dev(x, "x"); _dev(ws, "ws")
-    x = _bits16(x)
-    M = x.shape[0] if x.dim() == 2 else 1
-    if h is None:
-        h = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    x, M = _act(x, K)
+    h = _out(h, (M, N), x.device, "h")
     _check(_gemv_swiglu(_fmt(fmt), _ptr(tower), _ptr(x), _ptr(h), M, N, K, _ptr(ws), ws.numel(),
                         _stream(stream)), "qmv_gemv_swiglu")
     return h
@@ -212,8 +265,8 @@ def qmv_gemv_noalloc(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: in
     """qmv_gemv with the library's built-in scratch instead of a workspace. y is
     required (the caller owns every buffer); nothing is allocated."""
     _dev(packed_W, "packed_W"); _dev(x, "x"); _dev(y, "y")
-    x = _bits16(x)
-    M = x.shape[0] if x.dim() == 2 else 1
+    x, M = _act(x, K)
+    y = _out(y, (M, N), x.device, "y")
     _check(_gemv_noalloc(_fmt(fmt), _ptr(packed_W), _ptr(x), _ptr(y), M, N, K, _stream(stream)),
            "qmv_gemv_noalloc")
     return y
@@ -225,10 +278,11 @@ def qmv_grouped(fmt, tower: torch.Tensor, expert_ids: torch.Tensor, x: torch.Ten
     _dev(tower, "tower"); _dev(expert_ids, "expert_ids"); _dev(x, "x"); _dev(ws, "ws")
     if expert_ids.dtype != torch.int32 or expert_ids.dim() != 2:
         raise ValueError("expert_ids must be int32 [M, topk]")
+    if not expert_ids.is_contiguous():
+        raise ValueError("expert_ids must be contiguous")
     M, topk = expert_ids.shape
-    x = _bits16(x)
-    if y is None:
-        y = torch.empty((M, topk, N), dtype=torch.float32, device=x.device)
+    x, _ = _act(x, K, M * topk if x_per_pair else M)
+    y = _out(y, (M, topk, N), x.device, "y")
     _check(_grouped(_fmt(fmt), _ptr(tower), _ptr(expert_ids), _ptr(x), 1 if x_per_pair else 0, _ptr(y),
                     M, topk, N, K, E, _ptr(ws), ws.numel(), _stream(stream)), "qmv_grouped")
     return y
@@ -242,10 +296,11 @@ def qmv_grouped_swiglu(fmt, tower: torch.Tensor, expert_ids: torch.Tensor, x: to
     _dev(tower, "tower"); _dev(expert_ids, "expert_ids"); _dev(x, "x"); _dev(ws, "ws")
     if expert_ids.dtype != torch.int32 or expert_ids.dim() != 2:
         raise ValueError("expert_ids must be int32 [M, topk]")
+    if not expert_ids.is_contiguous():
+        raise ValueError("expert_ids must be contiguous")
     M, topk = expert_ids.shape
-    x = _bits16(x)
-    if h is None:
-        h = torch.empty((M, topk, N), dtype=torch.float32, device=x.device)
+    x, _ = _act(x, K, M)
+    h = _out(h, (M, topk, N), x.device, "h")
     _check(_grouped_swiglu(_fmt(fmt), _ptr(tower), _ptr(expert_ids), _ptr(x), _ptr(h), M, topk, N, K, E,
                            _ptr(ws), ws.numel(), _stream(stream)), "qmv_grouped_swiglu")
     return h
@@ -255,7 +310,12 @@ def qmv_quant_act_nvfp4(x: torch.Tensor, x_scale: float, codes: torch.Tensor | N
                         scales: torch.Tensor | None = None, stream=None):
     _dev(x, "x")
     x = _bits16(x)
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [M, K] tensor")
     M, K = x.shape
+    for t, n, name in ((codes, M * (K // 2), "codes"), (scales, M * (K // 16), "scales")):
+        if t is not None and (t.dtype != torch.uint8 or not t.is_contiguous() or t.numel() < n or not t.is_cuda):
+            raise ValueError(f"{name} must be a contiguous CUDA uint8 tensor of at least {n} bytes")
     if codes is None:
         codes = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
     if scales is None:
@@ -268,10 +328,8 @@ def qmv_quant_act_nvfp4(x: torch.Tensor, x_scale: float, codes: torch.Tensor | N
 def qmv_gemm_nvfp4_w4a4(packed_W: torch.Tensor, x: torch.Tensor, x_scale: float, N: int, K: int,
                         ws: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     _dev(packed_W, "packed_W"); _dev(x, "x"); _dev(ws, "ws")
-    x = _bits16(x)
-    M = x.shape[0]
-    if y is None:
-        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    x, M = _act(x, K)
+    y = _out(y, (M, N), x.device, "y")
     _check(_w4a4(_ptr(packed_W), _ptr(x), float(x_scale), _ptr(y), M, N, K, _ptr(ws), ws.numel(),
                  _stream(stream)), "qmv_gemm_nvfp4_w4a4")
     return y
@@ -281,10 +339,8 @@ def qmv_gemm_kquant(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int
                     y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """y = x . W^T for a K-quant W at prefill sizes (tensor cores, each weight read once)."""
     _dev(packed_W, "packed_W"); _dev(x, "x"); _dev(ws, "ws")
-    x = _bits16(x)
-    M = x.shape[0]
-    if y is None:
-        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    x, M = _act(x, K)
+    y = _out(y, (M, N), x.device, "y")
     _check(_kquant(_fmt(fmt), _ptr(packed_W), _ptr(x), _ptr(y), M, N, K, _ptr(ws), ws.numel(), _stream(stream)),
            "qmv_gemm_kquant")
     return y

@@ -2,6 +2,7 @@
 // host-side argument validation, the per-device status word, and dispatch to the
 // kernels. Nothing here allocates memory, synchronizes a stream or reads device
 // data, except qmv_device_status(), which is a diagnostics hook and says so.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 #include "qmv.h"
@@ -14,18 +15,23 @@ using namespace qmv;
 __device__ unsigned g_status;               // per-device latched status bits
 
 constexpr int kMaxDevices = 64;
-unsigned* g_status_ptr[kMaxDevices] = {nullptr};
+// device addresses of the status word, looked up once per device; host threads that
+// race on the first look-up store the same value (the address of the symbol in the
+// device's current context: after cudaDeviceReset the library must be reloaded)
+std::atomic<unsigned*> g_status_ptr[kMaxDevices];
 thread_local int g_last_route = 0;
 
 unsigned* status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (g_status_ptr[dev] == nullptr) {
+  unsigned* cached = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (cached == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<unsigned*>(p);
+    cached = static_cast<unsigned*>(p);
+    g_status_ptr[dev].store(cached, std::memory_order_release);
   }
-  return g_status_ptr[dev];
+  return cached;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -34,13 +40,11 @@ qmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ECU
 
 bool valid_fmt(int f) { return f >= QMV_Q8_0 && f <= QMV_Q5_K; }
 
-// CTAs of a stream-kernel grid for `slabs` slabs. Two CTAs per SM hide the
-// consumers' latency better than one and win at M > 1 and for the grouped call.
-// A dense M = 1 call keeps one per SM: the free slots let the next call's CTAs
-// start and prefetch their first slabs early, which wins in back-to-back layers.
-int stream_grid(int64_t slabs, int M, bool grouped, int sms) {
-  const int64_t n = (M > 1 || grouped) ? 2 * (int64_t)sms : (int64_t)sms;
-  return (int)(slabs < n ? slabs : n);
+void apply_plan(StreamArgs* a, const StreamPlan& p) {
+  a->num_ctas = p.grid;
+  a->cells = p.cells;
+  a->cpc = p.cpc;
+  a->maxslots = p.maxslots;
 }
 
 }  // namespace
@@ -97,18 +101,22 @@ qmv_status qmv_dequant(qmv_fmt fmt, const void* packed, int64_t N, int64_t K, in
 }
 
 size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, int64_t E, int topk) {
-  (void)E; (void)topk;
   if (!valid_fmt(fmt) || M <= 0 || N <= 0 || K <= 0) return 0;
   const int sms = num_sms_current_device();
   if (sms <= 0) return 0;
-  // room for the largest grid the entry point launches (two CTAs per SM)
-  if (entry == QMV_ENTRY_GEMV || entry == QMV_ENTRY_GROUPED) {
-    if (M > QMV_MAX_M) return 0;
-    return (size_t)ws_plan_stream(M, 0, 2 * sms).total;
+  if (entry == QMV_ENTRY_GEMV || entry == QMV_ENTRY_SWIGLU) {
+    const int passes = entry == QMV_ENTRY_SWIGLU ? 2 : 1;
+    Layout L;
+    if (M > QMV_MAX_M || !make_layout((int)fmt, N, K, passes, &L)) return 0;
+    return (size_t)plan_stream_dense(passes * L.row_tiles * L.k_groups, M, passes, sms, false).ws_bytes;
   }
-  if (entry == QMV_ENTRY_SWIGLU || entry == QMV_ENTRY_GROUPED_SWIGLU) {
-    if (M > QMV_MAX_M) return 0;
-    return (size_t)ws_plan_stream(M, 0, 2 * sms, 2).total;
+  if (entry == QMV_ENTRY_GROUPED || entry == QMV_ENTRY_GROUPED_SWIGLU) {
+    const int passes = entry == QMV_ENTRY_GROUPED_SWIGLU ? 2 : 1;
+    Layout L;
+    if (M > QMV_MAX_M || topk < 1 || E < 1 || !make_layout((int)fmt, N, K, passes * E, &L)) return 0;
+    const int64_t experts = (int64_t)M * topk < E ? (int64_t)M * topk : E;
+    return (size_t)plan_stream_grouped(passes * experts * L.row_tiles * L.k_groups, M, passes, L.k_groups, sms)
+        .ws_bytes;
   }
   if (entry == QMV_ENTRY_KQUANT) {
     if ((fmt != QMV_Q4_K && fmt != QMV_Q5_K) || K % 256) return 0;
@@ -133,9 +141,8 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
   if (!aligned(packed_W, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
-  const int64_t slabs = L.row_tiles * L.k_groups;
-  const int ctas = stream_grid(slabs, M, false, sms);
-  if (ws_bytes < (size_t)ws_plan_stream(M, 0, ctas).total) return QMV_EWORKSPACE;
+  const StreamPlan plan = plan_stream_dense(L.row_tiles * L.k_groups, M, 1, sms, false);
+  if (ws_bytes < (size_t)plan.ws_bytes) return QMV_EWORKSPACE;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
   StreamArgs a;
@@ -145,7 +152,7 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
   a.M = M; a.topk = 1; a.x_per_pair = 0; a.swiglu = 0;
   a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
   a.status = status;
-  a.num_ctas = ctas;
+  apply_plan(&a, plan);
   int variant = 0;
   qmv_status st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
@@ -170,8 +177,8 @@ qmv_status qmv_grouped(qmv_fmt fmt, const void* tower, const int32_t* expert_ids
   // the distinct experts are found on the device: size the grid for the most
   // there can be (CTAs beyond the slab count get empty ranges)
   const int64_t experts = (int64_t)M * topk < E ? (int64_t)M * topk : E;
-  const int ctas = stream_grid(experts * L.row_tiles * L.k_groups, M, true, sms);
-  if (ws_bytes < (size_t)ws_plan_stream(M, 0, ctas).total) return QMV_EWORKSPACE;
+  const StreamPlan plan = plan_stream_grouped(experts * L.row_tiles * L.k_groups, M, 1, L.k_groups, sms);
+  if (ws_bytes < (size_t)plan.ws_bytes) return QMV_EWORKSPACE;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
   StreamArgs a;
@@ -181,7 +188,7 @@ qmv_status qmv_grouped(qmv_fmt fmt, const void* tower, const int32_t* expert_ids
   a.M = M; a.topk = topk; a.x_per_pair = x_per_pair; a.swiglu = 0;
   a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
   a.status = status;
-  a.num_ctas = ctas;
+  apply_plan(&a, plan);
   int variant = 0;
   qmv_status st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
@@ -197,9 +204,8 @@ qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, fl
   if (!aligned(tower, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(h, 4)) return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
-  const int64_t slabs = 2 * L.row_tiles * L.k_groups;
-  const int ctas = stream_grid(slabs, M, false, sms);
-  if (ws_bytes < (size_t)ws_plan_stream(M, 0, ctas, 2).total) return QMV_EWORKSPACE;
+  const StreamPlan plan = plan_stream_dense(2 * L.row_tiles * L.k_groups, M, 2, sms, false);
+  if (ws_bytes < (size_t)plan.ws_bytes) return QMV_EWORKSPACE;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
   StreamArgs a;
@@ -209,7 +215,7 @@ qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, fl
   a.M = M; a.topk = 1; a.x_per_pair = 0; a.swiglu = 1;
   a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
   a.status = status;
-  a.num_ctas = ctas;
+  apply_plan(&a, plan);
   int variant = 0;
   qmv_status st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
@@ -231,8 +237,8 @@ qmv_status qmv_grouped_swiglu(qmv_fmt fmt, const void* tower, const int32_t* exp
     return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
-  const int ctas = stream_grid(2 * experts * L.row_tiles * L.k_groups, M, true, sms);
-  if (ws_bytes < (size_t)ws_plan_stream(M, 0, ctas, 2).total) return QMV_EWORKSPACE;
+  const StreamPlan plan = plan_stream_grouped(2 * experts * L.row_tiles * L.k_groups, M, 2, L.k_groups, sms);
+  if (ws_bytes < (size_t)plan.ws_bytes) return QMV_EWORKSPACE;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
   StreamArgs a;
@@ -242,7 +248,7 @@ qmv_status qmv_grouped_swiglu(qmv_fmt fmt, const void* tower, const int32_t* exp
   a.M = M; a.topk = topk; a.x_per_pair = 0; a.swiglu = 1;
   a.ws = static_cast<uint8_t*>(ws); a.ws_bytes = (int64_t)ws_bytes;
   a.status = status;
-  a.num_ctas = ctas;
+  apply_plan(&a, plan);
   int variant = 0;
   qmv_status st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
@@ -321,6 +327,10 @@ const char* qmv_status_str(qmv_status s) {
 
 int qmv_last_route(void) { return g_last_route; }
 
+void qmv_debug_split_k_fault(int mode, uint64_t wait_limit_ns) {
+  set_split_fault(mode, (unsigned long long)wait_limit_ns);
+}
+
 qmv_status qmv_device_status(int reset) {
   unsigned* p = status_ptr();
   if (!p) return QMV_ECUDA;
@@ -351,19 +361,19 @@ static __device__ __align__(256) unsigned char g_gemv_scratch[QMV_STATIC_SCRATCH
 
 namespace {
 
-uint8_t* g_scratch_ptr[kMaxDevices] = {nullptr};
+std::atomic<uint8_t*> g_scratch_ptr[kMaxDevices];     // as g_status_ptr
 
 // Set-up, once per device, with that device current: the device address of the
 // scratch array. The first qmv_gemv_noalloc call on each device runs it.
 qmv_status scratch_ptr(uint8_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMV_ECUDA;
-  if (g_scratch_ptr[dev] == nullptr) {
-    uint8_t* ptr = nullptr;
+  uint8_t* ptr = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (ptr == nullptr) {
     if (cudaGetSymbolAddress((void**)&ptr, g_gemv_scratch) != cudaSuccess) return QMV_ECUDA;
-    g_scratch_ptr[dev] = ptr;
+    g_scratch_ptr[dev].store(ptr, std::memory_order_release);
   }
-  *out = g_scratch_ptr[dev];
+  *out = ptr;
   return QMV_OK;
 }
 
@@ -378,8 +388,10 @@ extern "C" qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const 
   if (!aligned(packed_W, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
-  const WsPlan plan = ws_plan_stream(M, 0, sms);
-  if ((size_t)plan.total > (size_t)QMV_STATIC_SCRATCH_BYTES) return QMV_EWORKSPACE;
+  // two cells per CTA at every M (one CTA per SM): the cells, and so the order of
+  // the sums, are those of qmv_gemv, whose results this entry reproduces bit for bit
+  const StreamPlan plan = plan_stream_dense(L.row_tiles * L.k_groups, M, 1, sms, true);
+  if ((size_t)plan.ws_bytes > (size_t)QMV_STATIC_SCRATCH_BYTES) return QMV_EWORKSPACE;
   uint8_t* scratch = nullptr;
   qmv_status st = scratch_ptr(&scratch);
   if (st != QMV_OK) return st;
@@ -387,7 +399,7 @@ extern "C" qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const 
   if (!status) return QMV_ECUDA;
   // The array keeps whatever the previous call left; the partial-sum words must
   // start at zero (a successful call leaves them zero, a failed one may not).
-  st = from_cuda(cudaMemsetAsync(scratch + plan.partials_off, 0, (size_t)plan.partials_bytes, stream));
+  st = from_cuda(cudaMemsetAsync(scratch, 0, (size_t)plan.ws_bytes, stream));
   if (st != QMV_OK) return st;
   StreamArgs a;
   a.L = L;
@@ -396,8 +408,7 @@ extern "C" qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const 
   a.M = M; a.topk = 1; a.x_per_pair = 0; a.swiglu = 0;
   a.ws = scratch; a.ws_bytes = (int64_t)QMV_STATIC_SCRATCH_BYTES;
   a.status = status;
-  const int64_t slabs = L.row_tiles * L.k_groups;
-  a.num_ctas = (int)(slabs < sms ? slabs : sms);
+  apply_plan(&a, plan);
   int variant = 0;
   st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;

@@ -26,15 +26,30 @@ struct StreamArgs {
   int64_t ws_bytes;
   unsigned* status;          // per-device status word
   int num_ctas;              // persistent grid size
+  int cells;                 // dense: cells of the accumulation order (> 0); grouped: 0
+  int cpc;                   // dense: cells per CTA (1 or 2)
+  int maxslots;              // workspace slots (published pieces) per CTA
 };
 
-// workspace carve-up (bytes), shared by the host size query and the kernels
-struct WsPlan {
-  int64_t partials_off, partials_bytes;
-  int64_t total;
+// Grid, accumulation cells and workspace of one stream-kernel call (host side),
+// shared by the entry points and the workspace size query.
+//  - dense: V = min(2 x SMs, slabs) cells, a function of the matrix and the SM count
+//    only, so that every M (and the no-workspace entry) adds in the same order;
+//    two cells per CTA at M = 1 (one CTA per SM, so the next call's CTAs fit beside
+//    it) or when two_cells is set, else one (two CTAs per SM);
+//  - grouped: every slab is a cell; min(2 x SMs, slabs_max) CTAs.
+// passes: 1, or 2 for the fused gate|up (gate and up sums).
+struct StreamPlan {
+  int grid, cells, cpc, maxslots;
+  int64_t ws_bytes;          // split-K workspace (published pieces), 256-byte multiple
 };
-// passes: 1, or 2 for the fused gate|up (gate and up partial sums)
-WsPlan ws_plan_stream(int M, int64_t tiles_max, int num_ctas, int passes = 1);
+StreamPlan plan_stream_dense(int64_t slabs, int M, int passes, int sms, bool two_cells);
+StreamPlan plan_stream_grouped(int64_t slabs_max, int M, int passes, int64_t k_groups, int sms);
+// Test hook of the reduction (see qmv_debug_split_k_fault in qmv.h): mode 1, peers
+// publish nothing and reducers wait peer_wait_ns, then latch QMV_ETIMEOUT; mode 2,
+// reducers latch QMV_ETIMEOUT at once and leave the peers' pieces in the workspace;
+// mode 0 restores normal operation.
+void set_split_fault(int mode, unsigned long long peer_wait_ns);
 
 int num_sms_current_device();
 

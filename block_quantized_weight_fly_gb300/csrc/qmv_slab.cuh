@@ -4,25 +4,41 @@
 // A consumer warp w owns rows 16w .. 16w+15 of the slab. The inner product runs
 // on mma.sync m16n8k16 with the weight rows as the 16-row A operand; the weights
 // are decoded in registers straight into A fragments:
-//   K-quants -> bf16:  one AND-OR per two 4-bit fields gives {128 + q_lo, 128 + q_hi}
-//                      exactly (the packed layout stores element pairs at nibbles
-//                      (p, p+4) of each 32-bit word); the +128 offset is removed with
-//                      the per-block min term through X = sum x.
-//   NVFP4, FP8 -> f16: hardware cvt of FP4/FP8 pairs to f16x2 (exact); for NVFP4 the
-//                      E4M3 block scale is multiplied in with one exact f16x2 multiply.
+//   Q4_K, Q6_K -> bf16: masks alone turn element pairs into exact bf16 values
+//                      {q, q'} x 2^-133 .. 2^-127 through bf16's linear (subnormal and
+//                      first normal) range; x is scaled by a power of two so that
+//                      every product lands at one scale (see the Q4_K and Q6_K notes).
+//   Q5_K, Q8_0 -> bf16: one AND-OR per two fields gives {128 + q, 128 + q'} exactly
+//                      (element pairs at fields (p, p+4) of each 32-bit word); the
+//                      +128 offset is removed with the per-block term through X = sum x.
+//   NVFP4, FP8 -> f16: hardware cvt of FP4/FP8 pairs to f16x2 (exact).
 // Products of these small exact values with the activations are exact and the
 // tensor core accumulates in fp32.
 //
 // The 8 columns of the mma output are used in one of two ways:
-//   M = 1 ("unit columns"): column n holds the partial sum of sub-block (unit) n
-//     of the slab. A thread's B registers carry activations only for its own unit,
-//     zero elsewhere, so one accumulator collects all 8 units' partial sums at once
-//     and each block scale is applied once per slab. A thread (g, t) ends with the
-//     partial sums of rows g, g+8 over units 2t, 2t+1; the four threads of a quad
-//     are added at the end of the row tile.
-//   M = 2..8 ("token columns"): column n is token n; each 32-value sub-block gets
-//     its own accumulator and its scale is applied per sub-block. Thread (g, t)
-//     holds rows g, g+8 x tokens 2t, 2t+1.
+//   M = 1 ("unit columns"): column n holds the partial sum of one unit (sub-block
+//     or block) of the slab. A thread's B registers carry activations only for its
+//     own unit, zero elsewhere, so one accumulator collects the partial sums of 8
+//     units at once and each block scale is applied once per slab.
+//   M = 2..8 ("token columns"): column n is token n; each unit gets its own MMA
+//     chain started from zero.
+//
+// One accumulation order for every M (so that row m of an M-row call equals the
+// one-row call on x[m] bit for bit). The units of a slab are split among the four
+// threads t of an mma quad exactly as the unit columns place them: quad position t
+// owns the units of chunks 2t and 2t+1 (Q4_K, Q5_K, Q8_0, FP8: units 2t, 2t+1; Q6_K
+// units 4t .. 4t+3; NVFP4 blocks 4t .. 4t+3). Per output (row, token):
+//   * every unit sum is the same MMA chain over the same operands in both forms
+//     (in the unit-column form the other columns only add exact zeros);
+//   * c_t = the format's combination of position t's unit sums with their scales
+//     (the *_comb functions below, written with explicit roundings so that the
+//     compiler cannot contract them differently in the two forms);
+//   * A_t = the fp32 sum of c_t over the slabs of a piece, in k order;
+//   * the piece value is (A_0 + A_1) + (A_2 + A_3).
+// How pieces are formed and added up is the stream kernel's part (qmv_stream.cu).
+// The unit-column form adds a thread's own c_t (it is quad position t) and the
+// quad's four sums are joined with two shuffles; the token-column form keeps the
+// four sums A_0..A_3 of each of its outputs.
 #pragma once
 #include <cstdint>
 #include "qmv_layout.cuh"
@@ -157,43 +173,54 @@ __device__ __forceinline__ uint2 ldx64(const uint8_t* xs, bool mine, uint32_t of
 template <int FMT, int MT>
 struct Slab;
 
-// ============================================================================
-// Q4_K. w = a_j q - b_j (a_j = d sc_j, b_j = dmin m_j, sub-block j = 32 values);
-// with A = 128 + q: sum w x = a_j D_j - c_j X_j, c_j = 128 a_j + b_j.
-// ============================================================================
-__device__ __forceinline__ void q4k_pair_scales(const uint4 hd, int t, float* a, float* c) {
-  // sc_j, m_j of sub-blocks j = 2t, 2t+1 (12 consecutive bits each)
-  const float2 dd = h2x2f(hd.x);
-  const uint64_t lo = ((uint64_t)hd.z << 32) | hd.y, hi = ((uint64_t)hd.w << 32) | hd.z;
-  const uint32_t s = (uint32_t)(lo >> (12 * t)), m = (uint32_t)(hi >> (16 + 12 * t));
-  a[0] = dd.x * u6f(s);
-  a[1] = dd.x * u6f(s >> 6);
-  c[0] = fmaf(128.0f, a[0], dd.y * u6f(m));
-  c[1] = fmaf(128.0f, a[1], dd.y * u6f(m >> 6));
+// ---------------------------------------------------------------------------
+// Canonical combinations c_t of one quad position's unit sums (shared by both
+// forms; explicit roundings, no contraction)
+// ---------------------------------------------------------------------------
+// Q4_K and Q5_K over two 32-value sub-blocks: a_i D_i - b_i X_i
+__device__ __forceinline__ float kq_comb(float a0, float a1, float b0, float b1, float D0, float D1, float X0,
+                                         float X1) {
+  return __fmaf_rn(a0, D0, __fmaf_rn(a1, D1, -__fmaf_rn(b0, X0, __fmul_rn(b1, X1))));
 }
-// the same from a record in shared memory: the scale stream starts at byte 4 and
-// the fields of sub-blocks 2t, 2t+1 sit at stream bits 12t (sc) and 48 + 12t (m);
-// each pair is taken from two aligned 32-bit words with one funnel shift
-__device__ __forceinline__ void q4k_pair_scales_rec(const uint8_t* rec, int t, float* a, float* c) {
-  const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 4);
-  const int bs = 12 * t, bm = 48 + 12 * t;
-  const uint32_t s = __funnelshift_r(sw[bs >> 5], sw[(bs >> 5) + 1], bs & 31);
-  const uint32_t m = __funnelshift_r(sw[bm >> 5], sw[(bm >> 5) + 1], bm & 31);
-  const float2 dd = h2x2f(*reinterpret_cast<const uint32_t*>(rec));
-  a[0] = dd.x * u6f(s);
-  a[1] = dd.x * u6f(s >> 6);
-  c[0] = fmaf(128.0f, a[0], dd.y * u6f(m));
-  c[1] = fmaf(128.0f, a[1], dd.y * u6f(m >> 6));
+// Q8_0: sum q x of one 32-value chunk = lo + 16 hi - 2304 X (fields taken as 128 + nibble)
+__device__ __forceinline__ float q80_part(float lo, float hi, float X) {
+  return __fmaf_rn(-2304.0f, X, __fmaf_rn(16.0f, hi, lo));
 }
+__device__ __forceinline__ float q80_comb(float d0, float d1, float lo0, float hi0, float X0, float lo1, float hi1,
+                                          float X1) {
+  return __fmaf_rn(d0, q80_part(lo0, hi0, X0), __fmul_rn(d1, q80_part(lo1, hi1, X1)));
+}
+// Q6_K: one 16-value unit folded into v; a66 = d sc 2^66, m32 = -32 d sc
+__device__ __forceinline__ float q6k_step(float v, float a66, float m32, float lo, float hi, float X) {
+  return __fmaf_rn(a66, __fadd_rn(lo, hi), __fmaf_rn(m32, X, v));
+}
+__device__ __forceinline__ float q6k_a66(float a) { return __fmul_rn(a, 7.3786976294838206e19f); }  // exact
+__device__ __forceinline__ float q6k_m32(float a) { return __fmul_rn(-32.0f, a); }                 // exact
+// NVFP4: four 16-value blocks with their E4M3 scales
+__device__ __forceinline__ float nv_comb(float s0, float s1, float s2, float s3, float B0, float B1, float B2,
+                                         float B3) {
+  return __fmaf_rn(s0, B0, __fmaf_rn(s1, B1, __fmaf_rn(s2, B2, __fmul_rn(s3, B3))));
+}
+// FP8: two chunk sums (the row scale multiplies the row's total)
+__device__ __forceinline__ float fp8_comb(float D0, float D1) { return __fadd_rn(D0, D1); }
+// the piece value from the four quad positions' sums
+__device__ __forceinline__ float quad_join(float a0, float a1, float a2, float a3) {
+  return __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3));
+}
+// the token-column form adds c into A_t of output e
+__device__ __forceinline__ void tc_add(float (&a)[4][4], int t, int e, float c) { a[t][e] = __fadd_rn(a[t][e], c); }
 
-// M = 1 decodes through bf16's linear range instead: the bit patterns 0..255 of a
-// bf16 are exactly the values 0..255 x 2^-133 (subnormals and the first normal
-// binade), so a word masked with 0x000F000F gives {q, q'} x 2^-133 and masked with
-// 0x00F000F0 gives {q, q'} x 2^-129 -- no shift for two of the four pairs and no
-// +128 offset. The activations are scaled by 2^67 (low-nibble pairs) or 2^63
-// (high-nibble pairs) with one exact bf16x2 multiply each, so every product is
-// q x 2^-66: a normal fp32 value for 2^-60 <= |x| < 2^61 (the tensor core keeps
-// subnormal bf16 operands exactly). The sum is rescaled by 2^66 through a_j.
+// ============================================================================
+// Q4_K. w = a_j q - b_j (a_j = d sc_j, b_j = dmin m_j, sub-block j = 32 values).
+// Decoded through bf16's linear range: the bit patterns 0..255 of a bf16 are
+// exactly the values 0..255 x 2^-133 (subnormals and the first normal binade), so a
+// word masked with 0x000F000F gives {q, q'} x 2^-133 and masked with 0x00F000F0
+// gives {q, q'} x 2^-129 -- no shift for two of the four pairs and no offset. The
+// activations are scaled by 2^67 (low-nibble pairs) or 2^63 (high-nibble pairs)
+// with one exact bf16x2 multiply each, so every product is q x 2^-66: a normal fp32
+// value for 2^-60 <= |x| < 2^61 (the tensor core keeps subnormal bf16 operands
+// exactly). The sum is rescaled by 2^66 through a_j.
+// ============================================================================
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -204,22 +231,58 @@ constexpr uint32_t kX63 = 0x5F005F00u;   // bf16x2 {2^63, 2^63}
 constexpr uint32_t kX71 = 0x63006300u;   // bf16x2 {2^71, 2^71}
 constexpr uint32_t kX69 = 0x62006200u;   // bf16x2 {2^69, 2^69}
 constexpr uint32_t kX65 = 0x60006000u;   // bf16x2 {2^65, 2^65}
-// a_j x 2^66 and b_j for sub-blocks 2t, 2t+1 of a record in shared memory
-__device__ __forceinline__ void q4k_pair_scales_lin_rec(const uint8_t* rec, int t, float* a, float* b) {
+
+// sc_j, m_j of sub-blocks 2t, 2t+1 of a header (12 consecutive stream bits each):
+// from the header words in registers, or from a record in shared memory (the scale
+// stream starts at byte 4, the fields at stream bits 12t (sc) and 48 + 12t (m), each
+// pair taken from two aligned words with one funnel shift)
+__device__ __forceinline__ void q4k_fields(const uint4 hd, int t, uint32_t* s, uint32_t* m) {
+  const uint64_t lo = ((uint64_t)hd.z << 32) | hd.y, hi = ((uint64_t)hd.w << 32) | hd.z;
+  *s = (uint32_t)(lo >> (12 * t));
+  *m = (uint32_t)(hi >> (16 + 12 * t));
+}
+__device__ __forceinline__ void q4k_fields_rec(const uint8_t* rec, int t, uint32_t* s, uint32_t* m) {
   const uint32_t* sw = reinterpret_cast<const uint32_t*>(rec + 4);
   const int bs = 12 * t, bm = 48 + 12 * t;
-  const uint32_t s = __funnelshift_r(sw[bs >> 5], sw[(bs >> 5) + 1], bs & 31);
-  const uint32_t m = __funnelshift_r(sw[bm >> 5], sw[(bm >> 5) + 1], bm & 31);
-  const float2 dd = h2x2f(*reinterpret_cast<const uint32_t*>(rec));
-  const float d66 = dd.x * 7.3786976294838206e19f;      // d x 2^66 (exact)
-  a[0] = d66 * u6f(s);
-  a[1] = d66 * u6f(s >> 6);
-  b[0] = dd.y * u6f(m);
-  b[1] = dd.y * u6f(m >> 6);
+  *s = __funnelshift_r(sw[bs >> 5], sw[(bs >> 5) + 1], bs & 31);
+  *m = __funnelshift_r(sw[bm >> 5], sw[(bm >> 5) + 1], bm & 31);
+}
+// Q4_K: a_j x 2^66 and b_j (all products exact)
+__device__ __forceinline__ void q4k_scales_lin(uint32_t dw, uint32_t s, uint32_t m, float* a, float* b) {
+  const float2 dd = h2x2f(dw);
+  const float d66 = __fmul_rn(dd.x, 7.3786976294838206e19f);      // d x 2^66
+  a[0] = __fmul_rn(d66, u6f(s));
+  a[1] = __fmul_rn(d66, u6f(s >> 6));
+  b[0] = __fmul_rn(dd.y, u6f(m));
+  b[1] = __fmul_rn(dd.y, u6f(m >> 6));
+}
+// Q5_K (fields taken as 128 + q): a_j and c_j = 128 a_j + b_j (exact)
+__device__ __forceinline__ void q5k_scales(uint32_t dw, uint32_t s, uint32_t m, float* a, float* c) {
+  const float2 dd = h2x2f(dw);
+  a[0] = __fmul_rn(dd.x, u6f(s));
+  a[1] = __fmul_rn(dd.x, u6f(s >> 6));
+  c[0] = __fmaf_rn(128.0f, a[0], __fmul_rn(dd.y, u6f(m)));
+  c[1] = __fmaf_rn(128.0f, a[1], __fmul_rn(dd.y, u6f(m >> 6)));
+}
+
+// the sub-block sums of one Q4_K chunk of rows (g, g+8): words wa, wb (thread t's
+// 8 elements of each row), activations b (the same 8 positions, unscaled bf16)
+__device__ __forceinline__ void q4k_chunk_mma(float* d, uint32_t wa, uint32_t wb, const uint4 b) {
+  const uint32_t ha = wa >> 8, hb = wb >> 8;
+  mma_bf16(d, wa & 0x000F000Fu, wb & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x00F000F0u, bmul2(b.x, kX67),
+           bmul2(b.y, kX63));
+  mma_bf16(d, ha & 0x000F000Fu, hb & 0x000F000Fu, ha & 0x00F000F0u, hb & 0x00F000F0u, bmul2(b.z, kX67),
+           bmul2(b.w, kX63));
+}
+__device__ __forceinline__ void ones_mma(float* xx, const uint4 b) {
+  mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, b.x, b.y);
+  mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, b.z, b.w);
 }
 
 template <>
 struct Slab<F_Q4_K, 1> {
+  // unit j = chunk j in column j: even chunks accumulate in dE, odd ones in dO, so
+  // thread t's units 2t, 2t+1 are dE column 2t and dO column 2t+1
   __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int, int w, int lane,
                              float2*, float* acc) {
     const int g = lane >> 2, t = lane & 3;
@@ -231,85 +294,60 @@ struct Slab<F_Q4_K, 1> {
     load8(rB + q4k_word_off(t, 0), WB);
     float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t wa = WA[j], wb = WB[j], ha = wa >> 8, hb = wb >> 8;
-      const uint4 b = ldx128(xs, g == j, xo);
-      float* d = (j & 1) ? dO : dE;
-      mma_bf16(d, wa & 0x000F000Fu, wb & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x00F000F0u, bmul2(b.x, kX67),
-               bmul2(b.y, kX63));
-      mma_bf16(d, ha & 0x000F000Fu, hb & 0x000F000Fu, ha & 0x00F000F0u, hb & 0x00F000F0u, bmul2(b.z, kX67),
-               bmul2(b.w, kX63));
-    }
-    const uint4 xv = lds128v(xs + xo);
-    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
-    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+    for (int j = 0; j < 8; ++j) q4k_chunk_mma((j & 1) ? dO : dE, WA[j], WB[j], ldx128(xs, g == j, xo));
+    ones_mma(xx, lds128v(xs + xo));
+    uint32_t s, m;
     float aA[2], bA[2], aB[2], bB[2];
-    q4k_pair_scales_lin_rec(rA, t, aA, bA);
-    q4k_pair_scales_lin_rec(rB, t, aB, bB);
-    acc[0] += fmaf(aA[0], dE[0] + dO[0], fmaf(aA[1], dE[1] + dO[1], -fmaf(bA[0], xx[0], bA[1] * xx[1])));
-    acc[1] += fmaf(aB[0], dE[2] + dO[2], fmaf(aB[1], dE[3] + dO[3], -fmaf(bB[0], xx[2], bB[1] * xx[3])));
+    q4k_fields_rec(rA, t, &s, &m);
+    q4k_scales_lin(lds32(rA), s, m, aA, bA);
+    q4k_fields_rec(rB, t, &s, &m);
+    q4k_scales_lin(lds32(rB), s, m, aB, bB);
+    acc[0] = __fadd_rn(acc[0], kq_comb(aA[0], aA[1], bA[0], bA[1], dE[0], dO[1], xx[0], xx[1]));
+    acc[1] = __fadd_rn(acc[1], kq_comb(aB[0], aB[1], bB[0], bB[1], dE[2], dO[3], xx[2], xx[3]));
   }
 };
-
-// the same from the header words in registers (the M > 1 scale tables)
-__device__ __forceinline__ void q4k_pair_scales_lin(const uint4 hd, int t, float* a, float* b) {
-  const float2 dd = h2x2f(hd.x);
-  const uint64_t lo = ((uint64_t)hd.z << 32) | hd.y, hi = ((uint64_t)hd.w << 32) | hd.z;
-  const uint32_t s = (uint32_t)(lo >> (12 * t)), m = (uint32_t)(hi >> (16 + 12 * t));
-  const float d66 = dd.x * 7.3786976294838206e19f;      // d x 2^66 (exact)
-  a[0] = d66 * u6f(s);
-  a[1] = d66 * u6f(s >> 6);
-  b[0] = dd.y * u6f(m);
-  b[1] = dd.y * u6f(m >> 6);
-}
 
 template <>
 struct Slab<F_Q4_K, 8> {
   __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int R, int w, int lane,
-                             float2* tbl, float* acc) {
-    const int g = lane >> 2, t = lane & 3;
+                             float2* tbl, float (&a)[4][4]) {
+    const int g = lane >> 2, tq = lane & 3;
     {   // scale table of the warp's 16 rows: lane -> (row lane/2, sub-blocks 4h..4h+3)
       const int rl = lane >> 1, h = lane & 1;
       const uint4 hd = lds128v(st + (16 * w + rl) * 144);
-      float a[2], b[2];
-      q4k_pair_scales_lin(hd, 2 * h, a, b);
-      tbl[rl * kTblStride + 4 * h + 0] = make_float2(a[0], b[0]);
-      tbl[rl * kTblStride + 4 * h + 1] = make_float2(a[1], b[1]);
-      q4k_pair_scales_lin(hd, 2 * h + 1, a, b);
-      tbl[rl * kTblStride + 4 * h + 2] = make_float2(a[0], b[0]);
-      tbl[rl * kTblStride + 4 * h + 3] = make_float2(a[1], b[1]);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        uint32_t s, m;
+        float sa[2], sb[2];
+        q4k_fields(hd, 2 * h + p, &s, &m);
+        q4k_scales_lin(hd.x, s, m, sa, sb);
+        tbl[rl * kTblStride + 4 * h + 2 * p] = make_float2(sa[0], sb[0]);
+        tbl[rl * kTblStride + 4 * h + 2 * p + 1] = make_float2(sa[1], sb[1]);
+      }
     }
     __syncwarp();
-    uint32_t WA[8], WB[8];
-    load8(st + (16 * w + g) * 144 + q4k_word_off(t, 0), WA);
-    load8(st + (16 * w + g + 8) * 144 + q4k_word_off(t, 0), WB);
+    const uint8_t* wA = st + (16 * w + g) * 144 + q4k_word_off(tq, 0);
+    const uint8_t* wB = wA + 8 * 144;
     const bool has_x = g < R;
 #pragma unroll
-    for (int j0 = 0; j0 < 8; j0 += 4) {
-      float dd[4][4], xx[4][4];
+    for (int t = 0; t < 4; ++t) {
+      // the words of chunks 2t, 2t+1 only (fewer live registers than the whole slab's)
+      const uint2 WA = lds64(wA + 8 * t), WB = lds64(wB + 8 * t);
+      float dd[2][4], xx[2][4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < 2; ++q) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) dd[q][e] = xx[q][e] = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = j0 + q;
-        const uint32_t wa = WA[j], wb = WB[j], ha = wa >> 8, hb = wb >> 8;
-        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
-        mma_bf16(dd[q], wa & 0x000F000Fu, wb & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x00F000F0u,
-                 bmul2(xv.x, kX67), bmul2(xv.y, kX63));
-        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
-        mma_bf16(dd[q], ha & 0x000F000Fu, hb & 0x000F000Fu, ha & 0x00F000F0u, hb & 0x00F000F0u,
-                 bmul2(xv.z, kX67), bmul2(xv.w, kX63));
-        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+        const int j = 2 * t + q;
+        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * tq) : make_uint4(0u, 0u, 0u, 0u);
+        q4k_chunk_mma(dd[q], q ? WA.y : WA.x, q ? WB.y : WB.x, xv);
+        ones_mma(xx[q], xv);
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 sA = tbl[g * kTblStride + j0 + q], sB = tbl[(g + 8) * kTblStride + j0 + q];
-        acc[0] = fmaf(sA.x, dd[q][0], fmaf(-sA.y, xx[q][0], acc[0]));
-        acc[1] = fmaf(sA.x, dd[q][1], fmaf(-sA.y, xx[q][1], acc[1]));
-        acc[2] = fmaf(sB.x, dd[q][2], fmaf(-sB.y, xx[q][2], acc[2]));
-        acc[3] = fmaf(sB.x, dd[q][3], fmaf(-sB.y, xx[q][3], acc[3]));
+      for (int e = 0; e < 4; ++e) {
+        const int row = (e < 2) ? g : g + 8;
+        const float2 s0 = tbl[row * kTblStride + 2 * t], s1 = tbl[row * kTblStride + 2 * t + 1];
+        tc_add(a, t, e, kq_comb(s0.x, s1.x, s0.y, s1.y, dd[0][e], dd[1][e], xx[0][e], xx[1][e]));
       }
     }
     __syncwarp();
@@ -317,9 +355,10 @@ struct Slab<F_Q4_K, 8> {
 };
 
 // ============================================================================
-// Q5_K. The Q4_K scheme with q = 0..31: A = 128 + q is still exact in bf16, the
-// header (d, dmin, scale stream) is Q4_K's, and the pairs come from the 5-bit
-// words plus the chunk's nibble word (packed layout: qmv_layout.cuh).
+// Q5_K. The Q4_K header (d, dmin, scale stream) with q = 0..31 taken as the exact
+// bf16 value A = 128 + q; the pairs come from the 5-bit words plus the chunk's
+// nibble word (packed layout: qmv_layout.cuh). sum w x = a_j D_j - c_j X_j with
+// D_j = sum A x and c_j = 128 a_j + b_j.
 // ============================================================================
 // the four pairs {128 + q(8t+2p), 128 + q(8t+2p+1)} of a thread's 5-bit word v;
 // u = the chunk's nibble word already shifted right by 4t
@@ -328,6 +367,10 @@ __device__ __forceinline__ void q5k_quad(uint32_t v, uint32_t u, uint32_t* a) {
   a[1] = and_or(v >> 5, 0x001F001Fu, 0x43004300u);
   a[2] = and_or(v >> 10, 0x001F001Fu, 0x43004300u);
   a[3] = and_or(v >> 11, 0x00100010u, and_or(u, 0x000F000Fu, 0x43004300u));
+}
+__device__ __forceinline__ void q5k_chunk_mma(float* d, const uint32_t* pa, const uint32_t* pb, const uint4 b) {
+  mma_bf16(d, pa[0], pb[0], pa[1], pb[1], b.x, b.y);
+  mma_bf16(d, pa[2], pb[2], pa[3], pb[3], b.z, b.w);
 }
 
 template <>
@@ -350,75 +393,68 @@ struct Slab<F_Q5_K, 1> {
       uint32_t pa[4], pb[4];
       q5k_quad(WA[j], UA[j] >> us, pa);
       q5k_quad(WB[j], UB[j] >> us, pb);
-      const uint4 b = ldx128(xs, g == j, xo);
-      float* d = (j & 1) ? dO : dE;
-      mma_bf16(d, pa[0], pb[0], pa[1], pb[1], b.x, b.y);
-      mma_bf16(d, pa[2], pb[2], pa[3], pb[3], b.z, b.w);
+      q5k_chunk_mma((j & 1) ? dO : dE, pa, pb, ldx128(xs, g == j, xo));
     }
-    const uint4 xv = lds128v(xs + xo);
-    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
-    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+    ones_mma(xx, lds128v(xs + xo));
+    uint32_t s, m;
     float aA[2], cA[2], aB[2], cB[2];
-    q4k_pair_scales_rec(rA, t, aA, cA);
-    q4k_pair_scales_rec(rB, t, aB, cB);
-    acc[0] += fmaf(aA[0], dE[0] + dO[0], fmaf(aA[1], dE[1] + dO[1], -fmaf(cA[0], xx[0], cA[1] * xx[1])));
-    acc[1] += fmaf(aB[0], dE[2] + dO[2], fmaf(aB[1], dE[3] + dO[3], -fmaf(cB[0], xx[2], cB[1] * xx[3])));
+    q4k_fields_rec(rA, t, &s, &m);
+    q5k_scales(lds32(rA), s, m, aA, cA);
+    q4k_fields_rec(rB, t, &s, &m);
+    q5k_scales(lds32(rB), s, m, aB, cB);
+    acc[0] = __fadd_rn(acc[0], kq_comb(aA[0], aA[1], cA[0], cA[1], dE[0], dO[1], xx[0], xx[1]));
+    acc[1] = __fadd_rn(acc[1], kq_comb(aB[0], aB[1], cB[0], cB[1], dE[2], dO[3], xx[2], xx[3]));
   }
 };
 
 template <>
 struct Slab<F_Q5_K, 8> {
   __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int R, int w, int lane,
-                             float2* tbl, float* acc) {
-    const int g = lane >> 2, t = lane & 3;
+                             float2* tbl, float (&a)[4][4]) {
+    const int g = lane >> 2, tq = lane & 3;
     {   // scale table of the warp's 16 rows: lane -> (row lane/2, sub-blocks 4h..4h+3)
       const int rl = lane >> 1, h = lane & 1;
       const uint4 hd = lds128v(st + (16 * w + rl) * 176);
-      float a[2], c[2];
-      q4k_pair_scales(hd, 2 * h, a, c);
-      tbl[rl * kTblStride + 4 * h + 0] = make_float2(a[0], c[0]);
-      tbl[rl * kTblStride + 4 * h + 1] = make_float2(a[1], c[1]);
-      q4k_pair_scales(hd, 2 * h + 1, a, c);
-      tbl[rl * kTblStride + 4 * h + 2] = make_float2(a[0], c[0]);
-      tbl[rl * kTblStride + 4 * h + 3] = make_float2(a[1], c[1]);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        uint32_t s, m;
+        float sa[2], sc[2];
+        q4k_fields(hd, 2 * h + p, &s, &m);
+        q5k_scales(hd.x, s, m, sa, sc);
+        tbl[rl * kTblStride + 4 * h + 2 * p] = make_float2(sa[0], sc[0]);
+        tbl[rl * kTblStride + 4 * h + 2 * p + 1] = make_float2(sa[1], sc[1]);
+      }
     }
     __syncwarp();
     const uint8_t* rA = st + (16 * w + g) * 176;
     const uint8_t* rB = rA + 8 * 176;
-    uint32_t WA[8], WB[8];
-    load8(rA + q5k_word_off(t, 0), WA);
-    load8(rB + q5k_word_off(t, 0), WB);
-    const int us = 4 * t;
+    const int us = 4 * tq;
     const bool has_x = g < R;
 #pragma unroll
-    for (int j0 = 0; j0 < 8; j0 += 4) {
-      // the nibble words of these four chunks only (fewer live registers)
-      const uint4 ua = lds128v(rA + q5k_nib_off(j0)), ub = lds128v(rB + q5k_nib_off(j0));
-      const uint32_t UA[4] = {ua.x, ua.y, ua.z, ua.w}, UB[4] = {ub.x, ub.y, ub.z, ub.w};
-      float dd[4][4], xx[4][4];
+    for (int t = 0; t < 4; ++t) {
+      // the 5-bit and nibble words of chunks 2t, 2t+1 only (fewer live registers)
+      const uint2 wa = lds64(rA + q5k_word_off(tq, 2 * t)), wb = lds64(rB + q5k_word_off(tq, 2 * t));
+      const uint2 ua = lds64(rA + q5k_nib_off(2 * t)), ub = lds64(rB + q5k_nib_off(2 * t));
+      const uint32_t WA[2] = {wa.x, wa.y}, WB[2] = {wb.x, wb.y};
+      const uint32_t UA[2] = {ua.x, ua.y}, UB[2] = {ub.x, ub.y};
+      float dd[2][4], xx[2][4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < 2; ++q) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) dd[q][e] = xx[q][e] = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = j0 + q;
+        const int j = 2 * t + q;
         uint32_t pa[4], pb[4];
-        q5k_quad(WA[j], UA[q] >> us, pa);
-        q5k_quad(WB[j], UB[q] >> us, pb);
-        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
-        mma_bf16(dd[q], pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
-        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
-        mma_bf16(dd[q], pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
-        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+        q5k_quad(WA[q], UA[q] >> us, pa);
+        q5k_quad(WB[q], UB[q] >> us, pb);
+        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * tq) : make_uint4(0u, 0u, 0u, 0u);
+        q5k_chunk_mma(dd[q], pa, pb, xv);
+        ones_mma(xx[q], xv);
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 sA = tbl[g * kTblStride + j0 + q], sB = tbl[(g + 8) * kTblStride + j0 + q];
-        acc[0] = fmaf(sA.x, dd[q][0], fmaf(-sA.y, xx[q][0], acc[0]));
-        acc[1] = fmaf(sA.x, dd[q][1], fmaf(-sA.y, xx[q][1], acc[1]));
-        acc[2] = fmaf(sB.x, dd[q][2], fmaf(-sB.y, xx[q][2], acc[2]));
-        acc[3] = fmaf(sB.x, dd[q][3], fmaf(-sB.y, xx[q][3], acc[3]));
+      for (int e = 0; e < 4; ++e) {
+        const int row = (e < 2) ? g : g + 8;
+        const float2 s0 = tbl[row * kTblStride + 2 * t], s1 = tbl[row * kTblStride + 2 * t + 1];
+        tc_add(a, t, e, kq_comb(s0.x, s1.x, s0.y, s1.y, dd[0][e], dd[1][e], xx[0][e], xx[1][e]));
       }
     }
     __syncwarp();
@@ -426,11 +462,19 @@ struct Slab<F_Q5_K, 8> {
 };
 
 // ============================================================================
-// Q8_0. q = u - 128 with u = 16 uh + ul; D_lo / D_hi over (128 + ul) / (128 + uh):
-// sum q x = D_lo + 16 D_hi - 2304 X; w = d q (d per 32-value chunk).
+// Q8_0. q = u - 128 with u = 16 uh + ul; lo / hi over (128 + ul) / (128 + uh):
+// sum q x = lo + 16 hi - 2304 X; w = d q (d per 32-value chunk).
 // ============================================================================
+__device__ __forceinline__ void q80_chunk_mma(float* lo, float* hi, uint2 wa, uint2 wb, const uint4 b) {
+  mma_bf16(lo, nib_pair(wa.x, 0), nib_pair(wb.x, 0), nib_pair(wa.x, 1), nib_pair(wb.x, 1), b.x, b.y);
+  mma_bf16(hi, nib_pair(wa.x, 2), nib_pair(wb.x, 2), nib_pair(wa.x, 3), nib_pair(wb.x, 3), b.x, b.y);
+  mma_bf16(lo, nib_pair(wa.y, 0), nib_pair(wb.y, 0), nib_pair(wa.y, 1), nib_pair(wb.y, 1), b.z, b.w);
+  mma_bf16(hi, nib_pair(wa.y, 2), nib_pair(wb.y, 2), nib_pair(wa.y, 3), nib_pair(wb.y, 3), b.z, b.w);
+}
+
 template <>
 struct Slab<F_Q8_0, 1> {
+  // unit j = chunk j in column j of the single lo / hi / X accumulators
   __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int, int w, int lane,
                              float2*, float* acc) {
     const int g = lane >> 2, t = lane & 3;
@@ -442,72 +486,44 @@ struct Slab<F_Q8_0, 1> {
     load16(rB + q80_word_off(t, 0), WB);
     float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint2 wa = make_uint2(WA[2 * j], WA[2 * j + 1]), wb = make_uint2(WB[2 * j], WB[2 * j + 1]);
-      const uint4 bv = ldx128(xs, g == j, xo);
-      const uint32_t b0 = bv.x, b1 = bv.y, b2 = bv.z, b3 = bv.w;
-      mma_bf16(lo, nib_pair(wa.x, 0), nib_pair(wb.x, 0), nib_pair(wa.x, 1), nib_pair(wb.x, 1), b0, b1);
-      mma_bf16(hi, nib_pair(wa.x, 2), nib_pair(wb.x, 2), nib_pair(wa.x, 3), nib_pair(wb.x, 3), b0, b1);
-      mma_bf16(lo, nib_pair(wa.y, 0), nib_pair(wb.y, 0), nib_pair(wa.y, 1), nib_pair(wb.y, 1), b2, b3);
-      mma_bf16(hi, nib_pair(wa.y, 2), nib_pair(wb.y, 2), nib_pair(wa.y, 3), nib_pair(wb.y, 3), b2, b3);
-    }
-    const uint4 xv = lds128v(xs + xo);
-    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
-    mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
-    const uint32_t dA = lds32(rA + 4 * t), dB = lds32(rB + 4 * t);     // d of chunks 2t, 2t+1
-    const float2 da = h2x2f(dA), db = h2x2f(dB);
-    const float a0 = da.x, a1 = da.y, b0 = db.x, b1 = db.y;
-    acc[0] += fmaf(a0, fmaf(16.f, hi[0], lo[0]) - 2304.f * xx[0], a1 * (fmaf(16.f, hi[1], lo[1]) - 2304.f * xx[1]));
-    acc[1] += fmaf(b0, fmaf(16.f, hi[2], lo[2]) - 2304.f * xx[2], b1 * (fmaf(16.f, hi[3], lo[3]) - 2304.f * xx[3]));
+    for (int j = 0; j < 8; ++j)
+      q80_chunk_mma(lo, hi, make_uint2(WA[2 * j], WA[2 * j + 1]), make_uint2(WB[2 * j], WB[2 * j + 1]),
+                    ldx128(xs, g == j, xo));
+    ones_mma(xx, lds128v(xs + xo));
+    const float2 da = h2x2f(lds32(rA + 4 * t)), db = h2x2f(lds32(rB + 4 * t));     // d of chunks 2t, 2t+1
+    acc[0] = __fadd_rn(acc[0], q80_comb(da.x, da.y, lo[0], hi[0], xx[0], lo[1], hi[1], xx[1]));
+    acc[1] = __fadd_rn(acc[1], q80_comb(db.x, db.y, lo[2], hi[2], xx[2], lo[3], hi[3], xx[3]));
   }
 };
 
 template <>
 struct Slab<F_Q8_0, 8> {
   __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int R, int w, int lane,
-                             float2* tbl, float* acc) {
-    const int g = lane >> 2, t = lane & 3;
-    {
-      const int rl = lane >> 1, h = lane & 1;
-      const uint2 dv = lds64(st + (16 * w + rl) * 272 + 8 * h);
-      const uint32_t dw[2] = {dv.x, dv.y};
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const float d = h2f(dw[jj >> 1] >> (16 * (jj & 1)));
-        tbl[rl * kTblStride + 4 * h + jj] = make_float2(d, 2304.0f * d);
-      }
-    }
-    __syncwarp();
-    uint32_t WA[16], WB[16];
-    load16(st + (16 * w + g) * 272 + q80_word_off(t, 0), WA);
-    load16(st + (16 * w + g + 8) * 272 + q80_word_off(t, 0), WB);
+                             float2*, float (&a)[4][4]) {
+    const int g = lane >> 2, tq = lane & 3;
+    const uint8_t* rA = st + (16 * w + g) * 272;
+    const uint8_t* rB = rA + 8 * 272;
     const bool has_x = g < R;
 #pragma unroll
-    for (int j0 = 0; j0 < 8; j0 += 2) {
+    for (int t = 0; t < 4; ++t) {
+      // the words of chunks 2t, 2t+1 only (fewer live registers than the whole slab's)
+      const uint4 WA = lds128v(rA + q80_word_off(tq, 2 * t)), WB = lds128v(rB + q80_word_off(tq, 2 * t));
       float lo[2][4], hi[2][4], xx[2][4];
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < 2; ++q) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) lo[q][e] = hi[q][e] = xx[q][e] = 0.f;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int j = j0 + q;
-        const uint2 wa = make_uint2(WA[2 * j], WA[2 * j + 1]), wb = make_uint2(WB[2 * j], WB[2 * j + 1]);
-        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
-        mma_bf16(lo[q], nib_pair(wa.x, 0), nib_pair(wb.x, 0), nib_pair(wa.x, 1), nib_pair(wb.x, 1), xv.x, xv.y);
-        mma_bf16(hi[q], nib_pair(wa.x, 2), nib_pair(wb.x, 2), nib_pair(wa.x, 3), nib_pair(wb.x, 3), xv.x, xv.y);
-        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
-        mma_bf16(lo[q], nib_pair(wa.y, 0), nib_pair(wb.y, 0), nib_pair(wa.y, 1), nib_pair(wb.y, 1), xv.z, xv.w);
-        mma_bf16(hi[q], nib_pair(wa.y, 2), nib_pair(wb.y, 2), nib_pair(wa.y, 3), nib_pair(wb.y, 3), xv.z, xv.w);
-        mma_bf16(xx[q], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.z, xv.w);
+        const int j = 2 * t + q;
+        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * tq) : make_uint4(0u, 0u, 0u, 0u);
+        q80_chunk_mma(lo[q], hi[q], q ? make_uint2(WA.z, WA.w) : make_uint2(WA.x, WA.y),
+                      q ? make_uint2(WB.z, WB.w) : make_uint2(WB.x, WB.y), xv);
+        ones_mma(xx[q], xv);
       }
+      const float2 da = h2x2f(lds32(rA + 4 * t)), db = h2x2f(lds32(rB + 4 * t));   // d of chunks 2t, 2t+1
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const float2 sA = tbl[g * kTblStride + j0 + q], sB = tbl[(g + 8) * kTblStride + j0 + q];
-        acc[0] = fmaf(sA.x, fmaf(16.f, hi[q][0], lo[q][0]), fmaf(-sA.y, xx[q][0], acc[0]));
-        acc[1] = fmaf(sA.x, fmaf(16.f, hi[q][1], lo[q][1]), fmaf(-sA.y, xx[q][1], acc[1]));
-        acc[2] = fmaf(sB.x, fmaf(16.f, hi[q][2], lo[q][2]), fmaf(-sB.y, xx[q][2], acc[2]));
-        acc[3] = fmaf(sB.x, fmaf(16.f, hi[q][3], lo[q][3]), fmaf(-sB.y, xx[q][3], acc[3]));
+      for (int e = 0; e < 4; ++e) {
+        const float2 d = (e < 2) ? da : db;
+        tc_add(a, t, e, q80_comb(d.x, d.y, lo[0][e], hi[0][e], xx[0][e], lo[1][e], hi[1][e], xx[1][e]));
       }
     }
     __syncwarp();
@@ -515,17 +531,16 @@ struct Slab<F_Q8_0, 8> {
 };
 
 // ============================================================================
-// Q6_K. q = ql + 16 qh, w = a_u (q - 32), a_u = d sc_u per 16-value sub-block u;
-// sum w x = a_u (D_lo + 16 D_hi - 2208 X). k-step s of chunk j covers sub-block
-// u = 2j + s; the thread's slots hold elements 16s + 4t .. 16s + 4t + 3 of chunk j.
+// Q6_K. q = ql + 16 qh, w = a_u (q - 32), a_u = d sc_u per 16-value unit u = 2j + s
+// (chunk j, half s). Through bf16's linear range: the low nibbles of pair p of an
+// ql word sit at nibbles (p, p+4), their 2-bit highs at bits (2k, 2k+16) of the
+// thread's qh word (k = p), so masks alone give exact bf16 values {v, v'} x
+// 2^(s - 133): s = 0, 4 for nibble pairs 0, 1 (pairs 2, 3 after one shift by 8) and
+// s = 0, 2, 4, 6 for the 2-bit pairs. x is scaled per k position to bring every
+// product to (lo + 16 hi) x 2^-66, so the lo and hi MMAs add into sums of one scale:
+// lo gets x 2^67 | 2^63, hi x 2^71 | 2^69 (pairs 0, 1) and x 2^67 | 2^65 (pairs 2, 3).
+// Exact for |x| < 2^56. sum w x = a_u 2^66 (lo + hi) - 32 a_u X.
 // ============================================================================
-// Q6_K through bf16's linear range: the low nibbles of pair p of an ql word sit at
-// nibbles (p, p+4), their 2-bit highs at bits (2k, 2k+16) of the thread's qh word (k = p),
-// so masks alone give exact bf16 values {v, v'} x 2^(s - 133): s = 0, 4 for nibble pairs
-// 0, 1 (pairs 2, 3 after one shift by 8) and s = 0, 2, 4, 6 for the 2-bit pairs. x is
-// scaled per k position to bring every product to (lo + 16 hi) x 2^-66, so the lo and hi
-// MMAs add into sums of one scale: lo gets x 2^67 | 2^63, hi x 2^71 | 2^69 (pairs 0, 1)
-// and x 2^67 | 2^65 (pairs 2, 3). Exact for |x| < 2^56.
 __device__ __forceinline__ void q6k_linear_mma(float* lo, float* hi, uint32_t la, uint32_t lb, uint32_t ha,
                                                uint32_t hb, int s2, uint2 xv) {
   if (s2 == 0) {
@@ -541,11 +556,15 @@ __device__ __forceinline__ void q6k_linear_mma(float* lo, float* hi, uint32_t la
              bmul2(xv.y, kX65));
   }
 }
+__device__ __forceinline__ void ones_mma64(float* xx, const uint2 b) {
+  mma_bf16(xx, kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, b.x, b.y);
+}
 
 template <>
 struct Slab<F_Q6_K, 1> {
-  // 16 units (sub-blocks): units 0..7 -> accumulator group 0, 8..15 -> group 1,
-  // column n = u % 8. Thread (g', t) carries activations for units g' and g' + 8.
+  // Unit u = 2j + s sits in accumulator group j & 1, column 2(j >> 1) + s, so thread
+  // t's columns 2t, 2t+1 hold the units of chunks 2t (group 0) and 2t+1 (group 1):
+  // units 4t .. 4t+3. Thread (g', t) carries the activations of the unit in column g'.
   __device__ static void run(const uint8_t* st, const uint8_t* dplane, const uint8_t* xs, int, int w,
                              int lane, float2*, float* acc) {
     const int g = lane >> 2, t = lane & 3;
@@ -553,9 +572,9 @@ struct Slab<F_Q6_K, 1> {
     const uint8_t* rA = st + rowA * 208;
     const uint8_t* rB = st + rowB * 208;
     const int hsh = 8 * (t & 1);
-    // unit g' = 2j' + s': chunk j' = g'/2, s' = g' & 1; unit g' + 8: chunk j' + 4
-    const uint2 x0 = lds64(xs + 64 * (g >> 1) + 32 * (g & 1) + 8 * t);
-    const uint2 x1 = lds64(xs + 64 * ((g >> 1) + 4) + 32 * (g & 1) + 8 * t);
+    // column g of group q: chunk 2(g >> 1) + q, half g & 1
+    const uint2 x0 = lds64(xs + 128 * (g >> 1) + 32 * (g & 1) + 8 * t);
+    const uint2 x1 = lds64(xs + 128 * (g >> 1) + 64 + 32 * (g & 1) + 8 * t);
     uint32_t LA[8], LB[8], HA[8], HB[8];
     load8(rA + q6k_ql_word_off(t, 0), LA);
     load8(rB + q6k_ql_word_off(t, 0), LB);
@@ -568,49 +587,40 @@ struct Slab<F_Q6_K, 1> {
       for (int e = 0; e < 4; ++e) lo[q][e] = hi[q][e] = xx[q][e] = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint32_t la = LA[j], lb = LB[j];
-      const uint32_t ha = HA[j] >> hsh;
-      const uint32_t hb = HB[j] >> hsh;
-      const int grp = j >> 2;
+      const uint32_t ha = HA[j] >> hsh, hb = HB[j] >> hsh;
 #pragma unroll
       for (int s2 = 0; s2 < 2; ++s2) {
-        const int u = 2 * j + s2;
-        const uint2 xv = ldx64(xs, (u & 7) == g, 32 * u + 8 * t);
-        q6k_linear_mma(lo[grp], hi[grp], la, lb, ha, hb, s2, xv);
+        const uint2 xv = ldx64(xs, (2 * (j >> 1) + s2) == g, 64 * j + 32 * s2 + 8 * t);
+        q6k_linear_mma(lo[j & 1], hi[j & 1], LA[j], LB[j], ha, hb, s2, xv);
       }
     }
-    mma_bf16(xx[0], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, x0.x, x0.y);
-    mma_bf16(xx[1], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, x1.x, x1.y);
-    // this thread's columns 2t, 2t+1 -> units {2t, 2t+1} (group 0), {8+2t, 9+2t} (group 1)
+    ones_mma64(xx[0], x0);
+    ones_mma64(xx[1], x1);
     const float dA = h2f(*reinterpret_cast<const unsigned short*>(dplane + 2 * rowA));
     const float dB = h2f(*reinterpret_cast<const unsigned short*>(dplane + 2 * rowB));
-    const uint32_t sA0 = *reinterpret_cast<const unsigned short*>(rA + 192 + 2 * t);
-    const uint32_t sA1 = *reinterpret_cast<const unsigned short*>(rA + 200 + 2 * t);
-    const uint32_t sB0 = *reinterpret_cast<const unsigned short*>(rB + 192 + 2 * t);
-    const uint32_t sB1 = *reinterpret_cast<const unsigned short*>(rB + 200 + 2 * t);
+    const uint32_t scA = lds32(rA + 192 + 4 * t), scB = lds32(rB + 192 + 4 * t);   // units 4t .. 4t+3
     float vA = 0.f, vB = 0.f;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const uint32_t scA = q ? sA1 : sA0, scB = q ? sB1 : sB0;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float aa = dA * i8f(scA >> (8 * e)), ab = dB * i8f(scB >> (8 * e));
-        // sum (q - 32) x = 2^66 (lo + hi) - 32 sum x
-        vA = fmaf(aa * 7.3786976294838206e19f, lo[q][e] + hi[q][e], fmaf(-32.f * aa, xx[q][e], vA));
-        vB = fmaf(ab * 7.3786976294838206e19f, lo[q][2 + e] + hi[q][2 + e], fmaf(-32.f * ab, xx[q][2 + e], vB));
+        const int k = 2 * q + e;
+        const float aa = __fmul_rn(dA, i8f(scA >> (8 * k))), ab = __fmul_rn(dB, i8f(scB >> (8 * k)));
+        vA = q6k_step(vA, q6k_a66(aa), q6k_m32(aa), lo[q][e], hi[q][e], xx[q][e]);
+        vB = q6k_step(vB, q6k_a66(ab), q6k_m32(ab), lo[q][2 + e], hi[q][2 + e], xx[q][2 + e]);
       }
     }
-    acc[0] += vA;
-    acc[1] += vB;
+    acc[0] = __fadd_rn(acc[0], vA);
+    acc[1] = __fadd_rn(acc[1], vB);
   }
 };
 
 template <>
 struct Slab<F_Q6_K, 8> {
   __device__ static void run(const uint8_t* st, const uint8_t* dplane, const uint8_t* xs, int R, int w,
-                             int lane, float2* tbl, float* acc) {
-    const int g = lane >> 2, t = lane & 3;
-    {
+                             int lane, float2* tbl, float (&a)[4][4]) {
+    const int g = lane >> 2, tq = lane & 3;
+    {   // scale table of the warp's 16 rows: lane -> (row lane/2, units 8h..8h+7)
       const int rl = lane >> 1, h = lane & 1;
       const int row = 16 * w + rl;
       const float d = h2f(*reinterpret_cast<const unsigned short*>(dplane + 2 * row));
@@ -618,86 +628,67 @@ struct Slab<F_Q6_K, 8> {
       const uint32_t sw[2] = {sv.x, sv.y};
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
-        const float a = d * i8f(sw[jj >> 2] >> (8 * (jj & 3)));
-        tbl[rl * kTblStride + 8 * h + jj] = make_float2(a * 7.3786976294838206e19f, 32.0f * a);
+        const float av = __fmul_rn(d, i8f(sw[jj >> 2] >> (8 * (jj & 3))));
+        tbl[rl * kTblStride + 8 * h + jj] = make_float2(q6k_a66(av), q6k_m32(av));
       }
     }
     __syncwarp();
     const uint8_t* rA = st + (16 * w + g) * 208;
     const uint8_t* rB = rA + 8 * 208;
-    const int hsh = 8 * (t & 1);
+    const int hsh = 8 * (tq & 1);
     const bool has_x = g < R;
-    uint32_t LA[8], LB[8], HA[8], HB[8];
-    load8(rA + q6k_ql_word_off(t, 0), LA);
-    load8(rB + q6k_ql_word_off(t, 0), LB);
-    load8(rA + q6k_qh_word_off(t >> 1, 0), HA);
-    load8(rB + q6k_qh_word_off(t >> 1, 0), HB);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t la = LA[j], lb = LB[j];
-      const uint32_t ha = HA[j] >> hsh;
-      const uint32_t hb = HB[j] >> hsh;
-      float lo[2][4], hi[2][4], xx[2][4];
+    for (int t = 0; t < 4; ++t) {
+      // the words of chunks 2t, 2t+1 only (fewer live registers than the whole slab's)
+      const uint2 la2 = lds64(rA + q6k_ql_word_off(tq, 2 * t)), lb2 = lds64(rB + q6k_ql_word_off(tq, 2 * t));
+      const uint2 ha2 = lds64(rA + q6k_qh_word_off(tq >> 1, 2 * t)), hb2 = lds64(rB + q6k_qh_word_off(tq >> 1, 2 * t));
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < 2; ++q) {
+        const int j = 2 * t + q;
+        const uint32_t la = q ? la2.y : la2.x, lb = q ? lb2.y : lb2.x;
+        const uint32_t ha = (q ? ha2.y : ha2.x) >> hsh, hb = (q ? hb2.y : hb2.x) >> hsh;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) lo[q][e] = hi[q][e] = xx[q][e] = 0.f;
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const int u = 2 * j + s2;
+          const uint2 xv = has_x ? lds64(xs + 64 * j + 32 * s2 + 8 * tq) : make_uint2(0u, 0u);
+          float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};
+          q6k_linear_mma(lo, hi, la, lb, ha, hb, s2, xv);
+          ones_mma64(xx, xv);
 #pragma unroll
-      for (int s2 = 0; s2 < 2; ++s2) {
-        const uint2 xv = has_x ? lds64(xs + 64 * j + 32 * s2 + 8 * t) : make_uint2(0u, 0u);
-        q6k_linear_mma(lo[s2], hi[s2], la, lb, ha, hb, s2, xv);
-        mma_bf16(xx[s2], kOnesBf16, kOnesBf16, kOnesBf16, kOnesBf16, xv.x, xv.y);
+          for (int e = 0; e < 4; ++e) {
+            const float2 s = tbl[((e < 2) ? g : g + 8) * kTblStride + u];
+            v[e] = q6k_step(v[e], s.x, s.y, lo[e], hi[e], xx[e]);
+          }
+        }
       }
 #pragma unroll
-      for (int s2 = 0; s2 < 2; ++s2) {
-        const float2 sA = tbl[g * kTblStride + 2 * j + s2], sB = tbl[(g + 8) * kTblStride + 2 * j + s2];
-        acc[0] = fmaf(sA.x, lo[s2][0] + hi[s2][0], fmaf(-sA.y, xx[s2][0], acc[0]));
-        acc[1] = fmaf(sA.x, lo[s2][1] + hi[s2][1], fmaf(-sA.y, xx[s2][1], acc[1]));
-        acc[2] = fmaf(sB.x, lo[s2][2] + hi[s2][2], fmaf(-sB.y, xx[s2][2], acc[2]));
-        acc[3] = fmaf(sB.x, lo[s2][3] + hi[s2][3], fmaf(-sB.y, xx[s2][3], acc[3]));
-      }
+      for (int e = 0; e < 4; ++e) tc_add(a, t, e, v[e]);
     }
     __syncwarp();
   }
 };
 
 // ============================================================================
-// NVFP4. A = e2m1(c) * s_b in f16 (exact), B = x in f16; s_T in the epilogue.
+// NVFP4. The codes go to the MMA as plain e2m1 values (f16) and each 16-value
+// block's E4M3 scale multiplies the block sum in fp32; s_T in the epilogue.
 // The codes of row r, K chunk j sit in the tensor-core tile at
-// (r/8)*1024 + j*128 + (r%8)*16 (thread t reads word t: elements 8t..8t+7); the
-// scales of the row's four blocks of K step ks are one 32-bit word of plane B at
-// ks*512 + 16*(r%32) + 4*(r/32); chunk j uses block 2(j%2) + t/2 of step j/2.
+// (r/8)*1024 + j*128 + (r%8)*16 (thread t reads word t: elements 8t..8t+7, all of
+// block t/2 of the chunk); the scales of the row's four blocks of K step ks are one
+// 32-bit word of plane B at ks*512 + 16*(r%32) + 4*(r/32). The blocks of chunks 2t,
+// 2t+1 (blocks 4t .. 4t+3) are K step t.
 // ============================================================================
-__device__ __forceinline__ void nv_load(const uint8_t* st, const uint8_t* sf, int r, int t, uint32_t* C,
-                                        uint32_t* S) {
-  const uint8_t* c = st + (r >> 3) * 1024 + (r & 7) * 16 + 4 * t;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) C[j] = lds32(c + 128 * j);
-  const uint8_t* s = sf + 16 * (r & 31) + 4 * (r >> 5);
-#pragma unroll
-  for (int ks = 0; ks < 4; ++ks) S[ks] = lds32(s + 512 * ks);
-}
-// the E4M3 scale byte of chunk j for thread t
-__device__ __forceinline__ uint32_t nv_sbyte(const uint32_t* S, int j, int t) {
-  return (S[j >> 1] >> (8 * (2 * (j & 1) + (t >> 1)))) & 0xFFu;
-}
-__device__ __forceinline__ void nv_frag(uint32_t code_word, uint32_t sbyte, uint32_t* p) {
-  const uint32_t s = e4m3x2_f16(sbyte | (sbyte << 8));
-  e2m1x4_f16(code_word, p);
-  p[0] = hmul2(p[0], s);
-  p[1] = hmul2(p[1], s);
-  p[2] = hmul2(p[2], s);
-  p[3] = hmul2(p[3], s);
+__device__ __forceinline__ uint32_t nv_code_word_addr_off(int r, int t) { return (r >> 3) * 1024 + (r & 7) * 16 + 4 * t; }
+__device__ __forceinline__ uint32_t nv_scale_word_off(int r, int ks) {
+  return 512 * ks + 16 * (r & 31) + 4 * (r >> 5);
 }
 
-// M = 1: block-separated unit columns. Chunk j's two 16-value blocks land in
-// columns 2(j/2) and 2(j/2) + 1 of accumulator set j%2, so each of a row's 16
-// blocks in the slab keeps its own output slot; the codes go to the MMA as plain
-// e2m1 values and each block's E4M3 scale multiplies its sum once, after the MMAs.
-// Column c is fed by lanes (c, t): x of chunk pair c/2, and only from the lanes
-// whose k positions hold block c%2 of the chunk (t/2 == c%2); other lanes feed 0.
-// Lane (g, t) ends with blocks 4t..4t+3 of rows g and g + 8 -- K step t of the
-// scale plane, one 32-bit word per row.
+// M = 1: block-separated unit columns. Chunk j's two blocks land in columns
+// 2(j/2) and 2(j/2) + 1 of accumulator set j%2, so each of a row's 16 blocks in the
+// slab keeps its own output slot. Column c is fed by lanes (c, t): x of chunk pair
+// c/2, and only from the lanes whose k positions hold block c%2 of the chunk
+// (t/2 == c%2); other lanes feed 0. Lane (g, t) ends with blocks 4t..4t+3 of rows g
+// and g + 8: dE columns 2t, 2t+1 (chunk 2t) and dO columns 2t, 2t+1 (chunk 2t+1).
 template <>
 struct Slab<F_NVFP4, 1> {
   __device__ static void run(const uint8_t* st, const uint8_t* sf, const uint8_t* xs, int, int w, int lane,
@@ -721,15 +712,14 @@ struct Slab<F_NVFP4, 1> {
     }
     uint32_t CA[8], CB[8];
     {
-      const uint8_t* ca = st + (rA >> 3) * 1024 + (rA & 7) * 16 + 4 * t;
-      const uint8_t* cb = st + (rB >> 3) * 1024 + (rB & 7) * 16 + 4 * t;
+      const uint8_t* ca = st + nv_code_word_addr_off(rA, t);
+      const uint8_t* cb = st + nv_code_word_addr_off(rB, t);
 #pragma unroll
       for (int j = 0; j < 8; ++j) { CA[j] = lds32(ca + 128 * j); CB[j] = lds32(cb + 128 * j); }
     }
     float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint32_t wa = CA[j], wb = CB[j];
       // the B operand is x only in the chunk pair this lane's column serves: zeroed by a
       // multiply with an f16x2 {1, 1} / {0, 0} mask on the FMA pipe (x is finite),
       // which keeps the ALU pipe for the decode
@@ -737,45 +727,64 @@ struct Slab<F_NVFP4, 1> {
       const uint32_t* xv = (j & 1) ? xo : xe;
       float* d = (j & 1) ? dO : dE;
       uint32_t pa[4], pb[4];
-      e2m1x4_f16(wa, pa);
-      e2m1x4_f16(wb, pb);
+      e2m1x4_f16(CA[j], pa);
+      e2m1x4_f16(CB[j], pb);
       mma_f16(d, pa[0], pb[0], pa[1], pb[1], hmul2(xv[0], mk), hmul2(xv[1], mk));
       mma_f16(d, pa[2], pb[2], pa[3], pb[3], hmul2(xv[2], mk), hmul2(xv[3], mk));
     }
-    const uint32_t sA = lds32(sf + 512 * t + 16 * (rA & 31) + 4 * (rA >> 5));
-    const uint32_t sB = lds32(sf + 512 * t + 16 * (rB & 31) + 4 * (rB >> 5));
     uint32_t hA[2], hB[2];
-    e4m3x4_f16(sA, hA);
-    e4m3x4_f16(sB, hB);
+    e4m3x4_f16(lds32(sf + nv_scale_word_off(rA, t)), hA);
+    e4m3x4_f16(lds32(sf + nv_scale_word_off(rB, t)), hB);
     const float2 a01 = h2x2f(hA[0]), a23 = h2x2f(hA[1]);
     const float2 b01 = h2x2f(hB[0]), b23 = h2x2f(hB[1]);
-    acc[0] += fmaf(a01.x, dE[0], fmaf(a01.y, dE[1], fmaf(a23.x, dO[0], a23.y * dO[1])));
-    acc[1] += fmaf(b01.x, dE[2], fmaf(b01.y, dE[3], fmaf(b23.x, dO[2], b23.y * dO[3])));
+    acc[0] = __fadd_rn(acc[0], nv_comb(a01.x, a01.y, a23.x, a23.y, dE[0], dE[1], dO[0], dO[1]));
+    acc[1] = __fadd_rn(acc[1], nv_comb(b01.x, b01.y, b23.x, b23.y, dE[2], dE[3], dO[2], dO[3]));
   }
 };
 
+// M > 1: token columns; each block of a chunk has its own MMA chain, whose B operand
+// keeps x only on the lanes holding that block (t/2 == block), as in the unit columns.
 template <>
 struct Slab<F_NVFP4, 8> {
   __device__ static void run(const uint8_t* st, const uint8_t* sf, const uint8_t* xs, int R, int w, int lane,
-                             float2*, float* acc) {
-    const int g = lane >> 2, t = lane & 3;
+                             float2*, float (&a)[4][4]) {
+    const int g = lane >> 2, tq = lane & 3;
+    const int rA = 16 * w + g, rB = rA + 8;
     const bool has_x = g < R;
-    uint32_t CA[8], CB[8], SA[4], SB[4];
-    nv_load(st, sf, 16 * w + g, t, CA, SA);
-    nv_load(st, sf, 16 * w + g + 8, t, CB, SB);
-    float dO[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint8_t* ca = st + nv_code_word_addr_off(rA, tq);
+    const uint8_t* cb = st + nv_code_word_addr_off(rB, tq);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t pa[4], pb[4];
-      nv_frag(CA[j], nv_sbyte(SA, j, t), pa);
-      nv_frag(CB[j], nv_sbyte(SB, j, t), pb);
-      uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
-      float* d = (j & 1) ? dO : acc;
-      mma_f16(d, pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);     // x already f16 (converted per stage)
-      mma_f16(d, pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
+    for (int t = 0; t < 4; ++t) {
+      float D[2][2][4];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int j = 2 * t + q;
+        // x already f16 (converted per stage)
+        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * tq) : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t pa[4], pb[4];
+        e2m1x4_f16(lds32(ca + 128 * j), pa);
+        e2m1x4_f16(lds32(cb + 128 * j), pb);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const bool on = (tq >> 1) == b;
+          const uint4 xb = on ? xv : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) D[q][b][e] = 0.f;
+          mma_f16(D[q][b], pa[0], pb[0], pa[1], pb[1], xb.x, xb.y);
+          mma_f16(D[q][b], pa[2], pb[2], pa[3], pb[3], xb.z, xb.w);
+        }
+      }
+      uint32_t hA[2], hB[2];
+      e4m3x4_f16(lds32(sf + nv_scale_word_off(rA, t)), hA);
+      e4m3x4_f16(lds32(sf + nv_scale_word_off(rB, t)), hB);
+      const float2 a01 = h2x2f(hA[0]), a23 = h2x2f(hA[1]);
+      const float2 b01 = h2x2f(hB[0]), b23 = h2x2f(hB[1]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 s01 = (e < 2) ? a01 : b01, s23 = (e < 2) ? a23 : b23;
+        tc_add(a, t, e, nv_comb(s01.x, s01.y, s23.x, s23.y, D[0][0][e], D[0][1][e], D[1][0][e], D[1][1][e]));
+      }
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] += dO[e];
   }
 };
 
@@ -783,8 +792,21 @@ struct Slab<F_NVFP4, 8> {
 // FP8 row-scaled. A = e4m3 in f16 (exact), B = x in f16; s_row in the epilogue.
 // The thread's 8 values of chunk j are bytes 8(t&1).. of 16-byte vector 2j + t/2.
 // ============================================================================
+__device__ __forceinline__ void fp8_chunk_mma(float* d, uint2 ca, uint2 cb, uint32_t x0, uint32_t x1, uint32_t x2,
+                                              uint32_t x3) {
+  uint32_t a0[2], b0[2], a1[2], b1[2];
+  e4m3x4_f16(ca.x, a0);
+  e4m3x4_f16(cb.x, b0);
+  e4m3x4_f16(ca.y, a1);
+  e4m3x4_f16(cb.y, b1);
+  mma_f16(d, a0[0], b0[0], a0[1], b0[1], x0, x1);
+  mma_f16(d, a1[0], b1[0], a1[1], b1[1], x2, x3);
+}
+
 template <>
 struct Slab<F_FP8, 1> {
+  // unit j = chunk j in column j: thread t's units 2t, 2t+1 are dE column 2t and dO
+  // column 2t+1
   __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int, int w, int lane,
                              float2*, float* acc) {
     const int g = lane >> 2, t = lane & 3;
@@ -798,48 +820,41 @@ struct Slab<F_FP8, 1> {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int v = 2 * j + (t >> 1);
-      const uint2 ca = lds64(rA + fp8_v_off(v, rowA & 7)), cb = lds64(rB + fp8_v_off(v, rowB & 7));
       const bool mine = (g == j);
-      float* d = (j & 1) ? dO : dE;
-      uint32_t a0[2], b0[2], a1[2], b1[2];
-      e4m3x4_f16(ca.x, a0);
-      e4m3x4_f16(cb.x, b0);
-      e4m3x4_f16(ca.y, a1);
-      e4m3x4_f16(cb.y, b1);
-      mma_f16(d, a0[0], b0[0], a0[1], b0[1], sel(mine, x0), sel(mine, x1));
-      mma_f16(d, a1[0], b1[0], a1[1], b1[1], sel(mine, x2), sel(mine, x3));
+      fp8_chunk_mma((j & 1) ? dO : dE, lds64(rA + fp8_v_off(v, rowA & 7)), lds64(rB + fp8_v_off(v, rowB & 7)),
+                    sel(mine, x0), sel(mine, x1), sel(mine, x2), sel(mine, x3));
     }
-    acc[0] += (dE[0] + dO[0]) + (dE[1] + dO[1]);
-    acc[1] += (dE[2] + dO[2]) + (dE[3] + dO[3]);
+    acc[0] = __fadd_rn(acc[0], fp8_comb(dE[0], dO[1]));
+    acc[1] = __fadd_rn(acc[1], fp8_comb(dE[2], dO[3]));
   }
 };
 
 template <>
 struct Slab<F_FP8, 8> {
   __device__ static void run(const uint8_t* st, const uint8_t*, const uint8_t* xs, int R, int w, int lane,
-                             float2*, float* acc) {
-    const int g = lane >> 2, t = lane & 3;
+                             float2*, float (&a)[4][4]) {
+    const int g = lane >> 2, tq = lane & 3;
     const int rowA = 16 * w + g, rowB = rowA + 8;
-    const uint8_t* rA = st + rowA * 256 + 8 * (t & 1);
-    const uint8_t* rB = st + rowB * 256 + 8 * (t & 1);
+    const uint8_t* rA = st + rowA * 256 + 8 * (tq & 1);
+    const uint8_t* rB = st + rowB * 256 + 8 * (tq & 1);
     const bool has_x = g < R;
-    float dO[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int v = 2 * j + (t >> 1);
-      const uint2 ca = lds64(rA + fp8_v_off(v, rowA & 7)), cb = lds64(rB + fp8_v_off(v, rowB & 7));
-      const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
-      float* d = (j & 1) ? dO : acc;
-      uint32_t a0[2], b0[2], a1[2], b1[2];
-      e4m3x4_f16(ca.x, a0);
-      e4m3x4_f16(cb.x, b0);
-      e4m3x4_f16(ca.y, a1);
-      e4m3x4_f16(cb.y, b1);
-      mma_f16(d, a0[0], b0[0], a0[1], b0[1], xv.x, xv.y);     // x already f16 (converted per stage)
-      mma_f16(d, a1[0], b1[0], a1[1], b1[1], xv.z, xv.w);
+    for (int t = 0; t < 4; ++t) {
+      float D[2][4];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int j = 2 * t + q;
+        const int v = 2 * j + (tq >> 1);
+        // x already f16 (converted per stage)
+        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * tq) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) D[q][e] = 0.f;
+        fp8_chunk_mma(D[q], lds64(rA + fp8_v_off(v, rowA & 7)), lds64(rB + fp8_v_off(v, rowB & 7)), xv.x, xv.y,
+                      xv.z, xv.w);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tc_add(a, t, e, fp8_comb(D[0][e], D[1][e]));
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] += dO[e];
   }
 };
 

@@ -124,11 +124,15 @@ __device__ __forceinline__ uint32_t ld_relaxed(const unsigned* p) {
 __device__ __forceinline__ void st_relaxed(unsigned* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// the bits of a partial sum as stored in the workspace: never zero
-__device__ __forceinline__ uint32_t nonzero_bits(float v) {
+// A piece as stored in the workspace: never zero, so that each word is its own
+// completion flag. +0.0 is stored as the NaN pattern 0x7FFFFFFF (no finite sum
+// produces it) and decoded back; every other value is stored as it is.
+constexpr uint32_t kZeroCode = 0x7FFFFFFFu;
+__device__ __forceinline__ uint32_t encode_piece(float v) {
   const uint32_t u = __float_as_uint(v);
-  return u == 0u ? 0x80000000u : u;
+  return u == 0u ? kZeroCode : u;
 }
+__device__ __forceinline__ float decode_piece(uint32_t u) { return u == kZeroCode ? 0.0f : __uint_as_float(u); }
 __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
@@ -145,8 +149,41 @@ struct KParams {
   int tbl_off;       // offset of the per-warp scale tables
   int stage_base;    // offset of stage 0
   int mt;            // partial stride (token columns per partial record)
-  float* partials;   // [num_ctas][128][mt]
+  int cells;         // dense: the number of cells V (> 0); grouped: 0 (every slab is a cell)
+  int cpc;           // dense: cells per CTA (1 or 2)
+  int maxslots;      // published pieces a CTA may hold (slots per CTA in the workspace)
+  int fault;         // test hook: 1 = peers publish nothing (reducers' bounded waits run
+                     // out); 2 = reducers abandon their gathers at once (pieces left behind)
+  unsigned long long peer_wait_ns;   // bound of a reducer's wait for a peer's piece
+  float* partials;   // [num_ctas][maxslots][128][mt]
 };
+
+// The cell partition of one call's slab sequence (S slabs, see the kernel): dense
+// calls cut it into kp.cells cells of floor(i S / V) slabs, kp.cpc per CTA; grouped
+// calls give CTA i the slabs [floor(i S / P), floor((i+1) S / P)), every slab its own
+// cell. 32-bit arithmetic: i * Sr < V * V.
+struct CellMap {
+  int V, cpc, Sq, Sr;
+  __device__ __forceinline__ int cell_start(int i) const { return i * Sq + (i * Sr) / V; }
+  __device__ __forceinline__ int cta_start(int i) const {
+    const int k = i * cpc;
+    return cell_start(k < V ? k : V);
+  }
+  // the start of a two-cell CTA's second cell (else the range end)
+  __device__ __forceinline__ int cta_mid(int i) const {
+    if (cpc != 2) return cta_start(i + 1);
+    const int k = 2 * i + 1;
+    return cell_start(k < V ? k : V);
+  }
+};
+__device__ __forceinline__ CellMap cell_map(int cells, int cpc, int S, int P) {
+  CellMap m;
+  m.V = cells > 0 ? cells : P;
+  m.cpc = cells > 0 ? cpc : 1;
+  m.Sq = S / m.V;
+  m.Sr = S % m.V;
+  return m;
+}
 
 // SW: fused gate|up with the SwiGLU epilogue. The tower holds 2E experts: the E
 // gate matrices, then the E up matrices (E = 1 for the dense call). Each segment is
@@ -305,11 +342,20 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   const int Eh = SW ? (int)(L.E / 2) : 0;        // SW: the up matrix of expert e is expert Eh + e
   const int P = (int)gridDim.x;
   const int c = (int)blockIdx.x;
-  // range start of CTA i: floor(i * S / P), in 32-bit arithmetic (S = Sq * P + Sr;
-  // i * Sr < P * P), so that the peer loops below stay cheap
-  const int Sq = S / P, Sr = S % P;
-  auto range_start = [&](int i) { return i * Sq + (i * Sr) / P; };
-  const int s0 = range_start(c), s1 = range_start(c + 1);
+  // Cells: the fixed partition of the slab sequence that the accumulation order
+  // follows (pieces never cross a cell boundary). Dense calls: V = kp.cells cells,
+  // cell i = slabs [floor(i S / V), floor((i+1) S / V)), kp.cpc consecutive cells per
+  // CTA; V depends on the matrix and the SM count only, never on M, so every M sums
+  // in the same order. Grouped calls: every slab is a cell, and CTA i holds slabs
+  // [floor(i S / P), floor((i+1) S / P)). In 32-bit arithmetic (i * Sr < V * V).
+  const bool dense_cells = kp.cells > 0;
+  int s0, s1, smid;
+  {
+    const CellMap cm = cell_map(kp.cells, kp.cpc, S, P);
+    s0 = cm.cta_start(c);
+    s1 = cm.cta_start(c + 1);
+    smid = cm.cta_mid(c);
+  }
   if (s0 >= s1) return;
   // the last k-group is narrower than 256 only for formats with 16/32-value blocks
   constexpr bool kMayBeRagged = (FMT == F_Q8_0 || FMT == F_NVFP4 || FMT == F_FP8);
@@ -480,71 +526,105 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   // ------------------------------ consumers ---------------------------------
   // After an abort (a wait that timed out, here or in another warp) a warp still
   // walks its slab sequence but skips the waits, the arithmetic and the stores.
+  //
+  // The accumulation order (the same for every M): a unit is a row tile of one
+  // segment (SW: its gate k-groups, then its up k-groups); a piece is a maximal run
+  // of a unit's slabs inside one cell and one pass. Per output, a piece's value is
+  // (A_0 + A_1) + (A_2 + A_3) of its slabs (qmv_slab.cuh), and a unit's value (per
+  // pass) is the fp32 sum of its pieces in k order, starting from zero. The CTA
+  // holding a unit's first slab (its reducer) adds its own pieces as it goes and then
+  // the pieces that later CTAs published, in order; every other CTA publishes each
+  // piece of the unit in the workspace slot (CTA, piece ordinal).
   const int w = warp - 1;               // this warp owns rows 16w .. 16w+15 of a slab
   constexpr bool kConvX = (MT > 1) && (FMT == F_NVFP4 || FMT == F_FP8);
   const int g = lane >> 2, tq = lane & 3;
   float2* tbl = tbls + w * (16 * kTblStride);
   const int rA = 16 * w + g, rB = rA + 8;
-  // accumulator words per thread: rows rA, rB x tokens 2tq, 2tq+1 (x gate, up for SW)
-  constexpr int NV = SW ? 8 : 4;
-  constexpr int UG = SW ? 2 : 1;          // k-group passes per unit (gate, up)
+  constexpr int UG = SW ? 2 : 1;          // passes per unit (gate, up)
   const int UL = UG * G;                  // slabs per unit
-  const int pstride = kSlabRows * kp.mt;  // partial words per pass
-  float acc[NV];
-#pragma unroll
-  for (int e = 0; e < NV; ++e) acc[e] = 0.f;
-  int T = s0 / UL;                        // current unit: a row tile of one segment (SW: of both)
+  const int pstride = kSlabRows * kp.mt;  // words of one published piece
+  unsigned* const parts = reinterpret_cast<unsigned*>(kp.partials);
+  float pa1[2];                           // M = 1: this thread's A_t of rows rA, rB
+  float pa8[4][4];                        // M > 1: A_0 .. A_3 of the thread's four outputs
+  float uacc[UG][4];                      // the unit's value per pass (reducer; M > 1)
+  // M = 1: the reducer's running unit sums of rows rA, rB (per pass) stay in shared
+  // memory while the slabs stream (fewer live registers in the decode loop); lane
+  // tq == 0 of each quad keeps them
+  // (the segment table's tail: an M = 1 call has at most 8 segments)
+  static_assert(8 * sizeof(Seg) + kConsumerWarps * 8 * 4 * sizeof(float) <= kMaxSeg * sizeof(Seg), "usm");
+  float* usm = reinterpret_cast<float*>(smem + 512 + 8 * sizeof(Seg)) + (w * 8 + g) * 4;
+  int T = s0 / UL;                        // current unit
   int tt = T % RT, seg = T / RT;
   int stage = 0;
   uint32_t fphase = 0;                   // parity of the full barrier for this stage round
   bool aborted = false;
-  for (int s = s0; s < s1;) {
-    aborted = aborted || misc[0];
+  int s = s0;
+  while (s < s1) {
     const Seg& sg = segs[seg];
     const int R = sg.R < MT ? sg.R : MT;
     const bool has_x = g < R;
     const int head = T * UL, tail = head + UL;
     const int send = tail < s1 ? tail : s1;
-    const bool full_cover = (s0 <= head) && (s1 >= tail);
     const bool reducer = (s0 <= head);
-    for (; s < send; ++s) {
-      bool have = false;
-      if (!aborted) {
-        if (!mbar_wait(&full[stage], fphase, a.status)) {
-          misc[0] = 1;
-          aborted = true;
-        } else {
-          have = true;
-        }
+    if constexpr (MT == 1) {
+      if (tq == 0) usm[0] = usm[1] = usm[2] = usm[3] = 0.f;
+    } else {
+#pragma unroll
+      for (int pp = 0; pp < UG; ++pp)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) uacc[pp][e] = 0.f;
+    }
+    while (s < send) {
+      // ---- one piece [s, pe): inside one cell and one pass of unit T ----
+      aborted = aborted || misc[0];
+      int pe = send;
+      if (!dense_cells) pe = s + 1;
+      else if (s < smid && smid < pe) pe = smid;
+      if (SW && s - head < G && head + G < pe) pe = head + G;
+      if constexpr (MT == 1) {
+        pa1[0] = pa1[1] = 0.f;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pa8[t][e] = 0.f;
       }
-      if constexpr (kConvX) {
-        // the f16-operand formats at M > 1: the eight consumer warps turn the stage's x
-        // rows from bf16 into f16 in place, warp w row w, 16 bytes per lane (zeros past
-        // a ragged K), once for all warps; every warp meets the barrier once per slab,
-        // whether it waited for the slab or not
-        if (have && w < (segs[seg].R < MT ? segs[seg].R : MT)) {
-          uint4* xv = reinterpret_cast<uint4*>(smem + kp.stage_base + stage * kp.stage_bytes + kp.x_off +
-                                               w * kXStride + 16 * lane);
-          const int gk = (s - head) % G;
-          uint4 v = *xv;
-          if (kMayBeRagged && gk == G - 1 && 8 * lane >= kv_last) {
-            v = make_uint4(0u, 0u, 0u, 0u);
+      for (; s < pe; ++s) {
+        bool have = false;
+        if (!aborted) {
+          if (!mbar_wait(&full[stage], fphase, a.status)) {
+            misc[0] = 1;
+            aborted = true;
           } else {
-            v.x = bf16x2_to_f16x2(v.x);
-            v.y = bf16x2_to_f16x2(v.y);
-            v.z = bf16x2_to_f16x2(v.z);
-            v.w = bf16x2_to_f16x2(v.w);
+            have = true;
           }
-          *xv = v;
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-      }
-      if (have) {
-        {
+        if constexpr (kConvX) {
+          // the f16-operand formats at M > 1: the eight consumer warps turn the stage's x
+          // rows from bf16 into f16 in place, warp w row w, 16 bytes per lane (zeros past
+          // a ragged K), once for all warps; every warp meets the barrier once per slab,
+          // whether it waited for the slab or not
+          if (have && w < R) {
+            uint4* xv = reinterpret_cast<uint4*>(smem + kp.stage_base + stage * kp.stage_bytes + kp.x_off +
+                                                 w * kXStride + 16 * lane);
+            const int gk = (s - head) % G;
+            uint4 v = *xv;
+            if (kMayBeRagged && gk == G - 1 && 8 * lane >= kv_last) {
+              v = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+              v.x = bf16x2_to_f16x2(v.x);
+              v.y = bf16x2_to_f16x2(v.y);
+              v.z = bf16x2_to_f16x2(v.z);
+              v.w = bf16x2_to_f16x2(v.w);
+            }
+            *xv = v;
+          }
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+        }
+        if (have) {
           const uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
           const uint8_t* xrow0 = st + kp.x_off;
           const int gk = (s - head) % G;
-          float* ap = acc + ((SW && s - head >= G) ? 4 : 0);
           // a last k-group narrower than 256: its padded blocks are zero and the x
           // beyond K is never copied, so the stale tail of each x row is zeroed (by
           // one thread of each warp, before that warp reads it; the converted formats
@@ -556,121 +636,163 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
             }
             __syncwarp();
           }
-          if (MT == 1) {
-            Slab<FMT, 1>::run(st, st + kp.b_off, xrow0, R, w, lane, tbl, ap);
+          if constexpr (MT == 1) {
+            Slab<FMT, 1>::run(st, st + kp.b_off, xrow0, R, w, lane, tbl, pa1);
           } else {
-            Slab<FMT, MT>::run(st, st + kp.b_off, xrow0 + (has_x ? g : 0) * kXStride, R, w, lane, tbl, ap);
+            Slab<FMT, MT>::run(st, st + kp.b_off, xrow0 + (has_x ? g : 0) * kXStride, R, w, lane, tbl, pa8);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[stage]);
         }
+        if (++stage == kp.stages) { stage = 0; fphase ^= 1u; }
       }
-      if (++stage == kp.stages) { stage = 0; fphase ^= 1u; }
-    }
-
-    // ---- end of unit T: this thread owns rows rA, rB of it and tokens 2tq, 2tq+1 ----
-    {
-      asm volatile("griddepcontrol.wait;" ::: "memory");   // workspace and y after earlier kernels
-      if (MT == 1) {
-        // unit columns: add the quad's partial sums of rows rA, rB (token 0)
+      // ---- the piece's value: (A_0 + A_1) + (A_2 + A_3) per output ----
+      const int pass = (SW && pe - 1 - head >= G) ? 1 : 0;   // the piece's pass (from its last slab)
+      float pv[4];
+      if constexpr (MT == 1) {
+        // unit columns: quad position tq holds A_tq of rows rA, rB (token 0)
+        float vA = pa1[0], vB = pa1[1];
+        vA = __fadd_rn(vA, __shfl_xor_sync(0xffffffffu, vA, 1));
+        vB = __fadd_rn(vB, __shfl_xor_sync(0xffffffffu, vB, 1));
+        vA = __fadd_rn(vA, __shfl_xor_sync(0xffffffffu, vA, 2));
+        vB = __fadd_rn(vB, __shfl_xor_sync(0xffffffffu, vB, 2));
+        pv[0] = vA; pv[1] = 0.f; pv[2] = vB; pv[3] = 0.f;
+      } else {
 #pragma unroll
-        for (int pp = 0; pp < UG; ++pp) {
-          float vA = acc[4 * pp], vB = acc[4 * pp + 1];
-          vA += __shfl_xor_sync(0xffffffffu, vA, 1);
-          vB += __shfl_xor_sync(0xffffffffu, vB, 1);
-          vA += __shfl_xor_sync(0xffffffffu, vA, 2);
-          vB += __shfl_xor_sync(0xffffffffu, vB, 2);
-          acc[4 * pp] = vA; acc[4 * pp + 1] = 0.f; acc[4 * pp + 2] = vB; acc[4 * pp + 3] = 0.f;
-        }
+        for (int e = 0; e < 4; ++e) pv[e] = quad_join(pa8[0][e], pa8[1][e], pa8[2][e], pa8[3][e]);
       }
-      if (!full_cover && !reducer) {
-        // peer: publish the partial sums. Each word is its own completion flag: a
-        // stored word is never zero (+0.0 is stored as -0.0, which adds the same),
-        // and the reducer waits for each word to become non-zero -- no fence, no flag.
-        if (!aborted) {
-          unsigned* part = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)c * (UG * pstride);
-#pragma unroll
-          for (int e = 0; e < NV; ++e) {
-            const int tok = 2 * tq + (e & 1), row = ((e & 3) < 2) ? rA : rB;
-            if (tok < R) st_relaxed(part + (e >> 2) * pstride + row * kp.mt + tok, nonzero_bits(acc[e]));
+      if (reducer) {
+        if constexpr (MT == 1) {
+          if (tq == 0) {
+            usm[pass] = __fadd_rn(usm[pass], pv[0]);
+            usm[2 + pass] = __fadd_rn(usm[2 + pass], pv[2]);
           }
-        }
-      } else if (!full_cover && !aborted) {
-        // reducer: add the peers' partial sums in CTA order, clearing each word after
-        // reading it (the workspace is all zero again when the call ends). The words
-        // of up to KB peers are loaded at once, so that their latencies overlap.
-        constexpr int KB = SW ? 2 : 4;
-        int cp = c + 1;
-        bool more = true;
-        while (more && !aborted) {
-          int pid[KB];
+        } else {
 #pragma unroll
-          for (int k = 0; k < KB; ++k) {          // the next KB peers (-1: none)
-            pid[k] = -1;
-            while (cp < P) {
-              const int ps0 = range_start(cp), ps1 = range_start(cp + 1);
-              if (ps0 >= tail) { cp = P; break; }
-              ++cp;
-              if (ps0 < ps1) { pid[k] = cp - 1; break; }   // an empty range publishes nothing
-            }
-          }
-          more = (pid[KB - 1] >= 0);
-          uint32_t u[KB][NV];
-#pragma unroll
-          for (int k = 0; k < KB; ++k) {
-#pragma unroll
-            for (int e = 0; e < NV; ++e) {
-              const int tok = 2 * tq + (e & 1), row = ((e & 3) < 2) ? rA : rB;
-              u[k][e] = 0u;
-              if (pid[k] >= 0 && tok < R)
-                u[k][e] = ld_relaxed(reinterpret_cast<const unsigned*>(kp.partials) +
-                                     (int64_t)pid[k] * (UG * pstride) + (e >> 2) * pstride + row * kp.mt + tok);
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < KB; ++k) {
-#pragma unroll
-            for (int e = 0; e < NV; ++e) {
-              const int tok = 2 * tq + (e & 1), row = ((e & 3) < 2) ? rA : rB;
-              if (pid[k] < 0 || tok >= R || aborted) continue;
-              unsigned* wp = reinterpret_cast<unsigned*>(kp.partials) + (int64_t)pid[k] * (UG * pstride) +
-                             (e >> 2) * pstride + row * kp.mt + tok;
-              uint32_t v = u[k][e];
-              if (v == 0u) {
-                const unsigned long long t0 = globaltimer();
-                while ((v = ld_relaxed(wp)) == 0u) {
-                  if (globaltimer() - t0 > kTimeoutNs) break;
-                }
-                if (v == 0u) { atomicOr(a.status, kStatTimeout); misc[0] = 1; aborted = true; continue; }
-              }
-              st_relaxed(wp, 0u);
-              acc[e] += __uint_as_float(v);
-            }
+          for (int e = 0; e < 4; ++e) {
+            if (SW && pass) uacc[UG - 1][e] = __fadd_rn(uacc[UG - 1][e], pv[e]);
+            else uacc[0][e] = __fadd_rn(uacc[0][e], pv[e]);
           }
         }
-      }
-      if (!aborted && (full_cover || reducer)) {
-        const uint8_t* extras = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + L.k_groups * L.group_bytes;
-        const uint8_t* extras_u = extras + (int64_t)Eh * L.expert_bytes;     // SW: the up expert's
+      } else if (!aborted && kp.fault != 1) {
+        // peer: publish the piece. Each stored word is its own completion flag: it is
+        // never zero (+0.0 is stored as a NaN pattern that no sum produces here, and
+        // decoded back to +0.0), and the reducer waits for each word to become
+        // non-zero -- no fence, no flag.
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // the workspace after earlier kernels
+        // the piece's first slab: in the second cell iff its last one is (pieces do not
+        // cross cells); grouped pieces are single slabs
+        const int slot = dense_cells ? ((pe - 1 >= smid ? 1 : 0) * UG + pass) : (pe - 1 - s0);
+        unsigned* part = parts + ((int64_t)c * kp.maxslots + slot) * pstride;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
+          if (MT == 1 && (e & 1)) continue;
           const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
-          const int64_t n = (int64_t)tt * kSlabRows + row;
-          if (tok >= R || n >= L.N) continue;
-          float v = acc[e];
-          if (FMT == F_NVFP4) v *= *reinterpret_cast<const float*>(extras);
-          if (FMT == F_FP8) v *= reinterpret_cast<const float*>(extras)[n];
-          if (SW) {
-            float u = acc[4 + e];
-            if (FMT == F_NVFP4) u *= *reinterpret_cast<const float*>(extras_u);
-            if (FMT == F_FP8) u *= reinterpret_cast<const float*>(extras_u)[n];
-            v = (v / (1.0f + expf(-v))) * u;               // silu(g) * u
-          }
-          a.y[(int64_t)sg.yrow[tok] * L.N + n] = v;
+          if (tok < R) st_relaxed(part + row * kp.mt + tok, encode_piece(pv[e]));
         }
       }
+    }
+
+    // ---- end of unit T in this CTA: this thread owns rows rA, rB and tokens 2tq, 2tq+1 ----
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // workspace and y after earlier kernels
+    if constexpr (MT == 1) {
+      if (reducer) {   // the running sums back into registers (valid in lanes tq == 0)
+        uacc[0][0] = usm[0];
+        uacc[UG - 1][0] = usm[UG - 1];
+        uacc[0][2] = usm[2];
+        uacc[UG - 1][2] = usm[2 + UG - 1];
+      }
+    }
+    if (reducer && !aborted && tail > s1) {
+      // the pieces of unit T that later CTAs published, in slab order, KB at a time so
+      // that their load latencies overlap; each word is cleared after it is read (the
+      // workspace is all zero again when the call ends)
+      constexpr int KB = SW ? 2 : 4;
+      // the cell map again (recomputed here, so that it is not held through the slabs)
+      const CellMap cm = cell_map(kp.cells, kp.cpc, misc[1] * RT * G * UG, P);
+      int p = s1, cp = c + 1;
+      if (kp.fault == 2) { atomicOr(a.status, kStatTimeout); misc[0] = 1; aborted = true; }
+      while (p < tail && !aborted) {
+        int base[KB], pps[KB];
+        bool valid[KB];
 #pragma unroll
-      for (int e = 0; e < NV; ++e) acc[e] = 0.f;
+        for (int k = 0; k < KB; ++k) {
+          valid[k] = p < tail;
+          base[k] = 0;
+          pps[k] = 0;
+          if (valid[k]) {
+            while (cm.cta_start(cp + 1) <= p) ++cp;       // the CTA holding slab p
+            const int ps = (SW && p - head >= G) ? 1 : 0;
+            int pe2, slot;
+            if (dense_cells) {
+              const int m = cm.cta_mid(cp);
+              const int kc = (p >= m) ? 1 : 0;            // its first or second cell
+              pe2 = kc ? cm.cta_start(cp + 1) : m;
+              if (pe2 > tail) pe2 = tail;
+              if (SW && ps == 0 && head + G < pe2) pe2 = head + G;
+              slot = kc * UG + ps;
+            } else {
+              pe2 = p + 1;
+              slot = p - cm.cta_start(cp);
+            }
+            base[k] = (cp * kp.maxslots + slot) * pstride;
+            pps[k] = ps;
+            p = pe2;
+          }
+        }
+        uint32_t u[KB][4];
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+            u[k][e] = 0u;
+            if (MT == 1 && (e & 1)) continue;
+            if (valid[k] && tok < R) u[k][e] = ld_relaxed(parts + base[k] + row * kp.mt + tok);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+            if ((MT == 1 && (e & 1)) || !valid[k] || tok >= R || aborted) continue;
+            unsigned* wp = parts + base[k] + row * kp.mt + tok;
+            uint32_t v = u[k][e];
+            if (v == 0u) {
+              const unsigned long long t0 = globaltimer();
+              while ((v = ld_relaxed(wp)) == 0u) {
+                if (globaltimer() - t0 > kp.peer_wait_ns) break;
+              }
+              if (v == 0u) { atomicOr(a.status, kStatTimeout); misc[0] = 1; aborted = true; continue; }
+            }
+            st_relaxed(wp, 0u);
+            const float f = decode_piece(v);
+            if (SW && pps[k]) uacc[UG - 1][e] = __fadd_rn(uacc[UG - 1][e], f);
+            else uacc[0][e] = __fadd_rn(uacc[0][e], f);
+          }
+        }
+      }
+    }
+    if (reducer && !aborted) {
+      const uint8_t* extras = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + L.k_groups * L.group_bytes;
+      const uint8_t* extras_u = extras + (int64_t)Eh * L.expert_bytes;     // SW: the up expert's
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
+        const int64_t n = (int64_t)tt * kSlabRows + row;
+        if ((MT == 1 && (e & 1)) || tok >= R || n >= L.N) continue;
+        float v = uacc[0][e];
+        if (FMT == F_NVFP4) v *= *reinterpret_cast<const float*>(extras);
+        if (FMT == F_FP8) v *= reinterpret_cast<const float*>(extras)[n];
+        if (SW) {
+          float uv = uacc[UG - 1][e];
+          if (FMT == F_NVFP4) uv *= *reinterpret_cast<const float*>(extras_u);
+          if (FMT == F_FP8) uv *= reinterpret_cast<const float*>(extras_u)[n];
+          v = (v / (1.0f + expf(-v))) * uv;               // silu(g) * u
+        }
+        a.y[(int64_t)sg.yrow[tok] * L.N + n] = v;
+      }
     }
     ++T;
     if (++tt == RT) { tt = 0; ++seg; }
@@ -680,14 +802,40 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-WsPlan ws_plan_stream(int M, int64_t tiles_max, int num_ctas, int passes) {
-  (void)tiles_max;
-  WsPlan p;
-  const int mt = (M <= 1) ? 1 : 8;
-  p.partials_off = 0;
-  p.partials_bytes = align_up((int64_t)num_ctas * passes * kSlabRows * mt * 4, 256);
-  p.total = p.partials_off + p.partials_bytes;
+static int64_t piece_bytes(int M) { return (int64_t)kSlabRows * (M <= 1 ? 1 : 8) * 4; }
+
+StreamPlan plan_stream_dense(int64_t slabs, int M, int passes, int sms, bool two_cells) {
+  StreamPlan p;
+  const int64_t v = slabs < 2 * (int64_t)sms ? slabs : 2 * (int64_t)sms;
+  p.cells = (int)(v > 0 ? v : 1);
+  p.cpc = (M <= 1 || two_cells) ? 2 : 1;
+  p.grid = (p.cells + p.cpc - 1) / p.cpc;
+  p.maxslots = p.cpc * passes;          // a CTA publishes pieces of its first unit only
+  p.ws_bytes = align_up((int64_t)p.grid * p.maxslots * piece_bytes(M), 256);
   return p;
+}
+
+StreamPlan plan_stream_grouped(int64_t slabs_max, int M, int passes, int64_t k_groups, int sms) {
+  StreamPlan p;
+  const int64_t n = slabs_max < 2 * (int64_t)sms ? slabs_max : 2 * (int64_t)sms;
+  p.grid = (int)(n > 0 ? n : 1);
+  p.cells = 0;
+  p.cpc = 1;
+  // every slab of a CTA's first unit but the unit's first one may be a published piece
+  const int64_t unit = passes * k_groups;
+  const int64_t per_cta = (slabs_max + p.grid - 1) / p.grid;
+  int64_t ms = unit - 1 < per_cta ? unit - 1 : per_cta;
+  p.maxslots = (int)(ms > 0 ? ms : 1);
+  p.ws_bytes = align_up((int64_t)p.grid * p.maxslots * piece_bytes(M), 256);
+  return p;
+}
+
+static int g_fault = 0;
+static unsigned long long g_peer_wait_ns = kTimeoutNs;
+
+void set_split_fault(int mode, unsigned long long peer_wait_ns) {
+  g_fault = (mode == 1 || mode == 2) ? mode : 0;
+  g_peer_wait_ns = (g_fault == 1 && peer_wait_ns > 0) ? peer_wait_ns : kTimeoutNs;
 }
 
 int num_sms_current_device() {
@@ -733,8 +881,15 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   const int64_t e_ids = SW ? a.L.E / 2 : a.L.E;      // experts the ids may name
   const int64_t segs_max = a.ids ? (pairs < e_ids ? pairs : e_ids) : 1;
   if (!slab_count_ok(a.L, segs_max * (SW ? 2 : 1))) return cudaErrorInvalidValue;
-  const WsPlan plan = ws_plan_stream(MT, 0, a.num_ctas, SW ? 2 : 1);
-  kp.partials = reinterpret_cast<float*>(a.ws + plan.partials_off);
+  kp.cells = a.cells;
+  kp.cpc = a.cpc;
+  kp.maxslots = a.maxslots;
+  kp.fault = g_fault;
+  kp.peer_wait_ns = g_peer_wait_ns;
+  if (a.cells > 0 && (a.cpc < 1 || a.cpc > 2 || (int64_t)a.num_ctas * a.cpc < a.cells)) return cudaErrorInvalidValue;
+  if (a.maxslots < 1 || (int64_t)a.num_ctas * a.maxslots * kSlabRows * MT * 4 > a.ws_bytes)
+    return cudaErrorInvalidValue;
+  kp.partials = reinterpret_cast<float*>(a.ws);
   const int smem = kp.stage_base + kp.stages * kp.stage_bytes;
   // M = 1 grouped calls have an instance of their own (the producer's first-stage start)
   const bool gr = MT == 1 && a.ids != nullptr;

@@ -151,7 +151,7 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
                     int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Bytes of the device scratch array built into the library for qmv_gemv_noalloc. */
-#define QMV_STATIC_SCRATCH_BYTES (1u << 20)
+#define QMV_STATIC_SCRATCH_BYTES (4u << 20)
 
 /* qmv_gemv without a workspace argument; it allocates nothing. The pages have no
  * counterpart: it is a library convenience. It serves callers that cannot hand
@@ -167,9 +167,11 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
  * left: each call first clears the words it uses on `stream` (cudaMemsetAsync, no
  * allocation). Calls that overlap in time (on other streams or host threads)
  * race on the array; the caller must serialize them.
- * Its grid is always one CTA per SM, whose partial sums take SMs x 128 x c x 4
- * bytes (c = 1 at M = 1, else 8; rounded up to 256). Returns QMV_EWORKSPACE when
- * that exceeds QMV_STATIC_SCRATCH_BYTES (M = 2..8 on a device of more than 256
+ * Its grid is one CTA per SM at every M, and it adds up in the same order as
+ * qmv_gemv, so its results equal qmv_gemv's bit for bit. Its partial sums take
+ * (CTAs) x 2 x 128 x c x 4 bytes (c = 1 at M = 1, else 8; rounded up to 256): at
+ * most 8 KiB per SM, 1,245,184 bytes on a 152-SM GB300. Returns QMV_EWORKSPACE
+ * when that exceeds QMV_STATIC_SCRATCH_BYTES (M = 2..8 on a device of more than 512
  * SMs). Otherwise arguments, results and errors as qmv_gemv. */
 qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y,
                             int M, int64_t N, int64_t K, cudaStream_t stream);
@@ -272,6 +274,20 @@ const char* qmv_status_str(qmv_status s);
  * mma.sync GEMV, 3 = grouped, 4 = W4A4 tcgen05, 5 = dequant, 6 = pack,
  * 7 = quantize, 8 = activation quantizer, 9 = fused gate|up SwiGLU). Test hook. */
 int qmv_last_route(void);
+
+/* Test hook for the split-K reduction of qmv_gemv, qmv_grouped and their SwiGLU and
+ * no-workspace forms; it changes the launches made after it, from any host thread
+ * (a process-wide setting, not thread-safe; for tests only).
+ *   mode 1: peers publish no partial sums, so every reducer that needs one waits
+ *           wait_limit_ns (0: one second), then latches QMV_ETIMEOUT in the device
+ *           status word, skips its outputs and exits;
+ *   mode 2: reducers latch QMV_ETIMEOUT and exit without reading their peers'
+ *           partial sums, which stay in the workspace (or the built-in scratch);
+ *   mode 0: normal operation.
+ * No other wait is affected; nothing faults and the context stays usable. After such
+ * a call, zero-fill the workspace and clear the status, as after any device status
+ * error (qmv_gemv_noalloc clears its scratch itself). */
+void qmv_debug_split_k_fault(int mode, uint64_t wait_limit_ns);
 
 /* Read (and, if reset != 0, clear) the device status word of the current
  * device. Synchronizes the device. Returns QMV_OK or the first latched device

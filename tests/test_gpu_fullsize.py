@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import synth
-from cases import TOL, device_matrix, host_rows_dequant, norm_err, sample_rows
+from cases import TOL, device_matrix, host_dequant, host_rows_dequant, norm_err, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -128,4 +128,34 @@ def test_tower_swiglu_full_size_sampled(q):
                 err = np.abs(h[t, j, rows][None, :] - href) / bound
                 assert float(err.max()) <= 1.0, (M, t, j, e, float(err.max()))
     del tower
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mat", ["gate", "up", "down"])
+def test_q4k_mlp_whole_output(q, mat):
+    """The headline configuration's whole output, not a sample: the Q4_K MLP matrices
+    of Qwen3.8-27B (gate, up [17408, 5120], down [5120, 17408]) at M = 1 and M = 8,
+    every one of the N x M outputs against the oracle's fp64 dots over its own
+    encoding and BlockToFloat of the same seeded weights."""
+    N, K = (QWEN_MLP, QWEN_HIDDEN) if mat != "down" else (QWEN_HIDDEN, QWEN_MLP)
+    seed = {"gate": 811, "up": 812, "down": 813}[mat]
+    # the seeded generator gives the same bits on the device as on the host (integer
+    # hash, exact fp32); drawing the 89 M weights there only saves time. The encoding,
+    # BlockToFloat and dots are the oracle's own.
+    W = synth.weights(seed, N, K, device="cuda").cpu().numpy()
+    canon = oracle.encode("q4_k", W)
+    del W
+    D = host_dequant("q4_k", canon, N, K)
+    x = synth.activations(seed, 8, K)
+    ref, den = oracle.gemv_f64(D, synth.bf16_bits(x))
+    del D
+    packed = q.qmv_pack("q4_k", torch.from_numpy(canon).cuda(), N, K)
+    for M in (1, 8):
+        ws = q.workspace(q.QMV_ENTRY_GEMV, "q4_k", M, N, K)
+        y = q.qmv_gemv("q4_k", packed, x[:M].cuda(), N, K, ws).cpu().numpy()
+        assert q.qmv_device_status() == 0
+        assert y.shape == (M, N)
+        e = norm_err(y, ref[:M], den[:M])
+        assert e <= TOL, (M, e)
+    del packed
     torch.cuda.empty_cache()

@@ -179,21 +179,6 @@ def test_q6k_activation_range(q, lo, hi, M):
     assert norm_err(y, ref, den) <= TOL
 
 
-def test_gemv_rows_of_m8_match_m1_within_tolerance(q):
-    fmt, N, K = "q6_k", 640, 1024
-    W, canon = host_matrix(fmt, 17, N, K)
-    packed = q.qmv_pack(fmt, torch.from_numpy(canon).cuda(), N, K)
-    x = synth.activations(17, 8, K)
-    ref, den = oracle.gemv_f64(host_dequant(fmt, canon, N, K), synth.bf16_bits(x))
-    ws = q.workspace(q.QMV_ENTRY_GEMV, fmt, 8, N, K)
-    y8 = q.qmv_gemv(fmt, packed, x.cuda(), N, K, ws).cpu().numpy()
-    for m in (0, 5, 7):
-        ws1 = q.workspace(q.QMV_ENTRY_GEMV, fmt, 1, N, K)
-        y1 = q.qmv_gemv(fmt, packed, x[m:m + 1].cuda(), N, K, ws1).cpu().numpy()[0]
-        assert norm_err(y1, ref[m], den[m]) <= TOL
-        assert norm_err(y8[m], ref[m], den[m]) <= TOL
-
-
 # ---------------------------------------------------------------------------
 # grouped
 # ---------------------------------------------------------------------------
@@ -231,7 +216,7 @@ def test_errors(q):
         q.qmv_gemv("q4_k", packed, x, N, K, ws[:1024])
     assert ei.value.status == 8
     with pytest.raises(q.QmvError) as ei:
-        q.qmv_gemv("q4_k", packed, x, N, 300, ws)            # K not a multiple of 256
+        q.qmv_gemv("q4_k", packed, synth.activations(23, 1, 288).cuda(), N, 288, ws)   # K % 256 != 0
     assert ei.value.status == 3
     # arguments that disagree with the packed header: detected on the device
     q.qmv_device_status(reset=True)
