@@ -44,6 +44,7 @@ void apply_plan(StreamArgs* a, const StreamPlan& p) {
   a->num_ctas = p.grid;
   a->cells = p.cells;
   a->cpc = p.cpc;
+  a->gp = p.gp;
   a->maxslots = p.maxslots;
 }
 

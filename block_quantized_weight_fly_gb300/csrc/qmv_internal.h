@@ -28,6 +28,7 @@ struct StreamArgs {
   int num_ctas;              // persistent grid size
   int cells;                 // dense: cells of the accumulation order (> 0); grouped: 0
   int cpc;                   // dense: cells per CTA (1 or 2)
+  int gp;                    // grouped: slabs per cell
   int maxslots;              // workspace slots (published pieces) per CTA
 };
 
@@ -37,10 +38,10 @@ struct StreamArgs {
 //    only, so that every M (and the no-workspace entry) adds in the same order;
 //    two cells per CTA at M = 1 (one CTA per SM, so the next call's CTAs fit beside
 //    it) or when two_cells is set, else one (two CTAs per SM);
-//  - grouped: every slab is a cell; min(2 x SMs, slabs_max) CTAs.
+//  - grouped: every slab is a cell (gp = 1), whatever the routing; two CTAs per SM.
 // passes: 1, or 2 for the fused gate|up (gate and up sums).
 struct StreamPlan {
-  int grid, cells, cpc, maxslots;
+  int grid, cells, cpc, gp, maxslots;
   int64_t ws_bytes;          // split-K workspace (published pieces), 256-byte multiple
 };
 StreamPlan plan_stream_dense(int64_t slabs, int M, int passes, int sms, bool two_cells);

@@ -49,6 +49,13 @@ constexpr int kMaxStages = 16;
 // bytes per row of plane B (Q6_K d, NVFP4 block scales)
 template <int FMT> constexpr int plane_b_row() { return FMT == F_Q6_K ? 2 : FMT == F_NVFP4 ? 16 : 0; }
 constexpr int kMaxSeg = 64;
+// the reducer's gather list (built by the producer warp): kMaxGather entries in the
+// misc area of shared memory, then the mbarrier that publishes them
+// (after misc[0..11], the control words of the misc area at byte 272)
+constexpr int kGatherOff = 320;
+constexpr int kMaxGather = 36;
+constexpr int kGbarOff = 472;
+static_assert(kGatherOff + 4 * kMaxGather <= kGbarOff && kGbarOff + 8 <= 512, "misc area");
 constexpr unsigned long long kTimeoutNs = 1000000000ull;   // 1 s
 constexpr uint32_t kSuspendNs = 2000;    // a waiting thread sleeps up to this long per try (wakes on completion)
 
@@ -151,6 +158,7 @@ struct KParams {
   int mt;            // partial stride (token columns per partial record)
   int cells;         // dense: the number of cells V (> 0); grouped: 0 (every slab is a cell)
   int cpc;           // dense: cells per CTA (1 or 2)
+  int gp;            // grouped: slabs per cell
   int maxslots;      // published pieces a CTA may hold (slots per CTA in the workspace)
   int fault;         // test hook: 1 = peers publish nothing (reducers' bounded waits run
                      // out); 2 = reducers abandon their gathers at once (pieces left behind)
@@ -158,31 +166,244 @@ struct KParams {
   float* partials;   // [num_ctas][maxslots][128][mt]
 };
 
-// The cell partition of one call's slab sequence (S slabs, see the kernel): dense
-// calls cut it into kp.cells cells of floor(i S / V) slabs, kp.cpc per CTA; grouped
-// calls give CTA i the slabs [floor(i S / P), floor((i+1) S / P)), every slab its own
-// cell. 32-bit arithmetic: i * Sr < V * V.
+// The cell partition of one call's slab sequence (S slabs in units of UL slabs; see
+// the kernel). Dense calls: kp.cells = V cells of floor(i S / V) slabs, kp.cpc per
+// CTA. Grouped calls: each unit is cut into CU = ceil(UL / gp) cells of gp slabs, and
+// CTA c holds cells [floor(c C / P), floor((c+1) C / P)) of the C cells. 32-bit
+// arithmetic: i * Sr < V * V and c * Cr < P * P.
 struct CellMap {
-  int V, cpc, Sq, Sr;
-  __device__ __forceinline__ int cell_start(int i) const { return i * Sq + (i * Sr) / V; }
-  __device__ __forceinline__ int cta_start(int i) const {
-    const int k = i * cpc;
-    return cell_start(k < V ? k : V);
+  bool grouped;
+  int V, cpc, Sq, Sr;        // dense
+  int CU, UL, gp, P, Cq, Cr; // grouped
+  __device__ __forceinline__ int cell_start(int i) const {
+    if (grouped) {
+      const int k = (i % CU) * gp;
+      return (i / CU) * UL + (k < UL ? k : UL);
+    }
+    return i * Sq + (i * Sr) / V;
   }
-  // the start of a two-cell CTA's second cell (else the range end)
-  __device__ __forceinline__ int cta_mid(int i) const {
-    if (cpc != 2) return cta_start(i + 1);
-    const int k = 2 * i + 1;
+  __device__ __forceinline__ int first_cell(int c) const {
+    if (grouped) return c * Cq + (c * Cr) / P;
+    const int k = c * cpc;
+    return k < V ? k : V;
+  }
+  __device__ __forceinline__ int cta_start(int c) const { return cell_start(first_cell(c)); }
+  // the cell of slab p (grouped)
+  __device__ __forceinline__ int cell_of(int p) const { return (p / UL) * CU + (p % UL) / gp; }
+  // dense: the start of a two-cell CTA's second cell (else the range end)
+  __device__ __forceinline__ int cta_mid(int c) const {
+    if (grouped || cpc != 2) return cta_start(c + 1);
+    const int k = 2 * c + 1;
     return cell_start(k < V ? k : V);
   }
 };
-__device__ __forceinline__ CellMap cell_map(int cells, int cpc, int S, int P) {
+__device__ __forceinline__ CellMap cell_map(int cells, int cpc, int gp, int S, int UL, int P) {
   CellMap m;
-  m.V = cells > 0 ? cells : P;
+  m.grouped = cells <= 0;
+  m.V = cells > 0 ? cells : 1;
   m.cpc = cells > 0 ? cpc : 1;
   m.Sq = S / m.V;
   m.Sr = S % m.V;
+  m.UL = UL;
+  m.gp = gp > 0 ? gp : 1;
+  m.CU = (UL + m.gp - 1) / m.gp;
+  m.P = P;
+  const int C = (S / UL) * m.CU;
+  m.Cq = C / P;
+  m.Cr = C % P;
   return m;
+}
+
+// The next piece of unit [head, tail) from slab *p on, held by CTA *cp or a later one
+// (*cp is advanced to it): returns the piece's workspace word index (a multiple of
+// 128) with its pass in bit 0, and moves *p to the piece's end.
+__device__ __forceinline__ int next_piece(const CellMap cm, int head, int tail, int G, int UG, int maxslots,
+                                       int pstride, int* p, int* cp) {
+  const int q = *p;
+  int c = *cp;
+  while (cm.cta_start(c + 1) <= q) ++c;               // the CTA holding slab q
+  const int ps = (UG == 2 && q - head >= G) ? 1 : 0;
+  int pe, slot;
+  if (!cm.grouped) {
+    const int m = cm.cta_mid(c);
+    const int kc = (q >= m) ? 1 : 0;                  // its first or second cell
+    pe = kc ? cm.cta_start(c + 1) : m;
+    slot = kc * UG + ps;
+  } else {
+    const int ci = cm.cell_of(q);
+    pe = cm.cell_start(ci + 1);
+    slot = (ci - cm.first_cell(c)) * UG + ps;
+  }
+  if (pe > tail) pe = tail;
+  if (UG == 2 && ps == 0 && head + G < pe) pe = head + G;
+  *p = pe;
+  *cp = c;
+  return (c * maxslots + slot) * pstride + ps;
+}
+
+// ---------------------------------------------------------------------------
+// Cold paths, out of line: their code stays away from the decode loop, whose
+// instruction footprint must stay small (one copy each; their calls are rare).
+// ---------------------------------------------------------------------------
+// Set-up (one thread): the CTA's slab range in the cells of the call, into
+// misc[6] = start, misc[7] = end, misc[8] = the start of a two-cell CTA's second cell
+// (dense calls; else the end).
+__device__ __noinline__ void cta_range(volatile int* misc, int cells, int cpc, int gp, int S, int UL, int P,
+                                       int c) {
+  const CellMap cm = cell_map(cells, cpc, gp, S, UL, P);
+  misc[6] = cm.cta_start(c);
+  misc[7] = cm.cta_start(c + 1);
+  misc[8] = cm.cta_mid(c);
+}
+
+// The producer's gather list, built by the whole producer warp: the pieces of the
+// CTA's last unit that later CTAs hold, when this CTA holds the unit's first slab, in
+// slab order. Lane l takes the l-th cell after the CTA's range (a piece, or two when
+// the cell holds both passes of a fused unit); a warp prefix sum places the entries.
+// At most kMaxGather entries in glist, their count in misc[2]; when more pieces
+// follow, misc[5] = 1 and misc[3], misc[4] = where they start (slab, a CTA at or
+// before its holder).
+__device__ __noinline__ void build_gather_list(volatile int* misc, volatile int* glist, int cells, int cpc, int gp,
+                                               int S, int UL, int G, int UG, int P, int c, int maxslots,
+                                               int pstride, int lane) {
+  const int s0 = misc[6], s1 = misc[7];
+  const int head = ((s1 - 1) / UL) * UL, tail = head + UL;
+  int n = 0, more = 0, rest = tail;
+  if (head >= s0 && tail > s1) {
+    const CellMap cm = cell_map(cells, cpc, gp, S, UL, P);
+    const int ncells = cm.grouped ? (S / UL) * cm.CU : cm.V;
+    const int base = cm.first_cell(c + 1);
+    for (int round = 0;; ++round) {
+      const int i = base + 32 * round + lane;
+      int cnt = 0, e0 = -1, e1 = -1, cs = tail;
+      if (i < ncells) cs = cm.cell_start(i);
+      if (cs < tail) {
+        int ce = cm.cell_start(i + 1);
+        if (ce > tail) ce = tail;
+        // the CTA holding cell i
+        int cp;
+        if (!cm.grouped) {
+          cp = i / cm.cpc;
+        } else {
+          cp = (int)(((int64_t)i * P) / ((int64_t)(S / UL) * cm.CU));
+          while (cp + 1 <= P && cm.first_cell(cp + 1) <= i) ++cp;
+          while (cp > 0 && cm.first_cell(cp) > i) --cp;
+        }
+        const int ord = i - cm.first_cell(cp);
+        const int ps0 = (UG == 2 && cs - head >= G) ? 1 : 0;
+        e0 = (cp * maxslots + ord * UG + ps0) * pstride + ps0;
+        cnt = 1;
+        if (UG == 2 && ps0 == 0 && head + G < ce) {       // the cell also holds up slabs
+          e1 = (cp * maxslots + ord * UG + 1) * pstride + 1;
+          cnt = 2;
+        }
+      }
+      // exclusive prefix of cnt over the lanes
+      int pre = cnt;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, pre, d);
+        if (lane >= d) pre += v;
+      }
+      const int total = __shfl_sync(0xffffffffu, pre, 31);
+      pre -= cnt;
+      if (n + total > kMaxGather) {                    // the rest: computed by the reducer
+        more = 1;
+        rest = __shfl_sync(0xffffffffu, cs, 0);        // the first cell of this round
+        break;
+      }
+      if (cnt > 0) glist[n + pre] = e0;
+      if (cnt > 1) glist[n + pre + 1] = e1;
+      n += total;
+      const bool done = __any_sync(0xffffffffu, i >= ncells || cs >= tail);
+      if (done) break;
+    }
+    if (lane == 0 && more) {
+      misc[3] = rest;
+      misc[4] = c + 1;
+    }
+  }
+  if (lane == 0) {
+    misc[2] = n;
+    misc[5] = more;
+  }
+  __syncwarp();
+}
+
+// The reducer's gather past the end of the producer's list (rare: a unit cut into
+// more pieces than the list holds): the remaining pieces of unit [head, tail), computed
+// here in slab order, KB at a time so that their load latencies overlap, added into
+// uacc[pass][e] (e: this thread's outputs, rows rA/rB x tokens 2tq, 2tq+1; at M = 1
+// e = 0, 2 only). Each word is cleared after it is read. Returns false when a bounded
+// wait ran out (the status is latched).
+struct GatherArgs {
+  volatile int* misc;
+  const volatile int* glist;
+  unsigned* parts;
+  unsigned* status;
+  unsigned long long wait_ns;
+  int cells, cpc, gp, S, UL, G, P, maxslots, pstride, mt, R, tq, rA, rB, head, tail;
+};
+template <int MT, bool SW>
+__device__ __noinline__ bool gather_unit(const GatherArgs ga, float* uacc /* [UG][4] */) {
+  constexpr int UG = SW ? 2 : 1;
+  constexpr int KB = (MT == 1 ? 8 : 4) / (SW ? 2 : 1);
+  constexpr int NE = MT == 1 ? 2 : 4;                  // outputs e of this thread (M = 1: e = 0, 2)
+  // (called only when the producer's list did not hold every piece: the list has
+  // been gathered inline; this continues from where it stopped)
+  const int n = 0;
+  const bool more = true;
+  int i = 0, p = ga.misc[3], cp = ga.misc[4];
+  for (;;) {
+    int pc[KB];
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      pc[k] = -1;
+      if (i < n) {
+        pc[k] = ga.glist[i++];
+      } else if (more && p < ga.tail) {
+        pc[k] = next_piece(cell_map(ga.cells, ga.cpc, ga.gp, ga.S, ga.UL, ga.P), ga.head, ga.tail, ga.G, UG,
+                           ga.maxslots, ga.pstride, &p, &cp);
+      }
+    }
+    if (pc[0] < 0) return true;
+    uint32_t u[KB][NE];
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+#pragma unroll
+      for (int j = 0; j < NE; ++j) {
+        const int e = MT == 1 ? 2 * j : j;
+        const int tok = 2 * ga.tq + (e & 1), row = (e < 2) ? ga.rA : ga.rB;
+        u[k][j] = 0u;
+        if (pc[k] >= 0 && tok < ga.R) u[k][j] = ld_relaxed(ga.parts + (pc[k] & ~1) + row * ga.mt + tok);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+#pragma unroll
+      for (int j = 0; j < NE; ++j) {
+        const int e = MT == 1 ? 2 * j : j;
+        const int tok = 2 * ga.tq + (e & 1), row = (e < 2) ? ga.rA : ga.rB;
+        if (pc[k] < 0 || tok >= ga.R) continue;
+        unsigned* wp = ga.parts + (pc[k] & ~1) + row * ga.mt + tok;
+        uint32_t v = u[k][j];
+        if (v == 0u) {
+          const unsigned long long t0 = globaltimer();
+          while ((v = ld_relaxed(wp)) == 0u) {
+            if (globaltimer() - t0 > ga.wait_ns) break;
+          }
+          if (v == 0u) {
+            atomicOr(ga.status, kStatTimeout);
+            ga.misc[0] = 1;
+            return false;
+          }
+        }
+        st_relaxed(wp, 0u);
+        float* dst = uacc + ((SW && (pc[k] & 1)) ? 4 * (UG - 1) : 0) + e;
+        *dst = __fadd_rn(*dst, decode_piece(v));
+      }
+    }
+  }
 }
 
 // SW: fused gate|up with the SwiGLU epilogue. The tower holds 2E experts: the E
@@ -247,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       mbar_init(&full[i], MT == 1 ? 1 : 1 + 32);   // M > 1: + one cp.async arrival per producer lane
       mbar_init(&empty[i], kConsumerWarps);
     }
+    mbar_init(reinterpret_cast<uint64_t*>(smem + kGbarOff), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -331,6 +553,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       }
     }
   }
+  if (tid == 0 && !misc[0]) {
+    // the CTA's slab range in the cells of this call (CellMap), in misc[6..8]; 32-bit
+    // slab counts (the host refuses larger problems)
+    cta_range(misc, kp.cells, kp.cpc, kp.gp, misc[1] * (int)L.row_tiles * (int)L.k_groups * (SW ? 2 : 1),
+              (int)L.k_groups * (SW ? 2 : 1), (int)gridDim.x, (int)blockIdx.x);
+  }
   __syncthreads();
   if (misc[0]) return;
 
@@ -348,14 +576,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   // CTA; V depends on the matrix and the SM count only, never on M, so every M sums
   // in the same order. Grouped calls: every slab is a cell, and CTA i holds slabs
   // [floor(i S / P), floor((i+1) S / P)). In 32-bit arithmetic (i * Sr < V * V).
-  const bool dense_cells = kp.cells > 0;
-  int s0, s1, smid;
-  {
-    const CellMap cm = cell_map(kp.cells, kp.cpc, S, P);
-    s0 = cm.cta_start(c);
-    s1 = cm.cta_start(c + 1);
-    smid = cm.cta_mid(c);
-  }
+  constexpr bool dense_cells = !GR;       // GR: a grouped call (its own instances)
+  const int s0 = misc[6], s1 = misc[7];
   if (s0 >= s1) return;
   // the last k-group is narrower than 256 only for formats with 16/32-value blocks
   constexpr bool kMayBeRagged = (FMT == F_Q8_0 || FMT == F_NVFP4 || FMT == F_FP8);
@@ -520,6 +742,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     } else {
       produce8();
     }
+    // the gather list of the CTA's last unit: built once here, where the warp has time,
+    // instead of by every consumer warp at the end
+    __syncwarp();
+    build_gather_list(misc, reinterpret_cast<volatile int*>(smem + kGatherOff), kp.cells, kp.cpc, kp.gp, S,
+                      G * (SW ? 2 : 1), G, SW ? 2 : 1, P, c, kp.maxslots, kSlabRows * kp.mt, lane);
+    if (lane == 0) mbar_arrive(reinterpret_cast<uint64_t*>(smem + kGbarOff));   // release: the list is visible
     __syncwarp();
     return;
   }
@@ -546,40 +774,38 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   unsigned* const parts = reinterpret_cast<unsigned*>(kp.partials);
   float pa1[2];                           // M = 1: this thread's A_t of rows rA, rB
   float pa8[4][4];                        // M > 1: A_0 .. A_3 of the thread's four outputs
-  float uacc[UG][4];                      // the unit's value per pass (reducer; M > 1)
-  // M = 1: the reducer's running unit sums of rows rA, rB (per pass) stay in shared
-  // memory while the slabs stream (fewer live registers in the decode loop); lane
-  // tq == 0 of each quad keeps them
-  // (the segment table's tail: an M = 1 call has at most 8 segments)
-  static_assert(8 * sizeof(Seg) + kConsumerWarps * 8 * 4 * sizeof(float) <= kMaxSeg * sizeof(Seg), "usm");
-  float* usm = reinterpret_cast<float*>(smem + 512 + 8 * sizeof(Seg)) + (w * 8 + g) * 4;
+  float uacc[UG][4];                      // the unit's value per pass (reducer)
   int T = s0 / UL;                        // current unit
   int tt = T % RT, seg = T / RT;
   int stage = 0;
   uint32_t fphase = 0;                   // parity of the full barrier for this stage round
   bool aborted = false;
-  int s = s0;
-  while (s < s1) {
+  int cell_ord = 0;                      // grouped: ordinal of the current cell in the range
+  for (int s = s0; s < s1;) {
     const Seg& sg = segs[seg];
     const int R = sg.R < MT ? sg.R : MT;
     const bool has_x = g < R;
     const int head = T * UL, tail = head + UL;
     const int send = tail < s1 ? tail : s1;
     const bool reducer = (s0 <= head);
-    if constexpr (MT == 1) {
-      if (tq == 0) usm[0] = usm[1] = usm[2] = usm[3] = 0.f;
-    } else {
 #pragma unroll
-      for (int pp = 0; pp < UG; ++pp)
+    for (int pp = 0; pp < UG; ++pp)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) uacc[pp][e] = 0.f;
-    }
+      for (int e = 0; e < 4; ++e) uacc[pp][e] = 0.f;
     while (s < send) {
       // ---- one piece [s, pe): inside one cell and one pass of unit T ----
       aborted = aborted || misc[0];
       int pe = send;
-      if (!dense_cells) pe = s + 1;
-      else if (s < smid && smid < pe) pe = smid;
+      int ce = 0;                                   // grouped: the end of s's cell
+      if constexpr (!dense_cells) {
+        const int gsh = kp.gp >> 1;
+        ce = head + ((((s - head) >> gsh) + 1) << gsh);
+        if (ce > tail) ce = tail;
+        if (ce < pe) pe = ce;
+      } else {
+        const int sm = misc[8];
+        if (s < sm && sm < pe) pe = sm;
+      }
       if (SW && s - head < G && head + G < pe) pe = head + G;
       if constexpr (MT == 1) {
         pa1[0] = pa1[1] = 0.f;
@@ -624,12 +850,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         if (have) {
           const uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
           const uint8_t* xrow0 = st + kp.x_off;
-          const int gk = (s - head) % G;
           // a last k-group narrower than 256: its padded blocks are zero and the x
           // beyond K is never copied, so the stale tail of each x row is zeroed (by
           // one thread of each warp, before that warp reads it; the converted formats
           // zeroed it above)
-          if (!kConvX && kMayBeRagged && gk == G - 1 && kv_last < kSlabK) {
+          if (!kConvX && kMayBeRagged && (s - head) % G == G - 1 && kv_last < kSlabK) {
             if (has_x && tq == 0) {
               uint8_t* xw = const_cast<uint8_t*>(xrow0) + g * kXStride;
               for (int o = kv_last * 2; o < kSlabK * 2; o += 4) *reinterpret_cast<uint32_t*>(xw + o) = 0u;
@@ -662,17 +887,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         for (int e = 0; e < 4; ++e) pv[e] = quad_join(pa8[0][e], pa8[1][e], pa8[2][e], pa8[3][e]);
       }
       if (reducer) {
-        if constexpr (MT == 1) {
-          if (tq == 0) {
-            usm[pass] = __fadd_rn(usm[pass], pv[0]);
-            usm[2 + pass] = __fadd_rn(usm[2 + pass], pv[2]);
-          }
-        } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (SW && pass) uacc[UG - 1][e] = __fadd_rn(uacc[UG - 1][e], pv[e]);
-            else uacc[0][e] = __fadd_rn(uacc[0][e], pv[e]);
-          }
+        for (int e = 0; e < 4; ++e) {
+          if (MT == 1 && (e & 1)) continue;            // M = 1: token 0 only
+          if (SW && pass) uacc[UG - 1][e] = __fadd_rn(uacc[UG - 1][e], pv[e]);
+          else uacc[0][e] = __fadd_rn(uacc[0][e], pv[e]);
         }
       } else if (!aborted && kp.fault != 1) {
         // peer: publish the piece. Each stored word is its own completion flag: it is
@@ -680,9 +899,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         // decoded back to +0.0), and the reducer waits for each word to become
         // non-zero -- no fence, no flag.
         asm volatile("griddepcontrol.wait;" ::: "memory");   // the workspace after earlier kernels
-        // the piece's first slab: in the second cell iff its last one is (pieces do not
-        // cross cells); grouped pieces are single slabs
-        const int slot = dense_cells ? ((pe - 1 >= smid ? 1 : 0) * UG + pass) : (pe - 1 - s0);
+        // dense: the piece is in the CTA's second cell iff its last slab is (pieces do
+        // not cross cells); grouped: one slot per (cell, pass) of the CTA's range
+        const int slot = dense_cells ? ((pe - 1 >= misc[8] ? 1 : 0) * UG + pass) : (cell_ord * UG + pass);
         unsigned* part = parts + ((int64_t)c * kp.maxslots + slot) * pstride;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -691,74 +910,47 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
           if (tok < R) st_relaxed(part + row * kp.mt + tok, encode_piece(pv[e]));
         }
       }
+      if constexpr (!dense_cells) {
+        if (pe == ce) ++cell_ord;
+      }
     }
 
     // ---- end of unit T in this CTA: this thread owns rows rA, rB and tokens 2tq, 2tq+1 ----
     asm volatile("griddepcontrol.wait;" ::: "memory");   // workspace and y after earlier kernels
-    if constexpr (MT == 1) {
-      if (reducer) {   // the running sums back into registers (valid in lanes tq == 0)
-        uacc[0][0] = usm[0];
-        uacc[UG - 1][0] = usm[UG - 1];
-        uacc[0][2] = usm[2];
-        uacc[UG - 1][2] = usm[2 + UG - 1];
-      }
-    }
     if (reducer && !aborted && tail > s1) {
-      // the pieces of unit T that later CTAs published, in slab order, KB at a time so
-      // that their load latencies overlap; each word is cleared after it is read (the
-      // workspace is all zero again when the call ends)
-      constexpr int KB = SW ? 2 : 4;
-      // the cell map again (recomputed here, so that it is not held through the slabs)
-      const CellMap cm = cell_map(kp.cells, kp.cpc, misc[1] * RT * G * UG, P);
-      int p = s1, cp = c + 1;
+      if (!mbar_wait(reinterpret_cast<uint64_t*>(smem + kGbarOff), 0u, a.status)) { misc[0] = 1; aborted = true; }
       if (kp.fault == 2) { atomicOr(a.status, kStatTimeout); misc[0] = 1; aborted = true; }
-      while (p < tail && !aborted) {
-        int base[KB], pps[KB];
-        bool valid[KB];
+      // the pieces of unit T that later CTAs published, in slab order, from the list
+      // the producer warp built, KB at a time so that their load latencies overlap; each
+      // word is cleared after it is read (the workspace is all zero again when the
+      // call ends)
+      constexpr int KB = SW ? 2 : 4;
+      constexpr int NE = MT == 1 ? 2 : 4;          // outputs e of this thread (M = 1: e = 0, 2)
+      const volatile int* glist = reinterpret_cast<const volatile int*>(smem + kGatherOff);
+      const int n = misc[2];
+      for (int i0 = 0; i0 < n && !aborted; i0 += KB) {
+        uint32_t u[KB][NE];
+        int pc[KB];
 #pragma unroll
         for (int k = 0; k < KB; ++k) {
-          valid[k] = p < tail;
-          base[k] = 0;
-          pps[k] = 0;
-          if (valid[k]) {
-            while (cm.cta_start(cp + 1) <= p) ++cp;       // the CTA holding slab p
-            const int ps = (SW && p - head >= G) ? 1 : 0;
-            int pe2, slot;
-            if (dense_cells) {
-              const int m = cm.cta_mid(cp);
-              const int kc = (p >= m) ? 1 : 0;            // its first or second cell
-              pe2 = kc ? cm.cta_start(cp + 1) : m;
-              if (pe2 > tail) pe2 = tail;
-              if (SW && ps == 0 && head + G < pe2) pe2 = head + G;
-              slot = kc * UG + ps;
-            } else {
-              pe2 = p + 1;
-              slot = p - cm.cta_start(cp);
-            }
-            base[k] = (cp * kp.maxslots + slot) * pstride;
-            pps[k] = ps;
-            p = pe2;
-          }
-        }
-        uint32_t u[KB][4];
+          pc[k] = (i0 + k < n) ? glist[i0 + k] : -1;
 #pragma unroll
-        for (int k = 0; k < KB; ++k) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
+          for (int j = 0; j < NE; ++j) {
+            const int e = MT == 1 ? 2 * j : j;
             const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
-            u[k][e] = 0u;
-            if (MT == 1 && (e & 1)) continue;
-            if (valid[k] && tok < R) u[k][e] = ld_relaxed(parts + base[k] + row * kp.mt + tok);
+            u[k][j] = 0u;
+            if (pc[k] >= 0 && tok < R) u[k][j] = ld_relaxed(parts + (pc[k] & ~1) + row * kp.mt + tok);
           }
         }
 #pragma unroll
         for (int k = 0; k < KB; ++k) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
+          for (int j = 0; j < NE; ++j) {
+            const int e = MT == 1 ? 2 * j : j;
             const int tok = 2 * tq + (e & 1), row = (e < 2) ? rA : rB;
-            if ((MT == 1 && (e & 1)) || !valid[k] || tok >= R || aborted) continue;
-            unsigned* wp = parts + base[k] + row * kp.mt + tok;
-            uint32_t v = u[k][e];
+            if (pc[k] < 0 || tok >= R || aborted) continue;
+            unsigned* wp = parts + (pc[k] & ~1) + row * kp.mt + tok;
+            uint32_t v = u[k][j];
             if (v == 0u) {
               const unsigned long long t0 = globaltimer();
               while ((v = ld_relaxed(wp)) == 0u) {
@@ -768,10 +960,22 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
             }
             st_relaxed(wp, 0u);
             const float f = decode_piece(v);
-            if (SW && pps[k]) uacc[UG - 1][e] = __fadd_rn(uacc[UG - 1][e], f);
+            if (SW && (pc[k] & 1)) uacc[UG - 1][e] = __fadd_rn(uacc[UG - 1][e], f);
             else uacc[0][e] = __fadd_rn(uacc[0][e], f);
           }
         }
+      }
+      if (!aborted && misc[5]) {
+        GatherArgs ga;
+        ga.misc = misc;
+        ga.glist = reinterpret_cast<const volatile int*>(smem + kGatherOff);
+        ga.parts = parts;
+        ga.status = a.status;
+        ga.wait_ns = kp.peer_wait_ns;
+        ga.cells = kp.cells; ga.cpc = kp.cpc; ga.gp = kp.gp; ga.S = S; ga.UL = UL; ga.G = G; ga.P = P;
+        ga.maxslots = kp.maxslots; ga.pstride = pstride; ga.mt = kp.mt; ga.R = R; ga.tq = tq;
+        ga.rA = rA; ga.rB = rB; ga.head = head; ga.tail = tail;
+        if (!gather_unit<MT, SW>(ga, &uacc[0][0])) aborted = true;
       }
     }
     if (reducer && !aborted) {
@@ -809,6 +1013,7 @@ StreamPlan plan_stream_dense(int64_t slabs, int M, int passes, int sms, bool two
   const int64_t v = slabs < 2 * (int64_t)sms ? slabs : 2 * (int64_t)sms;
   p.cells = (int)(v > 0 ? v : 1);
   p.cpc = (M <= 1 || two_cells) ? 2 : 1;
+  p.gp = 1;
   p.grid = (p.cells + p.cpc - 1) / p.cpc;
   p.maxslots = p.cpc * passes;          // a CTA publishes pieces of its first unit only
   p.ws_bytes = align_up((int64_t)p.grid * p.maxslots * piece_bytes(M), 256);
@@ -816,15 +1021,18 @@ StreamPlan plan_stream_dense(int64_t slabs, int M, int passes, int sms, bool two
 }
 
 StreamPlan plan_stream_grouped(int64_t slabs_max, int M, int passes, int64_t k_groups, int sms) {
+  (void)M;
   StreamPlan p;
-  const int64_t n = slabs_max < 2 * (int64_t)sms ? slabs_max : 2 * (int64_t)sms;
-  p.grid = (int)(n > 0 ? n : 1);
+  const int64_t unit = passes * k_groups;
   p.cells = 0;
   p.cpc = 1;
-  // every slab of a CTA's first unit but the unit's first one may be a published piece
-  const int64_t unit = passes * k_groups;
+  p.gp = 1;                 // every slab its own cell: CTA ranges stay slab-granular
+  const int64_t n = 2 * (int64_t)sms;
+  p.grid = (int)(slabs_max < n ? (slabs_max > 0 ? slabs_max : 1) : n);
+  // a CTA publishes the slabs of its first unit but the unit's first one; the slot of
+  // a slab is (its ordinal in the CTA's range) x passes + its pass
   const int64_t per_cta = (slabs_max + p.grid - 1) / p.grid;
-  int64_t ms = unit - 1 < per_cta ? unit - 1 : per_cta;
+  const int64_t ms = (unit - 1 < per_cta ? unit - 1 : per_cta) * passes;
   p.maxslots = (int)(ms > 0 ? ms : 1);
   p.ws_bytes = align_up((int64_t)p.grid * p.maxslots * piece_bytes(M), 256);
   return p;
@@ -883,6 +1091,7 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   if (!slab_count_ok(a.L, segs_max * (SW ? 2 : 1))) return cudaErrorInvalidValue;
   kp.cells = a.cells;
   kp.cpc = a.cpc;
+  kp.gp = a.gp;
   kp.maxslots = a.maxslots;
   kp.fault = g_fault;
   kp.peer_wait_ns = g_peer_wait_ns;
@@ -892,8 +1101,11 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   kp.partials = reinterpret_cast<float*>(a.ws);
   const int smem = kp.stage_base + kp.stages * kp.stage_bytes;
   // M = 1 grouped calls have an instance of their own (the producer's first-stage start)
-  const bool gr = MT == 1 && a.ids != nullptr;
-  void (*kern)(const KParams) = gr ? stream_kernel<FMT, MT, SW, MT == 1> : stream_kernel<FMT, MT, SW, false>;
+  // grouped calls have instances of their own (cells, and at M = 1 the producer's
+  // first-stage start)
+  const bool gr = a.ids != nullptr;
+  void (*kern)(const KParams) = gr ? stream_kernel<FMT, MT, SW, true> : stream_kernel<FMT, MT, SW, false>;
+  if (gr != (a.cells <= 0)) return cudaErrorInvalidValue;
   // opt in to the large dynamic shared memory once per device and instance (not per
   // launch, so that stream capture records launches only)
   static int opted[2][64] = {{0}};
