@@ -321,7 +321,8 @@ class DeviceWorkload:
         else:
             step_w = sum(canon_bytes(self.fmt, N, K) * (2 if (self.fused and i == 0) else 1)
                          for i, (_, N, K) in enumerate(self.mats))
-        self.copies = max(2, math.ceil(4 * L2_BYTES / max(step_w, 1)) + 1)
+        self.copies = rotation_copies(name)
+        assert self.copies == max(2, math.ceil(4 * L2_BYTES / max(step_w, 1)) + 1)
         self.packed = [base] + [[b.clone() for b in base] for _ in range(self.copies - 1)]
         # activations, outputs, workspaces
         self.x, self.y, self.ws = [], [], []
@@ -511,15 +512,10 @@ def run_device(args, rank, world, dev):
         "vs_baseline": None,
         "dtype": "f16" if wl.fmt in ("nvfp4", "fp8_row") else "bf16",
         "data": "synthetic (seeded N(0,0.02) weights quantized by the library, bf16 N(0,1) activations)",
-        "config": {
-            "workload": WORKLOADS[args.workload]["desc"],
-            "workload_id": args.workload,
-            "weights": wl.fmt,
-            "M": wl.M,
-            "matrices": [f"{n}[{N},{K}]" + (f"x{wl.E}" if wl.tower else "") for n, N, K in wl.mats],
+        "config": workload_config(args.workload),
+        "details": {
             "bytes_per_step": int(bytes_per_step),
-            "l2": f"inputs larger than L2: weights rotated over {wl.copies} copies "
-                  f"({wl.copies} x {int(bytes_per_step / 1e6)} MB per cycle)",
+            "rotation": f"{wl.copies} copies x {int(bytes_per_step / 1e6)} MB per cycle",
             "graph": f"CUDA graphs of {u} step(s) each",
             "arithmetic": "weights decoded exactly to " + ("f16" if wl.fmt in ("nvfp4", "fp8_row") else "bf16")
                           + ", products on mma.sync, fp32 accumulation",
@@ -549,8 +545,7 @@ def run_device(args, rank, world, dev):
         result["metric"] = "NVFP4 W4A4 prefill throughput (M=512)"
         result["unit"] = "TFLOP/s"
         result["dtype"] = "fp4 (e2m1 x e2m1, ue4m3 block scales, fp32 accumulation)"
-        result["config"]["arithmetic"] = "tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X, TMEM fp32 accumulators"
-        result["config"]["flops_per_step"] = wl.step_flops()
+        result["details"]["arithmetic"] = "tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X, TMEM fp32 accumulators"
         del result["pct_of_nominal_8000"]
         result["pct_of_peak"] = round(100.0 * value / world / peak, 2)
         result["roofline"].update({
@@ -565,9 +560,8 @@ def run_device(args, rank, world, dev):
         result["metric"] = f"{wl.fmt.upper()} prefill GEMM throughput (M=512)"
         result["unit"] = "TFLOP/s"
         result["dtype"] = f"f16 (exactly decoded {wl.fmt.upper()} sc*q x f16 x, fp32 accumulation)"
-        result["config"]["arithmetic"] = ("tcgen05.mma kind::f16, per-superblock TMEM accumulators folded with "
-                                          "d and dmin in fp32")
-        result["config"]["flops_per_step"] = wl.step_flops()
+        result["details"]["arithmetic"] = ("tcgen05.mma kind::f16, per-superblock TMEM accumulators folded with "
+                                           "d and dmin in fp32")
         del result["pct_of_nominal_8000"]
         result["pct_of_peak"] = round(100.0 * value / world / peak, 2)
         result["roofline"].update({
@@ -579,7 +573,7 @@ def run_device(args, rank, world, dev):
         result["e2e"]["unit"] = "TFLOP/s"
         result["e2e"]["value"] = round(wl.step_flops() * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, 2)
     if wl.tower:
-        result["config"]["unique_experts_mean"] = round(float(np.mean(wl.unique)), 2)
+        result["details"]["unique_experts_mean"] = round(float(np.mean(wl.unique)), 2)
     return result
 
 
@@ -600,6 +594,31 @@ def oracle_sample(workload, rows_per_mat):
         x = synth.bf16_bits(synth.activations(200 + i, w["M"], K))
         items.append((fmt, canon, r, K, x))
     return items
+
+
+def rotation_copies(workload):
+    """Packed weight copies the GPU arm rotates over: the bytes between two uses of one
+    copy exceed 4x the L2 cache (a function of the workload only)."""
+    w = WORKLOADS[workload]
+    fused, E = w.get("fused", False), w.get("E", 1)
+    per = [canon_bytes(w["fmt"], N, K) * (2 if (fused and i == 0) else 1) for i, (_, N, K) in enumerate(w["mats"])]
+    step_w = sum(per) * (min(E, w["M"] * w.get("topk", 1)) if w.get("tower") else 1)
+    return max(2, math.ceil(4 * L2_BYTES / max(step_w, 1)) + 1)
+
+
+def workload_config(workload):
+    """The `config` of both arms' JSON lines: what names the workload (its shapes,
+    format, batch) and how the timed region defeats L2; nothing about one arm's
+    implementation, so that the two arms' configs compare equal."""
+    w = WORKLOADS[workload]
+    cfg = {"workload": w["desc"], "workload_id": workload, "weights": w["fmt"], "M": w["M"],
+           "matrices": [f"{n}[{N},{K}]" + (f"x{w.get('E', 1)}" if w.get("tower") else "") for n, N, K in w["mats"]],
+           "l2": f"inputs larger than L2: weights rotated over {rotation_copies(workload)} copies"}
+    if w.get("tower"):
+        cfg["topk"] = w["topk"]
+    if tensor_workload(workload):
+        cfg["flops_per_step"] = sum(2.0 * w["M"] * N * K for _, N, K in w["mats"])
+    return cfg
 
 
 def tensor_workload(workload):
@@ -680,7 +699,7 @@ def run_reference(args):
         "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": args.gpus, "steps": K, "warmup": W,
         "ms_per_step": round(secs * 1e3 / max(K, 1), 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w["desc"], "workload_id": args.workload, "weights": w["fmt"], "M": w["M"]},
+        "config": workload_config(args.workload),
         "impl": "reference",
         "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

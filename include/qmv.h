@@ -112,28 +112,44 @@ size_t qmv_canon_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
  * Q5_K, Q6_K). Returns 0 if unsupported. */
 size_t qmv_pack_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
 
-/* Repack canonical bytes into the device layout. canon: device, qmv_canon_size
- * bytes. dst: device, qmv_pack_size bytes, 256-B aligned; fully overwritten
- * (header, slabs, padding). One-time load-phase work (the stacked tower loader
- * and planar repack of the pages), not part of the per-token path. */
+/* Repack canonical bytes into the device layout. Defined by: the stacked keep-quant
+ * tower loader whose packed residency the grouped kernel consumes, loaded once
+ * ("feat(BACKEND-TENSTORRENT-KEEPQUANT): the 27B arm — on-core decode residency, TT
+ * grouped keep-quant GEMM, e2e gate", Scope item 2: load-phase streaming, experts
+ * packed and fully resident), laid out as dense planes with the row on the lane axis
+ * ("A 320B MoE on a free Kaggle TPU", "The 110 GB claim, checked against the tensor
+ * index"). canon: device, qmv_canon_size bytes (the canonical stream of a whole
+ * tower; NVFP4 carries its per-matrix tensor scale inside it, FP8_ROW its row
+ * scales). dst: device, qmv_pack_size bytes, 256-B aligned; fully overwritten
+ * (header, slabs, padding). One-time load-phase work, not part of the per-token
+ * path. */
 qmv_status qmv_pack(qmv_fmt fmt, const void* canon, int64_t N, int64_t K, int64_t E,
                     void* dst, cudaStream_t stream);
 
 /* Encode fp32 W[rows, K] (device, row-major) into canonical bytes (device,
  * qmv_canon_size(fmt, rows, K, 1) bytes) with the round-to-nearest quantizers
- * used for synthetic data. tensor_scale is the NVFP4 per-tensor scale s_T (a
- * given constant); ignored for other formats. Not on the per-token path. */
+ * used for synthetic data. Defined by: quantizing on the host side of the load path,
+ * one tensor at a time, from the original weights ("Qwen3.8-27B on one Tenstorrent
+ * P150", "2. Building the 27B quant"); plain rounding, not the error-compensated
+ * variant of its section 8. tensor_scale is the NVFP4 per-tensor scale s_T (a given
+ * constant); ignored for other formats. Not on the per-token path. */
 qmv_status qmv_quantize(qmv_fmt fmt, const float* W, int64_t rows, int64_t K,
                         float tensor_scale, void* canon, cudaStream_t stream);
 
 /* BlockToFloat on the device layout: W_out[r][k] (fp32, device) for rows
- * row0 .. row0+rows-1 of the stacked tower (row = e*N + n). Bit-exact with the
- * canonical decode formulas above, in that op order. Used to check the layout. */
+ * row0 .. row0+rows-1 of the stacked tower (row = e*N + n). Defined by: the CPU
+ * BlockToFloat that the on-core word-shadow decode is held bit-exact against
+ * ("feat(BACKEND-TENSTORRENT-KEEPQUANT) ...", the W4 residency paragraph). Bit-exact
+ * with the canonical decode formulas above, in that op order. Used to check the
+ * layout. N, E and row0 are this library's additions (a window of a tower). */
 qmv_status qmv_dequant(qmv_fmt fmt, const void* packed, int64_t N, int64_t K, int64_t E,
                        int64_t row0, int64_t rows, float* W_out, cudaStream_t stream);
 
 /* Workspace bytes needed by an entry point for these sizes (host-only query; it
- * reads the SM count of the current device). The workspace must be zero-filled
+ * reads the SM count of the current device). This library's own call (the pages
+ * stage nothing per call: "feat(BACKEND-TENSTORRENT-KEEPQUANT) ...", Scope item 1,
+ * capture-safety -- every buffer is sized and allocated before capture, and replay
+ * allocates nothing); E and topk size the grouped entries. The workspace must be zero-filled
  * once before its first use. It holds the partial sums of row tiles split
  * between CTAs (a zero word means "not yet written"); a call that returns
  * without a device status error leaves the whole workspace zero again, so the
@@ -142,7 +158,13 @@ qmv_status qmv_dequant(qmv_fmt fmt, const void* packed, int64_t N, int64_t K, in
 size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, int64_t E,
                           int topk);
 
-/* Decode GEMV, M = 1..8: y[m][n] = sum_k W[n][k] * x[m][k].
+/* Decode GEMV, M = 1..8: y[m][n] = sum_k W[n][k] * x[m][k]. Defined by: the dense
+ * keep-quant matmul Y = X . W^T whose kernel decodes the packed weight words per call
+ * ("feat(BACKEND-TENSTORRENT-KEEPQUANT) ...", Scope item 1, MatmulBTQuantKernel; the
+ * "Re-anchor" comment: E = 1 covers dense), the M = 2..8 rows being the verify block
+ * of speculative decoding ("Qwen3.8-27B on one Tenstorrent P150", "5. DFlash2 on
+ * Blackhole"). Every row of an M-row call equals the one-row call on that row bit
+ * for bit: the order of the fp32 sums depends on (N, K) and the SM count only.
  * packed_W: device layout of one [N, K] matrix (E = 1). x: device bf16 [M][K]
  * (raw bits, row-major). y: device fp32 [M][N], fully overwritten. ws: device,
  * qmv_workspace_size(QMV_ENTRY_GEMV, ...) bytes. The weights are streamed from
@@ -219,7 +241,9 @@ qmv_status qmv_grouped_swiglu(qmv_fmt fmt, const void* tower, const int32_t* exp
                               const uint16_t* x, float* h, int M, int topk, int64_t N, int64_t K,
                               int64_t E, void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* NVFP4 activation quantizer (W4A4 prefill): per 16-value block of bf16 x[M][K],
+/* NVFP4 activation quantizer (W4A4 prefill: "I Built a Custom Blackwell Kernel for
+ * Qwen3.8-27B", "What the custom path actually does", quantising the activation into
+ * Blackwell's FP4 format with a static input scale): per 16-value block of bf16 x[M][K],
  * s_b = e4m3_rne_sat(amax_b / (6 x_scale)); codes = e2m1_rne_sat(x / (s_b x_scale)),
  * zero when s_b is zero. x_scale: the static per-site activation scale.
  * codes: device [M][K/2] (element 2i in the low nibble); scales: device [M][K/16]. */

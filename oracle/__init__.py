@@ -77,6 +77,8 @@ def _load():
     lib.or_quant_act_nvfp4.argtypes = [P, I64, I64, ctypes.c_float, P, P]
     lib.or_swiglu_f64.restype = None
     lib.or_swiglu_f64.argtypes = [P, P, I64, P]
+    lib.or_w4a4_f64.restype = None
+    lib.or_w4a4_f64.argtypes = [P, I64, I64, ctypes.c_float, P, I64, P, P]
     _lib = lib
     return lib
 
@@ -182,6 +184,23 @@ def quant_act_nvfp4(x_bf16: np.ndarray, x_scale: float):
     scales = np.zeros((M, K // 16), dtype=np.uint8)
     _load().or_quant_act_nvfp4(_ptr(x), M, K, float(x_scale), _ptr(codes), _ptr(scales))
     return codes, scales
+
+
+def w4a4_f64(W: np.ndarray, x_bf16: np.ndarray, x_scale: float):
+    """W4A4 reference: the activation quantized by the oracle's NVFP4 quantizer under
+    the static x_scale and dequantized (e2m1 * e4m3 * x_scale), then fp64 dots with the
+    BlockToFloat weights W[N, K]. Returns (y [M, N], den [M, N] = sum |terms|)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    N, K = W.shape
+    M = x.shape[0]
+    assert x.shape[1] == K and K % 16 == 0
+    y = np.empty((M, N), dtype=np.float64)
+    den = np.empty((M, N), dtype=np.float64)
+    _load().or_w4a4_f64(_ptr(x), M, K, float(x_scale), _ptr(W), N, _ptr(y), _ptr(den))
+    return y, den
 
 
 def swiglu_f64(g: np.ndarray, u: np.ndarray) -> np.ndarray:

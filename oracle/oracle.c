@@ -496,6 +496,40 @@ void or_quant_act_nvfp4(const uint16_t* x_bf16, int64_t M, int64_t K, float x_sc
         }
 }
 
+/* W4A4 prefill ("I Built a Custom Blackwell Kernel for Qwen3.8-27B", "What the
+ * custom path actually does": W4A4 kernels after the activation is quantised to
+ * NVFP4). The activation goes through the quantizer above with the given static
+ * x_scale, each value is dequantized as e2m1(code) * e4m3(s_b) * x_scale, and
+ * y[m][n] = sum_k a[m][k] * W[n][k] in fp64 over the BlockToFloat weights W (which
+ * carry the tensor scale); den[m][n] = sum_k |a[m][k] * W[n][k]|. */
+void or_w4a4_f64(const uint16_t* x_bf16, int64_t M, int64_t K, float x_scale, const float* W, int64_t N,
+                 double* y, double* den) {
+    uint8_t* codes = (uint8_t*)malloc((size_t)(M * (K / 2)));
+    uint8_t* scales = (uint8_t*)malloc((size_t)(M * (K / 16)));
+    double* a = (double*)malloc(sizeof(double) * (size_t)K);
+    or_quant_act_nvfp4(x_bf16, M, K, x_scale, codes, scales);
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t k = 0; k < K; k++) {
+            uint8_t c = (uint8_t)((codes[m * (K / 2) + k / 2] >> (4 * (k & 1))) & 15);
+            a[k] = (double)or_e2m1_to_f32(c) * (double)or_e4m3_to_f32(scales[m * (K / 16) + k / 16]) *
+                   (double)x_scale;
+        }
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0, ab = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double t = a[k] * (double)W[n * K + k];
+                acc += t;
+                ab += fabs(t);
+            }
+            y[m * N + n] = acc;
+            if (den) den[m * N + n] = ab;
+        }
+    }
+    free(codes);
+    free(scales);
+    free(a);
+}
+
 /* SwiGLU of the gate/up projection read as one ("Qwen3.8-27B on one Tenstorrent
  * P150", "4. Measuring the ceiling, and lots of dead ends": the MLP gate/up
  * projection and its fused SwiGLU; "A 320B MoE on a free Kaggle TPU": the gate

@@ -74,6 +74,11 @@ int64_t or_unique_experts(const int32_t* ids, int64_t n, int32_t* out);
 void or_quant_act_nvfp4(const uint16_t* x_bf16, int64_t M, int64_t K, float x_scale,
                         uint8_t* codes, uint8_t* scales);
 
+/* W4A4: y[m][n] = sum_k dq(quant_act(x))[m][k] * W[n][k] in fp64, W = BlockToFloat of
+ * the NVFP4 weights [N][K]; den = sum |terms| */
+void or_w4a4_f64(const uint16_t* x_bf16, int64_t M, int64_t K, float x_scale, const float* W, int64_t N,
+                 double* y, double* den);
+
 /* SwiGLU: h = silu(g) * u, silu(g) = g / (1 + exp(-g)), fp64 elementwise */
 void or_swiglu_f64(const double* g, const double* u, int64_t n, double* h);
 

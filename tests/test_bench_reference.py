@@ -30,6 +30,21 @@ def test_reference_line_rank0():
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload_id"] == "q8_0_tiny"
+    # the same config as the GPU arm prints (both come from bench.workload_config)
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["config"] == json.loads(json.dumps(bench.workload_config("q8_0_tiny")))
+
+
+def test_every_workload_config_is_gpu_free():
+    """Every workload's config is computable on a machine without a GPU (it names the
+    workload only) and states how the timed region defeats L2."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for name in bench.WORKLOADS:
+        cfg = bench.workload_config(name)
+        assert cfg["workload_id"] == name and cfg["l2"].startswith("inputs larger than L2")
+        assert bench.rotation_copies(name) >= 2
 
 
 def test_reference_other_ranks_do_nothing():

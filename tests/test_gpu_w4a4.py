@@ -1,9 +1,9 @@
 """GPU parity of the NVFP4 W4A4 prefill GEMM (tcgen05 block-scaled MMA).
 
-Expected values come from the CPU oracle only: its NVFP4 activation quantizer
-(the same static x_scale), its BlockToFloat of the weights, and fp64 dots of the
-dequantized operands. The quantized activations are dequantized with the
-oracle's own scalar decoders (E2M1 and E4M3 tables built from them).
+Expected values come from the CPU oracle alone (oracle.w4a4_f64): its NVFP4
+activation quantizer under the same static x_scale, the dequantized activations,
+its BlockToFloat of the weights and fp64 dots, with the sum of |terms| as the
+error scale. The test assembles no expected value of its own.
 """
 import numpy as np
 import pytest
@@ -15,9 +15,6 @@ from cases import TOL, device_matrix, host_dequant, host_matrix, host_rows_dequa
 
 pytestmark = pytest.mark.gpu
 
-E2M1 = np.array([oracle.e2m1_to_f32(c) for c in range(16)], dtype=np.float64)
-E4M3 = np.array([oracle.e4m3_to_f32(c) for c in range(256)], dtype=np.float64)
-
 
 @pytest.fixture(scope="module")
 def q():
@@ -27,26 +24,8 @@ def q():
     return q
 
 
-def act_dequant(x, x_scale):
-    """Oracle-quantized activations, dequantized in fp64: e2m1(c) * e4m3(s_b) * x_scale."""
-    xb = synth.bf16_bits(x)
-    codes, scales = oracle.quant_act_nvfp4(xb, x_scale)
-    M, K = xb.shape
-    c = np.empty((M, K), dtype=np.int64)
-    c[:, 0::2] = codes & 15
-    c[:, 1::2] = codes >> 4
-    s = np.repeat(scales.astype(np.int64), 16, axis=1)
-    return E2M1[c] * E4M3[s] * np.float64(x_scale)
-
-
 def x_scale_of(x):
     return float(np.float32(np.abs(x.float().numpy()).max()) / np.float32(2688.0))
-
-
-def ref_w4a4(Wd, Xd):
-    """fp64 y[m][n] = sum_k Xd[m,k] Wd[n,k] and the normalising sum of |terms|."""
-    Wd = Wd.astype(np.float64)
-    return Xd @ Wd.T, np.abs(Xd) @ np.abs(Wd).T
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (200, 384, 1024), (130, 640, 512), (1, 128, 256)])
@@ -55,7 +34,7 @@ def test_w4a4_small(q, M, N, K):
     Wd = host_dequant("nvfp4", canon, N, K)
     x = synth.activations(43 + M, M, K)
     xs = x_scale_of(x)
-    ref, den = ref_w4a4(Wd, act_dequant(x, xs))
+    ref, den = oracle.w4a4_f64(Wd, synth.bf16_bits(x), xs)
     packed = q.qmv_pack("nvfp4", torch.from_numpy(canon).cuda(), N, K)
     ws = q.workspace(q.QMV_ENTRY_W4A4, "nvfp4", M, N, K)
     y = q.qmv_gemm_nvfp4_w4a4(packed, x.cuda(), xs, N, K, ws)
@@ -75,7 +54,7 @@ def test_w4a4_split_k_deterministic_and_clean(q, M, N, K):
     Wd = host_dequant("nvfp4", canon, N, K)
     x = synth.activations(53 + M, M, K)
     xs = x_scale_of(x)
-    ref, den = ref_w4a4(Wd, act_dequant(x, xs))
+    ref, den = oracle.w4a4_f64(Wd, synth.bf16_bits(x), xs)
     packed = q.qmv_pack("nvfp4", torch.from_numpy(canon).cuda(), N, K)
     ws = q.workspace(q.QMV_ENTRY_W4A4, "nvfp4", M, N, K)
     y1 = q.qmv_gemm_nvfp4_w4a4(packed, x.cuda(), xs, N, K, ws).clone()
@@ -105,7 +84,7 @@ def test_w4a4_full_size_sampled(q, N, K):
     got = y[:, torch.from_numpy(rows).cuda()].cpu().numpy()
     assert q.qmv_device_status() == 0
     Wd = host_rows_dequant("nvfp4", seed, rows, N, K)
-    ref, den = ref_w4a4(Wd, act_dequant(x, xs))
+    ref, den = oracle.w4a4_f64(Wd, synth.bf16_bits(x), xs)
     assert norm_err(got, ref, den) <= TOL
     assert bool(torch.isfinite(y).all())
 

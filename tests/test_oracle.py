@@ -609,3 +609,59 @@ def test_swiglu_odd_part_is_identity():
     # linear in u
     u = rng.normal(size=1000)
     assert np.allclose(oracle.swiglu_f64(x, 3.0 * u), 3.0 * oracle.swiglu_f64(x, u), rtol=1e-15, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# W4A4: the activation quantized (static x_scale), dequantized, fp64 dots
+# ---------------------------------------------------------------------------
+def _bf16_bits_of(vals):
+    return synth.bf16_bits(torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).reshape(1, -1))
+
+
+def test_w4a4_handbuilt_literal():
+    """One token, two 16-value blocks, x_scale = 1. Block 0 has amax 6 -> block scale
+    1.0; 2.59375 (bf16 of 2.6) rounds to the E2M1 value 3. Block 1 has amax 12 -> block
+    scale 2.0, and 0.75 / 2 = 0.375 rounds to 0.5 -> 1.0. Worked by hand:
+    y = 6*0.5 - 3*2 + 1.5*(-1) + 0*4 + 3*1 + 0.5*8 + 12*0.25 + 1*(-2) = 3.5,
+    sum |terms| = 3 + 6 + 1.5 + 0 + 3 + 4 + 3 + 2 = 22.5."""
+    x = np.zeros(32, dtype=np.float32)
+    x[:6] = [6.0, -3.0, 1.5, 0.0, 2.6, 0.5]
+    x[16:18] = [12.0, 0.75]
+    W = np.zeros((1, 32), dtype=np.float32)
+    W[0, :6] = [0.5, 2.0, -1.0, 4.0, 1.0, 8.0]
+    W[0, 16:18] = [0.25, -2.0]
+    y, den = oracle.w4a4_f64(W, _bf16_bits_of(x), 1.0)
+    assert y[0, 0] == 3.5 and den[0, 0] == 22.5
+
+
+def test_w4a4_handbuilt_static_scale():
+    """x_scale = 0.25: block amax 1.5 -> scale e4m3(1.5 / (6 * 0.25)) = 1.0; 1.5 ->
+    code 6 -> 6 * 1 * 0.25 = 1.5; bf16(0.3) = 0.30078125 -> 1.203125 -> E2M1 1 -> 0.25.
+    y = 1.5 * 2 + 0.25 * 4 = 4."""
+    x = np.zeros(16, dtype=np.float32)
+    x[:2] = [1.5, 0.3]
+    W = np.zeros((2, 16), dtype=np.float32)
+    W[0, :2] = [2.0, 4.0]
+    W[1, :2] = [-1.0, 0.0]
+    y, den = oracle.w4a4_f64(W, _bf16_bits_of(x), 0.25)
+    assert y[0].tolist() == [4.0, -1.5]
+    assert den[0].tolist() == [4.0, 1.5]
+
+
+def test_w4a4_on_grid_activations_reduce_to_gemv():
+    """Activations already on the NVFP4 grid (E2M1 values times a power of two per
+    block, each block holding its 6 * 2^k) quantize without error, so the W4A4 result
+    equals the plain fp64 GEMV of the same weights."""
+    rng = np.random.default_rng(17)
+    M, N, K = 3, 40, 128
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], dtype=np.float32)
+    x = grid[rng.integers(0, 8, size=(M, K))] * np.where(rng.random((M, K)) < 0.5, -1, 1).astype(np.float32)
+    x = x.reshape(M, K // 16, 16)
+    x[:, :, 0] = 6.0
+    x = x * np.float32(2.0) ** rng.integers(-2, 3, size=(M, K // 16, 1)).astype(np.float32)
+    x = x.reshape(M, K)
+    xb = synth.bf16_bits(torch.from_numpy(x).to(torch.bfloat16))
+    W = synth.weights(19, N, K).numpy()
+    y, den = oracle.w4a4_f64(W, xb, 1.0)
+    ref, dref = oracle.gemv_f64(W, xb)
+    assert np.array_equal(y, ref) and np.array_equal(den, dref)

@@ -55,6 +55,17 @@ MUTANTS = [
     ("activation nibble order", "codes[m * (K / 2) + e / 2] |= (uint8_t)(c << (4 * (e & 1)));",
      "codes[m * (K / 2) + e / 2] |= (uint8_t)(c << (4 * (1 - (e & 1))));"),
     ("distinct experts sorted descending", "while (j >= 0 && out[j] > v)", "while (j >= 0 && out[j] < v)"),
+    ("w4a4 takes the raw activations",
+     "a[k] = (double)or_e2m1_to_f32(c) * (double)or_e4m3_to_f32(scales[m * (K / 16) + k / 16]) *\n"
+     "                   (double)x_scale;",
+     "a[k] = (double)or_bf16_to_f32(x_bf16[m * K + k]) + 0.0 * (double)c * (double)scales[0] *\n"
+     "                   (double)x_scale;"),
+    ("w4a4 static scale dropped",
+     "a[k] = (double)or_e2m1_to_f32(c) * (double)or_e4m3_to_f32(scales[m * (K / 16) + k / 16]) *\n"
+     "                   (double)x_scale;",
+     "a[k] = (double)or_e2m1_to_f32(c) * (double)or_e4m3_to_f32(scales[m * (K / 16) + k / 16]) *\n"
+     "                   1.0;"),
+    ("w4a4 error scale signed", "                ab += fabs(t);", "                ab += t;"),
 ]
 
 
