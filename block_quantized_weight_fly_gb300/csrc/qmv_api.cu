@@ -109,7 +109,7 @@ size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, i
     const int passes = entry == QMV_ENTRY_SWIGLU ? 2 : 1;
     Layout L;
     if (M > QMV_MAX_M || !make_layout((int)fmt, N, K, passes, &L)) return 0;
-    return (size_t)plan_stream_dense(passes * L.row_tiles * L.k_groups, M, passes, sms, false).ws_bytes;
+    return (size_t)plan_stream_dense(passes * L.row_tiles * L.k_groups, M, passes, sms).ws_bytes;
   }
   if (entry == QMV_ENTRY_GROUPED || entry == QMV_ENTRY_GROUPED_SWIGLU) {
     const int passes = entry == QMV_ENTRY_GROUPED_SWIGLU ? 2 : 1;
@@ -142,7 +142,7 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
   if (!aligned(packed_W, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
-  const StreamPlan plan = plan_stream_dense(L.row_tiles * L.k_groups, M, 1, sms, false);
+  const StreamPlan plan = plan_stream_dense(L.row_tiles * L.k_groups, M, 1, sms);
   if (ws_bytes < (size_t)plan.ws_bytes) return QMV_EWORKSPACE;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
@@ -205,7 +205,7 @@ qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, fl
   if (!aligned(tower, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(h, 4)) return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
-  const StreamPlan plan = plan_stream_dense(2 * L.row_tiles * L.k_groups, M, 2, sms, false);
+  const StreamPlan plan = plan_stream_dense(2 * L.row_tiles * L.k_groups, M, 2, sms);
   if (ws_bytes < (size_t)plan.ws_bytes) return QMV_EWORKSPACE;
   unsigned* status = status_ptr();
   if (!status) return QMV_ECUDA;
@@ -389,9 +389,9 @@ extern "C" qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const 
   if (!aligned(packed_W, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
   const int sms = num_sms_current_device();
   if (sms <= 0) return QMV_ECUDA;
-  // two cells per CTA at every M (one CTA per SM): the cells, and so the order of
-  // the sums, are those of qmv_gemv, whose results this entry reproduces bit for bit
-  const StreamPlan plan = plan_stream_dense(L.row_tiles * L.k_groups, M, 1, sms, true);
+  // the plan of qmv_gemv: the same cells, and so the same order of the sums, whose
+  // results this entry reproduces bit for bit
+  const StreamPlan plan = plan_stream_dense(L.row_tiles * L.k_groups, M, 1, sms);
   if ((size_t)plan.ws_bytes > (size_t)QMV_STATIC_SCRATCH_BYTES) return QMV_EWORKSPACE;
   uint8_t* scratch = nullptr;
   qmv_status st = scratch_ptr(&scratch);

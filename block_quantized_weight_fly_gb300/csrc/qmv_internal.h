@@ -35,16 +35,16 @@ struct StreamArgs {
 // Grid, accumulation cells and workspace of one stream-kernel call (host side),
 // shared by the entry points and the workspace size query.
 //  - dense: V = min(2 x SMs, slabs) cells, a function of the matrix and the SM count
-//    only, so that every M (and the no-workspace entry) adds in the same order;
-//    two cells per CTA at M = 1 (one CTA per SM, so the next call's CTAs fit beside
-//    it) or when two_cells is set, else one (two CTAs per SM);
+//    only, so that every M (and the no-workspace entry) adds in the same order; one
+//    cell per CTA (two CTAs per SM) at M > 1 or when cells are 8 slabs or longer,
+//    else two (one CTA per SM, so the next call's CTAs fit beside it);
 //  - grouped: every slab is a cell (gp = 1), whatever the routing; two CTAs per SM.
 // passes: 1, or 2 for the fused gate|up (gate and up sums).
 struct StreamPlan {
   int grid, cells, cpc, gp, maxslots;
   int64_t ws_bytes;          // split-K workspace (published pieces), 256-byte multiple
 };
-StreamPlan plan_stream_dense(int64_t slabs, int M, int passes, int sms, bool two_cells);
+StreamPlan plan_stream_dense(int64_t slabs, int M, int passes, int sms);
 StreamPlan plan_stream_grouped(int64_t slabs_max, int M, int passes, int64_t k_groups, int sms);
 // Test hook of the reduction (see qmv_debug_split_k_fault in qmv.h): mode 1, peers
 // publish nothing and reducers wait peer_wait_ns, then latch QMV_ETIMEOUT; mode 2,

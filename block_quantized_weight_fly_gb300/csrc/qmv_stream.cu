@@ -1008,11 +1008,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
 // ---------------------------------------------------------------------------
 static int64_t piece_bytes(int M) { return (int64_t)kSlabRows * (M <= 1 ? 1 : 8) * 4; }
 
-StreamPlan plan_stream_dense(int64_t slabs, int M, int passes, int sms, bool two_cells) {
+StreamPlan plan_stream_dense(int64_t slabs, int M, int passes, int sms) {
   StreamPlan p;
   const int64_t v = slabs < 2 * (int64_t)sms ? slabs : 2 * (int64_t)sms;
   p.cells = (int)(v > 0 ? v : 1);
-  p.cpc = (M <= 1 || two_cells) ? 2 : 1;
+  // One cell per CTA, two CTAs per SM, whose warps hide each other's latency: at
+  // M > 1 and for long cells (8 slabs or more). Short cells at M = 1: two cells per
+  // CTA, one CTA per SM, so that the next call's CTAs are resident beside this
+  // call's and copy their first slabs meanwhile. Either way the cells, and so the
+  // order of the sums, are the same.
+  p.cpc = (M > 1 || slabs >= 8 * (int64_t)p.cells) ? 1 : 2;
   p.gp = 1;
   p.grid = (p.cells + p.cpc - 1) / p.cpc;
   p.maxslots = p.cpc * passes;          // a CTA publishes pieces of its first unit only

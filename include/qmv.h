@@ -189,10 +189,11 @@ qmv_status qmv_gemv(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float*
  * left: each call first clears the words it uses on `stream` (cudaMemsetAsync, no
  * allocation). Calls that overlap in time (on other streams or host threads)
  * race on the array; the caller must serialize them.
- * Its grid is one CTA per SM at every M, and it adds up in the same order as
- * qmv_gemv, so its results equal qmv_gemv's bit for bit. Its partial sums take
- * (CTAs) x 2 x 128 x c x 4 bytes (c = 1 at M = 1, else 8; rounded up to 256): at
- * most 8 KiB per SM, 1,245,184 bytes on a 152-SM GB300. Returns QMV_EWORKSPACE
+ * It runs qmv_gemv's grid and adds up in the same cells and order, so its results
+ * equal qmv_gemv's bit for bit. Its partial sums take one 128 x c x 4-byte record
+ * per cell of the slab sequence (at most 2 cells per SM; c = 1 at M = 1, else 8;
+ * rounded up to 256): at most 8 KiB per SM, 1,245,184 bytes on a 152-SM GB300.
+ * Returns QMV_EWORKSPACE
  * when that exceeds QMV_STATIC_SCRATCH_BYTES (M = 2..8 on a device of more than 512
  * SMs). Otherwise arguments, results and errors as qmv_gemv. */
 qmv_status qmv_gemv_noalloc(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y,
