@@ -20,9 +20,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
-Q8_0, Q4_K, Q6_K, NVFP4, FP8_ROW, Q5_K = 1, 2, 3, 4, 5, 6
+Q8_0, Q4_K, Q6_K, NVFP4, FP8_ROW, Q5_K, IQ4_XS = 1, 2, 3, 4, 5, 6, 7
 FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "q6_k": Q6_K, "nvfp4": NVFP4, "fp8_row": FP8_ROW,
-           "q5_k": Q5_K}
+           "q5_k": Q5_K, "iq4_xs": IQ4_XS}
+CODEBOOK_FORMATS = ("iq4_xs",)
 
 _lib = None
 
@@ -67,6 +68,8 @@ def _load():
     lib.or_canon_bytes.argtypes = [ctypes.c_int, I64, I64]
     lib.or_encode.restype = ctypes.c_int
     lib.or_encode.argtypes = [ctypes.c_int, P, I64, I64, ctypes.c_float, P]
+    lib.or_encode_cb.restype = ctypes.c_int
+    lib.or_encode_cb.argtypes = [ctypes.c_int, P, I64, I64, P, P]
     lib.or_block_to_float.restype = ctypes.c_int
     lib.or_block_to_float.argtypes = [ctypes.c_int, P, I64, I64, P]
     lib.or_gemv_f64.restype = None
@@ -131,12 +134,18 @@ def canon_bytes(fmt, rows: int, K: int) -> int:
 
 
 # ---- matrices -----------------------------------------------------------------
-def encode(fmt, W: np.ndarray, tensor_scale: float = 0.0) -> np.ndarray:
-    """fp32 W[rows, K] -> canonical bytes (synthetic-data encoder)."""
+def encode(fmt, W: np.ndarray, tensor_scale: float = 0.0, codebook=None) -> np.ndarray:
+    """fp32 W[rows, K] -> canonical bytes (synthetic-data encoder). The codebook
+    formats (IQ4_XS) take the matrix's codebook, 16 int8 values."""
     W = np.ascontiguousarray(W, dtype=np.float32)
     rows, K = W.shape
     out = np.zeros(canon_bytes(fmt, rows, K), dtype=np.uint8)
-    rc = _load().or_encode(_fmt(fmt), _ptr(W), rows, K, float(tensor_scale), _ptr(out))
+    if _fmt(fmt) == IQ4_XS:
+        cb = np.ascontiguousarray(codebook, dtype=np.int8)
+        assert cb.shape == (16,)
+        rc = _load().or_encode_cb(_fmt(fmt), _ptr(W), rows, K, _ptr(cb), _ptr(out))
+    else:
+        rc = _load().or_encode(_fmt(fmt), _ptr(W), rows, K, float(tensor_scale), _ptr(out))
     if rc:
         raise ValueError(f"or_encode failed ({rc}) for fmt={fmt} K={K}")
     return out

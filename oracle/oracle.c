@@ -22,7 +22,10 @@
  * family, named with Q4_K/Q6_K/Q8_0 in "#3030" scope item 1 and owed by the
  * grouped kernel in its "Re-anchor" comment; the pages print no layout for it, so
  * it is Q4_K's header and nibbles plus one 32-byte plane of fifth bits), NVFP4 16-value blocks with an E4M3 scale and one fp32
- * tensor scale, FP8 E4M3 with one fp32 scale per row.
+ * tensor scale, FP8 E4M3 with one fp32 scale per row. IQ4_XS 136 B / 256 ("A 320B MoE
+ * on a free Kaggle TPU", section "What '3-bit' costs, measured": the GGUF block
+ * sizes of the codebook formats): a weight is an entry of the matrix's 16-value
+ * codebook times its sub-block scale.
  *
  * Where the pages give no bit-level layout, the reading taken is the one written
  * in oracle.h (the plainest one consistent with the printed sizes).
@@ -132,6 +135,7 @@ int64_t or_block_values(int fmt) {
     case OR_Q6_K: return 256;
     case OR_NVFP4: return 16;
     case OR_FP8_ROW: return 1;
+    case OR_IQ4_XS: return 256;
     default: return 0;
     }
 }
@@ -144,6 +148,7 @@ int64_t or_canon_bytes(int fmt, int64_t rows, int64_t K) {
     case OR_Q6_K: return rows * (K / 256) * 210;
     case OR_NVFP4: return rows * (K / 2) + rows * (K / 16) + 4;
     case OR_FP8_ROW: return rows * K + rows * 4;
+    case OR_IQ4_XS: return rows * (K / 256) * 136 + 16;
     default: return -1;
     }
 }
@@ -285,6 +290,58 @@ static void enc_q6_k_block(const float* x, uint8_t* blk) {
     wr16(blk + 208, d);
 }
 
+/* IQ4_XS: sub-block j gets the signed scale s_j that maps its element of largest
+ * magnitude onto the codebook entry of largest magnitude (the first such entry);
+ * d = max_j |s_j| / 31 rounded to fp16; ls_j = clamp(rint(s_j / d) + 32, 0, 63); each
+ * element takes the entry c nearest to it, |w - a_j C[c]| with a_j = d (ls_j - 32)
+ * (fp32), ties to the lower index. */
+static void enc_iq4_xs_block(const float* x, const int8_t* cb, uint8_t* blk) {
+    int cm = 0;
+    for (int c = 1; c < 16; c++)
+        if (abs(cb[c]) > abs(cb[cm])) cm = c;
+    float s[8], smax = 0.0f;
+    for (int j = 0; j < 8; j++) {
+        int em = 0;
+        for (int i = 1; i < 32; i++)
+            if (fabsf(x[32 * j + i]) > fabsf(x[32 * j + em])) em = i;
+        s[j] = (cb[cm] != 0) ? x[32 * j + em] / (float)cb[cm] : 0.0f;
+        if (fabsf(s[j]) > smax) smax = fabsf(s[j]);
+    }
+    memset(blk, 0, 136);
+    uint16_t dh = or_f32_to_fp16(smax / 31.0f);
+    float d = or_fp16_to_f32(dh);
+    wr16(blk, dh);
+    uint16_t sh = 0;
+    for (int j = 0; j < 8; j++) {
+        int ls = 32;
+        if (d > 0.0f) ls = (int)clampf(rintf(s[j] / d) + 32.0f, 0.0f, 63.0f);
+        sh |= (uint16_t)(((ls >> 4) & 3) << (2 * j));
+        blk[4 + j / 2] |= (uint8_t)((ls & 15) << (4 * (j & 1)));
+        float a = d * (float)(ls - 32);
+        for (int i = 0; i < 32; i++) {
+            int best = 0;
+            float be = fabsf(x[32 * j + i] - a * (float)cb[0]);
+            for (int c = 1; c < 16; c++) {
+                float e = fabsf(x[32 * j + i] - a * (float)cb[c]);
+                if (e < be) { be = e; best = c; }
+            }
+            int e = 32 * j + i;
+            blk[8 + e / 2] |= (uint8_t)(best << (4 * (e & 1)));
+        }
+    }
+    wr16(blk + 2, sh);
+}
+
+int or_encode_cb(int fmt, const float* W, int64_t rows, int64_t K, const int8_t* codebook,
+                 uint8_t* canon) {
+    if (fmt != OR_IQ4_XS || K % 256 != 0 || codebook == NULL) return 1;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t b = 0; b < K / 256; b++)
+            enc_iq4_xs_block(W + r * K + b * 256, codebook, canon + (r * (K / 256) + b) * 136);
+    memcpy(canon + rows * (K / 256) * 136, codebook, 16);
+    return 0;
+}
+
 int or_encode(int fmt, const float* W, int64_t rows, int64_t K, float tensor_scale,
               uint8_t* canon) {
     int64_t bv = or_block_values(fmt);
@@ -348,6 +405,7 @@ int or_encode(int fmt, const float* W, int64_t rows, int64_t K, float tensor_sca
  *   Q6_K : w = (d * sc_j) * (q - 32)                   (exact)
  *   NVFP4: w = (e2m1(c) * e4m3(s_b)) * s_T             (one rounding)
  *   FP8  : w = e4m3(c) * s_row                         (one rounding)
+ *   IQ4_XS: w = (d * (ls_j - 32)) * C[q]               (one rounding)
  * ------------------------------------------------------------------------- */
 static int nvfp4_to_float(const uint8_t* canon, int64_t rows, int64_t K, float* W) {
     const uint8_t* codes = canon;
@@ -371,13 +429,32 @@ static int fp8_row_to_float(const uint8_t* canon, int64_t rows, int64_t K, float
     return 0;
 }
 
-/* For NVFP4 and FP8_ROW `canon` is the whole matrix stream of `rows` rows
- * (codes, scales, then the tensor scale / row scales). */
+static int iq4_xs_to_float(const uint8_t* canon, int64_t rows, int64_t K, float* W) {
+    const int8_t* cb = (const int8_t*)(canon + rows * (K / 256) * 136);
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t b = 0; b < K / 256; b++) {
+            const uint8_t* blk = canon + (r * (K / 256) + b) * 136;
+            float d = or_fp16_to_f32(rd16(blk));
+            int sh = rd16(blk + 2);
+            for (int e = 0; e < 256; e++) {
+                int j = e / 32;
+                int ls = ((blk[4 + j / 2] >> (4 * (j & 1))) & 15) | (((sh >> (2 * j)) & 3) << 4);
+                int q = (blk[8 + e / 2] >> (4 * (e & 1))) & 15;
+                float a = d * (float)(ls - 32);
+                W[r * K + b * 256 + e] = a * (float)cb[q];
+            }
+        }
+    return 0;
+}
+
+/* For NVFP4, FP8_ROW and IQ4_XS `canon` is the whole matrix stream of `rows` rows
+ * (codes, scales, then the tensor scale / row scales / codebook). */
 int or_block_to_float(int fmt, const uint8_t* canon, int64_t rows, int64_t K, float* W) {
     int64_t bv = or_block_values(fmt);
     if (bv == 0 || K % bv != 0) return 1;
     if (fmt == OR_NVFP4) return nvfp4_to_float(canon, rows, K, W);
     if (fmt == OR_FP8_ROW) return fp8_row_to_float(canon, rows, K, W);
+    if (fmt == OR_IQ4_XS) return iq4_xs_to_float(canon, rows, K, W);
     for (int64_t r = 0; r < rows; r++) {
         float* w = W + r * K;
         if (fmt == OR_Q8_0) {

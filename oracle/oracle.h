@@ -29,6 +29,13 @@
  *   NVFP4 per matrix: codes [rows][K/2] (element 2i in the low nibble of byte i)
  *         | E4M3 block scales [rows][K/16] | fp32 tensor scale
  *   FP8_ROW per matrix: E4M3 codes [rows][K] | fp32 row scales [rows]
+ *   IQ4_XS per matrix: 136-byte blocks of 256 values [rows][K/256] | codebook C,
+ *         16 x int8. Block: fp16 d | u16 sh | 4 B sl | 128 B indices. Scale of
+ *         32-value sub-block j: ls_j = (sl byte j/2, nibble j%2) | (sh bits 2j..2j+1)
+ *         << 4, in 0..63; index byte b: low nibble = element 2b, high = 2b+1.
+ *         The pages fix the block size (136 B / 256) and that a weight is a
+ *         codebook entry; the field order, the signed scale ls - 32 and the
+ *         caller-supplied codebook are this reading (no GGUF layout is printed).
  * A stacked tower of E experts is E such matrices back to back (for the
  * K-quants this is the same bytes as one [E*N, K] matrix).
  */
@@ -41,7 +48,7 @@
 extern "C" {
 #endif
 
-enum { OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q6_K = 3, OR_NVFP4 = 4, OR_FP8_ROW = 5, OR_Q5_K = 6 };
+enum { OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q6_K = 3, OR_NVFP4 = 4, OR_FP8_ROW = 5, OR_Q5_K = 6, OR_IQ4_XS = 7 };
 
 /* scalar number formats */
 float or_fp16_to_f32(uint16_t h);
@@ -59,6 +66,9 @@ int64_t or_canon_bytes(int fmt, int64_t rows, int64_t K);
 /* encoders: synthetic-data generation only (not on the hot path) */
 int or_encode(int fmt, const float* W, int64_t rows, int64_t K, float tensor_scale,
               uint8_t* canon);
+/* the codebook formats (IQ4_XS): the matrix's codebook C (16 x int8) is an input */
+int or_encode_cb(int fmt, const float* W, int64_t rows, int64_t K, const int8_t* codebook,
+                 uint8_t* canon);
 
 /* BlockToFloat: canonical bytes of `rows` rows -> fp32 W[rows][K] */
 int or_block_to_float(int fmt, const uint8_t* canon, int64_t rows, int64_t K, float* W);

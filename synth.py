@@ -21,6 +21,7 @@ minus six: mean 0, variance 1 (to within 2^-32), support [-6, 6].
   activations:  x = bf16_rne(z)                      -- N(0, 1)
   expert ids:   per token, a partial Fisher-Yates shuffle of range(E) driven by
                 the same hash: top-k distinct ids, uniform without replacement.
+  codebooks:    the same shuffle over -127..127: n distinct int8 values, sorted.
 
 Element index i of a weight matrix W[N, K] of stream s is r*K + k; a stacked
 tower of E experts uses r = e*N + n, so any subset of rows can be regenerated on
@@ -37,6 +38,7 @@ M32 = 0xFFFFFFFF
 STREAM_W = 1
 STREAM_X = 2
 STREAM_IDS = 3
+STREAM_CODEBOOK = 4
 
 
 def _mul32(x: torch.Tensor, c: int) -> torch.Tensor:
@@ -144,6 +146,18 @@ def expert_ids(seed: int, M: int, topk: int, E: int, stream: int = STREAM_IDS) -
             perm[j], perm[r] = perm[r], perm[j]
             out[t, j] = perm[j]
     return out
+
+
+def codebook(seed: int, n: int = 16, stream: int = STREAM_CODEBOOK) -> np.ndarray:
+    """int8 codebook[n]: n distinct values drawn uniformly from -127..127 (a partial
+    Fisher-Yates shuffle driven by the hash), ascending."""
+    key = _key(seed, stream, 0)
+    perm = list(range(-127, 128))
+    for j in range(n):
+        h = _lowbias32_int(_lowbias32_int(j ^ key) ^ 0x3C6EF372)
+        r = j + h % (len(perm) - j)
+        perm[j], perm[r] = perm[r], perm[j]
+    return np.array(sorted(perm[:n]), dtype=np.int8)
 
 
 def bf16_bits(x: torch.Tensor) -> np.ndarray:

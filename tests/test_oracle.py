@@ -319,6 +319,86 @@ def test_fp8_row_handbuilt():
 
 
 # ---------------------------------------------------------------------------
+# IQ4_XS: 136-byte blocks, a weight is a codebook entry times its sub-block scale
+# ---------------------------------------------------------------------------
+CB_HAND = [-127, -100, -60, -33, -20, -9, -2, 0, 1, 5, 11, 25, 40, 66, 90, 127]
+
+
+def _iq4xs_block(d16, ls, q):
+    """IQ4_XS as read: fp16 d, u16 of scale high bits, 4 bytes of scale low nibbles,
+    128 bytes of index nibbles (element 2b low, 2b+1 high)."""
+    blk = bytearray(136)
+    blk[0:2] = d16.to_bytes(2, "little")
+    sh = 0
+    for j in range(8):
+        sh |= ((ls[j] >> 4) & 3) << (2 * j)
+        blk[4 + j // 2] |= (ls[j] & 15) << (4 * (j & 1))
+    blk[2:4] = sh.to_bytes(2, "little")
+    for b in range(128):
+        blk[8 + b] = q[2 * b] | (q[2 * b + 1] << 4)
+    return bytes(blk)
+
+
+def _iq4xs_decode(blocks, cb, rows, K):
+    canon = b"".join(blocks) + bytes(np.array(cb, dtype=np.int8).view(np.uint8))
+    return oracle.block_to_float("iq4_xs", np.frombuffer(canon, np.uint8), rows, K)
+
+
+def test_iq4_xs_sizes_match_pages():
+    g = _golden()
+    assert oracle.canon_bytes("iq4_xs", 1, 256) - 16 == g["iq4_xs_block_bytes"] == 136
+    assert (oracle.canon_bytes("iq4_xs", 1, 256) - 16) * 8 / 256 == g["iq4_xs_bits_per_weight"]
+    assert oracle.canon_bytes("iq4_xs", 1, 32 * 256) - 16 == g["fixture_iq4_xs_bytes"]   # 32 blocks
+
+
+def test_iq4_xs_handbuilt_values():
+    # d = 0.5; ls = 33, 31, 0, 63, then 32 (scale 0); q = e % 16
+    blk = _iq4xs_block(0x3800, [33, 31, 0, 63, 32, 32, 32, 32], [e % 16 for e in range(256)])
+    w = _iq4xs_decode([blk], CB_HAND, 1, 256)[0]
+    # e=0: a = 0.5 * 1, C[0] = -127 -> -63.5        e=1: 0.5 * -100 -> -50
+    # e=33: a = 0.5 * -1, C[1] = -100 -> 50         e=47: a = -0.5, C[15] = 127 -> -63.5
+    # e=64: a = 0.5 * -32 = -16, C[0] -> 2032       e=79: -16 * 127 -> -2032
+    # e=111: a = 0.5 * 31 = 15.5, C[15] -> 1968.5    e=103: 15.5 * C[7] = 0 -> 0
+    # e=200: a = 0 -> 0
+    hand = {0: -63.5, 1: -50.0, 33: 50.0, 47: -63.5, 64: 2032.0, 79: -2032.0, 111: 1968.5, 103: 0.0,
+            200: 0.0}
+    for e, v in hand.items():
+        assert w[e] == v, (e, w[e], v)
+
+
+def test_iq4_xs_every_index_reads_its_entry():
+    """d = 1, ls = 33 (scale 1): the decoded values are the codebook itself, in index order."""
+    blk = _iq4xs_block(0x3C00, [33] * 8, [e % 16 for e in range(256)])
+    cb = synth.codebook(5)
+    w = _iq4xs_decode([blk], cb, 1, 256)[0]
+    assert np.array_equal(w, np.tile(cb.astype(np.float32), 16))
+
+
+@pytest.mark.parametrize("j", range(8))
+def test_iq4_xs_scale_bit_positions(j):
+    """Only sub-block j gets ls = 48 (low nibble 0, high bits 3 -> scale 16); the low
+    nibble alone (ls = 15 -> -17) is checked the same way."""
+    for ls_hot, a in ((48, 16.0), (15, -17.0)):
+        ls = [32] * 8
+        ls[j] = ls_hot
+        w = _iq4xs_decode([_iq4xs_block(0x3C00, ls, [15] * 256)], CB_HAND, 1, 256)[0]
+        want = np.zeros(256, np.float32)
+        want[32 * j:32 * j + 32] = a * 127
+        assert np.array_equal(w, want), (j, ls_hot)
+
+
+def test_iq4_xs_codebook_per_matrix_in_a_tower():
+    """Two experts back to back, each with its own codebook after its blocks."""
+    blk = _iq4xs_block(0x3C00, [33] * 8, [3] * 256)
+    cb0, cb1 = synth.codebook(1), synth.codebook(2)
+    canon = (blk + bytes(cb0.view(np.uint8))) + (blk + bytes(cb1.view(np.uint8)))
+    per = oracle.canon_bytes("iq4_xs", 1, 256)
+    w0 = oracle.block_to_float("iq4_xs", np.frombuffer(canon[:per], np.uint8), 1, 256)[0]
+    w1 = oracle.block_to_float("iq4_xs", np.frombuffer(canon[per:], np.uint8), 1, 256)[0]
+    assert np.all(w0 == float(cb0[3])) and np.all(w1 == float(cb1[3]))
+
+
+# ---------------------------------------------------------------------------
 # encode -> decode round trips on N(0, 0.02) data and edge blocks
 # ---------------------------------------------------------------------------
 def _data(rows, K, seed=0):
@@ -432,6 +512,34 @@ def test_roundtrip_fp8_row():
     bound = np.maximum(np.abs(W) * 2**-4, s[:, None] * 2**-10) * (1 + 2**-20)
     assert np.all(np.abs(W - D) <= bound + 1e-12)
     assert np.all(D[0] == 0)
+
+
+@pytest.mark.parametrize("cb_seed", [0, 7])
+def test_roundtrip_iq4_xs(cb_seed):
+    """Error of each element <= |a_j| x (half the widest gap of the codebook, or the
+    codebook's shortfall on the side opposite its largest entry) + the scale's
+    rounding, (d / 2) |C_ext|; all-zero rows decode to zero."""
+    W = _data(8, 1024)
+    cb = CB_HAND if cb_seed == 0 else list(synth.codebook(cb_seed))
+    c = oracle.encode("iq4_xs", W, codebook=cb)
+    assert list(c[-16:].view(np.int8)) == list(cb)
+    D = oracle.block_to_float("iq4_xs", c, 8, 1024)
+    blocks = c[:-16].reshape(8, 4, 136)
+    d = _f16(blocks[:, :, 0].astype(np.uint16) | (blocks[:, :, 1].astype(np.uint16) << 8))
+    sh = blocks[:, :, 2].astype(np.int64) | (blocks[:, :, 3].astype(np.int64) << 8)
+    cbs = np.array(sorted(cb), dtype=np.float64)
+    ext = cbs[np.argmax(np.abs(cbs))]
+    opp = np.max(np.abs(cbs[np.sign(cbs) == -np.sign(ext)])) if np.any(np.sign(cbs) == -np.sign(ext)) else 0.0
+    reach = max(np.max(np.diff(cbs)) / 2, abs(ext) - opp)
+    for j in range(8):
+        ls = ((blocks[:, :, 4 + j // 2].astype(np.int64) >> (4 * (j & 1))) & 15) | (((sh >> (2 * j)) & 3) << 4)
+        a = d * (ls - 32)
+        bound = np.abs(a) * reach + d / 2 * abs(ext) + 1e-6
+        err = np.abs(W - D).reshape(8, 4, 8, 32)[:, :, j, :].max(-1)
+        assert np.all(err <= bound), j
+    assert np.all(D[0] == 0)
+    rel = np.linalg.norm(W[3:] - D[3:]) / np.linalg.norm(W[3:])
+    assert rel < 0.25
 
 
 # ---------------------------------------------------------------------------

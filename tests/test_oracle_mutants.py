@@ -66,6 +66,18 @@ MUTANTS = [
      "a[k] = (double)or_e2m1_to_f32(c) * (double)or_e4m3_to_f32(scales[m * (K / 16) + k / 16]) *\n"
      "                   1.0;"),
     ("w4a4 error scale signed", "                ab += fabs(t);", "                ab += t;"),
+    ("iq4_xs scale offset sign", "float a = d * (float)(ls - 32);\n                W[r * K + b * 256 + e]",
+     "float a = d * (float)(32 - ls);\n                W[r * K + b * 256 + e]"),
+    ("iq4_xs scale nibble order", "int ls = ((blk[4 + j / 2] >> (4 * (j & 1))) & 15)",
+     "int ls = ((blk[4 + j / 2] >> (4 * (1 - (j & 1)))) & 15)"),
+    ("iq4_xs scale high bits one per bit", "(((sh >> (2 * j)) & 3) << 4);\n                int q",
+     "(((sh >> j) & 3) << 4);\n                int q"),
+    ("iq4_xs index nibble order", "int q = (blk[8 + e / 2] >> (4 * (e & 1))) & 15;\n                float a = d * (float)(ls",
+     "int q = (blk[8 + e / 2] >> (4 * (1 - (e & 1)))) & 15;\n                float a = d * (float)(ls"),
+    ("iq4_xs sub-blocks of 16", "                int j = e / 32;\n                int ls = ((blk[4",
+     "                int j = (e / 16) & 7;\n                int ls = ((blk[4"),
+    ("iq4_xs codebook read before the blocks", "const int8_t* cb = (const int8_t*)(canon + rows * (K / 256) * 136);",
+     "const int8_t* cb = (const int8_t*)(canon);"),
 ]
 
 
