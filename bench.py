@@ -111,6 +111,15 @@ WORKLOADS = {
                            mats=[("gate|up", 2048, 4096), ("down", 4096, 2048)],
                            desc="grouped Q4_K tower, 288 experts, top-8, M=8: fused gate|up with the SwiGLU "
                                 "epilogue, then down"),
+    "iq4xs_tower_down_m1": dict(fmt="iq4_xs", M=1, tower=True, E=288, topk=8, mats=[("down", 4096, 2048)],
+                                desc="grouped IQ4_XS down-projection tower, 288 experts [4096,2048], a 16-entry "
+                                     "codebook per expert, top-8, one x row per pair, M=1"),
+    "iq4xs_tower_down_m8": dict(fmt="iq4_xs", M=8, tower=True, E=288, topk=8, mats=[("down", 4096, 2048)],
+                                desc="grouped IQ4_XS down-projection tower, 288 experts [4096,2048], top-8, M=8"),
+    "iq4xs_mlp_m1": dict(fmt="iq4_xs", M=1, mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
+                                                  ("down", QWEN_HIDDEN, QWEN_MLP)],
+                         desc="IQ4_XS codebook GEMV at the Qwen3.8-27B MLP shapes (gate, up [17408,5120], "
+                              "down [5120,17408]), M=1"),
 }
 DEFAULT_WORKLOAD = "q4k_mlp_m1"
 DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, "q6k_head_m8": 2000,
@@ -119,11 +128,12 @@ DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, 
                  "tower_m4": 10000, "tower_m8": 5000, "nvfp4_w4a4_m512": 2000,
                  "q4k_mlp_fused_m1": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000,
                  "tower_fused_m1": 20000, "tower_fused_m8": 5000, "q4k_prefill_m512": 2000,
-                 "q5k_prefill_m512": 2000}
+                 "q5k_prefill_m512": 2000, "iq4xs_tower_down_m1": 20000, "iq4xs_tower_down_m8": 5000,
+                 "iq4xs_mlp_m1": 20000}
 
 METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"
 CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q5_k": 176 / 256, "q6_k": 210 / 256,
-                   "nvfp4": 18 / 32, "fp8_row": 1.0}
+                   "nvfp4": 18 / 32, "fp8_row": 1.0, "iq4_xs": 136 / 256}
 
 
 def canon_bytes(fmt, N, K):
@@ -131,6 +141,8 @@ def canon_bytes(fmt, N, K):
         return N * K // 2 + N * K // 16 + 4
     if fmt == "fp8_row":
         return N * K + 4 * N
+    if fmt == "iq4_xs":
+        return N * (K // 256) * 136 + 16
     return int(round(N * K * CANON_PER_VALUE[fmt]))
 
 
@@ -274,6 +286,11 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # device workload
 # ----------------------------------------------------------------------------
+def codebook_of(seed, e):
+    """The IQ4_XS codebook of expert e of a seeded matrix (16 int8 values)."""
+    return synth.codebook(seed + 7919 * e)
+
+
 def build_packed(q, fmt, seed, N, K, E, dev):
     """Seeded weights -> library quantizer -> packed device tower (load phase, untimed)."""
     chunk_rows = max(1, (1 << 26) // K)
@@ -283,6 +300,15 @@ def build_packed(q, fmt, seed, N, K, E, dev):
             W = synth.weights(seed, N, K, device=dev, row0=e * N, chunk_rows=chunk_rows)
             canon_parts.append(q.qmv_quantize(fmt, W, NVFP4_TS if fmt == "nvfp4" else 0.0))
             del W
+        elif fmt == "iq4_xs":
+            # each expert's stream: its blocks, then its own codebook
+            cb = codebook_of(seed, e)
+            for r0 in range(0, N, chunk_rows):
+                n = min(chunk_rows, N - r0)
+                W = synth.weights(seed, n, K, device=dev, row0=e * N + r0, chunk_rows=n)
+                canon_parts.append(q.qmv_quantize_codebook(fmt, W, cb)[:n * (K // 256) * 136])
+                del W
+            canon_parts.append(torch.from_numpy(cb.view(np.uint8).copy()).to(dev))
         else:
             for r0 in range(0, N, chunk_rows):
                 n = min(chunk_rows, N - r0)
@@ -590,7 +616,8 @@ def oracle_sample(workload, rows_per_mat):
     for i, (_, N, K) in enumerate(w["mats"]):
         r = min(rows_per_mat[i], N)
         W = synth.weights_rows(100 + i, np.arange(r), K).numpy()
-        canon = oracle.encode(fmt, W, NVFP4_TS if fmt == "nvfp4" else 0.0)
+        canon = oracle.encode(fmt, W, NVFP4_TS if fmt == "nvfp4" else 0.0,
+                              codebook=codebook_of(100 + i, 0) if fmt == "iq4_xs" else None)
         x = synth.bf16_bits(synth.activations(200 + i, w["M"], K))
         items.append((fmt, canon, r, K, x))
     return items

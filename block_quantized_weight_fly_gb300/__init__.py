@@ -16,9 +16,9 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqmv.so")
 
-QMV_Q8_0, QMV_Q4_K, QMV_Q6_K, QMV_NVFP4, QMV_FP8_ROW, QMV_Q5_K = 1, 2, 3, 4, 5, 6
+QMV_Q8_0, QMV_Q4_K, QMV_Q6_K, QMV_NVFP4, QMV_FP8_ROW, QMV_Q5_K, QMV_IQ4_XS = 1, 2, 3, 4, 5, 6, 7
 FORMATS = {"q8_0": QMV_Q8_0, "q4_k": QMV_Q4_K, "q6_k": QMV_Q6_K, "nvfp4": QMV_NVFP4,
-           "fp8_row": QMV_FP8_ROW, "q5_k": QMV_Q5_K}
+           "fp8_row": QMV_FP8_ROW, "q5_k": QMV_Q5_K, "iq4_xs": QMV_IQ4_XS}
 QMV_ENTRY_GEMV, QMV_ENTRY_GROUPED, QMV_ENTRY_W4A4, QMV_ENTRY_SWIGLU = 1, 2, 3, 4
 QMV_ENTRY_GROUPED_SWIGLU, QMV_ENTRY_KQUANT = 5, 6
 QMV_MAX_M = 8
@@ -56,6 +56,7 @@ _canon_size = _sig("qmv_canon_size", _SZ, [_I, _I64, _I64, _I64])
 _pack_size = _sig("qmv_pack_size", _SZ, [_I, _I64, _I64, _I64])
 _pack = _sig("qmv_pack", _I, [_I, _P, _I64, _I64, _I64, _P, _P])
 _quantize = _sig("qmv_quantize", _I, [_I, _P, _I64, _I64, _F, _P, _P])
+_quantize_cb = _sig("qmv_quantize_codebook", _I, [_I, _P, _I64, _I64, _P, _P, _P])
 _dequant = _sig("qmv_dequant", _I, [_I, _P, _I64, _I64, _I64, _I64, _I64, _P, _P])
 _ws_size = _sig("qmv_workspace_size", _SZ, [_I, _I, _I, _I64, _I64, _I64, _I])
 _gemv = _sig("qmv_gemv", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
@@ -75,7 +76,7 @@ EXPORTED = ["qmv_canon_size", "qmv_pack_size", "qmv_pack", "qmv_quantize", "qmv_
             "qmv_workspace_size", "qmv_gemv", "qmv_grouped", "qmv_quant_act_nvfp4",
             "qmv_gemm_nvfp4_w4a4", "qmv_status_str", "qmv_last_route", "qmv_device_status",
             "qmv_gemv_noalloc", "qmv_gemv_swiglu", "qmv_grouped_swiglu", "qmv_gemm_kquant",
-            "qmv_debug_split_k_fault"]
+            "qmv_debug_split_k_fault", "qmv_quantize_codebook"]
 
 
 def _fmt(fmt) -> int:
@@ -217,6 +218,26 @@ def qmv_quantize(fmt, W: torch.Tensor, tensor_scale: float = 0.0, canon: torch.T
         raise ValueError(f"canon must be a contiguous CUDA tensor of at least {size} bytes")
     _check(_quantize(_fmt(fmt), _ptr(W), rows, K, float(tensor_scale), _ptr(canon), _stream(stream)),
            "qmv_quantize")
+    return canon
+
+
+def qmv_quantize_codebook(fmt, W: torch.Tensor, codebook, canon: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """The codebook formats' encoder: codebook = 16 int8 values (host sequence)."""
+    _dev(W, "W")
+    if W.dtype != torch.float32 or W.dim() != 2 or not W.is_contiguous():
+        raise ValueError("W must be a contiguous 2-D float32 tensor")
+    if len(codebook) != 16:
+        raise ValueError("codebook must hold 16 values")
+    cb = (ctypes.c_int8 * 16)(*[int(v) for v in codebook])
+    rows, K = W.shape
+    size = qmv_canon_size(fmt, rows, K, 1)
+    if canon is None:
+        canon = torch.empty(size, dtype=torch.uint8, device=W.device)
+    elif not canon.is_cuda or not canon.is_contiguous() or canon.numel() * canon.element_size() < size:
+        raise ValueError(f"canon must be a contiguous CUDA tensor of at least {size} bytes")
+    _check(_quantize_cb(_fmt(fmt), _ptr(W), rows, K, ctypes.cast(cb, ctypes.c_void_p), _ptr(canon),
+                        _stream(stream)), "qmv_quantize_codebook")
     return canon
 
 

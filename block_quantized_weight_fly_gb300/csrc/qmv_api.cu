@@ -38,7 +38,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 qmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ECUDA; }
 
-bool valid_fmt(int f) { return f >= QMV_Q8_0 && f <= QMV_Q5_K; }
+bool valid_fmt(int f) { return f >= QMV_Q8_0 && f <= QMV_IQ4_XS; }
 
 void apply_plan(StreamArgs* a, const StreamPlan& p) {
   a->num_ctas = p.grid;
@@ -80,9 +80,22 @@ qmv_status qmv_quantize(qmv_fmt fmt, const float* W, int64_t rows, int64_t K, fl
                         void* canon, cudaStream_t stream) {
   if (!valid_fmt(fmt) || !W || !canon || rows <= 0 || K <= 0) return QMV_EINVAL;
   if (qmv_canon_size(fmt, rows, K, 1) == 0) return QMV_EUNSUPPORTED;
+  if (fmt == QMV_IQ4_XS) return QMV_EUNSUPPORTED;     // needs a codebook (an input, not a rounding)
   if (fmt == QMV_NVFP4 && !(tensor_scale >= 0.0f)) return QMV_EINVAL;
   if (!aligned(W, 4)) return QMV_EALIGN;
   qmv_status st = from_cuda(launch_quantize((int)fmt, W, rows, K, tensor_scale, static_cast<uint8_t*>(canon), stream));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + 7;
+  return st;
+}
+
+qmv_status qmv_quantize_codebook(qmv_fmt fmt, const float* W, int64_t rows, int64_t K, const int8_t* codebook,
+                                 void* canon, cudaStream_t stream) {
+  if (fmt != QMV_IQ4_XS) return valid_fmt(fmt) ? QMV_EUNSUPPORTED : QMV_EINVAL;
+  if (!W || !codebook || !canon || rows <= 0 || K <= 0) return QMV_EINVAL;
+  if (qmv_canon_size(fmt, rows, K, 1) == 0) return QMV_EUNSUPPORTED;
+  if (!aligned(W, 4)) return QMV_EALIGN;
+  qmv_status st = from_cuda(launch_quantize_codebook((int)fmt, W, rows, K, codebook,
+                                                     static_cast<uint8_t*>(canon), stream));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + 7;
   return st;
 }

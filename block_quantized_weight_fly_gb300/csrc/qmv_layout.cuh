@@ -16,6 +16,11 @@
 //   Q6_K : record = 128 B ql | 64 B qh | 16 B int8 scales                     (208 B)
 //          plus a second plane of n_pad fp16 d                                (2 B)
 //   FP8  : record = 256 E4M3 codes, its 16-byte vectors rotated by (row & 7)  (256 B)
+//   IQ4_XS: record = 128 B of codebook indices, thread-major 16-byte vectors rotated
+//          by (row & 7) (below)                                              (128 B)
+//          plus a plane B per 128-row tile: the rows' 8-byte scale fields (fp16 d,
+//          u16 sh, u32 sl, canonical order), then the matrix's 16-byte codebook, so
+//          that every slab copy brings its codebook along         (128 x 8 + 16 B)
 //
 // so the bytes of (any row range) x (one k-group) are one contiguous span per
 // plane: one bulk copy moves a 128-row x 256-value slab into shared memory. The
@@ -46,6 +51,9 @@
 //          8s + 2k, 8s + 2k + 16 (k indexes the same four pairs as the ql word)
 // NVFP4 and FP8 codes keep their canonical order (element 2i in the low nibble or
 // byte), which the hardware FP4/FP8 -> f16x2 conversions consume directly.
+// IQ4_XS: word t of chunk j = the canonical index bytes of elements 8t..8t+7 (element
+// 8t+i at nibble i, unchanged); the 16-byte vector v = 2t + (j >> 2) of the record
+// holds the words of chunks 4(j >> 2) .. +3 of thread t, stored at 16 (v ^ (row & 7)).
 //
 // NVFP4 tiles. The codes of a 128-row tile of a k-group (16 KB) are stored as the
 // K-major "core matrices" of the 5th-generation tensor core: 8 rows x 16 bytes (32
@@ -86,7 +94,10 @@ constexpr int kHeaderBytes = 256;
 constexpr uint32_t kMagic = 0x31564D51u;  // "QMV1"
 constexpr uint32_t kVersion = 5;
 
-enum Fmt { F_Q8_0 = 1, F_Q4_K = 2, F_Q6_K = 3, F_NVFP4 = 4, F_FP8 = 5, F_Q5_K = 6 };
+enum Fmt { F_Q8_0 = 1, F_Q4_K = 2, F_Q6_K = 3, F_NVFP4 = 4, F_FP8 = 5, F_Q5_K = 6, F_IQ4_XS = 7 };
+constexpr int F_LAST = F_IQ4_XS;
+// IQ4_XS plane B per 128-row tile: 8 bytes of scale fields per row, then the codebook
+constexpr int kIq4TileB = 128 * 8 + 16;
 
 struct PackedHeader {                 // first 256 bytes of a packed buffer
   uint32_t magic, version, fmt, reserved;
@@ -98,7 +109,7 @@ __host__ __device__ inline int64_t align_up(int64_t v, int64_t a) { return (v + 
 
 // Granule of K the packed layout serves.
 __host__ __device__ inline int64_t k_granule(int fmt) {
-  return (fmt == F_Q4_K || fmt == F_Q5_K || fmt == F_Q6_K) ? 256 : (fmt == F_NVFP4 ? 16 : 32);
+  return (fmt == F_Q4_K || fmt == F_Q5_K || fmt == F_Q6_K || fmt == F_IQ4_XS) ? 256 : (fmt == F_NVFP4 ? 16 : 32);
 }
 
 // bytes of one row record of plane A (per 256 values)
@@ -110,6 +121,7 @@ __host__ __device__ inline int rec_bytes(int fmt) {
     case F_Q6_K: return 208;
     case F_NVFP4: return 128;
     case F_FP8: return 256;
+    case F_IQ4_XS: return 128;
     default: return 0;
   }
 }
@@ -122,7 +134,8 @@ struct Layout {
   int64_t n_pad;        // N rounded up to 128
   int64_t k_groups;     // ceil(K / 256)
   int64_t plane_a;      // bytes of one k-group's plane A (n_pad * rec)
-  int64_t plane_b;      // bytes of one k-group's plane B (Q6_K d: n_pad * 2; NVFP4 scales: n_pad * 16), else 0
+  int64_t plane_b;      // bytes of one k-group's plane B (Q6_K d: n_pad * 2; NVFP4 scales: n_pad * 16;
+                        // IQ4_XS: row_tiles * (128 * 8 + 16)), else 0
   int64_t group_bytes;  // plane_a + plane_b
   int64_t extras;       // per-expert extras bytes (aligned to 256)
   int64_t expert_bytes; // bytes per expert (aligned to 256)
@@ -130,7 +143,7 @@ struct Layout {
 };
 
 __host__ __device__ inline bool make_layout(int fmt, int64_t N, int64_t K, int64_t E, Layout* L) {
-  if (fmt < F_Q8_0 || fmt > F_Q5_K || N <= 0 || K <= 0 || E <= 0) return false;
+  if (fmt < F_Q8_0 || fmt > F_LAST || N <= 0 || K <= 0 || E <= 0) return false;
   if (K % k_granule(fmt) != 0 || K % 32 != 0) return false;
   L->fmt = fmt;
   L->rec = rec_bytes(fmt);
@@ -139,7 +152,10 @@ __host__ __device__ inline bool make_layout(int fmt, int64_t N, int64_t K, int64
   L->n_pad = L->row_tiles * kSlabRows;
   L->k_groups = (K + kSlabK - 1) / kSlabK;
   L->plane_a = L->n_pad * L->rec;
-  L->plane_b = (fmt == F_Q6_K) ? L->n_pad * 2 : (fmt == F_NVFP4) ? L->n_pad * 16 : 0;
+  L->plane_b = (fmt == F_Q6_K)     ? L->n_pad * 2
+               : (fmt == F_NVFP4)  ? L->n_pad * 16
+               : (fmt == F_IQ4_XS) ? L->row_tiles * kIq4TileB
+                                   : 0;
   L->group_bytes = L->plane_a + L->plane_b;
   int64_t ex = 0;
   if (fmt == F_NVFP4) ex = 256;
@@ -158,6 +174,7 @@ __host__ __device__ inline int64_t canon_matrix_bytes(int fmt, int64_t N, int64_
     case F_Q6_K: return N * (K / 256) * 210;
     case F_NVFP4: return N * (K / 2) + N * (K / 16) + 4;
     case F_FP8: return N * K + N * 4;
+    case F_IQ4_XS: return N * (K / 256) * 136 + 16;
     default: return 0;
   }
 }
@@ -186,6 +203,13 @@ __host__ __device__ inline int q6k_ql_word_off(int t, int j) { return 32 * t + 4
 __host__ __device__ inline int q6k_qh_word_off(int h, int j) { return 128 + 32 * h + 4 * j; }
 // FP8: 16-byte vector v (0..15) of row r sits at 16 * (v ^ (r & 7))
 __host__ __device__ inline int fp8_v_off(int v, int r) { return 16 * (v ^ (r & 7)); }
+// IQ4_XS: index word t of chunk j of row r, and the offset (within the k-group's plane
+// B) of row n's scale fields and of the codebook copy of its tile
+__host__ __device__ inline int iq4_word_off(int t, int j, int r) {
+  return 16 * ((2 * t + (j >> 2)) ^ (r & 7)) + 4 * (j & 3);
+}
+__host__ __device__ inline int64_t iq4_scale_off(int64_t n) { return (n >> 7) * kIq4TileB + (n & 127) * 8; }
+__host__ __device__ inline int64_t iq4_codebook_off(int64_t n) { return (n >> 7) * kIq4TileB + 128 * 8; }
 
 // ---- scalar decoders (exact) -------------------------------------------------
 __device__ __forceinline__ float h2f(uint32_t h) {

@@ -110,6 +110,17 @@ __global__ void pack_kernel(Layout L, const uint8_t* __restrict__ canon, uint8_t
       copy_bytes(rec + fp8_v_off(2 * cl + 1, r), ce + n * L.K + 32 * c + 16, 16);
       if (c == 0) copy_bytes(extras + 4 * n, ce + L.N * L.K + 4 * n, 4);
     } break;
+    case F_IQ4_XS: {
+      const uint8_t* ce = canon + e * canon_matrix_bytes(F_IQ4_XS, L.N, L.K);
+      const uint8_t* blk = ce + (n * (L.K / 256) + g) * 136;
+      const int r = (int)(n & 7);
+      for (int wd = 0; wd < 4; ++wd)
+        *reinterpret_cast<uint32_t*>(rec + iq4_word_off(wd, cl, r)) = load_u32(blk + 8 + 16 * cl + 4 * wd);
+      if (cl == 0) copy_bytes(plane + L.plane_a + iq4_scale_off(n), blk, 8);
+      // every 128-row tile's plane B ends with the matrix's codebook
+      if (cl == 0 && (n & 127) == 0)
+        copy_bytes(plane + L.plane_a + iq4_codebook_off(n), ce + L.N * (L.K / 256) * 136, 16);
+    } break;
   }
 }
 
@@ -214,6 +225,20 @@ __global__ void dequant_kernel(Layout L, const uint8_t* __restrict__ packed, int
       const float s = reinterpret_cast<const float*>(extras)[n];
       for (int i = 0; i < 16; ++i) o[i] = __fmul_rn(e4m3f(c0[i]), s);
       for (int i = 0; i < 16; ++i) o[16 + i] = __fmul_rn(e4m3f(c1[i]), s);
+    } break;
+    case F_IQ4_XS: {
+      const uint8_t* sf = plane + L.plane_a + iq4_scale_off(n);
+      const int8_t* cb = reinterpret_cast<const int8_t*>(plane + L.plane_a + iq4_codebook_off(n));
+      const float d = h2f(*reinterpret_cast<const uint16_t*>(sf));
+      const uint32_t sh = *reinterpret_cast<const uint16_t*>(sf + 2);
+      const uint32_t sl = *reinterpret_cast<const uint32_t*>(sf + 4);
+      const int ls = (int)(((sl >> (4 * cl)) & 15u) | (((sh >> (2 * cl)) & 3u) << 4));
+      const float a = __fmul_rn(d, (float)(ls - 32));
+      const int r = (int)(n & 7);
+      for (int wd = 0; wd < 4; ++wd) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + iq4_word_off(wd, cl, r));
+        for (int i = 0; i < 8; ++i) o[8 * wd + i] = __fmul_rn(a, (float)cb[(w >> (4 * i)) & 15u]);
+      }
     } break;
   }
 }
@@ -446,6 +471,68 @@ __global__ void quant_fp8_kernel(const float* __restrict__ W, int64_t rows, int6
   for (int64_t k = threadIdx.x; k < K; k += blockDim.x)
     out[r * K + k] = (uint8_t)((s == 0.0f) ? 0u : f2e4m3(__fdiv_rn(x[k], s)));
   if (threadIdx.x == 0) *reinterpret_cast<float*>(out + rows * K + 4 * r) = s;
+}
+
+// IQ4_XS: sub-block j gets the signed scale s_j that maps its element of largest
+// magnitude onto the codebook entry of largest magnitude (the first such entry);
+// d = max_j |s_j| / 31 in fp16; ls_j = clamp(rint(s_j / d) + 32, 0, 63); each element
+// takes the entry c nearest to it, |w - a_j C[c]| with a_j = d (ls_j - 32), ties to
+// the lower index. Block 0's thread also writes the codebook after the blocks.
+__global__ void quant_iq4_xs_kernel(const float* __restrict__ W, int64_t nblk, Codebook16 cb,
+                                    uint8_t* __restrict__ out) {
+  int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b == 0)
+    for (int i = 0; i < 16; ++i) out[nblk * 136 + i] = (uint8_t)cb.v[i];
+  if (b >= nblk) return;
+  const float* x = W + b * 256;
+  int cm = 0;
+  for (int c = 1; c < 16; ++c)
+    if (abs((int)cb.v[c]) > abs((int)cb.v[cm])) cm = c;
+  float s[8], smax = 0.0f;
+  for (int j = 0; j < 8; ++j) {
+    int em = 0;
+    for (int i = 1; i < 32; ++i)
+      if (fabsf(x[32 * j + i]) > fabsf(x[32 * j + em])) em = i;
+    s[j] = (cb.v[cm] != 0) ? __fdiv_rn(x[32 * j + em], (float)cb.v[cm]) : 0.0f;
+    if (fabsf(s[j]) > smax) smax = fabsf(s[j]);
+  }
+  const uint32_t dh = f2h_bits(__fdiv_rn(smax, 31.0f));
+  const float d = h2f(dh);
+  uint32_t words[34];
+  for (int i = 0; i < 34; ++i) words[i] = 0u;
+  uint32_t sh = 0u;
+  for (int j = 0; j < 8; ++j) {
+    int ls = 32;
+    if (d > 0.0f) ls = (int)clampf(__fadd_rn(rintf(__fdiv_rn(s[j], d)), 32.0f), 0.0f, 63.0f);
+    sh |= (uint32_t)((ls >> 4) & 3) << (2 * j);
+    words[1] |= (uint32_t)(ls & 15) << (4 * j);
+    const float a = __fmul_rn(d, (float)(ls - 32));
+    for (int i = 0; i < 32; ++i) {
+      const float v = x[32 * j + i];
+      int best = 0;
+      float be = fabsf(__fsub_rn(v, __fmul_rn(a, (float)cb.v[0])));
+      for (int c = 1; c < 16; ++c) {
+        const float e = fabsf(__fsub_rn(v, __fmul_rn(a, (float)cb.v[c])));
+        if (e < be) { be = e; best = c; }
+      }
+      const int e = 32 * j + i;                     // nibble e of the 128 index bytes
+      words[2 + (e >> 3)] |= (uint32_t)best << (4 * (e & 7));
+    }
+  }
+  words[0] = dh | (sh << 16);
+  uint8_t* o = out + b * 136;
+  for (int i = 0; i < 136; ++i) o[i] = (uint8_t)(words[i >> 2] >> (8 * (i & 3)));
+}
+
+cudaError_t launch_quantize_codebook(int fmt, const float* W, int64_t rows, int64_t K, const int8_t* codebook,
+                                     uint8_t* canon, cudaStream_t s) {
+  if (fmt != F_IQ4_XS) return cudaErrorInvalidValue;
+  Codebook16 cb;
+  for (int i = 0; i < 16; ++i) cb.v[i] = codebook[i];
+  const int threads = 128;
+  const int64_t n = rows * (K / 256);
+  quant_iq4_xs_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, n, cb, canon);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(int fmt, const float* W, int64_t rows, int64_t K, float ts,

@@ -12,6 +12,8 @@
 //                      (element pairs at fields (p, p+4) of each 32-bit word); the
 //                      +128 offset is removed with the per-block term through X = sum x.
 //   NVFP4, FP8 -> f16: hardware cvt of FP4/FP8 pairs to f16x2 (exact).
+//   IQ4_XS     -> f16: a byte-permute lookup of the 16-entry codebook, placed under
+//                      the f16 pattern of 1024 ({1152 + C[q], 1152 + C[q']} exactly).
 // Products of these small exact values with the activations are exact and the
 // tensor core accumulates in fp32.
 //
@@ -26,7 +28,7 @@
 // One accumulation order for every M (so that row m of an M-row call equals the
 // one-row call on x[m] bit for bit). The units of a slab are split among the four
 // threads t of an mma quad exactly as the unit columns place them: quad position t
-// owns the units of chunks 2t and 2t+1 (Q4_K, Q5_K, Q8_0, FP8: units 2t, 2t+1; Q6_K
+// owns the units of chunks 2t and 2t+1 (Q4_K, Q5_K, Q8_0, FP8, IQ4_XS: units 2t, 2t+1; Q6_K
 // units 4t .. 4t+3; NVFP4 blocks 4t .. 4t+3). Per output (row, token):
 //   * every unit sum is the same MMA chain over the same operands in both forms
 //     (in the unit-column form the other columns only add exact zeros);
@@ -203,6 +205,10 @@ __device__ __forceinline__ float nv_comb(float s0, float s1, float s2, float s3,
 }
 // FP8: two chunk sums (the row scale multiplies the row's total)
 __device__ __forceinline__ float fp8_comb(float D0, float D1) { return __fadd_rn(D0, D1); }
+// IQ4_XS over two 32-value chunks: a_i (D_i - 1152 X_i), D_i over 1152 + C[q]
+__device__ __forceinline__ float iq4_comb(float a0, float a1, float D0, float D1, float X0, float X1) {
+  return __fmaf_rn(a0, __fmaf_rn(-1152.0f, X0, D0), __fmul_rn(a1, __fmaf_rn(-1152.0f, X1, D1)));
+}
 // the piece value from the four quad positions' sums
 __device__ __forceinline__ float quad_join(float a0, float a1, float a2, float a3) {
   return __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3));
@@ -854,6 +860,137 @@ struct Slab<F_FP8, 8> {
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) tc_add(a, t, e, fp8_comb(D[0][e], D[1][e]));
+    }
+  }
+};
+
+// ============================================================================
+// IQ4_XS. A weight is the matrix's codebook entry C[q] (16 x int8) times the
+// sub-block scale a_j = d (ls_j - 32) of its 32-value chunk. The decode is a
+// lookup in registers: the table bytes C + 128 sit in four registers; one prmt
+// picks the bytes of indices 0..7 and one those of indices 8..15 (three selector
+// bits each), and a third, driven by the top bit of each index, selects between
+// them. One more prmt per pair places two table bytes b under the f16 pattern 0x64
+// (1024 + b), so each A register holds {1152 + C[q], 1152 + C[q']} exactly. x goes
+// to the MMA in f16; sum C x = D - 1152 X with X = sum x.
+// ============================================================================
+constexpr uint32_t kOnesF16 = 0x3C003C00u;
+
+__device__ __forceinline__ void iq4_table(const uint8_t* cbp, uint32_t (&T)[4]) {
+  const uint4 c = lds128v(cbp);
+  T[0] = c.x ^ 0x80808080u;
+  T[1] = c.y ^ 0x80808080u;
+  T[2] = c.z ^ 0x80808080u;
+  T[3] = c.w ^ 0x80808080u;
+}
+// the table bytes of the four indices in the low 16 bits of s (index i at nibble i)
+__device__ __forceinline__ uint32_t iq4_look4(uint32_t s, const uint32_t (&T)[4]) {
+  const uint32_t s7 = s & 0x7777u;
+  const uint32_t lo = __byte_perm(T[0], T[1], s7), hi = __byte_perm(T[2], T[3], s7);
+  const uint32_t m = __byte_perm(0x0000FF00u, 0u, (s >> 3) & 0x1111u);   // 0xFF where index >= 8
+  return (lo & ~m) | (hi & m);
+}
+// word w (elements 0..7 at nibbles 0..7) -> the A registers {e0,e1}, {e2,e3}, {e4,e5}, {e6,e7}
+__device__ __forceinline__ void iq4_word(uint32_t w, const uint32_t (&T)[4], uint32_t* p) {
+  const uint32_t v0 = iq4_look4(w, T), v1 = iq4_look4(w >> 16, T);
+  p[0] = __byte_perm(v0, 0x64646464u, 0x4140);
+  p[1] = __byte_perm(v0, 0x64646464u, 0x4342);
+  p[2] = __byte_perm(v1, 0x64646464u, 0x4140);
+  p[3] = __byte_perm(v1, 0x64646464u, 0x4342);
+}
+__device__ __forceinline__ void iq4_chunk_mma(float* d, uint32_t wa, uint32_t wb, const uint32_t (&T)[4],
+                                              uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3) {
+  uint32_t pa[4], pb[4];
+  iq4_word(wa, T, pa);
+  iq4_word(wb, T, pb);
+  mma_f16(d, pa[0], pb[0], pa[1], pb[1], x0, x1);
+  mma_f16(d, pa[2], pb[2], pa[3], pb[3], x2, x3);
+}
+__device__ __forceinline__ void ones_mma_f16(float* xx, uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3) {
+  mma_f16(xx, kOnesF16, kOnesF16, kOnesF16, kOnesF16, x0, x1);
+  mma_f16(xx, kOnesF16, kOnesF16, kOnesF16, kOnesF16, x2, x3);
+}
+// a_j = d (ls_j - 32) of chunks 2t, 2t+1 from a row's scale fields (fp16 d, u16 sh, u32 sl)
+__device__ __forceinline__ void iq4_scales(const uint8_t* sf, int t, float* a) {
+  const uint2 v = lds64(sf);
+  const float d = h2f(v.x);
+  const uint32_t sh = (v.x >> 16) >> (4 * t), sl = v.y >> (8 * t);
+  a[0] = __fmul_rn(d, (float)((int)((sl & 15u) | ((sh & 3u) << 4)) - 32));
+  a[1] = __fmul_rn(d, (float)((int)(((sl >> 4) & 15u) | (((sh >> 2) & 3u) << 4)) - 32));
+}
+
+template <>
+struct Slab<F_IQ4_XS, 1> {
+  // unit j = chunk j in column j: even chunks accumulate in dE, odd ones in dO, so
+  // position t's units 2t, 2t+1 are dE column 2t and dO column 2t+1
+  __device__ static void run(const uint8_t* st, const uint8_t* pb, const uint8_t* xs, int, int w, int lane,
+                             float2*, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    const int rowA = 16 * w + g, rowB = rowA + 8;   // both at rotation g (row & 7)
+    const uint8_t* rA = st + rowA * 128;
+    const uint8_t* rB = st + rowB * 128;
+    uint32_t T[4];
+    iq4_table(pb + 128 * 8, T);
+    const uint4 xr = lds128v(xs + 64 * g + 16 * t);   // the lane's unit: chunk g, elements 8t..8t+7
+    const uint32_t x0 = bf16x2_to_f16x2(xr.x), x1 = bf16x2_to_f16x2(xr.y);
+    const uint32_t x2 = bf16x2_to_f16x2(xr.z), x3 = bf16x2_to_f16x2(xr.w);
+    const uint4 a0 = lds128v(rA + 16 * ((2 * t) ^ g)), a1 = lds128v(rA + 16 * ((2 * t + 1) ^ g));
+    const uint4 b0 = lds128v(rB + 16 * ((2 * t) ^ g)), b1 = lds128v(rB + 16 * ((2 * t + 1) ^ g));
+    const uint32_t WA[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t WB[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f}, xx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      // B is x only in the column of chunk j: an f16x2 {1, 1} / {0, 0} mask multiply on
+      // the FMA pipe (x is finite), which keeps the ALU pipe for the lookups
+      const uint32_t mk = (g == j) ? kOnesF16 : 0u;
+      iq4_chunk_mma((j & 1) ? dO : dE, WA[j], WB[j], T, hmul2(x0, mk), hmul2(x1, mk), hmul2(x2, mk),
+                    hmul2(x3, mk));
+    }
+    ones_mma_f16(xx, x0, x1, x2, x3);
+    float aA[2], aB[2];
+    iq4_scales(pb + rowA * 8, t, aA);
+    iq4_scales(pb + rowB * 8, t, aB);
+    acc[0] = __fadd_rn(acc[0], iq4_comb(aA[0], aA[1], dE[0], dO[1], xx[0], xx[1]));
+    acc[1] = __fadd_rn(acc[1], iq4_comb(aB[0], aB[1], dE[2], dO[3], xx[2], xx[3]));
+  }
+};
+
+template <>
+struct Slab<F_IQ4_XS, 8> {
+  __device__ static void run(const uint8_t* st, const uint8_t* pb, const uint8_t* xs, int R, int w, int lane,
+                             float2*, float (&a)[4][4]) {
+    const int g = lane >> 2, tq = lane & 3;
+    const int rowA = 16 * w + g, rowB = rowA + 8;
+    const uint8_t* rA = st + rowA * 128;
+    const uint8_t* rB = st + rowB * 128;
+    const bool has_x = g < R;
+    uint32_t T[4];
+    iq4_table(pb + 128 * 8, T);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      // the words of chunks 2t, 2t+1: vector 2tq + (t >> 1) (rotated by g), words 2(t & 1), +1
+      const int v = (2 * tq + (t >> 1)) ^ g;
+      const uint2 WA = lds64(rA + 16 * v + 8 * (t & 1)), WB = lds64(rB + 16 * v + 8 * (t & 1));
+      float D[2][4], X[2][4];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) D[q][e] = X[q][e] = 0.f;
+        const int j = 2 * t + q;
+        // x already f16 (converted per stage)
+        const uint4 xv = has_x ? lds128v(xs + 64 * j + 16 * tq) : make_uint4(0u, 0u, 0u, 0u);
+        iq4_chunk_mma(D[q], q ? WA.y : WA.x, q ? WB.y : WB.x, T, xv.x, xv.y, xv.z, xv.w);
+        ones_mma_f16(X[q], xv.x, xv.y, xv.z, xv.w);
+      }
+      float sA[2], sB[2];
+      iq4_scales(pb + rowA * 8, t, sA);
+      iq4_scales(pb + rowB * 8, t, sB);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float* sc = (e < 2) ? sA : sB;
+        tc_add(a, t, e, iq4_comb(sc[0], sc[1], D[0][e], D[1][e], X[0][e], X[1][e]));
+      }
     }
   }
 };

@@ -46,8 +46,11 @@ constexpr int kThreads = 32 * (1 + kConsumerWarps);
 // prologue and first weight copies during the running call's compute.
 template <int MT> constexpr int ctas_per_sm() { return 2; }
 constexpr int kMaxStages = 16;
-// bytes per row of plane B (Q6_K d, NVFP4 block scales)
-template <int FMT> constexpr int plane_b_row() { return FMT == F_Q6_K ? 2 : FMT == F_NVFP4 ? 16 : 0; }
+// bytes of plane B per 128-row tile (Q6_K d, NVFP4 block scales, IQ4_XS scale fields
+// and codebook)
+template <int FMT> constexpr int plane_b_tile() {
+  return FMT == F_Q6_K ? kSlabRows * 2 : FMT == F_NVFP4 ? kSlabRows * 16 : FMT == F_IQ4_XS ? kIq4TileB : 0;
+}
 constexpr int kMaxSeg = 64;
 // the reducer's gather list (built by the producer warp): kMaxGather entries in the
 // misc area of shared memory, then the mbarrier that publishes them
@@ -591,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     uint32_t rphase = 0;          // parity of the current round over the stage ring
     int it = 0;
     const uint32_t abytes = (uint32_t)(kSlabRows * L.rec);
-    const uint32_t bbytes = (uint32_t)(kSlabRows * plane_b_row<FMT>());
+    const uint32_t bbytes = (uint32_t)plane_b_tile<FMT>();
     // The first round of stages: weights first (independent of earlier kernels),
     // then wait for the previous grid, then the activations of those stages.
     const int first = (s1 - s0) < kp.stages ? (s1 - s0) : kp.stages;
@@ -661,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
     uint32_t rphase = 0;          // parity of the current round over the stage ring
     int it = 0;
     const uint32_t abytes = (uint32_t)(kSlabRows * L.rec);
-    const uint32_t bbytes = (uint32_t)(kSlabRows * plane_b_row<FMT>());
+    const uint32_t bbytes = (uint32_t)plane_b_tile<FMT>();
     // The first round of stages: weights first (independent of earlier kernels),
     // then wait for the previous grid, then the activations of those stages.
     const int first = (s1 - s0) < kp.stages ? (s1 - s0) : kp.stages;
@@ -764,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   // the pieces that later CTAs published, in order; every other CTA publishes each
   // piece of the unit in the workspace slot (CTA, piece ordinal).
   const int w = warp - 1;               // this warp owns rows 16w .. 16w+15 of a slab
-  constexpr bool kConvX = (MT > 1) && (FMT == F_NVFP4 || FMT == F_FP8);
+  constexpr bool kConvX = (MT > 1) && (FMT == F_NVFP4 || FMT == F_FP8 || FMT == F_IQ4_XS);
   const int g = lane >> 2, tq = lane & 3;
   float2* tbl = tbls + w * (16 * kTblStride);
   const int rA = 16 * w + g, rB = rA + 8;
@@ -1084,7 +1087,7 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   kp.stage_base = (int)align_up(kp.tbl_off + tbl_bytes, 1024);
   const int abytes = kSlabRows * a.L.rec;
   kp.b_off = (int)align_up(abytes, 128);
-  const int bbytes = kSlabRows * plane_b_row<FMT>();
+  const int bbytes = plane_b_tile<FMT>();
   kp.x_off = (int)align_up(kp.b_off + bbytes, 128);
   kp.stage_bytes = (int)align_up(kp.x_off + MT * kXStride, 1024);
   kp.stages = (smem_max - kp.stage_base) / kp.stage_bytes;
@@ -1162,6 +1165,7 @@ cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant) {
     case F_Q6_K: return launch_fmt<F_Q6_K>(a, s, variant);
     case F_NVFP4: return launch_fmt<F_NVFP4>(a, s, variant);
     case F_FP8: return launch_fmt<F_FP8>(a, s, variant);
+    case F_IQ4_XS: return launch_fmt<F_IQ4_XS>(a, s, variant);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -69,7 +69,11 @@ typedef enum {
     QMV_Q6_K = 3,
     QMV_NVFP4 = 4,
     QMV_FP8_ROW = 5,
-    QMV_Q5_K = 6
+    QMV_Q5_K = 6,
+    QMV_IQ4_XS = 7         /* codebook format: 136 B / 256 values, a per-matrix 16-entry
+                              int8 codebook at the end of each matrix's canonical stream
+                              ("A 320B MoE on a free Kaggle TPU", "What '3-bit' costs,
+                              measured") */
 } qmv_fmt;
 
 typedef enum {
@@ -109,7 +113,9 @@ size_t qmv_canon_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
  * is aligned; rows are padded to a multiple of 128 with zero blocks. The slab
  * bytes are the canonical bytes, only reordered (the per-value cost is
  * unchanged). K must be a multiple of 32 (Q8_0, NVFP4, FP8_ROW) or 256 (Q4_K,
- * Q5_K, Q6_K). Returns 0 if unsupported. */
+ * Q5_K, Q6_K, IQ4_XS). Returns 0 if unsupported. IQ4_XS repeats its 16-byte
+ * codebook after the scale fields of every 128-row tile of every k-group (16 B per
+ * slab, so that each slab copy brings it along). */
 size_t qmv_pack_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
 
 /* Repack canonical bytes into the device layout. Defined by: the stacked keep-quant
@@ -120,7 +126,7 @@ size_t qmv_pack_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
  * ("A 320B MoE on a free Kaggle TPU", "The 110 GB claim, checked against the tensor
  * index"). canon: device, qmv_canon_size bytes (the canonical stream of a whole
  * tower; NVFP4 carries its per-matrix tensor scale inside it, FP8_ROW its row
- * scales). dst: device, qmv_pack_size bytes, 256-B aligned; fully overwritten
+ * scales, IQ4_XS its codebook). dst: device, qmv_pack_size bytes, 256-B aligned; fully overwritten
  * (header, slabs, padding). One-time load-phase work, not part of the per-token
  * path. */
 qmv_status qmv_pack(qmv_fmt fmt, const void* canon, int64_t N, int64_t K, int64_t E,
@@ -132,9 +138,22 @@ qmv_status qmv_pack(qmv_fmt fmt, const void* canon, int64_t N, int64_t K, int64_
  * one tensor at a time, from the original weights ("Qwen3.8-27B on one Tenstorrent
  * P150", "2. Building the 27B quant"); plain rounding, not the error-compensated
  * variant of its section 8. tensor_scale is the NVFP4 per-tensor scale s_T (a given
- * constant); ignored for other formats. Not on the per-token path. */
+ * constant); ignored for other formats. IQ4_XS returns QMV_EUNSUPPORTED: its
+ * encoding needs a codebook, which is an input of the format, not a rounding rule.
+ * Not on the per-token path. */
 qmv_status qmv_quantize(qmv_fmt fmt, const float* W, int64_t rows, int64_t K,
                         float tensor_scale, void* canon, cudaStream_t stream);
+
+/* The encoder of the codebook formats (IQ4_XS): as qmv_quantize, with the matrix's
+ * codebook (host pointer to 16 int8 values, read during the call) in place of a
+ * rounding constant ("A 320B MoE on a free Kaggle TPU", "What '3-bit' costs,
+ * measured": a weight is an entry of the format's codebook). Per 32-value sub-block:
+ * the scale that maps its element of largest magnitude onto the entry of largest
+ * magnitude, 6 bits under an fp16 d; each element takes the nearest entry. canon:
+ * device, qmv_canon_size(fmt, rows, K, 1) bytes (the blocks, then the codebook).
+ * Other formats: QMV_EUNSUPPORTED. Not on the per-token path. */
+qmv_status qmv_quantize_codebook(qmv_fmt fmt, const float* W, int64_t rows, int64_t K,
+                                 const int8_t* codebook, void* canon, cudaStream_t stream);
 
 /* BlockToFloat on the device layout: W_out[r][k] (fp32, device) for rows
  * row0 .. row0+rows-1 of the stacked tower (row = e*N + n). Defined by: the CPU

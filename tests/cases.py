@@ -25,6 +25,20 @@ def tensor_scale(fmt) -> float:
     return NVFP4_TS if fmt == "nvfp4" else 0.0
 
 
+# formats whose canonical stream is per matrix (a tower is E streams back to back)
+PER_MATRIX = ("nvfp4", "fp8_row", "iq4_xs")
+
+
+def codebook(fmt, seed, e):
+    """The IQ4_XS codebook of expert e of a seeded tower (each expert its own); None
+    for the other formats."""
+    return synth.codebook(seed + 7919 * e) if fmt == "iq4_xs" else None
+
+
+def _encode(fmt, W, seed, e):
+    return oracle.encode(fmt, W, tensor_scale(fmt), codebook=codebook(fmt, seed, e))
+
+
 def norm_err(y, ref, den) -> float:
     y = np.asarray(y, dtype=np.float64)
     zero = den == 0
@@ -42,16 +56,15 @@ def host_matrix(fmt, seed, N, K, E=1):
     Formats whose canonical stream is per matrix (NVFP4, FP8_ROW) are encoded one
     expert at a time and concatenated."""
     W = synth.weights(seed, E * N, K).numpy()
-    if fmt in ("nvfp4", "fp8_row"):
-        canon = np.concatenate([oracle.encode(fmt, W[e * N:(e + 1) * N], tensor_scale(fmt))
-                                for e in range(E)])
+    if fmt in PER_MATRIX:
+        canon = np.concatenate([_encode(fmt, W[e * N:(e + 1) * N], seed, e) for e in range(E)])
     else:
         canon = oracle.encode(fmt, W, tensor_scale(fmt))
     return W, canon
 
 
 def host_dequant(fmt, canon, N, K, E=1):
-    if fmt in ("nvfp4", "fp8_row"):
+    if fmt in PER_MATRIX:
         per = oracle.canon_bytes(fmt, N, K)
         return np.concatenate([oracle.block_to_float(fmt, canon[e * per:(e + 1) * per], N, K)
                                for e in range(E)])
@@ -63,6 +76,13 @@ def host_rows_dequant(fmt, seed, rows, N, K):
     (row = e*N + n). NVFP4 uses the static tensor scale; FP8 row scales are per row,
     so each row is a one-row matrix."""
     W = synth.weights_rows(seed, rows, K).numpy()
+    if fmt == "iq4_xs":
+        # blocks are per row: each row encodes alone with its expert's codebook
+        out = np.empty_like(W)
+        for i, r in enumerate(np.asarray(rows).reshape(-1)):
+            c = _encode(fmt, W[i:i + 1], seed, int(r) // N)
+            out[i] = oracle.block_to_float(fmt, c, 1, K)[0]
+        return out
     if fmt in ("nvfp4", "fp8_row"):
         out = np.empty_like(W)
         for i in range(W.shape[0]):
@@ -85,9 +105,15 @@ def device_matrix(q, fmt, seed, N, K, E=1, dev="cuda"):
             W = synth.weights(seed, n, K, device=dev, row0=e * N + r0)
             if fmt in ("nvfp4", "fp8_row"):
                 parts.append(W)
+            elif fmt == "iq4_xs":
+                # the blocks of this chunk, without the codebook the encoder appends
+                parts.append(q.qmv_quantize_codebook(fmt, W, codebook(fmt, seed, e))[:n * (K // 256) * 136])
             else:
                 parts.append(q.qmv_quantize(fmt, W))
-        if fmt in ("nvfp4", "fp8_row"):
+        if fmt == "iq4_xs":
+            cb = torch.from_numpy(codebook(fmt, seed, e).view(np.uint8).copy()).to(dev)
+            canon_parts.append(torch.cat(parts + [cb]))
+        elif fmt in ("nvfp4", "fp8_row"):
             # per-matrix stream: quantize the whole expert matrix at once
             Wm = torch.cat(parts)
             canon_parts.append(q.qmv_quantize(fmt, Wm, tensor_scale(fmt)))

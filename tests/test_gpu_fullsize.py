@@ -99,6 +99,35 @@ def test_tower_full_size_sampled(q, mat, M):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("M", [1, 8])
+def test_iq4_xs_tower_full_size_sampled(q, M):
+    """The 288-expert down-projection tower [4096, 2048] in IQ4_XS, each expert with
+    its own codebook (the down matrices the pages list in IQ4_XS, "A 320B MoE on a
+    free Kaggle TPU", table of formats by layer), top-8, one x row per pair; sampled
+    rows of every routed expert of the first tokens against the oracle."""
+    fmt, E, topk, N, K, seed = "iq4_xs", 288, 8, 4096, 2048, 740
+    tower = device_matrix(q, fmt, seed, N, K, E)
+    ids = synth.expert_ids(seed + M, M, topk, E)
+    x = synth.activations(seed + 10 * M, M * topk, K)
+    ws = q.workspace(q.QMV_ENTRY_GROUPED, fmt, M, N, K, E, topk)
+    y = q.qmv_grouped(fmt, tower, torch.from_numpy(ids).cuda(), x.cuda(), N, K, E, ws, x_per_pair=True)
+    assert q.qmv_last_route() == q.FORMATS[fmt] * 100 + 3
+    y = y.cpu().numpy()
+    assert q.qmv_device_status() == 0
+    assert int(ws.count_nonzero()) == 0
+    xb = synth.bf16_bits(x)
+    rows = sample_rows(N, 16, seed + M)
+    for t in range(min(M, 2)):
+        for j in range(topk):
+            e = int(ids[t, j])
+            D = host_rows_dequant(fmt, seed, e * N + rows, N, K)
+            ref, den = oracle.gemv_f64(D, xb[t * topk + j][None, :])
+            err = norm_err(y[t, j, rows][None, :], ref, den)
+            assert err <= TOL, (t, j, e, err)
+    del tower
+    torch.cuda.empty_cache()
+
+
 def test_tower_swiglu_full_size_sampled(q):
     """Fused gate|up SwiGLU over the 288-expert tower at its full gate/up shape
     [2048, 4096] (a 576-expert tower: gates, then ups), top-8, M = 1 and 8; sampled

@@ -18,7 +18,7 @@ from cases import (TOL, host_dequant, host_matrix, norm_err, tensor_scale)
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["q8_0", "q4_k", "q5_k", "q6_k", "nvfp4", "fp8_row"]
+FMTS = ["q8_0", "q4_k", "q5_k", "q6_k", "nvfp4", "fp8_row", "iq4_xs"]
 
 
 @pytest.fixture(scope="module")
@@ -34,7 +34,8 @@ def _sms():
 
 
 def _kq(fmt):
-    return fmt in ("q4_k", "q5_k", "q6_k")
+    """formats whose K granule is 256"""
+    return fmt in ("q4_k", "q5_k", "q6_k", "iq4_xs")
 
 
 # ---------------------------------------------------------------------------
@@ -49,8 +50,13 @@ def test_quantize_bit_exact(q, fmt):
     W[2, :256] = 0.0123
     W[3] *= 1e-4
     W[4, 5] = 0.5                                      # an outlier
-    want = oracle.encode(fmt, W, tensor_scale(fmt))
-    got = q.qmv_quantize(fmt, torch.from_numpy(W).cuda(), tensor_scale(fmt)).cpu().numpy()
+    if fmt == "iq4_xs":
+        cb = synth.codebook(3)
+        want = oracle.encode(fmt, W, codebook=cb)
+        got = q.qmv_quantize_codebook(fmt, torch.from_numpy(W).cuda(), cb).cpu().numpy()
+    else:
+        want = oracle.encode(fmt, W, tensor_scale(fmt))
+        got = q.qmv_quantize(fmt, torch.from_numpy(W).cuda(), tensor_scale(fmt)).cpu().numpy()
     torch.cuda.synchronize()
     assert got.shape == want.shape
     bad = np.flatnonzero(got != want)
@@ -122,7 +128,7 @@ def test_gemv_tiny_config_q8_0(q):
     assert norm_err(y, ref, den) <= TOL
 
 
-@pytest.mark.parametrize("fmt", ["q4_k", "nvfp4"])
+@pytest.mark.parametrize("fmt", ["q4_k", "nvfp4", "iq4_xs"])
 def test_gemv_deterministic_and_guarded(q, fmt):
     N, K, M = 1000, 2048, 4
     W, canon = host_matrix(fmt, 13, N, K)
@@ -167,6 +173,27 @@ def test_q6k_activation_range(q, lo, hi, M):
     fmt, N, K = "q6_k", 1000, 2048
     W, canon = host_matrix(fmt, 23, N, K)
     z = synth.activations(23, M, K).float()
+    rng = np.random.default_rng((lo + 100) * 1000 + hi + 100 + M)
+    e = torch.from_numpy(rng.integers(lo, hi + 1, size=(M, K)).astype(np.float32))
+    x = (z * torch.pow(2.0, e)).to(torch.bfloat16)
+    ref, den = oracle.gemv_f64(host_dequant(fmt, canon, N, K), synth.bf16_bits(x))
+    packed = q.qmv_pack(fmt, torch.from_numpy(canon).cuda(), N, K)
+    ws = q.workspace(q.QMV_ENTRY_GEMV, fmt, M, N, K)
+    y = q.qmv_gemv(fmt, packed, x.cuda(), N, K, ws).cpu().numpy()
+    assert q.qmv_device_status() == 0
+    assert np.isfinite(y).all()
+    assert norm_err(y, ref, den) <= TOL
+
+
+@pytest.mark.parametrize("lo,hi", [(-12, 12), (-14, 0), (0, 12)])
+@pytest.mark.parametrize("M", [1, 3])
+def test_iq4_xs_activation_range(q, lo, hi, M):
+    """IQ4_XS feeds x to the MMA in f16: exact for 2^-14 <= |x| < 65504 (|z| < 8 here,
+    so e <= 12). Activations spread over that range (per element 2^e) meet the
+    tolerance, including the largest codebook offsets."""
+    fmt, N, K = "iq4_xs", 1000, 2048
+    W, canon = host_matrix(fmt, 29, N, K)
+    z = synth.activations(29, M, K).float()
     rng = np.random.default_rng((lo + 100) * 1000 + hi + 100 + M)
     e = torch.from_numpy(rng.integers(lo, hi + 1, size=(M, K)).astype(np.float32))
     x = (z * torch.pow(2.0, e)).to(torch.bfloat16)
