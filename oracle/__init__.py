@@ -20,10 +20,11 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
-Q8_0, Q4_K, Q6_K, NVFP4, FP8_ROW, Q5_K, IQ4_XS = 1, 2, 3, 4, 5, 6, 7
+Q8_0, Q4_K, Q6_K, NVFP4, FP8_ROW, Q5_K, IQ4_XS, IQ3_S, IQ2_S = 1, 2, 3, 4, 5, 6, 7, 8, 9
 FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "q6_k": Q6_K, "nvfp4": NVFP4, "fp8_row": FP8_ROW,
-           "q5_k": Q5_K, "iq4_xs": IQ4_XS}
-CODEBOOK_FORMATS = ("iq4_xs",)
+           "q5_k": Q5_K, "iq4_xs": IQ4_XS, "iq3_s": IQ3_S, "iq2_s": IQ2_S}
+CODEBOOK_FORMATS = ("iq4_xs", "iq3_s", "iq2_s")
+GRID_SHAPES = {"iq3_s": (512, 4), "iq2_s": (1024, 8)}
 
 _lib = None
 
@@ -70,6 +71,8 @@ def _load():
     lib.or_encode.argtypes = [ctypes.c_int, P, I64, I64, ctypes.c_float, P]
     lib.or_encode_cb.restype = ctypes.c_int
     lib.or_encode_cb.argtypes = [ctypes.c_int, P, I64, I64, P, P]
+    lib.or_grid_bytes.restype = I64
+    lib.or_grid_bytes.argtypes = [ctypes.c_int]
     lib.or_block_to_float.restype = ctypes.c_int
     lib.or_block_to_float.argtypes = [ctypes.c_int, P, I64, I64, P]
     lib.or_gemv_f64.restype = None
@@ -134,15 +137,24 @@ def canon_bytes(fmt, rows: int, K: int) -> int:
 
 
 # ---- matrices -----------------------------------------------------------------
+def grid_bytes(fmt) -> int:
+    return int(_load().or_grid_bytes(_fmt(fmt)))
+
+
 def encode(fmt, W: np.ndarray, tensor_scale: float = 0.0, codebook=None) -> np.ndarray:
     """fp32 W[rows, K] -> canonical bytes (synthetic-data encoder). The codebook
-    formats (IQ4_XS) take the matrix's codebook, 16 int8 values."""
+    formats take their table: IQ4_XS the matrix's codebook (16 int8 values), IQ3_S
+    and IQ2_S the grid (uint8 magnitudes [512, 4] / [1024, 8])."""
     W = np.ascontiguousarray(W, dtype=np.float32)
     rows, K = W.shape
     out = np.zeros(canon_bytes(fmt, rows, K), dtype=np.uint8)
-    if _fmt(fmt) == IQ4_XS:
-        cb = np.ascontiguousarray(codebook, dtype=np.int8)
-        assert cb.shape == (16,)
+    if _fmt(fmt) in (IQ4_XS, IQ3_S, IQ2_S):
+        if _fmt(fmt) == IQ4_XS:
+            cb = np.ascontiguousarray(codebook, dtype=np.int8).reshape(-1)
+            assert cb.shape == (16,)
+        else:
+            cb = np.ascontiguousarray(codebook, dtype=np.uint8).reshape(-1)
+            assert cb.size == grid_bytes(fmt)
         rc = _load().or_encode_cb(_fmt(fmt), _ptr(W), rows, K, _ptr(cb), _ptr(out))
     else:
         rc = _load().or_encode(_fmt(fmt), _ptr(W), rows, K, float(tensor_scale), _ptr(out))

@@ -25,7 +25,10 @@
  * tensor scale, FP8 E4M3 with one fp32 scale per row. IQ4_XS 136 B / 256 ("A 320B MoE
  * on a free Kaggle TPU", section "What '3-bit' costs, measured": the GGUF block
  * sizes of the codebook formats): a weight is an entry of the matrix's 16-value
- * codebook times its sub-block scale.
+ * codebook times its sub-block scale. IQ3_S 110 B / 256 and IQ2_S 82 B / 256 (same
+ * section; "The kernel, and why 64 tok/s is not a bandwidth number": a group of
+ * weights is one entry of the format's grid, 1,024 entries of 8 weights for IQ2_S,
+ * groups of four for IQ3_S, with sign bits).
  *
  * Where the pages give no bit-level layout, the reading taken is the one written
  * in oracle.h (the plainest one consistent with the printed sizes).
@@ -136,6 +139,8 @@ int64_t or_block_values(int fmt) {
     case OR_NVFP4: return 16;
     case OR_FP8_ROW: return 1;
     case OR_IQ4_XS: return 256;
+    case OR_IQ3_S: return 256;
+    case OR_IQ2_S: return 256;
     default: return 0;
     }
 }
@@ -149,8 +154,14 @@ int64_t or_canon_bytes(int fmt, int64_t rows, int64_t K) {
     case OR_NVFP4: return rows * (K / 2) + rows * (K / 16) + 4;
     case OR_FP8_ROW: return rows * K + rows * 4;
     case OR_IQ4_XS: return rows * (K / 256) * 136 + 16;
+    case OR_IQ3_S: return or_grid_bytes(fmt) + rows * (K / 256) * 110;
+    case OR_IQ2_S: return or_grid_bytes(fmt) + rows * (K / 256) * 82;
     default: return -1;
     }
+}
+
+int64_t or_grid_bytes(int fmt) {
+    return fmt == OR_IQ3_S ? 512 * 4 : (fmt == OR_IQ2_S ? 1024 * 8 : 0);
 }
 
 static uint16_t rd16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
@@ -332,14 +343,78 @@ static void enc_iq4_xs_block(const float* x, const int8_t* cb, uint8_t* blk) {
     wr16(blk + 2, sh);
 }
 
-int or_encode_cb(int fmt, const float* W, int64_t rows, int64_t K, const int8_t* codebook,
+/* IQ3_S / IQ2_S: per sub-block (32 / 16 values) s = amax / gmax, gmax = the largest
+ * magnitude in the grid; d = max s / 31 in fp16; sc = clamp(rint((s / d - 1) / 2), 0, 15),
+ * a = d (2 sc + 1); per group (4 / 8 weights) the signs of its weights and the grid
+ * entry nearest to their magnitudes: sum_i (|w_i| - a G[c][i])^2 in fp32, i in order,
+ * ties to the lower index. */
+static void enc_grid_block(int fmt, const float* x, const uint8_t* G, uint8_t* blk) {
+    const int iq3 = (fmt == OR_IQ3_S);
+    const int gw = iq3 ? 4 : 8, ne = iq3 ? 512 : 1024, sbs = iq3 ? 32 : 16, bb = iq3 ? 110 : 82;
+    int gmax = 0;
+    for (int i = 0; i < ne * gw; i++)
+        if (G[i] > gmax) gmax = G[i];
+    float s[16], smax = 0.0f;
+    for (int k = 0; k < 256 / sbs; k++) {
+        float amax = 0.0f;
+        for (int i = 0; i < sbs; i++)
+            if (fabsf(x[k * sbs + i]) > amax) amax = fabsf(x[k * sbs + i]);
+        s[k] = (gmax > 0) ? amax / (float)gmax : 0.0f;
+        if (s[k] > smax) smax = s[k];
+    }
+    memset(blk, 0, (size_t)bb);
+    uint16_t dh = or_f32_to_fp16(smax / 31.0f);
+    float d = or_fp16_to_f32(dh);
+    wr16(blk, dh);
+    for (int k = 0; k < 256 / sbs; k++) {
+        int sc = 0;
+        if (d > 0.0f) sc = (int)clampf(rintf((s[k] / d - 1.0f) / 2.0f), 0.0f, 15.0f);
+        blk[(iq3 ? 106 : 74) + k / 2] |= (uint8_t)(sc << (4 * (k & 1)));
+        float a = d * (float)(2 * sc + 1);
+        for (int g = k * sbs / gw; g < (k + 1) * sbs / gw; g++) {
+            const float* xg = x + g * gw;
+            int best = 0;
+            float be = 0.0f;
+            for (int c = 0; c < ne; c++) {
+                float e = 0.0f;
+                for (int i = 0; i < gw; i++) {
+                    float t = fabsf(xg[i]) - a * (float)G[c * gw + i];
+                    e = e + t * t;
+                }
+                if (c == 0 || e < be) { be = e; best = c; }
+            }
+            blk[2 + g] = (uint8_t)(best & 255);
+            if (iq3) blk[66 + g / 8] |= (uint8_t)(((best >> 8) & 1) << (g & 7));
+            else blk[66 + g / 4] |= (uint8_t)(((best >> 8) & 3) << (2 * (g & 3)));
+            for (int i = 0; i < gw; i++)
+                if (xg[i] < 0.0f) {
+                    if (iq3) blk[74 + (g * 4 + i) / 8] |= (uint8_t)(1 << ((g * 4 + i) & 7));
+                    else blk[34 + g] |= (uint8_t)(1 << i);
+                }
+        }
+    }
+}
+
+int or_encode_cb(int fmt, const float* W, int64_t rows, int64_t K, const void* codebook,
                  uint8_t* canon) {
-    if (fmt != OR_IQ4_XS || K % 256 != 0 || codebook == NULL) return 1;
-    for (int64_t r = 0; r < rows; r++)
-        for (int64_t b = 0; b < K / 256; b++)
-            enc_iq4_xs_block(W + r * K + b * 256, codebook, canon + (r * (K / 256) + b) * 136);
-    memcpy(canon + rows * (K / 256) * 136, codebook, 16);
-    return 0;
+    if (K % 256 != 0 || codebook == NULL) return 1;
+    if (fmt == OR_IQ4_XS) {
+        for (int64_t r = 0; r < rows; r++)
+            for (int64_t b = 0; b < K / 256; b++)
+                enc_iq4_xs_block(W + r * K + b * 256, (const int8_t*)codebook, canon + (r * (K / 256) + b) * 136);
+        memcpy(canon + rows * (K / 256) * 136, codebook, 16);
+        return 0;
+    }
+    if (fmt == OR_IQ3_S || fmt == OR_IQ2_S) {
+        const int64_t gb = or_grid_bytes(fmt), bb = (fmt == OR_IQ3_S) ? 110 : 82;
+        memcpy(canon, codebook, (size_t)gb);
+        for (int64_t r = 0; r < rows; r++)
+            for (int64_t b = 0; b < K / 256; b++)
+                enc_grid_block(fmt, W + r * K + b * 256, (const uint8_t*)codebook,
+                               canon + gb + (r * (K / 256) + b) * bb);
+        return 0;
+    }
+    return 1;
 }
 
 int or_encode(int fmt, const float* W, int64_t rows, int64_t K, float tensor_scale,
@@ -406,6 +481,7 @@ int or_encode(int fmt, const float* W, int64_t rows, int64_t K, float tensor_sca
  *   NVFP4: w = (e2m1(c) * e4m3(s_b)) * s_T             (one rounding)
  *   FP8  : w = e4m3(c) * s_row                         (one rounding)
  *   IQ4_XS: w = (d * (ls_j - 32)) * C[q]               (one rounding)
+ *   IQ3_S, IQ2_S: w = (d * (2 sc + 1)) * (+-G[idx][i])  (exact)
  * ------------------------------------------------------------------------- */
 static int nvfp4_to_float(const uint8_t* canon, int64_t rows, int64_t K, float* W) {
     const uint8_t* codes = canon;
@@ -447,14 +523,45 @@ static int iq4_xs_to_float(const uint8_t* canon, int64_t rows, int64_t K, float*
     return 0;
 }
 
+static int grid_to_float(int fmt, const uint8_t* canon, int64_t rows, int64_t K, float* W) {
+    const int iq3 = (fmt == OR_IQ3_S);
+    const int gw = iq3 ? 4 : 8, sbs = iq3 ? 32 : 16, bb = iq3 ? 110 : 82;
+    const uint8_t* G = canon;
+    const uint8_t* blocks = canon + or_grid_bytes(fmt);
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t b = 0; b < K / 256; b++) {
+            const uint8_t* blk = blocks + (r * (K / 256) + b) * bb;
+            float d = or_fp16_to_f32(rd16(blk));
+            for (int e = 0; e < 256; e++) {
+                int g = e / gw, i = e % gw, k = e / sbs;
+                int idx, sg, sc;
+                if (iq3) {
+                    idx = blk[2 + g] | (((blk[66 + g / 8] >> (g & 7)) & 1) << 8);
+                    sg = (blk[74 + e / 8] >> (e & 7)) & 1;
+                    sc = (blk[106 + k / 2] >> (4 * (k & 1))) & 15;
+                } else {
+                    idx = blk[2 + g] | (((blk[66 + g / 4] >> (2 * (g & 3))) & 3) << 8);
+                    sg = (blk[34 + g] >> i) & 1;
+                    sc = (blk[74 + k / 2] >> (4 * (k & 1))) & 15;
+                }
+                float a = d * (float)(2 * sc + 1);
+                float m = (float)G[idx * gw + i];
+                W[r * K + b * 256 + e] = a * (sg ? -m : m);
+            }
+        }
+    return 0;
+}
+
 /* For NVFP4, FP8_ROW and IQ4_XS `canon` is the whole matrix stream of `rows` rows
- * (codes, scales, then the tensor scale / row scales / codebook). */
+ * (codes, scales, then the tensor scale / row scales / codebook); for IQ3_S and
+ * IQ2_S it is the grid, then the blocks of the rows. */
 int or_block_to_float(int fmt, const uint8_t* canon, int64_t rows, int64_t K, float* W) {
     int64_t bv = or_block_values(fmt);
     if (bv == 0 || K % bv != 0) return 1;
     if (fmt == OR_NVFP4) return nvfp4_to_float(canon, rows, K, W);
     if (fmt == OR_FP8_ROW) return fp8_row_to_float(canon, rows, K, W);
     if (fmt == OR_IQ4_XS) return iq4_xs_to_float(canon, rows, K, W);
+    if (fmt == OR_IQ3_S || fmt == OR_IQ2_S) return grid_to_float(fmt, canon, rows, K, W);
     for (int64_t r = 0; r < rows; r++) {
         float* w = W + r * K;
         if (fmt == OR_Q8_0) {

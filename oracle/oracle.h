@@ -36,6 +36,21 @@
  *         The pages fix the block size (136 B / 256) and that a weight is a
  *         codebook entry; the field order, the signed scale ls - 32 and the
  *         caller-supplied codebook are this reading (no GGUF layout is printed).
+ *   IQ3_S, IQ2_S per tower: the grid G (a table of the format, caller-supplied:
+ *         IQ3_S 512 entries x 4 uint8 magnitudes, IQ2_S 1024 x 8), then the blocks
+ *         of all rows [rows][K/256]. A group of 4 (IQ3_S) or 8 (IQ2_S) consecutive
+ *         weights is one grid entry with one sign bit per weight:
+ *         w = (d * (2 sc + 1)) * G[idx][i] * (sign ? -1 : +1)   (exact).
+ *         IQ3_S 110 B: fp16 d | 64 B idx bits 0..7 of group i (elements 4i..4i+3) |
+ *           8 B: bit i = idx bit 8 of group i | 32 B: bit e = sign of element e |
+ *           4 B: nibble j (byte j/2, low nibble for even j) = sc of 32-value sub-block j
+ *         IQ2_S 82 B: fp16 d | 32 B idx bits 0..7 of group i (elements 8i..8i+7) |
+ *           32 B: byte i bit k = sign of element 8i+k | 8 B: bits 2i..2i+1 = idx bits
+ *           8..9 of group i | 8 B: nibble k = sc of 16-value sub-block k
+ *         The pages fix the block sizes (110 and 82 B / 256), the group widths (four
+ *         gathers per group of four for IQ3_S; 1,024 entries of 8 weights for IQ2_S)
+ *         and the sign bits; field order, the odd scale 2 sc + 1 and the caller-
+ *         supplied grid are this reading (no grid values are printed).
  * A stacked tower of E experts is E such matrices back to back (for the
  * K-quants this is the same bytes as one [E*N, K] matrix).
  */
@@ -48,7 +63,8 @@
 extern "C" {
 #endif
 
-enum { OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q6_K = 3, OR_NVFP4 = 4, OR_FP8_ROW = 5, OR_Q5_K = 6, OR_IQ4_XS = 7 };
+enum { OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q6_K = 3, OR_NVFP4 = 4, OR_FP8_ROW = 5, OR_Q5_K = 6, OR_IQ4_XS = 7,
+       OR_IQ3_S = 8, OR_IQ2_S = 9 };
 
 /* scalar number formats */
 float or_fp16_to_f32(uint16_t h);
@@ -66,9 +82,12 @@ int64_t or_canon_bytes(int fmt, int64_t rows, int64_t K);
 /* encoders: synthetic-data generation only (not on the hot path) */
 int or_encode(int fmt, const float* W, int64_t rows, int64_t K, float tensor_scale,
               uint8_t* canon);
-/* the codebook formats (IQ4_XS): the matrix's codebook C (16 x int8) is an input */
-int or_encode_cb(int fmt, const float* W, int64_t rows, int64_t K, const int8_t* codebook,
+/* the codebook formats: IQ4_XS takes the matrix's codebook C (16 x int8); IQ3_S and
+ * IQ2_S take the grid G (512 x 4 / 1024 x 8 uint8 magnitudes) */
+int or_encode_cb(int fmt, const float* W, int64_t rows, int64_t K, const void* codebook,
                  uint8_t* canon);
+/* grid bytes of a grid format (0 for the others) */
+int64_t or_grid_bytes(int fmt);
 
 /* BlockToFloat: canonical bytes of `rows` rows -> fp32 W[rows][K] */
 int or_block_to_float(int fmt, const uint8_t* canon, int64_t rows, int64_t K, float* W);

@@ -22,6 +22,8 @@ minus six: mean 0, variance 1 (to within 2^-32), support [-6, 6].
   expert ids:   per token, a partial Fisher-Yates shuffle of range(E) driven by
                 the same hash: top-k distinct ids, uniform without replacement.
   codebooks:    the same shuffle over -127..127: n distinct int8 values, sorted.
+  grids:        per entry and position, one of a few magnitude levels (the same
+                shuffle over 1..63), picked by the hash.
 
 Element index i of a weight matrix W[N, K] of stream s is r*K + k; a stacked
 tower of E experts uses r = e*N + n, so any subset of rows can be regenerated on
@@ -158,6 +160,22 @@ def codebook(seed: int, n: int = 16, stream: int = STREAM_CODEBOOK) -> np.ndarra
         r = j + h % (len(perm) - j)
         perm[j], perm[r] = perm[r], perm[j]
     return np.array(sorted(perm[:n]), dtype=np.int8)
+
+
+def grid(seed: int, entries: int, width: int, levels: int, stream: int = STREAM_CODEBOOK) -> np.ndarray:
+    """uint8 grid[entries, width] of magnitudes: `levels` distinct values drawn from
+    1..63 (the same shuffle), each entry value one of them picked by the hash."""
+    key = _key(seed, stream, 1)
+    perm = list(range(1, 64))
+    for j in range(levels):
+        h = _lowbias32_int(_lowbias32_int(j ^ key) ^ 0x3C6EF372)
+        r = j + h % (len(perm) - j)
+        perm[j], perm[r] = perm[r], perm[j]
+    lv = np.array(sorted(perm[:levels]), dtype=np.uint8)
+    idx = np.arange(entries * width, dtype=np.uint32)
+    with np.errstate(over="ignore"):
+        h = _lowbias32_np(_lowbias32_np(idx ^ np.uint32(key)) ^ np.uint32(0x5BD1E995))
+    return lv[(h % np.uint32(levels)).astype(np.int64)].reshape(entries, width)
 
 
 def bf16_bits(x: torch.Tensor) -> np.ndarray:

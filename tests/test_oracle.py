@@ -399,6 +399,189 @@ def test_iq4_xs_codebook_per_matrix_in_a_tower():
 
 
 # ---------------------------------------------------------------------------
+# IQ3_S, IQ2_S: a group of weights is one grid entry with per-weight sign bits
+# ---------------------------------------------------------------------------
+def test_grid_formats_sizes_match_pages():
+    g = _golden()
+    for fmt, gw, ne in (("iq3_s", 4, 512), ("iq2_s", 8, 1024)):
+        gb = oracle.grid_bytes(fmt)
+        assert gb == ne * gw
+        blk = oracle.canon_bytes(fmt, 1, 256) - gb
+        assert blk == g[f"{fmt}_block_bytes"]
+        assert blk * 8 / 256 == g[f"{fmt}_bits_per_weight"]
+        assert oracle.canon_bytes(fmt, 1, 32 * 256) - gb == g[f"fixture_{fmt}_bytes"]   # 32 blocks
+    assert oracle.grid_bytes("iq2_s") == g["iq2_s_grid_entries"] * g["iq2_s_grid_width"]
+    assert oracle.grid_bytes("iq3_s") // 512 == g["iq3_s_group_width"]
+
+
+def _iq3s_block(d16, sc, idx, neg):
+    """IQ3_S as read: fp16 d | idx low bytes of 64 groups | idx bit 8 of group i at bit
+    i | sign of element e at bit e | 4-bit scales of the 8 sub-blocks."""
+    blk = bytearray(110)
+    blk[0:2] = d16.to_bytes(2, "little")
+    qh, sg = 0, 0
+    for g in range(64):
+        blk[2 + g] = idx[g] & 255
+        qh |= ((idx[g] >> 8) & 1) << g
+    for e in range(256):
+        sg |= (1 if e in neg else 0) << e
+    blk[66:74] = qh.to_bytes(8, "little")
+    blk[74:106] = sg.to_bytes(32, "little")
+    for j in range(8):
+        blk[106 + j // 2] |= sc[j] << (4 * (j & 1))
+    return bytes(blk)
+
+
+def _iq2s_block(d16, sc, idx, neg):
+    """IQ2_S as read: fp16 d | idx low bytes of 32 groups | sign byte of each group |
+    idx bits 8..9 of group i at bits 2i, 2i+1 | 4-bit scales of the 16 sub-blocks."""
+    blk = bytearray(82)
+    blk[0:2] = d16.to_bytes(2, "little")
+    qh = 0
+    for g in range(32):
+        blk[2 + g] = idx[g] & 255
+        qh |= ((idx[g] >> 8) & 3) << (2 * g)
+        for i in range(8):
+            if 8 * g + i in neg:
+                blk[34 + g] |= 1 << i
+    blk[66:74] = qh.to_bytes(8, "little")
+    for k in range(16):
+        blk[74 + k // 2] |= sc[k] << (4 * (k & 1))
+    return bytes(blk)
+
+
+def _grid_decode(fmt, G, blocks, rows=1):
+    canon = bytes(np.ascontiguousarray(G, dtype=np.uint8).reshape(-1)) + b"".join(blocks)
+    return oracle.block_to_float(fmt, np.frombuffer(canon, np.uint8), rows, 256 * len(blocks) // rows)
+
+
+def test_iq3_s_handbuilt_values():
+    G = np.zeros((512, 4), np.uint8)
+    G[0] = [1, 2, 3, 4]
+    G[300] = [10, 20, 30, 40]
+    G[511] = [255, 0, 7, 128]
+    idx = [0] * 64
+    idx[0], idx[8], idx[63] = 300, 0, 511
+    sc = [1, 15, 0, 0, 0, 0, 0, 7]
+    w = _grid_decode("iq3_s", G, [_iq3s_block(0x3800, sc, idx, {1, 253})])[0]
+    # d = 0.5. Group 0 (sub-block 0, a = 0.5 * 3 = 1.5), entry 300, element 1 negative:
+    # 15, -30, 45, 60. Group 8 = elements 32..35 (sub-block 1, a = 0.5 * 31 = 15.5), entry 0:
+    # 15.5, 31, 46.5, 62. Group 1 (elements 4..7), entry 0: 1.5, 3, 4.5, 6.
+    # Group 63 = elements 252..255 (sub-block 7, a = 0.5 * 15 = 7.5), entry 511, element 253
+    # negative: 1912.5, -0, 52.5, 960. Group 40 (elements 160..163, sub-block 5, a = 0.5): 0.5, 1, 1.5, 2.
+    hand = {0: 15.0, 1: -30.0, 2: 45.0, 3: 60.0, 32: 15.5, 33: 31.0, 34: 46.5, 35: 62.0, 4: 1.5, 7: 6.0,
+            252: 1912.5, 253: -0.0, 254: 52.5, 255: 960.0, 160: 0.5, 163: 2.0}
+    for e, v in hand.items():
+        assert w[e] == v, (e, w[e], v)
+    assert np.signbit(w[253])
+
+
+def test_iq2_s_handbuilt_values():
+    G = np.zeros((1024, 8), np.uint8)
+    G[1000] = [1, 2, 3, 4, 5, 6, 7, 8]
+    G[5] = [9, 9, 9, 9, 9, 9, 9, 9]
+    G[256] = [100, 0, 0, 0, 0, 0, 0, 200]
+    idx = [5] * 32
+    idx[0], idx[3], idx[31] = 1000, 256, 1000
+    sc = [2] + [0] * 14 + [15]
+    w = _grid_decode("iq2_s", G, [_iq2s_block(0x3400, sc, idx, {0, 7, 255})])[0]
+    # d = 0.25. Group 0 (sub-block 0, a = 0.25 * 5 = 1.25), entry 1000, elements 0 and 7
+    # negative: -1.25, 2.5, 3.75, 5, 6.25, 7.5, 8.75, -10. Group 1 (elements 8..15, same
+    # sub-block), entry 5: 11.25. Group 3 (elements 24..31, sub-block 1, a = 0.25), entry
+    # 256: 25, 0, ..., 50. Group 31 (elements 248..255, sub-block 15, a = 0.25 * 31 = 7.75),
+    # entry 1000, element 255 negative: 7.75, ..., -62.
+    hand = {0: -1.25, 1: 2.5, 2: 3.75, 6: 8.75, 7: -10.0, 8: 11.25, 15: 11.25, 24: 25.0, 25: 0.0, 31: 50.0,
+            16: 2.25, 248: 7.75, 254: 54.25, 255: -62.0}
+    for e, v in hand.items():
+        assert w[e] == v, (e, w[e], v)
+
+
+@pytest.mark.parametrize("g", [0, 7, 8, 37, 63])
+def test_iq3_s_index_high_bit_and_sign_positions(g):
+    """Only group g takes entry 256 + 1 (its bit 8 set) and only its third element is
+    negative: just those four values change."""
+    G = np.zeros((512, 4), np.uint8)
+    G[1] = [1, 1, 1, 1]
+    G[257] = [2, 3, 4, 5]
+    idx = [1] * 64
+    idx[g] = 257
+    w = _grid_decode("iq3_s", G, [_iq3s_block(0x3C00, [0] * 8, idx, {4 * g + 2})])[0]
+    want = np.ones(256, np.float32)
+    want[4 * g:4 * g + 4] = [2, 3, -4, 5]
+    assert np.array_equal(w, want)
+
+
+@pytest.mark.parametrize("g", [0, 3, 4, 17, 31])
+def test_iq2_s_index_high_bits_and_sign_positions(g):
+    """Only group g takes entry 512 + 256 + 1 (bits 8 and 9 set) and only its element 6
+    is negative."""
+    G = np.zeros((1024, 8), np.uint8)
+    G[1] = 1
+    G[769] = [2, 3, 4, 5, 6, 7, 8, 9]
+    idx = [1] * 32
+    idx[g] = 769
+    w = _grid_decode("iq2_s", G, [_iq2s_block(0x3C00, [0] * 16, idx, {8 * g + 6})])[0]
+    want = np.ones(256, np.float32)
+    want[8 * g:8 * g + 8] = [2, 3, 4, 5, 6, 7, -8, 9]
+    assert np.array_equal(w, want)
+
+
+@pytest.mark.parametrize("fmt,k", [("iq3_s", 0), ("iq3_s", 5), ("iq2_s", 0), ("iq2_s", 9), ("iq2_s", 15)])
+def test_grid_scale_nibble_positions(fmt, k):
+    """Only sub-block k gets sc = 6 (scale 13); every weight is entry 0 = all ones."""
+    ne, gw = (512, 4) if fmt == "iq3_s" else (1024, 8)
+    sbs = 32 if fmt == "iq3_s" else 16
+    G = np.ones((ne, gw), np.uint8)
+    sc = [0] * (256 // sbs)
+    sc[k] = 6
+    mk = _iq3s_block if fmt == "iq3_s" else _iq2s_block
+    w = _grid_decode(fmt, G, [mk(0x3C00, sc, [0] * (256 // gw), set())])[0]
+    want = np.ones(256, np.float32)
+    want[k * sbs:(k + 1) * sbs] = 13.0
+    assert np.array_equal(w, want)
+
+
+def test_grid_is_one_table_for_a_tower():
+    """A tower is one grid, then the blocks of all its rows (as one [E*N, K] matrix)."""
+    G = synth.grid(4, 512, 4, 8)
+    W = synth.weights(9, 6, 512).numpy()
+    c_all = oracle.encode("iq3_s", W, codebook=G)
+    gb = oracle.grid_bytes("iq3_s")
+    c_top = oracle.encode("iq3_s", W[:2], codebook=G)
+    assert np.array_equal(c_all[:gb], G.reshape(-1)) and np.array_equal(c_top[gb:], c_all[gb:gb + 2 * 2 * 110])
+
+
+@pytest.mark.parametrize("fmt", ["iq3_s", "iq2_s"])
+def test_grid_encoder_takes_the_nearest_entry(fmt):
+    """Brute force over the whole grid (fp64): each group's chosen entry is the nearest
+    one to the group's magnitudes at the scale the block carries; signs follow the
+    weights; decoded magnitudes are a * G[idx]."""
+    ne, gw, lv = (512, 4, 8) if fmt == "iq3_s" else (1024, 8, 4)
+    sbs = 32 if fmt == "iq3_s" else 16
+    G = synth.grid(11, ne, gw, lv)
+    W = synth.weights(12, 2, 512).numpy()
+    c = oracle.encode(fmt, W, codebook=G)
+    D = oracle.block_to_float(fmt, c, 2, 512)
+    assert np.all((D < 0) <= (W < 0)) and np.all((W > 0) <= (D >= 0))
+    Gf = G.astype(np.float64)
+    for r in range(2):
+        for g in range(512 // gw):
+            k = (g * gw) // sbs
+            seg = np.abs(W[r, g * gw:(g + 1) * gw]).astype(np.float64)
+            got = np.abs(D[r, g * gw:(g + 1) * gw]).astype(np.float64)
+            # the scale a = d (2 sc + 1) of this sub-block, read from the block's bytes
+            blk = c[oracle.grid_bytes(fmt) + (r * 2 + (g * gw) // 256) * (110 if fmt == "iq3_s" else 82):]
+            d = float(np.frombuffer(bytes(blk[:2]), np.float16)[0])
+            kk = k % (256 // sbs)
+            off = 106 if fmt == "iq3_s" else 74
+            sc = (blk[off + kk // 2] >> (4 * (kk & 1))) & 15
+            a = d * (2 * int(sc) + 1)
+            errs = ((seg[None, :] - a * Gf) ** 2).sum(1)
+            mine = ((seg - got) ** 2).sum()
+            assert mine <= errs.min() * (1 + 1e-5) + 1e-12, (r, g)
+
+
+# ---------------------------------------------------------------------------
 # encode -> decode round trips on N(0, 0.02) data and edge blocks
 # ---------------------------------------------------------------------------
 def _data(rows, K, seed=0):

@@ -76,6 +76,18 @@ MUTANTS = [
      "int q = (blk[8 + e / 2] >> (4 * (1 - (e & 1)))) & 15;\n                float a = d * (float)(ls"),
     ("iq4_xs sub-blocks of 16", "                int j = e / 32;\n                int ls = ((blk[4",
      "                int j = (e / 16) & 7;\n                int ls = ((blk[4"),
+    ("iq3_s index bit 8 from the next group",
+     "idx = blk[2 + g] | (((blk[66 + g / 8] >> (g & 7)) & 1) << 8);",
+     "idx = blk[2 + g] | (((blk[66 + (g + 1) % 64 / 8] >> ((g + 1) & 7)) & 1) << 8);"),
+    ("iq3_s sign bits per group", "sg = (blk[74 + e / 8] >> (e & 7)) & 1;", "sg = (blk[74 + g / 8] >> (g & 7)) & 1;"),
+    ("iq3_s even scales", "float a = d * (float)(2 * sc + 1);\n                float m",
+     "float a = d * (float)(2 * sc);\n                float m"),
+    ("iq2_s index bits 8..9 one bit apart", "idx = blk[2 + g] | (((blk[66 + g / 4] >> (2 * (g & 3))) & 3) << 8);",
+     "idx = blk[2 + g] | (((blk[66 + g / 8] >> (g & 7)) & 3) << 8);"),
+    ("iq2_s sign bit order", "sg = (blk[34 + g] >> i) & 1;", "sg = (blk[34 + g] >> (7 - i)) & 1;"),
+    ("iq2_s scales per 32 values", "int g = e / gw, i = e % gw, k = e / sbs;",
+     "int g = e / gw, i = e % gw, k = e / (2 * sbs);"),
+    ("grid entries read column-wise", "float m = (float)G[idx * gw + i];", "float m = (float)G[i * 512 + idx % 512];"),
     ("iq4_xs codebook read before the blocks", "const int8_t* cb = (const int8_t*)(canon + rows * (K / 256) * 136);",
      "const int8_t* cb = (const int8_t*)(canon);"),
 ]
