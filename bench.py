@@ -116,6 +116,13 @@ WORKLOADS = {
                                      "codebook per expert, top-8, one x row per pair, M=1"),
     "iq4xs_tower_down_m8": dict(fmt="iq4_xs", M=8, tower=True, E=288, topk=8, mats=[("down", 4096, 2048)],
                                 desc="grouped IQ4_XS down-projection tower, 288 experts [4096,2048], top-8, M=8"),
+    "iq2s_tower_gateup_m1": dict(fmt="iq2_s", M=1, tower=True, E=288, topk=8, pair_last=False,
+                                 mats=[("gate", 2048, 4096), ("up", 2048, 4096)],
+                                 desc="grouped IQ2_S gate and up towers, 288 experts [2048,4096], one grid "
+                                      "(1024 x 8) per tower, top-8, M=1"),
+    "iq3s_tower_down_m1": dict(fmt="iq3_s", M=1, tower=True, E=288, topk=8, mats=[("down", 4096, 2048)],
+                               desc="grouped IQ3_S down-projection tower, 288 experts [4096,2048], one grid "
+                                    "(512 x 4) per tower, top-8, one x row per pair, M=1"),
     "iq4xs_mlp_m1": dict(fmt="iq4_xs", M=1, mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
                                                   ("down", QWEN_HIDDEN, QWEN_MLP)],
                          desc="IQ4_XS codebook GEMV at the Qwen3.8-27B MLP shapes (gate, up [17408,5120], "
@@ -129,11 +136,14 @@ DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, 
                  "q4k_mlp_fused_m1": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000,
                  "tower_fused_m1": 20000, "tower_fused_m8": 5000, "q4k_prefill_m512": 2000,
                  "q5k_prefill_m512": 2000, "iq4xs_tower_down_m1": 20000, "iq4xs_tower_down_m8": 5000,
-                 "iq4xs_mlp_m1": 20000}
+                 "iq4xs_mlp_m1": 20000, "iq2s_tower_gateup_m1": 20000, "iq3s_tower_down_m1": 20000}
 
 METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"
 CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q5_k": 176 / 256, "q6_k": 210 / 256,
-                   "nvfp4": 18 / 32, "fp8_row": 1.0, "iq4_xs": 136 / 256}
+                   "nvfp4": 18 / 32, "fp8_row": 1.0, "iq4_xs": 136 / 256, "iq3_s": 110 / 256, "iq2_s": 82 / 256}
+# the grid formats' table (uint8 magnitudes): entries, width, levels of the seeded grid;
+# read once per call on top of the routed experts' blocks
+GRIDS = {"iq3_s": (512, 4, 8), "iq2_s": (1024, 8, 4)}
 
 
 def canon_bytes(fmt, N, K):
@@ -291,11 +301,26 @@ def codebook_of(seed, e):
     return synth.codebook(seed + 7919 * e)
 
 
+def grid_of(fmt, seed):
+    """The grid of a seeded IQ3_S / IQ2_S tower (uint8 [entries, width])."""
+    ne, gw, lv = GRIDS[fmt]
+    return synth.grid(seed, ne, gw, lv)
+
+
 def build_packed(q, fmt, seed, N, K, E, dev):
     """Seeded weights -> library quantizer -> packed device tower (load phase, untimed)."""
     chunk_rows = max(1, (1 << 26) // K)
     canon_parts = []
-    for e in range(E):
+    if fmt in GRIDS:
+        # one grid for the tower, then the blocks of all its rows
+        G = grid_of(fmt, seed)
+        canon_parts.append(torch.from_numpy(G.reshape(-1).copy()).to(dev))
+        for r0 in range(0, E * N, chunk_rows):
+            n = min(chunk_rows, E * N - r0)
+            W = synth.weights(seed, n, K, device=dev, row0=r0, chunk_rows=n)
+            canon_parts.append(q.qmv_quantize_codebook(fmt, W, G)[G.size:])
+            del W
+    for e in range(E if fmt not in GRIDS else 0):
         if fmt in ("nvfp4", "fp8_row"):
             W = synth.weights(seed, N, K, device=dev, row0=e * N, chunk_rows=chunk_rows)
             canon_parts.append(q.qmv_quantize(fmt, W, NVFP4_TS if fmt == "nvfp4" else 0.0))
@@ -353,7 +378,7 @@ class DeviceWorkload:
         # activations, outputs, workspaces
         self.x, self.y, self.ws = [], [], []
         for i, (_, N, K) in enumerate(self.mats):
-            rows = self.M * self.topk if (self.tower and i == len(self.mats) - 1) else self.M
+            rows = self.M * self.topk if self.pair_x(i) else self.M
             self.x.append(synth.activations(200 + i, rows, K, device=dev))
             ysh = (self.M, self.topk, N) if self.tower else (self.M, N)
             self.y.append(torch.empty(ysh, dtype=torch.float32, device=dev))
@@ -376,6 +401,11 @@ class DeviceWorkload:
         # W4A4 runs the activation quantizer and the GEMM per matrix
         self.launches_per_step = len(self.mats) * (2 if (self.w4a4 or self.kquant) else 1)
 
+    def pair_x(self, i):
+        """Tower matrices whose x has one row per (token, slot): the down projection
+        (the last matrix of a layer), unless the workload holds no down projection."""
+        return self.tower and i == len(self.mats) - 1 and WORKLOADS[self.name].get("pair_last", True)
+
     def step_flops(self):
         return sum(2.0 * self.M * N * K for _, N, K in self.mats)
 
@@ -385,12 +415,13 @@ class DeviceWorkload:
         for i, (_, N, K) in enumerate(self.mats):
             xb = self.x[i].numel() * 2
             yb = self.y[i].numel() * 4
+            gb = GRIDS[self.fmt][0] * GRIDS[self.fmt][1] if self.fmt in GRIDS else 0   # the grid, once per call
             if self.tower:
                 u = self.unique[s % len(self.unique)]
                 wb = canon_bytes(self.fmt, N, K) * (2 if (self.fused and i == 0) else 1)
-                tot += u * wb + xb + yb + self.M * self.topk * 4
+                tot += u * wb + xb + yb + self.M * self.topk * 4 + gb
             else:
-                tot += canon_bytes(self.fmt, N, K) * (2 if (self.fused and i == 0) else 1) + xb + yb
+                tot += canon_bytes(self.fmt, N, K) * (2 if (self.fused and i == 0) else 1) + xb + yb + gb
         return tot
 
     def launch_step(self, s):
@@ -402,7 +433,7 @@ class DeviceWorkload:
                                      self.E, self.ws[i], h=self.y[i])
             elif self.tower:
                 q.qmv_grouped(self.fmt, self.packed[c][i], self.ids[s % len(self.ids)], self.x[i], N, K, self.E,
-                              self.ws[i], x_per_pair=(i == len(self.mats) - 1), y=self.y[i])
+                              self.ws[i], x_per_pair=self.pair_x(i), y=self.y[i])
             elif self.fused and i == 0:
                 q.qmv_gemv_swiglu(self.fmt, self.packed[c][i], self.x[i], N, K, self.ws[i], h=self.y[i])
             elif self.kquant:
@@ -616,8 +647,8 @@ def oracle_sample(workload, rows_per_mat):
     for i, (_, N, K) in enumerate(w["mats"]):
         r = min(rows_per_mat[i], N)
         W = synth.weights_rows(100 + i, np.arange(r), K).numpy()
-        canon = oracle.encode(fmt, W, NVFP4_TS if fmt == "nvfp4" else 0.0,
-                              codebook=codebook_of(100 + i, 0) if fmt == "iq4_xs" else None)
+        table = codebook_of(100 + i, 0) if fmt == "iq4_xs" else (grid_of(fmt, 100 + i) if fmt in GRIDS else None)
+        canon = oracle.encode(fmt, W, NVFP4_TS if fmt == "nvfp4" else 0.0, codebook=table)
         x = synth.bf16_bits(synth.activations(200 + i, w["M"], K))
         items.append((fmt, canon, r, K, x))
     return items

@@ -16,9 +16,12 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqmv.so")
 
-QMV_Q8_0, QMV_Q4_K, QMV_Q6_K, QMV_NVFP4, QMV_FP8_ROW, QMV_Q5_K, QMV_IQ4_XS = 1, 2, 3, 4, 5, 6, 7
+QMV_Q8_0, QMV_Q4_K, QMV_Q6_K, QMV_NVFP4, QMV_FP8_ROW, QMV_Q5_K = 1, 2, 3, 4, 5, 6
+QMV_IQ4_XS, QMV_IQ3_S, QMV_IQ2_S = 7, 8, 9
 FORMATS = {"q8_0": QMV_Q8_0, "q4_k": QMV_Q4_K, "q6_k": QMV_Q6_K, "nvfp4": QMV_NVFP4,
-           "fp8_row": QMV_FP8_ROW, "q5_k": QMV_Q5_K, "iq4_xs": QMV_IQ4_XS}
+           "fp8_row": QMV_FP8_ROW, "q5_k": QMV_Q5_K, "iq4_xs": QMV_IQ4_XS, "iq3_s": QMV_IQ3_S,
+           "iq2_s": QMV_IQ2_S}
+GRID_BYTES = {"iq3_s": 512 * 4, "iq2_s": 1024 * 8}
 QMV_ENTRY_GEMV, QMV_ENTRY_GROUPED, QMV_ENTRY_W4A4, QMV_ENTRY_SWIGLU = 1, 2, 3, 4
 QMV_ENTRY_GROUPED_SWIGLU, QMV_ENTRY_KQUANT = 5, 6
 QMV_MAX_M = 8
@@ -223,13 +226,17 @@ def qmv_quantize(fmt, W: torch.Tensor, tensor_scale: float = 0.0, canon: torch.T
 
 def qmv_quantize_codebook(fmt, W: torch.Tensor, codebook, canon: torch.Tensor | None = None,
                           stream=None) -> torch.Tensor:
-    """The codebook formats' encoder: codebook = 16 int8 values (host sequence)."""
+    """The codebook formats' encoder: IQ4_XS takes 16 int8 values, IQ3_S / IQ2_S the
+    grid (uint8 magnitudes, 512 x 4 / 1024 x 8) -- host sequences."""
     _dev(W, "W")
     if W.dtype != torch.float32 or W.dim() != 2 or not W.is_contiguous():
         raise ValueError("W must be a contiguous 2-D float32 tensor")
-    if len(codebook) != 16:
-        raise ValueError("codebook must hold 16 values")
-    cb = (ctypes.c_int8 * 16)(*[int(v) for v in codebook])
+    name = fmt if isinstance(fmt, str) else next(k for k, v in FORMATS.items() if v == int(fmt))
+    vals = [int(v) for v in (codebook.reshape(-1) if hasattr(codebook, "reshape") else codebook)]
+    n = GRID_BYTES.get(name, 16)
+    if len(vals) != n:
+        raise ValueError(f"the {name} table holds {n} values")
+    cb = (ctypes.c_int8 * 16)(*vals) if n == 16 else (ctypes.c_uint8 * n)(*vals)
     rows, K = W.shape
     size = qmv_canon_size(fmt, rows, K, 1)
     if canon is None:

@@ -38,7 +38,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 qmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ECUDA; }
 
-bool valid_fmt(int f) { return f >= QMV_Q8_0 && f <= QMV_IQ4_XS; }
+bool valid_fmt(int f) { return f >= QMV_Q8_0 && f <= QMV_IQ2_S; }
 
 void apply_plan(StreamArgs* a, const StreamPlan& p) {
   a->num_ctas = p.grid;
@@ -56,7 +56,9 @@ size_t qmv_canon_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E) {
   if (!valid_fmt(fmt) || N <= 0 || K <= 0 || E <= 0) return 0;
   const int64_t bv = (fmt == QMV_Q8_0) ? 32 : (fmt == QMV_NVFP4) ? 16 : (fmt == QMV_FP8_ROW) ? 1 : 256;
   if (K % bv) return 0;
-  return (size_t)(E * canon_matrix_bytes((int)fmt, N, K));
+  // the grid formats' stream starts with the tower's grid (one table for all experts)
+  const int64_t grid = is_grid_fmt((int)fmt) ? (int64_t)grid_entries((int)fmt) * grid_width((int)fmt) : 0;
+  return (size_t)(grid + E * canon_matrix_bytes((int)fmt, N, K));
 }
 
 size_t qmv_pack_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E) {
@@ -80,7 +82,7 @@ qmv_status qmv_quantize(qmv_fmt fmt, const float* W, int64_t rows, int64_t K, fl
                         void* canon, cudaStream_t stream) {
   if (!valid_fmt(fmt) || !W || !canon || rows <= 0 || K <= 0) return QMV_EINVAL;
   if (qmv_canon_size(fmt, rows, K, 1) == 0) return QMV_EUNSUPPORTED;
-  if (fmt == QMV_IQ4_XS) return QMV_EUNSUPPORTED;     // needs a codebook (an input, not a rounding)
+  if (fmt >= QMV_IQ4_XS) return QMV_EUNSUPPORTED;     // needs a codebook (an input, not a rounding)
   if (fmt == QMV_NVFP4 && !(tensor_scale >= 0.0f)) return QMV_EINVAL;
   if (!aligned(W, 4)) return QMV_EALIGN;
   qmv_status st = from_cuda(launch_quantize((int)fmt, W, rows, K, tensor_scale, static_cast<uint8_t*>(canon), stream));
@@ -88,13 +90,13 @@ qmv_status qmv_quantize(qmv_fmt fmt, const float* W, int64_t rows, int64_t K, fl
   return st;
 }
 
-qmv_status qmv_quantize_codebook(qmv_fmt fmt, const float* W, int64_t rows, int64_t K, const int8_t* codebook,
+qmv_status qmv_quantize_codebook(qmv_fmt fmt, const float* W, int64_t rows, int64_t K, const void* codebook,
                                  void* canon, cudaStream_t stream) {
-  if (fmt != QMV_IQ4_XS) return valid_fmt(fmt) ? QMV_EUNSUPPORTED : QMV_EINVAL;
+  if (fmt != QMV_IQ4_XS && fmt != QMV_IQ3_S && fmt != QMV_IQ2_S) return valid_fmt(fmt) ? QMV_EUNSUPPORTED : QMV_EINVAL;
   if (!W || !codebook || !canon || rows <= 0 || K <= 0) return QMV_EINVAL;
   if (qmv_canon_size(fmt, rows, K, 1) == 0) return QMV_EUNSUPPORTED;
   if (!aligned(W, 4)) return QMV_EALIGN;
-  qmv_status st = from_cuda(launch_quantize_codebook((int)fmt, W, rows, K, codebook,
+  qmv_status st = from_cuda(launch_quantize_codebook((int)fmt, W, rows, K, static_cast<const uint8_t*>(codebook),
                                                      static_cast<uint8_t*>(canon), stream));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + 7;
   return st;

@@ -65,9 +65,10 @@ cudaError_t launch_dequant(const Layout& L, const uint8_t* packed, int64_t row0,
                            float* out, unsigned* status, cudaStream_t s);
 cudaError_t launch_quantize(int fmt, const float* W, int64_t rows, int64_t K, float ts,
                             uint8_t* canon, cudaStream_t s);
-// the codebook formats (IQ4_XS): 16 int8 entries passed by value
+// the codebook formats: IQ4_XS's 16 int8 entries (passed to the kernel by value),
+// or the grid of IQ3_S / IQ2_S (host bytes, copied to the front of canon first)
 struct Codebook16 { int8_t v[16]; };
-cudaError_t launch_quantize_codebook(int fmt, const float* W, int64_t rows, int64_t K, const int8_t* codebook,
+cudaError_t launch_quantize_codebook(int fmt, const float* W, int64_t rows, int64_t K, const uint8_t* codebook,
                                      uint8_t* canon, cudaStream_t s);
 cudaError_t launch_quant_act(const uint16_t* x, float xs, uint8_t* codes, uint8_t* scales, int M,
                              int64_t K, cudaStream_t s);

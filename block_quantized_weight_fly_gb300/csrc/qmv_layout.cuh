@@ -21,6 +21,16 @@
 //          plus a plane B per 128-row tile: the rows' 8-byte scale fields (fp16 d,
 //          u16 sh, u32 sl, canonical order), then the matrix's 16-byte codebook, so
 //          that every slab copy brings its codebook along         (128 x 8 + 16 B)
+//   IQ3_S: record = 64 B of index low bytes, then 32 B of sign bits, both
+//          thread-major (below)                                               (96 B)
+//          plus a plane B of 14 B per row: fp16 d, the 4 bytes of 4-bit scales, the
+//          index bits 8 as one u16 per thread                                 (14 B)
+//   IQ2_S: record = 32 B of index low bytes (per thread pair), then 32 B of sign
+//          bits (per thread)                                                  (64 B)
+//          plus a plane B of 18 B per row: fp16 d, the 8 bytes of 4-bit scales, the
+//          index bits 8..9 as one u32 per thread pair                         (18 B)
+//   The grid of IQ3_S / IQ2_S (one table per tower) is stored once, as f16 values,
+//   between the header and the first expert (the "prefix").
 //
 // so the bytes of (any row range) x (one k-group) are one contiguous span per
 // plane: one bulk copy moves a 128-row x 256-value slab into shared memory. The
@@ -54,6 +64,13 @@
 // IQ4_XS: word t of chunk j = the canonical index bytes of elements 8t..8t+7 (element
 // 8t+i at nibble i, unchanged); the 16-byte vector v = 2t + (j >> 2) of the record
 // holds the words of chunks 4(j >> 2) .. +3 of thread t, stored at 16 (v ^ (row & 7)).
+// IQ3_S, IQ2_S: the MMA (chunk j, half s) of thread t covers elements 32j + 16s + 4t
+// .. +3, which is one IQ3_S group (8j + 4s + t) and half (t & 1) of one IQ2_S group
+// (4j + 2s + (t >> 1)). Slot m = 2j + s of a thread: index low byte at 16t + m (IQ3_S)
+// or 16(t >> 1) + m (IQ2_S); its four sign bits at bits 4m .. 4m+3 of the thread's
+// 64-bit sign word (IQ3_S at 64 + 8t, IQ2_S at 32 + 8t); the index bit 8 at bit m of
+// the thread's u16 in plane B (IQ3_S), bits 8..9 at bits 2m, 2m+1 of the thread
+// pair's u32 (IQ2_S).
 //
 // NVFP4 tiles. The codes of a 128-row tile of a k-group (16 KB) are stored as the
 // K-major "core matrices" of the 5th-generation tensor core: 8 rows x 16 bytes (32
@@ -94,8 +111,15 @@ constexpr int kHeaderBytes = 256;
 constexpr uint32_t kMagic = 0x31564D51u;  // "QMV1"
 constexpr uint32_t kVersion = 5;
 
-enum Fmt { F_Q8_0 = 1, F_Q4_K = 2, F_Q6_K = 3, F_NVFP4 = 4, F_FP8 = 5, F_Q5_K = 6, F_IQ4_XS = 7 };
-constexpr int F_LAST = F_IQ4_XS;
+enum Fmt { F_Q8_0 = 1, F_Q4_K = 2, F_Q6_K = 3, F_NVFP4 = 4, F_FP8 = 5, F_Q5_K = 6, F_IQ4_XS = 7,
+           F_IQ3_S = 8, F_IQ2_S = 9 };
+constexpr int F_LAST = F_IQ2_S;
+__host__ __device__ constexpr bool is_grid_fmt(int fmt) { return fmt == F_IQ3_S || fmt == F_IQ2_S; }
+// grid entries and weights per entry (IQ3_S 512 x 4, IQ2_S 1024 x 8)
+__host__ __device__ constexpr int grid_entries(int fmt) { return fmt == F_IQ3_S ? 512 : (fmt == F_IQ2_S ? 1024 : 0); }
+__host__ __device__ constexpr int grid_width(int fmt) { return fmt == F_IQ3_S ? 4 : (fmt == F_IQ2_S ? 8 : 0); }
+// plane B bytes per row of the grid formats
+__host__ __device__ constexpr int grid_brow(int fmt) { return fmt == F_IQ3_S ? 14 : 18; }
 // IQ4_XS plane B per 128-row tile: 8 bytes of scale fields per row, then the codebook
 constexpr int kIq4TileB = 128 * 8 + 16;
 
@@ -109,7 +133,7 @@ __host__ __device__ inline int64_t align_up(int64_t v, int64_t a) { return (v + 
 
 // Granule of K the packed layout serves.
 __host__ __device__ inline int64_t k_granule(int fmt) {
-  return (fmt == F_Q4_K || fmt == F_Q5_K || fmt == F_Q6_K || fmt == F_IQ4_XS) ? 256 : (fmt == F_NVFP4 ? 16 : 32);
+  return (fmt == F_Q4_K || fmt == F_Q5_K || fmt == F_Q6_K || fmt >= F_IQ4_XS) ? 256 : (fmt == F_NVFP4 ? 16 : 32);
 }
 
 // bytes of one row record of plane A (per 256 values)
@@ -122,6 +146,8 @@ __host__ __device__ inline int rec_bytes(int fmt) {
     case F_NVFP4: return 128;
     case F_FP8: return 256;
     case F_IQ4_XS: return 128;
+    case F_IQ3_S: return 96;
+    case F_IQ2_S: return 64;
     default: return 0;
   }
 }
@@ -139,7 +165,9 @@ struct Layout {
   int64_t group_bytes;  // plane_a + plane_b
   int64_t extras;       // per-expert extras bytes (aligned to 256)
   int64_t expert_bytes; // bytes per expert (aligned to 256)
-  int64_t total;        // header + E * expert_bytes
+  int64_t prefix;       // the grid formats' f16 grid after the header, else 0 (256-aligned)
+  int64_t base;         // offset of expert 0 = header + prefix
+  int64_t total;        // header + prefix + E * expert_bytes
 };
 
 __host__ __device__ inline bool make_layout(int fmt, int64_t N, int64_t K, int64_t E, Layout* L) {
@@ -155,6 +183,7 @@ __host__ __device__ inline bool make_layout(int fmt, int64_t N, int64_t K, int64
   L->plane_b = (fmt == F_Q6_K)     ? L->n_pad * 2
                : (fmt == F_NVFP4)  ? L->n_pad * 16
                : (fmt == F_IQ4_XS) ? L->row_tiles * kIq4TileB
+               : is_grid_fmt(fmt)  ? L->n_pad * grid_brow(fmt)
                                    : 0;
   L->group_bytes = L->plane_a + L->plane_b;
   int64_t ex = 0;
@@ -162,7 +191,9 @@ __host__ __device__ inline bool make_layout(int fmt, int64_t N, int64_t K, int64
   if (fmt == F_FP8) ex = align_up(L->n_pad * 4, 256);
   L->extras = ex;
   L->expert_bytes = align_up(L->k_groups * L->group_bytes + ex, 256);
-  L->total = kHeaderBytes + E * L->expert_bytes;
+  L->prefix = is_grid_fmt(fmt) ? align_up((int64_t)grid_entries(fmt) * grid_width(fmt) * 2, 256) : 0;
+  L->base = kHeaderBytes + L->prefix;
+  L->total = L->base + E * L->expert_bytes;
   return true;
 }
 
@@ -175,6 +206,8 @@ __host__ __device__ inline int64_t canon_matrix_bytes(int fmt, int64_t N, int64_
     case F_NVFP4: return N * (K / 2) + N * (K / 16) + 4;
     case F_FP8: return N * K + N * 4;
     case F_IQ4_XS: return N * (K / 256) * 136 + 16;
+    case F_IQ3_S: return N * (K / 256) * 110;     // per matrix; a tower adds the grid once
+    case F_IQ2_S: return N * (K / 256) * 82;
     default: return 0;
   }
 }

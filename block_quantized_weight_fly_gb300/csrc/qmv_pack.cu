@@ -22,7 +22,7 @@ __device__ __forceinline__ uint32_t load_u32(const uint8_t* p) {
 }
 
 __device__ __forceinline__ uint8_t* group_plane(const Layout& L, uint8_t* base, int64_t e, int64_t g) {
-  return base + kHeaderBytes + e * L.expert_bytes + g * L.group_bytes;
+  return base + L.base + e * L.expert_bytes + g * L.group_bytes;
 }
 
 __global__ void pack_kernel(Layout L, const uint8_t* __restrict__ canon, uint8_t* __restrict__ dst) {
@@ -44,7 +44,7 @@ __global__ void pack_kernel(Layout L, const uint8_t* __restrict__ canon, uint8_t
   const int cl = (int)(c % kChunksPerSlab);
   uint8_t* plane = group_plane(L, dst, e, g);
   uint8_t* rec = plane + n * L.rec;
-  uint8_t* extras = dst + kHeaderBytes + e * L.expert_bytes + L.k_groups * L.group_bytes;
+  uint8_t* extras = dst + L.base + e * L.expert_bytes + L.k_groups * L.group_bytes;
   const int64_t row = e * L.N + n;          // row of the stacked tower
   switch (L.fmt) {
     case F_Q8_0: {
@@ -121,7 +121,67 @@ __global__ void pack_kernel(Layout L, const uint8_t* __restrict__ canon, uint8_t
       if (cl == 0 && (n & 127) == 0)
         copy_bytes(plane + L.plane_a + iq4_codebook_off(n), ce + L.N * (L.K / 256) * 136, 16);
     } break;
+    case F_IQ3_S: {
+      // chunk cl of the block: groups 8cl .. 8cl+7; thread t's slots m = 2cl + s hold group 8cl + 4s + t
+      const uint8_t* blk = canon + grid_entries(F_IQ3_S) * 4 + (row * (L.K / 256) + g) * 110;
+      for (int t = 0; t < 4; ++t)
+        for (int sh = 0; sh < 2; ++sh) {
+          const int gr = 8 * cl + 4 * sh + t, m = 2 * cl + sh;
+          rec[16 * t + m] = blk[2 + gr];
+          const uint32_t sg = (blk[74 + gr / 2] >> (4 * (gr & 1))) & 15u;   // elements 4gr..4gr+3
+          rec[64 + 8 * t + m / 2] |= (uint8_t)(sg << (4 * (m & 1)));
+        }
+      if (cl == 0) {   // plane B of the row: d, scales, and every slot's index bit 8
+        uint8_t* pb = plane + L.plane_a + n * 14;
+        copy_bytes(pb, blk, 2);
+        copy_bytes(pb + 2, blk + 106, 4);
+        for (int t = 0; t < 4; ++t) {
+          uint32_t h = 0u;
+          for (int m = 0; m < 16; ++m) {
+            const int gr = 8 * (m >> 1) + 4 * (m & 1) + t;
+            h |= ((uint32_t)(blk[66 + gr / 8] >> (gr & 7)) & 1u) << m;
+          }
+          pb[6 + 2 * t] = (uint8_t)h;
+          pb[7 + 2 * t] = (uint8_t)(h >> 8);
+        }
+      }
+    } break;
+    case F_IQ2_S: {
+      // chunk cl: groups 4cl .. 4cl+3; pair p's slots m = 2cl + s hold group 4cl + 2s + p, and
+      // thread t's sign slot m holds half (t & 1) of that group (t >> 1 = p)
+      const uint8_t* blk = canon + grid_entries(F_IQ2_S) * 8 + (row * (L.K / 256) + g) * 82;
+      for (int p = 0; p < 2; ++p)
+        for (int sh = 0; sh < 2; ++sh) {
+          const int gr = 4 * cl + 2 * sh + p, m = 2 * cl + sh;
+          rec[16 * p + m] = blk[2 + gr];
+          for (int hf = 0; hf < 2; ++hf) {
+            const int t = 2 * p + hf;
+            const uint32_t sg = (blk[34 + gr] >> (4 * hf)) & 15u;
+            rec[32 + 8 * t + m / 2] |= (uint8_t)(sg << (4 * (m & 1)));
+          }
+        }
+      if (cl == 0) {   // plane B of the row: d, scales, and every slot's index bits 8..9
+        uint8_t* pb = plane + L.plane_a + n * 18;
+        copy_bytes(pb, blk, 2);
+        copy_bytes(pb + 2, blk + 74, 8);
+        for (int p = 0; p < 2; ++p) {
+          uint32_t h = 0u;
+          for (int m = 0; m < 16; ++m) {
+            const int gr = 4 * (m >> 1) + 2 * (m & 1) + p;
+            h |= ((uint32_t)(blk[66 + gr / 4] >> (2 * (gr & 3))) & 3u) << (2 * m);
+          }
+          for (int i = 0; i < 4; ++i) pb[10 + 4 * p + i] = (uint8_t)(h >> (8 * i));
+        }
+      }
+    } break;
   }
+}
+
+// the grid formats' table (canonical uint8 magnitudes at the front of the stream) ->
+// f16 values in the packed prefix
+__global__ void pack_grid_kernel(int n, const uint8_t* __restrict__ canon, uint8_t* __restrict__ dst) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) reinterpret_cast<__half*>(dst + kHeaderBytes)[i] = __ushort2half_rn((unsigned short)canon[i]);
 }
 
 cudaError_t launch_pack(const Layout& L, const uint8_t* canon, uint8_t* dst, cudaStream_t s) {
@@ -131,6 +191,10 @@ cudaError_t launch_pack(const Layout& L, const uint8_t* canon, uint8_t* dst, cud
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
   pack_kernel<<<(unsigned)blocks, threads, 0, s>>>(L, canon, dst);
+  if (is_grid_fmt(L.fmt)) {
+    const int n = grid_entries(L.fmt) * grid_width(L.fmt);
+    pack_grid_kernel<<<(n + threads - 1) / threads, threads, 0, s>>>(n, canon, dst);
+  }
   return cudaGetLastError();
 }
 
@@ -159,9 +223,9 @@ __global__ void dequant_kernel(Layout L, const uint8_t* __restrict__ packed, int
   const int64_t e = row / L.N, n = row % L.N;
   const int64_t g = c / kChunksPerSlab;
   const int cl = (int)(c % kChunksPerSlab);
-  const uint8_t* plane = packed + kHeaderBytes + e * L.expert_bytes + g * L.group_bytes;
+  const uint8_t* plane = packed + L.base + e * L.expert_bytes + g * L.group_bytes;
   const uint8_t* rec = plane + n * L.rec;
-  const uint8_t* extras = packed + kHeaderBytes + e * L.expert_bytes + L.k_groups * L.group_bytes;
+  const uint8_t* extras = packed + L.base + e * L.expert_bytes + L.k_groups * L.group_bytes;
   float* o = out + (row - row0) * L.K + c * kChunk;
   switch (L.fmt) {
     case F_Q8_0: {
@@ -238,6 +302,40 @@ __global__ void dequant_kernel(Layout L, const uint8_t* __restrict__ packed, int
       for (int wd = 0; wd < 4; ++wd) {
         const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + iq4_word_off(wd, cl, r));
         for (int i = 0; i < 8; ++i) o[8 * wd + i] = __fmul_rn(a, (float)cb[(w >> (4 * i)) & 15u]);
+      }
+    } break;
+    case F_IQ3_S:
+    case F_IQ2_S: {
+      // w = (d (2 sc + 1)) (+-G[idx][i]); G from the packed prefix (f16, exact)
+      const bool iq3 = L.fmt == F_IQ3_S;
+      const __half* G = reinterpret_cast<const __half*>(packed + kHeaderBytes);
+      const uint8_t* pb = plane + L.plane_a + n * grid_brow(L.fmt);
+      const float d = h2f((uint32_t)pb[0] | ((uint32_t)pb[1] << 8));
+      for (int sh = 0; sh < 2; ++sh) {
+        const int m = 2 * cl + sh;
+        const int k = iq3 ? cl : m;                              // sub-block of 32 / 16 values
+        const int sc = (pb[2 + k / 2] >> (4 * (k & 1))) & 15;
+        const float a = __fmul_rn(d, (float)(2 * sc + 1));
+        for (int t = 0; t < 4; ++t) {
+          int idx, gw, off;
+          if (iq3) {
+            const int hb = (pb[6 + 2 * t + m / 8] >> (m & 7)) & 1;
+            idx = rec[16 * t + m] | (hb << 8);
+            gw = 4;
+            off = 0;
+          } else {
+            const int p = t >> 1;
+            const int hb = (pb[10 + 4 * p + (2 * m) / 8] >> ((2 * m) & 7)) & 3;
+            idx = rec[16 * p + m] | (hb << 8);
+            gw = 8;
+            off = 4 * (t & 1);
+          }
+          const uint32_t sg = (rec[(iq3 ? 64 : 32) + 8 * t + m / 2] >> (4 * (m & 1))) & 15u;
+          for (int i = 0; i < 4; ++i) {
+            const float mg = __half2float(G[idx * gw + off + i]);
+            o[16 * sh + 4 * t + i] = __fmul_rn(a, ((sg >> i) & 1u) ? -mg : mg);
+          }
+        }
       }
     } break;
   }
@@ -524,14 +622,90 @@ __global__ void quant_iq4_xs_kernel(const float* __restrict__ W, int64_t nblk, C
   for (int i = 0; i < 136; ++i) o[i] = (uint8_t)(words[i >> 2] >> (8 * (i & 3)));
 }
 
-cudaError_t launch_quantize_codebook(int fmt, const float* W, int64_t rows, int64_t K, const int8_t* codebook,
+// IQ3_S / IQ2_S: per sub-block (32 / 16 values) s = amax / gmax, gmax = the largest
+// magnitude in the grid; d = max s / 31 in fp16; sc = clamp(rint((s / d - 1) / 2), 0, 15),
+// a = d (2 sc + 1); per group (4 / 8 weights) the signs of its weights and the grid
+// entry nearest to their magnitudes, sum_i (|w_i| - a G[c][i])^2 in fp32 in i order,
+// ties to the lower index. One thread per block; G (uint8) is in global memory.
+template <int FMT>
+__global__ void quant_grid_kernel(const float* __restrict__ W, int64_t nblk, const uint8_t* __restrict__ G,
+                                  int gmax, uint8_t* __restrict__ out) {
+  constexpr bool kIq3 = FMT == F_IQ3_S;
+  constexpr int gw = kIq3 ? 4 : 8, ne = kIq3 ? 512 : 1024, sbs = kIq3 ? 32 : 16, bb = kIq3 ? 110 : 82;
+  constexpr int nsb = 256 / sbs;
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  const float* x = W + b * 256;
+  // the block is assembled in 32-bit words, then stored byte by byte
+  uint32_t wd[(bb + 3) / 4];
+  for (int i = 0; i < (bb + 3) / 4; ++i) wd[i] = 0u;
+  auto put = [&](int byte, uint32_t v) { wd[byte >> 2] |= (v & 0xFFu) << (8 * (byte & 3)); };
+  float s[nsb], smax = 0.0f;
+  for (int k = 0; k < nsb; ++k) {
+    float amax = 0.0f;
+    for (int i = 0; i < sbs; ++i)
+      if (fabsf(x[k * sbs + i]) > amax) amax = fabsf(x[k * sbs + i]);
+    s[k] = (gmax > 0) ? __fdiv_rn(amax, (float)gmax) : 0.0f;
+    if (s[k] > smax) smax = s[k];
+  }
+  const uint32_t dh = f2h_bits(__fdiv_rn(smax, 31.0f));
+  const float d = h2f(dh);
+  put(0, dh);
+  put(1, dh >> 8);
+  for (int k = 0; k < nsb; ++k) {
+    int sc = 0;
+    if (d > 0.0f) sc = (int)clampf(rintf(__fdiv_rn(__fsub_rn(__fdiv_rn(s[k], d), 1.0f), 2.0f)), 0.0f, 15.0f);
+    put((kIq3 ? 106 : 74) + k / 2, (uint32_t)sc << (4 * (k & 1)));
+    const float a = __fmul_rn(d, (float)(2 * sc + 1));
+    for (int g = k * sbs / gw; g < (k + 1) * sbs / gw; ++g) {
+      const float* xg = x + g * gw;
+      float m[gw];
+      for (int i = 0; i < gw; ++i) m[i] = fabsf(xg[i]);
+      int best = 0;
+      float be = 0.0f;
+      for (int c = 0; c < ne; ++c) {
+        float e = 0.0f;
+        for (int i = 0; i < gw; ++i) {
+          const float t = __fsub_rn(m[i], __fmul_rn(a, (float)G[c * gw + i]));
+          e = __fadd_rn(e, __fmul_rn(t, t));
+        }
+        if (c == 0 || e < be) { be = e; best = c; }
+      }
+      put(2 + g, (uint32_t)best);
+      if (kIq3) put(66 + g / 8, (uint32_t)((best >> 8) & 1) << (g & 7));
+      else put(66 + g / 4, (uint32_t)((best >> 8) & 3) << (2 * (g & 3)));
+      for (int i = 0; i < gw; ++i)
+        if (xg[i] < 0.0f) {
+          if (kIq3) put(74 + (g * 4 + i) / 8, 1u << ((g * 4 + i) & 7));
+          else put(34 + g, 1u << i);
+        }
+    }
+  }
+  uint8_t* o = out + b * bb;
+  for (int i = 0; i < bb; ++i) o[i] = (uint8_t)(wd[i >> 2] >> (8 * (i & 3)));
+}
+
+cudaError_t launch_quantize_codebook(int fmt, const float* W, int64_t rows, int64_t K, const uint8_t* codebook,
                                      uint8_t* canon, cudaStream_t s) {
-  if (fmt != F_IQ4_XS) return cudaErrorInvalidValue;
-  Codebook16 cb;
-  for (int i = 0; i < 16; ++i) cb.v[i] = codebook[i];
   const int threads = 128;
   const int64_t n = rows * (K / 256);
-  quant_iq4_xs_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, n, cb, canon);
+  if (fmt == F_IQ4_XS) {
+    Codebook16 cb;
+    for (int i = 0; i < 16; ++i) cb.v[i] = (int8_t)codebook[i];
+    quant_iq4_xs_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, n, cb, canon);
+    return cudaGetLastError();
+  }
+  if (!is_grid_fmt(fmt)) return cudaErrorInvalidValue;
+  // the grid goes first in the stream (and is what the kernel reads)
+  const size_t gb = (size_t)grid_entries(fmt) * grid_width(fmt);
+  int gmax = 0;
+  for (size_t i = 0; i < gb; ++i) gmax = codebook[i] > gmax ? codebook[i] : gmax;
+  cudaError_t err = cudaMemcpyAsync(canon, codebook, gb, cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) return err;
+  if (fmt == F_IQ3_S)
+    quant_grid_kernel<F_IQ3_S><<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, n, canon, gmax, canon + gb);
+  else
+    quant_grid_kernel<F_IQ2_S><<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(W, n, canon, gmax, canon + gb);
   return cudaGetLastError();
 }
 

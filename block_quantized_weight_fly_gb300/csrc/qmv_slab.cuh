@@ -14,6 +14,8 @@
 //   NVFP4, FP8 -> f16: hardware cvt of FP4/FP8 pairs to f16x2 (exact).
 //   IQ4_XS     -> f16: a byte-permute lookup of the 16-entry codebook, placed under
 //                      the f16 pattern of 1024 ({1152 + C[q], 1152 + C[q']} exactly).
+//   IQ3_S, IQ2_S -> f16: an 8-byte shared-memory load of the grid entry (f16
+//                      magnitudes), signs applied with one multiply and one AND-XOR.
 // Products of these small exact values with the activations are exact and the
 // tensor core accumulates in fp32.
 //
@@ -28,8 +30,9 @@
 // One accumulation order for every M (so that row m of an M-row call equals the
 // one-row call on x[m] bit for bit). The units of a slab are split among the four
 // threads t of an mma quad exactly as the unit columns place them: quad position t
-// owns the units of chunks 2t and 2t+1 (Q4_K, Q5_K, Q8_0, FP8, IQ4_XS: units 2t, 2t+1; Q6_K
-// units 4t .. 4t+3; NVFP4 blocks 4t .. 4t+3). Per output (row, token):
+// owns the units of chunks 2t and 2t+1 (Q4_K, Q5_K, Q8_0, FP8, IQ4_XS, IQ3_S: units
+// 2t, 2t+1; Q6_K, IQ2_S units 4t .. 4t+3; NVFP4 blocks 4t .. 4t+3). Per output
+// (row, token):
 //   * every unit sum is the same MMA chain over the same operands in both forms
 //     (in the unit-column form the other columns only add exact zeros);
 //   * c_t = the format's combination of position t's unit sums with their scales
@@ -205,6 +208,14 @@ __device__ __forceinline__ float nv_comb(float s0, float s1, float s2, float s3,
 }
 // FP8: two chunk sums (the row scale multiplies the row's total)
 __device__ __forceinline__ float fp8_comb(float D0, float D1) { return __fadd_rn(D0, D1); }
+// IQ3_S over two 32-value chunks, IQ2_S over four 16-value units (no offset term)
+__device__ __forceinline__ float grid_comb(float a0, float a1, float D0, float D1) {
+  return __fmaf_rn(a0, D0, __fmul_rn(a1, D1));
+}
+__device__ __forceinline__ float grid16_comb(float a0, float a1, float a2, float a3, float D0, float D1, float D2,
+                                             float D3) {
+  return __fmaf_rn(a3, D3, __fmaf_rn(a2, D2, __fmaf_rn(a1, D1, __fmul_rn(a0, D0))));
+}
 // IQ4_XS over two 32-value chunks: a_i (D_i - 1152 X_i), D_i over 1152 + C[q]
 __device__ __forceinline__ float iq4_comb(float a0, float a1, float D0, float D1, float X0, float X1) {
   return __fmaf_rn(a0, __fmaf_rn(-1152.0f, X0, D0), __fmul_rn(a1, __fmaf_rn(-1152.0f, X1, D1)));
@@ -990,6 +1001,221 @@ struct Slab<F_IQ4_XS, 8> {
       for (int e = 0; e < 4; ++e) {
         const float* sc = (e < 2) ? sA : sB;
         tc_add(a, t, e, iq4_comb(sc[0], sc[1], D[0][e], D[1][e], X[0][e], X[1][e]));
+      }
+    }
+  }
+};
+
+// ============================================================================
+// IQ3_S, IQ2_S. A group of weights is one entry of the format's grid, kept in shared
+// memory as f16 magnitudes, with one sign bit per weight: w = a G[idx][i] (+-), a =
+// d (2 sc + 1) per 32 (IQ3_S) / 16 (IQ2_S) values. The MMA of slot m = 2j + s (chunk
+// j, half s) covers elements 32j + 16s + 4t .. +3 in thread t: one IQ3_S group, half
+// an IQ2_S group. Its four magnitudes are one 8-byte shared-memory load (two f16
+// pairs); its four sign bits are spread onto the pairs' sign bits with one multiply
+// each (no carries: the two shifted copies of the nibble do not overlap) and applied
+// with one AND-XOR. x goes to the MMA in f16.
+// ============================================================================
+__device__ __forceinline__ uint32_t lds16(const void* p) { return *reinterpret_cast<const unsigned short*>(p); }
+
+// the two A registers of a slot: grid entry bytes at e (4 f16), sign nibble nib
+__device__ __forceinline__ void grid_slot(const uint8_t* e, uint32_t nib, uint32_t& p01, uint32_t& p23) {
+  const uint2 v = lds64(e);
+  p01 = v.x ^ ((nib * 0x40008000u) & 0x80008000u);   // sign bits 0, 1 -> bits 15, 31
+  p23 = v.y ^ ((nib * 0x10002000u) & 0x80008000u);   // sign bits 2, 3 -> bits 15, 31
+}
+// index low byte m of a 16-byte vector (4 words), compile-time m
+__device__ __forceinline__ uint32_t byte_of(const uint32_t (&Q)[4], int m) { return (Q[m >> 2] >> (8 * (m & 3))) & 0xFFu; }
+
+template <>
+struct Slab<F_IQ3_S, 1> {
+  // unit j = chunk j in column j: even chunks accumulate in dE, odd ones in dO, so
+  // position t's units 2t, 2t+1 are dE column 2t and dO column 2t+1
+  __device__ static void run(const uint8_t* st, const uint8_t* pb, const uint8_t* xs, int, int w, int lane,
+                             float2* gtab, float* acc) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* G = reinterpret_cast<const uint8_t*>(gtab);   // 512 entries x 4 f16 (8 B)
+    const int rowA = 16 * w + g, rowB = rowA + 8;
+    const uint8_t* rA = st + rowA * 96;
+    const uint8_t* rB = st + rowB * 96;
+    const uint8_t* bA = pb + rowA * 14;
+    const uint8_t* bB = pb + rowB * 14;
+    // the lane's unit: chunk g, elements 16s + 4t .. +3 (s = 0, 1)
+    const uint2 xa = lds64(xs + 64 * g + 8 * t), xb = lds64(xs + 64 * g + 32 + 8 * t);
+    const uint32_t x0 = bf16x2_to_f16x2(xa.x), x1 = bf16x2_to_f16x2(xa.y);
+    const uint32_t x2 = bf16x2_to_f16x2(xb.x), x3 = bf16x2_to_f16x2(xb.y);
+    const uint4 qa = lds128v(rA + 16 * t), qb = lds128v(rB + 16 * t);
+    const uint32_t QA[4] = {qa.x, qa.y, qa.z, qa.w}, QB[4] = {qb.x, qb.y, qb.z, qb.w};
+    const uint2 sA = lds64(rA + 64 + 8 * t), sB = lds64(rB + 64 + 8 * t);
+    const uint32_t hA = lds16(bA + 6 + 2 * t), hB = lds16(bB + 6 + 2 * t);
+    float dE[4] = {0.f, 0.f, 0.f, 0.f}, dO[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const int j = m >> 1, sh = m & 1;
+      const uint32_t mk = (g == j) ? kOnesF16 : 0u;
+      const uint32_t iA = byte_of(QA, m) | (((hA >> m) & 1u) << 8), iB = byte_of(QB, m) | (((hB >> m) & 1u) << 8);
+      const uint32_t nA = ((m < 8 ? sA.x : sA.y) >> (4 * (m & 7))) & 15u;
+      const uint32_t nB = ((m < 8 ? sB.x : sB.y) >> (4 * (m & 7))) & 15u;
+      uint32_t a01, a23, b01, b23;
+      grid_slot(G + 8 * iA, nA, a01, a23);
+      grid_slot(G + 8 * iB, nB, b01, b23);
+      mma_f16((j & 1) ? dO : dE, a01, b01, a23, b23, hmul2(sh ? x2 : x0, mk), hmul2(sh ? x3 : x1, mk));
+    }
+    const float dA = h2f(lds16(bA)), dB = h2f(lds16(bB));
+    const uint32_t cA = bA[2 + t], cB = bB[2 + t];                  // scales of chunks 2t, 2t+1
+    const float aA0 = __fmul_rn(dA, (float)(2 * (int)(cA & 15u) + 1)), aA1 = __fmul_rn(dA, (float)(2 * (int)(cA >> 4) + 1));
+    const float aB0 = __fmul_rn(dB, (float)(2 * (int)(cB & 15u) + 1)), aB1 = __fmul_rn(dB, (float)(2 * (int)(cB >> 4) + 1));
+    acc[0] = __fadd_rn(acc[0], grid_comb(aA0, aA1, dE[0], dO[1]));
+    acc[1] = __fadd_rn(acc[1], grid_comb(aB0, aB1, dE[2], dO[3]));
+  }
+};
+
+template <>
+struct Slab<F_IQ3_S, 8> {
+  __device__ static void run(const uint8_t* st, const uint8_t* pb, const uint8_t* xs, int R, int w, int lane,
+                             float2* gtab, float (&a)[4][4]) {
+    const int g = lane >> 2, tq = lane & 3;
+    const uint8_t* G = reinterpret_cast<const uint8_t*>(gtab);
+    const int rowA = 16 * w + g, rowB = rowA + 8;
+    const uint8_t* rA = st + rowA * 96;
+    const uint8_t* rB = st + rowB * 96;
+    const uint8_t* bA = pb + rowA * 14;
+    const uint8_t* bB = pb + rowB * 14;
+    const bool has_x = g < R;
+    const uint4 qa = lds128v(rA + 16 * tq), qb = lds128v(rB + 16 * tq);
+    const uint32_t QA[4] = {qa.x, qa.y, qa.z, qa.w}, QB[4] = {qb.x, qb.y, qb.z, qb.w};
+    const uint2 sA = lds64(rA + 64 + 8 * tq), sB = lds64(rB + 64 + 8 * tq);
+    const uint32_t hA = lds16(bA + 6 + 2 * tq), hB = lds16(bB + 6 + 2 * tq);
+    const float dA = h2f(lds16(bA)), dB = h2f(lds16(bB));
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      float D[2][4];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int j = 2 * t + q;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) D[q][e] = 0.f;
+#pragma unroll
+        for (int sh = 0; sh < 2; ++sh) {
+          const int m = 2 * j + sh;
+          // x already f16 (converted per stage)
+          const uint2 xv = has_x ? lds64(xs + 64 * j + 32 * sh + 8 * tq) : make_uint2(0u, 0u);
+          const uint32_t iA = byte_of(QA, m) | (((hA >> m) & 1u) << 8), iB = byte_of(QB, m) | (((hB >> m) & 1u) << 8);
+          const uint32_t nA = ((m < 8 ? sA.x : sA.y) >> (4 * (m & 7))) & 15u;
+          const uint32_t nB = ((m < 8 ? sB.x : sB.y) >> (4 * (m & 7))) & 15u;
+          uint32_t a01, a23, b01, b23;
+          grid_slot(G + 8 * iA, nA, a01, a23);
+          grid_slot(G + 8 * iB, nB, b01, b23);
+          mma_f16(D[q], a01, b01, a23, b23, xv.x, xv.y);
+        }
+      }
+      const uint32_t cA = bA[2 + t], cB = bB[2 + t];
+      const float sA0 = __fmul_rn(dA, (float)(2 * (int)(cA & 15u) + 1)), sA1 = __fmul_rn(dA, (float)(2 * (int)(cA >> 4) + 1));
+      const float sB0 = __fmul_rn(dB, (float)(2 * (int)(cB & 15u) + 1)), sB1 = __fmul_rn(dB, (float)(2 * (int)(cB >> 4) + 1));
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        tc_add(a, t, e, (e < 2) ? grid_comb(sA0, sA1, D[0][e], D[1][e]) : grid_comb(sB0, sB1, D[0][e], D[1][e]));
+    }
+  }
+};
+
+template <>
+struct Slab<F_IQ2_S, 1> {
+  // Unit u = 2j + s (16 values) sits in accumulator group j & 1, column 2(j >> 1) + s
+  // (as Q6_K): position t's columns 2t, 2t+1 hold units 4t .. 4t+3. Thread (g', t)
+  // carries the activations of the unit in column g'.
+  __device__ static void run(const uint8_t* st, const uint8_t* pb, const uint8_t* xs, int, int w, int lane,
+                             float2* gtab, float* acc) {
+    const int g = lane >> 2, t = lane & 3, p = t >> 1;
+    const uint8_t* G = reinterpret_cast<const uint8_t*>(gtab) + 8 * (t & 1);   // 1024 entries x 8 f16 (16 B)
+    const int rowA = 16 * w + g, rowB = rowA + 8;
+    const uint8_t* rA = st + rowA * 64;
+    const uint8_t* rB = st + rowB * 64;
+    const uint8_t* bA = pb + rowA * 18;
+    const uint8_t* bB = pb + rowB * 18;
+    // column g of group q: chunk 2(g >> 1) + q, half g & 1, elements 4t .. 4t+3
+    const uint2 xa = lds64(xs + 128 * (g >> 1) + 32 * (g & 1) + 8 * t);
+    const uint2 xb = lds64(xs + 128 * (g >> 1) + 64 + 32 * (g & 1) + 8 * t);
+    const uint32_t x0 = bf16x2_to_f16x2(xa.x), x1 = bf16x2_to_f16x2(xa.y);
+    const uint32_t x2 = bf16x2_to_f16x2(xb.x), x3 = bf16x2_to_f16x2(xb.y);
+    const uint4 qa = lds128v(rA + 16 * p), qb = lds128v(rB + 16 * p);
+    const uint32_t QA[4] = {qa.x, qa.y, qa.z, qa.w}, QB[4] = {qb.x, qb.y, qb.z, qb.w};
+    const uint2 sA = lds64(rA + 32 + 8 * t), sB = lds64(rB + 32 + 8 * t);
+    const uint32_t hA = lds16(bA + 10 + 4 * p) | (lds16(bA + 12 + 4 * p) << 16);
+    const uint32_t hB = lds16(bB + 10 + 4 * p) | (lds16(bB + 12 + 4 * p) << 16);
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const int j = m >> 1, sh = m & 1;
+      const uint32_t mk = ((2 * (j >> 1) + sh) == g) ? kOnesF16 : 0u;
+      const uint32_t iA = byte_of(QA, m) | (((hA >> (2 * m)) & 3u) << 8), iB = byte_of(QB, m) | (((hB >> (2 * m)) & 3u) << 8);
+      const uint32_t nA = ((m < 8 ? sA.x : sA.y) >> (4 * (m & 7))) & 15u;
+      const uint32_t nB = ((m < 8 ? sB.x : sB.y) >> (4 * (m & 7))) & 15u;
+      uint32_t a01, a23, b01, b23;
+      grid_slot(G + 16 * iA, nA, a01, a23);
+      grid_slot(G + 16 * iB, nB, b01, b23);
+      mma_f16((j & 1) ? d1 : d0, a01, b01, a23, b23, hmul2((j & 1) ? x2 : x0, mk), hmul2((j & 1) ? x3 : x1, mk));
+    }
+    const float dA = h2f(lds16(bA)), dB = h2f(lds16(bB));
+    const uint32_t cA = lds16(bA + 2 + 2 * t), cB = lds16(bB + 2 + 2 * t);   // scales of units 4t .. 4t+3
+    float aA[4], aB[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      aA[k] = __fmul_rn(dA, (float)(2 * (int)((cA >> (4 * k)) & 15u) + 1));
+      aB[k] = __fmul_rn(dB, (float)(2 * (int)((cB >> (4 * k)) & 15u) + 1));
+    }
+    acc[0] = __fadd_rn(acc[0], grid16_comb(aA[0], aA[1], aA[2], aA[3], d0[0], d0[1], d1[0], d1[1]));
+    acc[1] = __fadd_rn(acc[1], grid16_comb(aB[0], aB[1], aB[2], aB[3], d0[2], d0[3], d1[2], d1[3]));
+  }
+};
+
+template <>
+struct Slab<F_IQ2_S, 8> {
+  __device__ static void run(const uint8_t* st, const uint8_t* pb, const uint8_t* xs, int R, int w, int lane,
+                             float2* gtab, float (&a)[4][4]) {
+    const int g = lane >> 2, tq = lane & 3, p = tq >> 1;
+    const uint8_t* G = reinterpret_cast<const uint8_t*>(gtab) + 8 * (tq & 1);
+    const int rowA = 16 * w + g, rowB = rowA + 8;
+    const uint8_t* rA = st + rowA * 64;
+    const uint8_t* rB = st + rowB * 64;
+    const uint8_t* bA = pb + rowA * 18;
+    const uint8_t* bB = pb + rowB * 18;
+    const bool has_x = g < R;
+    const uint4 qa = lds128v(rA + 16 * p), qb = lds128v(rB + 16 * p);
+    const uint32_t QA[4] = {qa.x, qa.y, qa.z, qa.w}, QB[4] = {qb.x, qb.y, qb.z, qb.w};
+    const uint2 sA = lds64(rA + 32 + 8 * tq), sB = lds64(rB + 32 + 8 * tq);
+    const uint32_t hA = lds16(bA + 10 + 4 * p) | (lds16(bA + 12 + 4 * p) << 16);
+    const uint32_t hB = lds16(bB + 10 + 4 * p) | (lds16(bB + 12 + 4 * p) << 16);
+    const float dA = h2f(lds16(bA)), dB = h2f(lds16(bB));
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      float D[4][4];            // units 4t .. 4t+3 = slots m = 4t .. 4t+3
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int m = 4 * t + k, j = m >> 1, sh = m & 1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) D[k][e] = 0.f;
+        // x already f16 (converted per stage)
+        const uint2 xv = has_x ? lds64(xs + 64 * j + 32 * sh + 8 * tq) : make_uint2(0u, 0u);
+        const uint32_t iA = byte_of(QA, m) | (((hA >> (2 * m)) & 3u) << 8), iB = byte_of(QB, m) | (((hB >> (2 * m)) & 3u) << 8);
+        const uint32_t nA = ((m < 8 ? sA.x : sA.y) >> (4 * (m & 7))) & 15u;
+        const uint32_t nB = ((m < 8 ? sB.x : sB.y) >> (4 * (m & 7))) & 15u;
+        uint32_t a01, a23, b01, b23;
+        grid_slot(G + 16 * iA, nA, a01, a23);
+        grid_slot(G + 16 * iB, nB, b01, b23);
+        mma_f16(D[k], a01, b01, a23, b23, xv.x, xv.y);
+      }
+      const uint32_t cA = lds16(bA + 2 + 2 * t), cB = lds16(bB + 2 + 2 * t);
+      float sA4[4], sB4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        sA4[k] = __fmul_rn(dA, (float)(2 * (int)((cA >> (4 * k)) & 15u) + 1));
+        sB4[k] = __fmul_rn(dB, (float)(2 * (int)((cB >> (4 * k)) & 15u) + 1));
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float* sc = (e < 2) ? sA4 : sB4;
+        tc_add(a, t, e, grid16_comb(sc[0], sc[1], sc[2], sc[3], D[0][e], D[1][e], D[2][e], D[3][e]));
       }
     }
   }

@@ -49,8 +49,13 @@ constexpr int kMaxStages = 16;
 // bytes of plane B per 128-row tile (Q6_K d, NVFP4 block scales, IQ4_XS scale fields
 // and codebook)
 template <int FMT> constexpr int plane_b_tile() {
-  return FMT == F_Q6_K ? kSlabRows * 2 : FMT == F_NVFP4 ? kSlabRows * 16 : FMT == F_IQ4_XS ? kIq4TileB : 0;
+  return FMT == F_Q6_K ? kSlabRows * 2 : FMT == F_NVFP4 ? kSlabRows * 16 : FMT == F_IQ4_XS ? kIq4TileB
+       : FMT == F_IQ3_S ? kSlabRows * 14 : FMT == F_IQ2_S ? kSlabRows * 18 : 0;
 }
+// the grid formats' f16 grid, copied into shared memory once per CTA
+template <int FMT> constexpr int grid_smem_bytes() { return FMT == F_IQ3_S ? 512 * 4 * 2 : FMT == F_IQ2_S ? 1024 * 8 * 2 : 0; }
+// the mbarrier of that copy (a spare slot after the stage barriers)
+constexpr int kGridBarOff = 256;
 constexpr int kMaxSeg = 64;
 // the reducer's gather list (built by the producer warp): kMaxGather entries in the
 // misc area of shared memory, then the mbarrier that publishes them
@@ -157,6 +162,7 @@ struct KParams {
   int x_off;         // offset of the x slices inside a stage
   int b_off;         // offset of plane B (Q6_K d) inside a stage
   int tbl_off;       // offset of the per-warp scale tables
+  int grid_off;      // offset of the grid formats' f16 grid
   int stage_base;    // offset of stage 0
   int mt;            // partial stride (token columns per partial record)
   int cells;         // dense: the number of cells V (> 0); grouped: 0 (every slab is a cell)
@@ -472,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       mbar_init(&empty[i], kConsumerWarps);
     }
     mbar_init(reinterpret_cast<uint64_t*>(smem + kGbarOff), 1);
+    mbar_init(reinterpret_cast<uint64_t*>(smem + kGridBarOff), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -608,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         const Seg& sg = segs[c2.seg];
         uint8_t* st = smem + kp.stage_base + i * kp.stage_bytes;
         const uint8_t* plane =
-            a.packed + kHeaderBytes + (sg.expert + c2.pass * Eh) * L.expert_bytes + c2.g * L.group_bytes;
+            a.packed + L.base + (sg.expert + c2.pass * Eh) * L.expert_bytes + c2.g * L.group_bytes;
         const int kv = (kMayBeRagged && c2.g == G - 1) ? kv_last : kSlabK;
         const int R = sg.R < MT ? sg.R : MT;
         mbar_expect_tx(&full[i], abytes + bbytes + (uint32_t)(kv * 2) * (uint32_t)R);
@@ -626,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       const Seg& sg = segs[cur.seg];
       uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
       const uint8_t* plane =
-          a.packed + kHeaderBytes + (sg.expert + cur.pass * Eh) * L.expert_bytes + cur.g * L.group_bytes;
+          a.packed + L.base + (sg.expert + cur.pass * Eh) * L.expert_bytes + cur.g * L.group_bytes;
       const int kv = (kMayBeRagged && cur.g == G - 1) ? kv_last : kSlabK;
       const uint32_t xbytes = (uint32_t)(kv * 2);
       const int R = sg.R < MT ? sg.R : MT;
@@ -674,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         const Seg& sg = segs[c2.seg];
         uint8_t* st = smem + kp.stage_base + i * kp.stage_bytes;
         const uint8_t* plane =
-            a.packed + kHeaderBytes + (sg.expert + c2.pass * Eh) * L.expert_bytes + c2.g * L.group_bytes;
+            a.packed + L.base + (sg.expert + c2.pass * Eh) * L.expert_bytes + c2.g * L.group_bytes;
         const int kv = (kMayBeRagged && c2.g == G - 1) ? kv_last : kSlabK;
         const int R = sg.R < MT ? sg.R : MT;
         const uint32_t xtx = (MT == 1) ? (uint32_t)(kv * 2) * (uint32_t)R : 0u;
@@ -696,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       const Seg& sg = segs[cur.seg];
       uint8_t* st = smem + kp.stage_base + stage * kp.stage_bytes;
       const uint8_t* plane =
-          a.packed + kHeaderBytes + (sg.expert + cur.pass * Eh) * L.expert_bytes + cur.g * L.group_bytes;
+          a.packed + L.base + (sg.expert + cur.pass * Eh) * L.expert_bytes + cur.g * L.group_bytes;
       const int kv = (kMayBeRagged && cur.g == G - 1) ? kv_last : kSlabK;
       const uint32_t xbytes = (uint32_t)(kv * 2);
       const int R = sg.R < MT ? sg.R : MT;
@@ -740,11 +747,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
 
   if (warp == 0) {
     // ---------------------------- producer --------------------------------
+    // the grid formats: the f16 grid (one table for the call) lands once, before the
+    // first slab is decoded; the producer waits for it before it leaves
+    const bool grid_copy = is_grid_fmt(FMT) && !misc[0];
+    if (grid_copy && lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // after the set-up's plain stores
+      uint64_t* gb = reinterpret_cast<uint64_t*>(smem + kGridBarOff);
+      mbar_expect_tx(gb, (uint32_t)grid_smem_bytes<FMT>());
+      bulk_g2s(smem + kp.grid_off, a.packed + kHeaderBytes, (uint32_t)grid_smem_bytes<FMT>(), gb);
+    }
     if constexpr (MT == 1) {
       if (lane == 0) produce1();
     } else {
       produce8();
     }
+    if (grid_copy && lane == 0) (void)mbar_wait(reinterpret_cast<uint64_t*>(smem + kGridBarOff), 0u, a.status);
     // the gather list of the CTA's last unit: built once here, where the warp has time,
     // instead of by every consumer warp at the end
     __syncwarp();
@@ -767,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   // the pieces that later CTAs published, in order; every other CTA publishes each
   // piece of the unit in the workspace slot (CTA, piece ordinal).
   const int w = warp - 1;               // this warp owns rows 16w .. 16w+15 of a slab
-  constexpr bool kConvX = (MT > 1) && (FMT == F_NVFP4 || FMT == F_FP8 || FMT == F_IQ4_XS);
+  constexpr bool kConvX = (MT > 1) && (FMT == F_NVFP4 || FMT == F_FP8 || FMT >= F_IQ4_XS);
   const int g = lane >> 2, tq = lane & 3;
   float2* tbl = tbls + w * (16 * kTblStride);
   const int rA = 16 * w + g, rB = rA + 8;
@@ -784,6 +801,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   uint32_t fphase = 0;                   // parity of the full barrier for this stage round
   bool aborted = false;
   int cell_ord = 0;                      // grouped: ordinal of the current cell in the range
+  if constexpr (is_grid_fmt(FMT)) {
+    // the grid formats decode from the f16 grid in shared memory (passed to the
+    // decoders in the place of the scale tables, which they do not use)
+    tbl = reinterpret_cast<float2*>(smem + kp.grid_off);
+    if (!misc[0] && !mbar_wait(reinterpret_cast<uint64_t*>(smem + kGridBarOff), 0u, a.status)) {
+      misc[0] = 1;
+      aborted = true;
+    }
+  }
   for (int s = s0; s < s1;) {
     const Seg& sg = segs[seg];
     const int R = sg.R < MT ? sg.R : MT;
@@ -982,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
       }
     }
     if (reducer && !aborted) {
-      const uint8_t* extras = a.packed + kHeaderBytes + sg.expert * L.expert_bytes + L.k_groups * L.group_bytes;
+      const uint8_t* extras = a.packed + L.base + sg.expert * L.expert_bytes + L.k_groups * L.group_bytes;
       const uint8_t* extras_u = extras + (int64_t)Eh * L.expert_bytes;     // SW: the up expert's
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -1084,7 +1110,10 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   kp.tbl_off = 512 + kMaxSeg * (int)sizeof(Seg);
   // the per-warp scale tables serve the token-column (M > 1) decoders only
   const int tbl_bytes = (MT > 1) ? kConsumerWarps * 16 * kTblStride * (int)sizeof(float2) : 0;
-  kp.stage_base = (int)align_up(kp.tbl_off + tbl_bytes, 1024);
+  // the grid lies past the segment sort's scratch (512 B at tbl_off, written before
+  // the grid copy lands), whether or not scale tables follow
+  kp.grid_off = (int)align_up(kp.tbl_off + (tbl_bytes > 512 ? tbl_bytes : 512), 128);
+  kp.stage_base = (int)align_up(kp.grid_off + grid_smem_bytes<FMT>(), 1024);
   const int abytes = kSlabRows * a.L.rec;
   kp.b_off = (int)align_up(abytes, 128);
   const int bbytes = plane_b_tile<FMT>();
@@ -1166,6 +1195,8 @@ cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant) {
     case F_NVFP4: return launch_fmt<F_NVFP4>(a, s, variant);
     case F_FP8: return launch_fmt<F_FP8>(a, s, variant);
     case F_IQ4_XS: return launch_fmt<F_IQ4_XS>(a, s, variant);
+    case F_IQ3_S: return launch_fmt<F_IQ3_S>(a, s, variant);
+    case F_IQ2_S: return launch_fmt<F_IQ2_S>(a, s, variant);
     default: return cudaErrorInvalidValue;
   }
 }

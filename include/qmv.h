@@ -70,10 +70,15 @@ typedef enum {
     QMV_NVFP4 = 4,
     QMV_FP8_ROW = 5,
     QMV_Q5_K = 6,
-    QMV_IQ4_XS = 7         /* codebook format: 136 B / 256 values, a per-matrix 16-entry
+    QMV_IQ4_XS = 7,        /* codebook format: 136 B / 256 values, a per-matrix 16-entry
                               int8 codebook at the end of each matrix's canonical stream
                               ("A 320B MoE on a free Kaggle TPU", "What '3-bit' costs,
                               measured") */
+    QMV_IQ3_S = 8,         /* grid formats (same article and section; "The kernel, and
+                              why 64 tok/s is not a bandwidth number"): 110 / 82 B per 256
+                              values; groups of 4 / 8 weights are entries of the format's */
+    QMV_IQ2_S = 9          /* grid (512 x 4 / 1024 x 8 uint8 magnitudes, at the front of a
+                              tower's canonical stream) with one sign bit per weight */
 } qmv_fmt;
 
 typedef enum {
@@ -103,7 +108,8 @@ enum {
 /* Largest decode batch served by qmv_gemv / qmv_grouped (M rows of x). */
 #define QMV_MAX_M 8
 
-/* Bytes of the canonical stream of an E-expert tower of [N, K] matrices.
+/* Bytes of the canonical stream of an E-expert tower of [N, K] matrices (IQ3_S and
+ * IQ2_S: the grid once, then the blocks of all E*N rows).
  * Returns 0 for an unknown format or a K that is not a multiple of the block. */
 size_t qmv_canon_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
 
@@ -113,9 +119,10 @@ size_t qmv_canon_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
  * is aligned; rows are padded to a multiple of 128 with zero blocks. The slab
  * bytes are the canonical bytes, only reordered (the per-value cost is
  * unchanged). K must be a multiple of 32 (Q8_0, NVFP4, FP8_ROW) or 256 (Q4_K,
- * Q5_K, Q6_K, IQ4_XS). Returns 0 if unsupported. IQ4_XS repeats its 16-byte
- * codebook after the scale fields of every 128-row tile of every k-group (16 B per
- * slab, so that each slab copy brings it along). */
+ * Q5_K, Q6_K and the codebook formats). Returns 0 if unsupported. IQ4_XS repeats its
+ * 16-byte codebook after the scale fields of every 128-row tile of every k-group
+ * (16 B per slab, so that each slab copy brings it along); IQ3_S and IQ2_S store
+ * their grid once, as f16 values, after the header (4 / 16 KiB). */
 size_t qmv_pack_size(qmv_fmt fmt, int64_t N, int64_t K, int64_t E);
 
 /* Repack canonical bytes into the device layout. Defined by: the stacked keep-quant
@@ -144,16 +151,20 @@ qmv_status qmv_pack(qmv_fmt fmt, const void* canon, int64_t N, int64_t K, int64_
 qmv_status qmv_quantize(qmv_fmt fmt, const float* W, int64_t rows, int64_t K,
                         float tensor_scale, void* canon, cudaStream_t stream);
 
-/* The encoder of the codebook formats (IQ4_XS): as qmv_quantize, with the matrix's
- * codebook (host pointer to 16 int8 values, read during the call) in place of a
- * rounding constant ("A 320B MoE on a free Kaggle TPU", "What '3-bit' costs,
- * measured": a weight is an entry of the format's codebook). Per 32-value sub-block:
- * the scale that maps its element of largest magnitude onto the entry of largest
- * magnitude, 6 bits under an fp16 d; each element takes the nearest entry. canon:
- * device, qmv_canon_size(fmt, rows, K, 1) bytes (the blocks, then the codebook).
- * Other formats: QMV_EUNSUPPORTED. Not on the per-token path. */
+/* The encoder of the codebook formats: as qmv_quantize, with the format's table (a
+ * host pointer, read during the call) in place of a rounding constant ("A 320B MoE
+ * on a free Kaggle TPU", "What '3-bit' costs, measured": a weight is an entry of
+ * the format's codebook). IQ4_XS: the matrix's 16 int8 values; per 32-value
+ * sub-block the scale that maps its element of largest magnitude onto the entry of
+ * largest magnitude, 6 bits under an fp16 d; each element takes the nearest entry;
+ * canon = the blocks, then the codebook. IQ3_S / IQ2_S: the grid, 512 x 4 / 1024 x 8
+ * uint8 magnitudes; per 32 / 16 values an odd 4-bit scale (2 sc + 1) under fp16 d
+ * sized by the grid's largest magnitude; per group the signs of its weights and
+ * the nearest entry in squared error; canon = the grid, then the blocks (encode a
+ * whole tower as one [E*N, K] matrix). canon: device, qmv_canon_size(fmt, rows, K, 1)
+ * bytes. Other formats: QMV_EUNSUPPORTED. Not on the per-token path. */
 qmv_status qmv_quantize_codebook(qmv_fmt fmt, const float* W, int64_t rows, int64_t K,
-                                 const int8_t* codebook, void* canon, cudaStream_t stream);
+                                 const void* codebook, void* canon, cudaStream_t stream);
 
 /* BlockToFloat on the device layout: W_out[r][k] (fp32, device) for rows
  * row0 .. row0+rows-1 of the stacked tower (row = e*N + n). Defined by: the CPU

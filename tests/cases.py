@@ -35,8 +35,24 @@ def codebook(fmt, seed, e):
     return synth.codebook(seed + 7919 * e) if fmt == "iq4_xs" else None
 
 
+GRID_FORMATS = {"iq3_s": (512, 4, 8), "iq2_s": (1024, 8, 4)}     # entries, width, levels
+
+
+def grid(fmt, seed):
+    """The grid of a seeded IQ3_S / IQ2_S tower (one table for all its experts)."""
+    ne, gw, lv = GRID_FORMATS[fmt]
+    return synth.grid(seed, ne, gw, lv)
+
+
 def _encode(fmt, W, seed, e):
     return oracle.encode(fmt, W, tensor_scale(fmt), codebook=codebook(fmt, seed, e))
+
+
+def _encode_tower_rows(fmt, W, seed):
+    """K-quants: rows in any grouping; grid formats: the tower's grid, then the rows."""
+    if fmt in GRID_FORMATS:
+        return oracle.encode(fmt, W, codebook=grid(fmt, seed))
+    return oracle.encode(fmt, W, tensor_scale(fmt))
 
 
 def norm_err(y, ref, den) -> float:
@@ -59,7 +75,7 @@ def host_matrix(fmt, seed, N, K, E=1):
     if fmt in PER_MATRIX:
         canon = np.concatenate([_encode(fmt, W[e * N:(e + 1) * N], seed, e) for e in range(E)])
     else:
-        canon = oracle.encode(fmt, W, tensor_scale(fmt))
+        canon = _encode_tower_rows(fmt, W, seed)
     return W, canon
 
 
@@ -89,7 +105,7 @@ def host_rows_dequant(fmt, seed, rows, N, K):
             c = oracle.encode(fmt, W[i:i + 1], tensor_scale(fmt))
             out[i] = oracle.block_to_float(fmt, c, 1, K)[0]
         return out
-    c = oracle.encode(fmt, W, tensor_scale(fmt))
+    c = _encode_tower_rows(fmt, W, seed)
     return oracle.block_to_float(fmt, c, W.shape[0], K)
 
 
@@ -108,6 +124,9 @@ def device_matrix(q, fmt, seed, N, K, E=1, dev="cuda"):
             elif fmt == "iq4_xs":
                 # the blocks of this chunk, without the codebook the encoder appends
                 parts.append(q.qmv_quantize_codebook(fmt, W, codebook(fmt, seed, e))[:n * (K // 256) * 136])
+            elif fmt in GRID_FORMATS:
+                # the blocks of this chunk, without the grid the encoder puts first
+                parts.append(q.qmv_quantize_codebook(fmt, W, grid(fmt, seed))[oracle.grid_bytes(fmt):])
             else:
                 parts.append(q.qmv_quantize(fmt, W))
         if fmt == "iq4_xs":
@@ -121,6 +140,8 @@ def device_matrix(q, fmt, seed, N, K, E=1, dev="cuda"):
         else:
             canon_parts.append(torch.cat(parts))
         del parts
+    if fmt in GRID_FORMATS:
+        canon_parts.insert(0, torch.from_numpy(grid(fmt, seed).reshape(-1).copy()).to(dev))
     canon = torch.cat(canon_parts)
     del canon_parts
     packed = q.qmv_pack(fmt, canon, N, K, E)

@@ -47,16 +47,18 @@ def test_binding_exposes_every_declared_symbol(lib):
 
 def test_sizes_match_oracle(lib):
     import block_quantized_weight_fly_gb300 as q
-    for fmt in ("q8_0", "q4_k", "q5_k", "q6_k", "nvfp4", "fp8_row", "iq4_xs"):
+    for fmt in ("q8_0", "q4_k", "q5_k", "q6_k", "nvfp4", "fp8_row", "iq4_xs", "iq3_s", "iq2_s"):
         for N, K in ((512, 1024), (17408, 5120), (248320, 5120), (300, 768)):
             assert q.qmv_canon_size(fmt, N, K) == oracle.canon_bytes(fmt, N, K)
     # the packed layout moves the canonical bytes; only row/K padding and alignment add
     for fmt, per in (("q8_0", 34 / 32), ("q4_k", 144 / 256), ("q5_k", 176 / 256), ("q6_k", 210 / 256),
-                     ("nvfp4", 18 / 32), ("fp8_row", 1.0), ("iq4_xs", 136 / 256)):
+                     ("nvfp4", 18 / 32), ("fp8_row", 1.0), ("iq4_xs", 136 / 256), ("iq3_s", 110 / 256),
+                     ("iq2_s", 82 / 256)):
         N, K = 17408, 5120
         body = q.qmv_pack_size(fmt, N, K) - 256
-        # IQ4_XS adds its 16-byte codebook once per 128 x 256 slab
-        extra = 16 * (N // 128) * (K // 256) if fmt == "iq4_xs" else 0
+        # IQ4_XS adds its 16-byte codebook once per 128 x 256 slab; IQ3_S / IQ2_S their
+        # f16 grid once
+        extra = {"iq4_xs": 16 * (N // 128) * (K // 256), "iq3_s": 4096, "iq2_s": 16384}.get(fmt, 0)
         assert N * K * per + extra <= body <= N * K * per + extra + 4 * N + 512
     assert q.qmv_pack_size("q4_k", 100, 100) == 0          # K not a multiple of 256
     assert q.qmv_pack_size("q5_k", 100, 1000) == 0
@@ -72,8 +74,8 @@ def test_host_validation_without_device(lib):
     assert gemv(2, None, one, one, 1, 128, 256, one, 1 << 20, None) == 1
     assert gemv(2, one, one, one, 0, 128, 256, one, 1 << 20, None) == 1
     assert gemv(2, one, one, one, 9, 128, 256, one, 1 << 20, None) == 1
-    assert gemv(9, one, one, one, 1, 128, 256, one, 1 << 20, None) == 1
-    assert gemv(8, one, one, one, 1, 128, 256, one, 1 << 20, None) == 1
+    assert gemv(99, one, one, one, 1, 128, 256, one, 1 << 20, None) == 1          # not a format
+    assert gemv(0, one, one, one, 1, 128, 256, one, 1 << 20, None) == 1
     assert gemv(7, one, one, one, 1, 128, 100, one, 1 << 20, None) == 3             # IQ4_XS: K % 256
     assert gemv(6, one, one, one, 1, 128, 100, one, 1 << 20, None) == 3
     assert gemv(2, one, one, one, 1, 128, 100, one, 1 << 20, None) == 3
@@ -100,8 +102,8 @@ def test_host_validation_new_entries(lib):
     kq = q._kquant               # fmt, W, x, y, M, N, K, ws, ws_bytes, stream
     assert kq(2, None, one, one, 512, 128, 256, one, 1 << 20, None) == 1
     assert kq(2, one, one, one, 0, 128, 256, one, 1 << 20, None) == 1
-    assert kq(8, one, one, one, 512, 128, 256, one, 1 << 20, None) == 1              # not a format
-    for fmt in (1, 3, 4, 5, 7):                                                      # Q8_0, Q6_K, NVFP4, FP8, IQ4_XS
+    assert kq(99, one, one, one, 512, 128, 256, one, 1 << 20, None) == 1             # not a format
+    for fmt in (1, 3, 4, 5, 7, 8, 9):                                                # Q8_0, Q6_K, NVFP4, FP8, IQ
         assert kq(fmt, one, one, one, 512, 128, 256, one, 1 << 20, None) == 3
     assert kq(2, one, one, one, 512, 128, 300, one, 1 << 20, None) == 3              # K % 256
     assert kq(6, one, one, one, 512, 128, 300, one, 1 << 20, None) == 3
@@ -143,7 +145,7 @@ def test_host_validation_remaining_entries(lib):
     pk = q._pack                 # fmt, canon, N, K, E, dst, stream
     assert pk(2, None, 128, 256, 1, one, None) == 1
     assert pk(2, one, 128, 256, 0, one, None) == 1                               # E = 0
-    assert pk(9, one, 128, 256, 1, one, None) == 1
+    assert pk(99, one, 128, 256, 1, one, None) == 1
     assert pk(2, one, 128, 100, 1, one, None) == 3
     assert pk(2, one, 128, 256, 1, P(257), None) == 2
     dq = q._dequant              # fmt, packed, N, K, E, row0, rows, out, stream
@@ -152,14 +154,15 @@ def test_host_validation_remaining_entries(lib):
     assert dq(2, one, 128, 256, 1, -1, 10, one, None) == 1
     qz = q._quantize             # fmt, W, rows, K, tensor_scale, canon, stream
     assert qz(2, None, 128, 256, 0.0, one, None) == 1
-    assert qz(9, one, 128, 256, 0.0, one, None) == 1
+    assert qz(99, one, 128, 256, 0.0, one, None) == 1
     assert qz(2, one, 128, 100, 0.0, one, None) == 3
     assert qz(7, one, 128, 256, 0.0, one, None) == 3                             # IQ4_XS needs a codebook
+    assert qz(9, one, 128, 256, 0.0, one, None) == 3                             # IQ2_S needs its grid
     qc = q._quantize_cb          # fmt, W, rows, K, codebook, canon, stream
     assert qc(7, None, 128, 256, one, one, None) == 1
     assert qc(7, one, 128, 256, None, one, None) == 1                            # no codebook
     assert qc(2, one, 128, 256, one, one, None) == 3                             # not a codebook format
-    assert qc(9, one, 128, 256, one, one, None) == 1
+    assert qc(99, one, 128, 256, one, one, None) == 1
     assert qc(7, one, 128, 100, one, one, None) == 3                             # K % 256
     assert qc(7, P(258), 128, 256, one, one, None) == 2
     # workspace sizes of impossible requests are 0

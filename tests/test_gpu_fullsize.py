@@ -99,18 +99,23 @@ def test_tower_full_size_sampled(q, mat, M):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("fmt,mat", [("iq4_xs", "down"), ("iq3_s", "down"), ("iq2_s", "gate")])
 @pytest.mark.parametrize("M", [1, 8])
-def test_iq4_xs_tower_full_size_sampled(q, M):
-    """The 288-expert down-projection tower [4096, 2048] in IQ4_XS, each expert with
-    its own codebook (the down matrices the pages list in IQ4_XS, "A 320B MoE on a
-    free Kaggle TPU", table of formats by layer), top-8, one x row per pair; sampled
-    rows of every routed expert of the first tokens against the oracle."""
-    fmt, E, topk, N, K, seed = "iq4_xs", 288, 8, 4096, 2048, 740
+def test_codebook_tower_full_size_sampled(q, fmt, mat, M):
+    """The 288-expert towers in the codebook formats the pages list for them ("A 320B
+    MoE on a free Kaggle TPU", table of formats by layer): IQ2_S gate [2048, 4096]
+    (x shared per token), IQ3_S and IQ4_XS down [4096, 2048] (one x row per pair; IQ4_XS
+    with a codebook per expert, the grid formats with one grid per tower), top-8;
+    sampled rows of every routed expert of the first tokens against the oracle."""
+    E, topk = 288, 8
+    N, K = (2048, 4096) if mat == "gate" else (4096, 2048)
+    x_per_pair = mat == "down"
+    seed = 740 + {"iq4_xs": 0, "iq3_s": 1, "iq2_s": 2}[fmt]
     tower = device_matrix(q, fmt, seed, N, K, E)
     ids = synth.expert_ids(seed + M, M, topk, E)
-    x = synth.activations(seed + 10 * M, M * topk, K)
+    x = synth.activations(seed + 10 * M, M * topk if x_per_pair else M, K)
     ws = q.workspace(q.QMV_ENTRY_GROUPED, fmt, M, N, K, E, topk)
-    y = q.qmv_grouped(fmt, tower, torch.from_numpy(ids).cuda(), x.cuda(), N, K, E, ws, x_per_pair=True)
+    y = q.qmv_grouped(fmt, tower, torch.from_numpy(ids).cuda(), x.cuda(), N, K, E, ws, x_per_pair=x_per_pair)
     assert q.qmv_last_route() == q.FORMATS[fmt] * 100 + 3
     y = y.cpu().numpy()
     assert q.qmv_device_status() == 0
@@ -121,7 +126,8 @@ def test_iq4_xs_tower_full_size_sampled(q, M):
         for j in range(topk):
             e = int(ids[t, j])
             D = host_rows_dequant(fmt, seed, e * N + rows, N, K)
-            ref, den = oracle.gemv_f64(D, xb[t * topk + j][None, :])
+            xr = xb[t * topk + j] if x_per_pair else xb[t]
+            ref, den = oracle.gemv_f64(D, xr[None, :])
             err = norm_err(y[t, j, rows][None, :], ref, den)
             assert err <= TOL, (t, j, e, err)
     del tower

@@ -34,6 +34,8 @@ DENSE = [
     ("q8_0", 512, 1024),                 # the tiny configuration
     ("q8_0", QWEN_HIDDEN, QWEN_HIDDEN),
     ("iq4_xs", 4096, 2048),              # a 288-expert model's down projection, one expert
+    ("iq3_s", 4096, 2048),
+    ("iq2_s", 2048, 4096),               # its gate / up
 ]
 
 
@@ -133,7 +135,7 @@ def test_tower_rows_equal_single_token(q, mat):
         _grouped_rows_equal(q, call, ids, x, x_per_pair, topk)
 
 
-@pytest.mark.parametrize("fmt", ["q8_0", "q5_k", "q6_k", "nvfp4", "fp8_row", "iq4_xs"])
+@pytest.mark.parametrize("fmt", ["q8_0", "q5_k", "q6_k", "nvfp4", "fp8_row", "iq4_xs", "iq3_s", "iq2_s"])
 def test_grouped_rows_equal_single_token_formats(q, fmt):
     E, topk, N, K, M = 24, 8, 640, 2048, 8
     tower = device_matrix(q, fmt, 53, N, K, E)

@@ -14,11 +14,11 @@ import torch
 
 import oracle
 import synth
-from cases import (TOL, host_dequant, host_matrix, norm_err, tensor_scale)
+from cases import (TOL, grid, host_dequant, host_matrix, norm_err, tensor_scale)
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["q8_0", "q4_k", "q5_k", "q6_k", "nvfp4", "fp8_row", "iq4_xs"]
+FMTS = ["q8_0", "q4_k", "q5_k", "q6_k", "nvfp4", "fp8_row", "iq4_xs", "iq3_s", "iq2_s"]
 
 
 @pytest.fixture(scope="module")
@@ -35,7 +35,7 @@ def _sms():
 
 def _kq(fmt):
     """formats whose K granule is 256"""
-    return fmt in ("q4_k", "q5_k", "q6_k", "iq4_xs")
+    return fmt in ("q4_k", "q5_k", "q6_k", "iq4_xs", "iq3_s", "iq2_s")
 
 
 # ---------------------------------------------------------------------------
@@ -50,8 +50,8 @@ def test_quantize_bit_exact(q, fmt):
     W[2, :256] = 0.0123
     W[3] *= 1e-4
     W[4, 5] = 0.5                                      # an outlier
-    if fmt == "iq4_xs":
-        cb = synth.codebook(3)
+    if fmt in ("iq4_xs", "iq3_s", "iq2_s"):
+        cb = synth.codebook(3) if fmt == "iq4_xs" else grid(fmt, 3)
         want = oracle.encode(fmt, W, codebook=cb)
         got = q.qmv_quantize_codebook(fmt, torch.from_numpy(W).cuda(), cb).cpu().numpy()
     else:
@@ -128,7 +128,7 @@ def test_gemv_tiny_config_q8_0(q):
     assert norm_err(y, ref, den) <= TOL
 
 
-@pytest.mark.parametrize("fmt", ["q4_k", "nvfp4", "iq4_xs"])
+@pytest.mark.parametrize("fmt", ["q4_k", "nvfp4", "iq4_xs", "iq2_s"])
 def test_gemv_deterministic_and_guarded(q, fmt):
     N, K, M = 1000, 2048, 4
     W, canon = host_matrix(fmt, 13, N, K)

@@ -16,7 +16,7 @@ from cases import TOL, host_dequant, host_matrix
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["q4_k", "q5_k", "q6_k", "q8_0", "nvfp4", "fp8_row", "iq4_xs"]
+FMTS = ["q4_k", "q5_k", "q6_k", "q8_0", "nvfp4", "fp8_row", "iq4_xs", "iq3_s", "iq2_s"]
 
 
 @pytest.fixture(scope="module")
@@ -36,7 +36,7 @@ def swiglu_bound(g, dg, u, du, h):
 @pytest.mark.parametrize("N,K", [(300, 512), (1000, 2048), (129, 768), (2000, 1280)])
 @pytest.mark.parametrize("M", [1, 3, 8])
 def test_swiglu_parity(q, fmt, N, K, M):
-    if fmt in ("q4_k", "q5_k", "q6_k", "iq4_xs") and K % 256:
+    if fmt in ("q4_k", "q5_k", "q6_k", "iq4_xs", "iq3_s", "iq2_s") and K % 256:
         pytest.skip("K-quants and IQ4_XS need K % 256 == 0")
     W, canon = host_matrix(fmt, 61, N, K, 2)                 # gate = expert 0, up = expert 1
     D = host_dequant(fmt, canon, N, K, 2)
