@@ -94,6 +94,9 @@ WORKLOADS = {
                              mats=[("up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
                              desc="Q5_K prefill, M=512: tcgen05 kind::f16 GEMM over exactly decoded Q5_K weights, "
                                   "[17408,5120] + [5120,17408]"),
+    "q6k_prefill_m512": dict(fmt="q6_k", M=512, kquant=True, mats=[("attn_qkv", 10240, QWEN_HIDDEN)],
+                             desc="Q6_K prefill, M=512: tcgen05 kind::f16 GEMM over exactly decoded Q6_K weights "
+                                  "(scale split into two exact f16 terms), fused attn_qkv [10240,5120]"),
     "tower_m1": dict(fmt="q4_k", M=1, tower=True, E=288, topk=8,
                      mats=[("gate", 2048, 4096), ("up", 2048, 4096), ("down", 4096, 2048)],
                      desc="grouped Q4_K tower, 288 experts x (gate,up [2048,4096], down [4096,2048]), top-8, M=1"),
@@ -135,7 +138,7 @@ DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, 
                  "tower_m4": 10000, "tower_m8": 5000, "nvfp4_w4a4_m512": 2000,
                  "q4k_mlp_fused_m1": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000,
                  "tower_fused_m1": 20000, "tower_fused_m8": 5000, "q4k_prefill_m512": 2000,
-                 "q5k_prefill_m512": 2000, "iq4xs_tower_down_m1": 20000, "iq4xs_tower_down_m8": 5000,
+                 "q5k_prefill_m512": 2000, "q6k_prefill_m512": 2000, "iq4xs_tower_down_m1": 20000, "iq4xs_tower_down_m8": 5000,
                  "iq4xs_mlp_m1": 20000, "iq2s_tower_gateup_m1": 20000, "iq3s_tower_down_m1": 20000}
 
 METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"

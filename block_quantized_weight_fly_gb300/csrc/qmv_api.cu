@@ -135,7 +135,7 @@ size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, i
         .ws_bytes;
   }
   if (entry == QMV_ENTRY_KQUANT) {
-    if ((fmt != QMV_Q4_K && fmt != QMV_Q5_K) || K % 256) return 0;
+    if ((fmt != QMV_Q4_K && fmt != QMV_Q5_K && fmt != QMV_Q6_K) || K % 256) return 0;
     return (size_t)kq_workspace_bytes(align_up(M, 128), K, sms);
   }
   if (entry == QMV_ENTRY_W4A4) {
@@ -274,7 +274,7 @@ qmv_status qmv_grouped_swiglu(qmv_fmt fmt, const void* tower, const int32_t* exp
 qmv_status qmv_gemm_kquant(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y, int M, int64_t N,
                            int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!valid_fmt(fmt) || !packed_W || !x || !y || !ws || M < 1 || N <= 0 || K <= 0) return QMV_EINVAL;
-  if (fmt != QMV_Q4_K && fmt != QMV_Q5_K) return QMV_EUNSUPPORTED;
+  if (fmt != QMV_Q4_K && fmt != QMV_Q5_K && fmt != QMV_Q6_K) return QMV_EUNSUPPORTED;
   Layout L;
   if (!make_layout((int)fmt, N, K, 1, &L)) return QMV_EUNSUPPORTED;
   if (!aligned(packed_W, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;

@@ -13,7 +13,11 @@
 //   D2[n][m] = sum_j m_j[n] (xs_hi[m][j] + xs_lo[m][j])      (f16 x f16, fp32 accumulator)
 //   y[m][n] += (d[n] 2^14) D1[n][m] - dmin[n] D2[n][m]       (fp32, per superblock)
 // where xs = the fp32 sum of x over the sub-block, split into two f16 (hi + lo, 2^-22
-// relative). sc_j q <= 63 * 15 = 945 (Q5_K: 63 * 31 = 1953) and m_j <= 63 are exact in
+// relative). Q6_K (w = d sc_u (q - 32) per 16-value unit u, sc_u int8) has no min
+// term; sc_u (q - 32) needs up to 12 significant bits, one more than f16 holds, so the
+// scale is split, sc_u = 16 sh_u + sl_u (sh_u = sc_u >> 4, sl_u = sc_u & 15), and each K
+// step takes two MMAs into D1: A = (q - 32) 16 sh_u (|.| <= 4096, 9 significant bits)
+// and A = (q - 32) sl_u (|.| <= 480); both exact, y[m][n] += d[n] D1[n][m]. sc_j q <= 63 * 15 = 945 (Q5_K: 63 * 31 = 1953) and m_j <= 63 are exact in
 // f16; the decoder makes sc_j q 2^-14 with one mask (the field lands in f16's subnormal
 // range: q 2^-24, or q 2^-20 for a Q4_K high nibble) and one f16 multiply by sc_j 2^10
 // (2^6), so every product is exact and only the fp32 accumulations round. x is taken in f16 (exact for bf16
@@ -189,6 +193,32 @@ __device__ __forceinline__ uint4 kq_decode_word(const uint4 (&cur)[NV], int t, i
   return out;
 }
 
+// Q6_K: the f16 values q - 32 of elements (8g .. 8g+7) of the 64-value K step s of a
+// packed record (ql word t of chunk j at 32t + 4j, qh word h at 128 + 32h + 4j; see
+// qmv_layout.cuh), as four f16 pairs
+template <int NV>
+__device__ __forceinline__ void q6k_step_pairs(const uint4 (&cur)[NV], int s, int g, uint32_t* v) {
+  const int j = 2 * s + (g >> 2);           // chunk
+  const int half = (g & 3) >> 1;            // 16-value half of the chunk
+  const int w0 = 2 * (g & 1);               // the two quads of 4 elements: w0, w0 + 1
+  const uint32_t qh = rec_word(cur, 128 + 32 * (w0 >> 1) + 4 * j);
+#pragma unroll
+  for (int qd = 0; qd < 2; ++qd) {
+    const int w = w0 + qd;
+    const uint32_t ql = rec_word(cur, 32 * w + 4 * j);
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      const int k = 2 * half + pr;          // pair index within the words
+      const uint32_t lo = (ql >> (4 * k)) & 0x000F000Fu;
+      const uint32_t hi = (qh >> (8 * (w & 1) + 2 * k)) & 0x00030003u;
+      const uint32_t p = lo | (hi << 4) | 0x64006400u;                 // {1024 + q, 1024 + q'}
+      uint32_t r;
+      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(0x64206420u));   // - 1056: {q - 32, q' - 32}
+      v[2 * qd + pr] = r;
+    }
+  }
+}
+
 struct KqParams {
   Layout L;
   const uint8_t* packed;
@@ -210,7 +240,9 @@ __device__ __forceinline__ int range_start(int i, int units, int P) {
 
 template <int FMT>
 __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
-  constexpr int kRec = (FMT == F_Q5_K) ? 176 : 144;     // record bytes per row and superblock
+  constexpr bool kQ6 = FMT == F_Q6_K;
+  constexpr int kRec = (FMT == F_Q5_K) ? 176 : kQ6 ? 208 : 144;   // record bytes per row and superblock
+  constexpr int kAPerStep = kQ6 ? 2 : 1;                    // decoded weight tiles per K step
   constexpr int kRecV = kRec / 16;
   extern __shared__ __align__(1024) uint8_t smem[];
   const Layout& L = p.L;
@@ -326,17 +358,23 @@ __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
         bool ok = true;
         if (i >= 2) ok = wait_bounded(&acc_free[b], (uint32_t)((i / 2 - 1) & 1));
         for (int s = 0; s < 4 && ok; ++s) {
-          ok = wait_bounded(&x_full[xs], xph) && wait_bounded(&a_full[as], aph);
-          if (!ok || *abort_flag) break;
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t xa = su32(xring + xs * kStepBytes), aa = su32(aring + as * kStepBytes);
+          ok = wait_bounded(&x_full[xs], xph);
+          const uint32_t xa = su32(xring + xs * kStepBytes);
+          for (int h = 0; h < kAPerStep && ok; ++h) {
+            ok = wait_bounded(&a_full[as], aph);
+            if (!ok || *abort_flag) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t aa = su32(aring + as * kStepBytes);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_f16(d1, sdesc(aa + 256 * k, 128, 1024), sdesc(xa + 256 * k, 128, 1024), idesc, (s | k) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              mma_f16(d1, sdesc(aa + 256 * k, 128, 1024), sdesc(xa + 256 * k, 128, 1024), idesc,
+                      (s | k | h) ? 1u : 0u);
+            commit(&a_empty[as]);
+            if (++as == kASlots) { as = 0; aph ^= 1u; }
+          }
+          if (!ok || *abort_flag) break;
           commit(&x_empty[xs]);
-          commit(&a_empty[as]);
           if (++xs == kXSlots) { xs = 0; xph ^= 1u; }
-          if (++as == kASlots) { as = 0; aph ^= 1u; }
         }
         if (ok) ok = wait_bounded(&sx_full[ss], sph) && wait_bounded(&sd_full[ss], sph);
         if (!ok) {
@@ -346,7 +384,7 @@ __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
         if (*abort_flag) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t sb = su32(sring + ss * kSBytes);
-        mma_f16(d2, sdesc(sb + kMinsOff, 128, 256), sdesc(sb + kSumsOff, 128, 256), idesc, 0u);
+        if (!kQ6) mma_f16(d2, sdesc(sb + kMinsOff, 128, 256), sdesc(sb + kSumsOff, 128, 256), idesc, 0u);
         commit(&s_empty[ss]);
         commit(&acc_full[b]);
         if (++ss == kSSlots) { ss = 0; sph ^= 1u; }
@@ -357,11 +395,14 @@ __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
     // ------------------------------ decoders --------------------------------
     const int r = threadIdx.x - 64;                         // weight row of the tile
     uint4 nxt[kRecV];
+    uint32_t nxt_d = 0u;                                    // Q6_K: the row's fp16 d (plane B)
     auto load_rec = [&](int u) {
       const int kb = u % KB, nt = (u / KB) / p.m_tiles;
-      const uint8_t* rec = p.packed + kHeaderBytes + (int64_t)kb * L.group_bytes + ((int64_t)nt * 128 + r) * kRec;
+      const uint8_t* plane = p.packed + kHeaderBytes + (int64_t)kb * L.group_bytes;
+      const uint8_t* rec = plane + ((int64_t)nt * 128 + r) * kRec;
 #pragma unroll
       for (int v = 0; v < kRecV; ++v) nxt[v] = ldg_nc(rec + 16 * v);
+      if constexpr (kQ6) nxt_d = __ldg(reinterpret_cast<const unsigned short*>(plane + L.plane_a) + (nt * 128 + r));
     };
     if (n > 0 && !bad_header) load_rec(u0);
     int as = 0, ss = 0, ai = 0;
@@ -370,9 +411,10 @@ __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
       uint4 cur[kRecV];
 #pragma unroll
       for (int v = 0; v < kRecV; ++v) cur[v] = nxt[v];
+      const uint32_t cur_d = nxt_d;
       if (i + 1 < n) load_rec(u0 + i + 1);
       const uint32_t hw[4] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w};
-      const float d = h2f(hw[0]), dmin = h2f(hw[0] >> 16);
+      const float d = kQ6 ? h2f(cur_d) : h2f(hw[0]), dmin = kQ6 ? 0.0f : h2f(hw[0] >> 16);
       // mins tile row r and the row scales
       if (i >= kSSlots && !warp_wait(&s_empty[ss], sph ^ 1u, lane)) {
         if (lane == 0) { atomicOr(p.status, kStatTimeout); *abort_flag = 1; }
@@ -380,19 +422,22 @@ __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
       }
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;   // one decision per warp
       {
-        uint32_t mh[4];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const uint32_t m0 = q4k_field(hw[1], hw[2], hw[3], 8 + 2 * jj);
-          const uint32_t m1 = q4k_field(hw[1], hw[2], hw[3], 9 + 2 * jj);
-          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(mh[jj]) : "f"((float)m1), "f"((float)m0));
-        }
         uint8_t* sl = sring + ss * kSBytes;
-        const uint4 mv = make_uint4(mh[0], mh[1], mh[2], mh[3]);
-        const int ro = (r >> 3) * 256 + (r & 7) * 16;
-        *reinterpret_cast<uint4*>(sl + kMinsOff + ro) = mv;          // columns 0..7:  m_0..m_7
-        *reinterpret_cast<uint4*>(sl + kMinsOff + ro + 128) = mv;    // columns 8..15: m_0..m_7
-        *reinterpret_cast<float2*>(sl + kSclOff + 8 * r) = make_float2(d * 16384.0f, dmin);
+        if constexpr (!kQ6) {
+          uint32_t mh[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t m0 = q4k_field(hw[1], hw[2], hw[3], 8 + 2 * jj);
+            const uint32_t m1 = q4k_field(hw[1], hw[2], hw[3], 9 + 2 * jj);
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(mh[jj]) : "f"((float)m1), "f"((float)m0));
+          }
+          const uint4 mv = make_uint4(mh[0], mh[1], mh[2], mh[3]);
+          const int ro = (r >> 3) * 256 + (r & 7) * 16;
+          *reinterpret_cast<uint4*>(sl + kMinsOff + ro) = mv;          // columns 0..7:  m_0..m_7
+          *reinterpret_cast<uint4*>(sl + kMinsOff + ro + 128) = mv;    // columns 8..15: m_0..m_7
+        }
+        // the row scales: Q4_K / Q5_K (d 2^14, dmin); Q6_K (d, 0)
+        *reinterpret_cast<float2*>(sl + kSclOff + 8 * r) = make_float2(kQ6 ? d : d * 16384.0f, dmin);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) arrive(&sd_full[ss]);
@@ -407,21 +452,54 @@ __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
           break;
         }
         if (__shfl_sync(0xffffffffu, *abort_flag, 0)) { stop = true; break; }
-        uint8_t* at = aring + as * kStepBytes + (r >> 3) * 1024 + (r & 7) * 16;
+        if constexpr (kQ6) {
+          // two tiles per K step, slots as and as2: (q - 32) 16 sh_u, then (q - 32) sl_u;
+          // the second slot is waited for here too, so each pair of values is decoded once
+          const int as2 = (as + 1 == kASlots) ? 0 : as + 1;
+          const uint32_t aph2 = (as + 1 == kASlots) ? (aph ^ 1u) : aph;
+          if (ai + 1 >= kASlots && !warp_wait(&a_empty[as2], aph2 ^ 1u, lane)) {
+            if (lane == 0) { atomicOr(p.status, kStatTimeout); *abort_flag = 1; }
+            stop = true;
+            break;
+          }
+          if (__shfl_sync(0xffffffffu, *abort_flag, 0)) { stop = true; break; }
+          uint8_t* at1 = aring + as * kStepBytes + (r >> 3) * 1024 + (r & 7) * 16;
+          uint8_t* at2 = aring + as2 * kStepBytes + (r >> 3) * 1024 + (r & 7) * 16;
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * s + jj;                              // sub-block (32 values)
-          const float sc = (float)q4k_field(hw[1], hw[2], hw[3], j);
-          const uint32_t S = f16x2_dup(sc * 1024.0f), S16 = f16x2_dup(sc * 64.0f);
+          for (int g = 0; g < 8; ++g) {
+            uint32_t v[4];
+            q6k_step_pairs(cur, s, g, v);
+            const int u = 4 * s + (g >> 1);                        // 16-value unit of the superblock
+            const int sc = (int)(int8_t)(rec_word(cur, 192 + (u & ~3)) >> (8 * (u & 3)));
+            const uint32_t S1 = f16x2_dup((float)(16 * (sc >> 4))), S2 = f16x2_dup((float)(sc & 15));
+            *reinterpret_cast<uint4*>(at1 + g * 128) =
+                make_uint4(hmul2(v[0], S1), hmul2(v[1], S1), hmul2(v[2], S1), hmul2(v[3], S1));
+            *reinterpret_cast<uint4*>(at2 + g * 128) =
+                make_uint4(hmul2(v[0], S2), hmul2(v[1], S2), hmul2(v[2], S2), hmul2(v[3], S2));
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) { arrive(&a_full[as]); arrive(&a_full[as2]); }
+          ai += 2;
+          for (int h = 0; h < 2; ++h)
+            if (++as == kASlots) { as = 0; aph ^= 1u; }
+        } else {
+          uint8_t* at = aring + as * kStepBytes + (r >> 3) * 1024 + (r & 7) * 16;
 #pragma unroll
-          for (int t = 0; t < 4; ++t)                             // word t: elements 8t..8t+7
-            *reinterpret_cast<uint4*>(at + (4 * jj + t) * 128) = kq_decode_word<FMT>(cur, t, j, S, S16);
+          for (int jj = 0; jj < 2; ++jj) {
+            const int j = 2 * s + jj;                              // sub-block (32 values)
+            const float sc = (float)q4k_field(hw[1], hw[2], hw[3], j);
+            const uint32_t S = f16x2_dup(sc * 1024.0f), S16 = f16x2_dup(sc * 64.0f);
+#pragma unroll
+            for (int t = 0; t < 4; ++t)                             // word t: elements 8t..8t+7
+              *reinterpret_cast<uint4*>(at + (4 * jj + t) * 128) = kq_decode_word<FMT>(cur, t, j, S, S16);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) arrive(&a_full[as]);
+          ++ai;
+          if (++as == kASlots) { as = 0; aph ^= 1u; }
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) arrive(&a_full[as]);
-        ++ai;
-        if (++as == kASlots) { as = 0; aph ^= 1u; }
       }
       if (stop) break;
     }
@@ -468,11 +546,16 @@ __global__ void __launch_bounds__(kKqThreads, 1) kq_kernel(const KqParams p) {
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t r1[16], r2[16];
           tld16(r1, tq + (uint32_t)(b * 256 + 16 * cc));
-          tld16(r2, tq + (uint32_t)(b * 256 + 128 + 16 * cc));
+          if constexpr (!kQ6) tld16(r2, tq + (uint32_t)(b * 256 + 128 + 16 * cc));
           tld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            acc[16 * cc + e] = fmaf(sc.x, __uint_as_float(r1[e]), fmaf(-sc.y, __uint_as_float(r2[e]), acc[16 * cc + e]));
+          for (int e = 0; e < 16; ++e) {
+            if constexpr (kQ6)
+              acc[16 * cc + e] = fmaf(sc.x, __uint_as_float(r1[e]), acc[16 * cc + e]);
+            else
+              acc[16 * cc + e] =
+                  fmaf(sc.x, __uint_as_float(r1[e]), fmaf(-sc.y, __uint_as_float(r2[e]), acc[16 * cc + e]));
+          }
         }
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
@@ -624,6 +707,8 @@ cudaError_t launch_kq(const Layout& L, const uint8_t* packed, const uint16_t* x,
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(kq_kernel<F_Q5_K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKqSmem);
     if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kq_kernel<F_Q6_K>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKqSmem);
+    if (err != cudaSuccess) return err;
     opted[dev] = 1;
   }
   const int grid = (int)(units < sms ? units : sms);
@@ -640,7 +725,9 @@ cudaError_t launch_kq(const Layout& L, const uint8_t* packed, const uint16_t* x,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = (L.fmt == F_Q5_K) ? cudaLaunchKernelEx(&cfg, kq_kernel<F_Q5_K>, p) : cudaLaunchKernelEx(&cfg, kq_kernel<F_Q4_K>, p);
+  err = (L.fmt == F_Q5_K)   ? cudaLaunchKernelEx(&cfg, kq_kernel<F_Q5_K>, p)
+        : (L.fmt == F_Q6_K) ? cudaLaunchKernelEx(&cfg, kq_kernel<F_Q6_K>, p)
+                            : cudaLaunchKernelEx(&cfg, kq_kernel<F_Q4_K>, p);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

@@ -305,13 +305,16 @@ qmv_status qmv_gemm_nvfp4_w4a4(const void* packed_W, const uint16_t* x, float x_
  * thousands of tokens: y[m][n] = sum_k x[m][k] BlockToFloat(W)[n][k], each weight
  * superblock streamed from HBM once per call rather than once per 8 tokens (the
  * re-streaming prefill bug: "Qwen3.8-27B on one Tenstorrent P150", "3. Porting the 9B
- * stack to 27B geometry", its prefill fixes). fmt: QMV_Q4_K or QMV_Q5_K (others return
- * QMV_EUNSUPPORTED). Per superblock,
+ * stack to 27B geometry", its prefill fixes). fmt: QMV_Q4_K, QMV_Q5_K or QMV_Q6_K (others
+ * return QMV_EUNSUPPORTED). Per superblock,
  * tcgen05.mma kind::f16 forms sum_k (sc_j q) x and sum_j m_j xsum_j in fp32 tensor memory
  * (sc_j q <= 1953 and m_j exact in f16; x in f16, exact for |x| in [2^-14, 65504]; xsum_j = the
  * fp32 sum of x over the 32-value sub-block, as two f16 terms, so |xsum_j| < 65504),
- * and y gathers d 2^14 and dmin times them in fp32. packed_W: the device layout of one
- * Q4_K or Q5_K [N, K] matrix (qmv_pack); K a multiple of 256; any N and M >= 1. x: device bf16
+ * and y gathers d 2^14 and dmin times them in fp32. Q6_K: sc_u (q - 32) can need 12
+ * significant bits, so the int8 scale is split, sc_u = 16 sh_u + sl_u, and each K step
+ * takes two MMAs, (q - 32) 16 sh_u and (q - 32) sl_u (both exact in f16); y gathers d
+ * times the sum. packed_W: the device layout of one
+ * Q4_K, Q5_K or Q6_K [N, K] matrix (qmv_pack); K a multiple of 256; any N and M >= 1. x: device bf16
  * [M][K], 16-byte aligned. y: device fp32 [M][N], fully overwritten. ws: device,
  * qmv_workspace_size(QMV_ENTRY_KQUANT, fmt, M, N, K, 1, 1) bytes: x's f16 tiles and
  * sub-block sums (rewritten by every call), one 64 KB slot of split-K partial sums and

@@ -103,7 +103,7 @@ def test_host_validation_new_entries(lib):
     assert kq(2, None, one, one, 512, 128, 256, one, 1 << 20, None) == 1
     assert kq(2, one, one, one, 0, 128, 256, one, 1 << 20, None) == 1
     assert kq(99, one, one, one, 512, 128, 256, one, 1 << 20, None) == 1             # not a format
-    for fmt in (1, 3, 4, 5, 7, 8, 9):                                                # Q8_0, Q6_K, NVFP4, FP8, IQ
+    for fmt in (1, 4, 5, 7, 8, 9):                                                   # Q8_0, NVFP4, FP8, IQ
         assert kq(fmt, one, one, one, 512, 128, 256, one, 1 << 20, None) == 3
     assert kq(2, one, one, one, 512, 128, 300, one, 1 << 20, None) == 3              # K % 256
     assert kq(6, one, one, one, 512, 128, 300, one, 1 << 20, None) == 3

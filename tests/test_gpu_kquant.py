@@ -1,8 +1,11 @@
-"""GPU parity of the K-quant (Q4_K) prefill GEMM on the tensor cores (tcgen05 kind::f16).
+"""GPU parity of the K-quant (Q4_K, Q5_K, Q6_K) prefill GEMM on the tensor cores
+(tcgen05 kind::f16).
 
-Expected values come from the CPU oracle only: BlockToFloat of the Q4_K weights and
-fp64 dots with the bf16 activations -- the same definition the GEMV meets. The bound
-is the GEMV's: |y - y_ref| <= 1e-5 sum_k |w x| per output.
+Expected values come from the CPU oracle only: BlockToFloat of the weights and fp64
+dots with the bf16 activations -- the same definition the GEMV meets. The bound is
+the GEMV's: |y - y_ref| <= 1e-5 sum_k |w x| per output. Q6_K's scale is split into
+two exact f16 terms (16 sh + sl); a test with arbitrary block bytes covers every
+int8 scale, including -128, and every 6-bit code.
 """
 import numpy as np
 import pytest
@@ -31,7 +34,7 @@ def flags_view(q, ws, M, K):
     return ws[off:off + 4 * sms]
 
 
-@pytest.mark.parametrize("fmt", ["q4_k", "q5_k"])
+@pytest.mark.parametrize("fmt", ["q4_k", "q5_k", "q6_k"])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (1, 128, 256), (129, 200, 512), (300, 384, 1024),
                                    (257, 1000, 2048), (512, 640, 4096)])
 def test_kquant_parity(q, fmt, M, N, K):
@@ -49,7 +52,7 @@ def test_kquant_parity(q, fmt, M, N, K):
     assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
 
 
-@pytest.mark.parametrize("fmt,M,N,K", [("q4_k", 2048, 384, 1024), ("q5_k", 1000, 260, 512)])
+@pytest.mark.parametrize("fmt,M,N,K", [("q4_k", 2048, 384, 1024), ("q5_k", 1000, 260, 512), ("q6_k", 1000, 260, 512)])
 def test_kquant_large_and_ragged_m(q, fmt, M, N, K):
     """Many token tiles (M = 2048: 16 tiles) and a ragged last token tile (M = 1000)."""
     W, canon = host_matrix(fmt, 65, N, K)
@@ -64,7 +67,8 @@ def test_kquant_large_and_ragged_m(q, fmt, M, N, K):
     assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
 
 
-@pytest.mark.parametrize("fmt,M,N,K", [("q4_k", 256, 256, 2048), ("q4_k", 384, 130, 4096), ("q5_k", 256, 300, 2048)])
+@pytest.mark.parametrize("fmt,M,N,K", [("q4_k", 256, 256, 2048), ("q4_k", 384, 130, 4096), ("q5_k", 256, 300, 2048),
+                                       ("q6_k", 256, 300, 2048)])
 def test_kquant_split_k_deterministic(q, fmt, M, N, K):
     """Few tiles over many CTAs: every tile is split across CTAs and finished from
     its peers' partial tiles. Two calls give identical bits, the flags end at zero."""
@@ -83,9 +87,11 @@ def test_kquant_split_k_deterministic(q, fmt, M, N, K):
     assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
 
 
-@pytest.mark.parametrize("fmt,N,K", [("q4_k", 17408, 5120), ("q4_k", 5120, 17408), ("q5_k", 17408, 5120)])
+@pytest.mark.parametrize("fmt,N,K", [("q4_k", 17408, 5120), ("q4_k", 5120, 17408), ("q5_k", 17408, 5120),
+                                     ("q6_k", 10240, 5120)])
 def test_kquant_full_size_sampled(q, fmt, N, K):
-    """The 27B MLP matrices at M = 512 (the prefill configuration), sampled rows."""
+    """The 27B MLP matrices and the Q6_K fused attn_qkv [10240, 5120] at M = 512 (the
+    prefill configuration), sampled rows."""
     M, seed = 512, 61
     packed = device_matrix(q, fmt, seed, N, K)
     rows = sample_rows(N, 24, seed)
@@ -106,7 +112,7 @@ def test_kquant_errors(q):
     packed = q.qmv_pack("q4_k", torch.from_numpy(canon).cuda(), N, K)
     x = synth.activations(63, M, K).cuda()
     ws = q.workspace(q.QMV_ENTRY_KQUANT, "q4_k", M, N, K)
-    for fmt in ("q6_k", "q8_0", "nvfp4", "fp8_row"):
+    for fmt in ("q8_0", "nvfp4", "fp8_row", "iq4_xs", "iq2_s"):
         with pytest.raises(q.QmvError) as ei:
             q.qmv_gemm_kquant(fmt, packed, x, N, K, ws)
         assert ei.value.status == 3
@@ -121,3 +127,25 @@ def test_kquant_errors(q):
     assert q.qmv_device_status(reset=True) == 5
     assert bool((y == 3.0).all())
     assert int(flags_view(q, ws, M, K).count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("M", [1, 130])
+def test_kquant_q6k_any_bytes(q, M):
+    """Q6_K blocks of arbitrary bytes (every int8 scale, -128 included, and every code)
+    with a positive fp16 d: the two-term scale split stays exact."""
+    N, K = 256, 1024
+    rng = np.random.default_rng(91 + M)
+    blocks = rng.integers(0, 256, size=(N * K // 256, 210), dtype=np.uint8)
+    d = rng.uniform(1e-4, 1e-3, size=N * K // 256).astype(np.float16).view(np.uint16)
+    blocks[:, 208] = d & 0xFF
+    blocks[:, 209] = d >> 8
+    blocks[0, 192:208] = np.array([0x80, 0x7F] * 8, dtype=np.uint8)      # scales -128, 127
+    canon = blocks.reshape(-1)
+    D = host_dequant("q6_k", canon, N, K)
+    x = synth.activations(93, M, K)
+    ref, den = oracle.gemv_f64(D, synth.bf16_bits(x))
+    packed = q.qmv_pack("q6_k", torch.from_numpy(canon).cuda(), N, K)
+    ws = q.workspace(q.QMV_ENTRY_KQUANT, "q6_k", M, N, K)
+    y = q.qmv_gemm_kquant("q6_k", packed, x.cuda(), N, K, ws).cpu().numpy()
+    assert q.qmv_device_status() == 0
+    assert norm_err(y, ref, den) <= TOL
