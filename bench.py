@@ -55,6 +55,13 @@ WORKLOADS = {
                              mats=[("gate|up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
                              desc="Q4_K decode MLP, Qwen3.8-27B geometry, M=1: fused gate|up [2 x 17408, 5120] "
                                   "with the SwiGLU epilogue, then down [5120,17408]"),
+    "q4k_mlp_layer_m1": dict(fmt="q4_k", M=1, fused=True, layer=True,
+                             mats=[("gate|up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
+                             desc="Q4_K decode MLP layer in one launch (qmv_mlp_layer), Qwen3.8-27B geometry, M=1: "
+                                  "fused gate|up [2 x 17408, 5120] with SwiGLU, h in bf16, then down [5120,17408]"),
+    "q4k_mlp_layer_m8": dict(fmt="q4_k", M=8, fused=True, layer=True,
+                             mats=[("gate|up", QWEN_MLP, QWEN_HIDDEN), ("down", QWEN_HIDDEN, QWEN_MLP)],
+                             desc="Q4_K decode MLP layer in one launch, Qwen3.8-27B geometry, M=8"),
     "q4k_mlp_m8": dict(fmt="q4_k", M=8, mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
                                               ("down", QWEN_HIDDEN, QWEN_MLP)],
                        desc="Q4_K decode MLP, Qwen3.8-27B geometry, M=8 (speculative verify block)"),
@@ -136,7 +143,7 @@ DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, 
                  "q6k_qkv_m1": 40000, "q6k_qkv_m8": 40000, "nvfp4_mlp_m1": 20000, "nvfp4_mlp_m8": 20000,
                  "fp8_m1": 40000, "fp8_m8": 40000, "q8_0_tiny": 20000, "tower_m1": 20000,
                  "tower_m4": 10000, "tower_m8": 5000, "nvfp4_w4a4_m512": 2000,
-                 "q4k_mlp_fused_m1": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000,
+                 "q4k_mlp_fused_m1": 20000, "q4k_mlp_layer_m1": 20000, "q4k_mlp_layer_m8": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000,
                  "tower_fused_m1": 20000, "tower_fused_m8": 5000, "q4k_prefill_m512": 2000,
                  "q5k_prefill_m512": 2000, "q6k_prefill_m512": 2000, "iq4xs_tower_down_m1": 20000, "iq4xs_tower_down_m8": 5000,
                  "iq4xs_mlp_m1": 20000, "iq2s_tower_gateup_m1": 20000, "iq3s_tower_down_m1": 20000}
@@ -359,6 +366,7 @@ class DeviceWorkload:
         self.w4a4 = w.get("w4a4", False)
         self.kquant = w.get("kquant", False)
         self.fused = w.get("fused", False)
+        self.layer = w.get("layer", False)      # the MLP layer in one launch (qmv_mlp_layer)
         self.E = w.get("E", 1)
         self.topk = w.get("topk", 1)
         self.mats = w["mats"]
@@ -390,6 +398,9 @@ class DeviceWorkload:
                 entry = q.QMV_ENTRY_KQUANT
             if self.fused and i == 0:
                 entry = q.QMV_ENTRY_GROUPED_SWIGLU if self.tower else q.QMV_ENTRY_SWIGLU
+            if self.layer:
+                entry = q.QMV_ENTRY_MLP_LAYER       # one workspace, sized by gate|up's [N_ff, K_h]
+                N, K = self.mats[0][1], self.mats[0][2]
             self.ws.append(q.workspace(entry, self.fmt, self.M, N, K, self.E, self.topk, device=dev))
         # W4A4: the static activation scale of each x (amax / (448 * 6)), computed once
         self.x_scale = [float(x.float().abs().max()) / 2688.0 for x in self.x] if self.w4a4 else []
@@ -402,7 +413,7 @@ class DeviceWorkload:
                 self.ids.append(torch.from_numpy(ids).to(dev))
                 self.unique.append(len(np.unique(ids)))
         # W4A4 runs the activation quantizer and the GEMM per matrix
-        self.launches_per_step = len(self.mats) * (2 if (self.w4a4 or self.kquant) else 1)
+        self.launches_per_step = 1 if self.layer else len(self.mats) * (2 if (self.w4a4 or self.kquant) else 1)
 
     def pair_x(self, i):
         """Tower matrices whose x has one row per (token, slot): the down projection
@@ -430,6 +441,11 @@ class DeviceWorkload:
     def launch_step(self, s):
         q = self.q
         c = s % self.copies
+        if self.layer:
+            (_, N_ff, K_h) = self.mats[0]
+            q.qmv_mlp_layer(self.fmt, self.packed[c][0], self.packed[c][1], self.x[0], N_ff, K_h, self.ws[0],
+                            y=self.y[1])
+            return
         for i, (_, N, K) in enumerate(self.mats):
             if self.tower and self.fused and i == 0:
                 q.qmv_grouped_swiglu(self.fmt, self.packed[c][i], self.ids[s % len(self.ids)], self.x[i], N, K,
@@ -585,7 +601,8 @@ def run_device(args, rank, world, dev):
         "pct_of_nominal_8000": round(100.0 * value / world / 8000.0, 2),
         "roofline": {
             "bound": "hbm",
-            "kernel": f"qmv::stream_kernel<{wl.fmt}, M={wl.M}>" + (" (grouped)" if wl.tower else ""),
+            "kernel": (f"qmv::layer_kernel<{wl.fmt}, M={wl.M}>" if wl.layer else
+                       f"qmv::stream_kernel<{wl.fmt}, M={wl.M}>" + (" (grouped)" if wl.tower else "")),
             "achieved": round(achieved, 2),
             "peak": peak,
             "peak_kind": peak_kind,

@@ -23,7 +23,7 @@ FORMATS = {"q8_0": QMV_Q8_0, "q4_k": QMV_Q4_K, "q6_k": QMV_Q6_K, "nvfp4": QMV_NV
            "iq2_s": QMV_IQ2_S}
 GRID_BYTES = {"iq3_s": 512 * 4, "iq2_s": 1024 * 8}
 QMV_ENTRY_GEMV, QMV_ENTRY_GROUPED, QMV_ENTRY_W4A4, QMV_ENTRY_SWIGLU = 1, 2, 3, 4
-QMV_ENTRY_GROUPED_SWIGLU, QMV_ENTRY_KQUANT = 5, 6
+QMV_ENTRY_GROUPED_SWIGLU, QMV_ENTRY_KQUANT, QMV_ENTRY_MLP_LAYER = 5, 6, 7
 QMV_MAX_M = 8
 
 STATUS = {0: "QMV_OK", 1: "QMV_EINVAL", 2: "QMV_EALIGN", 3: "QMV_EUNSUPPORTED", 4: "QMV_ECUDA",
@@ -66,6 +66,7 @@ _gemv = _sig("qmv_gemv", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
 _gemv_swiglu = _sig("qmv_gemv_swiglu", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
 _gemv_noalloc = _sig("qmv_gemv_noalloc", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P])
 _grouped = _sig("qmv_grouped", _I, [_I, _P, _P, _P, _I, _P, _I, _I, _I64, _I64, _I64, _P, _SZ, _P])
+_mlp_layer = _sig("qmv_mlp_layer", _I, [_I, _P, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
 _grouped_swiglu = _sig("qmv_grouped_swiglu", _I, [_I, _P, _P, _P, _P, _I, _I, _I64, _I64, _I64, _P, _SZ, _P])
 _quant_act = _sig("qmv_quant_act_nvfp4", _I, [_P, _F, _P, _P, _I, _I64, _P])
 _w4a4 = _sig("qmv_gemm_nvfp4_w4a4", _I, [_P, _P, _F, _P, _I, _I64, _I64, _P, _SZ, _P])
@@ -79,7 +80,7 @@ EXPORTED = ["qmv_canon_size", "qmv_pack_size", "qmv_pack", "qmv_quantize", "qmv_
             "qmv_workspace_size", "qmv_gemv", "qmv_grouped", "qmv_quant_act_nvfp4",
             "qmv_gemm_nvfp4_w4a4", "qmv_status_str", "qmv_last_route", "qmv_device_status",
             "qmv_gemv_noalloc", "qmv_gemv_swiglu", "qmv_grouped_swiglu", "qmv_gemm_kquant",
-            "qmv_debug_split_k_fault", "qmv_quantize_codebook"]
+            "qmv_debug_split_k_fault", "qmv_quantize_codebook", "qmv_mlp_layer"]
 
 
 def _fmt(fmt) -> int:
@@ -286,6 +287,18 @@ def qmv_gemv_swiglu(fmt, tower: torch.Tensor, x: torch.Tensor, N: int, K: int, w
     _check(_gemv_swiglu(_fmt(fmt), _ptr(tower), _ptr(x), _ptr(h), M, N, K, _ptr(ws), ws.numel(),
                         _stream(stream)), "qmv_gemv_swiglu")
     return h
+
+
+def qmv_mlp_layer(fmt, gateup: torch.Tensor, down: torch.Tensor, x: torch.Tensor, N_ff: int, K_h: int,
+                  ws: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = bf16(silu(x Wg^T) * (x Wu^T)) Wd^T in one launch: gateup = the 2-matrix
+    [N_ff, K_h] tower (gate, up), down = the [K_h, N_ff] matrix."""
+    _dev(gateup, "gateup"); _dev(down, "down"); _dev(x, "x"); _dev(ws, "ws")
+    x, M = _act(x, K_h)
+    y = _out(y, (M, K_h), x.device, "y")
+    _check(_mlp_layer(_fmt(fmt), _ptr(gateup), _ptr(down), _ptr(x), _ptr(y), M, N_ff, K_h, _ptr(ws), ws.numel(),
+                      _stream(stream)), "qmv_mlp_layer")
+    return y
 
 
 def qmv_gemv_noalloc(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int,

@@ -48,6 +48,30 @@ void apply_plan(StreamArgs* a, const StreamPlan& p) {
   a->maxslots = p.maxslots;
 }
 
+// The MLP layer entry's workspace: the two passes' published pieces (sized for the
+// layer's grid, the larger of the two plans'), h as bf16 [M][N_ff], and the counter the
+// CTAs arrive on between the passes.
+struct LayerPlan {
+  StreamPlan p1, p2;
+  int grid;
+  int64_t off2, off_h, off_cnt, total;
+};
+bool layer_plan(int fmt, int M, int64_t N_ff, int64_t K_h, int sms, Layout* L1, Layout* L2, LayerPlan* lp) {
+  if (!make_layout(fmt, N_ff, K_h, 2, L1) || !make_layout(fmt, K_h, N_ff, 1, L2)) return false;
+  if (!slab_count_ok(*L1, 2) || !slab_count_ok(*L2, 1)) return false;
+  lp->p1 = plan_stream_dense(2 * L1->row_tiles * L1->k_groups, M, 2, sms);
+  lp->p2 = plan_stream_dense(L2->row_tiles * L2->k_groups, M, 1, sms);
+  lp->grid = lp->p1.grid > lp->p2.grid ? lp->p1.grid : lp->p2.grid;
+  const int64_t pb = 128 * (M <= 1 ? 1 : 8) * 4;
+  const int64_t w1 = align_up((int64_t)lp->grid * lp->p1.maxslots * pb, 256);
+  const int64_t w2 = align_up((int64_t)lp->grid * lp->p2.maxslots * pb, 256);
+  lp->off2 = w1;
+  lp->off_h = w1 + w2;
+  lp->off_cnt = lp->off_h + align_up((int64_t)M * N_ff * 2, 256);
+  lp->total = lp->off_cnt + 256;
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -133,6 +157,12 @@ size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, i
     const int64_t experts = (int64_t)M * topk < E ? (int64_t)M * topk : E;
     return (size_t)plan_stream_grouped(passes * experts * L.row_tiles * L.k_groups, M, passes, L.k_groups, sms)
         .ws_bytes;
+  }
+  if (entry == QMV_ENTRY_MLP_LAYER) {
+    Layout L1, L2;
+    LayerPlan lp;
+    if (M > QMV_MAX_M || !layer_plan((int)fmt, M, N, K, sms, &L1, &L2, &lp)) return 0;
+    return (size_t)lp.total;
   }
   if (entry == QMV_ENTRY_KQUANT) {
     if ((fmt != QMV_Q4_K && fmt != QMV_Q5_K && fmt != QMV_Q6_K) || K % 256) return 0;
@@ -235,6 +265,47 @@ qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, fl
   int variant = 0;
   qmv_status st = from_cuda(launch_stream(a, stream, &variant));
   if (st == QMV_OK) g_last_route = (int)fmt * 100 + variant;
+  return st;
+}
+
+qmv_status qmv_mlp_layer(qmv_fmt fmt, const void* gateup, const void* down, const uint16_t* x, float* y, int M,
+                         int64_t N_ff, int64_t K_h, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !gateup || !down || !x || !y || !ws) return QMV_EINVAL;
+  if (M < 1 || M > QMV_MAX_M || N_ff <= 0 || K_h <= 0) return QMV_EINVAL;
+  if (!aligned(gateup, 256) || !aligned(down, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4))
+    return QMV_EALIGN;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return QMV_ECUDA;
+  Layout L1, L2;
+  LayerPlan lp;
+  if (!layer_plan((int)fmt, M, N_ff, K_h, sms, &L1, &L2, &lp)) return QMV_EUNSUPPORTED;
+  if (ws_bytes < (size_t)lp.total) return QMV_EWORKSPACE;
+  unsigned* status = status_ptr();
+  if (!status) return QMV_ECUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  StreamArgs a1, a2;
+  a1.L = L1;
+  a1.packed = static_cast<const uint8_t*>(gateup);
+  a1.x = x;
+  a1.y = reinterpret_cast<float*>(w + lp.off_h);          // h, written as bf16
+  a1.ids = nullptr;
+  a1.M = M; a1.topk = 1; a1.x_per_pair = 0; a1.swiglu = 1;
+  a1.ws = w; a1.ws_bytes = lp.off2;
+  a1.status = status;
+  apply_plan(&a1, lp.p1);
+  a1.num_ctas = lp.grid;
+  a2.L = L2;
+  a2.packed = static_cast<const uint8_t*>(down);
+  a2.x = reinterpret_cast<const uint16_t*>(w + lp.off_h);
+  a2.y = y;
+  a2.ids = nullptr;
+  a2.M = M; a2.topk = 1; a2.x_per_pair = 0; a2.swiglu = 0;
+  a2.ws = w + lp.off2; a2.ws_bytes = lp.off_h - lp.off2;
+  a2.status = status;
+  apply_plan(&a2, lp.p2);
+  a2.num_ctas = lp.grid;
+  qmv_status st = from_cuda(launch_layer(a1, a2, reinterpret_cast<unsigned*>(w + lp.off_cnt), stream));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + 12;
   return st;
 }
 

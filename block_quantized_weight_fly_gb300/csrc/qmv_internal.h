@@ -88,5 +88,9 @@ cudaError_t launch_kq(const Layout& L, const uint8_t* packed, const uint16_t* x,
 int64_t kq_workspace_bytes(int64_t m_pad, int64_t K, int sms);
 // returns the route variant launched (1 = M=1, 2 = M>1, 3 = grouped, 9 = fused gate|up SwiGLU)
 cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant);
+// The MLP layer in one launch (layer_kernel): a1 = the fused gate|up pass (its y = h,
+// written as bf16), a2 = the down pass over h; both with the same num_ctas. counter:
+// a workspace word the CTAs count their arrivals on between the phases.
+cudaError_t launch_layer(const StreamArgs& a1, const StreamArgs& a2, unsigned* counter, cudaStream_t s);
 
 }  // namespace qmv

@@ -33,6 +33,7 @@
 //
 // Every wait (mbarrier, peer partial sum) is bounded in time; on expiry the CTA latches
 // QMV_ETIMEOUT in the device status word and stops.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include "qmv_internal.h"
 #include "qmv_slab.cuh"
@@ -87,6 +88,9 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 }
 __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_inval(uint64_t* b) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(b)) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
@@ -446,9 +450,38 @@ struct Cursor {
   }
 };
 
-template <int FMT, int MT, bool SW, bool GR>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(const KParams kp) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+// What the producer waits for before it copies the activations: the previous kernel
+// in the stream (griddepcontrol.wait), and in the second phase of the MLP layer kernel
+// also every CTA's first phase (a generation counter in global memory; counter ==
+// nullptr: none). The wait is bounded and latches QMV_ETIMEOUT.
+struct DepWait {
+  const unsigned* counter;
+  unsigned target;
+};
+__device__ __forceinline__ bool dep_wait(const DepWait& d, unsigned* status) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (d.counter == nullptr) return true;
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(d.counter) : "memory");
+    if ((int)(v - d.target) >= 0) break;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      atomicOr(status, kStatTimeout);
+      return false;
+    }
+    __nanosleep(100);
+  }
+  // the activations were written by plain stores of other CTAs: order them before
+  // this thread's bulk copies (the async proxy)
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+// One streaming GEMV pass (the whole kernel for qmv_gemv and its relatives; each of
+// the two phases of the MLP layer kernel). YB: the epilogue writes bf16 outputs.
+template <int FMT, int MT, bool SW, bool GR, bool YB>
+__device__ __forceinline__ void stream_body(const KParams& kp, uint8_t* smem, const DepWait dep) {
   const StreamArgs& a = kp.a;
   const Layout& L = a.L;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -460,11 +493,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
 
-  // Programmatic dependent launch: the next kernel in the stream may start its own
-  // prologue and weight prefetch as SMs free up. Everything that could depend on
-  // the previous kernel (the activations, the workspace, the outputs) is touched
-  // only after griddepcontrol.wait (a no-op when launched without the attribute).
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Everything that could depend on the previous kernel (the activations, the
+  // workspace, the outputs) is touched only after griddepcontrol.wait (a no-op when
+  // launched without the attribute).
 
   // ---- set-up: header check, segment table, barriers -----------------------
   if (tid == 0) {
@@ -624,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         c2.next(G, RT);
       }
     }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!dep_wait(dep, a.status)) misc[0] = 1;
     for (int s = s0; s < s1; ++s, ++it) {
       if (it >= kp.stages) {      // round r >= 1 waits for the consumers' release of round r-1
         if (!mbar_wait(&empty[stage], rphase ^ 1u, a.status)) { misc[0] = 1; break; }
@@ -691,7 +722,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
         c2.next(G, RT);
       }
     }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    {
+      bool ok = true;
+      if (lane == 0) ok = dep_wait(dep, a.status);
+      else asm volatile("griddepcontrol.wait;" ::: "memory");
+      ok = __shfl_sync(kPMask, ok, 0);
+      if (!ok && lane == 0) misc[0] = 1;
+      __syncwarp(kPMask);
+    }
     for (int s = s0; s < s1; ++s, ++it) {
       if (it >= kp.stages) {      // round r >= 1 waits for the consumers' release of round r-1
         bool ok = true;
@@ -1024,12 +1062,57 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(con
           if (FMT == F_FP8) uv *= reinterpret_cast<const float*>(extras_u)[n];
           v = (v / (1.0f + expf(-v))) * uv;               // silu(g) * u
         }
-        a.y[(int64_t)sg.yrow[tok] * L.N + n] = v;
+        if constexpr (YB)
+          reinterpret_cast<__nv_bfloat16*>(a.y)[(int64_t)sg.yrow[tok] * L.N + n] = __float2bfloat16_rn(v);
+        else
+          a.y[(int64_t)sg.yrow[tok] * L.N + n] = v;
       }
     }
     ++T;
     if (++tt == RT) { tt = 0; ++seg; }
   }
+}
+
+// The decode GEMV kernel: one pass. Programmatic dependent launch: the next kernel
+// in the stream may start its own prologue and weight prefetch as SMs free up.
+template <int FMT, int MT, bool SW, bool GR>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>()) stream_kernel(const KParams kp) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  stream_body<FMT, MT, SW, GR, false>(kp, smem, DepWait{nullptr, 0u});
+}
+
+// The MLP layer in one launch: phase 1 is the fused gate|up pass with the SwiGLU
+// epilogue, writing h as bf16 into the workspace; phase 2 is the down projection over
+// h. Between them every CTA arrives on a generation counter (its h rows are stored);
+// each CTA's producer issues its first phase-2 weight copies at once and waits on the
+// counter only before it copies h. All CTAs of the grid are resident together (at
+// most ctas_per_sm() per SM, as for the GEMV), so the wait ends.
+template <int FMT, int MT>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<MT>())
+    layer_kernel(const KParams kp1, const KParams kp2, unsigned* counter) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  stream_body<FMT, MT, true, false, true>(kp1, smem, DepWait{nullptr, 0u});
+  __syncthreads();
+  unsigned target = 0u;
+  if (threadIdx.x == 0) {
+    // this CTA's h stores (every warp passed the barrier above) before its arrival
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+    const unsigned old = atomicAdd(counter, 1u);
+    target = (old / gridDim.x + 1u) * gridDim.x;
+    // phase 1's barriers are idle: invalidate them for phase 2's set-up
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    for (int i = 0; i < kp1.stages; ++i) {
+      mbar_inval(&full[i]);
+      mbar_inval(&full[kMaxStages + i]);
+    }
+    mbar_inval(reinterpret_cast<uint64_t*>(smem + kGbarOff));
+    mbar_inval(reinterpret_cast<uint64_t*>(smem + kGridBarOff));
+  }
+  __syncthreads();
+  stream_body<FMT, MT, false, false, false>(kp2, smem, DepWait{counter, target});
 }
 
 // ---------------------------------------------------------------------------
@@ -1087,8 +1170,10 @@ int num_sms_current_device() {
   return n;
 }
 
+// The kernel parameters of one pass (shared-memory layout, stage count, the plan's
+// cells), validated; *smem = the dynamic shared memory the pass needs.
 template <int FMT, int MT, bool SW>
-static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
+static cudaError_t prep_kp(const StreamArgs& a, KParams& kp, int* smem_out, int* dev_out) {
   int dev = 0, smem_max = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -1104,7 +1189,6 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   // per CTA: its share of the SM less the 1 KB the hardware reserves per CTA
   const int smem_cta = smem_sm / ctas_per_sm<MT>() - 1024;
   if (smem_cta < smem_max) smem_max = smem_cta;
-  KParams kp;
   kp.a = a;
   kp.mt = MT;
   kp.tbl_off = 512 + kMaxSeg * (int)sizeof(Seg);
@@ -1136,7 +1220,17 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   if (a.maxslots < 1 || (int64_t)a.num_ctas * a.maxslots * kSlabRows * MT * 4 > a.ws_bytes)
     return cudaErrorInvalidValue;
   kp.partials = reinterpret_cast<float*>(a.ws);
-  const int smem = kp.stage_base + kp.stages * kp.stage_bytes;
+  *smem_out = kp.stage_base + kp.stages * kp.stage_bytes;
+  *dev_out = dev;
+  return cudaSuccess;
+}
+
+template <int FMT, int MT, bool SW>
+static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
+  KParams kp;
+  int smem = 0, dev = 0;
+  cudaError_t err = prep_kp<FMT, MT, SW>(a, kp, &smem, &dev);
+  if (err != cudaSuccess) return err;
   // M = 1 grouped calls have an instance of their own (the producer's first-stage start)
   // grouped calls have instances of their own (cells, and at M = 1 the producer's
   // first-stage start)
@@ -1171,6 +1265,63 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   err = cudaLaunchKernelEx(&cfg, kern, kp);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
+}
+
+template <int FMT, int MT>
+static cudaError_t launch_layer_t(const StreamArgs& a1, const StreamArgs& a2, unsigned* counter, cudaStream_t s) {
+  KParams kp1, kp2;
+  int smem1 = 0, smem2 = 0, dev = 0;
+  cudaError_t err = prep_kp<FMT, MT, true>(a1, kp1, &smem1, &dev);
+  if (err != cudaSuccess) return err;
+  err = prep_kp<FMT, MT, false>(a2, kp2, &smem2, &dev);
+  if (err != cudaSuccess) return err;
+  if (a1.num_ctas != a2.num_ctas || a1.ids || a2.ids || a1.cells <= 0 || a2.cells <= 0) return cudaErrorInvalidValue;
+  const int smem = smem1 > smem2 ? smem1 : smem2;
+  void (*kern)(const KParams, const KParams, unsigned*) = layer_kernel<FMT, MT>;
+  static int opted[64] = {0};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (opted[dev] < smem) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    opted[dev] = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a1.num_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  // at most ctas_per_sm() CTAs per SM (checked in prep_kp), so the whole grid is
+  // resident at once once the kernels before it have left: the wait between the
+  // phases ends
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kern, kp1, kp2, counter);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+template <int FMT>
+static cudaError_t launch_layer_fmt(const StreamArgs& a1, const StreamArgs& a2, unsigned* counter, cudaStream_t s) {
+  if (a1.M <= 1) return launch_layer_t<FMT, 1>(a1, a2, counter, s);
+  return launch_layer_t<FMT, 8>(a1, a2, counter, s);
+}
+
+cudaError_t launch_layer(const StreamArgs& a1, const StreamArgs& a2, unsigned* counter, cudaStream_t s) {
+  switch (a1.L.fmt) {
+    case F_Q8_0: return launch_layer_fmt<F_Q8_0>(a1, a2, counter, s);
+    case F_Q4_K: return launch_layer_fmt<F_Q4_K>(a1, a2, counter, s);
+    case F_Q5_K: return launch_layer_fmt<F_Q5_K>(a1, a2, counter, s);
+    case F_Q6_K: return launch_layer_fmt<F_Q6_K>(a1, a2, counter, s);
+    case F_NVFP4: return launch_layer_fmt<F_NVFP4>(a1, a2, counter, s);
+    case F_FP8: return launch_layer_fmt<F_FP8>(a1, a2, counter, s);
+    case F_IQ4_XS: return launch_layer_fmt<F_IQ4_XS>(a1, a2, counter, s);
+    case F_IQ3_S: return launch_layer_fmt<F_IQ3_S>(a1, a2, counter, s);
+    case F_IQ2_S: return launch_layer_fmt<F_IQ2_S>(a1, a2, counter, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int FMT>

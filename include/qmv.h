@@ -102,7 +102,8 @@ enum {
   QMV_ENTRY_W4A4 = 3,
   QMV_ENTRY_SWIGLU = 4,
   QMV_ENTRY_GROUPED_SWIGLU = 5,
-  QMV_ENTRY_KQUANT = 6
+  QMV_ENTRY_KQUANT = 6,
+  QMV_ENTRY_MLP_LAYER = 7
 };
 
 /* Largest decode batch served by qmv_gemv / qmv_grouped (M rows of x). */
@@ -268,6 +269,28 @@ qmv_status qmv_gemv_swiglu(qmv_fmt fmt, const void* tower, const uint16_t* x, fl
  * [M][K]. h: device fp32 [M][topk][N], fully overwritten. ws: device,
  * qmv_workspace_size(QMV_ENTRY_GROUPED_SWIGLU, ...) bytes, zero-filled once (as
  * for qmv_gemv). E <= 2^23. */
+/* The dense MLP layer in one launch: h = silu(x W_gate^T) * (x W_up^T) (as
+ * qmv_gemv_swiglu), rounded to bf16, then y = h W_down^T (as qmv_gemv over the bf16
+ * h). Defined by the matmul seam applied twice around the SwiGLU ("Qwen3.8-27B on one
+ * Tenstorrent P150", "4. Measuring the ceiling, and lots of dead ends": the fused
+ * gate/up and down of the decode MLP) and the joined gate|up projection ("I Built a
+ * Custom Blackwell Kernel for Qwen3.8-27B", "What the custom path actually does").
+ * One kernel: its CTAs run the gate|up pass, store their rows of h in the workspace
+ * and arrive on a counter there; each CTA copies its first down-projection weights
+ * at once and waits (bounded: QMV_ETIMEOUT) for every CTA's arrival before it reads
+ * h. The results equal qmv_gemv_swiglu, a bf16 round-to-nearest-even of h, then
+ * qmv_gemv, bit for bit (the same cells in both passes). gateup: the packed tower of
+ * 2 matrices [N_ff, K_h] (gate, then up; as qmv_gemv_swiglu). down: the packed
+ * [K_h, N_ff] matrix. Both of format fmt. x: device bf16 [M][K_h], 16-byte aligned.
+ * y: device fp32 [M][K_h], fully overwritten. M = 1..8. ws: device,
+ * qmv_workspace_size(QMV_ENTRY_MLP_LAYER, fmt, M, N_ff, K_h, 1, 1) bytes, 256-byte
+ * aligned, zero-filled once: the two passes' partial sums (zero again after every
+ * successful call), h, and the arrival counter (which counts on across calls; zero-
+ * fill the workspace again after a status error). Calls sharing a workspace must
+ * not overlap. */
+qmv_status qmv_mlp_layer(qmv_fmt fmt, const void* gateup, const void* down, const uint16_t* x, float* y,
+                         int M, int64_t N_ff, int64_t K_h, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 qmv_status qmv_grouped_swiglu(qmv_fmt fmt, const void* tower, const int32_t* expert_ids,
                               const uint16_t* x, float* h, int M, int topk, int64_t N, int64_t K,
                               int64_t E, void* ws, size_t ws_bytes, cudaStream_t stream);

@@ -55,6 +55,8 @@ def _load():
     lib.or_f32_to_fp16.argtypes = [ctypes.c_float]
     lib.or_bf16_to_f32.restype = ctypes.c_float
     lib.or_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.or_f64_to_bf16.restype = ctypes.c_uint16
+    lib.or_f64_to_bf16.argtypes = [ctypes.c_double]
     lib.or_e4m3_to_f32.restype = ctypes.c_float
     lib.or_e4m3_to_f32.argtypes = [ctypes.c_uint8]
     lib.or_f32_to_e4m3.restype = ctypes.c_uint8
@@ -109,6 +111,17 @@ def f32_to_fp16(f: float) -> int:
 
 def bf16_to_f32(b: int) -> float:
     return _load().or_bf16_to_f32(b)
+
+
+def f64_to_bf16(v: float) -> int:
+    return _load().or_f64_to_bf16(float(v))
+
+
+def f64_to_bf16_array(a: np.ndarray) -> np.ndarray:
+    """Elementwise bf16 round-to-nearest-even (uint16 bit patterns)."""
+    a = np.asarray(a, dtype=np.float64)
+    f = _load().or_f64_to_bf16
+    return np.array([f(float(v)) for v in a.reshape(-1)], dtype=np.uint16).reshape(a.shape)
 
 
 def e4m3_to_f32(c: int) -> float:

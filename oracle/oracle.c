@@ -82,6 +82,21 @@ uint16_t or_f32_to_fp16(float f) {
 }
 
 /* ---- bfloat16: the top half of an fp32 ----------------------------------- */
+/* round-to-nearest-even of a double to bfloat16 (8 significand bits, fp32's exponent
+ * range); overflow to infinity */
+uint16_t or_f64_to_bf16(double v) {
+    if (v != v) return 0x7FC0;
+    uint16_t sign = (v < 0 || (v == 0 && 1.0 / v < 0)) ? 0x8000 : 0;
+    double a = fabs(v);
+    double r = rne_to_format(a, 8, -126);
+    if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+    if (r == 0.0) return sign;
+    float f = (float)r;                     /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFF));
+}
+
 float or_bf16_to_f32(uint16_t b) {
     uint32_t u = (uint32_t)b << 16;
     float f;

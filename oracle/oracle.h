@@ -70,6 +70,7 @@ enum { OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q6_K = 3, OR_NVFP4 = 4, OR_FP8_ROW = 5, OR_Q
 float or_fp16_to_f32(uint16_t h);
 uint16_t or_f32_to_fp16(float f);
 float or_bf16_to_f32(uint16_t b);
+uint16_t or_f64_to_bf16(double v);
 float or_e4m3_to_f32(uint8_t c);
 uint8_t or_f32_to_e4m3(float f);
 float or_e2m1_to_f32(uint8_t c);

@@ -92,6 +92,26 @@ def test_block_lengths():
     assert [oracle.block_values(f) for f in ("q8_0", "q4_k", "q5_k", "q6_k", "nvfp4")] == [32, 256, 256, 256, 16]
 
 
+def test_bf16_rounding_of_doubles():
+    """or_f64_to_bf16: every bf16 value maps to itself; fp32 inputs round as torch's
+    fp32 -> bf16 conversion (round to nearest even); midpoints between neighbours go to
+    the even one; overflow gives infinity."""
+    pats = np.arange(0, 1 << 16, dtype=np.uint32)
+    vals = (pats << 16).view(np.float32)
+    finite = np.isfinite(vals)
+    got = oracle.f64_to_bf16_array(vals[finite].astype(np.float64))
+    assert np.array_equal(got[vals[finite] != 0], pats[finite][vals[finite] != 0].astype(np.uint16))
+    rng = np.random.default_rng(3)
+    v = np.concatenate([rng.standard_normal(20000), rng.standard_normal(2000) * 1e-39,
+                        rng.standard_normal(2000) * 1e37]).astype(np.float32)
+    want = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.f64_to_bf16_array(v.astype(np.float64)), want)
+    # 1 + 2^-8 is the midpoint of 1 and 1 + 2^-7: to 1 (even); 1 + 3 * 2^-8 to 1 + 2^-6
+    assert oracle.f64_to_bf16(1 + 2.0**-8) == 0x3F80 and oracle.f64_to_bf16(1 + 3 * 2.0**-8) == 0x3F82
+    assert oracle.f64_to_bf16(-(1 + 2.0**-8)) == 0xBF80
+    assert oracle.f64_to_bf16(1e39) == 0x7F80 and oracle.f64_to_bf16(-1e39) == 0xFF80
+
+
 def test_fp16_encode_vs_numpy_rne():
     rng = np.random.default_rng(1)
     vals = np.concatenate([
