@@ -85,6 +85,10 @@ def _load():
     lib.or_quant_act_nvfp4.argtypes = [P, I64, I64, ctypes.c_float, P, P]
     lib.or_swiglu_f64.restype = None
     lib.or_swiglu_f64.argtypes = [P, P, I64, P]
+    lib.or_quant_act_q8.restype = None
+    lib.or_quant_act_q8.argtypes = [P, I64, I64, P, P]
+    lib.or_int8dot_f64.restype = None
+    lib.or_int8dot_f64.argtypes = [P, I64, I64, P, I64, P, P]
     lib.or_w4a4_f64.restype = None
     lib.or_w4a4_f64.argtypes = [P, I64, I64, ctypes.c_float, P, I64, P, P]
     _lib = lib
@@ -234,6 +238,35 @@ def w4a4_f64(W: np.ndarray, x_bf16: np.ndarray, x_scale: float):
     y = np.empty((M, N), dtype=np.float64)
     den = np.empty((M, N), dtype=np.float64)
     _load().or_w4a4_f64(_ptr(x), M, K, float(x_scale), _ptr(W), N, _ptr(y), _ptr(den))
+    return y, den
+
+
+def quant_act_q8(x_bf16: np.ndarray):
+    """bf16 x[M, K] -> (int8 codes [M, K], fp32 scales [M, K/32]): d = amax / 127 per
+    32 values, q = clamp(rint(x / d), -127, 127)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    M, K = x.shape
+    codes = np.zeros((M, K), dtype=np.int8)
+    scales = np.zeros((M, K // 32), dtype=np.float32)
+    _load().or_quant_act_q8(_ptr(x), M, K, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def int8dot_f64(W: np.ndarray, x_bf16: np.ndarray):
+    """The int8-dot reference: x quantized by quant_act_q8, then fp64 dots with the
+    BlockToFloat weights W[N, K]. Returns (y [M, N], den [M, N] = sum |terms|)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    N, K = W.shape
+    M = x.shape[0]
+    assert x.shape[1] == K and K % 32 == 0
+    y = np.empty((M, N), dtype=np.float64)
+    den = np.empty((M, N), dtype=np.float64)
+    _load().or_int8dot_f64(_ptr(x), M, K, _ptr(W), N, _ptr(y), _ptr(den))
     return y, den
 
 

@@ -729,6 +729,52 @@ void or_w4a4_f64(const uint16_t* x_bf16, int64_t M, int64_t K, float x_scale, co
     free(a);
 }
 
+/* The int8-dot lever ("feat(BACKEND-TENSTORRENT-KEEPQUANT) ...", "Scope", its "Out of
+ * scope" line and the decode-cost note that books the lever as the repayment): the
+ * activation quantized to int8 per 32-value block, d = amax / 127 (fp32) and
+ * q = clamp(rint(x / d), -127, 127) (all zero when d = 0), and the product taken
+ * against those integers. */
+void or_quant_act_q8(const uint16_t* x_bf16, int64_t M, int64_t K, int8_t* codes, float* scales) {
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t b = 0; b < K / 32; b++) {
+            float xv[32], amax = 0.0f;
+            for (int i = 0; i < 32; i++) {
+                xv[i] = or_bf16_to_f32(x_bf16[m * K + b * 32 + i]);
+                if (fabsf(xv[i]) > amax) amax = fabsf(xv[i]);
+            }
+            float d = amax / 127.0f;
+            scales[m * (K / 32) + b] = d;
+            for (int i = 0; i < 32; i++)
+                codes[m * K + b * 32 + i] = (int8_t)((d == 0.0f) ? 0 : (int)clampf(rintf(xv[i] / d), -127.0f, 127.0f));
+        }
+}
+
+/* y = sum_k W[n][k] (d_b q_k) in fp64 with W = BlockToFloat of the weights [N][K] and
+ * the activation's int8 codes and block scales from or_quant_act_q8; den = sum |terms| */
+void or_int8dot_f64(const uint16_t* x_bf16, int64_t M, int64_t K, const float* W, int64_t N, double* y,
+                    double* den) {
+    int8_t* codes = (int8_t*)malloc((size_t)(M * K));
+    float* scales = (float*)malloc(sizeof(float) * (size_t)(M * (K / 32)));
+    double* a = (double*)malloc(sizeof(double) * (size_t)K);
+    or_quant_act_q8(x_bf16, M, K, codes, scales);
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t k = 0; k < K; k++) a[k] = (double)scales[m * (K / 32) + k / 32] * (double)codes[m * K + k];
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0, ab = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double term = a[k] * (double)W[n * K + k];
+                acc += term;
+                ab += fabs(term);
+            }
+            y[m * N + n] = acc;
+            if (den) den[m * N + n] = ab;
+        }
+    }
+    free(codes);
+    free(scales);
+    free(a);
+}
+
 /* SwiGLU of the gate/up projection read as one ("Qwen3.8-27B on one Tenstorrent
  * P150", "4. Measuring the ceiling, and lots of dead ends": the MLP gate/up
  * projection and its fused SwiGLU; "A 320B MoE on a free Kaggle TPU": the gate

@@ -109,6 +109,12 @@ void or_quant_act_nvfp4(const uint16_t* x_bf16, int64_t M, int64_t K, float x_sc
 void or_w4a4_f64(const uint16_t* x_bf16, int64_t M, int64_t K, float x_scale, const float* W, int64_t N,
                  double* y, double* den);
 
+/* int8-dot lever: x quantized to int8 per 32 values (d = amax / 127, q = rint(x / d));
+ * y = sum_k W[n][k] d q_k in fp64 against BlockToFloat W [N][K]; den = sum |terms| */
+void or_quant_act_q8(const uint16_t* x_bf16, int64_t M, int64_t K, int8_t* codes, float* scales);
+void or_int8dot_f64(const uint16_t* x_bf16, int64_t M, int64_t K, const float* W, int64_t N, double* y,
+                    double* den);
+
 /* SwiGLU: h = silu(g) * u, silu(g) = g / (1 + exp(-g)), fp64 elementwise */
 void or_swiglu_f64(const double* g, const double* u, int64_t n, double* h);
 

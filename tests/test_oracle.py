@@ -929,6 +929,64 @@ def _bf16_bits_of(vals):
     return synth.bf16_bits(torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).reshape(1, -1))
 
 
+def _bf16_of(vals):
+    return torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_quant_act_q8_handbuilt():
+    """Block 0: amax = 127/16 = 7.9375, so d = 1/16 exactly and on-grid values give their
+    own codes; x/d = 2.5 and 3.5 round to the even 2 and 4; -127/16 gives -127. Block 1
+    is all zero: d = 0 and every code 0."""
+    k = [127, -127, 0, 1, -1, 64, -64, 100] + [3] * 24
+    vals = [v / 16 for v in k]
+    vals[8], vals[9] = 2.5 / 16, 3.5 / 16
+    x = np.concatenate([_bf16_of(vals), _bf16_of([0.0] * 32)])[None, :]
+    codes, scales = oracle.quant_act_q8(x)
+    assert scales[0, 0] == 0.0625 and scales[0, 1] == 0.0
+    assert list(codes[0, :10]) == [127, -127, 0, 1, -1, 64, -64, 100, 2, 4]
+    assert np.all(codes[0, 10:32] == 3) and np.all(codes[0, 32:] == 0)
+
+
+def test_quant_act_q8_roundtrip_bound():
+    x = synth.bf16_bits(synth.activations(8, 3, 1024))
+    codes, scales = oracle.quant_act_q8(x)
+    xf = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(3, 32, 32)
+    d = scales.astype(np.float64)[:, :, None]
+    err = np.abs(xf - d * codes.astype(np.float64).reshape(3, 32, 32))
+    # half a step, plus the fp32 rounding of x / d (|x / d| <= 127) that decides a near-tie
+    assert np.all(err <= d * (0.5 + 128 * 2.0**-24) + 1e-30)
+    assert np.all(np.abs(codes).reshape(3, 32, 32).max(-1) == 127)      # the block's largest reaches 127
+
+
+def test_int8dot_on_grid_reduces_to_gemv():
+    """Activations that are exact multiples of their block's d (amax = 127 d) quantize
+    without error, so the int8-dot reference equals the plain GEMV on the same x."""
+    rng = np.random.default_rng(5)
+    q = rng.integers(-127, 128, size=(2, 256))
+    q[:, ::32] = 127
+    x = _bf16_of((q / 16.0).reshape(-1).tolist()).reshape(2, 256)
+    W = synth.weights(6, 40, 256).numpy()
+    y1, d1 = oracle.int8dot_f64(W, x)
+    y2, d2 = oracle.gemv_f64(W, x)
+    assert np.array_equal(y1, y2) and np.array_equal(d1, d2)
+
+
+def test_int8dot_handbuilt_literal():
+    """W = one row of 32 ones and 32 twos; x block 0 = 127/16 everywhere (d = 1/16, codes
+    127), block 1 = -127/8 (d = 1/8, codes -127): y = 32 * 7.9375 - 2 * 32 * 15.875 =
+    254 - 1016 = -762, and sum |terms| = 1270."""
+    x = np.concatenate([_bf16_of([127 / 16] * 32), _bf16_of([-127 / 8] * 32)])[None, :]
+    W = np.array([[1.0] * 32 + [2.0] * 32], dtype=np.float32)
+    y, den = oracle.int8dot_f64(W, x)
+    assert y[0, 0] == -762.0 and den[0, 0] == 1270.0
+    # off the grid: x = (127/16, 1.5/16, 0, ...): d = 1/16, 1.5 rounds to 2, so the second
+    # element enters as 2/16 = 0.125, not as its own 0.09375
+    x2 = _bf16_of([127 / 16, 1.5 / 16] + [0.0] * 30)[None, :]
+    W2 = np.array([[0.0, 1.0] + [0.0] * 30], dtype=np.float32)
+    y2, _ = oracle.int8dot_f64(W2, x2)
+    assert y2[0, 0] == 0.125
+
+
 def test_w4a4_handbuilt_literal():
     """One token, two 16-value blocks, x_scale = 1. Block 0 has amax 6 -> block scale
     1.0; 2.59375 (bf16 of 2.6) rounds to the E2M1 value 3. Block 1 has amax 12 -> block

@@ -76,6 +76,12 @@ MUTANTS = [
      "int q = (blk[8 + e / 2] >> (4 * (1 - (e & 1)))) & 15;\n                float a = d * (float)(ls"),
     ("iq4_xs sub-blocks of 16", "                int j = e / 32;\n                int ls = ((blk[4",
      "                int j = (e / 16) & 7;\n                int ls = ((blk[4"),
+    ("int8-dot scale over 128", "float d = amax / 127.0f;\n            scales[m * (K / 32) + b] = d;",
+     "float d = amax / 128.0f;\n            scales[m * (K / 32) + b] = d;"),
+    ("int8-dot codes truncated", "(int)clampf(rintf(xv[i] / d), -127.0f, 127.0f)",
+     "(int)clampf(xv[i] / d, -127.0f, 127.0f)"),
+    ("int8-dot raw activations", "for (int64_t k = 0; k < K; k++) a[k] = (double)scales[m * (K / 32) + k / 32] * (double)codes[m * K + k];",
+     "for (int64_t k = 0; k < K; k++) a[k] = (double)or_bf16_to_f32(x_bf16[m * K + k]) + 0.0 * codes[0];"),
     ("iq3_s index bit 8 from the next group",
      "idx = blk[2 + g] | (((blk[66 + g / 8] >> (g & 7)) & 1) << 8);",
      "idx = blk[2 + g] | (((blk[66 + (g + 1) % 64 / 8] >> ((g + 1) & 7)) & 1) << 8);"),
