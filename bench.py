@@ -137,6 +137,20 @@ WORKLOADS = {
                                                   ("down", QWEN_HIDDEN, QWEN_MLP)],
                          desc="IQ4_XS codebook GEMV at the Qwen3.8-27B MLP shapes (gate, up [17408,5120], "
                               "down [5120,17408]), M=1"),
+    "q4k_int8dot_mlp_m1": dict(fmt="q4_k", M=1, int8dot=True,
+                               mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
+                                     ("down", QWEN_HIDDEN, QWEN_MLP)],
+                               desc="Q4_K int8-dot decode MLP (x quantized to int8 per 32 values, dp4a), "
+                                    "Qwen3.8-27B geometry: gate+up [17408,5120], down [5120,17408], M=1"),
+    "q4k_int8dot_mlp_m8": dict(fmt="q4_k", M=8, int8dot=True,
+                               mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
+                                     ("down", QWEN_HIDDEN, QWEN_MLP)],
+                               desc="Q4_K int8-dot decode MLP, Qwen3.8-27B geometry, M=8"),
+    "q8_0_int8dot_mlp_m1": dict(fmt="q8_0", M=1, int8dot=True,
+                                mats=[("gate", QWEN_MLP, QWEN_HIDDEN), ("up", QWEN_MLP, QWEN_HIDDEN),
+                                      ("down", QWEN_HIDDEN, QWEN_MLP)],
+                                desc="Q8_0 int8-dot decode MLP (int8 weight codes x int8 activation codes, "
+                                     "dp4a), Qwen3.8-27B geometry, M=1"),
 }
 DEFAULT_WORKLOAD = "q4k_mlp_m1"
 DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, "q6k_head_m8": 2000,
@@ -146,7 +160,8 @@ DEFAULT_STEPS = {"q4k_mlp_m1": 20000, "q4k_mlp_m8": 20000, "q6k_head_m1": 2000, 
                  "q4k_mlp_fused_m1": 20000, "q4k_mlp_layer_m1": 20000, "q4k_mlp_layer_m8": 20000, "q5k_mlp_m1": 20000, "q5k_mlp_m8": 20000,
                  "tower_fused_m1": 20000, "tower_fused_m8": 5000, "q4k_prefill_m512": 2000,
                  "q5k_prefill_m512": 2000, "q6k_prefill_m512": 2000, "iq4xs_tower_down_m1": 20000, "iq4xs_tower_down_m8": 5000,
-                 "iq4xs_mlp_m1": 20000, "iq2s_tower_gateup_m1": 20000, "iq3s_tower_down_m1": 20000}
+                 "iq4xs_mlp_m1": 20000, "iq2s_tower_gateup_m1": 20000, "iq3s_tower_down_m1": 20000,
+                 "q4k_int8dot_mlp_m1": 20000, "q4k_int8dot_mlp_m8": 20000, "q8_0_int8dot_mlp_m1": 10000}
 
 METRIC = "effective weight-stream GB/s and % of HBM peak for M=1 quantized GEMV"
 CANON_PER_VALUE = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q5_k": 176 / 256, "q6_k": 210 / 256,
@@ -202,6 +217,8 @@ def kernel_unit(workload):
     w = WORKLOADS[workload]
     if w.get("w4a4"):
         return "qmv_w4a4.cu"
+    if w.get("int8dot"):
+        return "qmv_int8.cu"
     return "qmv_kq.cu" if w.get("kquant") else "qmv_stream.cu"
 
 
@@ -365,6 +382,7 @@ class DeviceWorkload:
         self.tower = w.get("tower", False)
         self.w4a4 = w.get("w4a4", False)
         self.kquant = w.get("kquant", False)
+        self.int8dot = w.get("int8dot", False)  # x quantized to int8 per 32 values (qmv_gemv_int8dot)
         self.fused = w.get("fused", False)
         self.layer = w.get("layer", False)      # the MLP layer in one launch (qmv_mlp_layer)
         self.E = w.get("E", 1)
@@ -396,6 +414,8 @@ class DeviceWorkload:
             entry = q.QMV_ENTRY_GROUPED if self.tower else (q.QMV_ENTRY_W4A4 if self.w4a4 else q.QMV_ENTRY_GEMV)
             if self.kquant:
                 entry = q.QMV_ENTRY_KQUANT
+            if self.int8dot:
+                entry = q.QMV_ENTRY_INT8DOT
             if self.fused and i == 0:
                 entry = q.QMV_ENTRY_GROUPED_SWIGLU if self.tower else q.QMV_ENTRY_SWIGLU
             if self.layer:
@@ -413,7 +433,8 @@ class DeviceWorkload:
                 self.ids.append(torch.from_numpy(ids).to(dev))
                 self.unique.append(len(np.unique(ids)))
         # W4A4 runs the activation quantizer and the GEMM per matrix
-        self.launches_per_step = 1 if self.layer else len(self.mats) * (2 if (self.w4a4 or self.kquant) else 1)
+        self.launches_per_step = 1 if self.layer else len(self.mats) * (2 if (self.w4a4 or self.kquant or
+                                                                              self.int8dot) else 1)
 
     def pair_x(self, i):
         """Tower matrices whose x has one row per (token, slot): the down projection
@@ -457,6 +478,8 @@ class DeviceWorkload:
                 q.qmv_gemv_swiglu(self.fmt, self.packed[c][i], self.x[i], N, K, self.ws[i], h=self.y[i])
             elif self.kquant:
                 q.qmv_gemm_kquant(self.fmt, self.packed[c][i], self.x[i], N, K, self.ws[i], y=self.y[i])
+            elif self.int8dot:
+                q.qmv_gemv_int8dot(self.fmt, self.packed[c][i], self.x[i], N, K, self.ws[i], y=self.y[i])
             elif self.w4a4:
                 q.qmv_gemm_nvfp4_w4a4(self.packed[c][i], self.x[i], self.x_scale[i], N, K, self.ws[i], y=self.y[i])
             else:
@@ -541,6 +564,10 @@ def run_device(args, rank, world, dev):
     achieved = (bytes_per_step / wl.launches_per_step) / avg_launch_s / 1e9
     peak, peak_kind = measured_peaks()
     traffic = recorded_traffic(args.workload)
+    if wl.int8dot:
+        # one unit per matrix: the x quantizer (a few KB) and the GEMV it feeds
+        avg_launch_s = (ms * 1e-3) / (K * len(wl.mats))
+        achieved = (bytes_per_step / len(wl.mats)) / avg_launch_s / 1e9
     if wl.w4a4 or wl.kquant:
         # a dense contraction: TFLOP/s against the tensor roofline; each matrix's
         # time includes its activation quantizer (the GEMM's share is in profiles/)
@@ -610,7 +637,8 @@ def run_device(args, rank, world, dev):
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
             "avg_launch_us": round(avg_launch_s * 1e6, 3),
-            "algorithmic_bytes_per_launch": int(bytes_per_step / wl.launches_per_step),
+            "algorithmic_bytes_per_launch": int(bytes_per_step / (len(wl.mats) if wl.int8dot
+                                                                  else wl.launches_per_step)),
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
@@ -649,6 +677,11 @@ def run_device(args, rank, world, dev):
         del result["roofline"]["algorithmic_bytes_per_launch"]
         result["e2e"]["unit"] = "TFLOP/s"
         result["e2e"]["value"] = round(wl.step_flops() * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, 2)
+    if wl.int8dot:
+        result["dtype"] = "int8 (weight codes x int8 activation codes, int32 dp4a, fp32 scaling)"
+        result["details"]["arithmetic"] = ("x quantized to int8 per 32 values (d = amax/127); dp4a int32 dots "
+                                           "of the weight codes, scaled in fp32 by the block scales and d")
+        result["roofline"]["kernel"] = f"qmv::int8dot_kernel<{wl.fmt}, M={wl.M}> (+ its x quantizer)"
     if wl.tower:
         result["details"]["unique_experts_mean"] = round(float(np.mean(wl.unique)), 2)
     return result
@@ -670,7 +703,7 @@ def oracle_sample(workload, rows_per_mat):
         table = codebook_of(100 + i, 0) if fmt == "iq4_xs" else (grid_of(fmt, 100 + i) if fmt in GRIDS else None)
         canon = oracle.encode(fmt, W, NVFP4_TS if fmt == "nvfp4" else 0.0, codebook=table)
         x = synth.bf16_bits(synth.activations(200 + i, w["M"], K))
-        items.append((fmt, canon, r, K, x))
+        items.append((fmt, canon, r, K, x, bool(w.get("int8dot"))))
     return items
 
 
@@ -721,9 +754,9 @@ def time_oracle(items, min_seconds):
     done_bytes, done_flops, reps = 0, 0, 0
     t0 = time.perf_counter()
     while True:
-        for fmt, canon, r, K, x in items:
+        for fmt, canon, r, K, x, int8 in items:
             D = oracle.block_to_float(fmt, canon, r, K)
-            oracle.gemv_f64(D, x)
+            (oracle.int8dot_f64 if int8 else oracle.gemv_f64)(D, x)
             done_bytes += canon.size + x.size * 2 + r * x.shape[0] * 4
             done_flops += 2 * r * K * x.shape[0]
         reps += 1
@@ -760,13 +793,13 @@ def run_reference(args):
     items = oracle_sample(args.workload, [rows] * len(w["mats"]))
     import oracle
     for _ in range(W):
-        for fmt, canon, r, K_, x in items:
-            oracle.gemv_f64(oracle.block_to_float(fmt, canon, r, K_), x)
+        for fmt, canon, r, K_, x, int8 in items:
+            (oracle.int8dot_f64 if int8 else oracle.gemv_f64)(oracle.block_to_float(fmt, canon, r, K_), x)
     nbytes, nflops = 0, 0
     t0 = time.perf_counter()
     for _ in range(K):
-        for fmt, canon, r, K_, x in items:
-            oracle.gemv_f64(oracle.block_to_float(fmt, canon, r, K_), x)
+        for fmt, canon, r, K_, x, int8 in items:
+            (oracle.int8dot_f64 if int8 else oracle.gemv_f64)(oracle.block_to_float(fmt, canon, r, K_), x)
             nbytes += canon.size + x.size * 2 + r * x.shape[0] * 4
             nflops += 2 * r * K_ * x.shape[0]
     secs = time.perf_counter() - t0

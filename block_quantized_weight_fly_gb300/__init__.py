@@ -23,7 +23,7 @@ FORMATS = {"q8_0": QMV_Q8_0, "q4_k": QMV_Q4_K, "q6_k": QMV_Q6_K, "nvfp4": QMV_NV
            "iq2_s": QMV_IQ2_S}
 GRID_BYTES = {"iq3_s": 512 * 4, "iq2_s": 1024 * 8}
 QMV_ENTRY_GEMV, QMV_ENTRY_GROUPED, QMV_ENTRY_W4A4, QMV_ENTRY_SWIGLU = 1, 2, 3, 4
-QMV_ENTRY_GROUPED_SWIGLU, QMV_ENTRY_KQUANT, QMV_ENTRY_MLP_LAYER = 5, 6, 7
+QMV_ENTRY_GROUPED_SWIGLU, QMV_ENTRY_KQUANT, QMV_ENTRY_MLP_LAYER, QMV_ENTRY_INT8DOT = 5, 6, 7, 8
 QMV_MAX_M = 8
 
 STATUS = {0: "QMV_OK", 1: "QMV_EINVAL", 2: "QMV_EALIGN", 3: "QMV_EUNSUPPORTED", 4: "QMV_ECUDA",
@@ -71,6 +71,7 @@ _grouped_swiglu = _sig("qmv_grouped_swiglu", _I, [_I, _P, _P, _P, _P, _I, _I, _I
 _quant_act = _sig("qmv_quant_act_nvfp4", _I, [_P, _F, _P, _P, _I, _I64, _P])
 _w4a4 = _sig("qmv_gemm_nvfp4_w4a4", _I, [_P, _P, _F, _P, _I, _I64, _I64, _P, _SZ, _P])
 _kquant = _sig("qmv_gemm_kquant", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
+_int8dot = _sig("qmv_gemv_int8dot", _I, [_I, _P, _P, _P, _I, _I64, _I64, _P, _SZ, _P])
 _status_str = _sig("qmv_status_str", ctypes.c_char_p, [_I])
 _last_route = _sig("qmv_last_route", _I, [])
 _dev_status = _sig("qmv_device_status", _I, [_I])
@@ -80,7 +81,7 @@ EXPORTED = ["qmv_canon_size", "qmv_pack_size", "qmv_pack", "qmv_quantize", "qmv_
             "qmv_workspace_size", "qmv_gemv", "qmv_grouped", "qmv_quant_act_nvfp4",
             "qmv_gemm_nvfp4_w4a4", "qmv_status_str", "qmv_last_route", "qmv_device_status",
             "qmv_gemv_noalloc", "qmv_gemv_swiglu", "qmv_grouped_swiglu", "qmv_gemm_kquant",
-            "qmv_debug_split_k_fault", "qmv_quantize_codebook", "qmv_mlp_layer"]
+            "qmv_debug_split_k_fault", "qmv_quantize_codebook", "qmv_mlp_layer", "qmv_gemv_int8dot"]
 
 
 def _fmt(fmt) -> int:
@@ -384,4 +385,15 @@ def qmv_gemm_kquant(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int
     y = _out(y, (M, N), x.device, "y")
     _check(_kquant(_fmt(fmt), _ptr(packed_W), _ptr(x), _ptr(y), M, N, K, _ptr(ws), ws.numel(), _stream(stream)),
            "qmv_gemm_kquant")
+    return y
+
+
+def qmv_gemv_int8dot(fmt, packed_W: torch.Tensor, x: torch.Tensor, N: int, K: int, ws: torch.Tensor,
+                     y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = q8(x) . W^T: x quantized to int8 per 32 values, integer dots (Q8_0, Q4_K; M <= 8)."""
+    _dev(packed_W, "packed_W"); _dev(x, "x"); _dev(ws, "ws")
+    x, M = _act(x, K)
+    y = _out(y, (M, N), x.device, "y")
+    _check(_int8dot(_fmt(fmt), _ptr(packed_W), _ptr(x), _ptr(y), M, N, K, _ptr(ws), ws.numel(), _stream(stream)),
+           "qmv_gemv_int8dot")
     return y

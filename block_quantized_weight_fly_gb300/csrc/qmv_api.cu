@@ -142,6 +142,11 @@ qmv_status qmv_dequant(qmv_fmt fmt, const void* packed, int64_t N, int64_t K, in
 
 size_t qmv_workspace_size(int entry, qmv_fmt fmt, int M, int64_t N, int64_t K, int64_t E, int topk) {
   if (!valid_fmt(fmt) || M <= 0 || N <= 0 || K <= 0) return 0;
+  if (entry == QMV_ENTRY_INT8DOT) {          // independent of the device
+    Layout L;
+    if ((fmt != QMV_Q8_0 && fmt != QMV_Q4_K) || M > QMV_MAX_M || !make_layout((int)fmt, N, K, 1, &L)) return 0;
+    return (size_t)int8dot_workspace_bytes(M, K);
+  }
   const int sms = num_sms_current_device();
   if (sms <= 0) return 0;
   if (entry == QMV_ENTRY_GEMV || entry == QMV_ENTRY_SWIGLU) {
@@ -394,6 +399,24 @@ qmv_status qmv_gemm_nvfp4_w4a4(const void* packed_W, const uint16_t* x, float x_
   st = from_cuda(launch_w4a4(L, static_cast<const uint8_t*>(packed_W), planes, partials, x_scale, y, M, m_pad,
                              status, stream));
   if (st == QMV_OK) g_last_route = QMV_NVFP4 * 100 + 4;
+  return st;
+}
+
+qmv_status qmv_gemv_int8dot(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y, int M, int64_t N,
+                            int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_fmt(fmt) || !packed_W || !x || !y || !ws) return QMV_EINVAL;
+  if (M < 1 || M > QMV_MAX_M || N <= 0 || K <= 0) return QMV_EINVAL;
+  if (fmt != QMV_Q8_0 && fmt != QMV_Q4_K) return QMV_EUNSUPPORTED;
+  Layout L;
+  if (!make_layout((int)fmt, N, K, 1, &L)) return QMV_EUNSUPPORTED;
+  if ((N + 7) / 8 >= ((int64_t)1 << 31)) return QMV_EUNSUPPORTED;
+  if (!aligned(packed_W, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
+  if (ws_bytes < (size_t)int8dot_workspace_bytes(M, K)) return QMV_EWORKSPACE;
+  unsigned* status = status_ptr();
+  if (!status) return QMV_ECUDA;
+  qmv_status st = from_cuda(launch_int8dot(L, static_cast<const uint8_t*>(packed_W), x, y, M,
+                                           static_cast<uint8_t*>(ws), status, stream));
+  if (st == QMV_OK) g_last_route = (int)fmt * 100 + 13;
   return st;
 }
 

@@ -86,6 +86,11 @@ int64_t w4a4_partials_bytes(int sms);
 cudaError_t launch_kq(const Layout& L, const uint8_t* packed, const uint16_t* x, float* y, int M, uint8_t* ws,
                       unsigned* status, cudaStream_t s);
 int64_t kq_workspace_bytes(int64_t m_pad, int64_t K, int sms);
+// int8-dot GEMV (Q8_0, Q4_K; M <= 8): x quantized to int8 per 32 values into ws, then
+// one warp per weight row with dp4a. ws: [codes: M*K, 256-aligned][scales: M*(K/32)*4]
+cudaError_t launch_int8dot(const Layout& L, const uint8_t* packed, const uint16_t* x, float* y, int M, uint8_t* ws,
+                           unsigned* status, cudaStream_t s);
+int64_t int8dot_workspace_bytes(int M, int64_t K);
 // returns the route variant launched (1 = M=1, 2 = M>1, 3 = grouped, 9 = fused gate|up SwiGLU)
 cudaError_t launch_stream(const StreamArgs& a, cudaStream_t s, int* variant);
 // The MLP layer in one launch (layer_kernel): a1 = the fused gate|up pass (its y = h,

@@ -103,7 +103,8 @@ enum {
   QMV_ENTRY_SWIGLU = 4,
   QMV_ENTRY_GROUPED_SWIGLU = 5,
   QMV_ENTRY_KQUANT = 6,
-  QMV_ENTRY_MLP_LAYER = 7
+  QMV_ENTRY_MLP_LAYER = 7,
+  QMV_ENTRY_INT8DOT = 8
 };
 
 /* Largest decode batch served by qmv_gemv / qmv_grouped (M rows of x). */
@@ -347,13 +348,34 @@ qmv_status qmv_gemm_nvfp4_w4a4(const void* packed_W, const uint16_t* x, float x_
 qmv_status qmv_gemm_kquant(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y, int M,
                            int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* The int8-dot decode GEMV (the lever the keep-quant issue books as the repayment of
+ * its slow decode: "feat(BACKEND-TENSTORRENT-KEEPQUANT) ...", "Scope", its "Out of
+ * scope" line and the accepted-cost note). x is quantized to int8 per 32-value block,
+ * d = amax / 127 (fp32, round to nearest) and q = clamp(rint(x / d), -127, 127), all
+ * zero when d = 0; then y[m][n] = sum over blocks of the weight block's scale(s) times d
+ * times the int32 dot of the weight codes with q (Q4_K: d sc_j dx sum(q x_q) -
+ * dmin m_j dx sum(x_q)), the products in int32 (dp4a), the rest in fp32. The result
+ * is the GEMV of the quantized x, not of x: it differs from qmv_gemv by x's int8
+ * rounding (up to d/2 per value). fmt: QMV_Q8_0 or QMV_Q4_K (others return
+ * QMV_EUNSUPPORTED). packed_W: the device layout of one [N, K] matrix (qmv_pack).
+ * x: device bf16 [M][K], 16-byte aligned, M = 1 .. QMV_MAX_M. y: device fp32 [M][N],
+ * fully overwritten. ws: device, qmv_workspace_size(QMV_ENTRY_INT8DOT, fmt, M, N, K,
+ * 1, 1) bytes, 256-byte aligned: x's int8 codes [M][K], then the block scales
+ * [M][K/32] (fp32), both rewritten by every call, so no zero-fill is needed; calls
+ * sharing a workspace must not overlap. Launches two kernels (the quantizer, then the
+ * GEMV, chained by programmatic dependent launch); a header that disagrees with the
+ * arguments latches QMV_EHEADER in the device status and leaves y unwritten. */
+qmv_status qmv_gemv_int8dot(qmv_fmt fmt, const void* packed_W, const uint16_t* x, float* y, int M,
+                            int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status. */
 const char* qmv_status_str(qmv_status s);
 
 /* Route id of the kernel the last successful call on this host thread launched:
  * format * 100 + variant (1 = M=1 streaming CUDA-core GEMV, 2 = M>1 streaming
  * mma.sync GEMV, 3 = grouped, 4 = W4A4 tcgen05, 5 = dequant, 6 = pack,
- * 7 = quantize, 8 = activation quantizer, 9 = fused gate|up SwiGLU). Test hook. */
+ * 7 = quantize, 8 = activation quantizer, 9 = fused gate|up SwiGLU, 11 = K-quant
+ * prefill, 12 = MLP layer, 13 = int8-dot GEMV). Test hook. */
 int qmv_last_route(void);
 
 /* Test hook for the split-K reduction of qmv_gemv, qmv_grouped and their SwiGLU and

@@ -108,6 +108,19 @@ def test_host_validation_new_entries(lib):
     assert kq(2, one, one, one, 512, 128, 300, one, 1 << 20, None) == 3              # K % 256
     assert kq(6, one, one, one, 512, 128, 300, one, 1 << 20, None) == 3
     assert kq(2, one, P(264), one, 512, 128, 256, one, 1 << 20, None) == 2           # x alignment
+    i8 = q._int8dot              # fmt, W, x, y, M, N, K, ws, ws_bytes, stream
+    assert i8(2, None, one, one, 1, 128, 256, one, 1 << 20, None) == 1
+    assert i8(2, one, one, one, 0, 128, 256, one, 1 << 20, None) == 1                # M = 0
+    assert i8(2, one, one, one, 9, 128, 256, one, 1 << 20, None) == 1                # M > 8
+    assert i8(99, one, one, one, 1, 128, 256, one, 1 << 20, None) == 1               # not a format
+    for fmt in (3, 4, 5, 6, 7, 8, 9):                                                # Q8_0 and Q4_K only
+        assert i8(fmt, one, one, one, 1, 128, 256, one, 1 << 20, None) == 3
+    assert i8(1, one, one, one, 1, 128, 48, one, 1 << 20, None) == 3                 # K % 32
+    assert i8(2, one, one, one, 1, 128, 288, one, 1 << 20, None) == 3                # K % 256
+    assert i8(2, P(257), one, one, 1, 128, 256, one, 1 << 20, None) == 2             # W alignment
+    assert i8(1, one, one, one, 2, 128, 256, one, 511, None) == 8                    # workspace too small
+    assert q.qmv_workspace_size(q.QMV_ENTRY_INT8DOT, "q4_k", 3, 128, 5120) == 15360 + 2048
+    assert q.qmv_workspace_size(q.QMV_ENTRY_INT8DOT, "q6_k", 1, 128, 5120) == 0
 
 
 def test_host_validation_remaining_entries(lib):

@@ -29,6 +29,8 @@ def test_every_workload_maps_to_a_kernel_source(bench):
             assert unit == "qmv_w4a4.cu"
         elif w.get("kquant"):
             assert unit == "qmv_kq.cu"
+        elif w.get("int8dot"):
+            assert unit == "qmv_int8.cu"
         else:
             assert unit == "qmv_stream.cu"
 
@@ -87,7 +89,11 @@ def test_committed_records_name_known_workloads(bench):
         assert name in bench.WORKLOADS, name
         assert rec["dram_bytes_per_launch"] > 0
         assert len(rec["kernel_hash"]) == 16
-        assert rec["source"].startswith("ncu ") and "--clock-control none" in rec["source"]
+        # the full command: the plain run, then the same command under ncu
+        src = rec["source"]
+        assert " && ncu " in src and "--clock-control none" in src, src
+        plain, profiled = src.split(" && ", 1)
+        assert plain.startswith("python bench.py ") and plain.split(" > ")[0] in profiled
 
 
 def test_clock_summary_parses_nvidia_smi_lines(bench):
