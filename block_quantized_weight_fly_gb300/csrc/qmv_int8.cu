@@ -7,10 +7,17 @@
 // note). Served for Q8_0 and Q4_K (w = d sc q - dmin m: the min term takes the sum of
 // the block's x codes), reading the same packed layout as the mma.sync GEMV.
 //
-// Two launches: the activation quantizer (one thread per 32-value block, fp32 ops
-// rounded one at a time, bit-exact with the oracle), then the GEMV: one warp per
-// weight row, all M rows of x, the lanes of a warp on the eight 32-value chunks of a
-// k-group (four lanes per chunk, eight values each), every weight byte read once.
+// Two launches, chained by programmatic dependent launch:
+//  - the activation quantizer: one thread per 32-value block, fp32 operations rounded
+//    one at a time (bit-exact with the oracle). Codes go to the workspace in the order
+//    the weight words hold their elements, so that the GEMV needs no byte shuffle:
+//    each 8-value slice of a block is one 8-byte word pair, Q8_0 in element order,
+//    Q4_K as the nibble order of a packed Q4_K word (low nibbles: elements 0, 4, 1, 5;
+//    high nibbles: 2, 6, 3, 7 of the slice);
+//  - the GEMV: one warp per weight row, all M rows of x. A k-group's record is read
+//    with one 16-byte load per lane (Q4_K: 8 lanes per group, 4 groups per warp step;
+//    Q8_0: 16 lanes, 2 groups), so a warp has several k-groups' bytes in flight.
+//    Lane sums are joined by a fixed butterfly at the end (the same for every M).
 #include "qmv_internal.h"
 
 namespace qmv {
@@ -23,7 +30,17 @@ __device__ __forceinline__ int dp4a_s8(uint32_t a, uint32_t b, int c) {
   return r;
 }
 
-// x (bf16 [M][K]) -> int8 codes [M][K] and fp32 block scales [M][K/32]
+__device__ __forceinline__ uint4 ldg128(const uint8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+// byte position, within its 8-value slice, of element p of the slice
+template <int FMT>
+__device__ __forceinline__ int slice_pos(int p) {
+  if constexpr (FMT == F_Q4_K) return ((p & 1) << 1 | (p >> 2)) + (((p >> 1) & 1) << 2);
+  return p;
+}
+
+// x (bf16 [M][K]) -> int8 codes [M][K] (slice order above) and fp32 block scales [M][K/32]
+template <int FMT>
 __global__ void quant_q8_kernel(const uint16_t* __restrict__ x, int64_t nblk, int8_t* __restrict__ codes,
                                 float* __restrict__ scales) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -53,7 +70,8 @@ __global__ void quant_q8_kernel(const uint16_t* __restrict__ x, int64_t nblk, in
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const int q = (d == 0.0f) ? 0 : (int)fminf(fmaxf(rintf(__fdiv_rn(xv[i], d)), -127.0f), 127.0f);
-    out[i >> 2] |= ((uint32_t)q & 0xFFu) << (8 * (i & 3));
+    const int pos = 8 * (i >> 3) + slice_pos<FMT>(i & 7);
+    out[pos >> 2] |= ((uint32_t)q & 0xFFu) << (8 * (pos & 3));
   }
   uint4* dst = reinterpret_cast<uint4*>(codes + b * 32);
   dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
@@ -61,21 +79,30 @@ __global__ void quant_q8_kernel(const uint16_t* __restrict__ x, int64_t nblk, in
   scales[b] = d;
 }
 
-// Q8_0 packed word pair of thread t, chunk j (elements 8t..8t+7) -> the eight signed codes
-// in element order. In a packed word the low nibbles of elements (0, 1) sit at nibbles
-// (0, 4), of (2, 3) at (1, 5), the high nibbles at (2, 6) and (3, 7) (codes XOR 0x80):
-// A = w & 0x0F0F0F0F holds lo(e0), hi(e0), lo(e1), hi(e1) in its bytes, B = w >> 4 the same
-// for e2, e3; byte 0 of A | A >> 4 is then e0's code, byte 2 e1's.
+// Q8_0 packed word (elements 4i .. 4i+3 of a slice, offset-binary nibbles) -> the four
+// signed codes in element order. In a packed word the low nibbles of elements (0, 1)
+// sit at nibbles (0, 4), of (2, 3) at (1, 5), the high nibbles at (2, 6) and (3, 7):
+// A = w & 0x0F0F0F0F holds lo(e0), hi(e0), lo(e1), hi(e1) in its bytes, B = w >> 4 the
+// same for e2, e3; byte 0 of A | A >> 4 is then e0's offset code, byte 2 e1's.
 __device__ __forceinline__ uint32_t q80_codes4(uint32_t w) {
   const uint32_t a = w & 0x0F0F0F0Fu, b = (w >> 4) & 0x0F0F0F0Fu;
   const uint32_t ca = a | (a >> 4), cb = b | (b >> 4);
   return __byte_perm(ca, cb, 0x6420) ^ 0x80808080u;
 }
 
-// One warp per weight row n (all MT rows of x): lanes (j, t) = (lane / 4, lane % 4) take
-// the eight values 8t..8t+7 of chunk j of every k-group.
+// exact int -> fp32 for |v| < 2^22 (one integer add and one subtraction of 1.5 x 2^23)
+__device__ __forceinline__ float i2f_small(int v) { return __int_as_float(v + 0x4B400000) - 12582912.0f; }
+__device__ __forceinline__ float u6f(uint32_t v) { return __uint_as_float((v & 63u) | 0x4B000000u) - 8388608.0f; }
+
+// One warp per weight row n (all MT rows of x). Lane l takes k-group slot l / LPG of
+// each warp step (LPG lanes per group) and 16-byte piece p = l % LPG of that group's
+// record:
+//   Q4_K (LPG 8): bytes 16 + 16p = word t = p / 2 of chunks j0 .. j0+3, j0 = 4 (p % 2)
+//     (elements 8t .. 8t+7 of each chunk); the 16-byte header by every lane;
+//   Q8_0 (LPG 16): bytes 16 + 16p = words 2t, 2t+1 (t = p / 4) of chunks j0, j0+1,
+//     j0 = 2 (p % 4); their fp16 d from header bytes 4 (p % 4).
 template <int FMT, int MT>
-__global__ void __launch_bounds__(256, 4) int8dot_kernel(Layout L, const uint8_t* __restrict__ packed,
+__global__ void __launch_bounds__(256) int8dot_kernel(Layout L, const uint8_t* __restrict__ packed,
                                                       const int8_t* __restrict__ codes,
                                                       const float* __restrict__ xsc, float* __restrict__ y,
                                                       int M, unsigned* status) {
@@ -90,64 +117,81 @@ __global__ void __launch_bounds__(256, 4) int8dot_kernel(Layout L, const uint8_t
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");      // the quantized x of the pre-pass
   if (n >= L.N) return;
-  const int j = lane >> 2, t = lane & 3;
+  constexpr int LPG = (FMT == F_Q4_K) ? 8 : 16;
+  constexpr int GPS = 32 / LPG;                           // k-groups per warp step
+  const int gs = lane / LPG, p = lane % LPG;
   float acc[MT];
 #pragma unroll
   for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-  const int64_t G = L.k_groups;
-#pragma unroll 4
-  for (int64_t g = 0; g < G; ++g) {
-    const uint8_t* rec = packed + L.base + g * L.group_bytes + n * L.rec;
-    const int64_t kx = g * 256 + 32 * j + 8 * t;           // first of this lane's 8 values
-    if constexpr (FMT == F_Q8_0) {
-      if (kx >= L.K) continue;                             // the chunks past K in a ragged last group
-      const uint2 w = *reinterpret_cast<const uint2*>(rec + q80_word_off(t, j));
-      const float dw = h2f(*reinterpret_cast<const uint16_t*>(rec + 2 * j));
-      const uint32_t c0 = q80_codes4(w.x), c1 = q80_codes4(w.y);
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        if (m >= M) break;
-        const uint2 xq = *reinterpret_cast<const uint2*>(codes + (int64_t)m * L.K + kx);
-        const int s = dp4a_s8(c1, xq.y, dp4a_s8(c0, xq.x, 0));
-        const float dx = xsc[(int64_t)m * (L.K / 32) + kx / 32];
-        acc[m] = __fmaf_rn(__fmul_rn(dw, dx), (float)s, acc[m]);
-      }
-    } else {   // Q4_K
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + q4k_word_off(t, j));
-      const uint4 hd = *reinterpret_cast<const uint4*>(rec);
+  const int64_t G = L.k_groups, KB = L.K / 32;
+  const uint8_t* rec0 = packed + L.base + n * L.rec;
+  // one warp step: this lane's piece of k-group g
+  auto step = [&](const int64_t g) {
+    const uint8_t* rec = rec0 + g * L.group_bytes;
+    if constexpr (FMT == F_Q4_K) {
+      const int t = p >> 1;
+      const uint4 w = ldg128(rec + 16 + 16 * p);
+      const uint4 hd = ldg128(rec);
+      // sc of chunks j0.. at bits 0, 6, 12, 18 of sw; their m at the same bits of mw
+      const uint32_t sw = (p & 1) ? __funnelshift_r(hd.y, hd.z, 24) : hd.y;
+      const uint32_t mw = (p & 1) ? (hd.w >> 8) : __funnelshift_r(hd.z, hd.w, 16);
       const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
-      const float a = __fmul_rn(d, (float)q4k_field(hd.y, hd.z, hd.w, j));
-      const float c = __fmul_rn(dmin, (float)q4k_field(hd.y, hd.z, hd.w, 8 + j));
-      // nibble k of the packed word holds element {0, 2, 4, 6, 1, 3, 5, 7}[k]: the low
-      // nibbles are elements 0, 4, 1, 5 and the high ones 2, 6, 3, 7, in byte order
-      const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+      const uint32_t W[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        if (m >= M) break;
-        const uint2 xq = *reinterpret_cast<const uint2*>(codes + (int64_t)m * L.K + kx);
-        const uint32_t xlo = __byte_perm(xq.x, xq.y, 0x5140), xhi = __byte_perm(xq.x, xq.y, 0x7362);
-        const int s = dp4a_s8(hi, xhi, dp4a_s8(lo, xlo, 0));
-        const int sx = dp4a_s8(0x01010101u, xq.y, dp4a_s8(0x01010101u, xq.x, 0));
-        const float dx = xsc[(int64_t)m * (L.K / 32) + kx / 32];
-        acc[m] = __fmaf_rn(__fmul_rn(a, dx), (float)s, __fmaf_rn(-__fmul_rn(c, dx), (float)sx, acc[m]));
+      for (int c = 0; c < 4; ++c) {
+        const int64_t blk = g * 8 + 4 * (p & 1) + c;
+        const float a = __fmul_rn(d, u6f(sw >> (6 * c))), cm = __fmul_rn(dmin, u6f(mw >> (6 * c)));
+        const uint32_t lo = W[c] & 0x0F0F0F0Fu, hi = (W[c] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m >= M) break;
+          const uint2 xq = *reinterpret_cast<const uint2*>(codes + m * L.K + blk * 32 + 8 * t);
+          const float dx = xsc[m * KB + blk];
+          const int s = dp4a_s8(hi, xq.y, dp4a_s8(lo, xq.x, 0));
+          const int sx = dp4a_s8(0x01010101u, xq.y, dp4a_s8(0x01010101u, xq.x, 0));
+          acc[m] = __fmaf_rn(__fmul_rn(a, dx), i2f_small(s), __fmaf_rn(-__fmul_rn(cm, dx), i2f_small(sx), acc[m]));
+        }
+      }
+    } else {   // Q8_0
+      const int t = p >> 2;
+      const uint4 w = ldg128(rec + 16 + 16 * p);
+      const uint32_t dw = *reinterpret_cast<const uint32_t*>(rec + 4 * (p & 3));
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int64_t blk = g * 8 + 2 * (p & 3) + c;
+        if (blk >= KB) continue;                          // the chunks past K of a ragged last group
+        const uint32_t c0 = q80_codes4(c ? w.z : w.x), c1 = q80_codes4(c ? w.w : w.y);
+        const float dwj = h2f(c ? (dw >> 16) : dw);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m >= M) break;
+          const uint2 xq = *reinterpret_cast<const uint2*>(codes + m * L.K + blk * 32 + 8 * t);
+          const float dx = xsc[m * KB + blk];
+          const int s = dp4a_s8(c1, xq.y, dp4a_s8(c0, xq.x, 0));
+          acc[m] = __fmaf_rn(__fmul_rn(dwj, dx), i2f_small(s), acc[m]);
+        }
       }
     }
-  }
+  };
+  // whole warp steps without a guard (so that the unrolled steps' loads can be issued
+  // ahead of their arithmetic), then the ragged last step
+  constexpr int kUnroll = MT == 1 ? 4 : 2;
+  int64_t g0 = 0;
+#pragma unroll kUnroll
+  for (; g0 + GPS <= G; g0 += GPS) step(g0 + gs);
+  if (g0 + gs < G) step(g0 + gs);
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     float v = acc[m];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
     if (lane == 0 && m < M) y[(int64_t)m * L.N + n] = v;
   }
 }
 
-}  // namespace
-
-int64_t int8dot_workspace_bytes(int M, int64_t K) { return align_up((int64_t)M * K, 256) + align_up((int64_t)M * (K / 32) * 4, 256); }
-
-cudaError_t launch_int8dot(const Layout& L, const uint8_t* packed, const uint16_t* x, float* y, int M, uint8_t* ws,
-                           unsigned* status, cudaStream_t s) {
+template <int FMT>
+cudaError_t launch_int8dot_t(const Layout& L, const uint8_t* packed, const uint16_t* x, float* y, int M,
+                             uint8_t* ws, unsigned* status, cudaStream_t s) {
   int8_t* codes = reinterpret_cast<int8_t*>(ws);
   float* xsc = reinterpret_cast<float*>(ws + align_up((int64_t)M * L.K, 256));
   const int64_t nblk = (int64_t)M * (L.K / 32);
@@ -160,24 +204,29 @@ cudaError_t launch_int8dot(const Layout& L, const uint8_t* packed, const uint16_
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, quant_q8_kernel, x, nblk, codes, xsc);
+  cudaError_t err = cudaLaunchKernelEx(&cfg, quant_q8_kernel<FMT>, x, nblk, codes, xsc);
   if (err != cudaSuccess) return err;
   cfg.gridDim = dim3((unsigned)((L.N + 7) / 8));
   cfg.blockDim = dim3(256);
-  if (L.fmt == F_Q8_0)
-    err = M <= 1 ? cudaLaunchKernelEx(&cfg, int8dot_kernel<F_Q8_0, 1>, L, packed, (const int8_t*)codes,
-                                      (const float*)xsc, y, M, status)
-                 : cudaLaunchKernelEx(&cfg, int8dot_kernel<F_Q8_0, 8>, L, packed, (const int8_t*)codes,
-                                      (const float*)xsc, y, M, status);
-  else if (L.fmt == F_Q4_K)
-    err = M <= 1 ? cudaLaunchKernelEx(&cfg, int8dot_kernel<F_Q4_K, 1>, L, packed, (const int8_t*)codes,
-                                      (const float*)xsc, y, M, status)
-                 : cudaLaunchKernelEx(&cfg, int8dot_kernel<F_Q4_K, 8>, L, packed, (const int8_t*)codes,
-                                      (const float*)xsc, y, M, status);
-  else
-    return cudaErrorInvalidValue;
+  err = M <= 1 ? cudaLaunchKernelEx(&cfg, int8dot_kernel<FMT, 1>, L, packed, (const int8_t*)codes,
+                                    (const float*)xsc, y, M, status)
+               : cudaLaunchKernelEx(&cfg, int8dot_kernel<FMT, 8>, L, packed, (const int8_t*)codes,
+                                    (const float*)xsc, y, M, status);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t int8dot_workspace_bytes(int M, int64_t K) {
+  return align_up((int64_t)M * K, 256) + align_up((int64_t)M * (K / 32) * 4, 256);
+}
+
+cudaError_t launch_int8dot(const Layout& L, const uint8_t* packed, const uint16_t* x, float* y, int M, uint8_t* ws,
+                           unsigned* status, cudaStream_t s) {
+  if (L.fmt == F_Q8_0) return launch_int8dot_t<F_Q8_0>(L, packed, x, y, M, ws, status, s);
+  if (L.fmt == F_Q4_K) return launch_int8dot_t<F_Q4_K>(L, packed, x, y, M, ws, status, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace qmv

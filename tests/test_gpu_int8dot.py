@@ -43,10 +43,16 @@ def _call(q, fmt, packed, x, N, K, ws=None):
     return y, ws
 
 
-def _ws_codes(ws, M, K):
-    """the quantizer's output in the workspace: codes [M][K] int8, scales [M][K/32] fp32"""
+# Q4_K: the quantizer stores each 8-value slice in a packed Q4_K word's nibble order
+# (byte SLICE_POS[p] holds element p of the slice); Q8_0 in element order
+SLICE_POS = {"q4_k": [0, 2, 4, 6, 1, 3, 5, 7], "q8_0": list(range(8))}
+
+
+def _ws_codes(ws, fmt, M, K):
+    """the quantizer's output in the workspace, back in element order: codes [M][K]
+    int8, scales [M][K/32] fp32"""
     w = ws.cpu().numpy()
-    codes = w[:M * K].view(np.int8).reshape(M, K)
+    codes = w[:M * K].view(np.int8).reshape(M, K // 8, 8)[:, :, SLICE_POS[fmt]].reshape(M, K)
     off = (M * K + 255) // 256 * 256
     scales = w[off:off + M * (K // 32) * 4].view(np.float32).reshape(M, K // 32)
     return codes, scales
@@ -88,7 +94,7 @@ def test_int8dot_against_oracle(q, fmt, N, K, M):
     y, ws = _call(q, fmt, packed, x, N, K)
     torch.cuda.synchronize()
     assert q.qmv_device_status() == 0
-    codes, scales = _ws_codes(ws, M, K)
+    codes, scales = _ws_codes(ws, fmt, M, K)
     rc, rs = oracle.quant_act_q8(xb)
     assert np.array_equal(codes, rc)
     assert np.array_equal(scales.view(np.uint32), rs.view(np.uint32))
@@ -114,7 +120,7 @@ def test_int8dot_quantizer_crafted(q):
     x = torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).cuda()
     y, ws = _call(q, fmt, packed, x, N, K)
     torch.cuda.synchronize()
-    codes, scales = _ws_codes(ws, 8, K)
+    codes, scales = _ws_codes(ws, fmt, 8, K)
     rc, rs = oracle.quant_act_q8(xb)
     assert np.array_equal(codes, rc)
     assert np.array_equal(scales.view(np.uint32), rs.view(np.uint32))
