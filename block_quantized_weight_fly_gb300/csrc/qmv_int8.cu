@@ -9,11 +9,13 @@
 //
 // Two launches, chained by programmatic dependent launch:
 //  - the activation quantizer: one thread per 32-value block, fp32 operations rounded
-//    one at a time (bit-exact with the oracle). Codes go to the workspace in the order
-//    the weight words hold their elements, so that the GEMV needs no byte shuffle:
-//    each 8-value slice of a block is one 8-byte word pair, Q8_0 in element order,
-//    Q4_K as the nibble order of a packed Q4_K word (low nibbles: elements 0, 4, 1, 5;
-//    high nibbles: 2, 6, 3, 7 of the slice);
+//    one at a time (bit-exact with the oracle). Codes go to the workspace the way the
+//    packed weights hold their words, so that a lane fetches its codes with one or two
+//    16-byte loads and needs no byte shuffle: per row of x and 256-value k-group,
+//    slice t (values 8t .. 8t+7) of chunk j at byte 64t + 8j, Q8_0 in element order,
+//    Q4_K in the nibble order of a packed Q4_K word (low nibbles: elements 0, 4, 1, 5;
+//    high nibbles: 2, 6, 3, 7 of the slice). Rows are Kp = 256 x (k-groups) bytes
+//    apart; the block scales [M][Kp/32] follow;
 //  - the GEMV: one warp per weight row, all M rows of x. A k-group's record is read
 //    with one 16-byte load per lane (Q4_K: 8 lanes per group, 4 groups per warp step;
 //    Q8_0: 16 lanes, 2 groups), so a warp has several k-groups' bytes in flight.
@@ -39,10 +41,10 @@ __device__ __forceinline__ int slice_pos(int p) {
   return p;
 }
 
-// x (bf16 [M][K]) -> int8 codes [M][K] (slice order above) and fp32 block scales [M][K/32]
+// x (bf16 [M][K]) -> int8 codes [M][Kp] and fp32 block scales [M][Kp/32] (order above)
 template <int FMT>
-__global__ void quant_q8_kernel(const uint16_t* __restrict__ x, int64_t nblk, int8_t* __restrict__ codes,
-                                float* __restrict__ scales) {
+__global__ void quant_q8_kernel(const uint16_t* __restrict__ x, int64_t nblk, int64_t kb, int64_t kp,
+                                int8_t* __restrict__ codes, float* __restrict__ scales) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");     // x may come from the kernel before
   const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -73,10 +75,12 @@ __global__ void quant_q8_kernel(const uint16_t* __restrict__ x, int64_t nblk, in
     const int pos = 8 * (i >> 3) + slice_pos<FMT>(i & 7);
     out[pos >> 2] |= ((uint32_t)q & 0xFFu) << (8 * (pos & 3));
   }
-  uint4* dst = reinterpret_cast<uint4*>(codes + b * 32);
-  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
-  scales[b] = d;
+  const int64_t m = b / kb, blk = b % kb, g = blk >> 3;
+  const int j = (int)(blk & 7);
+  int8_t* dst = codes + m * kp + g * 256 + 8 * j;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(dst + 64 * t) = make_uint2(out[2 * t], out[2 * t + 1]);
+  scales[m * (kp / 32) + blk] = d;
 }
 
 // Q8_0 packed word (elements 4i .. 4i+3 of a slice, offset-binary nibbles) -> the four
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(256) int8dot_kernel(Layout L, const uint8_t* _
   float acc[MT];
 #pragma unroll
   for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-  const int64_t G = L.k_groups, KB = L.K / 32;
+  const int64_t G = L.k_groups, KB = L.K / 32, Kp = G * 256, KBp = G * 8;
   const uint8_t* rec0 = packed + L.base + n * L.rec;
   // one warp step: this lane's piece of k-group g
   auto step = [&](const int64_t g) {
@@ -137,19 +141,28 @@ __global__ void __launch_bounds__(256) int8dot_kernel(Layout L, const uint8_t* _
       const uint32_t mw = (p & 1) ? (hd.w >> 8) : __funnelshift_r(hd.z, hd.w, 16);
       const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
       const uint32_t W[4] = {w.x, w.y, w.z, w.w};
+      const int j0 = 4 * (p & 1);
+      float a[4], cm[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int64_t blk = g * 8 + 4 * (p & 1) + c;
-        const float a = __fmul_rn(d, u6f(sw >> (6 * c))), cm = __fmul_rn(dmin, u6f(mw >> (6 * c)));
-        const uint32_t lo = W[c] & 0x0F0F0F0Fu, hi = (W[c] >> 4) & 0x0F0F0F0Fu;
+        a[c] = __fmul_rn(d, u6f(sw >> (6 * c)));
+        cm[c] = __fmul_rn(dmin, u6f(mw >> (6 * c)));
+      }
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          if (m >= M) break;
-          const uint2 xq = *reinterpret_cast<const uint2*>(codes + m * L.K + blk * 32 + 8 * t);
-          const float dx = xsc[m * KB + blk];
-          const int s = dp4a_s8(hi, xq.y, dp4a_s8(lo, xq.x, 0));
-          const int sx = dp4a_s8(0x01010101u, xq.y, dp4a_s8(0x01010101u, xq.x, 0));
-          acc[m] = __fmaf_rn(__fmul_rn(a, dx), i2f_small(s), __fmaf_rn(-__fmul_rn(cm, dx), i2f_small(sx), acc[m]));
+      for (int m = 0; m < MT; ++m) {
+        if (m >= M) break;
+        const int8_t* xg = codes + m * Kp + g * 256 + 64 * t + 8 * j0;          // chunks j0 .. j0+3
+        const uint4 xa = *reinterpret_cast<const uint4*>(xg), xb = *reinterpret_cast<const uint4*>(xg + 16);
+        const float4 dx4 = *reinterpret_cast<const float4*>(xsc + m * KBp + g * 8 + j0);
+        const uint32_t XL[4] = {xa.x, xa.z, xb.x, xb.z}, XH[4] = {xa.y, xa.w, xb.y, xb.w};
+        const float DX[4] = {dx4.x, dx4.y, dx4.z, dx4.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t lo = W[c] & 0x0F0F0F0Fu, hi = (W[c] >> 4) & 0x0F0F0F0Fu;
+          const int s = dp4a_s8(hi, XH[c], dp4a_s8(lo, XL[c], 0));
+          const int sx = dp4a_s8(0x01010101u, XH[c], dp4a_s8(0x01010101u, XL[c], 0));
+          acc[m] = __fmaf_rn(__fmul_rn(a[c], DX[c]), i2f_small(s),
+                             __fmaf_rn(-__fmul_rn(cm[c], DX[c]), i2f_small(sx), acc[m]));
         }
       }
     } else {   // Q8_0
@@ -158,17 +171,18 @@ __global__ void __launch_bounds__(256) int8dot_kernel(Layout L, const uint8_t* _
       const uint32_t dw = *reinterpret_cast<const uint32_t*>(rec + 4 * (p & 3));
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int64_t blk = g * 8 + 2 * (p & 3) + c;
-        if (blk >= KB) continue;                          // the chunks past K of a ragged last group
+        const int j = 2 * (p & 3) + c;
+        const int64_t blk = g * 8 + j;
+        if (blk >= KB) continue;      // a ragged last group: its codes and scales past K were never written
         const uint32_t c0 = q80_codes4(c ? w.z : w.x), c1 = q80_codes4(c ? w.w : w.y);
         const float dwj = h2f(c ? (dw >> 16) : dw);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           if (m >= M) break;
-          const uint2 xq = *reinterpret_cast<const uint2*>(codes + m * L.K + blk * 32 + 8 * t);
-          const float dx = xsc[m * KB + blk];
-          const int s = dp4a_s8(c1, xq.y, dp4a_s8(c0, xq.x, 0));
-          acc[m] = __fmaf_rn(__fmul_rn(dwj, dx), i2f_small(s), acc[m]);
+          const uint2 xq = *reinterpret_cast<const uint2*>(codes + m * Kp + g * 256 + 64 * t + 8 * j);
+          const float dx = xsc[m * KBp + blk];
+          const int sv = dp4a_s8(c1, xq.y, dp4a_s8(c0, xq.x, 0));
+          acc[m] = __fmaf_rn(__fmul_rn(dwj, dx), i2f_small(sv), acc[m]);
         }
       }
     }
@@ -192,8 +206,9 @@ __global__ void __launch_bounds__(256) int8dot_kernel(Layout L, const uint8_t* _
 template <int FMT>
 cudaError_t launch_int8dot_t(const Layout& L, const uint8_t* packed, const uint16_t* x, float* y, int M,
                              uint8_t* ws, unsigned* status, cudaStream_t s) {
+  const int64_t kp = L.k_groups * 256;
   int8_t* codes = reinterpret_cast<int8_t*>(ws);
-  float* xsc = reinterpret_cast<float*>(ws + align_up((int64_t)M * L.K, 256));
+  float* xsc = reinterpret_cast<float*>(ws + align_up((int64_t)M * kp, 256));
   const int64_t nblk = (int64_t)M * (L.K / 32);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -204,7 +219,7 @@ cudaError_t launch_int8dot_t(const Layout& L, const uint8_t* packed, const uint1
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, quant_q8_kernel<FMT>, x, nblk, codes, xsc);
+  cudaError_t err = cudaLaunchKernelEx(&cfg, quant_q8_kernel<FMT>, x, nblk, L.K / 32, kp, codes, xsc);
   if (err != cudaSuccess) return err;
   cfg.gridDim = dim3((unsigned)((L.N + 7) / 8));
   cfg.blockDim = dim3(256);
@@ -219,7 +234,8 @@ cudaError_t launch_int8dot_t(const Layout& L, const uint8_t* packed, const uint1
 }  // namespace
 
 int64_t int8dot_workspace_bytes(int M, int64_t K) {
-  return align_up((int64_t)M * K, 256) + align_up((int64_t)M * (K / 32) * 4, 256);
+  const int64_t kp = align_up(K, 256);
+  return align_up((int64_t)M * kp, 256) + align_up((int64_t)M * (kp / 32) * 4, 256);
 }
 
 cudaError_t launch_int8dot(const Layout& L, const uint8_t* packed, const uint16_t* x, float* y, int M, uint8_t* ws,

@@ -50,12 +50,16 @@ SLICE_POS = {"q4_k": [0, 2, 4, 6, 1, 3, 5, 7], "q8_0": list(range(8))}
 
 def _ws_codes(ws, fmt, M, K):
     """the quantizer's output in the workspace, back in element order: codes [M][K]
-    int8, scales [M][K/32] fp32"""
+    int8, scales [M][K/32] fp32. Rows of x are Kp = 256 x (k-groups) bytes apart; in
+    k-group g, slice t (values 8t .. 8t+7) of chunk j sits at byte 64t + 8j."""
+    G = -(-K // 256)
+    Kp = 256 * G
     w = ws.cpu().numpy()
-    codes = w[:M * K].view(np.int8).reshape(M, K // 8, 8)[:, :, SLICE_POS[fmt]].reshape(M, K)
-    off = (M * K + 255) // 256 * 256
-    scales = w[off:off + M * (K // 32) * 4].view(np.float32).reshape(M, K // 32)
-    return codes, scales
+    raw = w[:M * Kp].view(np.int8).reshape(M, G, 4, 8, 8)           # [m][g][t][j][slot]
+    codes = raw.transpose(0, 1, 3, 2, 4)[..., SLICE_POS[fmt]].reshape(M, Kp)[:, :K]
+    off = (M * Kp + 255) // 256 * 256
+    scales = w[off:off + M * (Kp // 32) * 4].view(np.float32).reshape(M, Kp // 32)[:, :K // 32]
+    return np.ascontiguousarray(codes), np.ascontiguousarray(scales)
 
 
 def _crafted_x(K, huge=False):
