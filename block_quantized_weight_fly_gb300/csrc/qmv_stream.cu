@@ -1143,9 +1143,17 @@ StreamPlan plan_stream_grouped(int64_t slabs_max, int M, int passes, int64_t k_g
   const int64_t unit = passes * k_groups;
   p.cells = 0;
   p.cpc = 1;
-  p.gp = 1;                 // every slab its own cell: CTA ranges stay slab-granular
+  // cells of gp k-groups within a unit (a function of K alone, so the order of the
+  // sums is the same for every M and routing): a reducer gathers a quarter of the
+  // pieces it would with one cell per slab; CTA ranges are whole cells
+  p.gp = (k_groups % 4 == 0) ? 4 : (k_groups % 2 == 0 ? 2 : 1);
+  const int64_t cells_max = (slabs_max + p.gp - 1) / p.gp;
   const int64_t n = 2 * (int64_t)sms;
-  p.grid = (int)(slabs_max < n ? (slabs_max > 0 ? slabs_max : 1) : n);
+  p.grid = (int)(cells_max < n ? (cells_max > 0 ? cells_max : 1) : n);
+  {   // as few CTAs as give the same cells per CTA at most
+    const int64_t per = (cells_max + p.grid - 1) / p.grid;
+    p.grid = (int)((cells_max + per - 1) / per);
+  }
   // a CTA publishes the slabs of its first unit but the unit's first one; the slot of
   // a slab is (its ordinal in the CTA's range) x passes + its pass
   const int64_t per_cta = (slabs_max + p.grid - 1) / p.grid;
