@@ -1122,14 +1122,17 @@ static int64_t piece_bytes(int M) { return (int64_t)kSlabRows * (M <= 1 ? 1 : 8)
 
 StreamPlan plan_stream_dense(int64_t slabs, int M, int passes, int sms) {
   StreamPlan p;
-  const int64_t v = slabs < 2 * (int64_t)sms ? slabs : 2 * (int64_t)sms;
+  // Long calls (8 slabs or more per cell at two cells per SM): one cell per CTA, two
+  // CTAs per SM, whose warps hide each other's latency. Shorter calls: one cell per
+  // SM and one CTA per SM, so that the next call's CTAs are resident beside this
+  // call's and copy their first slabs meanwhile, and a unit spans fewer cells (fewer
+  // pieces to gather). The cells, and so the order of the sums, depend on the matrix
+  // and the SM count only, never on M.
+  const bool long_call = slabs >= 16 * (int64_t)sms;
+  const int64_t vmax = long_call ? 2 * (int64_t)sms : (int64_t)sms;
+  const int64_t v = slabs < vmax ? slabs : vmax;
   p.cells = (int)(v > 0 ? v : 1);
-  // One cell per CTA, two CTAs per SM, whose warps hide each other's latency: at
-  // M > 1 and for long cells (8 slabs or more). Short cells at M = 1: two cells per
-  // CTA, one CTA per SM, so that the next call's CTAs are resident beside this
-  // call's and copy their first slabs meanwhile. Either way the cells, and so the
-  // order of the sums, are the same.
-  p.cpc = (M > 1 || slabs >= 8 * (int64_t)p.cells) ? 1 : 2;
+  p.cpc = 1;
   p.gp = 1;
   p.grid = (p.cells + p.cpc - 1) / p.cpc;
   p.maxslots = p.cpc * passes;          // a CTA publishes pieces of its first unit only
