@@ -34,11 +34,12 @@ struct StreamArgs {
 
 // Grid, accumulation cells and workspace of one stream-kernel call (host side),
 // shared by the entry points and the workspace size query.
-//  - dense: V = min(2 x SMs, slabs) cells, a function of the matrix and the SM count
-//    only, so that every M (and the no-workspace entry) adds in the same order; one
-//    cell per CTA (two CTAs per SM) at M > 1 or when cells are 8 slabs or longer,
-//    else two (one CTA per SM, so the next call's CTAs fit beside it);
-//  - grouped: every slab is a cell (gp = 1), whatever the routing; two CTAs per SM.
+//  - dense: V cells, a function of the matrix and the SM count only, so that every M
+//    (and the no-workspace entry) adds in the same order: V = min(2 x SMs, slabs) for
+//    long calls (16 slabs per SM or more; two CTAs per SM), else min(SMs, slabs) (one
+//    CTA per SM, so the next call's CTAs fit beside it); one cell per CTA;
+//  - grouped: each unit cut into cells of gp k-groups (4, 2 or 1: a function of K
+//    only), whatever the routing; CTAs take whole cells, at most two CTAs per SM.
 // passes: 1, or 2 for the fused gate|up (gate and up sums).
 struct StreamPlan {
   int grid, cells, cpc, gp, maxslots;
