@@ -169,9 +169,9 @@ struct KParams {
   int grid_off;      // offset of the grid formats' f16 grid
   int stage_base;    // offset of stage 0
   int mt;            // partial stride (token columns per partial record)
-  int cells;         // dense: the number of cells V (> 0); grouped: 0 (every slab is a cell)
-  int cpc;           // dense: cells per CTA (1 or 2)
-  int gp;            // grouped: slabs per cell
+  int cells;         // dense: the number of cells V (> 0); grouped: 0 (cells of gp slabs per unit)
+  int cpc;           // dense: cells per CTA (the plans use 1; the kernel also takes 2)
+  int gp;            // grouped: slabs (k-groups) per cell: 1, 2 or 4
   int maxslots;      // published pieces a CTA may hold (slots per CTA in the workspace)
   int fault;         // test hook: 1 = peers publish nothing (reducers' bounded waits run
                      // out); 2 = reducers abandon their gathers at once (pieces left behind)
@@ -615,8 +615,9 @@ __device__ __forceinline__ void stream_body(const KParams& kp, uint8_t* smem, co
   // follows (pieces never cross a cell boundary). Dense calls: V = kp.cells cells,
   // cell i = slabs [floor(i S / V), floor((i+1) S / V)), kp.cpc consecutive cells per
   // CTA; V depends on the matrix and the SM count only, never on M, so every M sums
-  // in the same order. Grouped calls: every slab is a cell, and CTA i holds slabs
-  // [floor(i S / P), floor((i+1) S / P)). In 32-bit arithmetic (i * Sr < V * V).
+  // in the same order. Grouped calls: each unit is cut into cells of gp slabs (gp a
+  // function of K only), and CTA c holds a contiguous range of whole cells. In 32-bit
+  // arithmetic (i * Sr < V * V).
   constexpr bool dense_cells = !GR;       // GR: a grouped call (its own instances)
   const int s0 = misc[6], s1 = misc[7];
   if (s0 >= s1) return;
@@ -1242,7 +1243,6 @@ static cudaError_t launch_t(const StreamArgs& a, cudaStream_t s) {
   int smem = 0, dev = 0;
   cudaError_t err = prep_kp<FMT, MT, SW>(a, kp, &smem, &dev);
   if (err != cudaSuccess) return err;
-  // M = 1 grouped calls have an instance of their own (the producer's first-stage start)
   // grouped calls have instances of their own (cells, and at M = 1 the producer's
   // first-stage start)
   const bool gr = a.ids != nullptr;
